@@ -1,0 +1,372 @@
+"""Throughput of the GB300 GEMM library on the workloads of the pages.
+
+Headline (the JSON line's `value`): fp32 SGEMM, nn, row-major, M = N = K = 4096,
+alpha = 1, beta = 0, A and B i.i.d. U[-1, 1) -- the problem of "Optimizing GEMM
+on Apple's M5 from scratch" (Parts 1 and 2) -- in TFLOP/s (2*M*N*K flops per
+step).  One step is one gemm() call through the C ABI on inputs resident in
+HBM.  The same line carries, measured in the same run:
+  fp16       fp16-operand / fp32-accumulate / fp16-output GEMM at 4096^3 in the
+             nn, tn and nt variants ("Metal GEMM Kernels for LoRA Training",
+             section 2), per-launch CUDA-event timing with L2 flushed before
+             every launch;
+  roofline   achieved / peak of the dominant kernel (FP32 FFMA pipe for the
+             SGEMM; the tensor pipe for the fp16 kernel);
+  e2e        the SGEMM through gemm_host(): pinned host buffers, the copies to
+             and from the GPU inside the timed region;
+  cpu_baseline  the CPU oracle (double accumulation) on a bounded sample of
+             rows of the same problem, on this host's cores.
+
+Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+For N > 1 run under torch.distributed.run: every rank runs its own replica of
+the workload on its own GPU (the GEMM does not shard across GPUs here), the
+timed region is bracketed by barriers and the slowest rank's time is used.
+`--impl reference` times the CPU oracle instead (rank 0 only).
+"""
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "GEMM TFLOP/s (fp32 4096³; fp16→fp32 nn/tn/nt) and % of roofline, 1×GB300"
+WORKLOAD = ("fp32 SGEMM nn, row-major, M=N=K=4096, alpha=1, beta=0, A and B i.i.d. "
+            "uniform[-1,1) (torch CPU generator, seeds 60/61)")
+M = N = K = 4096
+L2_BYTES = 129 * 1000 * 1000
+FP32_LANES_PER_SM = 128  # FP32 FMA lanes per SM (4 partitions x 32)
+
+
+# ------------------------------------------------------------------ helpers
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return {"hbm_gbs": float(d["hbm_gbs"]), "bf16_tflops": float(d["bf16_tflops"]),
+                "bf16_tflops_sustained": float(d.get("bf16_tflops_sustained", d["bf16_tflops"])),
+                "sm_max_mhz": float(d.get("sm_max_mhz", 2070.0)), "source": "measured"}
+    except Exception:
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
+                "sm_max_mhz": 2070.0, "source": "fallback"}
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled during the timed region."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int, period_ms: int = 100):
+        self.gpu = gpu_index
+        self.period = period_ms
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", f"-lms={self.period}"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.thread.join(timeout=2)
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx = float(parts[2])
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[5:9]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": mx, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        import torch
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if backend == "nccl":
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend=backend)
+    return world, rank, local
+
+
+def max_over_ranks(x: float, world: int, device=None) -> float:
+    if world <= 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+# ------------------------------------------------------------------ oracle leg
+def oracle_sample(rows: int, threads: int):
+    """Times the CPU oracle on the first `rows` rows of the headline problem.
+    Returns (seconds, flops)."""
+    import oracle
+    from dense_gemm_tiled_gb300 import inputs
+    A = inputs.uniform((rows, K), 60, "f32").numpy()  # the first rows of A (same generator stream)
+    B = inputs.uniform((K, N), 61, "f32").numpy()
+    t0 = time.perf_counter()
+    oracle.gemm_ref(A, B, threads=threads)
+    dt = time.perf_counter() - t0
+    return dt, 2.0 * rows * N * K
+
+
+def cpu_baseline(target_s: float = 12.0):
+    import oracle
+    threads = oracle.default_threads()
+    dt, fl = oracle_sample(8, threads)  # calibration
+    rows = max(8, min(M, int(8 * target_s / max(dt, 1e-3))))
+    rows = (rows // threads) * threads or threads
+    dt, fl = oracle_sample(rows, threads)
+    return {"value": fl / dt / 1e12, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+            "sample": f"rows 0..{rows - 1} of the {M}x{N}x{K} product (full K and N), "
+                      f"double accumulation, {dt:.1f} s"}
+
+
+def run_reference(args, world, rank):
+    if rank != 0:
+        return
+    import oracle
+    threads = oracle.default_threads()
+    dt, _ = oracle_sample(8, threads)
+    budget = max(0.2, min(2.0, 150.0 / max(1, args.steps + args.warmup)))
+    rows = max(threads, int(8 * budget / max(dt, 1e-3)) // threads * threads)
+    for _ in range(args.warmup):
+        oracle_sample(rows, threads)
+    tot_t, tot_f = 0.0, 0.0
+    for _ in range(args.steps):
+        dt, fl = oracle_sample(rows, threads)
+        tot_t += dt
+        tot_f += fl
+    value = tot_f / tot_t / 1e12
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": tot_t / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "sample_rows_per_step": rows},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+                         "sample": f"{rows} rows of the {M}^3 product per step"},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ------------------------------------------------------------------ GPU legs
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-fp16", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    world, rank, local = dist_setup()
+    if args.impl == "reference":
+        run_reference(args, world, rank)
+        return
+
+    import torch
+    from dense_gemm_tiled_gb300 import binding, inputs
+
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    props = torch.cuda.get_device_properties(dev)
+    sms = props.multi_processor_count
+    peaks = load_peaks()
+    stream = torch.cuda.Stream(dev)
+
+    # headline problem, resident in HBM
+    A = inputs.uniform((M, K), 60, "f32").to(dev)
+    B = inputs.uniform((K, N), 61, "f32").to(dev)
+    C = torch.empty((M, N), dtype=torch.float32, device=dev)
+    flops = 2.0 * M * N * K
+
+    def step():
+        binding.gemm(A, B, C, stream=stream)
+
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            step()
+    torch.cuda.synchronize()
+    assert binding.check_device_status(stream) == binding.OK
+
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    barrier(world)
+    torch.cuda.synchronize()
+    launches0 = binding.total_launches()
+    with ClockSampler(local) as clk:
+        t0 = time.perf_counter()
+        for i in range(args.steps):
+            starts[i].record(stream)
+            step()
+            ends[i].record(stream)
+        torch.cuda.synchronize()
+        t1 = time.perf_counter()
+    barrier(world)
+    launches = binding.total_launches() - launches0
+    path = binding.last_path()
+    wall = max_over_ranks(t1 - t0, world, dev)
+    ms_step = wall / args.steps * 1e3
+    kernel_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    avg_kernel_ms = sum(kernel_ms) / len(kernel_ms)
+    value = world * flops / (wall / args.steps) / 1e12
+    clocks = clk.summary()
+    assert binding.check_device_status(stream) == binding.OK
+
+    # FP32 FFMA peak from unit counts and clocks: SMs x 128 lanes x 2 flops
+    sm_max = clocks.get("sm_max_mhz") or peaks["sm_max_mhz"]
+    ffma_peak = sms * FP32_LANES_PER_SM * 2 * sm_max * 1e6 / 1e12
+    achieved = flops / (avg_kernel_ms * 1e-3) / 1e12
+    roofline = {"bound": "alu", "achieved": achieved, "peak": ffma_peak, "unit": "TFLOP/s",
+                "frac": achieved / ffma_peak, "traffic": None,
+                "kernel": "sgemm_ffma_kernel (fp32 nn, 128x128x16 tiles)",
+                "peak_basis": f"{sms} SMs x {FP32_LANES_PER_SM} FP32 lanes x 2 x {sm_max:.0f} MHz",
+                "frac_at_median_clock": (achieved / (sms * FP32_LANES_PER_SM * 2 *
+                                                     clocks["sm_mhz"] * 1e6 / 1e12)
+                                         if clocks.get("sm_mhz") else None)}
+    tpath = os.path.join(ROOT, "profiles", "traffic.json")
+    if os.path.exists(tpath):
+        try:
+            roofline["traffic"] = json.load(open(tpath)).get("sgemm_f32_nn_4096")
+        except Exception:
+            pass
+
+    # fp16 variants, per-launch timing, L2 flushed before each launch
+    fp16 = None
+    if not args.no_fp16:
+        fp16 = {}
+        flush = torch.empty(int(2.5 * L2_BYTES) // 4, dtype=torch.float32, device=dev)
+        for var in ("nn", "tn", "nt"):
+            tA, tB = inputs.VARIANTS[var]
+            p = inputs.hgemm_square(4096, var, seed=70)
+            Ah, Bh = p.A.to(dev), p.B.to(dev)
+            Ch = torch.empty((M, N), dtype=torch.float16, device=dev)
+            with torch.cuda.stream(stream):
+                for _ in range(args.warmup):
+                    binding.gemm(Ah, Bh, Ch, tA, tB, stream=stream)
+            ts = []
+            reps = max(10, min(50, args.steps))
+            for _ in range(reps):
+                with torch.cuda.stream(stream):
+                    flush.fill_(1.0)
+                s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                s.record(stream)
+                binding.gemm(Ah, Bh, Ch, tA, tB, stream=stream)
+                e.record(stream)
+                e.synchronize()
+                ts.append(s.elapsed_time(e))
+            hpath = binding.last_path()
+            med = statistics.median(ts)
+            ach = flops / (med * 1e-3) / 1e12
+            fp16[var] = {"tflops": ach, "ms_median": med, "ms_min": min(ts), "path": hpath,
+                         "roofline": {"bound": "tensor", "achieved": ach,
+                                      "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                                      "frac": ach / peaks["bf16_tflops"],
+                                      "peak_basis": f"{peaks['source']} bf16 dense burst "
+                                                    "(cuBLAS 8192^3) x 1 (fp16 rate = bf16 rate)"}}
+            del Ah, Bh, Ch
+        del flush
+        assert binding.check_device_status(stream) == binding.OK
+
+    # end to end through gemm_host(): pinned host inputs, result read back
+    Ah = inputs.uniform((M, K), 60, "f32").pin_memory()
+    Bh = inputs.uniform((K, N), 61, "f32").pin_memory()
+    Chost = torch.empty((M, N), dtype=torch.float32).pin_memory()
+    e2e_steps = max(3, min(20, args.steps // 10))
+    binding.gemm_host(Ah, Bh, Chost, stream=stream)
+    barrier(world)
+    t0 = time.perf_counter()
+    for _ in range(e2e_steps):
+        binding.gemm_host(Ah, Bh, Chost, stream=stream)
+    t1 = time.perf_counter()
+    e2e_wall = max_over_ranks(t1 - t0, world, dev)
+    e2e = {"value": world * flops * e2e_steps / e2e_wall / 1e12, "unit": "TFLOP/s",
+           "h2d_bytes_per_step": (M * K + K * N) * 4, "d2h_bytes_per_step": M * N * 4,
+           "steps": e2e_steps, "api": "gemm_host (C ABI), pinned host buffers"}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline()
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+            "data": "synthetic",
+            "config": {"workload": WORKLOAD,
+                       "l2": "inputs larger than L2: A, B, C are 192 MiB against a 129 MB L2; "
+                             "fp16 sub-results flush L2 (323 MB write) before each launch",
+                       "parallelism": "replicas" if world > 1 else "single GPU",
+                       "gpu": props.name, "sms": sms},
+            "path": path,
+            "kernel_ms_avg": avg_kernel_ms,
+            "roofline": roofline,
+            "fp16_4096": fp16,
+            "e2e": e2e,
+            "cpu_baseline": cpu,
+            "gpu_launches": launches,
+            "clocks": clocks,
+            "peaks": peaks,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

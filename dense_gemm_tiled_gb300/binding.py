@@ -1,0 +1,170 @@
+"""Thin Python binding over libgemm_gb300.so (include/gemm.h).
+
+Argument marshalling only: every step of the GEMM runs in the library's
+kernels.  PyTorch supplies device memory and the current CUDA stream.  If the
+library has not been built this module raises ImportError; there is no
+fallback implementation.
+"""
+import ctypes
+import os
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libgemm_gb300.so")
+
+if not os.path.exists(LIB_PATH):
+    raise ImportError(
+        f"{LIB_PATH} is missing: build it with `python -c 'import __graft_entry__ as g; g.build()'`"
+        " or `python -m dense_gemm_tiled_gb300.build`")
+
+_lib = ctypes.CDLL(LIB_PATH)
+
+_i64, _int, _flt, _vp = ctypes.c_int64, ctypes.c_int, ctypes.c_float, ctypes.c_void_p
+_GEMM_ARGS = [_int, _int, _i64, _i64, _i64, _int, _flt, _flt, _vp, _i64, _vp, _i64, _vp, _i64,
+              _vp]
+_lib.gemm.argtypes = _GEMM_ARGS
+_lib.gemm.restype = _int
+_lib.gemm_host.argtypes = _GEMM_ARGS
+_lib.gemm_host.restype = _int
+_lib.gemm_check_device_status.argtypes = [_vp]
+_lib.gemm_check_device_status.restype = _int
+_lib.gemm_status_string.argtypes = [_int]
+_lib.gemm_status_string.restype = ctypes.c_char_p
+_lib.gemm_version.restype = _int
+_lib.gemm_last_path.restype = _int
+_lib.gemm_last_launches.restype = _int
+_lib.gemm_total_launches.restype = _i64
+_lib.gemm_set_wait_timeout_ns.argtypes = [_i64]
+_lib.gemm_set_wait_timeout_ns.restype = None
+_lib.gemm_set_fault_injection.argtypes = [_int]
+_lib.gemm_set_fault_injection.restype = None
+
+F32 = 0
+F16_F32ACC = 1
+OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_ALIAS, ERR_CUDA, ERR_NO_MEMORY, ERR_TIMEOUT = range(7)
+PATHS = {0: "none", 1: "scale", 2: "ffma", 3: "ffma_splitk", 4: "tc", 5: "tc_splitk"}
+
+
+class GemmError(RuntimeError):
+    def __init__(self, code: int):
+        self.code = code
+        super().__init__(status_string(code))
+
+
+def status_string(code: int) -> str:
+    return _lib.gemm_status_string(int(code)).decode()
+
+
+def version() -> int:
+    return _lib.gemm_version()
+
+
+def last_path() -> str:
+    return PATHS.get(_lib.gemm_last_path(), "unknown")
+
+
+def last_launches() -> int:
+    return _lib.gemm_last_launches()
+
+
+def total_launches() -> int:
+    return _lib.gemm_total_launches()
+
+
+def set_wait_timeout_ns(ns: int) -> None:
+    _lib.gemm_set_wait_timeout_ns(int(ns))
+
+
+def set_fault_injection(mode: int) -> None:
+    _lib.gemm_set_fault_injection(int(mode))
+
+
+def gemm_raw(transA, transB, M, N, K, dtype, alpha, beta, A, lda, B, ldb, C, ldc,
+             stream=0) -> int:
+    """The C entry point with plain integers (device addresses, stream handle)."""
+    return _lib.gemm(int(transA), int(transB), int(M), int(N), int(K), int(dtype), float(alpha),
+                     float(beta), A or None, int(lda), B or None, int(ldb), C or None, int(ldc),
+                     stream or None)
+
+
+def gemm_host_raw(transA, transB, M, N, K, dtype, alpha, beta, A, lda, B, ldb, C, ldc,
+                  stream=0) -> int:
+    """gemm_host with plain integers (host addresses)."""
+    return _lib.gemm_host(int(transA), int(transB), int(M), int(N), int(K), int(dtype),
+                          float(alpha), float(beta), A or None, int(lda), B or None, int(ldb),
+                          C or None, int(ldc), stream or None)
+
+
+def _ld(t) -> int:
+    if t.dim() != 2:
+        raise ValueError("matrices are 2-D")
+    if t.shape[1] > 1 and t.stride(1) != 1:
+        raise ValueError("rows must be contiguous (stride(1) == 1)")
+    if t.shape[0] <= 1:  # a single row: any ld >= its length is valid
+        return max(int(t.stride(0)), int(t.shape[1]), 1)
+    return int(t.stride(0))
+
+
+def _dims(A, B, C, transA, transB):
+    import torch
+    if A.dtype != B.dtype or A.dtype != C.dtype:
+        raise TypeError("A, B and C must share a dtype")
+    if A.dtype == torch.float32:
+        dtype = F32
+    elif A.dtype == torch.float16:
+        dtype = F16_F32ACC
+    else:
+        raise TypeError(f"unsupported dtype {A.dtype}")
+    M, K = (A.shape[1], A.shape[0]) if transA else (A.shape[0], A.shape[1])
+    Kb, N = (B.shape[1], B.shape[0]) if transB else (B.shape[0], B.shape[1])
+    if K != Kb:
+        raise ValueError(f"inner dimensions differ: {K} vs {Kb}")
+    if tuple(C.shape) != (M, N):
+        raise ValueError(f"C is {tuple(C.shape)}, expected {(M, N)}")
+    return dtype, int(M), int(N), int(K)
+
+
+def gemm(A, B, C, transA=False, transB=False, alpha=1.0, beta=0.0, stream=None):
+    """C = alpha * op(A) @ op(B) + beta * C in place, on torch CUDA tensors.
+
+    A is [M,K] (or [K,M] with transA), B is [K,N] (or [N,K] with transB),
+    C is [M,N]; all float32 or all float16 (fp32 accumulation), rows
+    contiguous, any leading dimension.  Runs on `stream` (a torch.cuda.Stream)
+    or the current stream.  Returns C.
+    """
+    import torch
+    dtype, M, N, K = _dims(A, B, C, transA, transB)
+    for t in (A, B, C):
+        if not t.is_cuda:
+            raise ValueError("gemm() takes CUDA tensors; use gemm_host() for host memory")
+    s = stream if stream is not None else torch.cuda.current_stream(C.device)
+    rc = _lib.gemm(int(transA), int(transB), M, N, K, dtype, float(alpha), float(beta),
+                   A.data_ptr() or None, _ld(A), B.data_ptr() or None, _ld(B),
+                   C.data_ptr() or None, _ld(C), s.cuda_stream or None)
+    if rc != OK:
+        raise GemmError(rc)
+    return C
+
+
+def gemm_host(A, B, C, transA=False, transB=False, alpha=1.0, beta=0.0, stream=None):
+    """The same product on host (CPU) tensors, pinned or not; the library
+    copies them to the GPU, computes, copies C back and synchronises."""
+    import torch
+    dtype, M, N, K = _dims(A, B, C, transA, transB)
+    for t in (A, B, C):
+        if t.is_cuda:
+            raise ValueError("gemm_host() takes host tensors")
+    s = stream if stream is not None else torch.cuda.current_stream()
+    rc = _lib.gemm_host(int(transA), int(transB), M, N, K, dtype, float(alpha), float(beta),
+                        A.data_ptr() or None, _ld(A), B.data_ptr() or None, _ld(B),
+                        C.data_ptr() or None, _ld(C), s.cuda_stream or None)
+    if rc != OK:
+        raise GemmError(rc)
+    return C
+
+
+def check_device_status(stream=None) -> int:
+    """Synchronises the stream and returns (and clears) the device status:
+    OK, ERR_TIMEOUT (a kernel's bounded wait ran out) or ERR_CUDA."""
+    import torch
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return _lib.gemm_check_device_status(s.cuda_stream or None)

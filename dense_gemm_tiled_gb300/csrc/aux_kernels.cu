@@ -1,0 +1,155 @@
+// Small memory-bound kernels around the GEMM main loops.
+//
+//  splitk_reduce : C = alpha * sum_z P[z] + beta * C, the reduction step of
+//                  split-K ("Metal GEMM Kernels for LoRA Training", section 5:
+//                  the K range is cut into chunks, each chunk writes fp32 partial
+//                  sums to device memory, a second pass adds them).  The slices
+//                  are added in increasing z, so the result does not depend on
+//                  scheduling.
+//  scale         : C = beta * C, the K == 0 case of C = alpha*A*B + beta*C.
+//  repack_f16    : copies an fp16 operand whose rows are not 16-byte aligned
+//                  into a zero-padded buffer with a 16-byte row pitch, so the
+//                  tensor-memory-access unit can read it.
+//
+// All three are HBM-bound; they use grid-stride loops over 128-bit accesses
+// where the layout allows, with grids sized to a multiple of the SM count.
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace gb300 {
+namespace {
+
+int grid_for(int64_t work_items, int threads) {
+  static int sms = 0;
+  if (sms == 0) {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (sms <= 0) sms = 1;
+  }
+  int64_t blocks = (work_items + threads - 1) / threads;
+  const int64_t cap = (int64_t)sms * 8;
+  if (blocks > cap) blocks = cap;
+  if (blocks < 1) blocks = 1;
+  return (int)blocks;
+}
+
+__device__ __forceinline__ void store_out(float* C, int64_t i, float v) { C[i] = v; }
+__device__ __forceinline__ void store_out(__half* C, int64_t i, float v) {
+  C[i] = __float2half_rn(v);
+}
+__device__ __forceinline__ float load_out(const float* C, int64_t i) { return C[i]; }
+__device__ __forceinline__ float load_out(const __half* C, int64_t i) {
+  return __half2float(C[i]);
+}
+
+// One thread per 4 consecutive columns of a row (N % 4 == 0 path reads P with
+// float4); the general path handles one element per thread.
+template <typename T>
+__global__ void splitk_reduce_vec4(int M, int N, int splits, const float* __restrict__ P, T* C,
+                                   int64_t ldc, float alpha, float beta) {
+  const int64_t quads = (int64_t)M * (N / 4);
+  const int64_t slice = (int64_t)M * N;
+  for (int64_t q = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; q < quads;
+       q += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t m = q / (N / 4);
+    const int64_t n = (q - m * (N / 4)) * 4;
+    const float* src = P + m * N + n;
+    float4 s = *reinterpret_cast<const float4*>(src);
+    for (int z = 1; z < splits; ++z) {
+      const float4 t = *reinterpret_cast<const float4*>(src + z * slice);
+      s.x += t.x; s.y += t.y; s.z += t.z; s.w += t.w;
+    }
+    const float v[4] = {s.x, s.y, s.z, s.w};
+    const int64_t base = m * ldc + n;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      float o = alpha * v[j];
+      if (beta != 0.f) o = __fmaf_rn(beta, load_out(C, base + j), o);
+      store_out(C, base + j, o);
+    }
+  }
+}
+
+template <typename T>
+__global__ void splitk_reduce_scalar(int M, int N, int splits, const float* __restrict__ P, T* C,
+                                     int64_t ldc, float alpha, float beta) {
+  const int64_t total = (int64_t)M * N;
+  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < total;
+       i += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t m = i / N, n = i - m * N;
+    float s = P[i];
+    for (int z = 1; z < splits; ++z) s += P[i + z * total];
+    float o = alpha * s;
+    if (beta != 0.f) o = __fmaf_rn(beta, load_out(C, m * ldc + n), o);
+    store_out(C, m * ldc + n, o);
+  }
+}
+
+template <typename T>
+__global__ void scale_kernel(int M, int N, T* C, int64_t ldc, float beta) {
+  const int64_t total = (int64_t)M * N;
+  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < total;
+       i += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t m = i / N, n = i - m * N;
+    const int64_t off = m * ldc + n;
+    store_out(C, off, beta != 0.f ? beta * load_out(C, off) : 0.f);
+  }
+}
+
+__global__ void repack_f16_kernel(int rows, int cols, const __half* __restrict__ src,
+                                  int64_t ld_src, __half* __restrict__ dst, int64_t ld_dst) {
+  const int64_t total = (int64_t)rows * ld_dst;
+  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < total;
+       i += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t r = i / ld_dst, c = i - r * ld_dst;
+    dst[i] = (c < cols) ? src[r * ld_src + c] : __float2half_rn(0.f);
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_splitk_reduce(int dtype, int M, int N, int splits, const float* P, void* C,
+                                 int64_t ldc, float alpha, float beta, LaunchCtx& ctx) {
+  const int threads = 256;
+  const bool vec = (N % 4) == 0;
+  const int64_t items = vec ? (int64_t)M * (N / 4) : (int64_t)M * N;
+  const int grid = grid_for(items, threads);
+  if (dtype == 0) {
+    if (vec) splitk_reduce_vec4<float><<<grid, threads, 0, ctx.stream>>>(M, N, splits, P, (float*)C, ldc, alpha, beta);
+    else splitk_reduce_scalar<float><<<grid, threads, 0, ctx.stream>>>(M, N, splits, P, (float*)C, ldc, alpha, beta);
+  } else {
+    if (vec) splitk_reduce_vec4<__half><<<grid, threads, 0, ctx.stream>>>(M, N, splits, P, (__half*)C, ldc, alpha, beta);
+    else splitk_reduce_scalar<__half><<<grid, threads, 0, ctx.stream>>>(M, N, splits, P, (__half*)C, ldc, alpha, beta);
+  }
+  cudaError_t e = cudaGetLastError();
+  if (e == cudaSuccess) ctx.launches++;
+  return e;
+}
+
+cudaError_t launch_scale(int dtype, int M, int N, void* C, int64_t ldc, float beta,
+                         LaunchCtx& ctx) {
+  const int threads = 256;
+  const int grid = grid_for((int64_t)M * N, threads);
+  if (dtype == 0) scale_kernel<float><<<grid, threads, 0, ctx.stream>>>(M, N, (float*)C, ldc, beta);
+  else scale_kernel<__half><<<grid, threads, 0, ctx.stream>>>(M, N, (__half*)C, ldc, beta);
+  cudaError_t e = cudaGetLastError();
+  if (e == cudaSuccess) ctx.launches++;
+  return e;
+}
+
+cudaError_t launch_repack_f16(int rows, int cols, const __half* src, int64_t ld_src,
+                              __half* dst, int64_t ld_dst, LaunchCtx& ctx) {
+  const int threads = 256;
+  const int grid = grid_for((int64_t)rows * ld_dst, threads);
+  repack_f16_kernel<<<grid, threads, 0, ctx.stream>>>(rows, cols, src, ld_src, dst, ld_dst);
+  cudaError_t e = cudaGetLastError();
+  if (e == cudaSuccess) ctx.launches++;
+  return e;
+}
+
+}  // namespace gb300

@@ -1,0 +1,333 @@
+// The C ABI (include/gemm.h): argument checks, variant canonicalisation,
+// kernel-path choice, scratch management, launch, device status.
+//
+// Path choice:
+//   dtype fp32 -> CUDA-core FFMA kernel (sgemm_ffma.cu); split-K when the
+//                 output has too few tiles to fill the GPU.
+//   dtype fp16 -> tcgen05 kernel (hgemm_tcgen05.cu); split-K likewise.
+// The split-K rule follows "Metal GEMM Kernels for LoRA Training", section 5
+// (route by output-tile count; fp32 partials in device memory, then a
+// reduction), with the threshold set by this GPU's SM count instead of the
+// page's fixed 32 tiles, and with K slices that need not divide K evenly.
+#include <cuda.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+#include <string.h>
+
+#include <atomic>
+#include <mutex>
+
+#include "../../include/gemm.h"
+#include "internal.h"
+
+using namespace gb300;
+
+namespace {
+
+__device__ unsigned int g_status_word;  // per device: bits of STATUS_*
+
+constexpr int MAX_DEVICES = 64;
+std::mutex g_mu;
+unsigned int* g_status_ptr[MAX_DEVICES];
+int g_num_sms[MAX_DEVICES];
+std::atomic<int64_t> g_total_launches{0};
+std::atomic<int64_t> g_timeout_ns{2000000000LL};
+std::atomic<int> g_fault_injection{0};
+thread_local int tl_last_path = GEMM_PATH_NONE;
+thread_local int tl_last_launches = 0;
+
+// Per-device set-up, done once with that device current: the status word's
+// device address and the SM count.
+int device_state(int* dev_out, unsigned int** status, int* sms) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return GEMM_ERR_CUDA;
+  if (dev < 0 || dev >= MAX_DEVICES) return GEMM_ERR_UNSUPPORTED;
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (!g_status_ptr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_status_word) != cudaSuccess) return GEMM_ERR_CUDA;
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      return GEMM_ERR_CUDA;
+    g_num_sms[dev] = n > 0 ? n : 1;
+    g_status_ptr[dev] = static_cast<unsigned int*>(p);
+  }
+  *dev_out = dev;
+  *status = g_status_ptr[dev];
+  *sms = g_num_sms[dev];
+  return GEMM_OK;
+}
+
+inline int64_t footprint_bytes(int64_t rows, int64_t cols, int64_t ld, int64_t e) {
+  if (rows <= 0 || cols <= 0) return 0;
+  return ((rows - 1) * ld + cols) * e;
+}
+
+inline bool overlaps(const void* a, int64_t na, const void* b, int64_t nb) {
+  if (na <= 0 || nb <= 0) return false;
+  const uintptr_t a0 = (uintptr_t)a, b0 = (uintptr_t)b;
+  return a0 < b0 + (uintptr_t)nb && b0 < a0 + (uintptr_t)na;
+}
+
+// Checks shared by gemm() and gemm_host().  Sets the stored shapes of A and B.
+int check_args(int transA, int transB, int64_t M, int64_t N, int64_t K, int dtype,
+               const void* A, int64_t lda, const void* B, int64_t ldb, const void* C,
+               int64_t ldc, int64_t* a_rows, int64_t* a_cols, int64_t* b_rows,
+               int64_t* b_cols) {
+  if ((transA != 0 && transA != 1) || (transB != 0 && transB != 1)) return GEMM_ERR_INVALID_ARG;
+  if (dtype != GEMM_F32 && dtype != GEMM_F16_F32ACC) return GEMM_ERR_INVALID_ARG;
+  if (M < 0 || N < 0 || K < 0) return GEMM_ERR_INVALID_ARG;
+  const int64_t lim = (int64_t)1 << 31;
+  if (M >= lim || N >= lim || K >= lim) return GEMM_ERR_UNSUPPORTED;
+  *a_rows = transA ? K : M;
+  *a_cols = transA ? M : K;
+  *b_rows = transB ? N : K;
+  *b_cols = transB ? K : N;
+  if (ldc < (N > 1 ? N : 1)) return GEMM_ERR_INVALID_ARG;
+  if (lda < (*a_cols > 1 ? *a_cols : 1)) return GEMM_ERR_INVALID_ARG;
+  if (ldb < (*b_cols > 1 ? *b_cols : 1)) return GEMM_ERR_INVALID_ARG;
+  if (M == 0 || N == 0) return GEMM_OK;
+  const int64_t e = dtype == GEMM_F32 ? 4 : 2;
+  if (!C || ((uintptr_t)C % (uintptr_t)e) != 0) return GEMM_ERR_INVALID_ARG;
+  if (K > 0) {
+    if (!A || !B) return GEMM_ERR_INVALID_ARG;
+    if (((uintptr_t)A % (uintptr_t)e) != 0 || ((uintptr_t)B % (uintptr_t)e) != 0)
+      return GEMM_ERR_INVALID_ARG;
+    const int64_t nc = footprint_bytes(M, N, ldc, e);
+    if (overlaps(C, nc, A, footprint_bytes(*a_rows, *a_cols, lda, e)) ||
+        overlaps(C, nc, B, footprint_bytes(*b_rows, *b_cols, ldb, e)))
+      return GEMM_ERR_ALIAS;
+  }
+  return GEMM_OK;
+}
+
+int cuda_fail(cudaError_t e) { return e == cudaErrorMemoryAllocation ? GEMM_ERR_NO_MEMORY : GEMM_ERR_CUDA; }
+
+// Split-K plan: how many K slices, each a multiple of `kstep` long.
+void plan_splits(int64_t tiles, int64_t K, int kstep, int capacity, int min_steps_per_slice,
+                 int max_splits, int* splits, int* k_slice) {
+  const int64_t steps = (K + kstep - 1) / kstep;
+  int s = 1;
+  if (tiles * 2 <= capacity && steps >= 2 * min_steps_per_slice) {
+    int64_t want = capacity / (tiles > 0 ? tiles : 1);
+    int64_t cap_k = steps / min_steps_per_slice;
+    int64_t ss = want < cap_k ? want : cap_k;
+    if (ss > max_splits) ss = max_splits;
+    s = ss > 1 ? (int)ss : 1;
+  }
+  if (s <= 1) {
+    *splits = 1;
+    *k_slice = (int)(steps * kstep);
+    return;
+  }
+  const int64_t per = (steps + s - 1) / s;  // steps per slice
+  *k_slice = (int)(per * kstep);
+  *splits = (int)((steps + per - 1) / per);  // every slice non-empty
+}
+
+struct Scratch {
+  void* ptr = nullptr;
+  cudaStream_t stream = nullptr;
+  ~Scratch() {
+    if (ptr) cudaFreeAsync(ptr, stream);
+  }
+  cudaError_t get(size_t bytes, cudaStream_t s) {
+    stream = s;
+    return cudaMallocAsync(&ptr, bytes, s);
+  }
+};
+
+int run_gemm(int transA, int transB, int64_t M64, int64_t N64, int64_t K64, int dtype,
+             float alpha, float beta, const void* A, int64_t lda, const void* B, int64_t ldb,
+             void* C, int64_t ldc, cudaStream_t stream, int64_t a_rows, int64_t a_cols,
+             int64_t b_rows, int64_t b_cols) {
+  int dev, sms;
+  unsigned int* status;
+  int rc = device_state(&dev, &status, &sms);
+  if (rc != GEMM_OK) return rc;
+  LaunchCtx ctx{stream, status, (uint64_t)g_timeout_ns.load(), 0};
+  const int M = (int)M64, N = (int)N64, K = (int)K64;
+  int path = GEMM_PATH_NONE;
+  cudaError_t e = cudaSuccess;
+
+  if (K == 0) {
+    path = GEMM_PATH_SCALE;
+    e = launch_scale(dtype, M, N, C, ldc, beta, ctx);
+  } else if (dtype == GEMM_F32) {
+    const int64_t tiles = (int64_t)((M + SG_BM - 1) / SG_BM) * ((N + SG_BN - 1) / SG_BN);
+    int splits, k_slice;
+    plan_splits(tiles, K, SG_BK, 2 * sms, 8, 16, &splits, &k_slice);
+    SgemmArgs a{transA, transB, M, N, K, (const float*)A, lda, (const float*)B, ldb, (float*)C,
+                ldc, alpha, beta, splits, k_slice, nullptr};
+    Scratch ws;
+    if (splits > 1) {
+      e = ws.get((size_t)splits * M * N * sizeof(float), stream);
+      if (e != cudaSuccess) return cuda_fail(e);
+      a.partial = (float*)ws.ptr;
+    }
+    path = splits > 1 ? GEMM_PATH_FFMA_SPLITK : GEMM_PATH_FFMA;
+    e = launch_sgemm(a, ctx);
+    if (e == cudaSuccess && splits > 1)
+      e = launch_splitk_reduce(0, M, N, splits, a.partial, C, ldc, alpha, beta, ctx);
+  } else {
+    const int bn = hgemm_pick_bn(N, transB);
+    const int64_t tiles = (int64_t)((M + HG_BM - 1) / HG_BM) * ((N + bn - 1) / bn);
+    int splits, k_slice;
+    plan_splits(tiles, K, HG_BK, sms, 4, 32, &splits, &k_slice);
+    // The tensor-memory-access unit needs 16-byte aligned bases and row
+    // pitches; an operand that has neither is copied into padded scratch.
+    const __half* Ad = (const __half*)A;
+    const __half* Bd = (const __half*)B;
+    int64_t ldad = lda, ldbd = ldb;
+    const bool a_ok = ((uintptr_t)A % 16) == 0 && (lda % 8) == 0;
+    const bool b_ok = ((uintptr_t)B % 16) == 0 && (ldb % 8) == 0;
+    const int64_t lda_p = (a_cols + 7) / 8 * 8, ldb_p = (b_cols + 7) / 8 * 8;
+    size_t bytes_a = a_ok ? 0 : (size_t)(a_rows * lda_p * 2 + 255) / 256 * 256;
+    size_t bytes_b = b_ok ? 0 : (size_t)(b_rows * ldb_p * 2 + 255) / 256 * 256;
+    size_t bytes_p = splits > 1 ? (size_t)splits * M * N * sizeof(float) : 0;
+    Scratch ws;
+    if (bytes_a + bytes_b + bytes_p > 0) {
+      e = ws.get(bytes_a + bytes_b + bytes_p, stream);
+      if (e != cudaSuccess) return cuda_fail(e);
+    }
+    char* wp = (char*)ws.ptr;
+    if (!a_ok) {
+      __half* dst = (__half*)wp;
+      e = launch_repack_f16((int)a_rows, (int)a_cols, Ad, lda, dst, lda_p, ctx);
+      Ad = dst; ldad = lda_p; wp += bytes_a;
+    }
+    if (e == cudaSuccess && !b_ok) {
+      __half* dst = (__half*)wp;
+      e = launch_repack_f16((int)b_rows, (int)b_cols, Bd, ldb, dst, ldb_p, ctx);
+      Bd = dst; ldbd = ldb_p; wp += bytes_b;
+    }
+    if (e == cudaSuccess) {
+      HgemmArgs a{transA, transB, M, N, K, Ad, ldad, Bd, ldbd, (__half*)C, ldc, alpha, beta,
+                  splits, k_slice, splits > 1 ? (float*)wp : nullptr, sms,
+                  g_fault_injection.load()};
+      path = splits > 1 ? GEMM_PATH_TC_SPLITK : GEMM_PATH_TC;
+      e = launch_hgemm(a, ctx);
+      if (e == cudaSuccess && splits > 1)
+        e = launch_splitk_reduce(1, M, N, splits, a.partial, C, ldc, alpha, beta, ctx);
+    }
+  }
+  g_total_launches += ctx.launches;
+  if (e != cudaSuccess) {
+    tl_last_path = GEMM_PATH_NONE;
+    tl_last_launches = ctx.launches;
+    return cuda_fail(e);
+  }
+  tl_last_path = path;
+  tl_last_launches = ctx.launches;
+  return GEMM_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int gemm(int transA, int transB, int64_t M, int64_t N, int64_t K, int dtype, float alpha,
+         float beta, const void* A, int64_t lda, const void* B, int64_t ldb, void* C,
+         int64_t ldc, gemm_stream_t stream) {
+  int64_t ar, ac, br, bc;
+  tl_last_path = GEMM_PATH_NONE;
+  tl_last_launches = 0;
+  int rc = check_args(transA, transB, M, N, K, dtype, A, lda, B, ldb, C, ldc, &ar, &ac, &br, &bc);
+  if (rc != GEMM_OK) return rc;
+  if (M == 0 || N == 0) return GEMM_OK;
+  return run_gemm(transA, transB, M, N, K, dtype, alpha, beta, A, lda, B, ldb, C, ldc,
+                  (cudaStream_t)stream, ar, ac, br, bc);
+}
+
+int gemm_host(int transA, int transB, int64_t M, int64_t N, int64_t K, int dtype, float alpha,
+              float beta, const void* A, int64_t lda, const void* B, int64_t ldb, void* C,
+              int64_t ldc, gemm_stream_t stream_) {
+  int64_t ar, ac, br, bc;
+  tl_last_path = GEMM_PATH_NONE;
+  tl_last_launches = 0;
+  int rc = check_args(transA, transB, M, N, K, dtype, A, lda, B, ldb, C, ldc, &ar, &ac, &br, &bc);
+  if (rc != GEMM_OK) return rc;
+  if (M == 0 || N == 0) return GEMM_OK;
+  cudaStream_t stream = (cudaStream_t)stream_;
+  const int64_t e = dtype == GEMM_F32 ? 4 : 2;
+  const int64_t align = 16 / e;  // device pitch: whole 16-byte units
+  const int64_t lda_d = (ac + align - 1) / align * align;
+  const int64_t ldb_d = (bc + align - 1) / align * align;
+  const int64_t ldc_d = (N + align - 1) / align * align;
+  const size_t nA = K > 0 ? (size_t)(ar * lda_d * e + 255) / 256 * 256 : 0;
+  const size_t nB = K > 0 ? (size_t)(br * ldb_d * e + 255) / 256 * 256 : 0;
+  const size_t nC = (size_t)(M * ldc_d * e + 255) / 256 * 256;
+  Scratch buf;
+  cudaError_t ce = buf.get(nA + nB + nC, stream);
+  if (ce != cudaSuccess) return cuda_fail(ce);
+  char* dA = (char*)buf.ptr;
+  char* dB = dA + nA;
+  char* dC = dB + nB;
+  if (K > 0) {
+    ce = cudaMemcpy2DAsync(dA, lda_d * e, A, lda * e, ac * e, ar, cudaMemcpyHostToDevice, stream);
+    if (ce == cudaSuccess)
+      ce = cudaMemcpy2DAsync(dB, ldb_d * e, B, ldb * e, bc * e, br, cudaMemcpyHostToDevice,
+                             stream);
+  }
+  if (ce == cudaSuccess && beta != 0.f)
+    ce = cudaMemcpy2DAsync(dC, ldc_d * e, C, ldc * e, N * e, M, cudaMemcpyHostToDevice, stream);
+  if (ce != cudaSuccess) return cuda_fail(ce);
+  rc = run_gemm(transA, transB, M, N, K, dtype, alpha, beta, dA, lda_d, dB, ldb_d, dC, ldc_d,
+                stream, ar, ac, br, bc);
+  if (rc != GEMM_OK) return rc;
+  const int path = tl_last_path, launches = tl_last_launches;
+  ce = cudaMemcpy2DAsync(C, ldc * e, dC, ldc_d * e, N * e, M, cudaMemcpyDeviceToHost, stream);
+  if (ce != cudaSuccess) return cuda_fail(ce);
+  cudaFreeAsync(buf.ptr, stream);
+  buf.ptr = nullptr;
+  ce = cudaStreamSynchronize(stream);
+  tl_last_path = path;
+  tl_last_launches = launches;
+  return ce == cudaSuccess ? GEMM_OK : GEMM_ERR_CUDA;
+}
+
+int gemm_check_device_status(gemm_stream_t stream) {
+  int dev, sms;
+  unsigned int* status;
+  int rc = device_state(&dev, &status, &sms);
+  if (rc != GEMM_OK) return rc;
+  if (cudaStreamSynchronize((cudaStream_t)stream) != cudaSuccess) return GEMM_ERR_CUDA;
+  unsigned int word = 0;
+  if (cudaMemcpy(&word, status, sizeof(word), cudaMemcpyDeviceToHost) != cudaSuccess)
+    return GEMM_ERR_CUDA;
+  if (word != 0) {
+    const unsigned int zero = 0;
+    if (cudaMemcpy(status, &zero, sizeof(zero), cudaMemcpyHostToDevice) != cudaSuccess)
+      return GEMM_ERR_CUDA;
+    return GEMM_ERR_TIMEOUT;
+  }
+  return GEMM_OK;
+}
+
+const char* gemm_status_string(int status) {
+  switch (status) {
+    case GEMM_OK: return "GEMM_OK";
+    case GEMM_ERR_INVALID_ARG: return "GEMM_ERR_INVALID_ARG";
+    case GEMM_ERR_UNSUPPORTED: return "GEMM_ERR_UNSUPPORTED";
+    case GEMM_ERR_ALIAS: return "GEMM_ERR_ALIAS";
+    case GEMM_ERR_CUDA: return "GEMM_ERR_CUDA";
+    case GEMM_ERR_NO_MEMORY: return "GEMM_ERR_NO_MEMORY";
+    case GEMM_ERR_TIMEOUT: return "GEMM_ERR_TIMEOUT";
+    default: return "GEMM_ERR_UNKNOWN";
+  }
+}
+
+int gemm_version(void) { return (1 << 16) | 0; }
+
+int gemm_last_path(void) { return tl_last_path; }
+int gemm_last_launches(void) { return tl_last_launches; }
+int64_t gemm_total_launches(void) { return g_total_launches.load(); }
+
+void gemm_set_wait_timeout_ns(int64_t ns) {
+  g_timeout_ns.store(ns > 0 ? ns : 2000000000LL);
+}
+
+void gemm_set_fault_injection(int mode) { g_fault_injection.store(mode); }
+
+}  // extern "C"

@@ -1,0 +1,468 @@
+// fp16-operand / fp32-accumulate / fp16-output GEMM on the 5th-generation
+// tensor cores (tcgen05.mma, accumulators in tensor memory).
+//
+//   C = alpha * op(A) * op(B) + beta * C, variants nn / tn / nt (and tt).
+//
+// The regime is that of "Metal GEMM Kernels for LoRA Training on Apple
+// Silicon": fp16 operands with fp32 accumulation (section 1, type table), the
+// fp32 accumulator converted to fp16 on the way out (section 2), the three
+// transpose variants of the section 2 table, and fp32 partial sums plus a
+// reduction for skinny shapes (section 5, split-K).  The Metal design there (one
+// 32 x 32 simdgroup tile, staged output) is prior art only; this kernel is
+// built for sm_103a:
+//
+//  * Persistent, warp-specialised block of 6 warps, one block per SM:
+//      warp 0      TMA producer (one elected lane)
+//      warp 1      TMEM allocator + MMA issuer (one elected lane)
+//      warps 2..5  epilogue (128 threads = the 128 accumulator rows)
+//  * Operand tiles reach shared memory by TMA (cp.async.bulk.tensor) with the
+//    128-byte swizzle, through a ring of STAGES buffers guarded by mbarriers
+//    (full: TMA bytes landed; empty: the MMAs reading the buffer finished).
+//    Out-of-range rows/columns of edge tiles are zero-filled by the TMA unit.
+//  * The transposed operand is not moved: a K-contiguous operand (A[M,K],
+//    B[N,K]) is described to the tensor core as K-major, an MN-contiguous one
+//    (A[K,M], B[K,N]) as MN-major, by the shared-memory descriptor layout and
+//    the instruction descriptor's major bits.  Section 3 of the LoRA page
+//    found the transposed operand's cost in staging instructions; here there
+//    are none.
+//  * The 128 x BN fp32 accumulator lives in tensor memory, double buffered,
+//    so the epilogue of one tile overlaps the main loop of the next.
+//  * Fused epilogue: tcgen05.ld -> alpha * acc + beta * C_old -> fp16
+//    (round to nearest even) -> global; or raw fp32 partial sums (split-K).
+//
+// Every mbarrier wait is bounded (see common.cuh); on expiry the block stops
+// issuing work, drains its in-flight copies and MMAs, frees its tensor memory
+// and returns, leaving GEMM_ERR_TIMEOUT in the device status word.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace gb300 {
+namespace {
+
+constexpr int BM = HG_BM;     // 128 accumulator rows = 128 TMEM lanes
+constexpr int BK = HG_BK;     // 64 fp16 = 128 bytes = one swizzle atom row
+constexpr int UMMA_K = 16;    // K per tcgen05.mma kind::f16
+constexpr int THREADS = 192;
+constexpr int GROUP_M = 8;
+constexpr int A_TILE_BYTES = BM * BK * 2;  // 16 KiB
+constexpr int SMEM_BUDGET = 200 * 1024;
+
+template <int BN, bool B_MN>
+struct Cfg {
+  // An MN-major B tile is stored as 64-wide swizzle atoms, so it is at least
+  // one atom wide; the MMA reads only the first BN columns.
+  static constexpr int B_COLS = B_MN ? (BN < 64 ? 64 : BN) : BN;
+  static constexpr int B_TILE_BYTES = B_COLS * BK * 2;
+  static constexpr int STAGE_BYTES = A_TILE_BYTES + B_TILE_BYTES;
+  static constexpr int STAGES_RAW = SMEM_BUDGET / STAGE_BYTES;
+  static constexpr int STAGES = STAGES_RAW > 8 ? 8 : STAGES_RAW;
+  static constexpr int TMEM_COLS = (2 * BN < 32) ? 32 : 2 * BN;  // power of two for BN in {32..256}
+  static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 /*align*/ + 256 /*barriers*/;
+};
+
+struct HParams {
+  __half* C;
+  float* partial;
+  int64_t ldc;
+  int M, N, K;
+  int k_slice;
+  int tiles_m, tiles_n, splits;
+  float alpha, beta;
+  unsigned int* status;
+  uint64_t timeout_ns;
+  int fault_injection;
+  int c_vec_ok;  // C base 16-byte aligned and ldc % 8 == 0
+};
+
+// tcgen05 shared-memory matrix descriptor, 128-byte swizzle:
+//   bits  0-13  start address >> 4
+//   bits 16-29  leading-dimension byte offset >> 4
+//   bits 32-45  stride-dimension byte offset >> 4
+//   bits 46-48  fixed 0b001
+//   bits 61-63  layout: 2 = 128-byte swizzle
+// K-major:  rows of 128 B (64 fp16 along K), 8-row groups 1024 B apart (SBO);
+//           the leading offset is unused for a swizzled K-major operand.
+// MN-major: rows of 128 B (64 fp16 along M or N) indexed by k; 8-k-row groups
+//           1024 B apart (SBO); 64-wide M/N atoms BK*128 B apart (LBO).
+__device__ __forceinline__ uint64_t make_sdesc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+  return (uint64_t)((saddr & 0x3FFFFu) >> 4) | ((uint64_t)((lbo >> 4) & 0x3FFFu) << 16) |
+         ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46) | (2ull << 61);
+}
+
+// Instruction descriptor, kind::f16: D fp32 (bits 4-5 = 1), A and B fp16
+// (bits 7-9, 10-12 = 0), A major (bit 15), B major (bit 16; 1 = MN-major),
+// N >> 3 (bits 17-22), M >> 4 (bits 24-28).
+template <int BN, bool A_MN, bool B_MN>
+__device__ __forceinline__ constexpr uint32_t make_idesc() {
+  return (1u << 4) | ((A_MN ? 1u : 0u) << 15) | ((B_MN ? 1u : 0u) << 16) |
+         ((uint32_t)(BN >> 3) << 17) | ((uint32_t)(BM >> 4) << 24);
+}
+
+__device__ __forceinline__ void unit_coords(int u, const HParams& p, int& m0, int& n0, int& kbeg,
+                                            int& nkb) {
+  const int tiles = p.tiles_m * p.tiles_n;
+  const int z = u / tiles;
+  const int t = u - z * tiles;
+  const int per_group = GROUP_M * p.tiles_n;
+  const int first_m = (t / per_group) * GROUP_M;
+  const int gsize = min(p.tiles_m - first_m, GROUP_M);
+  const int tm = first_m + (t % per_group) % gsize;
+  const int tn = (t % per_group) / gsize;
+  m0 = tm * BM;
+  kbeg = z * p.k_slice;
+  const int kend = min(p.K, kbeg + p.k_slice);
+  nkb = (kend - kbeg + BK - 1) / BK;
+  n0 = tn;  // scaled by BN by the caller
+}
+
+template <int BN, bool A_MN, bool B_MN, bool SPLIT>
+__global__ void __launch_bounds__(THREADS, 1)
+    hgemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
+                    const __grid_constant__ CUtensorMap tmB, const HParams p) {
+  using C_ = Cfg<BN, B_MN>;
+  constexpr int STAGES = C_::STAGES;
+  constexpr uint32_t STAGE_TX = (uint32_t)C_::STAGE_BYTES;
+
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw_addr = smem_u32(smem_raw);
+  const uint32_t tiles_addr = (raw_addr + 1023u) & ~1023u;  // swizzle atoms need 1 KiB alignment
+  uint8_t* const tiles_ptr = smem_raw + (tiles_addr - raw_addr);
+  uint64_t* const bars = reinterpret_cast<uint64_t*>(tiles_ptr + STAGES * C_::STAGE_BYTES);
+  // barrier layout: full[STAGES], empty[STAGES], acc_full[2], acc_empty[2], drain
+  const uint32_t bar0 = smem_u32(bars);
+  auto full_bar = [&](int s) { return bar0 + 8u * (uint32_t)s; };
+  auto empty_bar = [&](int s) { return bar0 + 8u * (uint32_t)(STAGES + s); };
+  auto accf_bar = [&](int b) { return bar0 + 8u * (uint32_t)(2 * STAGES + b); };
+  auto acce_bar = [&](int b) { return bar0 + 8u * (uint32_t)(2 * STAGES + 2 + b); };
+  const uint32_t drain_bar = bar0 + 8u * (uint32_t)(2 * STAGES + 4);
+  uint32_t* const tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * STAGES + 5);
+  volatile uint32_t* const abort_flag = tmem_slot + 1;
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(full_bar(s), 1);
+      mbar_init(empty_bar(s), 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(accf_bar(b), 1);
+      mbar_init(acce_bar(b), 128);
+    }
+    mbar_init(drain_bar, 1);
+    *abort_flag = 0u;
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(tmem_slot), (uint32_t)C_::TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  const WaitCtl wc{p.status, abort_flag, p.timeout_ns};
+  const int total_units = p.tiles_m * p.tiles_n * p.splits;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      tma_prefetch_desc(&tmA);
+      tma_prefetch_desc(&tmB);
+      int stage = 0;
+      uint32_t phase = 0;
+      uint32_t pending = 0, pend_phase = 0;  // per-stage: last load issued / its parity
+      bool first = true;
+      bool ok = true;
+      for (int u = blockIdx.x; u < total_units && ok; u += gridDim.x) {
+        int m0, tn, kbeg, nkb;
+        unit_coords(u, p, m0, tn, kbeg, nkb);
+        const int n0 = tn * BN;
+        for (int kb = 0; kb < nkb; ++kb) {
+          if (!mbar_wait(empty_bar(stage), phase ^ 1u, wc)) { ok = false; break; }
+          const int k0 = kbeg + kb * BK;
+          const bool skip = first && p.fault_injection == 1;
+          first = false;
+          if (!skip) {
+            const uint32_t sa = tiles_addr + (uint32_t)(stage * C_::STAGE_BYTES);
+            const uint32_t sb = sa + (uint32_t)A_TILE_BYTES;
+            mbar_arrive_expect_tx(full_bar(stage), STAGE_TX);
+            if constexpr (A_MN) {
+              tma_load_2d(sa, &tmA, m0, k0, full_bar(stage));
+              tma_load_2d(sa + 8192u, &tmA, m0 + 64, k0, full_bar(stage));
+            } else {
+              tma_load_2d(sa, &tmA, k0, m0, full_bar(stage));
+            }
+            if constexpr (B_MN) {
+#pragma unroll
+              for (int h = 0; h < C_::B_COLS / 64; ++h)
+                tma_load_2d(sb + (uint32_t)h * 8192u, &tmB, n0 + 64 * h, k0, full_bar(stage));
+            } else {
+              tma_load_2d(sb, &tmB, k0, n0, full_bar(stage));
+            }
+            pending |= 1u << stage;
+            pend_phase = (pend_phase & ~(1u << stage)) | (phase << stage);
+          } else {
+            pending &= ~(1u << stage);
+          }
+          if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+        }
+      }
+      // Drain: every load issued must land before the block can exit.
+      for (int s = 0; s < STAGES; ++s)
+        if (pending & (1u << s)) mbar_wait_drain(full_bar(s), (pend_phase >> s) & 1u, p.timeout_ns);
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t idesc = make_idesc<BN, A_MN, B_MN>();
+      int stage = 0;
+      uint32_t phase = 0;
+      int it = 0;
+      bool ok = true;
+      for (int u = blockIdx.x; u < total_units && ok; u += gridDim.x, ++it) {
+        int m0, tn, kbeg, nkb;
+        unit_coords(u, p, m0, tn, kbeg, nkb);
+        const int buf = it & 1;
+        const uint32_t acc_phase = (uint32_t)(it >> 1) & 1u;
+        if (!mbar_wait(acce_bar(buf), acc_phase ^ 1u, wc)) { ok = false; break; }
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + (uint32_t)(buf * BN);
+        for (int kb = 0; kb < nkb; ++kb) {
+          if (!mbar_wait(full_bar(stage), phase, wc)) { ok = false; break; }
+          tc_fence_after();
+          const uint32_t sa = tiles_addr + (uint32_t)(stage * C_::STAGE_BYTES);
+          const uint32_t sb = sa + (uint32_t)A_TILE_BYTES;
+#pragma unroll
+          for (int kk = 0; kk < BK / UMMA_K; ++kk) {
+            uint64_t ad, bd;
+            if constexpr (A_MN) ad = make_sdesc(sa + (uint32_t)kk * 2048u, 8192u, 1024u);
+            else ad = make_sdesc(sa + (uint32_t)kk * 32u, 16u, 1024u);
+            if constexpr (B_MN) bd = make_sdesc(sb + (uint32_t)kk * 2048u, 8192u, 1024u);
+            else bd = make_sdesc(sb + (uint32_t)kk * 32u, 16u, 1024u);
+            tc_mma_f16(d_tmem, ad, bd, idesc, (kb | kk) != 0 ? 1u : 0u);
+          }
+          tc_commit(empty_bar(stage));  // buffer free once these MMAs finish
+          if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+        }
+        if (!ok) break;
+        tc_commit(accf_bar(buf));  // accumulator complete
+      }
+      // Drain: every MMA issued must finish before tensor memory is freed.
+      tc_commit(drain_bar);
+      mbar_wait_drain(drain_bar, 0u, p.timeout_ns);
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const int q = warp & 3;  // this warp may access TMEM lanes 32q .. 32q+31
+    const int row = q * 32 + lane;
+    int it = 0;
+    for (int u = blockIdx.x; u < total_units; u += gridDim.x, ++it) {
+      int m0, tn, kbeg, nkb;
+      unit_coords(u, p, m0, tn, kbeg, nkb);
+      const int n0 = tn * BN;
+      const int buf = it & 1;
+      const uint32_t acc_phase = (uint32_t)(it >> 1) & 1u;
+      // one lane waits, the warp follows: the TMEM loads below are
+      // warp-collective, so the whole warp must take the same branch
+      bool got = false;
+      if (lane == 0) got = mbar_wait(accf_bar(buf), acc_phase, wc);
+      got = __shfl_sync(0xffffffffu, got ? 1 : 0, 0) != 0;
+      if (!got) break;
+      tc_fence_after();
+      const int gm = m0 + row;
+      const uint32_t t_row = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(buf * BN);
+      const int z = u / (p.tiles_m * p.tiles_n);
+#pragma unroll 1
+      for (int c = 0; c < BN / 32; ++c) {
+        uint32_t r[32];
+        __syncwarp();
+        tmem_ld_32x32b_x32(t_row + (uint32_t)(c * 32), r);
+        tmem_ld_wait();
+        if (c == BN / 32 - 1) {
+          tc_fence_before();
+          mbar_arrive(acce_bar(buf));  // accumulator buffer may be overwritten
+        }
+        if (gm >= p.M) continue;  // rows past M: loaded (warp-collective) but not stored
+        const int gn0 = n0 + c * 32;
+        if constexpr (SPLIT) {
+          float* dst = p.partial + ((int64_t)z * p.M + gm) * p.N + gn0;
+          if (gn0 + 31 < p.N && (p.N & 3) == 0) {
+#pragma unroll
+            for (int v = 0; v < 8; ++v)
+              reinterpret_cast<float4*>(dst)[v] =
+                  make_float4(__uint_as_float(r[4 * v]), __uint_as_float(r[4 * v + 1]),
+                              __uint_as_float(r[4 * v + 2]), __uint_as_float(r[4 * v + 3]));
+          } else {
+            for (int j = 0; j < 32; ++j)
+              if (gn0 + j < p.N) dst[j] = __uint_as_float(r[j]);
+          }
+        } else {
+          __half* dst = p.C + (int64_t)gm * p.ldc + gn0;
+          float v[32];
+#pragma unroll
+          for (int j = 0; j < 32; ++j) v[j] = p.alpha * __uint_as_float(r[j]);
+          const bool full = (gn0 + 31 < p.N) && p.c_vec_ok;
+          if (full) {
+            if (p.beta != 0.f) {
+#pragma unroll
+              for (int w = 0; w < 4; ++w) {
+                const uint4 cv = reinterpret_cast<const uint4*>(dst)[w];
+                const __half2* ch = reinterpret_cast<const __half2*>(&cv);
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                  const float2 f = __half22float2(ch[e]);
+                  v[8 * w + 2 * e] = __fmaf_rn(p.beta, f.x, v[8 * w + 2 * e]);
+                  v[8 * w + 2 * e + 1] = __fmaf_rn(p.beta, f.y, v[8 * w + 2 * e + 1]);
+                }
+              }
+            }
+#pragma unroll
+            for (int w = 0; w < 4; ++w) {
+              uint4 o;
+              __half2* oh = reinterpret_cast<__half2*>(&o);
+#pragma unroll
+              for (int e = 0; e < 4; ++e)
+                oh[e] = __halves2half2(__float2half_rn(v[8 * w + 2 * e]),
+                                       __float2half_rn(v[8 * w + 2 * e + 1]));
+              reinterpret_cast<uint4*>(dst)[w] = o;
+            }
+          } else {
+            for (int j = 0; j < 32; ++j) {
+              if (gn0 + j < p.N) {
+                float o = v[j];
+                if (p.beta != 0.f) o = __fmaf_rn(p.beta, __half2float(dst[j]), o);
+                dst[j] = __float2half_rn(o);
+              }
+            }
+          }
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem_base, (uint32_t)C_::TMEM_COLS);
+  }
+}
+
+// ---------------------------------------------------------------- host side
+PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static bool tried = false;
+  if (!tried) {
+    tried = true;
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000,
+                                         cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+  }
+  return fn;
+}
+
+// 2-D fp16 tensor map over a row-major [rows, cols] array with row pitch
+// `ld` elements; box = box_cols (inner) x box_rows, 128-byte swizzle,
+// out-of-range elements read as zero.
+bool make_map(CUtensorMap* map, const void* base, int64_t rows, int64_t cols, int64_t ld,
+              int box_cols, int box_rows) {
+  auto enc = get_encode();
+  if (!enc) return false;
+  cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)(ld * 2)};
+  cuuint32_t box[2] = {(cuuint32_t)box_cols, (cuuint32_t)box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void*>(base), dims,
+                   strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                   CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+template <int BN, bool A_MN, bool B_MN, bool SPLIT>
+cudaError_t launch_cfg(const HgemmArgs& a, const HParams& p, LaunchCtx& ctx) {
+  using C_ = Cfg<BN, B_MN>;
+  CUtensorMap mA, mB;
+  bool ok;
+  if (A_MN) ok = make_map(&mA, a.A, a.K, a.M, a.lda, 64, 64);     // stored [K, M]
+  else ok = make_map(&mA, a.A, a.M, a.K, a.lda, 64, BM);          // stored [M, K]
+  if (!ok) return cudaErrorInvalidValue;
+  if (B_MN) ok = make_map(&mB, a.B, a.K, a.N, a.ldb, 64, 64);     // stored [K, N]
+  else ok = make_map(&mB, a.B, a.N, a.K, a.ldb, 64, BN);          // stored [N, K]
+  if (!ok) return cudaErrorInvalidValue;
+  auto kern = hgemm_tc_kernel<BN, A_MN, B_MN, SPLIT>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       C_::SMEM_BYTES);
+  if (e != cudaSuccess) return e;
+  const int units = p.tiles_m * p.tiles_n * p.splits;
+  const int grid = units < a.num_sms ? units : a.num_sms;
+  kern<<<grid, THREADS, C_::SMEM_BYTES, ctx.stream>>>(mA, mB, p);
+  e = cudaGetLastError();
+  if (e == cudaSuccess) ctx.launches++;
+  return e;
+}
+
+template <int BN>
+cudaError_t launch_bn(const HgemmArgs& a, const HParams& p, LaunchCtx& ctx) {
+  const bool A_MN = a.transA != 0, B_MN = a.transB == 0, split = a.splits > 1;
+#define GB300_HG(AM, BMN)                                                   \
+  if (A_MN == AM && B_MN == BMN)                                            \
+    return split ? launch_cfg<BN, AM, BMN, true>(a, p, ctx)                 \
+                 : launch_cfg<BN, AM, BMN, false>(a, p, ctx);
+  GB300_HG(false, true)
+  GB300_HG(true, true)
+  GB300_HG(false, false)
+  GB300_HG(true, false)
+#undef GB300_HG
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace
+
+int hgemm_pick_bn(int N, int transB) {
+  // An MN-major B (transB == 0) is staged in 64-column swizzle atoms, so its
+  // narrowest tile is 64 columns; a K-major B can go down to 32.
+  if (N <= 32 && transB) return 32;
+  if (N <= 64) return 64;
+  if (N <= 128) return 128;
+  return 256;
+}
+
+cudaError_t launch_hgemm(const HgemmArgs& a, LaunchCtx& ctx) {
+  HParams p;
+  p.C = a.C;
+  p.partial = a.partial;
+  p.ldc = a.ldc;
+  p.M = a.M; p.N = a.N; p.K = a.K;
+  p.splits = a.splits > 1 ? a.splits : 1;
+  p.k_slice = a.splits > 1 ? a.k_slice : ((a.K + BK - 1) / BK) * BK;
+  const int bn = hgemm_pick_bn(a.N, a.transB);
+  p.tiles_m = (a.M + BM - 1) / BM;
+  p.tiles_n = (a.N + bn - 1) / bn;
+  p.alpha = a.alpha; p.beta = a.beta;
+  p.status = ctx.status;
+  p.timeout_ns = ctx.timeout_ns;
+  p.fault_injection = a.fault_injection;
+  p.c_vec_ok = ((reinterpret_cast<uintptr_t>(a.C) & 15u) == 0 && (a.ldc % 8) == 0) ? 1 : 0;
+  switch (bn) {
+    case 32: return launch_bn<32>(a, p, ctx);
+    case 64: return launch_bn<64>(a, p, ctx);
+    case 128: return launch_bn<128>(a, p, ctx);
+    default: return launch_bn<256>(a, p, ctx);
+  }
+}
+
+}  // namespace gb300

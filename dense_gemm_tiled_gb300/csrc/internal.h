@@ -1,0 +1,71 @@
+// Host-side declarations shared by the library's translation units.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace gb300 {
+
+// One fp32 GEMM launch over a K range per grid z-slice.
+struct SgemmArgs {
+  int transA, transB;
+  int M, N, K;
+  const float* A;
+  int64_t lda;
+  const float* B;
+  int64_t ldb;
+  float* C;
+  int64_t ldc;
+  float alpha, beta;
+  // split-K: slice z covers k in [z*k_slice, min(K, (z+1)*k_slice)); when
+  // splits > 1 the kernel writes raw sums to partial[z][M][N] instead of C.
+  int splits;
+  int k_slice;
+  float* partial;
+};
+
+// One fp16 tcgen05 GEMM launch.
+struct HgemmArgs {
+  int transA, transB;
+  int M, N, K;
+  const __half* A;  // 16-byte aligned base, lda * 2 a multiple of 16
+  int64_t lda;
+  const __half* B;
+  int64_t ldb;
+  __half* C;
+  int64_t ldc;
+  float alpha, beta;
+  int splits;
+  int k_slice;      // multiple of the kernel's K block
+  float* partial;   // [splits][M][N] fp32 when splits > 1
+  int num_sms;
+  int fault_injection;  // test hook: 1 = producer skips its first stage
+};
+
+struct LaunchCtx {
+  cudaStream_t stream;
+  unsigned int* status;  // device status word
+  uint64_t timeout_ns;
+  int launches;          // incremented per kernel launched
+};
+
+// Launchers (return cudaSuccess or the launch error).
+cudaError_t launch_sgemm(const SgemmArgs& a, LaunchCtx& ctx);
+cudaError_t launch_hgemm(const HgemmArgs& a, LaunchCtx& ctx);
+// C[M,N] = alpha * sum_z P[z] + beta * C; dtype 0 = fp32 C, 1 = fp16 C.
+cudaError_t launch_splitk_reduce(int dtype, int M, int N, int splits, const float* P, void* C,
+                                 int64_t ldc, float alpha, float beta, LaunchCtx& ctx);
+// C = beta * C (K == 0); beta == 0 writes zeros.
+cudaError_t launch_scale(int dtype, int M, int N, void* C, int64_t ldc, float beta,
+                         LaunchCtx& ctx);
+// dst[r][c] = src[r][c] for c < cols, 0 for cols <= c < ld_dst (fp16 rows).
+cudaError_t launch_repack_f16(int rows, int cols, const __half* src, int64_t ld_src,
+                              __half* dst, int64_t ld_dst, LaunchCtx& ctx);
+
+// Tile sizes the dispatcher needs.
+constexpr int SG_BM = 128, SG_BN = 128, SG_BK = 16;
+constexpr int HG_BM = 128, HG_BK = 64;
+int hgemm_pick_bn(int N, int transB);
+
+}  // namespace gb300

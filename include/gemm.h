@@ -1,0 +1,159 @@
+/*
+ * gemm.h -- C ABI of the GB300 (sm_103a) dense GEMM library, libgemm_gb300.so.
+ *
+ * The library computes
+ *
+ *     C = alpha * op(A) * op(B) + beta * C
+ *
+ * over row-major matrices: full SGEMM as defined in the Introduction sidenote of
+ * "Optimizing GEMM on Apple's M5 from scratch, Part 1: Basics" (the pages fix
+ * alpha = 1, beta = 0 for their benchmark; the library takes both), for
+ *   - fp32 operands and result (the SGEMM of that page and of "Part 2"), and
+ *   - fp16 operands, fp32 accumulation and an fp16 result, the regime of
+ *     "Metal GEMM Kernels for LoRA Training on Apple Silicon", section 1 (table
+ *     of operand/accumulator types) and section 2 (output converted from the
+ *     fp32 accumulator on the way out),
+ * in the transpose variants of that page's section 2 variant table:
+ *     nn  A[M,K]   @ B[K,N]
+ *     tn  A[K,M]^T @ B[K,N]
+ *     nt  A[M,K]   @ B[N,K]^T
+ * (tt, both transposed, is not on the pages; it falls out of the same operand
+ * descriptors and is accepted.)
+ *
+ * Conventions (all entry points):
+ *   - Row-major storage; every leading dimension (lda, ldb, ldc) is in
+ *     ELEMENTS and is the distance between consecutive stored rows.
+ *   - op(A) is M x K: A is stored M x K (lda >= K) when transA == 0, and
+ *     K x M (lda >= M) when transA == 1.  op(B) is K x N: B is stored K x N
+ *     (ldb >= N) when transB == 0, N x K (ldb >= K) when transB == 1.
+ *     C is M x N, ldc >= N.  A sub-matrix is passed as a pointer at its first
+ *     element plus the parent's leading dimension (the row-offset entry of the
+ *     LoRA page, section 7).
+ *   - alpha and beta are fp32 for both dtypes.  beta == 0 makes C write-only:
+ *     it is not read, so NaN or garbage in C does not reach the result.
+ *   - M == 0 or N == 0 returns GEMM_OK without touching the GPU.  K == 0 sets
+ *     C = beta * C (zero when beta == 0).
+ *   - Pointers passed to gemm() are DEVICE pointers (cudaMalloc, the stream-
+ *     ordered allocator or a torch CUDA tensor's storage), aligned to the
+ *     element size.  The caller owns every buffer; the library never frees
+ *     caller memory.  C must not overlap A or B (GEMM_ERR_ALIAS).
+ *   - Calls are asynchronous on `stream` (0 = the legacy default stream) and
+ *     may be made from several host threads.  Scratch space the library needs
+ *     (split-K partial sums; zero-padded copies of operands whose rows are not
+ *     16-byte aligned) comes from the stream-ordered allocator on `stream` and
+ *     is released on the same stream.
+ *   - Argument errors are returned synchronously, before anything is
+ *     launched.  Launch failures return GEMM_ERR_CUDA.  A kernel whose
+ *     internal wait exceeds its time limit records the fact in a per-device
+ *     status word and exits early; gemm_check_device_status() reports it.
+ */
+#ifndef GEMM_GB300_H
+#define GEMM_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* cudaStream_t without pulling in the CUDA headers. */
+typedef struct CUstream_st* gemm_stream_t;
+
+typedef enum {
+    GEMM_F32 = 0,        /* A, B, C fp32; fp32 FMA accumulation */
+    GEMM_F16_F32ACC = 1  /* A, B, C fp16 (IEEE binary16); fp32 accumulation;
+                            result rounded to fp16 round-to-nearest-even */
+} gemm_dtype_t;
+
+typedef enum {
+    GEMM_OK = 0,
+    GEMM_ERR_INVALID_ARG = 1, /* bad dimension, leading dimension, pointer, flag or dtype */
+    GEMM_ERR_UNSUPPORTED = 2, /* valid but not handled (e.g. a dimension >= 2^31) */
+    GEMM_ERR_ALIAS = 3,       /* C overlaps A or B */
+    GEMM_ERR_CUDA = 4,        /* a CUDA runtime/driver call or a launch failed */
+    GEMM_ERR_NO_MEMORY = 5,   /* scratch allocation failed */
+    GEMM_ERR_TIMEOUT = 6      /* a kernel's bounded internal wait expired */
+} gemm_status_t;
+
+/*
+ * gemm -- C = alpha * op(A) * op(B) + beta * C on the GPU.
+ *
+ * transA, transB: 0 or 1 (see above).  M, N, K >= 0 and < 2^31.
+ * dtype: a gemm_dtype_t.  A, B, C: device pointers, element-aligned.
+ * lda, ldb, ldc: leading dimensions in elements (see above).
+ * stream: the CUDA stream to run on.
+ * Returns a gemm_status_t.  Nothing is launched unless it returns GEMM_OK.
+ */
+int gemm(int transA, int transB, int64_t M, int64_t N, int64_t K, int dtype, float alpha,
+         float beta, const void* A, int64_t lda, const void* B, int64_t ldb, void* C,
+         int64_t ldc, gemm_stream_t stream);
+
+/*
+ * gemm_host -- the same product on HOST buffers: copies A, B (and C when
+ * beta != 0) to device memory taken from the stream-ordered allocator, runs
+ * gemm() on `stream`, copies C back and synchronises `stream` before it
+ * returns.  A, B, C are host pointers with the same layout rules as gemm();
+ * page-locked (pinned) memory gives asynchronous DMA copies, pageable memory
+ * works but is staged by the driver.  The device copies are packed (ld equal
+ * to the row length) and freed before return.
+ */
+int gemm_host(int transA, int transB, int64_t M, int64_t N, int64_t K, int dtype, float alpha,
+              float beta, const void* A, int64_t lda, const void* B, int64_t ldb, void* C,
+              int64_t ldc, gemm_stream_t stream);
+
+/*
+ * gemm_check_device_status -- synchronises `stream`, then reads and clears
+ * the current device's status word.  Returns GEMM_ERR_TIMEOUT if a kernel
+ * gave up on a wait since the last check, GEMM_ERR_CUDA if the stream
+ * reported an error, GEMM_OK otherwise.
+ */
+int gemm_check_device_status(gemm_stream_t stream);
+
+/* Human-readable name of a gemm_status_t (a static string). */
+const char* gemm_status_string(int status);
+
+/* Library version, (major << 16) | minor. */
+int gemm_version(void);
+
+/*
+ * Diagnostics, per calling host thread: the kernel path the last successful
+ * gemm() call on this thread launched (a gemm_path_t), and the number of
+ * kernels it launched.  gemm_total_launches() counts kernels launched by the
+ * library in this process since it was loaded (all threads).
+ */
+typedef enum {
+    GEMM_PATH_NONE = 0,        /* nothing launched (empty problem or error) */
+    GEMM_PATH_SCALE = 1,       /* K == 0: C = beta * C */
+    GEMM_PATH_FFMA = 2,        /* fp32 FFMA tiled kernel */
+    GEMM_PATH_FFMA_SPLITK = 3, /* fp32 FFMA kernel over K slices + reduction */
+    GEMM_PATH_TC = 4,          /* fp16 tcgen05 kernel, fused epilogue */
+    GEMM_PATH_TC_SPLITK = 5    /* fp16 tcgen05 kernel over K slices + reduction */
+} gemm_path_t;
+
+int gemm_last_path(void);
+int gemm_last_launches(void);
+int64_t gemm_total_launches(void);
+
+/*
+ * Test hook: the time limit, in nanoseconds, of every bounded wait inside the
+ * kernels launched afterwards by this process (default 2e9, i.e. 2 s; values
+ * <= 0 restore the default).  A wait that runs out sets the device status
+ * word, releases what its block holds and returns.
+ */
+void gemm_set_wait_timeout_ns(int64_t ns);
+
+/*
+ * Test hook for failure detection: mode 1 makes the fp16 kernel's operand
+ * producer skip its first load (no copy, no arrival), so the consumer's
+ * bounded wait runs out and the kernel reports GEMM_ERR_TIMEOUT through
+ * gemm_check_device_status() instead of hanging.  Mode 0 (the default) turns
+ * it off.  Process-wide; not for production use.
+ */
+void gemm_set_fault_injection(int mode);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GEMM_GB300_H */

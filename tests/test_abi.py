@@ -1,0 +1,77 @@
+"""The C-ABI library: it builds, loads, exports every declared symbol, and
+rejects bad arguments before touching the GPU (CPU only)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "gemm.h")
+
+
+def declared_functions():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?[a-z_0-9]+\s*\*?\s*(gemm[a-z_0-9]*)\s*\(",
+                                 src, flags=re.M)))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for n in ["gemm", "gemm_host", "gemm_check_device_status", "gemm_status_string"]:
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(lib_path):
+    lib = ctypes.CDLL(lib_path)
+    missing = [n for n in declared_functions() if not hasattr(lib, n)]
+    assert not missing, missing
+
+
+@pytest.fixture(scope="module")
+def b(lib_path):
+    from dense_gemm_tiled_gb300 import binding
+    return binding
+
+
+# fake, well-aligned, non-overlapping "device" addresses: argument checks never
+# dereference them and no launch happens when a check fails
+PA, PB, PC = 0x10000000, 0x20000000, 0x30000000
+
+
+def test_status_strings(b):
+    assert b.status_string(0) == "GEMM_OK"
+    assert b.status_string(3) == "GEMM_ERR_ALIAS"
+    assert b.status_string(99) == "GEMM_ERR_UNKNOWN"
+    assert b.version() >> 16 == 1
+
+
+@pytest.mark.parametrize("args,code", [
+    # (transA, transB, M, N, K, dtype, A, lda, B, ldb, C, ldc)
+    ((2, 0, 4, 4, 4, 0, PA, 4, PB, 4, PC, 4), 1),       # bad trans flag
+    ((0, 0, 4, 4, 4, 7, PA, 4, PB, 4, PC, 4), 1),       # bad dtype
+    ((0, 0, -1, 4, 4, 0, PA, 4, PB, 4, PC, 4), 1),      # negative M
+    ((0, 0, 4, 4, 4, 0, PA, 3, PB, 4, PC, 4), 1),       # lda < K (nn)
+    ((1, 0, 8, 4, 4, 0, PA, 4, PB, 4, PC, 4), 1),       # lda < M (tn)
+    ((0, 1, 4, 8, 6, 0, PA, 6, PB, 5, PC, 8), 1),       # ldb < K (nt)
+    ((0, 0, 4, 8, 4, 0, PA, 4, PB, 8, PC, 7), 1),       # ldc < N
+    ((0, 0, 4, 4, 4, 0, 0, 4, PB, 4, PC, 4), 1),        # null A
+    ((0, 0, 4, 4, 4, 0, PA, 4, PB, 4, 0, 4), 1),        # null C
+    ((0, 0, 4, 4, 4, 0, PA + 2, 4, PB, 4, PC, 4), 1),   # misaligned fp32 A
+    ((0, 0, 4, 4, 4, 1, PA + 1, 4, PB, 4, PC, 4), 1),   # misaligned fp16 A
+    ((0, 0, 4, 4, 4, 0, PA, 4, PB, 4, PA + 16, 4), 3),  # C overlaps A
+    ((0, 0, 4, 4, 4, 0, PA, 4, PB, 4, PB - 8, 4), 3),   # C overlaps B from below
+    ((0, 0, 1 << 31, 4, 4, 0, PA, 4, PB, 4, PC, 4), 2),  # too large
+])
+def test_invalid_arguments(b, args, code):
+    tA, tB, M, N, K, dt, A, lda, B, ldb, C, ldc = args
+    assert b.gemm_raw(tA, tB, M, N, K, dt, 1.0, 0.0, A, lda, B, ldb, C, ldc) == code
+    assert b.last_path() == "none"
+
+
+def test_empty_output_returns_ok_without_gpu(b):
+    assert b.gemm_raw(0, 0, 0, 5, 3, 0, 1.0, 0.0, PA, 3, PB, 5, PC, 5) == 0
+    assert b.gemm_raw(0, 0, 5, 0, 3, 1, 1.0, 0.0, PA, 3, PB, 1, PC, 1) == 0
+    assert b.gemm_raw(0, 0, 0, 0, 0, 0, 1.0, 0.0, 0, 1, 0, 1, 0, 1) == 0
+    assert b.last_path() == "none"

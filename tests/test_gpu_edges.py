@@ -1,0 +1,137 @@
+"""Edge behaviour through the C ABI: beta == 0 never reads C, guard bands around
+C stay untouched, K == 0, sub-matrix views, host buffers, and the bounded wait
+reporting a timeout instead of hanging."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from oracle import compare
+from dense_gemm_tiled_gb300 import inputs
+from helpers import check_problem, to_np
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(autouse=True)
+def _lib(lib_path, gpu):
+    yield
+
+
+def _b():
+    from dense_gemm_tiled_gb300 import binding
+    return binding
+
+
+@pytest.mark.parametrize("dtype", ["f32", "f16"])
+def test_beta_zero_ignores_nan_in_c(dtype):
+    p = inputs.sweep_problem(200, 300, 100, "nn", dtype, 0.0, seed=300)
+    check_problem(p, c_init=float("nan"))
+
+
+@pytest.mark.parametrize("dtype", ["f32", "f16"])
+@pytest.mark.parametrize("variant", ["nn", "tn", "nt"])
+def test_guard_bands_untouched(dtype, variant):
+    """C lives inside a larger buffer (ldc > N, rows above and below); every
+    element outside the M x N window must keep its sentinel."""
+    b = _b()
+    M, N, K = 131, 257, 70
+    p = inputs.sweep_problem(M, N, K, variant, dtype, 0.5, seed=310)
+    dt = inputs.DTYPES[dtype]
+    pad_r, pad_c = 8, 24
+    sentinel = 1234.0  # exactly representable in fp32 and fp16
+    big = torch.full((M + 2 * pad_r, N + pad_c), sentinel, dtype=dt, device="cuda")
+    C = big[pad_r:pad_r + M, :N]
+    C.copy_(p.C_in.cuda())
+    b.gemm(p.A.cuda(), p.B.cuda(), C, p.transA, p.transB, p.alpha, p.beta)
+    torch.cuda.synchronize()
+    host = big.cpu().float().numpy()
+    mask = np.ones(host.shape, dtype=bool)
+    mask[pad_r:pad_r + M, :N] = False
+    assert np.all(host[mask] == sentinel)
+    ref, mag = oracle.gemm_ref(to_np(p.A), to_np(p.B), to_np(p.C_in), p.transA, p.transB,
+                               p.alpha, p.beta)
+    res = compare.check(to_np(C.cpu()), ref, mag, dtype)
+    assert res["ok"], res
+
+
+@pytest.mark.parametrize("dtype", ["f32", "f16"])
+def test_k_zero_scales_c(dtype):
+    b = _b()
+    dt = inputs.DTYPES[dtype]
+    A = torch.empty((64, 0), dtype=dt, device="cuda")
+    B = torch.empty((0, 48), dtype=dt, device="cuda")
+    C0 = inputs.uniform((64, 48), 320, dtype)
+    C = C0.cuda().clone()
+    b.gemm(A, B, C, beta=0.5)
+    torch.cuda.synchronize()
+    assert b.last_path() == "scale"
+    assert torch.equal(C.cpu(), (C0.float() * 0.5).to(dt))
+    b.gemm(A, B, C, beta=0.0)
+    torch.cuda.synchronize()
+    assert torch.count_nonzero(C).item() == 0
+
+
+@pytest.mark.parametrize("dtype", ["f32", "f16"])
+@pytest.mark.parametrize("variant", ["nn", "tn", "nt"])
+def test_submatrix_views(dtype, variant):
+    """Operands entered at an offset inside larger buffers (lda, ldb, ldc larger
+    than the rows), as the LoRA page's row-split enters A and C by offset."""
+    b = _b()
+    tA, tB = inputs.VARIANTS[variant]
+    M, N, K = 150, 210, 96
+    dt = inputs.DTYPES[dtype]
+    Abig = inputs.uniform((400, 400), 330, dtype)
+    Bbig = inputs.uniform((400, 400), 331, dtype)
+    ar, ac = (K, M) if tA else (M, K)
+    br, bc = (N, K) if tB else (K, N)
+    A = Abig[16:16 + ar, 8:8 + ac]
+    B = Bbig[24:24 + br, 32:32 + bc]
+    Cbig = torch.zeros((M + 10, N + 40), dtype=dt, device="cuda")
+    C = Cbig[5:5 + M, 8:8 + N]
+    b.gemm(Abig.cuda()[16:16 + ar, 8:8 + ac], Bbig.cuda()[24:24 + br, 32:32 + bc], C, tA, tB)
+    torch.cuda.synchronize()
+    ref, mag = oracle.gemm_ref(A.numpy(), B.numpy(), None, tA, tB)
+    res = compare.check(to_np(C.cpu()), ref, mag, dtype)
+    assert res["ok"], res
+
+
+@pytest.mark.parametrize("dtype", ["f32", "f16"])
+def test_gemm_host_buffers(dtype):
+    b = _b()
+    p = inputs.sweep_problem(300, 200, 150, "nt", dtype, 0.5, seed=340)
+    A = p.A.pin_memory()
+    B = p.B.pin_memory()
+    C = p.C_in.clone().pin_memory()
+    b.gemm_host(A, B, C, p.transA, p.transB, p.alpha, p.beta)
+    ref, mag = oracle.gemm_ref(to_np(p.A), to_np(p.B), to_np(p.C_in), p.transA, p.transB,
+                               p.alpha, p.beta)
+    res = compare.check(to_np(C), ref, mag, dtype)
+    assert res["ok"], res
+    # pageable memory too
+    C2 = p.C_in.clone()
+    b.gemm_host(p.A, p.B, C2, p.transA, p.transB, p.alpha, p.beta)
+    assert torch.equal(C2, C)
+
+
+def test_bounded_wait_reports_timeout_and_context_survives():
+    """A load that never arrives (test hook): the kernel's wait runs out after
+    its limit, the status word says so, and the next call works."""
+    b = _b()
+    p = inputs.make_problem(256, 256, 512, False, False, "f16", "integer", seed=350)
+    A, B = p.A.cuda(), p.B.cuda()
+    C = torch.zeros((256, 256), dtype=torch.float16, device="cuda")
+    assert b.check_device_status() == b.OK
+    b.set_wait_timeout_ns(100_000_000)  # 0.1 s
+    b.set_fault_injection(1)
+    try:
+        b.gemm(A, B, C)
+        assert b.check_device_status() == b.ERR_TIMEOUT
+    finally:
+        b.set_fault_injection(0)
+        b.set_wait_timeout_ns(0)
+    assert b.check_device_status() == b.OK  # cleared by the read
+    b.gemm(A, B, C)
+    assert b.check_device_status() == b.OK
+    ref, mag = oracle.gemm_ref(to_np(p.A), to_np(p.B))
+    assert compare.check(to_np(C.cpu()), ref, mag, "f16", exact=True)["ok"]

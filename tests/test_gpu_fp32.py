@@ -1,0 +1,62 @@
+"""fp32 SGEMM (CUDA-core FFMA kernel) against the oracle."""
+import pytest
+
+from dense_gemm_tiled_gb300 import inputs
+from helpers import check_problem
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(autouse=True)
+def _lib(lib_path, gpu):
+    yield
+
+
+def test_sgemm_512_uniform():
+    res = check_problem(inputs.sgemm_512())
+    assert res["path"] in ("ffma", "ffma_splitk")
+
+
+def test_sgemm_512_integer_bit_exact():
+    check_problem(inputs.sgemm_512(integer=True), exact=True)
+
+
+@pytest.mark.parametrize("variant", ["nn", "tn", "nt", "tt"])
+@pytest.mark.parametrize("beta", [0.0, 0.5])
+def test_variants_ragged(variant, beta):
+    # several tiles in each direction plus ragged tails in M, N and K
+    p = inputs.sweep_problem(300, 270, 131, variant, "f32", beta, seed=100)
+    check_problem(p)
+
+
+@pytest.mark.parametrize("variant", ["nn", "tn", "nt", "tt"])
+def test_variants_integer_exact(variant):
+    tA, tB = inputs.VARIANTS[variant]
+    p = inputs.make_problem(257, 130, 200, tA, tB, "f32", "integer", seed=101, alpha=2.0,
+                            beta=0.5, c_fill="integer")
+    check_problem(p, exact=True)
+
+
+@pytest.mark.parametrize("shape", [(1, 1, 1), (1, 7, 3), (17, 33, 5), (127, 129, 130),
+                                   (129, 127, 17), (1000, 3000, 777)])
+def test_odd_shapes(shape):
+    M, N, K = shape
+    for i, v in enumerate(["nn", "tn", "nt"]):
+        check_problem(inputs.sweep_problem(M, N, K, v, "f32", 0.0, seed=110 + i))
+
+
+def test_sgemm_4096_sampled():
+    check_problem(inputs.sgemm_4096(), full=False)
+
+
+@pytest.mark.parametrize("shape", [(8192, 32, 8192), (512, 32, 5632), (32, 2048, 512)])
+def test_skinny_split_k(shape):
+    M, N, K = shape
+    p = inputs.sweep_problem(M, N, K, "nn", "f32", 0.0, seed=120)
+    res = check_problem(p)
+    assert res["path"] == "ffma_splitk"
+
+
+def test_skinny_split_k_beta():
+    p = inputs.sweep_problem(512, 32, 5632, "tn", "f32", 0.5, seed=121)
+    check_problem(p)
