@@ -201,6 +201,37 @@ def run_reference(args, world, rank):
 
 
 # ------------------------------------------------------------------ GPU legs
+def run_case(args, local):
+    """One GEMM, `warmup` untimed launches then `steps` timed ones (CUDA events
+    per launch on the launching stream)."""
+    import torch
+    from dense_gemm_tiled_gb300 import binding, inputs
+    dt, var, size = args.case.split("_")
+    n = int(size)
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    tA, tB = inputs.VARIANTS[var]
+    p = inputs.make_problem(n, n, n, tA, tB, dtype=dt, seed=80)
+    A, B = p.A.to(dev), p.B.to(dev)
+    C = torch.empty((n, n), dtype=A.dtype, device=dev)
+    s = torch.cuda.Stream(dev)
+    for _ in range(args.warmup):
+        binding.gemm(A, B, C, tA, tB, stream=s)
+    ts = []
+    for _ in range(args.steps):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(s)
+        binding.gemm(A, B, C, tA, tB, stream=s)
+        e1.record(s)
+        e1.synchronize()
+        ts.append(e0.elapsed_time(e1))
+    assert binding.check_device_status(s) == binding.OK
+    med = statistics.median(ts)
+    print(json.dumps({"case": args.case, "path": binding.last_path(), "ms_median": med,
+                      "tflops": 2.0 * n ** 3 / (med * 1e-3) / 1e12, "steps": args.steps}),
+          flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -209,12 +240,18 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-fp16", action="store_true")
+    ap.add_argument("--case", default=None,
+                    help="run only one GEMM (e.g. f32_nn_4096, f16_tn_4096, f16_nn_8192): "
+                         "warm-up + steps, one short JSON line; used for profiling")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
     world, rank, local = dist_setup()
     if args.impl == "reference":
         run_reference(args, world, rank)
+        return
+    if args.case:
+        run_case(args, local)
         return
 
     import torch
