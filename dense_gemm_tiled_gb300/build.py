@@ -42,14 +42,20 @@ def up_to_date() -> bool:
     return all(os.path.getmtime(d) <= t for d in _deps())
 
 
-def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False) -> str:
-    if not force and up_to_date():
+def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False,
+          out: str = None, defines=()) -> str:
+    """Compiles csrc/*.cu and links them into `out` (default: the in-tree
+    library).  `defines` are extra -D settings of the kernels' compile-time
+    knobs."""
+    lib = out or LIB
+    if not force and out is None and not defines and up_to_date():
         return LIB
-    os.makedirs(BUILD, exist_ok=True)
-    extra = ["-Xptxas", "-v"] if ptxas_info else []
+    build_dir = BUILD if out is None and not defines else lib + ".objs"
+    os.makedirs(build_dir, exist_ok=True)
+    extra = (["-Xptxas", "-v"] if ptxas_info else []) + ["-D" + d for d in defines]
 
     def compile_one(src):
-        obj = os.path.join(BUILD, os.path.basename(src) + ".o")
+        obj = os.path.join(build_dir, os.path.basename(src) + ".o")
         cmd = [nvcc()] + ARCH + NVCC_FLAGS + extra + ["-c", src, "-o", obj]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
@@ -63,13 +69,13 @@ def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False) 
             if log:
                 sys.stderr.write(log)
     objs = [o for o, _ in results]
-    tmp = LIB + f".tmp{os.getpid()}"
+    tmp = lib + f".tmp{os.getpid()}"
     cmd = [nvcc()] + ARCH + ["-shared", "-cudart", "static", "-o", tmp] + objs
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
-    os.replace(tmp, LIB)
-    return LIB
+    os.replace(tmp, lib)
+    return lib
 
 
 if __name__ == "__main__":

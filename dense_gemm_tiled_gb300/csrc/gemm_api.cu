@@ -13,6 +13,7 @@
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
+#include <stdlib.h>
 #include <string.h>
 
 #include <atomic>
@@ -102,6 +103,16 @@ int check_args(int transA, int transB, int64_t M, int64_t N, int64_t K, int dtyp
   return GEMM_OK;
 }
 
+// Debug/bench override of the fp16 tile width (env GEMM_GB300_HG_BN); 0 = the
+// dispatcher's own choice.
+int forced_bn() {
+  static const int v = [] {
+    const char* e = getenv("GEMM_GB300_HG_BN");
+    return e ? atoi(e) : 0;
+  }();
+  return v;
+}
+
 int cuda_fail(cudaError_t e) { return e == cudaErrorMemoryAllocation ? GEMM_ERR_NO_MEMORY : GEMM_ERR_CUDA; }
 
 // Split-K plan: how many K slices, each a multiple of `kstep` long.
@@ -171,7 +182,11 @@ int run_gemm(int transA, int transB, int64_t M64, int64_t N64, int64_t K64, int 
     if (e == cudaSuccess && splits > 1)
       e = launch_splitk_reduce(0, M, N, splits, a.partial, C, ldc, alpha, beta, ctx);
   } else {
-    const int bn = hgemm_pick_bn(N, transB);
+    int bn = hgemm_pick_bn(M, N, transB, sms);
+    const int forced = forced_bn();
+    if (forced == 32 ? (N <= 32 && transB) : (forced == 64 || forced == 128 || forced == 192 ||
+                                              forced == 256))
+      bn = forced;
     const int64_t tiles = (int64_t)((M + HG_BM - 1) / HG_BM) * ((N + bn - 1) / bn);
     int splits, k_slice;
     plan_splits(tiles, K, HG_BK, sms, 4, 32, &splits, &k_slice);
@@ -204,7 +219,7 @@ int run_gemm(int transA, int transB, int64_t M64, int64_t N64, int64_t K64, int 
     }
     if (e == cudaSuccess) {
       HgemmArgs a{transA, transB, M, N, K, Ad, ldad, Bd, ldbd, (__half*)C, ldc, alpha, beta,
-                  splits, k_slice, splits > 1 ? (float*)wp : nullptr, sms,
+                  splits, k_slice, splits > 1 ? (float*)wp : nullptr, sms, bn,
                   g_fault_injection.load()};
       path = splits > 1 ? GEMM_PATH_TC_SPLITK : GEMM_PATH_TC;
       e = launch_hgemm(a, ctx);

@@ -62,7 +62,8 @@ struct Cfg {
   static constexpr int STAGE_BYTES = A_TILE_BYTES + B_TILE_BYTES;
   static constexpr int STAGES_RAW = SMEM_BUDGET / STAGE_BYTES;
   static constexpr int STAGES = STAGES_RAW > 8 ? 8 : STAGES_RAW;
-  static constexpr int TMEM_COLS = (2 * BN < 32) ? 32 : 2 * BN;  // power of two for BN in {32..256}
+  // two accumulator buffers of BN fp32 columns, rounded up to a power of two
+  static constexpr int TMEM_COLS = 2 * BN <= 64 ? 64 : 2 * BN <= 128 ? 128 : 2 * BN <= 256 ? 256 : 512;
   static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 /*align*/ + 256 /*barriers*/;
 };
 
@@ -432,13 +433,25 @@ cudaError_t launch_bn(const HgemmArgs& a, const HParams& p, LaunchCtx& ctx) {
 
 }  // namespace
 
-int hgemm_pick_bn(int N, int transB) {
+int hgemm_pick_bn(int M, int N, int transB, int num_sms) {
   // An MN-major B (transB == 0) is staged in 64-column swizzle atoms, so its
   // narrowest tile is 64 columns; a K-major B can go down to 32.
   if (N <= 32 && transB) return 32;
   if (N <= 64) return 64;
   if (N <= 128) return 128;
-  return 256;
+  // Wider N: the persistent grid runs ceil(tiles / SMs) rounds of tiles whose
+  // cost grows with BN, so pick the width with the fewest column-rounds
+  // (ties go to the wider tile, which re-reads A less).
+  const int64_t tm = (M + BM - 1) / BM;
+  int best = 256;
+  int64_t best_cost = -1;
+  for (int bn : {256, 192, 128}) {
+    const int64_t tiles = tm * ((N + bn - 1) / bn);
+    const int64_t rounds = (tiles + num_sms - 1) / num_sms;
+    const int64_t cost = rounds * bn;
+    if (best_cost < 0 || cost < best_cost) { best = bn; best_cost = cost; }
+  }
+  return best;
 }
 
 cudaError_t launch_hgemm(const HgemmArgs& a, LaunchCtx& ctx) {
@@ -449,7 +462,7 @@ cudaError_t launch_hgemm(const HgemmArgs& a, LaunchCtx& ctx) {
   p.M = a.M; p.N = a.N; p.K = a.K;
   p.splits = a.splits > 1 ? a.splits : 1;
   p.k_slice = a.splits > 1 ? a.k_slice : ((a.K + BK - 1) / BK) * BK;
-  const int bn = hgemm_pick_bn(a.N, a.transB);
+  const int bn = a.bn;
   p.tiles_m = (a.M + BM - 1) / BM;
   p.tiles_n = (a.N + bn - 1) / bn;
   p.alpha = a.alpha; p.beta = a.beta;
@@ -461,7 +474,9 @@ cudaError_t launch_hgemm(const HgemmArgs& a, LaunchCtx& ctx) {
     case 32: return launch_bn<32>(a, p, ctx);
     case 64: return launch_bn<64>(a, p, ctx);
     case 128: return launch_bn<128>(a, p, ctx);
-    default: return launch_bn<256>(a, p, ctx);
+    case 192: return launch_bn<192>(a, p, ctx);
+    case 256: return launch_bn<256>(a, p, ctx);
+    default: return cudaErrorInvalidValue;
   }
 }
 

@@ -40,6 +40,7 @@ struct HgemmArgs {
   int k_slice;      // multiple of the kernel's K block
   float* partial;   // [splits][M][N] fp32 when splits > 1
   int num_sms;
+  int bn;               // tile width: 32, 64, 128, 192 or 256
   int fault_injection;  // test hook: 1 = producer skips its first stage
 };
 
@@ -64,8 +65,8 @@ cudaError_t launch_repack_f16(int rows, int cols, const __half* src, int64_t ld_
                               __half* dst, int64_t ld_dst, LaunchCtx& ctx);
 
 // Tile sizes the dispatcher needs.
-constexpr int SG_BM = 128, SG_BN = 128, SG_BK = 16;
+constexpr int SG_BM = 128, SG_BN = 128, SG_BK = 32;
 constexpr int HG_BM = 128, HG_BK = 64;
-int hgemm_pick_bn(int N, int transB);
+int hgemm_pick_bn(int M, int N, int transB, int num_sms);
 
 }  // namespace gb300
