@@ -346,3 +346,112 @@ void gemm_set_wait_timeout_ns(int64_t ns) {
 void gemm_set_fault_injection(int mode) { g_fault_injection.store(mode); }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------
+// gemm_splitk_noalloc: the same product for callers that must not allocate
+// device memory, e.g. code running under an allocator that already owns the
+// whole device (a framework's caching allocator), or a host process whose
+// rules forbid runtime allocation once it is serving.  The split-K partial
+// sums, which gemm() takes from the stream-ordered allocator, live here in a
+// fixed array compiled into the library instead.
+//
+// The array is a file-scope __device__ variable: every GPU that loads this
+// library holds it (GEMM_NOALLOC_SCRATCH_BYTES) until the process exits.  Host
+// code cannot use its name as a device address, so its address is looked up
+// once per device with cudaGetSymbolAddress, with that device current, the
+// first time the entry point runs on it; that first call therefore makes a
+// runtime query and should come before any stream capture.  All calls share
+// the one array and it keeps whatever the last call left: every element a
+// call reads is written by the same call first (each K slice writes all of its
+// M x N partials before the reduction reads them), so nothing needs clearing,
+// but two calls that overlap on the GPU (different streams, no ordering
+// between them) race on it.
+// ---------------------------------------------------------------------------
+#define GEMM_NOALLOC_SCRATCH_BYTES (8u << 20)
+
+static __device__ __align__(256) float g_noalloc_scratch[GEMM_NOALLOC_SCRATCH_BYTES / sizeof(float)];
+
+namespace {
+float* g_noalloc_ptr[MAX_DEVICES];
+
+int noalloc_scratch(int dev, float** out) {
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (!g_noalloc_ptr[dev]) {
+    void* p = nullptr;
+    const cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    if (e != cudaSuccess || p == nullptr) return GEMM_ERR_CUDA;
+    g_noalloc_ptr[dev] = static_cast<float*>(p);
+  }
+  *out = g_noalloc_ptr[dev];
+  return GEMM_OK;
+}
+}  // namespace
+
+extern "C" int gemm_splitk_noalloc(int transA, int transB, int64_t M, int64_t N, int64_t K,
+                                   int dtype, float alpha, float beta, const void* A,
+                                   int64_t lda, const void* B, int64_t ldb, void* C,
+                                   int64_t ldc, gemm_stream_t stream_) {
+  int64_t ar, ac, br, bc;
+  tl_last_path = GEMM_PATH_NONE;
+  tl_last_launches = 0;
+  int rc = check_args(transA, transB, M, N, K, dtype, A, lda, B, ldb, C, ldc, &ar, &ac, &br, &bc);
+  if (rc != GEMM_OK) return rc;
+  if (M == 0 || N == 0) return GEMM_OK;
+  cudaStream_t stream = (cudaStream_t)stream_;
+  int dev, sms;
+  unsigned int* status;
+  rc = device_state(&dev, &status, &sms);
+  if (rc != GEMM_OK) return rc;
+  float* scratch = nullptr;
+  rc = noalloc_scratch(dev, &scratch);
+  if (rc != GEMM_OK) return rc;
+  LaunchCtx ctx{stream, status, (uint64_t)g_timeout_ns.load(), 0};
+  const int Mi = (int)M, Ni = (int)N, Ki = (int)K;
+  int path = GEMM_PATH_NONE;
+  cudaError_t e = cudaSuccess;
+  if (Ki == 0) {
+    path = GEMM_PATH_SCALE;
+    e = launch_scale(dtype, Mi, Ni, C, ldc, beta, ctx);
+  } else if (dtype == GEMM_F32) {
+    const int64_t tiles = (int64_t)((Mi + SG_BM - 1) / SG_BM) * ((Ni + SG_BN - 1) / SG_BN);
+    int splits, k_slice;
+    plan_splits(tiles, Ki, SG_BK, 2 * sms, 8, 16, &splits, &k_slice);
+    if (splits > 1 && (uint64_t)splits * (uint64_t)M * (uint64_t)N * sizeof(float) >
+                          GEMM_NOALLOC_SCRATCH_BYTES)
+      return GEMM_ERR_UNSUPPORTED;  // partial sums would not fit the fixed array
+    SgemmArgs a{transA, transB, Mi, Ni, Ki, (const float*)A, lda, (const float*)B, ldb,
+                (float*)C, ldc, alpha, beta, splits, k_slice, splits > 1 ? scratch : nullptr};
+    path = splits > 1 ? GEMM_PATH_FFMA_SPLITK : GEMM_PATH_FFMA;
+    e = launch_sgemm(a, ctx);
+    if (e == cudaSuccess && splits > 1)
+      e = launch_splitk_reduce(0, Mi, Ni, splits, scratch, C, ldc, alpha, beta, ctx);
+  } else {
+    // fp16 operands must already meet the tensor-memory-access unit's rules
+    // (16-byte aligned base and row pitch): padding them would need scratch.
+    if (((uintptr_t)A % 16) != 0 || (lda % 8) != 0 || ((uintptr_t)B % 16) != 0 || (ldb % 8) != 0)
+      return GEMM_ERR_UNSUPPORTED;
+    int bn = hgemm_pick_bn(Mi, Ni, transB, sms);
+    const int forced = forced_bn();
+    if (forced == 32 ? (Ni <= 32 && transB) : (forced == 64 || forced == 128 || forced == 192 ||
+                                               forced == 256))
+      bn = forced;
+    const int64_t tiles = (int64_t)((Mi + HG_BM - 1) / HG_BM) * ((Ni + bn - 1) / bn);
+    int splits, k_slice;
+    plan_splits(tiles, Ki, HG_BK, sms, 4, 32, &splits, &k_slice);
+    if (splits > 1 && (uint64_t)splits * (uint64_t)M * (uint64_t)N * sizeof(float) >
+                          GEMM_NOALLOC_SCRATCH_BYTES)
+      return GEMM_ERR_UNSUPPORTED;  // partial sums would not fit the fixed array
+    HgemmArgs a{transA, transB, Mi, Ni, Ki, (const __half*)A, lda, (const __half*)B, ldb,
+                (__half*)C, ldc, alpha, beta, splits, k_slice, splits > 1 ? scratch : nullptr,
+                sms, bn, g_fault_injection.load()};
+    path = splits > 1 ? GEMM_PATH_TC_SPLITK : GEMM_PATH_TC;
+    e = launch_hgemm(a, ctx);
+    if (e == cudaSuccess && splits > 1)
+      e = launch_splitk_reduce(1, Mi, Ni, splits, scratch, C, ldc, alpha, beta, ctx);
+  }
+  g_total_launches += ctx.launches;
+  tl_last_launches = ctx.launches;
+  if (e != cudaSuccess) return cuda_fail(e);
+  tl_last_path = path;
+  return GEMM_OK;
+}

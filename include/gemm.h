@@ -103,6 +103,34 @@ int gemm_host(int transA, int transB, int64_t M, int64_t N, int64_t K, int dtype
               int64_t ldc, gemm_stream_t stream);
 
 /*
+ * gemm_splitk_noalloc -- gemm() for callers that must not allocate device
+ * memory: code running under an allocator that already owns the whole GPU
+ * (a framework's caching allocator), or a process that forbids runtime
+ * allocation once it is serving.  It never calls cudaMalloc, cudaFree or any
+ * other allocating routine.  (No page of the method describes this entry
+ * point; it is a property of this library.)
+ *
+ * Same arguments, rules and results as gemm(), same kernels.  The split-K
+ * partial sums that gemm() takes from the stream-ordered allocator live in one
+ * fixed array of 8 MiB compiled into the library, which every GPU that loads
+ * the library holds until the process exits.  Limits:
+ *   - a problem whose split-K partials (splits x M x N x 4 bytes) exceed
+ *     8 MiB returns GEMM_ERR_UNSUPPORTED without launching anything;
+ *   - fp16 operands must have 16-byte aligned bases and row pitches (lda, ldb
+ *     multiples of 8), else GEMM_ERR_UNSUPPORTED (padding them would need
+ *     scratch).
+ * The first call on a device looks up the array's device address (a CUDA
+ * runtime query, done once per device with that device current); make that
+ * first call before any stream capture.  All calls share the array: calls
+ * whose kernels can overlap on the GPU (e.g. on two unordered streams) race
+ * on it, so order them on one stream or with events.  Nothing in it needs
+ * clearing between calls: a call writes every partial it reads.
+ */
+int gemm_splitk_noalloc(int transA, int transB, int64_t M, int64_t N, int64_t K, int dtype,
+                        float alpha, float beta, const void* A, int64_t lda, const void* B,
+                        int64_t ldb, void* C, int64_t ldc, gemm_stream_t stream);
+
+/*
  * gemm_check_device_status -- synchronises `stream`, then reads and clears
  * the current device's status word.  Returns GEMM_ERR_TIMEOUT if a kernel
  * gave up on a wait since the last check, GEMM_ERR_CUDA if the stream
