@@ -158,12 +158,24 @@ def oracle_sample(rows: int, threads: int):
     return dt, 2.0 * rows * N * K
 
 
+def calibrate_rows(threads: int, target_s: float) -> int:
+    """Rows of the headline problem the oracle finishes in about target_s:
+    two timed samples separate the per-row cost from the fixed cost (widening
+    B to double once per call)."""
+    r1, r2 = threads, 4 * threads
+    t1, _ = oracle_sample(r1, threads)
+    t2, _ = oracle_sample(r2, threads)
+    per_row = max((t2 - t1) / (r2 - r1), 1e-6)
+    fixed = max(t1 - r1 * per_row, 0.0)
+    rows = int(max(target_s - fixed, per_row) / per_row)
+    rows = max(threads, min(M, rows // threads * threads))
+    return rows
+
+
 def cpu_baseline(target_s: float = 12.0):
     import oracle
     threads = oracle.default_threads()
-    dt, fl = oracle_sample(8, threads)  # calibration
-    rows = max(8, min(M, int(8 * target_s / max(dt, 1e-3))))
-    rows = (rows // threads) * threads or threads
+    rows = calibrate_rows(threads, target_s)
     dt, fl = oracle_sample(rows, threads)
     return {"value": fl / dt / 1e12, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
             "sample": f"rows 0..{rows - 1} of the {M}x{N}x{K} product (full K and N), "
@@ -175,9 +187,8 @@ def run_reference(args, world, rank):
         return
     import oracle
     threads = oracle.default_threads()
-    dt, _ = oracle_sample(8, threads)
-    budget = max(0.2, min(2.0, 150.0 / max(1, args.steps + args.warmup)))
-    rows = max(threads, int(8 * budget / max(dt, 1e-3)) // threads * threads)
+    budget = max(0.3, min(2.0, 150.0 / max(1, args.steps + args.warmup)))
+    rows = calibrate_rows(threads, budget)
     for _ in range(args.warmup):
         oracle_sample(rows, threads)
     tot_t, tot_f = 0.0, 0.0

@@ -189,3 +189,38 @@ __device__ __forceinline__ void tmem_ld_wait() {
 }
 
 }  // namespace gb300
+
+namespace gb300 {
+// ---------------------------------------------------------------- clusters
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+// Every thread of every block of the cluster arrives and waits (the barrier
+// instructions are warp-aligned, so each warp is reconverged first).
+__device__ __forceinline__ void cluster_sync() {
+  __syncwarp();
+  asm volatile(
+      "barrier.cluster.arrive.release.aligned;\n\t"
+      "barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+// 2-D tiled load written to the same shared-memory offset of every block in
+// `mask`, each block's mbarrier at `bar` (same offset) receiving its bytes.
+__device__ __forceinline__ void tma_load_2d_mc(uint32_t dst, const CUtensorMap* map, int32_t x,
+                                               int32_t y, uint32_t bar, uint16_t mask) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
+      ".multicast::cluster [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(dst),
+      "l"(map), "r"(x), "r"(y), "r"(bar), "h"(mask)
+      : "memory");
+}
+// tcgen05.commit arriving on the mbarrier at `bar` in every block of `mask`.
+__device__ __forceinline__ void tc_commit_mc(uint32_t bar, uint16_t mask) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
+      " [%0], %1;" ::"r"(bar),
+      "h"(mask)
+      : "memory");
+}
+}  // namespace gb300

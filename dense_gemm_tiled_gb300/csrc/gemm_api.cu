@@ -103,6 +103,16 @@ int check_args(int transA, int transB, int64_t M, int64_t N, int64_t K, int dtyp
   return GEMM_OK;
 }
 
+// Debug/bench switch for the fp16 block pairs (env GEMM_GB300_HG_PAIR=0 turns
+// them off).
+int pair_enabled() {
+  static const int v = [] {
+    const char* e = getenv("GEMM_GB300_HG_PAIR");
+    return e ? atoi(e) : 1;
+  }();
+  return v;
+}
+
 // Debug/bench override of the fp16 tile width (env GEMM_GB300_HG_BN); 0 = the
 // dispatcher's own choice.
 int forced_bn() {
@@ -219,7 +229,7 @@ int run_gemm(int transA, int transB, int64_t M64, int64_t N64, int64_t K64, int 
     }
     if (e == cudaSuccess) {
       HgemmArgs a{transA, transB, M, N, K, Ad, ldad, Bd, ldbd, (__half*)C, ldc, alpha, beta,
-                  splits, k_slice, splits > 1 ? (float*)wp : nullptr, sms, bn,
+                  splits, k_slice, splits > 1 ? (float*)wp : nullptr, sms, bn, pair_enabled(),
                   g_fault_injection.load()};
       path = splits > 1 ? GEMM_PATH_TC_SPLITK : GEMM_PATH_TC;
       e = launch_hgemm(a, ctx);
@@ -443,7 +453,7 @@ extern "C" int gemm_splitk_noalloc(int transA, int transB, int64_t M, int64_t N,
       return GEMM_ERR_UNSUPPORTED;  // partial sums would not fit the fixed array
     HgemmArgs a{transA, transB, Mi, Ni, Ki, (const __half*)A, lda, (const __half*)B, ldb,
                 (__half*)C, ldc, alpha, beta, splits, k_slice, splits > 1 ? scratch : nullptr,
-                sms, bn, g_fault_injection.load()};
+                sms, bn, pair_enabled(), g_fault_injection.load()};
     path = splits > 1 ? GEMM_PATH_TC_SPLITK : GEMM_PATH_TC;
     e = launch_hgemm(a, ctx);
     if (e == cudaSuccess && splits > 1)

@@ -79,6 +79,7 @@ struct HParams {
   uint64_t timeout_ns;
   int fault_injection;
   int c_vec_ok;  // C base 16-byte aligned and ldc % 8 == 0
+  int pair;      // 1: clusters of two blocks share each B tile (TMA multicast)
 };
 
 // tcgen05 shared-memory matrix descriptor, 128-byte swizzle:
@@ -105,16 +106,22 @@ __device__ __forceinline__ constexpr uint32_t make_idesc() {
          ((uint32_t)(BN >> 3) << 17) | ((uint32_t)(BM >> 4) << 24);
 }
 
-__device__ __forceinline__ void unit_coords(int u, const HParams& p, int& m0, int& n0, int& kbeg,
-                                            int& nkb) {
-  const int tiles = p.tiles_m * p.tiles_n;
+// Work unit u -> tile.  Without pairs a unit is one 128 x BN tile; with pairs
+// (a cluster of two blocks sharing B) a unit is two vertically adjacent tiles,
+// and block `rank` of the pair takes tile row 2 * pair_row + rank.
+template <bool PAIR>
+__device__ __forceinline__ void unit_coords(int u, const HParams& p, int rank, int& m0, int& n0,
+                                            int& kbeg, int& nkb) {
+  const int rows = PAIR ? (p.tiles_m + 1) / 2 : p.tiles_m;
+  const int tiles = rows * p.tiles_n;
   const int z = u / tiles;
   const int t = u - z * tiles;
   const int per_group = GROUP_M * p.tiles_n;
   const int first_m = (t / per_group) * GROUP_M;
-  const int gsize = min(p.tiles_m - first_m, GROUP_M);
-  const int tm = first_m + (t % per_group) % gsize;
+  const int gsize = min(rows - first_m, GROUP_M);
+  const int tr = first_m + (t % per_group) % gsize;
   const int tn = (t % per_group) / gsize;
+  const int tm = PAIR ? 2 * tr + rank : tr;
   m0 = tm * BM;
   kbeg = z * p.k_slice;
   const int kend = min(p.K, kbeg + p.k_slice);
@@ -122,13 +129,19 @@ __device__ __forceinline__ void unit_coords(int u, const HParams& p, int& m0, in
   n0 = tn;  // scaled by BN by the caller
 }
 
-template <int BN, bool A_MN, bool B_MN, bool SPLIT>
+template <int BN, bool A_MN, bool B_MN, bool SPLIT, bool PAIR>
 __global__ void __launch_bounds__(THREADS, 1)
     hgemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
                     const __grid_constant__ CUtensorMap tmB, const HParams p) {
   using C_ = Cfg<BN, B_MN>;
   constexpr int STAGES = C_::STAGES;
   constexpr uint32_t STAGE_TX = (uint32_t)C_::STAGE_BYTES;
+  // Pairs: each block of the cluster loads half of the B tile and multicasts
+  // it to both, so a stage is only free again once both blocks' MMAs have
+  // read it (two arrivals on `empty`).
+  const int rank = PAIR ? (int)cluster_ctarank() : 0;
+  const int worker = PAIR ? (int)(blockIdx.x >> 1) : (int)blockIdx.x;
+  const int workers = PAIR ? (int)(gridDim.x >> 1) : (int)gridDim.x;
 
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = smem_u32(smem_raw);
@@ -151,7 +164,7 @@ __global__ void __launch_bounds__(THREADS, 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(full_bar(s), 1);
-      mbar_init(empty_bar(s), 1);
+      mbar_init(empty_bar(s), PAIR ? 2 : 1);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(accf_bar(b), 1);
@@ -166,12 +179,13 @@ __global__ void __launch_bounds__(THREADS, 1)
     tmem_relinquish();
   }
   tc_fence_before();
-  __syncthreads();
+  if constexpr (PAIR) cluster_sync();  // the peer's barriers exist before any multicast
+  else __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
 
   const WaitCtl wc{p.status, abort_flag, p.timeout_ns};
-  const int total_units = p.tiles_m * p.tiles_n * p.splits;
+  const int total_units = (PAIR ? (p.tiles_m + 1) / 2 : p.tiles_m) * p.tiles_n * p.splits;
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
@@ -183,9 +197,9 @@ __global__ void __launch_bounds__(THREADS, 1)
       uint32_t pending = 0, pend_phase = 0;  // per-stage: last load issued / its parity
       bool first = true;
       bool ok = true;
-      for (int u = blockIdx.x; u < total_units && ok; u += gridDim.x) {
+      for (int u = worker; u < total_units && ok; u += workers) {
         int m0, tn, kbeg, nkb;
-        unit_coords(u, p, m0, tn, kbeg, nkb);
+        unit_coords<PAIR>(u, p, rank, m0, tn, kbeg, nkb);
         const int n0 = tn * BN;
         for (int kb = 0; kb < nkb; ++kb) {
           if (!mbar_wait(empty_bar(stage), phase ^ 1u, wc)) { ok = false; break; }
@@ -202,7 +216,19 @@ __global__ void __launch_bounds__(THREADS, 1)
             } else {
               tma_load_2d(sa, &tmA, k0, m0, full_bar(stage));
             }
-            if constexpr (B_MN) {
+            if constexpr (PAIR) {
+              // this block's half of B, written into both blocks of the pair
+              if constexpr (B_MN) {
+                constexpr int ATOMS = C_::B_COLS / 64, MINE = ATOMS / 2;
+#pragma unroll
+                for (int h = rank * MINE; h < (rank + 1) * MINE; ++h)
+                  tma_load_2d_mc(sb + (uint32_t)h * 8192u, &tmB, n0 + 64 * h, k0,
+                                 full_bar(stage), (uint16_t)3u);
+              } else {
+                tma_load_2d_mc(sb + (uint32_t)(rank * (BN / 2) * 128), &tmB, k0,
+                               n0 + rank * (BN / 2), full_bar(stage), (uint16_t)3u);
+              }
+            } else if constexpr (B_MN) {
 #pragma unroll
               for (int h = 0; h < C_::B_COLS / 64; ++h)
                 tma_load_2d(sb + (uint32_t)h * 8192u, &tmB, n0 + 64 * h, k0, full_bar(stage));
@@ -229,9 +255,9 @@ __global__ void __launch_bounds__(THREADS, 1)
       uint32_t phase = 0;
       int it = 0;
       bool ok = true;
-      for (int u = blockIdx.x; u < total_units && ok; u += gridDim.x, ++it) {
+      for (int u = worker; u < total_units && ok; u += workers, ++it) {
         int m0, tn, kbeg, nkb;
-        unit_coords(u, p, m0, tn, kbeg, nkb);
+        unit_coords<PAIR>(u, p, rank, m0, tn, kbeg, nkb);
         const int buf = it & 1;
         const uint32_t acc_phase = (uint32_t)(it >> 1) & 1u;
         if (!mbar_wait(acce_bar(buf), acc_phase ^ 1u, wc)) { ok = false; break; }
@@ -251,7 +277,9 @@ __global__ void __launch_bounds__(THREADS, 1)
             else bd = make_sdesc(sb + (uint32_t)kk * 32u, 16u, 1024u);
             tc_mma_f16(d_tmem, ad, bd, idesc, (kb | kk) != 0 ? 1u : 0u);
           }
-          tc_commit(empty_bar(stage));  // buffer free once these MMAs finish
+          // buffer free once these MMAs finish (in both blocks of a pair)
+          if constexpr (PAIR) tc_commit_mc(empty_bar(stage), (uint16_t)3u);
+          else tc_commit(empty_bar(stage));
           if (++stage == STAGES) { stage = 0; phase ^= 1u; }
         }
         if (!ok) break;
@@ -266,9 +294,9 @@ __global__ void __launch_bounds__(THREADS, 1)
     const int q = warp & 3;  // this warp may access TMEM lanes 32q .. 32q+31
     const int row = q * 32 + lane;
     int it = 0;
-    for (int u = blockIdx.x; u < total_units; u += gridDim.x, ++it) {
+    for (int u = worker; u < total_units; u += workers, ++it) {
       int m0, tn, kbeg, nkb;
-      unit_coords(u, p, m0, tn, kbeg, nkb);
+      unit_coords<PAIR>(u, p, rank, m0, tn, kbeg, nkb);
       const int n0 = tn * BN;
       const int buf = it & 1;
       const uint32_t acc_phase = (uint32_t)(it >> 1) & 1u;
@@ -281,7 +309,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       tc_fence_after();
       const int gm = m0 + row;
       const uint32_t t_row = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(buf * BN);
-      const int z = u / (p.tiles_m * p.tiles_n);
+      const int z = u / ((PAIR ? (p.tiles_m + 1) / 2 : p.tiles_m) * p.tiles_n);
 #pragma unroll 1
       for (int c = 0; c < BN / 32; ++c) {
         uint32_t r[32];
@@ -351,7 +379,10 @@ __global__ void __launch_bounds__(THREADS, 1)
   }
 
   tc_fence_before();
-  __syncthreads();
+  // A pair leaves together: the peer's multicast copies and commit arrivals
+  // target this block's shared memory until both are done.
+  if constexpr (PAIR) cluster_sync();
+  else __syncthreads();
   if (warp == 1) {
     __syncwarp();
     tc_fence_after();
@@ -393,7 +424,7 @@ bool make_map(CUtensorMap* map, const void* base, int64_t rows, int64_t cols, in
   return r == CUDA_SUCCESS;
 }
 
-template <int BN, bool A_MN, bool B_MN, bool SPLIT>
+template <int BN, bool A_MN, bool B_MN, bool SPLIT, bool PAIR>
 cudaError_t launch_cfg(const HgemmArgs& a, const HParams& p, LaunchCtx& ctx) {
   using C_ = Cfg<BN, B_MN>;
   CUtensorMap mA, mB;
@@ -402,16 +433,42 @@ cudaError_t launch_cfg(const HgemmArgs& a, const HParams& p, LaunchCtx& ctx) {
   else ok = make_map(&mA, a.A, a.M, a.K, a.lda, 64, BM);          // stored [M, K]
   if (!ok) return cudaErrorInvalidValue;
   if (B_MN) ok = make_map(&mB, a.B, a.K, a.N, a.ldb, 64, 64);     // stored [K, N]
-  else ok = make_map(&mB, a.B, a.N, a.K, a.ldb, 64, BN);          // stored [N, K]
+  else ok = make_map(&mB, a.B, a.N, a.K, a.ldb, 64, PAIR ? BN / 2 : BN);  // stored [N, K]
   if (!ok) return cudaErrorInvalidValue;
-  auto kern = hgemm_tc_kernel<BN, A_MN, B_MN, SPLIT>;
+  auto kern = hgemm_tc_kernel<BN, A_MN, B_MN, SPLIT, PAIR>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        C_::SMEM_BYTES);
   if (e != cudaSuccess) return e;
-  const int units = p.tiles_m * p.tiles_n * p.splits;
-  const int grid = units < a.num_sms ? units : a.num_sms;
-  kern<<<grid, THREADS, C_::SMEM_BYTES, ctx.stream>>>(mA, mB, p);
-  e = cudaGetLastError();
+  if constexpr (PAIR) {
+    // persistent grid of as many pairs as can be resident at once
+    static int max_pairs = 0;  // per process: one GB300 model on the box
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.blockDim = dim3(THREADS);
+    cfg.dynamicSmemBytes = C_::SMEM_BYTES;
+    cfg.stream = ctx.stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (max_pairs == 0) {
+      cfg.gridDim = dim3(2 * (a.num_sms / 2));
+      int n = 0;
+      if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess || n <= 0) n = a.num_sms / 2;
+      max_pairs = n;
+    }
+    const int units = ((p.tiles_m + 1) / 2) * p.tiles_n * p.splits;
+    const int pairs = units < max_pairs ? units : max_pairs;
+    cfg.gridDim = dim3(2 * pairs);
+    e = cudaLaunchKernelEx(&cfg, kern, mA, mB, p);
+  } else {
+    const int units = p.tiles_m * p.tiles_n * p.splits;
+    const int grid = units < a.num_sms ? units : a.num_sms;
+    kern<<<grid, THREADS, C_::SMEM_BYTES, ctx.stream>>>(mA, mB, p);
+    e = cudaGetLastError();
+  }
   if (e == cudaSuccess) ctx.launches++;
   return e;
 }
@@ -419,10 +476,13 @@ cudaError_t launch_cfg(const HgemmArgs& a, const HParams& p, LaunchCtx& ctx) {
 template <int BN>
 cudaError_t launch_bn(const HgemmArgs& a, const HParams& p, LaunchCtx& ctx) {
   const bool A_MN = a.transA != 0, B_MN = a.transB == 0, split = a.splits > 1;
+  constexpr bool CAN_PAIR = BN == 128 || BN == 256;
 #define GB300_HG(AM, BMN)                                                   \
-  if (A_MN == AM && B_MN == BMN)                                            \
-    return split ? launch_cfg<BN, AM, BMN, true>(a, p, ctx)                 \
-                 : launch_cfg<BN, AM, BMN, false>(a, p, ctx);
+  if (A_MN == AM && B_MN == BMN) {                                          \
+    if (split) return launch_cfg<BN, AM, BMN, true, false>(a, p, ctx);      \
+    if (CAN_PAIR && p.pair) return launch_cfg<BN, AM, BMN, false, CAN_PAIR>(a, p, ctx); \
+    return launch_cfg<BN, AM, BMN, false, false>(a, p, ctx);                \
+  }
   GB300_HG(false, true)
   GB300_HG(true, true)
   GB300_HG(false, false)
@@ -439,17 +499,21 @@ int hgemm_pick_bn(int M, int N, int transB, int num_sms) {
   if (N <= 32 && transB) return 32;
   if (N <= 64) return 64;
   if (N <= 128) return 128;
-  // Wider N: the persistent grid runs ceil(tiles / SMs) rounds of tiles whose
-  // cost grows with BN, so pick the width with the fewest column-rounds
-  // (ties go to the wider tile, which re-reads A less).
+  // Wider N: the persistent grid runs ceil(tiles / SMs) rounds of tiles.  A
+  // round of 128 x BN tiles costs, relative to BN = 256 and measured on GB300
+  // at 4096^3: 0.76 (BN 128), 0.85 (BN 192), 1.0 (BN 256) -- narrower tiles
+  // re-read A from shared memory more often per flop.  Pick the cheapest;
+  // ties go to the wider tile.
   const int64_t tm = (M + BM - 1) / BM;
+  const int widths[3] = {256, 192, 128};
+  const double round_cost[3] = {1.0, 0.85, 0.76};
   int best = 256;
-  int64_t best_cost = -1;
-  for (int bn : {256, 192, 128}) {
-    const int64_t tiles = tm * ((N + bn - 1) / bn);
+  double best_cost = -1.0;
+  for (int w = 0; w < 3; ++w) {
+    const int64_t tiles = tm * ((N + widths[w] - 1) / widths[w]);
     const int64_t rounds = (tiles + num_sms - 1) / num_sms;
-    const int64_t cost = rounds * bn;
-    if (best_cost < 0 || cost < best_cost) { best = bn; best_cost = cost; }
+    const double cost = (double)rounds * round_cost[w];
+    if (best_cost < 0.0 || cost < best_cost - 1e-9) { best = widths[w]; best_cost = cost; }
   }
   return best;
 }
@@ -470,6 +534,9 @@ cudaError_t launch_hgemm(const HgemmArgs& a, LaunchCtx& ctx) {
   p.timeout_ns = ctx.timeout_ns;
   p.fault_injection = a.fault_injection;
   p.c_vec_ok = ((reinterpret_cast<uintptr_t>(a.C) & 15u) == 0 && (a.ldc % 8) == 0) ? 1 : 0;
+  // pairs of blocks share B tiles when there are at least two tile rows and no
+  // K split (the split-K path keeps single blocks)
+  p.pair = (a.pair && (bn == 128 || bn == 256) && p.tiles_m >= 2 && p.splits == 1) ? 1 : 0;
   switch (bn) {
     case 32: return launch_bn<32>(a, p, ctx);
     case 64: return launch_bn<64>(a, p, ctx);

@@ -41,6 +41,7 @@ struct HgemmArgs {
   float* partial;   // [splits][M][N] fp32 when splits > 1
   int num_sms;
   int bn;               // tile width: 32, 64, 128, 192 or 256
+  int pair;             // allow clusters of two blocks sharing B tiles
   int fault_injection;  // test hook: 1 = producer skips its first stage
 };
 
@@ -65,7 +66,12 @@ cudaError_t launch_repack_f16(int rows, int cols, const __half* src, int64_t ld_
                               __half* dst, int64_t ld_dst, LaunchCtx& ctx);
 
 // Tile sizes the dispatcher needs.
-constexpr int SG_BM = 128, SG_BN = 128, SG_BK = 32;
+// fp32 block tile: (64 * SG_WARPS_M) x 128, K step 32
+#ifndef GB300_SG_WARPS_M
+#define GB300_SG_WARPS_M 2
+#endif
+constexpr int SG_WARPS_M = GB300_SG_WARPS_M;
+constexpr int SG_BM = 64 * SG_WARPS_M, SG_BN = 128, SG_BK = 32;
 constexpr int HG_BM = 128, HG_BK = 64;
 int hgemm_pick_bn(int M, int N, int transB, int num_sms);
 

@@ -23,13 +23,13 @@
 //    coalesced; here every global load is a 16-byte cp.async and a warp's loads
 //    cover whole 64- or 512-byte row segments.
 //
-// Tile: 128 x 128 outputs per block, K step 32, 256 threads (8 warps as 2 x 4,
-// each warp 64 x 32, each lane 8 x 8 outputs split into 4-wide groups), two
-// blocks per SM.  The inner product runs on Blackwell's paired FP32 FMA
-// (fma.rn.f32x2): one instruction updates two adjacent outputs of a lane, which
-// halves the issue slots the FMAs take -- the original kernel was bound by
-// instruction issue, not by the FP32 lanes.  Each pair lane is an IEEE fp32 FMA
-// (round to nearest even); no fast-math, denormals kept.
+// Tile: (64 * WARPS_M) x 128 outputs per block, K step 32, 128 * WARPS_M threads
+// (warps WARPS_M x 4, each warp 64 x 32, each lane 8 x 8 outputs split into
+// 4-wide groups), one block per SM.  The inner product runs on Blackwell's
+// paired FP32 FMA (fma.rn.f32x2): one instruction updates two adjacent outputs
+// of a lane, halving the issue slots the FMAs take (the scalar-FMA version of
+// this kernel was bound by instruction issue).  Each half of the pair is an
+// IEEE fp32 FMA (round to nearest even); no fast-math, denormals kept.
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -40,39 +40,28 @@ namespace gb300 {
 namespace {
 
 constexpr int BM = SG_BM, BN = SG_BN, BK = SG_BK;
+constexpr int WARPS_M = SG_WARPS_M;          // warps along m (each 64 rows); 4 along n
+constexpr int THREADS = 128 * WARPS_M;
 constexpr int STAGES = 3;
-constexpr int THREADS = 256;
-constexpr int PAD = BN + 4;                 // k-major tile rows padded: conflict-free transposing writes
-constexpr int TILE_FLOATS = BK * PAD;       // 16.5 KiB per operand per stage
-constexpr int STAGE_FLOATS = 2 * TILE_FLOATS;
-constexpr int SMEM_BYTES = STAGES * STAGE_FLOATS * 4;  // 99 KiB: two blocks per SM
+constexpr int APAD = BM + 4;  // k-major tile rows padded: conflict-free transposing writes
+constexpr int BPAD = BN + 4;
+constexpr int A_FLOATS = (BM * BK > BK * APAD) ? BM * BK : BK * APAD;
+constexpr int B_FLOATS = BK * BPAD;
+constexpr int STAGE_FLOATS = A_FLOATS + B_FLOATS;
+constexpr int SMEM_BYTES = STAGES * STAGE_FLOATS * 4;
 constexpr int GROUP_M = 8;  // tile rasterisation: 8 tile-rows walked together
-static_assert(BM == BN, "square block tile");
+static_assert(BM == 64 * WARPS_M && BN == 128 && BK == 32, "tile shape");
 
-// Compile-time tuning knobs.
+// Compile-time tuning knobs (measured on GB300 at 4096^3; the defaults won):
 //  GB300_SG_MIN_BLOCKS  blocks per SM the register budget is sized for
 //  GB300_SG_KC_UNROLL   unrolling of the 4-k chunk loop
-//  GB300_SG_A_T         1: an A stored [M,K] is transposed into a k-major tile on
-//                       the way in (as B stored [N,K] always is)
-//  GB300_SG_MATH        0: scalar FMA; 1: paired FMA, A value splatted into both
-//                       halves; 2: paired FMA on (row, row+1) x (col, col+1)
-//                       pairs plus the column-swapped pair (no splat; needs a
-//                       k-major A tile)
 #ifndef GB300_SG_MIN_BLOCKS
 #define GB300_SG_MIN_BLOCKS 1
 #endif
 #ifndef GB300_SG_KC_UNROLL
 #define GB300_SG_KC_UNROLL 8
 #endif
-#ifndef GB300_SG_A_T
-#define GB300_SG_A_T 0
-#endif
-#ifndef GB300_SG_MATH
-#define GB300_SG_MATH 1
-#endif
 constexpr int KC_UNROLL = GB300_SG_KC_UNROLL;
-constexpr bool A_TRANSPOSE = GB300_SG_A_T != 0;
-constexpr int MATH = GB300_SG_MATH;
 
 struct Params {
   const float* A;
@@ -87,29 +76,33 @@ struct Params {
 };
 
 // ---------------------------------------------------------------- staging
-// Two tile layouts per operand and stage:
-//  "k-major" tile : 32 rows (k) x 128 (m or n), rows padded to 132 floats; an
-//                   operand stored with m/n contiguous (A[K,M], B[K,N]) is copied
-//                   row by row with 16-byte copies; one stored with k contiguous
-//                   (A[M,K], B[N,K]) can be transposed into it on the way in with
-//                   4-byte copies -- the transposing write of "Metal GEMM Kernels
-//                   for LoRA Training", section 3, done by the async-copy unit.
-//                   A warp then reads 4 rows x 32 bytes of global memory and,
-//                   thanks to the padding, writes 32 distinct banks.
-//  "row" tile     : 128 rows (m) x 32 k, 128-byte rows whose eight 16-byte chunks
+// Tile layouts per operand and stage:
+//  "k-major" tile : 32 rows (k) x BM or BN (m or n), rows padded by 4 floats.
+//                   An operand stored with m/n contiguous (A[K,M], B[K,N]) is
+//                   copied row by row with 16-byte copies.  B stored [N,K] is
+//                   transposed into it on the way in with 4-byte copies -- the
+//                   transposing write of "Metal GEMM Kernels for LoRA Training",
+//                   section 3, done by the async-copy unit: a warp reads 4 rows
+//                   x 32 bytes of global memory and, thanks to the padding,
+//                   writes 32 distinct banks.  B must be k-major because the
+//                   paired FMA needs column pairs (n, n+1) in adjacent registers.
+//  "row" tile     : BM rows (m) x 32 k, 128-byte rows whose eight 16-byte chunks
 //                   are permuted by chunk ^ ((row >> 2) & 7) so that the lanes
 //                   reading the same k of rows r and r+4 hit distinct banks;
-//                   filled from A[M,K] with 16-byte copies.
+//                   A stored [M,K] stays in this layout (measured faster than
+//                   transposing it, by copies or through registers).
 __device__ __forceinline__ int a_swz(int row, int chunk) { return chunk ^ ((row >> 2) & 7); }
 
-// source [R rows][K] (k contiguous) -> row tile
+// source [R rows][K] (k contiguous) -> row tile of BM rows
 template <bool VEC>
 __device__ __forceinline__ void load_rows(uint32_t dst, const float* __restrict__ g, int64_t ld,
                                           int r0, int R, int k0, int K, int tid) {
   if constexpr (VEC) {
+    constexpr int CHUNKS = BM * (BK / 4);
 #pragma unroll
-    for (int r = 0; r < 4; ++r) {
-      const int q = tid + r * THREADS;
+    for (int it = 0; it < (CHUNKS + THREADS - 1) / THREADS; ++it) {
+      const int q = tid + it * THREADS;
+      if (CHUNKS % THREADS != 0 && q >= CHUNKS) break;
       const int row = q >> 3, c = q & 7;
       const int gr = r0 + row, gk = k0 + c * 4;
       const bool ok = (gr < R) && (gk < K);
@@ -118,9 +111,11 @@ __device__ __forceinline__ void load_rows(uint32_t dst, const float* __restrict_
       cp_async_16(dst + (uint32_t)(row * BK + a_swz(row, c) * 4) * 4u, src, bytes);
     }
   } else {
+    constexpr int ELEMS = BM * BK;
 #pragma unroll 4
-    for (int r = 0; r < 16; ++r) {
-      const int e = tid + r * THREADS;
+    for (int it = 0; it < (ELEMS + THREADS - 1) / THREADS; ++it) {
+      const int e = tid + it * THREADS;
+      if (ELEMS % THREADS != 0 && e >= ELEMS) break;
       const int row = e >> 5, kk = e & 31;
       const int gr = r0 + row, gk = k0 + kk;
       const bool ok = (gr < R) && (gk < K);
@@ -131,49 +126,59 @@ __device__ __forceinline__ void load_rows(uint32_t dst, const float* __restrict_
   }
 }
 
-// source [K][R] (m/n contiguous) -> k-major tile
-template <bool VEC>
+// source [K][R] (m/n contiguous) -> k-major tile of W columns, row pitch PITCH
+template <bool VEC, int W, int PITCH>
 __device__ __forceinline__ void load_kmajor(uint32_t dst, const float* __restrict__ g, int64_t ld,
                                             int r0, int R, int k0, int K, int tid) {
   if constexpr (VEC) {
+    constexpr int CPR = W / 4;  // 16-byte chunks per k row
+    constexpr int CHUNKS = BK * CPR;
 #pragma unroll
-    for (int r = 0; r < 4; ++r) {
-      const int q = tid + r * THREADS;
-      const int krow = q >> 5, c = q & 31;
+    for (int it = 0; it < (CHUNKS + THREADS - 1) / THREADS; ++it) {
+      const int q = tid + it * THREADS;
+      if (CHUNKS % THREADS != 0 && q >= CHUNKS) break;
+      const int krow = q / CPR, c = q - krow * CPR;
       const int gk = k0 + krow, gr = r0 + c * 4;
       const bool ok = (gk < K) && (gr < R);
       const uint32_t bytes = ok ? (uint32_t)min(4, R - gr) * 4u : 0u;
       const float* src = ok ? g + (int64_t)gk * ld + gr : g;
-      cp_async_16(dst + (uint32_t)(krow * PAD + c * 4) * 4u, src, bytes);
+      cp_async_16(dst + (uint32_t)(krow * PITCH + c * 4) * 4u, src, bytes);
     }
   } else {
+    constexpr int ELEMS = BK * W;
 #pragma unroll 4
-    for (int r = 0; r < 16; ++r) {
-      const int e = tid + r * THREADS;
-      const int krow = e >> 7, rr = e & 127;
+    for (int it = 0; it < (ELEMS + THREADS - 1) / THREADS; ++it) {
+      const int e = tid + it * THREADS;
+      if (ELEMS % THREADS != 0 && e >= ELEMS) break;
+      const int krow = e / W, rr = e - krow * W;
       const int gk = k0 + krow, gr = r0 + rr;
       const bool ok = (gk < K) && (gr < R);
       const float* src = ok ? g + (int64_t)gk * ld + gr : g;
-      cp_async_4(dst + (uint32_t)(krow * PAD + rr) * 4u, src, ok ? 4u : 0u);
+      cp_async_4(dst + (uint32_t)(krow * PITCH + rr) * 4u, src, ok ? 4u : 0u);
     }
   }
 }
 
-// source [R rows][K] (k contiguous) -> k-major tile, transposed by 4-byte copies:
-// lane l reads k = l & 7 of row (l >> 3) of a 4-row group
+// source [R rows][K] (k contiguous) -> k-major tile of W columns, transposed by
+// 4-byte copies: lane l reads k = l & 7 of row (l >> 3) of a 4-row group
+template <int W, int PITCH>
 __device__ __forceinline__ void load_transpose(uint32_t dst, const float* __restrict__ g,
                                                int64_t ld, int r0, int R, int k0, int K,
                                                int tid) {
   const int warp = tid >> 5, lane = tid & 31;
   const int kl = lane & 7, rl = lane >> 3;
+  constexpr int GROUPS = (W / 4) * (BK / 8);  // 4-row x 8-k groups
+  constexpr int WARPS = THREADS / 32;
 #pragma unroll 4
-  for (int r = 0; r < 16; ++r) {
-    const int grp = r * 8 + warp;  // 0..127: 32 row-groups of 4 x 4 k-groups of 8
-    const int row = (grp & 31) * 4 + rl, k = (grp >> 5) * 8 + kl;
+  for (int it = 0; it < (GROUPS + WARPS - 1) / WARPS; ++it) {
+    const int grp = warp + it * WARPS;
+    if (GROUPS % WARPS != 0 && grp >= GROUPS) break;
+    const int rg = grp % (W / 4), kg = grp / (W / 4);
+    const int row = rg * 4 + rl, k = kg * 8 + kl;
     const int gr = r0 + row, gk = k0 + k;
     const bool ok = (gr < R) && (gk < K);
     const float* src = ok ? g + (int64_t)gr * ld + gk : g;
-    cp_async_4(dst + (uint32_t)(k * PAD + row) * 4u, src, ok ? 4u : 0u);
+    cp_async_4(dst + (uint32_t)(k * PITCH + row) * 4u, src, ok ? 4u : 0u);
   }
 }
 
@@ -191,78 +196,18 @@ __device__ __forceinline__ uint64_t splat2(float x) {
   asm("mov.b64 %0, {%1, %1};" : "=l"(r) : "f"(x));
   return r;
 }
-__device__ __forceinline__ uint64_t swap2(uint64_t v) {
-  uint64_t r;
-  asm("{\n\t.reg .b32 lo, hi;\n\tmov.b64 {lo, hi}, %1;\n\tmov.b64 %0, {hi, lo};\n\t}"
-      : "=l"(r) : "l"(v));
-  return r;
-}
 __device__ __forceinline__ float2 unpack2(uint64_t v) {
   float2 f;
   asm("mov.b64 {%0, %1}, %2;" : "=f"(f.x), "=f"(f.y) : "l"(v));
   return f;
-}
-__device__ __forceinline__ uint64_t pack2(float lo, float hi) {
-  uint64_t r;
-  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
-  return r;
 }
 
 __device__ __forceinline__ float4 lds128(const float* p) {
   return *reinterpret_cast<const float4*>(p);
 }
 
-// Accumulators of one lane's 8 x 8 block, in the representation MATH needs.
-template <int MODE>
-struct Acc;
-template <>
-struct Acc<0> {  // scalar
-  float v[8][8];
-  __device__ __forceinline__ void zero() {
-#pragma unroll
-    for (int i = 0; i < 8; ++i)
-#pragma unroll
-      for (int j = 0; j < 8; ++j) v[i][j] = 0.f;
-  }
-  __device__ __forceinline__ float get(int i, int j) const { return v[i][j]; }
-};
-template <>
-struct Acc<1> {  // pairs along n: p[i][jp] = (row i, cols 2jp, 2jp+1)
-  uint64_t p[8][4];
-  __device__ __forceinline__ void zero() {
-#pragma unroll
-    for (int i = 0; i < 8; ++i)
-#pragma unroll
-      for (int j = 0; j < 4; ++j) p[i][j] = 0ull;
-  }
-  __device__ __forceinline__ float get(int i, int j) const {
-    const float2 f = unpack2(p[i][j >> 1]);
-    return (j & 1) ? f.y : f.x;
-  }
-};
-template <>
-struct Acc<2> {  // d[q][r] = (acc(2q,2r), acc(2q+1,2r+1)); e[q][r] = (acc(2q,2r+1), acc(2q+1,2r))
-  uint64_t d[4][4], e[4][4];
-  __device__ __forceinline__ void zero() {
-#pragma unroll
-    for (int q = 0; q < 4; ++q)
-#pragma unroll
-      for (int r = 0; r < 4; ++r) { d[q][r] = 0ull; e[q][r] = 0ull; }
-  }
-  __device__ __forceinline__ float get(int i, int j) const {
-    const int q = i >> 1, r = j >> 1;
-    const bool ei = i & 1, ej = j & 1;
-    if (ei == ej) { const float2 f = unpack2(d[q][r]); return ei ? f.y : f.x; }
-    const float2 f = unpack2(e[q][r]);
-    return ei ? f.y : f.x;
-  }
-};
-
 template <bool A_K, bool B_K, bool VEC, bool SPLIT>
 __global__ void __launch_bounds__(THREADS, GB300_SG_MIN_BLOCKS) sgemm_ffma_kernel(const Params p) {
-  // A held as a row tile only when stored [M,K] and not transposed on the way in
-  constexpr bool A_ROWS = A_K && !A_TRANSPOSE;
-  constexpr int MODE = (MATH == 2 && A_ROWS) ? 1 : MATH;  // pairs of rows need a k-major A
   extern __shared__ __align__(16) float smem[];
   const int tid = threadIdx.x;
   const int warp = tid >> 5, lane = tid & 31;
@@ -290,16 +235,19 @@ __global__ void __launch_bounds__(THREADS, GB300_SG_MIN_BLOCKS) sgemm_ffma_kerne
   const uint32_t sbase = smem_u32(smem);
   auto stage_load = [&](int s, int k0) {
     const uint32_t st = sbase + (uint32_t)(s * STAGE_FLOATS) * 4u;
-    if constexpr (A_ROWS) load_rows<VEC>(st, p.A, p.lda, m0, p.M, k0, kend, tid);
-    else if constexpr (A_K) load_transpose(st, p.A, p.lda, m0, p.M, k0, kend, tid);
-    else load_kmajor<VEC>(st, p.A, p.lda, m0, p.M, k0, kend, tid);
-    const uint32_t sb = st + TILE_FLOATS * 4u;
-    if constexpr (B_K) load_transpose(sb, p.B, p.ldb, n0, p.N, k0, kend, tid);
-    else load_kmajor<VEC>(sb, p.B, p.ldb, n0, p.N, k0, kend, tid);
+    if constexpr (A_K) load_rows<VEC>(st, p.A, p.lda, m0, p.M, k0, kend, tid);
+    else load_kmajor<VEC, BM, APAD>(st, p.A, p.lda, m0, p.M, k0, kend, tid);
+    const uint32_t sb = st + A_FLOATS * 4u;
+    if constexpr (B_K) load_transpose<BN, BPAD>(sb, p.B, p.ldb, n0, p.N, k0, kend, tid);
+    else load_kmajor<VEC, BN, BPAD>(sb, p.B, p.ldb, n0, p.N, k0, kend, tid);
   };
 
-  Acc<MODE> acc;
-  acc.zero();
+  // acc[i][jp] holds the outputs (row i, columns 2jp and 2jp+1) as a pair
+  uint64_t acc[8][4];
+#pragma unroll
+  for (int i = 0; i < 8; ++i)
+#pragma unroll
+    for (int j = 0; j < 4; ++j) acc[i][j] = 0ull;
 
 #pragma unroll
   for (int s = 0; s < STAGES - 1; ++s) {
@@ -316,15 +264,15 @@ __global__ void __launch_bounds__(THREADS, GB300_SG_MIN_BLOCKS) sgemm_ffma_kerne
       cp_async_commit();
     }
     const float* As = smem + (kt % STAGES) * STAGE_FLOATS;
-    const float* Bs = As + TILE_FLOATS;
+    const float* Bs = As + A_FLOATS;
 #pragma unroll KC_UNROLL
     for (int kc = 0; kc < BK / 4; ++kc) {
       float a[8][4];  // a[i][kk]: row i, k = 4kc + kk (row-tile A)
 #pragma unroll
       for (int kk = 0; kk < 4; ++kk) {
         const int k = kc * 4 + kk;
-        const float* brow = Bs + k * PAD + bcol;
-        if constexpr (A_ROWS) {
+        float av[8];
+        if constexpr (A_K) {
           // two k at a time (64-bit loads) keeps 16 rather than 32 A values live
           if ((kk & 1) == 0) {
             const float* base = As + arow * BK + ((kc ^ aswz) * 4) + kk;
@@ -334,62 +282,30 @@ __global__ void __launch_bounds__(THREADS, GB300_SG_MIN_BLOCKS) sgemm_ffma_kerne
               a[i][kk] = v.x; a[i][kk + 1] = v.y;
             }
           }
-        }
-        if constexpr (MODE == 2) {
-          // k-major A and B: pairs (row 2q, 2q+1) and (col 2r, 2r+1)
-          const float* arow_p = As + k * PAD + arow;
-          const ulonglong2 a01 = *reinterpret_cast<const ulonglong2*>(arow_p);
-          const ulonglong2 a23 = *reinterpret_cast<const ulonglong2*>(arow_p + 32);
-          const ulonglong2 b01 = *reinterpret_cast<const ulonglong2*>(brow);
-          const ulonglong2 b23 = *reinterpret_cast<const ulonglong2*>(brow + 16);
-          const uint64_t ap[4] = {a01.x, a01.y, a23.x, a23.y};
-          const uint64_t bp[4] = {b01.x, b01.y, b23.x, b23.y};
-          uint64_t bs[4];
 #pragma unroll
-          for (int r = 0; r < 4; ++r) bs[r] = swap2(bp[r]);
-#pragma unroll
-          for (int q = 0; q < 4; ++q)
-#pragma unroll
-            for (int r = 0; r < 4; ++r) {
-              acc.d[q][r] = ffma2(ap[q], bp[r], acc.d[q][r]);
-              acc.e[q][r] = ffma2(ap[q], bs[r], acc.e[q][r]);
-            }
+          for (int i = 0; i < 8; ++i) av[i] = a[i][kk];
         } else {
-          float av[8];
-          if constexpr (A_ROWS) {
+          const float4 lo = lds128(As + k * APAD + arow);
+          const float4 hi = lds128(As + k * APAD + arow + 32);
+          av[0] = lo.x; av[1] = lo.y; av[2] = lo.z; av[3] = lo.w;
+          av[4] = hi.x; av[5] = hi.y; av[6] = hi.z; av[7] = hi.w;
+        }
+        const float* brow = Bs + k * BPAD + bcol;
+        const ulonglong2 b01 = *reinterpret_cast<const ulonglong2*>(brow);
+        const ulonglong2 b23 = *reinterpret_cast<const ulonglong2*>(brow + 16);
+        const uint64_t bp[4] = {b01.x, b01.y, b23.x, b23.y};
 #pragma unroll
-            for (int i = 0; i < 8; ++i) av[i] = a[i][kk];
-          } else {
-            const float4 lo = lds128(As + k * PAD + arow);
-            const float4 hi = lds128(As + k * PAD + arow + 32);
-            av[0] = lo.x; av[1] = lo.y; av[2] = lo.z; av[3] = lo.w;
-            av[4] = hi.x; av[5] = hi.y; av[6] = hi.z; av[7] = hi.w;
-          }
-          if constexpr (MODE == 1) {
-            const ulonglong2 b01 = *reinterpret_cast<const ulonglong2*>(brow);
-            const ulonglong2 b23 = *reinterpret_cast<const ulonglong2*>(brow + 16);
-            const uint64_t bp[4] = {b01.x, b01.y, b23.x, b23.y};
+        for (int i = 0; i < 8; ++i) {
+          const uint64_t ap = splat2(av[i]);
 #pragma unroll
-            for (int i = 0; i < 8; ++i) {
-              const uint64_t ap = splat2(av[i]);
-#pragma unroll
-              for (int j = 0; j < 4; ++j) acc.p[i][j] = ffma2(ap, bp[j], acc.p[i][j]);
-            }
-          } else {
-            const float4 b0 = lds128(brow), b1 = lds128(brow + 16);
-            const float bv[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
-#pragma unroll
-            for (int i = 0; i < 8; ++i)
-#pragma unroll
-              for (int j = 0; j < 8; ++j) acc.v[i][j] = __fmaf_rn(av[i], bv[j], acc.v[i][j]);
-          }
+          for (int j = 0; j < 4; ++j) acc[i][j] = ffma2(ap, bp[j], acc[i][j]);
         }
       }
     }
   }
   cp_async_wait<0>();
 
-  // epilogue: lane columns bcol + {0..3} and bcol + 16 + {0..3}
+  // epilogue: lane columns bcol + {0..3} (pairs 0, 1) and bcol + 16 + {0..3} (pairs 2, 3)
 #pragma unroll
   for (int i = 0; i < 8; ++i) {
     const int gm = m0 + arow + (i < 4 ? i : 32 + i - 4);
@@ -397,9 +313,8 @@ __global__ void __launch_bounds__(THREADS, GB300_SG_MIN_BLOCKS) sgemm_ffma_kerne
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
       const int gn = n0 + bcol + h * 16;
-      float v[4];
-#pragma unroll
-      for (int j = 0; j < 4; ++j) v[j] = acc.get(i, h * 4 + j);
+      const float2 lo = unpack2(acc[i][2 * h]), hi = unpack2(acc[i][2 * h + 1]);
+      const float v[4] = {lo.x, lo.y, hi.x, hi.y};
       if constexpr (SPLIT) {
         float* dst = p.partial + ((int64_t)blockIdx.z * p.M + gm) * p.N + gn;
         if (gn + 3 < p.N && (p.N & 3) == 0) {

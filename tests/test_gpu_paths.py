@@ -1,0 +1,44 @@
+"""Every fp16 kernel configuration against the oracle.
+
+The dispatcher picks one tile width (64/128/192/256 columns) and, for 128 and
+256, pairs of blocks sharing B tiles by multicast.  Each configuration is
+forced here in its own process (the switches are read once per process from
+GEMM_GB300_HG_PAIR and GEMM_GB300_HG_BN) and checked on ragged, multi-tile
+problems in all four variants, exact on small-integer inputs.
+"""
+import os
+import subprocess
+import sys
+
+import pytest
+
+pytestmark = pytest.mark.gpu
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+SCRIPT = r"""
+import sys
+sys.path.insert(0, {root!r}); sys.path.insert(0, {tests!r})
+from dense_gemm_tiled_gb300 import inputs
+from helpers import check_problem
+for v in ("nn", "tn", "nt", "tt"):
+    tA, tB = inputs.VARIANTS[v]
+    # 3 tile rows (odd: the last pair has a block past M), ragged N and K
+    p = inputs.make_problem(384, 640, 448, tA, tB, "f16", "integer", seed=600)
+    check_problem(p, exact=True)
+    p = inputs.make_problem(300, 520, 264, tA, tB, "f16", "uniform", seed=601, beta=0.5)
+    check_problem(p)
+    p = inputs.make_problem(1024, 768, 1000, tA, tB, "f16", "uniform", seed=602)
+    check_problem(p)
+print("ok")
+"""
+
+
+@pytest.mark.parametrize("pair,bn", [("1", "256"), ("0", "256"), ("1", "128"), ("0", "128"),
+                                     ("0", "192"), ("0", "64")])
+def test_forced_kernel_configuration(lib_path, gpu, pair, bn):
+    env = dict(os.environ, GEMM_GB300_HG_PAIR=pair, GEMM_GB300_HG_BN=bn)
+    code = SCRIPT.format(root=ROOT, tests=os.path.join(ROOT, "tests"))
+    r = subprocess.run([sys.executable, "-c", code], env=env, capture_output=True, text=True,
+                       timeout=900)
+    assert r.returncode == 0 and r.stdout.strip().endswith("ok"), r.stdout[-3000:] + r.stderr[-3000:]
