@@ -212,6 +212,61 @@ def run_reference(args, world, rank):
 
 
 # ------------------------------------------------------------------ GPU legs
+def lora_step(dev, stream, reps: int = 20):
+    """The 18 GEMMs of one LoRA MLP-block training step ("Metal GEMM Kernels for
+    LoRA Training", section 5: T=512, d=2048, FFN=5632, rank 32), fp16 with fp32
+    accumulation: per-GEMM device time (CUDA events, median) and the whole set
+    replayed as one CUDA graph."""
+    import torch
+    from dense_gemm_tiled_gb300 import binding, inputs
+    gemms = inputs.lora_step_gemms()
+    ops = []
+    for i, g in enumerate(gemms):
+        p = inputs.lora_problem(g, seed=500 + i)
+        A, B = p.A.to(dev), p.B.to(dev)
+        C = (p.C_in.to(dev).clone() if p.C_in is not None
+             else torch.empty((p.M, p.N), dtype=torch.float16, device=dev))
+        ops.append((g, p, A, B, C))
+
+    def one(op):
+        g, p, A, B, C = op
+        binding.gemm(A, B, C, p.transA, p.transB, p.alpha, p.beta, stream=stream)
+
+    for op in ops:  # warm-up (also the per-device set-up, before any capture)
+        one(op)
+    torch.cuda.synchronize()
+    per = {}
+    for op in ops:
+        ts = []
+        for _ in range(reps):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            one(op)
+            e1.record(stream)
+            e1.synchronize()
+            ts.append(e0.elapsed_time(e1))
+        per[op[0].name] = {"us": statistics.median(ts) * 1e3, "path": binding.last_path(),
+                           "shape": [op[0].M, op[0].N, op[0].K], "variant": op[0].variant}
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        for op in ops:
+            one(op)
+    for _ in range(3):
+        graph.replay()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(reps):
+        graph.replay()
+    e1.record()
+    e1.synchronize()
+    graph_ms = e0.elapsed_time(e1) / reps
+    flops = sum(2.0 * g.M * g.N * g.K for g in gemms)
+    return {"gemms": len(gemms), "gflop": flops / 1e9, "graph_ms": graph_ms,
+            "graph_tflops": flops / (graph_ms * 1e-3) / 1e12,
+            "sum_of_gemms_ms": sum(v["us"] for v in per.values()) / 1e3, "per_gemm": per}
+
+
 def run_case(args, local):
     """One GEMM, `warmup` untimed launches then `steps` timed ones (CUDA events
     per launch on the launching stream)."""
@@ -251,6 +306,7 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-fp16", action="store_true")
+    ap.add_argument("--no-lora", action="store_true")
     ap.add_argument("--case", default=None,
                     help="run only one GEMM (e.g. f32_nn_4096, f16_tn_4096, f16_nn_8192): "
                          "warm-up + steps, one short JSON line; used for profiling")
@@ -369,6 +425,8 @@ def main():
         del flush
         assert binding.check_device_status(stream) == binding.OK
 
+    lora = None if args.no_lora else lora_step(dev, stream)
+
     # end to end through gemm_host(): pinned host inputs, result read back
     Ah = inputs.uniform((M, K), 60, "f32").pin_memory()
     Bh = inputs.uniform((K, N), 61, "f32").pin_memory()
@@ -404,6 +462,7 @@ def main():
             "kernel_ms_avg": avg_kernel_ms,
             "roofline": roofline,
             "fp16_4096": fp16,
+            "lora_step": lora,
             "e2e": e2e,
             "cpu_baseline": cpu,
             "gpu_launches": launches,

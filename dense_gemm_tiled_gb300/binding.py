@@ -32,6 +32,7 @@ _lib.gemm_status_string.restype = ctypes.c_char_p
 _lib.gemm_version.restype = _int
 _lib.gemm_last_path.restype = _int
 _lib.gemm_last_launches.restype = _int
+_lib.gemm_last_grid.restype = _int
 _lib.gemm_total_launches.restype = _i64
 _lib.gemm_set_wait_timeout_ns.argtypes = [_i64]
 _lib.gemm_set_wait_timeout_ns.restype = None
@@ -64,6 +65,10 @@ def last_path() -> str:
 
 def last_launches() -> int:
     return _lib.gemm_last_launches()
+
+
+def last_grid() -> int:
+    return _lib.gemm_last_grid()
 
 
 def total_launches() -> int:

@@ -224,3 +224,27 @@ __device__ __forceinline__ void tc_commit_mc(uint32_t bar, uint16_t mask) {
       : "memory");
 }
 }  // namespace gb300
+
+namespace gb300 {
+// ---------------------------------------------------------------- TMA store
+// 2-D tiled store of the shared-memory box at `src` to coordinates (x, y) of
+// the tensor (clipped to the tensor's extent), in this thread's bulk group.
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, int32_t x, int32_t y,
+                                             uint32_t src) {
+  asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%1, %2}], [%3];" ::"l"(map),
+               "r"(x), "r"(y), "r"(src)
+               : "memory");
+}
+__device__ __forceinline__ void bulk_commit() {
+  asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+// wait until at most N bulk groups of this thread still read shared memory
+template <int N>
+__device__ __forceinline__ void bulk_wait_read() {
+  asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
+}
+// wait until every bulk group of this thread has completed
+__device__ __forceinline__ void bulk_wait_all() {
+  asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+}
+}  // namespace gb300

@@ -37,6 +37,7 @@ std::atomic<int64_t> g_timeout_ns{2000000000LL};
 std::atomic<int> g_fault_injection{0};
 thread_local int tl_last_path = GEMM_PATH_NONE;
 thread_local int tl_last_launches = 0;
+thread_local int tl_last_grid = 0;
 
 // Per-device set-up, done once with that device current: the status word's
 // device address and the SM count.
@@ -113,6 +114,28 @@ int pair_enabled() {
   return v;
 }
 
+// Debug/bench switch for the fp16 TMA-store epilogue (env GEMM_GB300_HG_CTMA=0
+// turns it off).
+int c_tma_enabled() {
+  static const int v = [] {
+    const char* e = getenv("GEMM_GB300_HG_CTMA");
+    return e ? atoi(e) : 1;
+  }();
+  return v;
+}
+
+// Switch for the fp16 tail split (env GEMM_GB300_HG_TAIL=1 turns it on).  Off
+// by default: measured on GB300 at 4096^3 and 8192^3 it was within noise of
+// the plain persistent grid (the last, partly idle round of tiles runs faster
+// per tile because fewer blocks share the L2-to-SM bandwidth).
+int tail_enabled() {
+  static const int v = [] {
+    const char* e = getenv("GEMM_GB300_HG_TAIL");
+    return e ? atoi(e) : 0;
+  }();
+  return v;
+}
+
 // Debug/bench override of the fp16 tile width (env GEMM_GB300_HG_BN); 0 = the
 // dispatcher's own choice.
 int forced_bn() {
@@ -147,6 +170,35 @@ void plan_splits(int64_t tiles, int64_t K, int kstep, int capacity, int min_step
   *splits = (int)((steps + per - 1) / per);  // every slice non-empty
 }
 
+// Scratch comes from a stream-ordered memory pool owned by the library, one
+// per device, that keeps freed memory for reuse (release threshold: never).
+// The device's default pool would hand its memory back at every
+// synchronisation, and re-mapping a few MB costs ~0.1 ms per call.
+cudaMemPool_t g_pool[MAX_DEVICES];
+
+cudaError_t scratch_pool(cudaMemPool_t* out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= MAX_DEVICES) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (!g_pool[dev]) {
+    cudaMemPoolProps props = {};
+    props.allocType = cudaMemAllocationTypePinned;
+    props.location.type = cudaMemLocationTypeDevice;
+    props.location.id = dev;
+    cudaMemPool_t pool;
+    e = cudaMemPoolCreate(&pool, &props);
+    if (e != cudaSuccess) return e;
+    uint64_t keep = UINT64_MAX;
+    e = cudaMemPoolSetAttribute(pool, cudaMemPoolAttrReleaseThreshold, &keep);
+    if (e != cudaSuccess) return e;
+    g_pool[dev] = pool;
+  }
+  *out = g_pool[dev];
+  return cudaSuccess;
+}
+
 struct Scratch {
   void* ptr = nullptr;
   cudaStream_t stream = nullptr;
@@ -155,7 +207,10 @@ struct Scratch {
   }
   cudaError_t get(size_t bytes, cudaStream_t s) {
     stream = s;
-    return cudaMallocAsync(&ptr, bytes, s);
+    cudaMemPool_t pool;
+    cudaError_t e = scratch_pool(&pool);
+    if (e != cudaSuccess) return e;
+    return cudaMallocFromPoolAsync(&ptr, bytes, pool, s);
   }
 };
 
@@ -211,12 +266,28 @@ int run_gemm(int transA, int transB, int64_t M64, int64_t N64, int64_t K64, int 
     size_t bytes_a = a_ok ? 0 : (size_t)(a_rows * lda_p * 2 + 255) / 256 * 256;
     size_t bytes_b = b_ok ? 0 : (size_t)(b_rows * ldb_p * 2 + 255) / 256 * 256;
     size_t bytes_p = splits > 1 ? (size_t)splits * M * N * sizeof(float) : 0;
+    // tail split of the persistent grid's last round (needs its own partials)
+    const int pair = pair_enabled();
+    const bool use_pair = hgemm_use_pair(bn, M, splits, pair);
+    TailPlan tail{0, 0, 0, 0, 0};
+    if (splits == 1 && tail_enabled())
+      tail = hgemm_plan_tail(M, N, K, bn, use_pair,
+                             use_pair ? hgemm_pair_slots(bn, transA, transB, sms) : sms);
+    const size_t bytes_t = tail.splits > 0 ? (tail.ws_bytes + 255) / 256 * 256 + tail.cnt_bytes : 0;
     Scratch ws;
-    if (bytes_a + bytes_b + bytes_p > 0) {
-      e = ws.get(bytes_a + bytes_b + bytes_p, stream);
+    if (bytes_a + bytes_b + bytes_p + bytes_t > 0) {
+      e = ws.get(bytes_a + bytes_b + bytes_p + bytes_t, stream);
       if (e != cudaSuccess) return cuda_fail(e);
     }
     char* wp = (char*)ws.ptr;
+    float* tail_ws = nullptr;
+    unsigned int* tail_cnt = nullptr;
+    if (tail.splits > 0) {
+      tail_ws = (float*)(wp + bytes_a + bytes_b + bytes_p);
+      tail_cnt = (unsigned int*)((char*)tail_ws + (tail.ws_bytes + 255) / 256 * 256);
+      e = cudaMemsetAsync(tail_cnt, 0, tail.cnt_bytes, stream);
+      if (e != cudaSuccess) return cuda_fail(e);
+    }
     if (!a_ok) {
       __half* dst = (__half*)wp;
       e = launch_repack_f16((int)a_rows, (int)a_cols, Ad, lda, dst, lda_p, ctx);
@@ -229,8 +300,15 @@ int run_gemm(int transA, int transB, int64_t M64, int64_t N64, int64_t K64, int 
     }
     if (e == cudaSuccess) {
       HgemmArgs a{transA, transB, M, N, K, Ad, ldad, Bd, ldbd, (__half*)C, ldc, alpha, beta,
-                  splits, k_slice, splits > 1 ? (float*)wp : nullptr, sms, bn, pair_enabled(),
-                  g_fault_injection.load()};
+                  splits, k_slice, splits > 1 ? (float*)wp : nullptr, sms, bn, pair,
+                  c_tma_enabled(), g_fault_injection.load()};
+      if (tail.splits > 0) {
+        a.dp_units = tail.dp_units;
+        a.tail_splits = tail.splits;
+        a.tail_k_slice = tail.k_slice;
+        a.tail_ws = tail_ws;
+        a.tail_cnt = tail_cnt;
+      }
       path = splits > 1 ? GEMM_PATH_TC_SPLITK : GEMM_PATH_TC;
       e = launch_hgemm(a, ctx);
       if (e == cudaSuccess && splits > 1)
@@ -238,6 +316,7 @@ int run_gemm(int transA, int transB, int64_t M64, int64_t N64, int64_t K64, int 
     }
   }
   g_total_launches += ctx.launches;
+  tl_last_grid = ctx.grid;
   if (e != cudaSuccess) {
     tl_last_path = GEMM_PATH_NONE;
     tl_last_launches = ctx.launches;
@@ -347,6 +426,7 @@ int gemm_version(void) { return (1 << 16) | 0; }
 
 int gemm_last_path(void) { return tl_last_path; }
 int gemm_last_launches(void) { return tl_last_launches; }
+int gemm_last_grid(void) { return tl_last_grid; }
 int64_t gemm_total_launches(void) { return g_total_launches.load(); }
 
 void gemm_set_wait_timeout_ns(int64_t ns) {
@@ -453,7 +533,7 @@ extern "C" int gemm_splitk_noalloc(int transA, int transB, int64_t M, int64_t N,
       return GEMM_ERR_UNSUPPORTED;  // partial sums would not fit the fixed array
     HgemmArgs a{transA, transB, Mi, Ni, Ki, (const __half*)A, lda, (const __half*)B, ldb,
                 (__half*)C, ldc, alpha, beta, splits, k_slice, splits > 1 ? scratch : nullptr,
-                sms, bn, pair_enabled(), g_fault_injection.load()};
+                sms, bn, pair_enabled(), c_tma_enabled(), g_fault_injection.load()};
     path = splits > 1 ? GEMM_PATH_TC_SPLITK : GEMM_PATH_TC;
     e = launch_hgemm(a, ctx);
     if (e == cudaSuccess && splits > 1)

@@ -38,6 +38,7 @@
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
+#include <string.h>
 
 #include "common.cuh"
 #include "internal.h"
@@ -64,7 +65,10 @@ struct Cfg {
   static constexpr int STAGES = STAGES_RAW > 8 ? 8 : STAGES_RAW;
   // two accumulator buffers of BN fp32 columns, rounded up to a power of two
   static constexpr int TMEM_COLS = 2 * BN <= 64 ? 64 : 2 * BN <= 128 ? 128 : 2 * BN <= 256 ? 256 : 512;
-  static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 /*align*/ + 256 /*barriers*/;
+  // + 4 epilogue warps x 2 buffers x (32 x 32 fp16) staging for TMA stores of C
+  static constexpr int STAGING_BYTES = 4 * 2 * 2048;
+  static constexpr int SMEM_BYTES =
+      STAGES * STAGE_BYTES + STAGING_BYTES + 1024 /*align*/ + 256 /*barriers*/;
 };
 
 struct HParams {
@@ -79,7 +83,15 @@ struct HParams {
   uint64_t timeout_ns;
   int fault_injection;
   int c_vec_ok;  // C base 16-byte aligned and ldc % 8 == 0
+  int c_tma;     // beta == 0 and C aligned: C leaves through TMA stores
   int pair;      // 1: clusters of two blocks share each B tile (TMA multicast)
+  // Tail split (only when splits == 1): units [0, dp_units) are whole tiles;
+  // the remaining tiles are cut into tail_splits K slices of tail_k_slice, each
+  // writing fp32 partials to tail_ws; per 32-row strip the last slice to
+  // arrive (tail_cnt) sums all slices in slice order and runs the epilogue.
+  int dp_units, tail_splits, tail_k_slice;
+  float* tail_ws;          // [tail tiles][pair ? 2 : 1][tail_splits][4 warps][32 x BN]
+  unsigned int* tail_cnt;  // [tail tiles][pair ? 2 : 1][4], zero on entry and on exit
 };
 
 // tcgen05 shared-memory matrix descriptor, 128-byte swizzle:
@@ -106,33 +118,96 @@ __device__ __forceinline__ constexpr uint32_t make_idesc() {
          ((uint32_t)(BN >> 3) << 17) | ((uint32_t)(BM >> 4) << 24);
 }
 
-// Work unit u -> tile.  Without pairs a unit is one 128 x BN tile; with pairs
-// (a cluster of two blocks sharing B) a unit is two vertically adjacent tiles,
-// and block `rank` of the pair takes tile row 2 * pair_row + rank.
+// Work unit u -> tile, K range, slice.  Without pairs a tile is 128 x BN;
+// with pairs (a cluster of two blocks sharing B) a unit covers two vertically
+// adjacent tiles and block `rank` of the pair takes tile row 2 * pair_row + rank.
+//  * split-K launches: unit = slice z of tile t, u = z * tiles + t;
+//  * tail split: units below dp_units are whole tiles; unit dp_units + v is
+//    slice v / tail_tiles of tail tile v % tail_tiles (`tail` >= 0);
+//  * otherwise: unit = whole tile.
 template <bool PAIR>
-__device__ __forceinline__ void unit_coords(int u, const HParams& p, int rank, int& m0, int& n0,
-                                            int& kbeg, int& nkb) {
+__device__ __forceinline__ void unit_coords(int u, const HParams& p, int rank, int& m0, int& tn,
+                                            int& kbeg, int& nkb, int& z, int& tail) {
   const int rows = PAIR ? (p.tiles_m + 1) / 2 : p.tiles_m;
   const int tiles = rows * p.tiles_n;
-  const int z = u / tiles;
-  const int t = u - z * tiles;
+  int t, ks;
+  tail = -1;
+  if (p.tail_splits > 0 && u >= p.dp_units) {
+    const int tail_tiles = tiles - p.dp_units;
+    const int v = u - p.dp_units;
+    tail = v % tail_tiles;
+    z = v / tail_tiles;
+    t = p.dp_units + tail;
+    ks = p.tail_k_slice;
+  } else {
+    z = u / tiles;
+    t = u - z * tiles;
+    ks = p.k_slice;
+  }
   const int per_group = GROUP_M * p.tiles_n;
   const int first_m = (t / per_group) * GROUP_M;
   const int gsize = min(rows - first_m, GROUP_M);
   const int tr = first_m + (t % per_group) % gsize;
-  const int tn = (t % per_group) / gsize;
+  tn = (t % per_group) / gsize;
   const int tm = PAIR ? 2 * tr + rank : tr;
   m0 = tm * BM;
-  kbeg = z * p.k_slice;
-  const int kend = min(p.K, kbeg + p.k_slice);
+  kbeg = z * ks;
+  const int kend = min(p.K, kbeg + ks);
   nkb = (kend - kbeg + BK - 1) / BK;
-  n0 = tn;  // scaled by BN by the caller
+}
+
+__device__ __forceinline__ int total_units(const HParams& p, bool pair) {
+  const int tiles = (pair ? (p.tiles_m + 1) / 2 : p.tiles_m) * p.tiles_n;
+  if (p.tail_splits > 0) return p.dp_units + (tiles - p.dp_units) * p.tail_splits;
+  return tiles * p.splits;
+}
+
+// alpha * v + beta * C_old -> fp16 (RN-even) -> C, for 32 columns of one row
+__device__ __forceinline__ void store_c32(const HParams& p, int gm, int gn0, float (&v)[32]) {
+  __half* dst = p.C + (int64_t)gm * p.ldc + gn0;
+#pragma unroll
+  for (int j = 0; j < 32; ++j) v[j] = p.alpha * v[j];
+  const bool full = (gn0 + 31 < p.N) && p.c_vec_ok;
+  if (full) {
+    if (p.beta != 0.f) {
+#pragma unroll
+      for (int w = 0; w < 4; ++w) {
+        const uint4 cv = reinterpret_cast<const uint4*>(dst)[w];
+        const __half2* ch = reinterpret_cast<const __half2*>(&cv);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float2 f = __half22float2(ch[e]);
+          v[8 * w + 2 * e] = __fmaf_rn(p.beta, f.x, v[8 * w + 2 * e]);
+          v[8 * w + 2 * e + 1] = __fmaf_rn(p.beta, f.y, v[8 * w + 2 * e + 1]);
+        }
+      }
+    }
+#pragma unroll
+    for (int w = 0; w < 4; ++w) {
+      uint4 o;
+      __half2* oh = reinterpret_cast<__half2*>(&o);
+#pragma unroll
+      for (int e = 0; e < 4; ++e)
+        oh[e] = __halves2half2(__float2half_rn(v[8 * w + 2 * e]),
+                               __float2half_rn(v[8 * w + 2 * e + 1]));
+      reinterpret_cast<uint4*>(dst)[w] = o;
+    }
+  } else {
+    for (int j = 0; j < 32; ++j) {
+      if (gn0 + j < p.N) {
+        float o = v[j];
+        if (p.beta != 0.f) o = __fmaf_rn(p.beta, __half2float(dst[j]), o);
+        dst[j] = __float2half_rn(o);
+      }
+    }
+  }
 }
 
 template <int BN, bool A_MN, bool B_MN, bool SPLIT, bool PAIR>
 __global__ void __launch_bounds__(THREADS, 1)
     hgemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
-                    const __grid_constant__ CUtensorMap tmB, const HParams p) {
+                    const __grid_constant__ CUtensorMap tmB,
+                    const __grid_constant__ CUtensorMap tmC, const HParams p) {
   using C_ = Cfg<BN, B_MN>;
   constexpr int STAGES = C_::STAGES;
   constexpr uint32_t STAGE_TX = (uint32_t)C_::STAGE_BYTES;
@@ -147,7 +222,10 @@ __global__ void __launch_bounds__(THREADS, 1)
   const uint32_t raw_addr = smem_u32(smem_raw);
   const uint32_t tiles_addr = (raw_addr + 1023u) & ~1023u;  // swizzle atoms need 1 KiB alignment
   uint8_t* const tiles_ptr = smem_raw + (tiles_addr - raw_addr);
-  uint64_t* const bars = reinterpret_cast<uint64_t*>(tiles_ptr + STAGES * C_::STAGE_BYTES);
+  // C staging (1 KiB aligned: the 64-byte swizzle pattern repeats every 512 B)
+  const uint32_t staging_addr = tiles_addr + (uint32_t)(STAGES * C_::STAGE_BYTES);
+  uint8_t* const staging_ptr = tiles_ptr + STAGES * C_::STAGE_BYTES;
+  uint64_t* const bars = reinterpret_cast<uint64_t*>(staging_ptr + C_::STAGING_BYTES);
   // barrier layout: full[STAGES], empty[STAGES], acc_full[2], acc_empty[2], drain
   const uint32_t bar0 = smem_u32(bars);
   auto full_bar = [&](int s) { return bar0 + 8u * (uint32_t)s; };
@@ -185,7 +263,7 @@ __global__ void __launch_bounds__(THREADS, 1)
   const uint32_t tmem_base = *tmem_slot;
 
   const WaitCtl wc{p.status, abort_flag, p.timeout_ns};
-  const int total_units = (PAIR ? (p.tiles_m + 1) / 2 : p.tiles_m) * p.tiles_n * p.splits;
+  const int n_units = total_units(p, PAIR);
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
@@ -197,9 +275,9 @@ __global__ void __launch_bounds__(THREADS, 1)
       uint32_t pending = 0, pend_phase = 0;  // per-stage: last load issued / its parity
       bool first = true;
       bool ok = true;
-      for (int u = worker; u < total_units && ok; u += workers) {
-        int m0, tn, kbeg, nkb;
-        unit_coords<PAIR>(u, p, rank, m0, tn, kbeg, nkb);
+      for (int u = worker; u < n_units && ok; u += workers) {
+        int m0, tn, kbeg, nkb, z, tail;
+        unit_coords<PAIR>(u, p, rank, m0, tn, kbeg, nkb, z, tail);
         const int n0 = tn * BN;
         for (int kb = 0; kb < nkb; ++kb) {
           if (!mbar_wait(empty_bar(stage), phase ^ 1u, wc)) { ok = false; break; }
@@ -255,9 +333,9 @@ __global__ void __launch_bounds__(THREADS, 1)
       uint32_t phase = 0;
       int it = 0;
       bool ok = true;
-      for (int u = worker; u < total_units && ok; u += workers, ++it) {
-        int m0, tn, kbeg, nkb;
-        unit_coords<PAIR>(u, p, rank, m0, tn, kbeg, nkb);
+      for (int u = worker; u < n_units && ok; u += workers, ++it) {
+        int m0, tn, kbeg, nkb, z, tail;
+        unit_coords<PAIR>(u, p, rank, m0, tn, kbeg, nkb, z, tail);
         const int buf = it & 1;
         const uint32_t acc_phase = (uint32_t)(it >> 1) & 1u;
         if (!mbar_wait(acce_bar(buf), acc_phase ^ 1u, wc)) { ok = false; break; }
@@ -294,9 +372,9 @@ __global__ void __launch_bounds__(THREADS, 1)
     const int q = warp & 3;  // this warp may access TMEM lanes 32q .. 32q+31
     const int row = q * 32 + lane;
     int it = 0;
-    for (int u = worker; u < total_units; u += workers, ++it) {
-      int m0, tn, kbeg, nkb;
-      unit_coords<PAIR>(u, p, rank, m0, tn, kbeg, nkb);
+    for (int u = worker; u < n_units; u += workers, ++it) {
+      int m0, tn, kbeg, nkb, z, tail;
+      unit_coords<PAIR>(u, p, rank, m0, tn, kbeg, nkb, z, tail);
       const int n0 = tn * BN;
       const int buf = it & 1;
       const uint32_t acc_phase = (uint32_t)(it >> 1) & 1u;
@@ -309,7 +387,15 @@ __global__ void __launch_bounds__(THREADS, 1)
       tc_fence_after();
       const int gm = m0 + row;
       const uint32_t t_row = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(buf * BN);
-      const int z = u / ((PAIR ? (p.tiles_m + 1) / 2 : p.tiles_m) * p.tiles_n);
+      // tail slice: this warp's 32 x BN partial sums for the tile live in a
+      // block of the workspace laid out as the warp holds them -- [chunk c]
+      // [float4 v][lane] -- so every store and load of a warp covers 512
+      // contiguous bytes
+      constexpr int P = PAIR ? 2 : 1;
+      constexpr int STRIP = 32 * BN;  // floats per warp strip
+      float* const tail_strip =
+          tail >= 0 ? p.tail_ws + ((((int64_t)(tail * P + rank) * p.tail_splits + z) * 4 + q) * STRIP)
+                    : nullptr;
 #pragma unroll 1
       for (int c = 0; c < BN / 32; ++c) {
         uint32_t r[32];
@@ -320,8 +406,18 @@ __global__ void __launch_bounds__(THREADS, 1)
           tc_fence_before();
           mbar_arrive(acce_bar(buf));  // accumulator buffer may be overwritten
         }
-        if (gm >= p.M) continue;  // rows past M: loaded (warp-collective) but not stored
+        if (tail >= 0) {
+          float4* dst = reinterpret_cast<float4*>(tail_strip) + (c * 8) * 32 + lane;
+#pragma unroll
+          for (int v = 0; v < 8; ++v)
+            dst[v * 32] = make_float4(__uint_as_float(r[4 * v]), __uint_as_float(r[4 * v + 1]),
+                                      __uint_as_float(r[4 * v + 2]), __uint_as_float(r[4 * v + 3]));
+          continue;
+        }
         const int gn0 = n0 + c * 32;
+        // rows past M: loaded (warp-collective) but not stored; the TMA path
+        // stays warp-uniform and lets the unit clip them
+        if (gm >= p.M && !(p.c_tma && !SPLIT)) continue;
         if constexpr (SPLIT) {
           float* dst = p.partial + ((int64_t)z * p.M + gm) * p.N + gn0;
           if (gn0 + 31 < p.N && (p.N & 3) == 0) {
@@ -334,48 +430,79 @@ __global__ void __launch_bounds__(THREADS, 1)
             for (int j = 0; j < 32; ++j)
               if (gn0 + j < p.N) dst[j] = __uint_as_float(r[j]);
           }
+        } else if (p.c_tma) {
+          // fp16 row segment -> this warp's staging buffer (64-byte swizzle:
+          // 16-byte chunk w of row l sits at chunk w ^ ((l >> 1) & 3), so the
+          // 8 lanes of each store phase hit distinct banks) -> TMA store of the
+          // 32 x 32 block, clipped by the unit at M and N
+          const uint32_t sbuf = staging_addr + (uint32_t)((q * 2 + (c & 1)) * 2048);
+          if (lane == 0) bulk_wait_read<1>();  // this buffer's previous store has read it
+          __syncwarp();
+#pragma unroll
+          for (int w = 0; w < 4; ++w) {
+            uint4 o;
+            __half2* oh = reinterpret_cast<__half2*>(&o);
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+              oh[e] = __floats2half2_rn(p.alpha * __uint_as_float(r[8 * w + 2 * e]),
+                                        p.alpha * __uint_as_float(r[8 * w + 2 * e + 1]));
+            const uint32_t dst = sbuf + (uint32_t)(lane * 64 + ((w ^ ((lane >> 1) & 3)) * 16));
+            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(dst), "r"(o.x),
+                         "r"(o.y), "r"(o.z), "r"(o.w)
+                         : "memory");
+          }
+          fence_proxy_async_smem();
+          __syncwarp();
+          // (a block wholly past M or N -- the second tile of a pair on an odd
+          // tile-row count -- is not stored at all)
+          if (lane == 0 && m0 + q * 32 < p.M && gn0 < p.N) {
+            tma_store_2d(&tmC, gn0, m0 + q * 32, sbuf);
+            bulk_commit();
+          }
         } else {
-          __half* dst = p.C + (int64_t)gm * p.ldc + gn0;
           float v[32];
 #pragma unroll
-          for (int j = 0; j < 32; ++j) v[j] = p.alpha * __uint_as_float(r[j]);
-          const bool full = (gn0 + 31 < p.N) && p.c_vec_ok;
-          if (full) {
-            if (p.beta != 0.f) {
+          for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
+          store_c32(p, gm, gn0, v);
+        }
+      }
+      if (tail >= 0) {
+        // Last slice to arrive for this 32-row strip finishes it: partial
+        // writes are fenced before the arrival, the slices are summed in slice
+        // order (so the result does not depend on which slice came last), and
+        // the counter is left at zero for the next launch.  No waiting on
+        // other blocks is involved.
+        __threadfence();
+        unsigned int old = 0;
+        unsigned int* cnt = p.tail_cnt + (tail * P + rank) * 4 + q;
+        if (lane == 0) old = atomicAdd(cnt, 1u);
+        old = __shfl_sync(0xffffffffu, old, 0);
+        if (old == (unsigned int)(p.tail_splits - 1)) {
+          __threadfence();
+          const float* strip0 =
+              p.tail_ws + (((int64_t)(tail * P + rank) * p.tail_splits * 4 + q) * STRIP);
+          const int64_t slice_stride = 4 * (int64_t)STRIP;
+#pragma unroll 1
+          for (int c = 0; c < BN / 32; ++c) {
+            float v[32];
 #pragma unroll
-              for (int w = 0; w < 4; ++w) {
-                const uint4 cv = reinterpret_cast<const uint4*>(dst)[w];
-                const __half2* ch = reinterpret_cast<const __half2*>(&cv);
+            for (int j = 0; j < 32; ++j) v[j] = 0.f;
+            for (int zz = 0; zz < p.tail_splits; ++zz) {
+              const float4* src =
+                  reinterpret_cast<const float4*>(strip0 + zz * slice_stride) + (c * 8) * 32 + lane;
 #pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                  const float2 f = __half22float2(ch[e]);
-                  v[8 * w + 2 * e] = __fmaf_rn(p.beta, f.x, v[8 * w + 2 * e]);
-                  v[8 * w + 2 * e + 1] = __fmaf_rn(p.beta, f.y, v[8 * w + 2 * e + 1]);
-                }
+              for (int w = 0; w < 8; ++w) {
+                const float4 f = __ldcg(src + w * 32);
+                v[4 * w] += f.x; v[4 * w + 1] += f.y; v[4 * w + 2] += f.z; v[4 * w + 3] += f.w;
               }
             }
-#pragma unroll
-            for (int w = 0; w < 4; ++w) {
-              uint4 o;
-              __half2* oh = reinterpret_cast<__half2*>(&o);
-#pragma unroll
-              for (int e = 0; e < 4; ++e)
-                oh[e] = __halves2half2(__float2half_rn(v[8 * w + 2 * e]),
-                                       __float2half_rn(v[8 * w + 2 * e + 1]));
-              reinterpret_cast<uint4*>(dst)[w] = o;
-            }
-          } else {
-            for (int j = 0; j < 32; ++j) {
-              if (gn0 + j < p.N) {
-                float o = v[j];
-                if (p.beta != 0.f) o = __fmaf_rn(p.beta, __half2float(dst[j]), o);
-                dst[j] = __float2half_rn(o);
-              }
-            }
+            if (gm < p.M) store_c32(p, gm, n0 + c * 32, v);
           }
+          if (lane == 0) atomicExch(cnt, 0u);
         }
       }
     }
+    if (lane == 0) bulk_wait_all();  // C stores complete before the block ends
   }
 
   tc_fence_before();
@@ -410,7 +537,8 @@ PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
 // `ld` elements; box = box_cols (inner) x box_rows, 128-byte swizzle,
 // out-of-range elements read as zero.
 bool make_map(CUtensorMap* map, const void* base, int64_t rows, int64_t cols, int64_t ld,
-              int box_cols, int box_rows) {
+              int box_cols, int box_rows,
+              CUtensorMapSwizzle swizzle = CU_TENSOR_MAP_SWIZZLE_128B) {
   auto enc = get_encode();
   if (!enc) return false;
   cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
@@ -419,9 +547,45 @@ bool make_map(CUtensorMap* map, const void* base, int64_t rows, int64_t cols, in
   cuuint32_t estr[2] = {1, 1};
   CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void*>(base), dims,
                    strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                   CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
+}
+
+// How many two-block clusters of the pair kernel can be resident at once
+// (fewer than SMs / 2 when the SMs of a GPC do not all pair up).  Queried once
+// per kernel configuration.
+template <int BN, bool A_MN, bool B_MN>
+int pair_slots(int num_sms) {
+  static int n = 0;
+  if (n == 0) {
+    using C_ = Cfg<BN, B_MN>;
+    auto kern = hgemm_tc_kernel<BN, A_MN, B_MN, false, true>;
+    int q = 0;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             C_::SMEM_BYTES) == cudaSuccess) {
+      cudaLaunchConfig_t cfg = {};
+      cudaLaunchAttribute attr[1];
+      attr[0].id = cudaLaunchAttributeClusterDimension;
+      attr[0].val.clusterDim.x = 2;
+      attr[0].val.clusterDim.y = 1;
+      attr[0].val.clusterDim.z = 1;
+      cfg.gridDim = dim3(2 * (num_sms / 2));
+      cfg.blockDim = dim3(THREADS);
+      cfg.dynamicSmemBytes = C_::SMEM_BYTES;
+      cfg.attrs = attr;
+      cfg.numAttrs = 1;
+      if (cudaOccupancyMaxActiveClusters(&q, kern, &cfg) != cudaSuccess) q = 0;
+    }
+    n = q > 0 ? q : num_sms / 2;
+  }
+  return n;
+}
+
+int host_total_units(const HParams& p, bool pair) {
+  const int tiles = (pair ? (p.tiles_m + 1) / 2 : p.tiles_m) * p.tiles_n;
+  if (p.tail_splits > 0) return p.dp_units + (tiles - p.dp_units) * p.tail_splits;
+  return tiles * p.splits;
 }
 
 template <int BN, bool A_MN, bool B_MN, bool SPLIT, bool PAIR>
@@ -435,13 +599,18 @@ cudaError_t launch_cfg(const HgemmArgs& a, const HParams& p, LaunchCtx& ctx) {
   if (B_MN) ok = make_map(&mB, a.B, a.K, a.N, a.ldb, 64, 64);     // stored [K, N]
   else ok = make_map(&mB, a.B, a.N, a.K, a.ldb, 64, PAIR ? BN / 2 : BN);  // stored [N, K]
   if (!ok) return cudaErrorInvalidValue;
+  // C: row-major [M, N], 32 x 32 boxes, 64-byte swizzle (used only when p.c_tma)
+  CUtensorMap mC;
+  memset(&mC, 0, sizeof(mC));
+  if (p.c_tma && !make_map(&mC, a.C, a.M, a.N, a.ldc, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B))
+    return cudaErrorInvalidValue;
   auto kern = hgemm_tc_kernel<BN, A_MN, B_MN, SPLIT, PAIR>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        C_::SMEM_BYTES);
   if (e != cudaSuccess) return e;
   if constexpr (PAIR) {
     // persistent grid of as many pairs as can be resident at once
-    static int max_pairs = 0;  // per process: one GB300 model on the box
+    const int max_pairs = pair_slots<BN, A_MN, B_MN>(a.num_sms);
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -453,20 +622,16 @@ cudaError_t launch_cfg(const HgemmArgs& a, const HParams& p, LaunchCtx& ctx) {
     cfg.stream = ctx.stream;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    if (max_pairs == 0) {
-      cfg.gridDim = dim3(2 * (a.num_sms / 2));
-      int n = 0;
-      if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess || n <= 0) n = a.num_sms / 2;
-      max_pairs = n;
-    }
-    const int units = ((p.tiles_m + 1) / 2) * p.tiles_n * p.splits;
+    const int units = host_total_units(p, true);
     const int pairs = units < max_pairs ? units : max_pairs;
     cfg.gridDim = dim3(2 * pairs);
-    e = cudaLaunchKernelEx(&cfg, kern, mA, mB, p);
+    ctx.grid = 2 * pairs;
+    e = cudaLaunchKernelEx(&cfg, kern, mA, mB, mC, p);
   } else {
-    const int units = p.tiles_m * p.tiles_n * p.splits;
+    const int units = host_total_units(p, false);
     const int grid = units < a.num_sms ? units : a.num_sms;
-    kern<<<grid, THREADS, C_::SMEM_BYTES, ctx.stream>>>(mA, mB, p);
+    ctx.grid = grid;
+    kern<<<grid, THREADS, C_::SMEM_BYTES, ctx.stream>>>(mA, mB, mC, p);
     e = cudaGetLastError();
   }
   if (e == cudaSuccess) ctx.launches++;
@@ -492,6 +657,50 @@ cudaError_t launch_bn(const HgemmArgs& a, const HParams& p, LaunchCtx& ctx) {
 }
 
 }  // namespace
+
+int hgemm_pair_slots(int bn, int transA, int transB, int num_sms) {
+  const bool A_MN = transA != 0, B_MN = transB == 0;
+#define GB300_SLOTS(W, AM, BMN) \
+  if (bn == W && A_MN == AM && B_MN == BMN) return pair_slots<W, AM, BMN>(num_sms);
+  GB300_SLOTS(128, false, true) GB300_SLOTS(128, true, true) GB300_SLOTS(128, false, false)
+  GB300_SLOTS(128, true, false) GB300_SLOTS(256, false, true) GB300_SLOTS(256, true, true)
+  GB300_SLOTS(256, false, false) GB300_SLOTS(256, true, false)
+#undef GB300_SLOTS
+  return num_sms / 2;
+}
+
+// Pairs of blocks share B tiles when the tile is 128 or 256 wide, there are at
+// least two tile rows, and K is not split (the split-K path keeps single
+// blocks).
+bool hgemm_use_pair(int bn, int M, int splits, int allowed) {
+  return allowed && (bn == 128 || bn == 256) && (M + BM - 1) / BM >= 2 && splits == 1;
+}
+
+// Tail split for the persistent grid (no split-K): with `workers` blocks (or
+// pairs) taking units round-robin, the last round holds units % workers tiles.
+// When that is at most half the workers, those tiles are cut into K slices so
+// that the last round spreads over all workers.
+TailPlan hgemm_plan_tail(int M, int N, int K, int bn, bool pair, int workers) {
+  TailPlan t{0, 0, 0, 0, 0};
+  const int tiles_m = (M + BM - 1) / BM, tiles_n = (N + bn - 1) / bn;
+  const int units = (pair ? (tiles_m + 1) / 2 : tiles_m) * tiles_n;
+  const int full = units / workers, rem = units % workers;
+  const int nkb = (K + BK - 1) / BK;
+  if (workers <= 0 || full == 0 || rem == 0 || rem * 2 > workers || nkb < 8) return t;
+  int sp = workers / rem;
+  if (sp > nkb / 4) sp = nkb / 4;
+  if (sp > 8) sp = 8;
+  if (sp < 2) return t;
+  const int per = (nkb + sp - 1) / sp;
+  t.splits = (nkb + per - 1) / per;
+  if (t.splits < 2) { t.splits = 0; return t; }
+  t.k_slice = per * BK;
+  t.dp_units = full * workers;
+  const int halves = pair ? 2 : 1;
+  t.ws_bytes = (size_t)rem * halves * t.splits * BM * bn * sizeof(float);
+  t.cnt_bytes = (size_t)rem * halves * 4 * sizeof(unsigned int);
+  return t;
+}
 
 int hgemm_pick_bn(int M, int N, int transB, int num_sms) {
   // An MN-major B (transB == 0) is staged in 64-column swizzle atoms, so its
@@ -534,9 +743,14 @@ cudaError_t launch_hgemm(const HgemmArgs& a, LaunchCtx& ctx) {
   p.timeout_ns = ctx.timeout_ns;
   p.fault_injection = a.fault_injection;
   p.c_vec_ok = ((reinterpret_cast<uintptr_t>(a.C) & 15u) == 0 && (a.ldc % 8) == 0) ? 1 : 0;
-  // pairs of blocks share B tiles when there are at least two tile rows and no
-  // K split (the split-K path keeps single blocks)
-  p.pair = (a.pair && (bn == 128 || bn == 256) && p.tiles_m >= 2 && p.splits == 1) ? 1 : 0;
+  p.c_tma = (p.c_vec_ok && a.beta == 0.f && a.splits <= 1 && a.c_tma) ? 1 : 0;
+  p.pair = hgemm_use_pair(bn, a.M, p.splits, a.pair) ? 1 : 0;
+  p.dp_units = a.dp_units;
+  p.tail_splits = a.tail_splits;
+  p.tail_k_slice = a.tail_k_slice;
+  p.tail_ws = a.tail_ws;
+  p.tail_cnt = a.tail_cnt;
+  if (p.tail_splits > 0 && (p.splits != 1 || !p.tail_ws || !p.tail_cnt)) return cudaErrorInvalidValue;
   switch (bn) {
     case 32: return launch_bn<32>(a, p, ctx);
     case 64: return launch_bn<64>(a, p, ctx);

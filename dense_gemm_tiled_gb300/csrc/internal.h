@@ -42,7 +42,17 @@ struct HgemmArgs {
   int num_sms;
   int bn;               // tile width: 32, 64, 128, 192 or 256
   int pair;             // allow clusters of two blocks sharing B tiles
+  int c_tma;            // allow TMA stores of C (used when beta == 0 and C is aligned)
   int fault_injection;  // test hook: 1 = producer skips its first stage
+  // tail split (see hgemm_plan_tail); tail_splits == 0 disables it
+  int dp_units = 0, tail_splits = 0, tail_k_slice = 0;
+  float* tail_ws = nullptr;
+  unsigned int* tail_cnt = nullptr;
+};
+
+struct TailPlan {
+  int dp_units, splits, k_slice;
+  size_t ws_bytes, cnt_bytes;
 };
 
 struct LaunchCtx {
@@ -50,6 +60,7 @@ struct LaunchCtx {
   unsigned int* status;  // device status word
   uint64_t timeout_ns;
   int launches;          // incremented per kernel launched
+  int grid = 0;          // blocks of the last main GEMM kernel launched
 };
 
 // Launchers (return cudaSuccess or the launch error).
@@ -74,5 +85,8 @@ constexpr int SG_WARPS_M = GB300_SG_WARPS_M;
 constexpr int SG_BM = 64 * SG_WARPS_M, SG_BN = 128, SG_BK = 32;
 constexpr int HG_BM = 128, HG_BK = 64;
 int hgemm_pick_bn(int M, int N, int transB, int num_sms);
+bool hgemm_use_pair(int bn, int M, int splits, int allowed);
+int hgemm_pair_slots(int bn, int transA, int transB, int num_sms);
+TailPlan hgemm_plan_tail(int M, int N, int K, int bn, bool pair, int workers);
 
 }  // namespace gb300

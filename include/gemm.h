@@ -40,8 +40,9 @@
  *   - Calls are asynchronous on `stream` (0 = the legacy default stream) and
  *     may be made from several host threads.  Scratch space the library needs
  *     (split-K partial sums; zero-padded copies of operands whose rows are not
- *     16-byte aligned) comes from the stream-ordered allocator on `stream` and
- *     is released on the same stream.
+ *     16-byte aligned) is taken in stream order on `stream` from a memory pool
+ *     the library creates once per device, and released on the same stream;
+ *     the pool keeps released memory for reuse until the process exits.
  *   - Argument errors are returned synchronously, before anything is
  *     launched.  Launch failures return GEMM_ERR_CUDA.  A kernel whose
  *     internal wait exceeds its time limit records the fact in a per-device
@@ -162,6 +163,9 @@ typedef enum {
 int gemm_last_path(void);
 int gemm_last_launches(void);
 int64_t gemm_total_launches(void);
+/* Blocks in the grid of the last main GEMM kernel gemm() launched on this
+ * thread (the persistent fp16 kernel sizes its grid to the resident blocks). */
+int gemm_last_grid(void);
 
 /*
  * Test hook: the time limit, in nanoseconds, of every bounded wait inside the

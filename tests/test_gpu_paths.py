@@ -1,10 +1,12 @@
 """Every fp16 kernel configuration against the oracle.
 
-The dispatcher picks one tile width (64/128/192/256 columns) and, for 128 and
-256, pairs of blocks sharing B tiles by multicast.  Each configuration is
+The dispatcher picks one tile width (64/128/192/256 columns), for 128 and 256
+pairs of blocks sharing B tiles by multicast, and a K split of the persistent
+grid's last round when it would run under half full.  Each configuration is
 forced here in its own process (the switches are read once per process from
-GEMM_GB300_HG_PAIR and GEMM_GB300_HG_BN) and checked on ragged, multi-tile
-problems in all four variants, exact on small-integer inputs.
+GEMM_GB300_HG_PAIR, GEMM_GB300_HG_BN and GEMM_GB300_HG_TAIL) and checked on
+ragged, multi-tile problems in all four variants, exact on small-integer
+inputs.
 """
 import os
 import subprocess
@@ -30,14 +32,20 @@ for v in ("nn", "tn", "nt", "tt"):
     check_problem(p)
     p = inputs.make_problem(1024, 768, 1000, tA, tB, "f16", "uniform", seed=602)
     check_problem(p)
+    # 2048 x 3072 with 256-wide tiles: 96 pair units (192 single tiles) over
+    # 76 pairs (152 blocks) leaves a last round under half full, which the
+    # tail split cuts into K slices
+    p = inputs.make_problem(2048, 3072, 512, tA, tB, "f16", "uniform", seed=603, beta=0.5)
+    check_problem(p)
 print("ok")
 """
 
 
-@pytest.mark.parametrize("pair,bn", [("1", "256"), ("0", "256"), ("1", "128"), ("0", "128"),
-                                     ("0", "192"), ("0", "64")])
-def test_forced_kernel_configuration(lib_path, gpu, pair, bn):
-    env = dict(os.environ, GEMM_GB300_HG_PAIR=pair, GEMM_GB300_HG_BN=bn)
+@pytest.mark.parametrize("pair,bn,tail", [("1", "256", "1"), ("0", "256", "1"), ("1", "256", "0"),
+                                          ("1", "128", "1"), ("0", "128", "1"), ("0", "192", "1"),
+                                          ("0", "64", "1")])
+def test_forced_kernel_configuration(lib_path, gpu, pair, bn, tail):
+    env = dict(os.environ, GEMM_GB300_HG_PAIR=pair, GEMM_GB300_HG_BN=bn, GEMM_GB300_HG_TAIL=tail)
     code = SCRIPT.format(root=ROOT, tests=os.path.join(ROOT, "tests"))
     r = subprocess.run([sys.executable, "-c", code], env=env, capture_output=True, text=True,
                        timeout=900)
