@@ -381,12 +381,18 @@ def main():
                 "frac_at_median_clock": (achieved / (sms * FP32_LANES_PER_SM * 2 *
                                                      clocks["sm_mhz"] * 1e6 / 1e12)
                                          if clocks.get("sm_mhz") else None)}
+    # DRAM bytes per launch of this kernel from the committed ncu capture
     tpath = os.path.join(ROOT, "profiles", "traffic.json")
+    traffic = {}
     if os.path.exists(tpath):
         try:
-            roofline["traffic"] = json.load(open(tpath)).get("sgemm_f32_nn_4096")
+            traffic = json.load(open(tpath))
         except Exception:
-            pass
+            traffic = {}
+    if "sgemm_f32_nn_4096" in traffic:
+        roofline["traffic"] = traffic["sgemm_f32_nn_4096"]["bytes"]
+        roofline["traffic_unit"] = "bytes per launch (ncu dram read + write)"
+        roofline["algorithmic_bytes"] = 4 * (M * K + K * N + M * N)
 
     # fp16 variants, per-launch timing, L2 flushed before each launch
     fp16 = None
@@ -416,6 +422,7 @@ def main():
             med = statistics.median(ts)
             ach = flops / (med * 1e-3) / 1e12
             fp16[var] = {"tflops": ach, "ms_median": med, "ms_min": min(ts), "path": hpath,
+                         "traffic": (traffic.get(f"hgemm_f16_{var}_4096") or {}).get("bytes"),
                          "roofline": {"bound": "tensor", "achieved": ach,
                                       "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
                                       "frac": ach / peaks["bf16_tflops"],

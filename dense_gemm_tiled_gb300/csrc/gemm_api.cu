@@ -104,8 +104,8 @@ int check_args(int transA, int transB, int64_t M, int64_t N, int64_t K, int dtyp
   return GEMM_OK;
 }
 
-// Debug/bench switch for the fp16 block pairs (env GEMM_GB300_HG_PAIR=0 turns
-// them off).
+// fp16 block pairs (env GEMM_GB300_HG_PAIR): 0 off, 1 pairs sharing B tiles by
+// TMA multicast, 2 pairs running 2-SM (cta_group::2) MMAs.
 int pair_enabled() {
   static const int v = [] {
     const char* e = getenv("GEMM_GB300_HG_PAIR");
@@ -272,7 +272,7 @@ int run_gemm(int transA, int transB, int64_t M64, int64_t N64, int64_t K64, int 
     TailPlan tail{0, 0, 0, 0, 0};
     if (splits == 1 && tail_enabled())
       tail = hgemm_plan_tail(M, N, K, bn, use_pair,
-                             use_pair ? hgemm_pair_slots(bn, transA, transB, sms) : sms);
+                             use_pair ? hgemm_pair_slots(bn, transA, transB, pair, sms) : sms);
     const size_t bytes_t = tail.splits > 0 ? (tail.ws_bytes + 255) / 256 * 256 + tail.cnt_bytes : 0;
     Scratch ws;
     if (bytes_a + bytes_b + bytes_p + bytes_t > 0) {

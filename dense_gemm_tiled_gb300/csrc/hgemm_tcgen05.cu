@@ -54,12 +54,16 @@ constexpr int GROUP_M = 8;
 constexpr int A_TILE_BYTES = BM * BK * 2;  // 16 KiB
 constexpr int SMEM_BUDGET = 200 * 1024;
 
-template <int BN, bool B_MN>
+// MODE: 0 = single blocks; 1 = pairs of blocks sharing each B tile by TMA
+// multicast (each block still holds the whole B tile); 2 = pairs running
+// 256-row MMAs across both SMs (tcgen05 cta_group::2): each block holds its
+// 128 rows of A and half of the B tile.
+template <int BN, bool B_MN, int MODE = 0>
 struct Cfg {
   // An MN-major B tile is stored as 64-wide swizzle atoms, so it is at least
   // one atom wide; the MMA reads only the first BN columns.
   static constexpr int B_COLS = B_MN ? (BN < 64 ? 64 : BN) : BN;
-  static constexpr int B_TILE_BYTES = B_COLS * BK * 2;
+  static constexpr int B_TILE_BYTES = (MODE == 2 ? B_COLS / 2 : B_COLS) * BK * 2;
   static constexpr int STAGE_BYTES = A_TILE_BYTES + B_TILE_BYTES;
   static constexpr int STAGES_RAW = SMEM_BUDGET / STAGE_BYTES;
   static constexpr int STAGES = STAGES_RAW > 8 ? 8 : STAGES_RAW;
@@ -112,10 +116,10 @@ __device__ __forceinline__ uint64_t make_sdesc(uint32_t saddr, uint32_t lbo, uin
 // Instruction descriptor, kind::f16: D fp32 (bits 4-5 = 1), A and B fp16
 // (bits 7-9, 10-12 = 0), A major (bit 15), B major (bit 16; 1 = MN-major),
 // N >> 3 (bits 17-22), M >> 4 (bits 24-28).
-template <int BN, bool A_MN, bool B_MN>
+template <int BN, bool A_MN, bool B_MN, int M_ROWS = BM>
 __device__ __forceinline__ constexpr uint32_t make_idesc() {
   return (1u << 4) | ((A_MN ? 1u : 0u) << 15) | ((B_MN ? 1u : 0u) << 16) |
-         ((uint32_t)(BN >> 3) << 17) | ((uint32_t)(BM >> 4) << 24);
+         ((uint32_t)(BN >> 3) << 17) | ((uint32_t)(M_ROWS >> 4) << 24);
 }
 
 // Work unit u -> tile, K range, slice.  Without pairs a tile is 128 x BN;
@@ -203,17 +207,23 @@ __device__ __forceinline__ void store_c32(const HParams& p, int gm, int gn0, flo
   }
 }
 
-template <int BN, bool A_MN, bool B_MN, bool SPLIT, bool PAIR>
+template <int BN, bool A_MN, bool B_MN, bool SPLIT, int MODE>
 __global__ void __launch_bounds__(THREADS, 1)
     hgemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
                     const __grid_constant__ CUtensorMap tmB,
                     const __grid_constant__ CUtensorMap tmC, const HParams p) {
-  using C_ = Cfg<BN, B_MN>;
+  constexpr bool PAIR = MODE != 0;
+  constexpr bool TWO_SM = MODE == 2;
+  using C_ = Cfg<BN, B_MN, MODE>;
   constexpr int STAGES = C_::STAGES;
-  constexpr uint32_t STAGE_TX = (uint32_t)C_::STAGE_BYTES;
-  // Pairs: each block of the cluster loads half of the B tile and multicasts
-  // it to both, so a stage is only free again once both blocks' MMAs have
-  // read it (two arrivals on `empty`).
+  // bytes that complete one stage: this block's (single, multicast pair), or
+  // both blocks' (2-SM pair: all loads of the pair complete on the even
+  // block's barrier)
+  constexpr uint32_t STAGE_TX = (uint32_t)C_::STAGE_BYTES * (TWO_SM ? 2u : 1u);
+  // Multicast pairs: each block of the cluster loads half of the B tile and
+  // multicasts it to both, so a stage is only free again once both blocks'
+  // MMAs have read it (two arrivals on `empty`).  2-SM pairs: the even block
+  // issues every MMA and its commits arrive on both blocks' barriers.
   const int rank = PAIR ? (int)cluster_ctarank() : 0;
   const int worker = PAIR ? (int)(blockIdx.x >> 1) : (int)blockIdx.x;
   const int workers = PAIR ? (int)(gridDim.x >> 1) : (int)gridDim.x;
@@ -242,19 +252,26 @@ __global__ void __launch_bounds__(THREADS, 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(full_bar(s), 1);
-      mbar_init(empty_bar(s), PAIR ? 2 : 1);
+      mbar_init(empty_bar(s), MODE == 1 ? 2 : 1);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(accf_bar(b), 1);
-      mbar_init(acce_bar(b), 128);
+      // 2-SM pairs: both blocks' epilogues release the accumulator to the
+      // even block's MMA issuer
+      mbar_init(acce_bar(b), TWO_SM ? 256 : 128);
     }
     mbar_init(drain_bar, 1);
     *abort_flag = 0u;
     fence_mbar_init();
   }
   if (warp == 1) {
-    tmem_alloc(smem_u32(tmem_slot), (uint32_t)C_::TMEM_COLS);
-    tmem_relinquish();
+    if constexpr (TWO_SM) {
+      tmem_alloc_pair(smem_u32(tmem_slot), (uint32_t)C_::TMEM_COLS);
+      tmem_relinquish_pair();
+    } else {
+      tmem_alloc(smem_u32(tmem_slot), (uint32_t)C_::TMEM_COLS);
+      tmem_relinquish();
+    }
   }
   tc_fence_before();
   if constexpr (PAIR) cluster_sync();  // the peer's barriers exist before any multicast
@@ -284,7 +301,32 @@ __global__ void __launch_bounds__(THREADS, 1)
           const int k0 = kbeg + kb * BK;
           const bool skip = first && p.fault_injection == 1;
           first = false;
-          if (!skip) {
+          if (!skip && TWO_SM) {
+            // this block's 128 rows of A and half of B, into its own shared
+            // memory, completing on the even block's `full` barrier
+            const uint32_t sa = tiles_addr + (uint32_t)(stage * C_::STAGE_BYTES);
+            const uint32_t sb = sa + (uint32_t)A_TILE_BYTES;
+            const uint32_t fb = mapa_shared(full_bar(stage), 0u);
+            if (rank == 0) mbar_arrive_expect_tx(full_bar(stage), STAGE_TX);
+            if constexpr (A_MN) {
+              tma_load_2d_pair(sa, &tmA, m0, k0, fb);
+              tma_load_2d_pair(sa + 8192u, &tmA, m0 + 64, k0, fb);
+            } else {
+              tma_load_2d_pair(sa, &tmA, k0, m0, fb);
+            }
+            if constexpr (B_MN) {
+              constexpr int MINE = (C_::B_COLS / 64) / 2;
+#pragma unroll
+              for (int h = 0; h < MINE; ++h)
+                tma_load_2d_pair(sb + (uint32_t)h * 8192u, &tmB, n0 + 64 * (rank * MINE + h), k0, fb);
+            } else {
+              tma_load_2d_pair(sb, &tmB, k0, n0 + rank * (BN / 2), fb);
+            }
+            if (rank == 0) {
+              pending |= 1u << stage;
+              pend_phase = (pend_phase & ~(1u << stage)) | (phase << stage);
+            }
+          } else if (!skip) {
             const uint32_t sa = tiles_addr + (uint32_t)(stage * C_::STAGE_BYTES);
             const uint32_t sb = sa + (uint32_t)A_TILE_BYTES;
             mbar_arrive_expect_tx(full_bar(stage), STAGE_TX);
@@ -294,7 +336,7 @@ __global__ void __launch_bounds__(THREADS, 1)
             } else {
               tma_load_2d(sa, &tmA, k0, m0, full_bar(stage));
             }
-            if constexpr (PAIR) {
+            if constexpr (MODE == 1) {
               // this block's half of B, written into both blocks of the pair
               if constexpr (B_MN) {
                 constexpr int ATOMS = C_::B_COLS / 64, MINE = ATOMS / 2;
@@ -327,8 +369,9 @@ __global__ void __launch_bounds__(THREADS, 1)
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
-      constexpr uint32_t idesc = make_idesc<BN, A_MN, B_MN>();
+    // 2-SM pairs: only the even block issues MMAs
+    if (lane == 0 && (!TWO_SM || rank == 0)) {
+      constexpr uint32_t idesc = make_idesc<BN, A_MN, B_MN, TWO_SM ? 2 * BM : BM>();
       int stage = 0;
       uint32_t phase = 0;
       int it = 0;
@@ -353,18 +396,23 @@ __global__ void __launch_bounds__(THREADS, 1)
             else ad = make_sdesc(sa + (uint32_t)kk * 32u, 16u, 1024u);
             if constexpr (B_MN) bd = make_sdesc(sb + (uint32_t)kk * 2048u, 8192u, 1024u);
             else bd = make_sdesc(sb + (uint32_t)kk * 32u, 16u, 1024u);
-            tc_mma_f16(d_tmem, ad, bd, idesc, (kb | kk) != 0 ? 1u : 0u);
+            if constexpr (TWO_SM) tc_mma_f16_pair(d_tmem, ad, bd, idesc, (kb | kk) != 0 ? 1u : 0u);
+            else tc_mma_f16(d_tmem, ad, bd, idesc, (kb | kk) != 0 ? 1u : 0u);
           }
           // buffer free once these MMAs finish (in both blocks of a pair)
-          if constexpr (PAIR) tc_commit_mc(empty_bar(stage), (uint16_t)3u);
+          if constexpr (TWO_SM) tc_commit_pair_mc(empty_bar(stage), (uint16_t)3u);
+          else if constexpr (PAIR) tc_commit_mc(empty_bar(stage), (uint16_t)3u);
           else tc_commit(empty_bar(stage));
           if (++stage == STAGES) { stage = 0; phase ^= 1u; }
         }
         if (!ok) break;
-        tc_commit(accf_bar(buf));  // accumulator complete
+        // accumulator complete (2-SM pairs: in both blocks' tensor memory)
+        if constexpr (TWO_SM) tc_commit_pair_mc(accf_bar(buf), (uint16_t)3u);
+        else tc_commit(accf_bar(buf));
       }
       // Drain: every MMA issued must finish before tensor memory is freed.
-      tc_commit(drain_bar);
+      if constexpr (TWO_SM) tc_commit_pair_mc(drain_bar, (uint16_t)1u);
+      else tc_commit(drain_bar);
       mbar_wait_drain(drain_bar, 0u, p.timeout_ns);
     }
   } else {
@@ -404,7 +452,10 @@ __global__ void __launch_bounds__(THREADS, 1)
         tmem_ld_wait();
         if (c == BN / 32 - 1) {
           tc_fence_before();
-          mbar_arrive(acce_bar(buf));  // accumulator buffer may be overwritten
+          // accumulator buffer may be overwritten (2-SM pairs: tell the even
+          // block, whose MMAs write both blocks' tensor memory)
+          if constexpr (TWO_SM) mbar_arrive_cluster(mapa_shared(acce_bar(buf), 0u));
+          else mbar_arrive(acce_bar(buf));
         }
         if (tail >= 0) {
           float4* dst = reinterpret_cast<float4*>(tail_strip) + (c * 8) * 32 + lane;
@@ -513,7 +564,8 @@ __global__ void __launch_bounds__(THREADS, 1)
   if (warp == 1) {
     __syncwarp();
     tc_fence_after();
-    tmem_dealloc(tmem_base, (uint32_t)C_::TMEM_COLS);
+    if constexpr (TWO_SM) tmem_dealloc_pair(tmem_base, (uint32_t)C_::TMEM_COLS);
+    else tmem_dealloc(tmem_base, (uint32_t)C_::TMEM_COLS);
   }
 }
 
@@ -555,12 +607,12 @@ bool make_map(CUtensorMap* map, const void* base, int64_t rows, int64_t cols, in
 // How many two-block clusters of the pair kernel can be resident at once
 // (fewer than SMs / 2 when the SMs of a GPC do not all pair up).  Queried once
 // per kernel configuration.
-template <int BN, bool A_MN, bool B_MN>
+template <int BN, bool A_MN, bool B_MN, int MODE>
 int pair_slots(int num_sms) {
   static int n = 0;
   if (n == 0) {
-    using C_ = Cfg<BN, B_MN>;
-    auto kern = hgemm_tc_kernel<BN, A_MN, B_MN, false, true>;
+    using C_ = Cfg<BN, B_MN, MODE>;
+    auto kern = hgemm_tc_kernel<BN, A_MN, B_MN, false, MODE>;
     int q = 0;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              C_::SMEM_BYTES) == cudaSuccess) {
@@ -588,9 +640,10 @@ int host_total_units(const HParams& p, bool pair) {
   return tiles * p.splits;
 }
 
-template <int BN, bool A_MN, bool B_MN, bool SPLIT, bool PAIR>
+template <int BN, bool A_MN, bool B_MN, bool SPLIT, int MODE>
 cudaError_t launch_cfg(const HgemmArgs& a, const HParams& p, LaunchCtx& ctx) {
-  using C_ = Cfg<BN, B_MN>;
+  constexpr bool PAIR = MODE != 0;
+  using C_ = Cfg<BN, B_MN, MODE>;
   CUtensorMap mA, mB;
   bool ok;
   if (A_MN) ok = make_map(&mA, a.A, a.K, a.M, a.lda, 64, 64);     // stored [K, M]
@@ -604,13 +657,13 @@ cudaError_t launch_cfg(const HgemmArgs& a, const HParams& p, LaunchCtx& ctx) {
   memset(&mC, 0, sizeof(mC));
   if (p.c_tma && !make_map(&mC, a.C, a.M, a.N, a.ldc, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B))
     return cudaErrorInvalidValue;
-  auto kern = hgemm_tc_kernel<BN, A_MN, B_MN, SPLIT, PAIR>;
+  auto kern = hgemm_tc_kernel<BN, A_MN, B_MN, SPLIT, MODE>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        C_::SMEM_BYTES);
   if (e != cudaSuccess) return e;
   if constexpr (PAIR) {
     // persistent grid of as many pairs as can be resident at once
-    const int max_pairs = pair_slots<BN, A_MN, B_MN>(a.num_sms);
+    const int max_pairs = pair_slots<BN, A_MN, B_MN, MODE>(a.num_sms);
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -642,11 +695,13 @@ template <int BN>
 cudaError_t launch_bn(const HgemmArgs& a, const HParams& p, LaunchCtx& ctx) {
   const bool A_MN = a.transA != 0, B_MN = a.transB == 0, split = a.splits > 1;
   constexpr bool CAN_PAIR = BN == 128 || BN == 256;
+  constexpr int M1 = CAN_PAIR ? 1 : 0, M2 = CAN_PAIR ? 2 : 0;
 #define GB300_HG(AM, BMN)                                                   \
   if (A_MN == AM && B_MN == BMN) {                                          \
-    if (split) return launch_cfg<BN, AM, BMN, true, false>(a, p, ctx);      \
-    if (CAN_PAIR && p.pair) return launch_cfg<BN, AM, BMN, false, CAN_PAIR>(a, p, ctx); \
-    return launch_cfg<BN, AM, BMN, false, false>(a, p, ctx);                \
+    if (split) return launch_cfg<BN, AM, BMN, true, 0>(a, p, ctx);          \
+    if (CAN_PAIR && p.pair == 2) return launch_cfg<BN, AM, BMN, false, M2>(a, p, ctx); \
+    if (CAN_PAIR && p.pair == 1) return launch_cfg<BN, AM, BMN, false, M1>(a, p, ctx); \
+    return launch_cfg<BN, AM, BMN, false, 0>(a, p, ctx);                    \
   }
   GB300_HG(false, true)
   GB300_HG(true, true)
@@ -658,10 +713,11 @@ cudaError_t launch_bn(const HgemmArgs& a, const HParams& p, LaunchCtx& ctx) {
 
 }  // namespace
 
-int hgemm_pair_slots(int bn, int transA, int transB, int num_sms) {
+int hgemm_pair_slots(int bn, int transA, int transB, int mode, int num_sms) {
   const bool A_MN = transA != 0, B_MN = transB == 0;
-#define GB300_SLOTS(W, AM, BMN) \
-  if (bn == W && A_MN == AM && B_MN == BMN) return pair_slots<W, AM, BMN>(num_sms);
+#define GB300_SLOTS(W, AM, BMN)                                                              \
+  if (bn == W && A_MN == AM && B_MN == BMN)                                                  \
+    return mode == 2 ? pair_slots<W, AM, BMN, 2>(num_sms) : pair_slots<W, AM, BMN, 1>(num_sms);
   GB300_SLOTS(128, false, true) GB300_SLOTS(128, true, true) GB300_SLOTS(128, false, false)
   GB300_SLOTS(128, true, false) GB300_SLOTS(256, false, true) GB300_SLOTS(256, true, true)
   GB300_SLOTS(256, false, false) GB300_SLOTS(256, true, false)
@@ -744,7 +800,7 @@ cudaError_t launch_hgemm(const HgemmArgs& a, LaunchCtx& ctx) {
   p.fault_injection = a.fault_injection;
   p.c_vec_ok = ((reinterpret_cast<uintptr_t>(a.C) & 15u) == 0 && (a.ldc % 8) == 0) ? 1 : 0;
   p.c_tma = (p.c_vec_ok && a.beta == 0.f && a.splits <= 1 && a.c_tma) ? 1 : 0;
-  p.pair = hgemm_use_pair(bn, a.M, p.splits, a.pair) ? 1 : 0;
+  p.pair = hgemm_use_pair(bn, a.M, p.splits, a.pair) ? a.pair : 0;
   p.dp_units = a.dp_units;
   p.tail_splits = a.tail_splits;
   p.tail_k_slice = a.tail_k_slice;

@@ -41,7 +41,7 @@ struct HgemmArgs {
   float* partial;   // [splits][M][N] fp32 when splits > 1
   int num_sms;
   int bn;               // tile width: 32, 64, 128, 192 or 256
-  int pair;             // allow clusters of two blocks sharing B tiles
+  int pair;             // block pairs allowed: 0 none, 1 multicast B, 2 2-SM MMAs
   int c_tma;            // allow TMA stores of C (used when beta == 0 and C is aligned)
   int fault_injection;  // test hook: 1 = producer skips its first stage
   // tail split (see hgemm_plan_tail); tail_splits == 0 disables it
@@ -86,7 +86,7 @@ constexpr int SG_BM = 64 * SG_WARPS_M, SG_BN = 128, SG_BK = 32;
 constexpr int HG_BM = 128, HG_BK = 64;
 int hgemm_pick_bn(int M, int N, int transB, int num_sms);
 bool hgemm_use_pair(int bn, int M, int splits, int allowed);
-int hgemm_pair_slots(int bn, int transA, int transB, int num_sms);
+int hgemm_pair_slots(int bn, int transA, int transB, int mode, int num_sms);
 TailPlan hgemm_plan_tail(int M, int N, int K, int bn, bool pair, int workers);
 
 }  // namespace gb300
