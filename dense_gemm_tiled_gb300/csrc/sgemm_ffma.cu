@@ -49,7 +49,10 @@ constexpr int A_FLOATS = (BM * BK > BK * APAD) ? BM * BK : BK * APAD;
 constexpr int B_FLOATS = BK * BPAD;
 constexpr int STAGE_FLOATS = A_FLOATS + B_FLOATS;
 constexpr int SMEM_BYTES = STAGES * STAGE_FLOATS * 4;
-constexpr int GROUP_M = 8;  // tile rasterisation: 8 tile-rows walked together
+// Tile rasterisation: blocks walk GROUP tile-rows column by column, so each B
+// panel is fetched from DRAM once per group while the group's A panels stay in
+// L2.  The host picks GROUP so those A panels take about half of L2 (64 MB).
+constexpr int64_t RASTER_L2_BYTES = 64ll << 20;
 static_assert(BM == 64 * WARPS_M && BN == 128 && BK == 32, "tile shape");
 
 // Compile-time tuning knobs (measured on GB300 at 4096^3; the defaults won):
@@ -72,6 +75,7 @@ struct Params {
   int M, N, K;
   int k_slice;
   int tiles_m, tiles_n;
+  int group_m;  // tile-rows per rasterisation group
   float alpha, beta;
 };
 
@@ -219,11 +223,11 @@ __global__ void __launch_bounds__(THREADS, GB300_SG_MIN_BLOCKS) sgemm_ffma_kerne
   const int aswz = (arow >> 2) & 7; // row-tile chunk permutation, shared by all 8 lane rows
 
   // grouped rasterisation of the tile grid (consecutive blocks share B panels
-  // within a group of GROUP_M tile-rows)
+  // within a group of group_m tile-rows)
   const int bid = blockIdx.x;
-  const int per_group = GROUP_M * p.tiles_n;
-  const int first_m = (bid / per_group) * GROUP_M;
-  const int gsize = min(p.tiles_m - first_m, GROUP_M);
+  const int per_group = p.group_m * p.tiles_n;
+  const int first_m = (bid / per_group) * p.group_m;
+  const int gsize = min(p.tiles_m - first_m, p.group_m);
   const int tm = first_m + (bid % per_group) % gsize;
   const int tn = (bid % per_group) / gsize;
   const int m0 = tm * BM, n0 = tn * BN;
@@ -383,6 +387,13 @@ cudaError_t launch_sgemm(const SgemmArgs& a, LaunchCtx& ctx) {
   p.k_slice = a.splits > 1 ? a.k_slice : a.K;
   p.tiles_m = (a.M + BM - 1) / BM;
   p.tiles_n = (a.N + BN - 1) / BN;
+  {
+    const int64_t panel = (int64_t)BM * (a.splits > 1 ? a.k_slice : a.K) * 4;
+    int64_t g = panel > 0 ? RASTER_L2_BYTES / panel : p.tiles_m;
+    if (g < 1) g = 1;
+    if (g > p.tiles_m) g = p.tiles_m;
+    p.group_m = (int)g;
+  }
   p.alpha = a.alpha; p.beta = a.beta;
   // 16-byte staging needs 16-byte aligned rows in every operand (C too: the
   // epilogue's float4 accesses share the flag).

@@ -39,7 +39,9 @@ def oracle_for(prob, full=None, seed=0):
     if full:
         ref, mag = oracle.gemm_ref(A, B, C, prob.transA, prob.transB, prob.alpha, prob.beta)
         return ref, mag, None
-    rows, cols = sample_points(prob.M, prob.N, seed)
+    # fewer random points when each costs a K-long strided dot product
+    n_random = 32768 if prob.K <= 4096 else 8192
+    rows, cols = sample_points(prob.M, prob.N, seed, n_random=n_random)
     ref, mag = oracle.gemm_ref_points(A, B, rows, cols, C, prob.transA, prob.transB, prob.alpha,
                                       prob.beta)
     return ref, mag, (rows, cols)
