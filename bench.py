@@ -121,7 +121,8 @@ def dist_setup():
     if world > 1:
         import torch.distributed as dist
         import torch
-        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        backend = os.environ.get("GEMM_BENCH_BACKEND") or (
+            "nccl" if torch.cuda.is_available() else "gloo")
         if backend == "nccl":
             torch.cuda.set_device(local)
         dist.init_process_group(backend=backend)

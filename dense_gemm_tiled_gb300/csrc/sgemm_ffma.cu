@@ -51,8 +51,10 @@ constexpr int STAGE_FLOATS = A_FLOATS + B_FLOATS;
 constexpr int SMEM_BYTES = STAGES * STAGE_FLOATS * 4;
 // Tile rasterisation: blocks walk GROUP tile-rows column by column, so each B
 // panel is fetched from DRAM once per group while the group's A panels stay in
-// L2.  The host picks GROUP so those A panels take about half of L2 (64 MB).
-constexpr int64_t RASTER_L2_BYTES = 64ll << 20;
+// L2.  The host picks GROUP so those A panels take about a quarter of L2
+// (32 MB): measured at 4096^3, 8-row groups read 352 MB from DRAM and 32-row
+// groups (64 MB of A panels) 520 MB -- the L2 is split between the two dies.
+constexpr int64_t RASTER_L2_BYTES = 32ll << 20;
 static_assert(BM == 64 * WARPS_M && BN == 128 && BK == 32, "tile shape");
 
 // Compile-time tuning knobs (measured on GB300 at 4096^3; the defaults won):
