@@ -10,6 +10,10 @@
 //  repack_f16    : copies an fp16 operand whose rows are not 16-byte aligned
 //                  into a zero-padded buffer with a 16-byte row pitch, so the
 //                  tensor-memory-access unit can read it.
+//  transpose_f32 : packs an fp32 operand stored with k contiguous into the
+//                  k-major layout the FP32 kernel reads fastest (the "packing"
+//                  step of a tuned BLAS, "From a C loop to a GPU kernel", "What
+//                  BLAS is buying").
 //
 // All three are HBM-bound; they use grid-stride loops over 128-bit accesses
 // where the layout allows, with grids sized to a multiple of the SM count.
@@ -111,7 +115,45 @@ __global__ void repack_f16_kernel(int rows, int cols, const __half* __restrict__
   }
 }
 
+// dst[c][r] = src[r][c] for a rows x cols fp32 matrix: 32 x 32 tiles staged
+// through shared memory (one padding column, so the transposed reads are
+// conflict-free); both the global reads and the global writes are coalesced.
+__global__ void __launch_bounds__(256) transpose_f32_kernel(int rows, int cols,
+                                                            const float* __restrict__ src,
+                                                            int64_t ld_src, float* __restrict__ dst,
+                                                            int64_t ld_dst) {
+  __shared__ float tile[32][33];
+  const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;  // 32 x 8 threads
+  const int tiles_c = (cols + 31) / 32;
+  const int64_t tiles = (int64_t)((rows + 31) / 32) * tiles_c;
+  for (int64_t t = blockIdx.x; t < tiles; t += gridDim.x) {
+    const int r0 = (int)(t / tiles_c) * 32, c0 = (int)(t % tiles_c) * 32;
+#pragma unroll
+    for (int i = ty; i < 32; i += 8) {
+      const int r = r0 + i, c = c0 + tx;
+      tile[i][tx] = (r < rows && c < cols) ? src[(int64_t)r * ld_src + c] : 0.f;
+    }
+    __syncthreads();
+#pragma unroll
+    for (int i = ty; i < 32; i += 8) {
+      const int c = c0 + i, r = r0 + tx;
+      if (c < cols && r < rows) dst[(int64_t)c * ld_dst + r] = tile[tx][i];
+    }
+    __syncthreads();
+  }
+}
+
 }  // namespace
+
+cudaError_t launch_transpose_f32(int rows, int cols, const float* src, int64_t ld_src,
+                                 float* dst, int64_t ld_dst, LaunchCtx& ctx) {
+  const int64_t tiles = (int64_t)((rows + 31) / 32) * ((cols + 31) / 32);
+  const int grid = grid_for(tiles * 256, 256);
+  transpose_f32_kernel<<<grid, 256, 0, ctx.stream>>>(rows, cols, src, ld_src, dst, ld_dst);
+  cudaError_t e = cudaGetLastError();
+  if (e == cudaSuccess) ctx.launches++;
+  return e;
+}
 
 cudaError_t launch_splitk_reduce(int dtype, int M, int N, int splits, const float* P, void* C,
                                  int64_t ldc, float alpha, float beta, LaunchCtx& ctx) {

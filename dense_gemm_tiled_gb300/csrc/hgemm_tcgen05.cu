@@ -766,12 +766,12 @@ int hgemm_pick_bn(int M, int N, int transB, int num_sms) {
   if (N <= 128) return 128;
   // Wider N: the persistent grid runs ceil(tiles / SMs) rounds of tiles.  A
   // round of 128 x BN tiles costs, relative to BN = 256 and measured on GB300
-  // at 4096^3: 0.76 (BN 128), 0.85 (BN 192), 1.0 (BN 256) -- narrower tiles
-  // re-read A from shared memory more often per flop.  Pick the cheapest;
-  // ties go to the wider tile.
+  // at 4096^3 with 2-SM pairs: 0.85 (BN 128), 0.92 (BN 192), 1.0 (BN 256) --
+  // narrower tiles re-read A more often per flop.  Pick the cheapest; ties go
+  // to the wider tile.
   const int64_t tm = (M + BM - 1) / BM;
   const int widths[3] = {256, 192, 128};
-  const double round_cost[3] = {1.0, 0.85, 0.76};
+  const double round_cost[3] = {1.0, 0.92, 0.85};
   int best = 256;
   double best_cost = -1.0;
   for (int w = 0; w < 3; ++w) {

@@ -72,6 +72,9 @@ cudaError_t launch_splitk_reduce(int dtype, int M, int N, int splits, const floa
 // C = beta * C (K == 0); beta == 0 writes zeros.
 cudaError_t launch_scale(int dtype, int M, int N, void* C, int64_t ldc, float beta,
                          LaunchCtx& ctx);
+// dst[c][r] = src[r][c] (fp32 rows x cols).
+cudaError_t launch_transpose_f32(int rows, int cols, const float* src, int64_t ld_src,
+                                 float* dst, int64_t ld_dst, LaunchCtx& ctx);
 // dst[r][c] = src[r][c] for c < cols, 0 for cols <= c < ld_dst (fp16 rows).
 cudaError_t launch_repack_f16(int rows, int cols, const __half* src, int64_t ld_src,
                               __half* dst, int64_t ld_dst, LaunchCtx& ctx);
