@@ -41,6 +41,7 @@ _lib.gemm_set_fault_injection.restype = None
 
 F32 = 0
 F16_F32ACC = 1
+BF16_F32ACC = 2
 OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_ALIAS, ERR_CUDA, ERR_NO_MEMORY, ERR_TIMEOUT = range(7)
 PATHS = {0: "none", 1: "scale", 2: "ffma", 3: "ffma_splitk", 4: "tc", 5: "tc_splitk"}
 
@@ -117,6 +118,8 @@ def _dims(A, B, C, transA, transB):
         dtype = F32
     elif A.dtype == torch.float16:
         dtype = F16_F32ACC
+    elif A.dtype == torch.bfloat16:
+        dtype = BF16_F32ACC
     else:
         raise TypeError(f"unsupported dtype {A.dtype}")
     M, K = (A.shape[1], A.shape[0]) if transA else (A.shape[0], A.shape[1])
@@ -132,7 +135,7 @@ def gemm(A, B, C, transA=False, transB=False, alpha=1.0, beta=0.0, stream=None):
     """C = alpha * op(A) @ op(B) + beta * C in place, on torch CUDA tensors.
 
     A is [M,K] (or [K,M] with transA), B is [K,N] (or [N,K] with transB),
-    C is [M,N]; all float32 or all float16 (fp32 accumulation), rows
+    C is [M,N]; all float32, all float16 or all bfloat16 (fp32 accumulation), rows
     contiguous, any leading dimension.  Runs on `stream` (a torch.cuda.Stream)
     or the current stream.  Returns C.
     """

@@ -7,7 +7,7 @@
 //                  are added in increasing z, so the result does not depend on
 //                  scheduling.
 //  scale         : C = beta * C, the K == 0 case of C = alpha*A*B + beta*C.
-//  repack_f16    : copies an fp16 operand whose rows are not 16-byte aligned
+//  repack_16     : copies an fp16/bf16 operand whose rows are not 16-byte aligned
 //                  into a zero-padded buffer with a 16-byte row pitch, so the
 //                  tensor-memory-access unit can read it.
 //  transpose_f32 : packs an fp32 operand stored with k contiguous into the
@@ -15,8 +15,9 @@
 //                  step of a tuned BLAS, "From a C loop to a GPU kernel", "What
 //                  BLAS is buying").
 //
-// All three are HBM-bound; they use grid-stride loops over 128-bit accesses
+// All are HBM-bound; they use grid-stride loops over 128-bit accesses
 // where the layout allows, with grids sized to a multiple of the SM count.
+#include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
@@ -49,6 +50,12 @@ __device__ __forceinline__ void store_out(__half* C, int64_t i, float v) {
 __device__ __forceinline__ float load_out(const float* C, int64_t i) { return C[i]; }
 __device__ __forceinline__ float load_out(const __half* C, int64_t i) {
   return __half2float(C[i]);
+}
+__device__ __forceinline__ void store_out(__nv_bfloat16* C, int64_t i, float v) {
+  C[i] = __float2bfloat16_rn(v);
+}
+__device__ __forceinline__ float load_out(const __nv_bfloat16* C, int64_t i) {
+  return __bfloat162float(C[i]);
 }
 
 // One thread per 4 consecutive columns of a row (N % 4 == 0 path reads P with
@@ -105,39 +112,62 @@ __global__ void scale_kernel(int M, int N, T* C, int64_t ldc, float beta) {
   }
 }
 
-__global__ void repack_f16_kernel(int rows, int cols, const __half* __restrict__ src,
-                                  int64_t ld_src, __half* __restrict__ dst, int64_t ld_dst) {
+// 16-bit elements copied as bit patterns (fp16 and bf16 alike; padding is +0)
+__global__ void repack_16_kernel(int rows, int cols, const uint16_t* __restrict__ src,
+                                 int64_t ld_src, uint16_t* __restrict__ dst, int64_t ld_dst) {
   const int64_t total = (int64_t)rows * ld_dst;
   for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < total;
        i += (int64_t)gridDim.x * blockDim.x) {
     const int64_t r = i / ld_dst, c = i - r * ld_dst;
-    dst[i] = (c < cols) ? src[r * ld_src + c] : __float2half_rn(0.f);
+    dst[i] = (c < cols) ? src[r * ld_src + c] : (uint16_t)0;
   }
 }
 
-// dst[c][r] = src[r][c] for a rows x cols fp32 matrix: 32 x 32 tiles staged
-// through shared memory (one padding column, so the transposed reads are
-// conflict-free); both the global reads and the global writes are coalesced.
+// dst[c][r] = src[r][c] for a rows x cols fp32 matrix: 64 x 64 tiles staged
+// through shared memory (one padding column), 128-bit global loads and stores
+// where rows are 16-byte aligned, scalar accesses at ragged edges.
+template <bool VEC>
 __global__ void __launch_bounds__(256) transpose_f32_kernel(int rows, int cols,
                                                             const float* __restrict__ src,
                                                             int64_t ld_src, float* __restrict__ dst,
                                                             int64_t ld_dst) {
-  __shared__ float tile[32][33];
-  const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;  // 32 x 8 threads
-  const int tiles_c = (cols + 31) / 32;
-  const int64_t tiles = (int64_t)((rows + 31) / 32) * tiles_c;
+  __shared__ float tile[64][65];
+  const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;  // 16 float4 columns x 16 rows
+  const int tiles_c = (cols + 63) / 64;
+  const int64_t tiles = (int64_t)((rows + 63) / 64) * tiles_c;
   for (int64_t t = blockIdx.x; t < tiles; t += gridDim.x) {
-    const int r0 = (int)(t / tiles_c) * 32, c0 = (int)(t % tiles_c) * 32;
+    const int r0 = (int)(t / tiles_c) * 64, c0 = (int)(t % tiles_c) * 64;
 #pragma unroll
-    for (int i = ty; i < 32; i += 8) {
-      const int r = r0 + i, c = c0 + tx;
-      tile[i][tx] = (r < rows && c < cols) ? src[(int64_t)r * ld_src + c] : 0.f;
+    for (int p = 0; p < 4; ++p) {
+      const int rr = ty + 16 * p, r = r0 + rr, c = c0 + 4 * tx;
+      float v[4];
+      if (VEC && r < rows && c + 3 < cols) {
+        const float4 f = __ldg(reinterpret_cast<const float4*>(src + (int64_t)r * ld_src + c));
+        v[0] = f.x; v[1] = f.y; v[2] = f.z; v[3] = f.w;
+      } else {
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+          v[e] = (r < rows && c + e < cols) ? src[(int64_t)r * ld_src + c + e] : 0.f;
+      }
+#pragma unroll
+      for (int e = 0; e < 4; ++e) tile[rr][4 * tx + e] = v[e];
     }
     __syncthreads();
 #pragma unroll
-    for (int i = ty; i < 32; i += 8) {
-      const int c = c0 + i, r = r0 + tx;
-      if (c < cols && r < rows) dst[(int64_t)c * ld_dst + r] = tile[tx][i];
+    for (int p = 0; p < 4; ++p) {
+      const int cc = ty + 16 * p, c = c0 + cc, r = r0 + 4 * tx;  // dst row c, columns r..r+3
+      if (c >= cols) continue;
+      const float v0 = tile[4 * tx][cc], v1 = tile[4 * tx + 1][cc], v2 = tile[4 * tx + 2][cc],
+                  v3 = tile[4 * tx + 3][cc];
+      float* d = dst + (int64_t)c * ld_dst + r;
+      if (VEC && r + 3 < rows) {
+        *reinterpret_cast<float4*>(d) = make_float4(v0, v1, v2, v3);
+      } else {
+        const float v[4] = {v0, v1, v2, v3};
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+          if (r + e < rows) d[e] = v[e];
+      }
     }
     __syncthreads();
   }
@@ -147,9 +177,13 @@ __global__ void __launch_bounds__(256) transpose_f32_kernel(int rows, int cols,
 
 cudaError_t launch_transpose_f32(int rows, int cols, const float* src, int64_t ld_src,
                                  float* dst, int64_t ld_dst, LaunchCtx& ctx) {
-  const int64_t tiles = (int64_t)((rows + 31) / 32) * ((cols + 31) / 32);
+  const int64_t tiles = (int64_t)((rows + 63) / 64) * ((cols + 63) / 64);
   const int grid = grid_for(tiles * 256, 256);
-  transpose_f32_kernel<<<grid, 256, 0, ctx.stream>>>(rows, cols, src, ld_src, dst, ld_dst);
+  // 128-bit accesses need 16-byte aligned rows on both sides
+  const bool vec = ((reinterpret_cast<uintptr_t>(src) | reinterpret_cast<uintptr_t>(dst)) & 15u) == 0 &&
+                   (ld_src % 4) == 0 && (ld_dst % 4) == 0;
+  if (vec) transpose_f32_kernel<true><<<grid, 256, 0, ctx.stream>>>(rows, cols, src, ld_src, dst, ld_dst);
+  else transpose_f32_kernel<false><<<grid, 256, 0, ctx.stream>>>(rows, cols, src, ld_src, dst, ld_dst);
   cudaError_t e = cudaGetLastError();
   if (e == cudaSuccess) ctx.launches++;
   return e;
@@ -164,9 +198,12 @@ cudaError_t launch_splitk_reduce(int dtype, int M, int N, int splits, const floa
   if (dtype == 0) {
     if (vec) splitk_reduce_vec4<float><<<grid, threads, 0, ctx.stream>>>(M, N, splits, P, (float*)C, ldc, alpha, beta);
     else splitk_reduce_scalar<float><<<grid, threads, 0, ctx.stream>>>(M, N, splits, P, (float*)C, ldc, alpha, beta);
-  } else {
+  } else if (dtype == 1) {
     if (vec) splitk_reduce_vec4<__half><<<grid, threads, 0, ctx.stream>>>(M, N, splits, P, (__half*)C, ldc, alpha, beta);
     else splitk_reduce_scalar<__half><<<grid, threads, 0, ctx.stream>>>(M, N, splits, P, (__half*)C, ldc, alpha, beta);
+  } else {
+    if (vec) splitk_reduce_vec4<__nv_bfloat16><<<grid, threads, 0, ctx.stream>>>(M, N, splits, P, (__nv_bfloat16*)C, ldc, alpha, beta);
+    else splitk_reduce_scalar<__nv_bfloat16><<<grid, threads, 0, ctx.stream>>>(M, N, splits, P, (__nv_bfloat16*)C, ldc, alpha, beta);
   }
   cudaError_t e = cudaGetLastError();
   if (e == cudaSuccess) ctx.launches++;
@@ -178,17 +215,19 @@ cudaError_t launch_scale(int dtype, int M, int N, void* C, int64_t ldc, float be
   const int threads = 256;
   const int grid = grid_for((int64_t)M * N, threads);
   if (dtype == 0) scale_kernel<float><<<grid, threads, 0, ctx.stream>>>(M, N, (float*)C, ldc, beta);
-  else scale_kernel<__half><<<grid, threads, 0, ctx.stream>>>(M, N, (__half*)C, ldc, beta);
+  else if (dtype == 1) scale_kernel<__half><<<grid, threads, 0, ctx.stream>>>(M, N, (__half*)C, ldc, beta);
+  else scale_kernel<__nv_bfloat16><<<grid, threads, 0, ctx.stream>>>(M, N, (__nv_bfloat16*)C, ldc, beta);
   cudaError_t e = cudaGetLastError();
   if (e == cudaSuccess) ctx.launches++;
   return e;
 }
 
-cudaError_t launch_repack_f16(int rows, int cols, const __half* src, int64_t ld_src,
-                              __half* dst, int64_t ld_dst, LaunchCtx& ctx) {
+cudaError_t launch_repack_16(int rows, int cols, const void* src, int64_t ld_src, void* dst,
+                             int64_t ld_dst, LaunchCtx& ctx) {
   const int threads = 256;
   const int grid = grid_for((int64_t)rows * ld_dst, threads);
-  repack_f16_kernel<<<grid, threads, 0, ctx.stream>>>(rows, cols, src, ld_src, dst, ld_dst);
+  repack_16_kernel<<<grid, threads, 0, ctx.stream>>>(rows, cols, (const uint16_t*)src, ld_src,
+                                                     (uint16_t*)dst, ld_dst);
   cudaError_t e = cudaGetLastError();
   if (e == cudaSuccess) ctx.launches++;
   return e;

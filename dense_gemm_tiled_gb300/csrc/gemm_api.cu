@@ -4,7 +4,7 @@
 // Path choice:
 //   dtype fp32 -> CUDA-core FFMA kernel (sgemm_ffma.cu); split-K when the
 //                 output has too few tiles to fill the GPU.
-//   dtype fp16 -> tcgen05 kernel (hgemm_tcgen05.cu); split-K likewise.
+//   dtype fp16 / bf16 -> tcgen05 kernel (hgemm_tcgen05.cuh); split-K likewise.
 // The split-K rule follows "Metal GEMM Kernels for LoRA Training", section 5
 // (route by output-tile count; fp32 partials in device memory, then a
 // reduction), with the threshold set by this GPU's SM count instead of the
@@ -78,7 +78,8 @@ int check_args(int transA, int transB, int64_t M, int64_t N, int64_t K, int dtyp
                int64_t ldc, int64_t* a_rows, int64_t* a_cols, int64_t* b_rows,
                int64_t* b_cols) {
   if ((transA != 0 && transA != 1) || (transB != 0 && transB != 1)) return GEMM_ERR_INVALID_ARG;
-  if (dtype != GEMM_F32 && dtype != GEMM_F16_F32ACC) return GEMM_ERR_INVALID_ARG;
+  if (dtype != GEMM_F32 && dtype != GEMM_F16_F32ACC && dtype != GEMM_BF16_F32ACC)
+    return GEMM_ERR_INVALID_ARG;
   if (M < 0 || N < 0 || K < 0) return GEMM_ERR_INVALID_ARG;
   const int64_t lim = (int64_t)1 << 31;
   if (M >= lim || N >= lim || K >= lim) return GEMM_ERR_UNSUPPORTED;
@@ -244,7 +245,7 @@ int run_gemm(int transA, int transB, int64_t M64, int64_t N64, int64_t K64, int 
   } else if (dtype == GEMM_F32) {
     const int64_t tiles = (int64_t)((M + SG_BM - 1) / SG_BM) * ((N + SG_BN - 1) / SG_BN);
     int splits, k_slice;
-    plan_splits(tiles, K, SG_BK, 2 * sms, 8, 16, &splits, &k_slice);
+    plan_splits(tiles, K, SG_BK, 2 * sms, 4, 16, &splits, &k_slice);
     SgemmArgs a{transA, transB, M, N, K, (const float*)A, lda, (const float*)B, ldb, (float*)C,
                 ldc, alpha, beta, splits, k_slice, nullptr};
     // Packing: the kernel reads A stored [K,M] and B stored [K,N] fastest
@@ -288,8 +289,8 @@ int run_gemm(int transA, int transB, int64_t M64, int64_t N64, int64_t K64, int 
     plan_splits(tiles, K, HG_BK, sms, 4, 32, &splits, &k_slice);
     // The tensor-memory-access unit needs 16-byte aligned bases and row
     // pitches; an operand that has neither is copied into padded scratch.
-    const __half* Ad = (const __half*)A;
-    const __half* Bd = (const __half*)B;
+    const void* Ad = A;
+    const void* Bd = B;
     int64_t ldad = lda, ldbd = ldb;
     const bool a_ok = ((uintptr_t)A % 16) == 0 && (lda % 8) == 0;
     const bool b_ok = ((uintptr_t)B % 16) == 0 && (ldb % 8) == 0;
@@ -320,19 +321,20 @@ int run_gemm(int transA, int transB, int64_t M64, int64_t N64, int64_t K64, int 
       if (e != cudaSuccess) return cuda_fail(e);
     }
     if (!a_ok) {
-      __half* dst = (__half*)wp;
-      e = launch_repack_f16((int)a_rows, (int)a_cols, Ad, lda, dst, lda_p, ctx);
+      void* dst = wp;
+      e = launch_repack_16((int)a_rows, (int)a_cols, Ad, lda, dst, lda_p, ctx);
       Ad = dst; ldad = lda_p; wp += bytes_a;
     }
     if (e == cudaSuccess && !b_ok) {
-      __half* dst = (__half*)wp;
-      e = launch_repack_f16((int)b_rows, (int)b_cols, Bd, ldb, dst, ldb_p, ctx);
+      void* dst = wp;
+      e = launch_repack_16((int)b_rows, (int)b_cols, Bd, ldb, dst, ldb_p, ctx);
       Bd = dst; ldbd = ldb_p; wp += bytes_b;
     }
     if (e == cudaSuccess) {
-      HgemmArgs a{transA, transB, M, N, K, Ad, ldad, Bd, ldbd, (__half*)C, ldc, alpha, beta,
+      HgemmArgs a{transA, transB, M, N, K, Ad, ldad, Bd, ldbd, C, ldc, alpha, beta,
                   splits, k_slice, splits > 1 ? (float*)wp : nullptr, sms, bn, pair,
                   c_tma_enabled(), g_fault_injection.load()};
+      a.dtype = dtype;
       if (tail.splits > 0) {
         a.dp_units = tail.dp_units;
         a.tail_splits = tail.splits;
@@ -343,7 +345,7 @@ int run_gemm(int transA, int transB, int64_t M64, int64_t N64, int64_t K64, int 
       path = splits > 1 ? GEMM_PATH_TC_SPLITK : GEMM_PATH_TC;
       e = launch_hgemm(a, ctx);
       if (e == cudaSuccess && splits > 1)
-        e = launch_splitk_reduce(1, M, N, splits, a.partial, C, ldc, alpha, beta, ctx);
+        e = launch_splitk_reduce(dtype, M, N, splits, a.partial, C, ldc, alpha, beta, ctx);
     }
   }
   g_total_launches += ctx.launches;
@@ -536,7 +538,7 @@ extern "C" int gemm_splitk_noalloc(int transA, int transB, int64_t M, int64_t N,
   } else if (dtype == GEMM_F32) {
     const int64_t tiles = (int64_t)((Mi + SG_BM - 1) / SG_BM) * ((Ni + SG_BN - 1) / SG_BN);
     int splits, k_slice;
-    plan_splits(tiles, Ki, SG_BK, 2 * sms, 8, 16, &splits, &k_slice);
+    plan_splits(tiles, Ki, SG_BK, 2 * sms, 4, 16, &splits, &k_slice);
     if (splits > 1 && (uint64_t)splits * (uint64_t)M * (uint64_t)N * sizeof(float) >
                           GEMM_NOALLOC_SCRATCH_BYTES)
       return GEMM_ERR_UNSUPPORTED;  // partial sums would not fit the fixed array
@@ -562,13 +564,14 @@ extern "C" int gemm_splitk_noalloc(int transA, int transB, int64_t M, int64_t N,
     if (splits > 1 && (uint64_t)splits * (uint64_t)M * (uint64_t)N * sizeof(float) >
                           GEMM_NOALLOC_SCRATCH_BYTES)
       return GEMM_ERR_UNSUPPORTED;  // partial sums would not fit the fixed array
-    HgemmArgs a{transA, transB, Mi, Ni, Ki, (const __half*)A, lda, (const __half*)B, ldb,
-                (__half*)C, ldc, alpha, beta, splits, k_slice, splits > 1 ? scratch : nullptr,
-                sms, bn, pair_enabled(), c_tma_enabled(), g_fault_injection.load()};
+    HgemmArgs a{transA, transB, Mi, Ni, Ki, A, lda, B, ldb, C, ldc, alpha, beta, splits,
+                k_slice, splits > 1 ? scratch : nullptr, sms, bn, pair_enabled(),
+                c_tma_enabled(), g_fault_injection.load()};
+    a.dtype = dtype;
     path = splits > 1 ? GEMM_PATH_TC_SPLITK : GEMM_PATH_TC;
     e = launch_hgemm(a, ctx);
     if (e == cudaSuccess && splits > 1)
-      e = launch_splitk_reduce(1, Mi, Ni, splits, scratch, C, ldc, alpha, beta, ctx);
+      e = launch_splitk_reduce(dtype, Mi, Ni, splits, scratch, C, ldc, alpha, beta, ctx);
   }
   g_total_launches += ctx.launches;
   tl_last_launches = ctx.launches;

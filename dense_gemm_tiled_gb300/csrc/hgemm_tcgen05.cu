@@ -1,723 +1,15 @@
-// fp16-operand / fp32-accumulate / fp16-output GEMM on the 5th-generation
-// tensor cores (tcgen05.mma, accumulators in tensor memory).
-//
-//   C = alpha * op(A) * op(B) + beta * C, variants nn / tn / nt (and tt).
-//
-// The regime is that of "Metal GEMM Kernels for LoRA Training on Apple
-// Silicon": fp16 operands with fp32 accumulation (section 1, type table), the
-// fp32 accumulator converted to fp16 on the way out (section 2), the three
-// transpose variants of the section 2 table, and fp32 partial sums plus a
-// reduction for skinny shapes (section 5, split-K).  The Metal design there (one
-// 32 x 32 simdgroup tile, staged output) is prior art only; this kernel is
-// built for sm_103a:
-//
-//  * Persistent, warp-specialised block of 6 warps, one block per SM:
-//      warp 0      TMA producer (one elected lane)
-//      warp 1      TMEM allocator + MMA issuer (one elected lane)
-//      warps 2..5  epilogue (128 threads = the 128 accumulator rows)
-//  * Operand tiles reach shared memory by TMA (cp.async.bulk.tensor) with the
-//    128-byte swizzle, through a ring of STAGES buffers guarded by mbarriers
-//    (full: TMA bytes landed; empty: the MMAs reading the buffer finished).
-//    Out-of-range rows/columns of edge tiles are zero-filled by the TMA unit.
-//  * The transposed operand is not moved: a K-contiguous operand (A[M,K],
-//    B[N,K]) is described to the tensor core as K-major, an MN-contiguous one
-//    (A[K,M], B[K,N]) as MN-major, by the shared-memory descriptor layout and
-//    the instruction descriptor's major bits.  Section 3 of the LoRA page
-//    found the transposed operand's cost in staging instructions; here there
-//    are none.
-//  * The 128 x BN fp32 accumulator lives in tensor memory, double buffered,
-//    so the epilogue of one tile overlaps the main loop of the next.
-//  * Fused epilogue: tcgen05.ld -> alpha * acc + beta * C_old -> fp16
-//    (round to nearest even) -> global; or raw fp32 partial sums (split-K).
-//
-// Every mbarrier wait is bounded (see common.cuh); on expiry the block stops
-// issuing work, drains its in-flight copies and MMAs, frees its tensor memory
-// and returns, leaving GEMM_ERR_TIMEOUT in the device status word.
-#include <cuda.h>
-#include <cudaTypedefs.h>
-#include <cuda_fp16.h>
-#include <cuda_runtime.h>
-#include <stdint.h>
-#include <string.h>
-
-#include "common.cuh"
-#include "internal.h"
+// fp16 instantiation of the tcgen05 GEMM (hgemm_tcgen05.cuh) and the
+// dispatcher's planning functions: tile width, block pairs, tail split.
+#include "hgemm_tcgen05.cuh"
 
 namespace gb300 {
-namespace {
-
-constexpr int BM = HG_BM;     // 128 accumulator rows = 128 TMEM lanes
-constexpr int BK = HG_BK;     // 64 fp16 = 128 bytes = one swizzle atom row
-constexpr int UMMA_K = 16;    // K per tcgen05.mma kind::f16
-constexpr int THREADS = 192;
-constexpr int GROUP_M = 8;
-constexpr int A_TILE_BYTES = BM * BK * 2;  // 16 KiB
-constexpr int SMEM_BUDGET = 200 * 1024;
-
-// MODE: 0 = single blocks; 1 = pairs of blocks sharing each B tile by TMA
-// multicast (each block still holds the whole B tile); 2 = pairs running
-// 256-row MMAs across both SMs (tcgen05 cta_group::2): each block holds its
-// 128 rows of A and half of the B tile.
-template <int BN, bool B_MN, int MODE = 0>
-struct Cfg {
-  // An MN-major B tile is stored as 64-wide swizzle atoms, so it is at least
-  // one atom wide; the MMA reads only the first BN columns.
-  static constexpr int B_COLS = B_MN ? (BN < 64 ? 64 : BN) : BN;
-  static constexpr int B_TILE_BYTES = (MODE == 2 ? B_COLS / 2 : B_COLS) * BK * 2;
-  static constexpr int STAGE_BYTES = A_TILE_BYTES + B_TILE_BYTES;
-  static constexpr int STAGES_RAW = SMEM_BUDGET / STAGE_BYTES;
-  static constexpr int STAGES = STAGES_RAW > 8 ? 8 : STAGES_RAW;
-  // two accumulator buffers of BN fp32 columns, rounded up to a power of two
-  static constexpr int TMEM_COLS = 2 * BN <= 64 ? 64 : 2 * BN <= 128 ? 128 : 2 * BN <= 256 ? 256 : 512;
-  // + 4 epilogue warps x 2 buffers x (32 x 32 fp16) staging for TMA stores of C
-  static constexpr int STAGING_BYTES = 4 * 2 * 2048;
-  static constexpr int SMEM_BYTES =
-      STAGES * STAGE_BYTES + STAGING_BYTES + 1024 /*align*/ + 256 /*barriers*/;
-};
-
-struct HParams {
-  __half* C;
-  float* partial;
-  int64_t ldc;
-  int M, N, K;
-  int k_slice;
-  int tiles_m, tiles_n, splits;
-  float alpha, beta;
-  unsigned int* status;
-  uint64_t timeout_ns;
-  int fault_injection;
-  int c_vec_ok;  // C base 16-byte aligned and ldc % 8 == 0
-  int c_tma;     // beta == 0 and C aligned: C leaves through TMA stores
-  int pair;      // 1: clusters of two blocks share each B tile (TMA multicast)
-  // Tail split (only when splits == 1): units [0, dp_units) are whole tiles;
-  // the remaining tiles are cut into tail_splits K slices of tail_k_slice, each
-  // writing fp32 partials to tail_ws; per 32-row strip the last slice to
-  // arrive (tail_cnt) sums all slices in slice order and runs the epilogue.
-  int dp_units, tail_splits, tail_k_slice;
-  float* tail_ws;          // [tail tiles][pair ? 2 : 1][tail_splits][4 warps][32 x BN]
-  unsigned int* tail_cnt;  // [tail tiles][pair ? 2 : 1][4], zero on entry and on exit
-};
-
-// tcgen05 shared-memory matrix descriptor, 128-byte swizzle:
-//   bits  0-13  start address >> 4
-//   bits 16-29  leading-dimension byte offset >> 4
-//   bits 32-45  stride-dimension byte offset >> 4
-//   bits 46-48  fixed 0b001
-//   bits 61-63  layout: 2 = 128-byte swizzle
-// K-major:  rows of 128 B (64 fp16 along K), 8-row groups 1024 B apart (SBO);
-//           the leading offset is unused for a swizzled K-major operand.
-// MN-major: rows of 128 B (64 fp16 along M or N) indexed by k; 8-k-row groups
-//           1024 B apart (SBO); 64-wide M/N atoms BK*128 B apart (LBO).
-__device__ __forceinline__ uint64_t make_sdesc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
-  return (uint64_t)((saddr & 0x3FFFFu) >> 4) | ((uint64_t)((lbo >> 4) & 0x3FFFu) << 16) |
-         ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46) | (2ull << 61);
-}
-
-// Instruction descriptor, kind::f16: D fp32 (bits 4-5 = 1), A and B fp16
-// (bits 7-9, 10-12 = 0), A major (bit 15), B major (bit 16; 1 = MN-major),
-// N >> 3 (bits 17-22), M >> 4 (bits 24-28).
-template <int BN, bool A_MN, bool B_MN, int M_ROWS = BM>
-__device__ __forceinline__ constexpr uint32_t make_idesc() {
-  return (1u << 4) | ((A_MN ? 1u : 0u) << 15) | ((B_MN ? 1u : 0u) << 16) |
-         ((uint32_t)(BN >> 3) << 17) | ((uint32_t)(M_ROWS >> 4) << 24);
-}
-
-// Work unit u -> tile, K range, slice.  Without pairs a tile is 128 x BN;
-// with pairs (a cluster of two blocks sharing B) a unit covers two vertically
-// adjacent tiles and block `rank` of the pair takes tile row 2 * pair_row + rank.
-//  * split-K launches: unit = slice z of tile t, u = z * tiles + t;
-//  * tail split: units below dp_units are whole tiles; unit dp_units + v is
-//    slice v / tail_tiles of tail tile v % tail_tiles (`tail` >= 0);
-//  * otherwise: unit = whole tile.
-template <bool PAIR>
-__device__ __forceinline__ void unit_coords(int u, const HParams& p, int rank, int& m0, int& tn,
-                                            int& kbeg, int& nkb, int& z, int& tail) {
-  const int rows = PAIR ? (p.tiles_m + 1) / 2 : p.tiles_m;
-  const int tiles = rows * p.tiles_n;
-  int t, ks;
-  tail = -1;
-  if (p.tail_splits > 0 && u >= p.dp_units) {
-    const int tail_tiles = tiles - p.dp_units;
-    const int v = u - p.dp_units;
-    tail = v % tail_tiles;
-    z = v / tail_tiles;
-    t = p.dp_units + tail;
-    ks = p.tail_k_slice;
-  } else {
-    z = u / tiles;
-    t = u - z * tiles;
-    ks = p.k_slice;
-  }
-  const int per_group = GROUP_M * p.tiles_n;
-  const int first_m = (t / per_group) * GROUP_M;
-  const int gsize = min(rows - first_m, GROUP_M);
-  const int tr = first_m + (t % per_group) % gsize;
-  tn = (t % per_group) / gsize;
-  const int tm = PAIR ? 2 * tr + rank : tr;
-  m0 = tm * BM;
-  kbeg = z * ks;
-  const int kend = min(p.K, kbeg + ks);
-  nkb = (kend - kbeg + BK - 1) / BK;
-}
-
-__device__ __forceinline__ int total_units(const HParams& p, bool pair) {
-  const int tiles = (pair ? (p.tiles_m + 1) / 2 : p.tiles_m) * p.tiles_n;
-  if (p.tail_splits > 0) return p.dp_units + (tiles - p.dp_units) * p.tail_splits;
-  return tiles * p.splits;
-}
-
-// alpha * v + beta * C_old -> fp16 (RN-even) -> C, for 32 columns of one row
-__device__ __forceinline__ void store_c32(const HParams& p, int gm, int gn0, float (&v)[32]) {
-  __half* dst = p.C + (int64_t)gm * p.ldc + gn0;
-#pragma unroll
-  for (int j = 0; j < 32; ++j) v[j] = p.alpha * v[j];
-  const bool full = (gn0 + 31 < p.N) && p.c_vec_ok;
-  if (full) {
-    if (p.beta != 0.f) {
-#pragma unroll
-      for (int w = 0; w < 4; ++w) {
-        const uint4 cv = reinterpret_cast<const uint4*>(dst)[w];
-        const __half2* ch = reinterpret_cast<const __half2*>(&cv);
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const float2 f = __half22float2(ch[e]);
-          v[8 * w + 2 * e] = __fmaf_rn(p.beta, f.x, v[8 * w + 2 * e]);
-          v[8 * w + 2 * e + 1] = __fmaf_rn(p.beta, f.y, v[8 * w + 2 * e + 1]);
-        }
-      }
-    }
-#pragma unroll
-    for (int w = 0; w < 4; ++w) {
-      uint4 o;
-      __half2* oh = reinterpret_cast<__half2*>(&o);
-#pragma unroll
-      for (int e = 0; e < 4; ++e)
-        oh[e] = __halves2half2(__float2half_rn(v[8 * w + 2 * e]),
-                               __float2half_rn(v[8 * w + 2 * e + 1]));
-      reinterpret_cast<uint4*>(dst)[w] = o;
-    }
-  } else {
-    for (int j = 0; j < 32; ++j) {
-      if (gn0 + j < p.N) {
-        float o = v[j];
-        if (p.beta != 0.f) o = __fmaf_rn(p.beta, __half2float(dst[j]), o);
-        dst[j] = __float2half_rn(o);
-      }
-    }
-  }
-}
-
-template <int BN, bool A_MN, bool B_MN, bool SPLIT, int MODE>
-__global__ void __launch_bounds__(THREADS, 1)
-    hgemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
-                    const __grid_constant__ CUtensorMap tmB,
-                    const __grid_constant__ CUtensorMap tmC, const HParams p) {
-  constexpr bool PAIR = MODE != 0;
-  constexpr bool TWO_SM = MODE == 2;
-  using C_ = Cfg<BN, B_MN, MODE>;
-  constexpr int STAGES = C_::STAGES;
-  // bytes that complete one stage: this block's (single, multicast pair), or
-  // both blocks' (2-SM pair: all loads of the pair complete on the even
-  // block's barrier)
-  constexpr uint32_t STAGE_TX = (uint32_t)C_::STAGE_BYTES * (TWO_SM ? 2u : 1u);
-  // Multicast pairs: each block of the cluster loads half of the B tile and
-  // multicasts it to both, so a stage is only free again once both blocks'
-  // MMAs have read it (two arrivals on `empty`).  2-SM pairs: the even block
-  // issues every MMA and its commits arrive on both blocks' barriers.
-  const int rank = PAIR ? (int)cluster_ctarank() : 0;
-  const int worker = PAIR ? (int)(blockIdx.x >> 1) : (int)blockIdx.x;
-  const int workers = PAIR ? (int)(gridDim.x >> 1) : (int)gridDim.x;
-
-  extern __shared__ uint8_t smem_raw[];
-  const uint32_t raw_addr = smem_u32(smem_raw);
-  const uint32_t tiles_addr = (raw_addr + 1023u) & ~1023u;  // swizzle atoms need 1 KiB alignment
-  uint8_t* const tiles_ptr = smem_raw + (tiles_addr - raw_addr);
-  // C staging (1 KiB aligned: the 64-byte swizzle pattern repeats every 512 B)
-  const uint32_t staging_addr = tiles_addr + (uint32_t)(STAGES * C_::STAGE_BYTES);
-  uint8_t* const staging_ptr = tiles_ptr + STAGES * C_::STAGE_BYTES;
-  uint64_t* const bars = reinterpret_cast<uint64_t*>(staging_ptr + C_::STAGING_BYTES);
-  // barrier layout: full[STAGES], empty[STAGES], acc_full[2], acc_empty[2], drain
-  const uint32_t bar0 = smem_u32(bars);
-  auto full_bar = [&](int s) { return bar0 + 8u * (uint32_t)s; };
-  auto empty_bar = [&](int s) { return bar0 + 8u * (uint32_t)(STAGES + s); };
-  auto accf_bar = [&](int b) { return bar0 + 8u * (uint32_t)(2 * STAGES + b); };
-  auto acce_bar = [&](int b) { return bar0 + 8u * (uint32_t)(2 * STAGES + 2 + b); };
-  const uint32_t drain_bar = bar0 + 8u * (uint32_t)(2 * STAGES + 4);
-  uint32_t* const tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * STAGES + 5);
-  volatile uint32_t* const abort_flag = tmem_slot + 1;
-
-  const int warp = threadIdx.x >> 5;
-  const int lane = threadIdx.x & 31;
-
-  if (threadIdx.x == 0) {
-    for (int s = 0; s < STAGES; ++s) {
-      mbar_init(full_bar(s), 1);
-      mbar_init(empty_bar(s), MODE == 1 ? 2 : 1);
-    }
-    for (int b = 0; b < 2; ++b) {
-      mbar_init(accf_bar(b), 1);
-      // 2-SM pairs: both blocks' epilogues release the accumulator to the
-      // even block's MMA issuer
-      mbar_init(acce_bar(b), TWO_SM ? 256 : 128);
-    }
-    mbar_init(drain_bar, 1);
-    *abort_flag = 0u;
-    fence_mbar_init();
-  }
-  if (warp == 1) {
-    if constexpr (TWO_SM) {
-      tmem_alloc_pair(smem_u32(tmem_slot), (uint32_t)C_::TMEM_COLS);
-      tmem_relinquish_pair();
-    } else {
-      tmem_alloc(smem_u32(tmem_slot), (uint32_t)C_::TMEM_COLS);
-      tmem_relinquish();
-    }
-  }
-  tc_fence_before();
-  if constexpr (PAIR) cluster_sync();  // the peer's barriers exist before any multicast
-  else __syncthreads();
-  tc_fence_after();
-  const uint32_t tmem_base = *tmem_slot;
-
-  const WaitCtl wc{p.status, abort_flag, p.timeout_ns};
-  const int n_units = total_units(p, PAIR);
-
-  if (warp == 0) {
-    // ------------------------------------------------------------ producer
-    if (lane == 0) {
-      tma_prefetch_desc(&tmA);
-      tma_prefetch_desc(&tmB);
-      int stage = 0;
-      uint32_t phase = 0;
-      uint32_t pending = 0, pend_phase = 0;  // per-stage: last load issued / its parity
-      bool first = true;
-      bool ok = true;
-      for (int u = worker; u < n_units && ok; u += workers) {
-        int m0, tn, kbeg, nkb, z, tail;
-        unit_coords<PAIR>(u, p, rank, m0, tn, kbeg, nkb, z, tail);
-        const int n0 = tn * BN;
-        for (int kb = 0; kb < nkb; ++kb) {
-          if (!mbar_wait(empty_bar(stage), phase ^ 1u, wc)) { ok = false; break; }
-          const int k0 = kbeg + kb * BK;
-          const bool skip = first && p.fault_injection == 1;
-          first = false;
-          if (!skip && TWO_SM) {
-            // this block's 128 rows of A and half of B, into its own shared
-            // memory, completing on the even block's `full` barrier
-            const uint32_t sa = tiles_addr + (uint32_t)(stage * C_::STAGE_BYTES);
-            const uint32_t sb = sa + (uint32_t)A_TILE_BYTES;
-            const uint32_t fb = mapa_shared(full_bar(stage), 0u);
-            if (rank == 0) mbar_arrive_expect_tx(full_bar(stage), STAGE_TX);
-            if constexpr (A_MN) {
-              tma_load_2d_pair(sa, &tmA, m0, k0, fb);
-              tma_load_2d_pair(sa + 8192u, &tmA, m0 + 64, k0, fb);
-            } else {
-              tma_load_2d_pair(sa, &tmA, k0, m0, fb);
-            }
-            if constexpr (B_MN) {
-              constexpr int MINE = (C_::B_COLS / 64) / 2;
-#pragma unroll
-              for (int h = 0; h < MINE; ++h)
-                tma_load_2d_pair(sb + (uint32_t)h * 8192u, &tmB, n0 + 64 * (rank * MINE + h), k0, fb);
-            } else {
-              tma_load_2d_pair(sb, &tmB, k0, n0 + rank * (BN / 2), fb);
-            }
-            if (rank == 0) {
-              pending |= 1u << stage;
-              pend_phase = (pend_phase & ~(1u << stage)) | (phase << stage);
-            }
-          } else if (!skip) {
-            const uint32_t sa = tiles_addr + (uint32_t)(stage * C_::STAGE_BYTES);
-            const uint32_t sb = sa + (uint32_t)A_TILE_BYTES;
-            mbar_arrive_expect_tx(full_bar(stage), STAGE_TX);
-            if constexpr (A_MN) {
-              tma_load_2d(sa, &tmA, m0, k0, full_bar(stage));
-              tma_load_2d(sa + 8192u, &tmA, m0 + 64, k0, full_bar(stage));
-            } else {
-              tma_load_2d(sa, &tmA, k0, m0, full_bar(stage));
-            }
-            if constexpr (MODE == 1) {
-              // this block's half of B, written into both blocks of the pair
-              if constexpr (B_MN) {
-                constexpr int ATOMS = C_::B_COLS / 64, MINE = ATOMS / 2;
-#pragma unroll
-                for (int h = rank * MINE; h < (rank + 1) * MINE; ++h)
-                  tma_load_2d_mc(sb + (uint32_t)h * 8192u, &tmB, n0 + 64 * h, k0,
-                                 full_bar(stage), (uint16_t)3u);
-              } else {
-                tma_load_2d_mc(sb + (uint32_t)(rank * (BN / 2) * 128), &tmB, k0,
-                               n0 + rank * (BN / 2), full_bar(stage), (uint16_t)3u);
-              }
-            } else if constexpr (B_MN) {
-#pragma unroll
-              for (int h = 0; h < C_::B_COLS / 64; ++h)
-                tma_load_2d(sb + (uint32_t)h * 8192u, &tmB, n0 + 64 * h, k0, full_bar(stage));
-            } else {
-              tma_load_2d(sb, &tmB, k0, n0, full_bar(stage));
-            }
-            pending |= 1u << stage;
-            pend_phase = (pend_phase & ~(1u << stage)) | (phase << stage);
-          } else {
-            pending &= ~(1u << stage);
-          }
-          if (++stage == STAGES) { stage = 0; phase ^= 1u; }
-        }
-      }
-      // Drain: every load issued must land before the block can exit.
-      for (int s = 0; s < STAGES; ++s)
-        if (pending & (1u << s)) mbar_wait_drain(full_bar(s), (pend_phase >> s) & 1u, p.timeout_ns);
-    }
-  } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer
-    // 2-SM pairs: only the even block issues MMAs
-    if (lane == 0 && (!TWO_SM || rank == 0)) {
-      constexpr uint32_t idesc = make_idesc<BN, A_MN, B_MN, TWO_SM ? 2 * BM : BM>();
-      int stage = 0;
-      uint32_t phase = 0;
-      int it = 0;
-      bool ok = true;
-      for (int u = worker; u < n_units && ok; u += workers, ++it) {
-        int m0, tn, kbeg, nkb, z, tail;
-        unit_coords<PAIR>(u, p, rank, m0, tn, kbeg, nkb, z, tail);
-        const int buf = it & 1;
-        const uint32_t acc_phase = (uint32_t)(it >> 1) & 1u;
-        if (!mbar_wait(acce_bar(buf), acc_phase ^ 1u, wc)) { ok = false; break; }
-        tc_fence_after();
-        const uint32_t d_tmem = tmem_base + (uint32_t)(buf * BN);
-        for (int kb = 0; kb < nkb; ++kb) {
-          if (!mbar_wait(full_bar(stage), phase, wc)) { ok = false; break; }
-          tc_fence_after();
-          const uint32_t sa = tiles_addr + (uint32_t)(stage * C_::STAGE_BYTES);
-          const uint32_t sb = sa + (uint32_t)A_TILE_BYTES;
-#pragma unroll
-          for (int kk = 0; kk < BK / UMMA_K; ++kk) {
-            uint64_t ad, bd;
-            if constexpr (A_MN) ad = make_sdesc(sa + (uint32_t)kk * 2048u, 8192u, 1024u);
-            else ad = make_sdesc(sa + (uint32_t)kk * 32u, 16u, 1024u);
-            if constexpr (B_MN) bd = make_sdesc(sb + (uint32_t)kk * 2048u, 8192u, 1024u);
-            else bd = make_sdesc(sb + (uint32_t)kk * 32u, 16u, 1024u);
-            if constexpr (TWO_SM) tc_mma_f16_pair(d_tmem, ad, bd, idesc, (kb | kk) != 0 ? 1u : 0u);
-            else tc_mma_f16(d_tmem, ad, bd, idesc, (kb | kk) != 0 ? 1u : 0u);
-          }
-          // buffer free once these MMAs finish (in both blocks of a pair)
-          if constexpr (TWO_SM) tc_commit_pair_mc(empty_bar(stage), (uint16_t)3u);
-          else if constexpr (PAIR) tc_commit_mc(empty_bar(stage), (uint16_t)3u);
-          else tc_commit(empty_bar(stage));
-          if (++stage == STAGES) { stage = 0; phase ^= 1u; }
-        }
-        if (!ok) break;
-        // accumulator complete (2-SM pairs: in both blocks' tensor memory)
-        if constexpr (TWO_SM) tc_commit_pair_mc(accf_bar(buf), (uint16_t)3u);
-        else tc_commit(accf_bar(buf));
-      }
-      // Drain: every MMA issued must finish before tensor memory is freed.
-      if constexpr (TWO_SM) tc_commit_pair_mc(drain_bar, (uint16_t)1u);
-      else tc_commit(drain_bar);
-      mbar_wait_drain(drain_bar, 0u, p.timeout_ns);
-    }
-  } else {
-    // ------------------------------------------------------------ epilogue
-    const int q = warp & 3;  // this warp may access TMEM lanes 32q .. 32q+31
-    const int row = q * 32 + lane;
-    int it = 0;
-    for (int u = worker; u < n_units; u += workers, ++it) {
-      int m0, tn, kbeg, nkb, z, tail;
-      unit_coords<PAIR>(u, p, rank, m0, tn, kbeg, nkb, z, tail);
-      const int n0 = tn * BN;
-      const int buf = it & 1;
-      const uint32_t acc_phase = (uint32_t)(it >> 1) & 1u;
-      // one lane waits, the warp follows: the TMEM loads below are
-      // warp-collective, so the whole warp must take the same branch
-      bool got = false;
-      if (lane == 0) got = mbar_wait(accf_bar(buf), acc_phase, wc);
-      got = __shfl_sync(0xffffffffu, got ? 1 : 0, 0) != 0;
-      if (!got) break;
-      tc_fence_after();
-      const int gm = m0 + row;
-      const uint32_t t_row = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(buf * BN);
-      // tail slice: this warp's 32 x BN partial sums for the tile live in a
-      // block of the workspace laid out as the warp holds them -- [chunk c]
-      // [float4 v][lane] -- so every store and load of a warp covers 512
-      // contiguous bytes
-      constexpr int P = PAIR ? 2 : 1;
-      constexpr int STRIP = 32 * BN;  // floats per warp strip
-      float* const tail_strip =
-          tail >= 0 ? p.tail_ws + ((((int64_t)(tail * P + rank) * p.tail_splits + z) * 4 + q) * STRIP)
-                    : nullptr;
-#pragma unroll 1
-      for (int c = 0; c < BN / 32; ++c) {
-        uint32_t r[32];
-        __syncwarp();
-        tmem_ld_32x32b_x32(t_row + (uint32_t)(c * 32), r);
-        tmem_ld_wait();
-        if (c == BN / 32 - 1) {
-          tc_fence_before();
-          // accumulator buffer may be overwritten (2-SM pairs: tell the even
-          // block, whose MMAs write both blocks' tensor memory)
-          if constexpr (TWO_SM) mbar_arrive_cluster(mapa_shared(acce_bar(buf), 0u));
-          else mbar_arrive(acce_bar(buf));
-        }
-        if (tail >= 0) {
-          float4* dst = reinterpret_cast<float4*>(tail_strip) + (c * 8) * 32 + lane;
-#pragma unroll
-          for (int v = 0; v < 8; ++v)
-            dst[v * 32] = make_float4(__uint_as_float(r[4 * v]), __uint_as_float(r[4 * v + 1]),
-                                      __uint_as_float(r[4 * v + 2]), __uint_as_float(r[4 * v + 3]));
-          continue;
-        }
-        const int gn0 = n0 + c * 32;
-        // rows past M: loaded (warp-collective) but not stored; the TMA path
-        // stays warp-uniform and lets the unit clip them
-        if (gm >= p.M && !(p.c_tma && !SPLIT)) continue;
-        if constexpr (SPLIT) {
-          float* dst = p.partial + ((int64_t)z * p.M + gm) * p.N + gn0;
-          if (gn0 + 31 < p.N && (p.N & 3) == 0) {
-#pragma unroll
-            for (int v = 0; v < 8; ++v)
-              reinterpret_cast<float4*>(dst)[v] =
-                  make_float4(__uint_as_float(r[4 * v]), __uint_as_float(r[4 * v + 1]),
-                              __uint_as_float(r[4 * v + 2]), __uint_as_float(r[4 * v + 3]));
-          } else {
-            for (int j = 0; j < 32; ++j)
-              if (gn0 + j < p.N) dst[j] = __uint_as_float(r[j]);
-          }
-        } else if (p.c_tma) {
-          // fp16 row segment -> this warp's staging buffer (64-byte swizzle:
-          // 16-byte chunk w of row l sits at chunk w ^ ((l >> 1) & 3), so the
-          // 8 lanes of each store phase hit distinct banks) -> TMA store of the
-          // 32 x 32 block, clipped by the unit at M and N
-          const uint32_t sbuf = staging_addr + (uint32_t)((q * 2 + (c & 1)) * 2048);
-          if (lane == 0) bulk_wait_read<1>();  // this buffer's previous store has read it
-          __syncwarp();
-#pragma unroll
-          for (int w = 0; w < 4; ++w) {
-            uint4 o;
-            __half2* oh = reinterpret_cast<__half2*>(&o);
-#pragma unroll
-            for (int e = 0; e < 4; ++e)
-              oh[e] = __floats2half2_rn(p.alpha * __uint_as_float(r[8 * w + 2 * e]),
-                                        p.alpha * __uint_as_float(r[8 * w + 2 * e + 1]));
-            const uint32_t dst = sbuf + (uint32_t)(lane * 64 + ((w ^ ((lane >> 1) & 3)) * 16));
-            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(dst), "r"(o.x),
-                         "r"(o.y), "r"(o.z), "r"(o.w)
-                         : "memory");
-          }
-          fence_proxy_async_smem();
-          __syncwarp();
-          // (a block wholly past M or N -- the second tile of a pair on an odd
-          // tile-row count -- is not stored at all)
-          if (lane == 0 && m0 + q * 32 < p.M && gn0 < p.N) {
-            tma_store_2d(&tmC, gn0, m0 + q * 32, sbuf);
-            bulk_commit();
-          }
-        } else {
-          float v[32];
-#pragma unroll
-          for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
-          store_c32(p, gm, gn0, v);
-        }
-      }
-      if (tail >= 0) {
-        // Last slice to arrive for this 32-row strip finishes it: partial
-        // writes are fenced before the arrival, the slices are summed in slice
-        // order (so the result does not depend on which slice came last), and
-        // the counter is left at zero for the next launch.  No waiting on
-        // other blocks is involved.
-        __threadfence();
-        unsigned int old = 0;
-        unsigned int* cnt = p.tail_cnt + (tail * P + rank) * 4 + q;
-        if (lane == 0) old = atomicAdd(cnt, 1u);
-        old = __shfl_sync(0xffffffffu, old, 0);
-        if (old == (unsigned int)(p.tail_splits - 1)) {
-          __threadfence();
-          const float* strip0 =
-              p.tail_ws + (((int64_t)(tail * P + rank) * p.tail_splits * 4 + q) * STRIP);
-          const int64_t slice_stride = 4 * (int64_t)STRIP;
-#pragma unroll 1
-          for (int c = 0; c < BN / 32; ++c) {
-            float v[32];
-#pragma unroll
-            for (int j = 0; j < 32; ++j) v[j] = 0.f;
-            for (int zz = 0; zz < p.tail_splits; ++zz) {
-              const float4* src =
-                  reinterpret_cast<const float4*>(strip0 + zz * slice_stride) + (c * 8) * 32 + lane;
-#pragma unroll
-              for (int w = 0; w < 8; ++w) {
-                const float4 f = __ldcg(src + w * 32);
-                v[4 * w] += f.x; v[4 * w + 1] += f.y; v[4 * w + 2] += f.z; v[4 * w + 3] += f.w;
-              }
-            }
-            if (gm < p.M) store_c32(p, gm, n0 + c * 32, v);
-          }
-          if (lane == 0) atomicExch(cnt, 0u);
-        }
-      }
-    }
-    if (lane == 0) bulk_wait_all();  // C stores complete before the block ends
-  }
-
-  tc_fence_before();
-  // A pair leaves together: the peer's multicast copies and commit arrivals
-  // target this block's shared memory until both are done.
-  if constexpr (PAIR) cluster_sync();
-  else __syncthreads();
-  if (warp == 1) {
-    __syncwarp();
-    tc_fence_after();
-    if constexpr (TWO_SM) tmem_dealloc_pair(tmem_base, (uint32_t)C_::TMEM_COLS);
-    else tmem_dealloc(tmem_base, (uint32_t)C_::TMEM_COLS);
-  }
-}
-
-// ---------------------------------------------------------------- host side
-PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-  static bool tried = false;
-  if (!tried) {
-    tried = true;
-    void* ptr = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000,
-                                         cudaEnableDefault, &q) == cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
-  }
-  return fn;
-}
-
-// 2-D fp16 tensor map over a row-major [rows, cols] array with row pitch
-// `ld` elements; box = box_cols (inner) x box_rows, 128-byte swizzle,
-// out-of-range elements read as zero.
-bool make_map(CUtensorMap* map, const void* base, int64_t rows, int64_t cols, int64_t ld,
-              int box_cols, int box_rows,
-              CUtensorMapSwizzle swizzle = CU_TENSOR_MAP_SWIZZLE_128B) {
-  auto enc = get_encode();
-  if (!enc) return false;
-  cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
-  cuuint64_t strides[1] = {(cuuint64_t)(ld * 2)};
-  cuuint32_t box[2] = {(cuuint32_t)box_cols, (cuuint32_t)box_rows};
-  cuuint32_t estr[2] = {1, 1};
-  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void*>(base), dims,
-                   strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                   swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS;
-}
-
-// How many two-block clusters of the pair kernel can be resident at once
-// (fewer than SMs / 2 when the SMs of a GPC do not all pair up).  Queried once
-// per kernel configuration.
-template <int BN, bool A_MN, bool B_MN, int MODE>
-int pair_slots(int num_sms) {
-  static int n = 0;
-  if (n == 0) {
-    using C_ = Cfg<BN, B_MN, MODE>;
-    auto kern = hgemm_tc_kernel<BN, A_MN, B_MN, false, MODE>;
-    int q = 0;
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             C_::SMEM_BYTES) == cudaSuccess) {
-      cudaLaunchConfig_t cfg = {};
-      cudaLaunchAttribute attr[1];
-      attr[0].id = cudaLaunchAttributeClusterDimension;
-      attr[0].val.clusterDim.x = 2;
-      attr[0].val.clusterDim.y = 1;
-      attr[0].val.clusterDim.z = 1;
-      cfg.gridDim = dim3(2 * (num_sms / 2));
-      cfg.blockDim = dim3(THREADS);
-      cfg.dynamicSmemBytes = C_::SMEM_BYTES;
-      cfg.attrs = attr;
-      cfg.numAttrs = 1;
-      if (cudaOccupancyMaxActiveClusters(&q, kern, &cfg) != cudaSuccess) q = 0;
-    }
-    n = q > 0 ? q : num_sms / 2;
-  }
-  return n;
-}
-
-int host_total_units(const HParams& p, bool pair) {
-  const int tiles = (pair ? (p.tiles_m + 1) / 2 : p.tiles_m) * p.tiles_n;
-  if (p.tail_splits > 0) return p.dp_units + (tiles - p.dp_units) * p.tail_splits;
-  return tiles * p.splits;
-}
-
-template <int BN, bool A_MN, bool B_MN, bool SPLIT, int MODE>
-cudaError_t launch_cfg(const HgemmArgs& a, const HParams& p, LaunchCtx& ctx) {
-  constexpr bool PAIR = MODE != 0;
-  using C_ = Cfg<BN, B_MN, MODE>;
-  CUtensorMap mA, mB;
-  bool ok;
-  if (A_MN) ok = make_map(&mA, a.A, a.K, a.M, a.lda, 64, 64);     // stored [K, M]
-  else ok = make_map(&mA, a.A, a.M, a.K, a.lda, 64, BM);          // stored [M, K]
-  if (!ok) return cudaErrorInvalidValue;
-  if (B_MN) ok = make_map(&mB, a.B, a.K, a.N, a.ldb, 64, 64);     // stored [K, N]
-  else ok = make_map(&mB, a.B, a.N, a.K, a.ldb, 64, PAIR ? BN / 2 : BN);  // stored [N, K]
-  if (!ok) return cudaErrorInvalidValue;
-  // C: row-major [M, N], 32 x 32 boxes, 64-byte swizzle (used only when p.c_tma)
-  CUtensorMap mC;
-  memset(&mC, 0, sizeof(mC));
-  if (p.c_tma && !make_map(&mC, a.C, a.M, a.N, a.ldc, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B))
-    return cudaErrorInvalidValue;
-  auto kern = hgemm_tc_kernel<BN, A_MN, B_MN, SPLIT, MODE>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       C_::SMEM_BYTES);
-  if (e != cudaSuccess) return e;
-  if constexpr (PAIR) {
-    // persistent grid of as many pairs as can be resident at once
-    const int max_pairs = pair_slots<BN, A_MN, B_MN, MODE>(a.num_sms);
-    cudaLaunchConfig_t cfg = {};
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = 2;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.blockDim = dim3(THREADS);
-    cfg.dynamicSmemBytes = C_::SMEM_BYTES;
-    cfg.stream = ctx.stream;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    const int units = host_total_units(p, true);
-    const int pairs = units < max_pairs ? units : max_pairs;
-    cfg.gridDim = dim3(2 * pairs);
-    ctx.grid = 2 * pairs;
-    e = cudaLaunchKernelEx(&cfg, kern, mA, mB, mC, p);
-  } else {
-    const int units = host_total_units(p, false);
-    const int grid = units < a.num_sms ? units : a.num_sms;
-    ctx.grid = grid;
-    kern<<<grid, THREADS, C_::SMEM_BYTES, ctx.stream>>>(mA, mB, mC, p);
-    e = cudaGetLastError();
-  }
-  if (e == cudaSuccess) ctx.launches++;
-  return e;
-}
-
-template <int BN>
-cudaError_t launch_bn(const HgemmArgs& a, const HParams& p, LaunchCtx& ctx) {
-  const bool A_MN = a.transA != 0, B_MN = a.transB == 0, split = a.splits > 1;
-  constexpr bool CAN_PAIR = BN == 128 || BN == 256;
-  constexpr int M1 = CAN_PAIR ? 1 : 0, M2 = CAN_PAIR ? 2 : 0;
-#define GB300_HG(AM, BMN)                                                   \
-  if (A_MN == AM && B_MN == BMN) {                                          \
-    if (split) return launch_cfg<BN, AM, BMN, true, 0>(a, p, ctx);          \
-    if (CAN_PAIR && p.pair == 2) return launch_cfg<BN, AM, BMN, false, M2>(a, p, ctx); \
-    if (CAN_PAIR && p.pair == 1) return launch_cfg<BN, AM, BMN, false, M1>(a, p, ctx); \
-    return launch_cfg<BN, AM, BMN, false, 0>(a, p, ctx);                    \
-  }
-  GB300_HG(false, true)
-  GB300_HG(true, true)
-  GB300_HG(false, false)
-  GB300_HG(true, false)
-#undef GB300_HG
-  return cudaErrorInvalidValue;
-}
-
-}  // namespace
 
 int hgemm_pair_slots(int bn, int transA, int transB, int mode, int num_sms) {
   const bool A_MN = transA != 0, B_MN = transB == 0;
 #define GB300_SLOTS(W, AM, BMN)                                                              \
   if (bn == W && A_MN == AM && B_MN == BMN)                                                  \
-    return mode == 2 ? pair_slots<W, AM, BMN, 2>(num_sms) : pair_slots<W, AM, BMN, 1>(num_sms);
+    return mode == 2 ? pair_slots<__half, W, AM, BMN, 2>(num_sms)                           \
+                     : pair_slots<__half, W, AM, BMN, 1>(num_sms);
   GB300_SLOTS(128, false, true) GB300_SLOTS(128, true, true) GB300_SLOTS(128, false, false)
   GB300_SLOTS(128, true, false) GB300_SLOTS(256, false, true) GB300_SLOTS(256, true, true)
   GB300_SLOTS(256, false, false) GB300_SLOTS(256, true, false)
@@ -784,37 +76,8 @@ int hgemm_pick_bn(int M, int N, int transB, int num_sms) {
 }
 
 cudaError_t launch_hgemm(const HgemmArgs& a, LaunchCtx& ctx) {
-  HParams p;
-  p.C = a.C;
-  p.partial = a.partial;
-  p.ldc = a.ldc;
-  p.M = a.M; p.N = a.N; p.K = a.K;
-  p.splits = a.splits > 1 ? a.splits : 1;
-  p.k_slice = a.splits > 1 ? a.k_slice : ((a.K + BK - 1) / BK) * BK;
-  const int bn = a.bn;
-  p.tiles_m = (a.M + BM - 1) / BM;
-  p.tiles_n = (a.N + bn - 1) / bn;
-  p.alpha = a.alpha; p.beta = a.beta;
-  p.status = ctx.status;
-  p.timeout_ns = ctx.timeout_ns;
-  p.fault_injection = a.fault_injection;
-  p.c_vec_ok = ((reinterpret_cast<uintptr_t>(a.C) & 15u) == 0 && (a.ldc % 8) == 0) ? 1 : 0;
-  p.c_tma = (p.c_vec_ok && a.beta == 0.f && a.splits <= 1 && a.c_tma) ? 1 : 0;
-  p.pair = hgemm_use_pair(bn, a.M, p.splits, a.pair) ? a.pair : 0;
-  p.dp_units = a.dp_units;
-  p.tail_splits = a.tail_splits;
-  p.tail_k_slice = a.tail_k_slice;
-  p.tail_ws = a.tail_ws;
-  p.tail_cnt = a.tail_cnt;
-  if (p.tail_splits > 0 && (p.splits != 1 || !p.tail_ws || !p.tail_cnt)) return cudaErrorInvalidValue;
-  switch (bn) {
-    case 32: return launch_bn<32>(a, p, ctx);
-    case 64: return launch_bn<64>(a, p, ctx);
-    case 128: return launch_bn<128>(a, p, ctx);
-    case 192: return launch_bn<192>(a, p, ctx);
-    case 256: return launch_bn<256>(a, p, ctx);
-    default: return cudaErrorInvalidValue;
-  }
+  if (a.dtype == 2) return launch_hgemm_bf16(a, ctx);
+  return launch_hgemm_t<__half>(a, ctx);
 }
 
 }  // namespace gb300

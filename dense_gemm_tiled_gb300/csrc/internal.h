@@ -25,15 +25,15 @@ struct SgemmArgs {
   float* partial;
 };
 
-// One fp16 tcgen05 GEMM launch.
+// One tcgen05 GEMM launch (fp16 or bf16 operands and output).
 struct HgemmArgs {
   int transA, transB;
   int M, N, K;
-  const __half* A;  // 16-byte aligned base, lda * 2 a multiple of 16
+  const void* A;  // 16-byte aligned base, lda * 2 a multiple of 16
   int64_t lda;
-  const __half* B;
+  const void* B;
   int64_t ldb;
-  __half* C;
+  void* C;
   int64_t ldc;
   float alpha, beta;
   int splits;
@@ -44,6 +44,7 @@ struct HgemmArgs {
   int pair;             // block pairs allowed: 0 none, 1 multicast B, 2 2-SM MMAs
   int c_tma;            // allow TMA stores of C (used when beta == 0 and C is aligned)
   int fault_injection;  // test hook: 1 = producer skips its first stage
+  int dtype = 1;        // 1 fp16, 2 bf16 (gemm_dtype_t)
   // tail split (see hgemm_plan_tail); tail_splits == 0 disables it
   int dp_units = 0, tail_splits = 0, tail_k_slice = 0;
   float* tail_ws = nullptr;
@@ -66,7 +67,8 @@ struct LaunchCtx {
 // Launchers (return cudaSuccess or the launch error).
 cudaError_t launch_sgemm(const SgemmArgs& a, LaunchCtx& ctx);
 cudaError_t launch_hgemm(const HgemmArgs& a, LaunchCtx& ctx);
-// C[M,N] = alpha * sum_z P[z] + beta * C; dtype 0 = fp32 C, 1 = fp16 C.
+cudaError_t launch_hgemm_bf16(const HgemmArgs& a, LaunchCtx& ctx);
+// C[M,N] = alpha * sum_z P[z] + beta * C; dtype 0 = fp32 C, 1 = fp16 C, 2 = bf16 C.
 cudaError_t launch_splitk_reduce(int dtype, int M, int N, int splits, const float* P, void* C,
                                  int64_t ldc, float alpha, float beta, LaunchCtx& ctx);
 // C = beta * C (K == 0); beta == 0 writes zeros.
@@ -75,9 +77,10 @@ cudaError_t launch_scale(int dtype, int M, int N, void* C, int64_t ldc, float be
 // dst[c][r] = src[r][c] (fp32 rows x cols).
 cudaError_t launch_transpose_f32(int rows, int cols, const float* src, int64_t ld_src,
                                  float* dst, int64_t ld_dst, LaunchCtx& ctx);
-// dst[r][c] = src[r][c] for c < cols, 0 for cols <= c < ld_dst (fp16 rows).
-cudaError_t launch_repack_f16(int rows, int cols, const __half* src, int64_t ld_src,
-                              __half* dst, int64_t ld_dst, LaunchCtx& ctx);
+// dst[r][c] = src[r][c] for c < cols, 0 for cols <= c < ld_dst (16-bit elements,
+// fp16 or bf16: +0 is the zero bit pattern in both).
+cudaError_t launch_repack_16(int rows, int cols, const void* src, int64_t ld_src, void* dst,
+                             int64_t ld_dst, LaunchCtx& ctx);
 
 // Tile sizes the dispatcher needs.
 // fp32 block tile: (64 * SG_WARPS_M) x 128, K step 32
@@ -85,7 +88,10 @@ cudaError_t launch_repack_f16(int rows, int cols, const __half* src, int64_t ld_
 #define GB300_SG_WARPS_M 2
 #endif
 constexpr int SG_WARPS_M = GB300_SG_WARPS_M;
-constexpr int SG_BM = 64 * SG_WARPS_M, SG_BN = 128, SG_BK = 32;
+#ifndef GB300_SG_BK
+#define GB300_SG_BK 64
+#endif
+constexpr int SG_BM = 64 * SG_WARPS_M, SG_BN = 128, SG_BK = GB300_SG_BK;
 constexpr int HG_BM = 128, HG_BK = 64;
 int hgemm_pick_bn(int M, int N, int transB, int num_sms);
 bool hgemm_use_pair(int bn, int M, int splits, int allowed);

@@ -23,7 +23,7 @@
 //    coalesced; here every global load is a 16-byte cp.async and a warp's loads
 //    cover whole 64- or 512-byte row segments.
 //
-// Tile: (64 * WARPS_M) x 128 outputs per block, K step 32, 128 * WARPS_M threads
+// Tile: (64 * WARPS_M) x 128 outputs per block, K step 64, 128 * WARPS_M threads
 // (warps WARPS_M x 4, each warp 64 x 32, each lane 8 x 8 outputs split into
 // 4-wide groups), one block per SM.  The inner product runs on Blackwell's
 // paired FP32 FMA (fma.rn.f32x2): one instruction updates two adjacent outputs
@@ -42,22 +42,28 @@ namespace {
 constexpr int BM = SG_BM, BN = SG_BN, BK = SG_BK;
 constexpr int WARPS_M = SG_WARPS_M;          // warps along m (each 64 rows); 4 along n
 constexpr int THREADS = 128 * WARPS_M;
-constexpr int STAGES = 3;
+#ifndef GB300_SG_STAGES
+#define GB300_SG_STAGES 3
+#endif
+constexpr int STAGES = GB300_SG_STAGES;
 constexpr int APAD = BM + 4;  // k-major tile rows padded: conflict-free transposing writes
 constexpr int BPAD = BN + 4;
 constexpr int A_FLOATS = (BM * BK > BK * APAD) ? BM * BK : BK * APAD;
 constexpr int B_FLOATS = BK * BPAD;
 constexpr int STAGE_FLOATS = A_FLOATS + B_FLOATS;
-constexpr int SMEM_BYTES = STAGES * STAGE_FLOATS * 4;
+constexpr int SMEM_BYTES = STAGES * STAGE_FLOATS * 4;  // 195 KiB at BK 64, 3 stages
 // Tile rasterisation: blocks walk GROUP tile-rows column by column, so each B
 // panel is fetched from DRAM once per group while the group's A panels stay in
 // L2.  The host picks GROUP so those A panels take about a quarter of L2
 // (32 MB): measured at 4096^3, 8-row groups read 352 MB from DRAM and 32-row
 // groups (64 MB of A panels) 520 MB -- the L2 is split between the two dies.
 constexpr int64_t RASTER_L2_BYTES = 32ll << 20;
-static_assert(BM == 64 * WARPS_M && BN == 128 && BK == 32, "tile shape");
+static_assert(BM == 64 * WARPS_M && BN == 128 && (BK == 16 || BK == 32 || BK == 64),
+              "tile shape");
 
-// Compile-time tuning knobs (measured on GB300 at 4096^3; the defaults won):
+// Compile-time tuning knobs (measured on GB300 at 4096^3; the defaults won;
+// K step and stage count are GB300_SG_BK in internal.h and GB300_SG_STAGES:
+// 64 x 3 beat 32 x 3, 32 x 4, 64 x 2 and 16 x 6 by 0.4-5 %):
 //  GB300_SG_MIN_BLOCKS  blocks per SM the register budget is sized for
 //  GB300_SG_KC_UNROLL   unrolling of the 4-k chunk loop
 #ifndef GB300_SG_MIN_BLOCKS
@@ -97,19 +103,23 @@ struct Params {
 //                   reading the same k of rows r and r+4 hit distinct banks;
 //                   A stored [M,K] stays in this layout (measured faster than
 //                   transposing it, by copies or through registers).
-__device__ __forceinline__ int a_swz(int row, int chunk) { return chunk ^ ((row >> 2) & 7); }
+// chunk permutation within a row tile row (BK/4 chunks): XOR with (row / 4)
+// modulo the chunk count, at most 8
+constexpr int SWZ_MASK = (BK / 4 < 8 ? BK / 4 : 8) - 1;
+__device__ __forceinline__ int a_swz(int row, int chunk) { return chunk ^ ((row >> 2) & SWZ_MASK); }
 
 // source [R rows][K] (k contiguous) -> row tile of BM rows
 template <bool VEC>
 __device__ __forceinline__ void load_rows(uint32_t dst, const float* __restrict__ g, int64_t ld,
                                           int r0, int R, int k0, int K, int tid) {
   if constexpr (VEC) {
-    constexpr int CHUNKS = BM * (BK / 4);
+    constexpr int CPR = BK / 4;  // 16-byte chunks per row
+    constexpr int CHUNKS = BM * CPR;
 #pragma unroll
     for (int it = 0; it < (CHUNKS + THREADS - 1) / THREADS; ++it) {
       const int q = tid + it * THREADS;
       if (CHUNKS % THREADS != 0 && q >= CHUNKS) break;
-      const int row = q >> 3, c = q & 7;
+      const int row = q / CPR, c = q % CPR;
       const int gr = r0 + row, gk = k0 + c * 4;
       const bool ok = (gr < R) && (gk < K);
       const uint32_t bytes = ok ? (uint32_t)min(4, K - gk) * 4u : 0u;
@@ -122,7 +132,7 @@ __device__ __forceinline__ void load_rows(uint32_t dst, const float* __restrict_
     for (int it = 0; it < (ELEMS + THREADS - 1) / THREADS; ++it) {
       const int e = tid + it * THREADS;
       if (ELEMS % THREADS != 0 && e >= ELEMS) break;
-      const int row = e >> 5, kk = e & 31;
+      const int row = e / BK, kk = e % BK;
       const int gr = r0 + row, gk = k0 + kk;
       const bool ok = (gr < R) && (gk < K);
       const float* src = ok ? g + (int64_t)gr * ld + gk : g;
@@ -222,7 +232,7 @@ __global__ void __launch_bounds__(THREADS, GB300_SG_MIN_BLOCKS) sgemm_ffma_kerne
   const int ty = lane >> 2, tx = lane & 3;
   const int arow = wm + ty * 4;     // lane rows: arow + {0..3}, arow + 32 + {0..3}
   const int bcol = wn + tx * 4;     // lane cols: bcol + {0..3}, bcol + 16 + {0..3}
-  const int aswz = (arow >> 2) & 7; // row-tile chunk permutation, shared by all 8 lane rows
+  const int aswz = (arow >> 2) & SWZ_MASK;  // row-tile chunk permutation, same for all 8 lane rows
 
   // grouped rasterisation of the tile grid (consecutive blocks share B panels
   // within a group of group_m tile-rows)

@@ -7,9 +7,9 @@ same (shape, seed) gives the same bits on every machine.
 Distributions (the workloads' own descriptions; the pages name no generator,
 so torch's CPU generator is the reading taken):
   uniform   i.i.d. U[-1, 1): torch.rand * 2 - 1 in fp32 (exact), then rounded
-            to fp16 (RN-even) for fp16 operands.
-  integer   i.i.d. integers in {-3..3}: exact in fp32 and fp16, so every
-            product and every partial sum at these sizes is exact.
+            (RN-even) to fp16 or bf16 for 16-bit operands.
+  integer   i.i.d. integers in {-3..3}: exact in fp32, fp16 and bf16, so
+            every product and every partial sum at these sizes is exact.
   normal    N(0, std^2) in fp32, then rounded to the operand type: weights
             std 0.02, activations std 1 (the LoRA MLP-block set).
 """
@@ -18,7 +18,7 @@ from typing import List, Optional, Tuple
 
 import torch
 
-DTYPES = {"f32": torch.float32, "f16": torch.float16}
+DTYPES = {"f32": torch.float32, "f16": torch.float16, "bf16": torch.bfloat16}
 
 
 def _gen(seed: int) -> torch.Generator:
@@ -152,12 +152,12 @@ def lora_step_gemms(T=512, d=2048, F=5632, r=32) -> List[LoraGemm]:
     return g
 
 
-def lora_problem(g: LoraGemm, seed: int) -> Problem:
+def lora_problem(g: LoraGemm, seed: int, dtype: str = "f16") -> Problem:
     tA, tB = VARIANTS[g.variant]
-    A = draw(g.a[0], stored_shape(tA, g.M, g.K), seed * 3 + 0, "f16", g.a[1])
-    B = draw(g.b[0], stored_shape(tB, g.K, g.N), seed * 3 + 1, "f16", g.b[1])
-    C_in = normal((g.M, g.N), seed * 3 + 2, 1.0, "f16") if g.beta != 0.0 else None
-    return Problem(g.M, g.N, g.K, tA, tB, "f16", 1.0, g.beta, A, B, C_in, g.name)
+    A = draw(g.a[0], stored_shape(tA, g.M, g.K), seed * 3 + 0, dtype, g.a[1])
+    B = draw(g.b[0], stored_shape(tB, g.K, g.N), seed * 3 + 1, dtype, g.b[1])
+    C_in = normal((g.M, g.N), seed * 3 + 2, 1.0, dtype) if g.beta != 0.0 else None
+    return Problem(g.M, g.N, g.K, tA, tB, dtype, 1.0, g.beta, A, B, C_in, g.name)
 
 
 SWEEP_SQUARES = [256, 512, 1024, 2048, 4096, 8192]

@@ -12,7 +12,7 @@
  *   - fp16 operands, fp32 accumulation and an fp16 result, the regime of
  *     "Metal GEMM Kernels for LoRA Training on Apple Silicon", section 1 (table
  *     of operand/accumulator types) and section 2 (output converted from the
- *     fp32 accumulator on the way out),
+ *     fp32 accumulator on the way out), and the same with bfloat16,
  * in the transpose variants of that page's section 2 variant table:
  *     nn  A[M,K]   @ B[K,N]
  *     tn  A[K,M]^T @ B[K,N]
@@ -62,9 +62,13 @@ extern "C" {
 typedef struct CUstream_st* gemm_stream_t;
 
 typedef enum {
-    GEMM_F32 = 0,        /* A, B, C fp32; fp32 FMA accumulation */
-    GEMM_F16_F32ACC = 1  /* A, B, C fp16 (IEEE binary16); fp32 accumulation;
-                            result rounded to fp16 round-to-nearest-even */
+    GEMM_F32 = 0,         /* A, B, C fp32; fp32 FMA accumulation */
+    GEMM_F16_F32ACC = 1,  /* A, B, C fp16 (IEEE binary16); fp32 accumulation;
+                             result rounded to fp16 round-to-nearest-even */
+    GEMM_BF16_F32ACC = 2  /* A, B, C bfloat16; fp32 accumulation; result
+                             rounded to bfloat16 round-to-nearest-even (the
+                             bfloat16 row of the LoRA page's section 1 type
+                             table, native on these tensor cores) */
 } gemm_dtype_t;
 
 typedef enum {
@@ -117,8 +121,8 @@ int gemm_host(int transA, int transB, int64_t M, int64_t N, int64_t K, int dtype
  * the library holds until the process exits.  Limits:
  *   - a problem whose split-K partials (splits x M x N x 4 bytes) exceed
  *     8 MiB returns GEMM_ERR_UNSUPPORTED without launching anything;
- *   - fp16 operands must have 16-byte aligned bases and row pitches (lda, ldb
- *     multiples of 8), else GEMM_ERR_UNSUPPORTED (padding them would need
+ *   - fp16/bf16 operands must have 16-byte aligned bases and row pitches (lda,
+ *     ldb multiples of 8), else GEMM_ERR_UNSUPPORTED (padding them would need
  *     scratch).
  * The first call on a device looks up the array's device address (a CUDA
  * runtime query, done once per device with that device current); make that
@@ -156,8 +160,8 @@ typedef enum {
     GEMM_PATH_SCALE = 1,       /* K == 0: C = beta * C */
     GEMM_PATH_FFMA = 2,        /* fp32 FFMA tiled kernel */
     GEMM_PATH_FFMA_SPLITK = 3, /* fp32 FFMA kernel over K slices + reduction */
-    GEMM_PATH_TC = 4,          /* fp16 tcgen05 kernel, fused epilogue */
-    GEMM_PATH_TC_SPLITK = 5    /* fp16 tcgen05 kernel over K slices + reduction */
+    GEMM_PATH_TC = 4,          /* fp16/bf16 tcgen05 kernel, fused epilogue */
+    GEMM_PATH_TC_SPLITK = 5    /* fp16/bf16 tcgen05 kernel over K slices + reduction */
 } gemm_path_t;
 
 int gemm_last_path(void);

@@ -20,6 +20,8 @@ from . import build_oracle
 
 F32 = 0
 F16 = 1
+BF16 = 2
+FORMATS = {"f32": F32, "f16": F16, "bf16": BF16}
 
 _lib = None
 
@@ -43,6 +45,10 @@ def bind(path: str):
     lib.oracle_half_array_to_double.restype = None
     lib.oracle_double_array_to_half_rne.argtypes = [vp, vp, i64]
     lib.oracle_double_array_to_half_rne.restype = None
+    lib.oracle_bf16_array_to_double.argtypes = [vp, vp, i64]
+    lib.oracle_bf16_array_to_double.restype = None
+    lib.oracle_double_array_to_bf16_rne.argtypes = [vp, vp, i64]
+    lib.oracle_double_array_to_bf16_rne.restype = None
     return lib
 
 
@@ -60,12 +66,16 @@ def default_threads() -> int:
         return os.cpu_count() or 1
 
 
-def _dtype_code(a: np.ndarray) -> int:
+def _dtype_code(a: np.ndarray, fmt=None) -> int:
+    """Element format of an operand array.  bfloat16 has no numpy dtype: pass
+    its bit patterns as uint16 with fmt='bf16'."""
+    if fmt is not None:
+        return FORMATS[fmt]
     if a.dtype == np.float32:
         return F32
     if a.dtype in (np.float16, np.uint16):
         return F16
-    raise TypeError(f"oracle takes float32 or float16 arrays, got {a.dtype}")
+    raise TypeError(f"oracle takes float32, float16 or (fmt='bf16') uint16 arrays, got {a.dtype}")
 
 
 def _ld(a: np.ndarray) -> int:
@@ -92,7 +102,7 @@ def _shape(transA, transB, A, B):
 
 
 def gemm_ref(A, B, C=None, transA=False, transB=False, alpha=1.0, beta=0.0, threads=None,
-             lib=None):
+             lib=None, fmt=None):
     """(ref, mag) for C_out = alpha*op(A)@op(B) + beta*C, both float64 [M, N].
 
     A, B, C are numpy float32 or float16 arrays (2-D row-major views; an ld
@@ -100,8 +110,8 @@ def gemm_ref(A, B, C=None, transA=False, transB=False, alpha=1.0, beta=0.0, thre
     trans flag is set, i.e. a transposed operand is stored [K, M] / [N, K].
     C is read only when beta != 0.
     """
-    dt = _dtype_code(A)
-    if _dtype_code(B) != dt or (C is not None and _dtype_code(C) != dt):
+    dt = _dtype_code(A, fmt)
+    if _dtype_code(B, fmt) != dt or (C is not None and _dtype_code(C, fmt) != dt):
         raise TypeError("A, B and C must have one dtype")
     M, N, K = _shape(transA, transB, A, B)
     ref = np.empty((M, N), dtype=np.float64)
@@ -120,9 +130,9 @@ def gemm_ref(A, B, C=None, transA=False, transB=False, alpha=1.0, beta=0.0, thre
 
 
 def gemm_ref_points(A, B, rows, cols, C=None, transA=False, transB=False, alpha=1.0, beta=0.0,
-                    threads=None):
+                    threads=None, fmt=None):
     """(ref, mag) at the output positions (rows[p], cols[p]); float64 [npts]."""
-    dt = _dtype_code(A)
+    dt = _dtype_code(A, fmt)
     M, N, K = _shape(transA, transB, A, B)
     rows = np.ascontiguousarray(rows, dtype=np.int64)
     cols = np.ascontiguousarray(cols, dtype=np.int64)
@@ -157,4 +167,20 @@ def round_half_rne(x) -> np.ndarray:
     x = np.ascontiguousarray(x, dtype=np.float64)
     out = np.empty(x.shape, dtype=np.uint16)
     _load().oracle_double_array_to_half_rne(x.ctypes.data, out.ctypes.data, x.size)
+    return out
+
+
+def bf16_to_double(h) -> np.ndarray:
+    """bfloat16 bit patterns (uint16 array) -> float64, exact."""
+    h = np.ascontiguousarray(h).view(np.uint16)
+    out = np.empty(h.shape, dtype=np.float64)
+    _load().oracle_bf16_array_to_double(h.ctypes.data, out.ctypes.data, h.size)
+    return out
+
+
+def round_bf16_rne(x) -> np.ndarray:
+    """float64 -> bfloat16 bit patterns (uint16), round to nearest, ties to even."""
+    x = np.ascontiguousarray(x, dtype=np.float64)
+    out = np.empty(x.shape, dtype=np.uint16)
+    _load().oracle_double_array_to_bf16_rne(x.ctypes.data, out.ctypes.data, x.size)
     return out

@@ -19,11 +19,13 @@
  *     reproduce the plain loop exactly.
  *   - "Metal GEMM Kernels for LoRA Training on Apple Silicon", section 2
  *     "GEMM structure", variant table: nn A[M,K]@B[K,N], tn A[K,M]^T@B[K,N],
- *     nt A[M,K]@B[N,K]^T; fp16 operands with fp32 accumulation (section 1).
+ *     nt A[M,K]@B[N,K]^T; fp16 operands with fp32 accumulation (section 1,
+ *     whose type table also lists bfloat16 operands -- emulated on that GPU,
+ *     native on this one).
  *
- * Arithmetic: every input element is widened exactly to double (fp32 and fp16
- * values are exactly representable in double), every product of two such
- * values is exact in double (at most 24+24 significant bits), and the sum for
+ * Arithmetic: every input element is widened exactly to double (fp32, fp16 and
+ * bfloat16 values are exactly representable in double), every product of two
+ * such values is exact in double (at most 24+24 significant bits), and the sum for
  * each output element is accumulated in double in strict increasing k.  The
  * file is built with -ffp-contract=off so no multiply is fused into an add.
  *
@@ -42,6 +44,7 @@
 
 #define ORACLE_F32 0
 #define ORACLE_F16 1
+#define ORACLE_BF16 2
 
 /* ---------------------------------------------------------------------------
  * IEEE 754 binary16 <-> double, written from the format's definition:
@@ -94,8 +97,42 @@ uint16_t oracle_double_to_half_rne(double x) {
     return (uint16_t)(s | (uint16_t)((e + 15) << 10) | (uint16_t)((int)r - 1024));
 }
 
+/* ---------------------------------------------------------------------------
+ * bfloat16 <-> double.  bfloat16 is the upper half of an IEEE binary32: 1 sign
+ * bit, 8 exponent bits (bias 127), 7 fraction bits.  Widening puts the 16 bits
+ * on top of a binary32 with zero low bits, which is exact.
+ * ------------------------------------------------------------------------- */
+double oracle_bf16_to_double(uint16_t b) {
+    const uint32_t bits = (uint32_t)b << 16;
+    float f;
+    memcpy(&f, &bits, sizeof f);
+    return (double)f;
+}
+
+/* double -> bfloat16, round to nearest, ties to even; overflow gives inf. */
+uint16_t oracle_double_to_bf16_rne(double x) {
+    uint16_t s = signbit(x) ? 0x8000 : 0;
+    if (isnan(x)) return (uint16_t)(s | 0x7fc0);
+    double a = fabs(x);
+    if (a == 0.0) return s;
+    if (isinf(a)) return (uint16_t)(s | 0x7f80);
+    int ex;
+    frexp(a, &ex);
+    int e = ex - 1; /* a in [2^e, 2^(e+1)) */
+    if (e < -126) {
+        /* subnormal range: quantum 2^-133; r == 128 is the smallest normal */
+        double r = rne_integer(ldexp(a, 133));
+        return (uint16_t)(s | (uint16_t)r);
+    }
+    double r = rne_integer(ldexp(a, 7 - e)); /* in [128, 256] */
+    if (r == 256.0) { r = 128.0; e += 1; }
+    if (e > 127) return (uint16_t)(s | 0x7f80);
+    return (uint16_t)(s | (uint16_t)((e + 127) << 7) | (uint16_t)((int)r - 128));
+}
+
 static inline double load_elem(const void* p, int dtype, int64_t idx) {
     if (dtype == ORACLE_F16) return oracle_half_to_double(((const uint16_t*)p)[idx]);
+    if (dtype == ORACLE_BF16) return oracle_bf16_to_double(((const uint16_t*)p)[idx]);
     return (double)((const float*)p)[idx];
 }
 
@@ -173,7 +210,7 @@ int oracle_gemm(int transA, int transB, int64_t M, int64_t N, int64_t K, int dty
                 int64_t ldb, const void* Cin, int64_t ldc, double* ref, double* mag,
                 int nthreads) {
     if (M < 0 || N < 0 || K < 0) return 1;
-    if (dtype != ORACLE_F32 && dtype != ORACLE_F16) return 1;
+    if (dtype != ORACLE_F32 && dtype != ORACLE_F16 && dtype != ORACLE_BF16) return 1;
     if (M == 0 || N == 0) return 0;
     if (!ref || !mag) return 1;
     if (K > 0 && (!A || !B)) return 1;
@@ -262,7 +299,7 @@ int oracle_gemm_points(int transA, int transB, int64_t M, int64_t N, int64_t K, 
                        const int64_t* cols, int64_t npts, double* ref, double* mag,
                        int nthreads) {
     if (M < 0 || N < 0 || K < 0 || npts < 0) return 1;
-    if (dtype != ORACLE_F32 && dtype != ORACLE_F16) return 1;
+    if (dtype != ORACLE_F32 && dtype != ORACLE_F16 && dtype != ORACLE_BF16) return 1;
     if (npts == 0) return 0;
     if (!rows || !cols || !ref || !mag) return 1;
     if (K > 0 && (!A || !B)) return 1;
@@ -292,10 +329,16 @@ int oracle_gemm_points(int transA, int transB, int64_t M, int64_t N, int64_t K, 
     return 0;
 }
 
-/* Elementwise binary16 conversions over arrays (used by the checker). */
+/* Elementwise conversions over arrays (used by the checker). */
 void oracle_half_array_to_double(const uint16_t* h, double* out, int64_t n) {
     for (int64_t i = 0; i < n; ++i) out[i] = oracle_half_to_double(h[i]);
 }
 void oracle_double_array_to_half_rne(const double* x, uint16_t* out, int64_t n) {
     for (int64_t i = 0; i < n; ++i) out[i] = oracle_double_to_half_rne(x[i]);
+}
+void oracle_bf16_array_to_double(const uint16_t* h, double* out, int64_t n) {
+    for (int64_t i = 0; i < n; ++i) out[i] = oracle_bf16_to_double(h[i]);
+}
+void oracle_double_array_to_bf16_rne(const double* x, uint16_t* out, int64_t n) {
+    for (int64_t i = 0; i < n; ++i) out[i] = oracle_double_to_bf16_rne(x[i]);
 }

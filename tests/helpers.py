@@ -27,7 +27,16 @@ def sample_points(M, N, seed, n_random=32768, corner=32):
 
 
 def to_np(t: torch.Tensor) -> np.ndarray:
-    return t.detach().cpu().contiguous().numpy()
+    """CPU numpy view; bfloat16 (no numpy dtype) comes back as uint16 bit
+    patterns, which the oracle reads with fmt='bf16'."""
+    t = t.detach().cpu().contiguous()
+    if t.dtype == torch.bfloat16:
+        return t.view(torch.int16).numpy().view(np.uint16)
+    return t.numpy()
+
+
+def fmt_of(dtype: str):
+    return "bf16" if dtype == "bf16" else None
 
 
 def oracle_for(prob, full=None, seed=0):
@@ -37,13 +46,14 @@ def oracle_for(prob, full=None, seed=0):
     if full is None:
         full = prob.M * prob.N * max(prob.K, 1) <= FULL_LIMIT
     if full:
-        ref, mag = oracle.gemm_ref(A, B, C, prob.transA, prob.transB, prob.alpha, prob.beta)
+        ref, mag = oracle.gemm_ref(A, B, C, prob.transA, prob.transB, prob.alpha, prob.beta,
+                                   fmt=fmt_of(prob.dtype))
         return ref, mag, None
     # fewer random points when each costs a K-long strided dot product
     n_random = 32768 if prob.K <= 4096 else 8192
     rows, cols = sample_points(prob.M, prob.N, seed, n_random=n_random)
     ref, mag = oracle.gemm_ref_points(A, B, rows, cols, C, prob.transA, prob.transB, prob.alpha,
-                                      prob.beta)
+                                      prob.beta, fmt=fmt_of(prob.dtype))
     return ref, mag, (rows, cols)
 
 

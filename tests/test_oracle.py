@@ -117,8 +117,64 @@ def pin_fp16_ties_to_even(lib=None):
     assert np.array_equal(got, want)
 
 
+def pin_bf16_exhaustive(lib=None):
+    """All 65536 bfloat16 patterns widen to the binary32 whose upper half they
+    are (numpy's view of the bits), and rounding that value back returns the
+    same pattern."""
+    h = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    with np.errstate(invalid="ignore"):
+        want = (h.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    l = lib or oracle._load()
+    got = np.empty(65536, dtype=np.float64)
+    l.oracle_bf16_array_to_double(h.ctypes.data, got.ctypes.data, h.size)
+    nan = np.isnan(want)
+    assert np.array_equal(np.isnan(got), nan)
+    assert np.array_equal(got[~nan], want[~nan])
+    assert np.array_equal(np.signbit(got[~nan]), np.signbit(want[~nan]))
+    back = np.empty(65536, dtype=np.uint16)
+    l.oracle_double_array_to_bf16_rne(got.ctypes.data, back.ctypes.data, got.size)
+    assert np.array_equal(back[~nan], h[~nan])
+
+
+def pin_bf16_ties_to_even(lib=None):
+    """Midpoints between adjacent finite bfloat16 values round to the even
+    pattern, and fp32 values round as torch's RN-even float32 -> bfloat16 cast."""
+    import torch
+    l = lib or oracle._load()
+    pos = np.arange(0, 0x7f80, dtype=np.uint32)
+    with np.errstate(invalid="ignore"):
+        vals = (pos << 16).view(np.float32).astype(np.float64)
+    mid = np.concatenate([(vals[:-1] + vals[1:]) / 2, -(vals[:-1] + vals[1:]) / 2])
+    ev = np.where(pos[:-1] % 2 == 0, pos[:-1], pos[1:]).astype(np.uint16)
+    want = np.concatenate([ev, ev | 0x8000]).astype(np.uint16)
+    got = np.empty(mid.size, dtype=np.uint16)
+    l.oracle_double_array_to_bf16_rne(mid.ctypes.data, got.ctypes.data, mid.size)
+    assert np.array_equal(got, want)
+    x = torch.randn(200000, generator=torch.Generator().manual_seed(5)) * \
+        torch.exp2(torch.randint(-140, 120, (200000,), generator=torch.Generator().manual_seed(6)).float())
+    x = x[torch.isfinite(x)]
+    want = x.to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    xd = x.numpy().astype(np.float64)
+    got = np.empty(xd.size, dtype=np.uint16)
+    l.oracle_double_array_to_bf16_rne(xd.ctypes.data, got.ctypes.data, xd.size)
+    assert np.array_equal(got, want)
+
+
+def pin_bf16_integer_exact(lib=None):
+    """bfloat16 small-integer operands: the oracle's product equals numpy's
+    exact int64 matmul."""
+    r = _rng(12)
+    for v, (tA, tB) in VAR.items():
+        A = r.integers(-3, 4, size=(9, 7) if tA else (7, 9))
+        B = r.integers(-3, 4, size=(5, 9) if tB else (9, 5))
+        as_bf16 = lambda a: (a.astype(np.float32).view(np.uint32) >> 16).astype(np.uint16)
+        ref, _ = oracle.gemm_ref(as_bf16(A), as_bf16(B), None, tA, tB, lib=lib, fmt="bf16")
+        want = (A.T if tA else A) @ (B.T if tB else B)
+        assert np.array_equal(ref, want.astype(np.float64)), v
+
+
 PINS = [pin_hand_products, pin_integer_exact, pin_transpose_identity, pin_fp16_exhaustive,
-        pin_fp16_ties_to_even]
+        pin_fp16_ties_to_even, pin_bf16_exhaustive, pin_bf16_ties_to_even, pin_bf16_integer_exact]
 
 
 # ---------------------------------------------------------------------------
@@ -265,6 +321,14 @@ MUTATIONS = {
     "fp16_subnormal_scale": ("v = ldexp((double)f, -24);", "v = ldexp((double)f, -25);"),
     "ties_away_from_zero": ("return (fmod(fl, 2.0) == 0.0) ? fl : fl + 1.0;", "return fl + 1.0;"),
     "rounding_truncates": ("if (d > 0.5) return fl + 1.0;", "if (d > 2.0) return fl + 1.0;"),
+    "bf16_widen_shift": ("const uint32_t bits = (uint32_t)b << 16;",
+                         "const uint32_t bits = (uint32_t)b << 15;"),
+    "bf16_subnormal_scale": ("double r = rne_integer(ldexp(a, 133));",
+                             "double r = rne_integer(ldexp(a, 132));"),
+    "bf16_bias": ("return (uint16_t)(s | (uint16_t)((e + 127) << 7) | (uint16_t)((int)r - 128));",
+                  "return (uint16_t)(s | (uint16_t)((e + 126) << 7) | (uint16_t)((int)r - 128));"),
+    "bf16_read_as_fp16": ("if (dtype == ORACLE_BF16) return oracle_bf16_to_double(((const uint16_t*)p)[idx]);",
+                          "if (dtype == ORACLE_BF16) return oracle_half_to_double(((const uint16_t*)p)[idx]);"),
 }
 
 
