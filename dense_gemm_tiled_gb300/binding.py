@@ -25,6 +25,9 @@ _lib.gemm.argtypes = _GEMM_ARGS
 _lib.gemm.restype = _int
 _lib.gemm_host.argtypes = _GEMM_ARGS
 _lib.gemm_host.restype = _int
+_lib.gemm_strided_batched.argtypes = [_int, _int, _i64, _i64, _i64, _int, _flt, _flt, _vp, _i64,
+                                      _i64, _vp, _i64, _i64, _vp, _i64, _i64, _i64, _vp]
+_lib.gemm_strided_batched.restype = _int
 _lib.gemm_check_device_status.argtypes = [_vp]
 _lib.gemm_check_device_status.restype = _int
 _lib.gemm_status_string.argtypes = [_int]
@@ -43,7 +46,8 @@ F32 = 0
 F16_F32ACC = 1
 BF16_F32ACC = 2
 OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_ALIAS, ERR_CUDA, ERR_NO_MEMORY, ERR_TIMEOUT = range(7)
-PATHS = {0: "none", 1: "scale", 2: "ffma", 3: "ffma_splitk", 4: "tc", 5: "tc_splitk"}
+PATHS = {0: "none", 1: "scale", 2: "ffma", 3: "ffma_splitk", 4: "tc", 5: "tc_splitk",
+         6: "ffma_batched", 7: "tc_batched", 8: "per_entry"}
 
 
 class GemmError(RuntimeError):
@@ -98,6 +102,52 @@ def gemm_host_raw(transA, transB, M, N, K, dtype, alpha, beta, A, lda, B, ldb, C
     return _lib.gemm_host(int(transA), int(transB), int(M), int(N), int(K), int(dtype),
                           float(alpha), float(beta), A or None, int(lda), B or None, int(ldb),
                           C or None, int(ldc), stream or None)
+
+
+def gemm_strided_batched_raw(transA, transB, M, N, K, dtype, alpha, beta, A, lda, strideA, B,
+                             ldb, strideB, C, ldc, strideC, batch, stream=0) -> int:
+    """gemm_strided_batched with plain integers (device addresses, element
+    pitches, stream handle)."""
+    return _lib.gemm_strided_batched(int(transA), int(transB), int(M), int(N), int(K), int(dtype),
+                                     float(alpha), float(beta), A or None, int(lda), int(strideA),
+                                     B or None, int(ldb), int(strideB), C or None, int(ldc),
+                                     int(strideC), int(batch), stream or None)
+
+
+def _batch_pitch(t) -> int:
+    """Element pitch between the matrices of a [batch, rows, cols] tensor (0
+    for a broadcast operand made with expand())."""
+    if t.dim() != 3:
+        raise ValueError("batched operands are 3-D [batch, rows, cols]")
+    return int(t.stride(0)) if t.shape[0] > 1 else 0
+
+
+def gemm_strided_batched(A, B, C, transA=False, transB=False, alpha=1.0, beta=0.0, stream=None):
+    """C[b] = alpha * op(A[b]) @ op(B[b]) + beta * C[b] for every b, in place.
+
+    A, B, C are 3-D CUDA tensors [batch, rows, cols] with contiguous rows; the
+    batch pitch is each tensor's stride(0) (0, via expand(), shares one A or
+    B across the batch).  Shapes per entry as gemm().  Returns C.
+    """
+    import torch
+    if A.dim() != 3 or B.dim() != 3 or C.dim() != 3:
+        raise ValueError("batched operands are 3-D [batch, rows, cols]")
+    batch = int(C.shape[0])
+    if A.shape[0] != batch or B.shape[0] != batch:
+        raise ValueError("A, B and C must have the same batch size")
+    dtype, M, N, K = _dims(A[0], B[0], C[0], transA, transB)
+    for t in (A, B, C):
+        if not t.is_cuda:
+            raise ValueError("gemm_strided_batched() takes CUDA tensors")
+    s = stream if stream is not None else torch.cuda.current_stream(C.device)
+    rc = _lib.gemm_strided_batched(
+        int(transA), int(transB), M, N, K, dtype, float(alpha), float(beta),
+        A.data_ptr() or None, _ld(A[0]), _batch_pitch(A), B.data_ptr() or None, _ld(B[0]),
+        _batch_pitch(B), C.data_ptr() or None, _ld(C[0]), _batch_pitch(C), batch,
+        s.cuda_stream or None)
+    if rc != OK:
+        raise GemmError(rc)
+    return C
 
 
 def _ld(t) -> int:

@@ -117,16 +117,6 @@ __device__ __forceinline__ bool mbar_wait_drain(uint32_t bar, uint32_t parity,
 __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(map) : "memory");
 }
-// 2-D tiled load of the box at coordinates (x = inner, y = outer) into shared
-// memory, completing `bytes` on mbarrier `bar`.
-__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int32_t x,
-                                            int32_t y, uint32_t bar) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
-      " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
-      "l"(map), "r"(x), "r"(y), "r"(bar)
-      : "memory");
-}
 __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
@@ -205,16 +195,6 @@ __device__ __forceinline__ void cluster_sync() {
       "barrier.cluster.arrive.release.aligned;\n\t"
       "barrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
-// 2-D tiled load written to the same shared-memory offset of every block in
-// `mask`, each block's mbarrier at `bar` (same offset) receiving its bytes.
-__device__ __forceinline__ void tma_load_2d_mc(uint32_t dst, const CUtensorMap* map, int32_t x,
-                                               int32_t y, uint32_t bar, uint16_t mask) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
-      ".multicast::cluster [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(dst),
-      "l"(map), "r"(x), "r"(y), "r"(bar), "h"(mask)
-      : "memory");
-}
 // tcgen05.commit arriving on the mbarrier at `bar` in every block of `mask`.
 __device__ __forceinline__ void tc_commit_mc(uint32_t bar, uint16_t mask) {
   asm volatile(
@@ -227,14 +207,6 @@ __device__ __forceinline__ void tc_commit_mc(uint32_t bar, uint16_t mask) {
 
 namespace gb300 {
 // ---------------------------------------------------------------- TMA store
-// 2-D tiled store of the shared-memory box at `src` to coordinates (x, y) of
-// the tensor (clipped to the tensor's extent), in this thread's bulk group.
-__device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, int32_t x, int32_t y,
-                                             uint32_t src) {
-  asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%1, %2}], [%3];" ::"l"(map),
-               "r"(x), "r"(y), "r"(src)
-               : "memory");
-}
 __device__ __forceinline__ void bulk_commit() {
   asm volatile("cp.async.bulk.commit_group;" ::: "memory");
 }
@@ -263,17 +235,6 @@ __device__ __forceinline__ uint32_t mapa_shared(uint32_t addr, uint32_t rank) {
 __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
   asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr)
                : "memory");
-}
-// 2-D tiled load into this block's shared memory whose completion is signalled
-// on the mbarrier at cluster-window address `bar`, which may belong to the
-// peer block of the pair.
-__device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap* map, int32_t x,
-                                                 int32_t y, uint32_t bar) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
-      " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
-      "l"(map), "r"(x), "r"(y), "r"(bar)
-      : "memory");
 }
 // Tensor memory of both blocks of the pair, allocated (and freed) collectively
 // by one warp in each block.
@@ -308,5 +269,50 @@ __device__ __forceinline__ void tc_commit_pair_mc(uint32_t bar, uint16_t mask) {
       " [%0], %1;" ::"r"(bar),
       "h"(mask)
       : "memory");
+}
+}  // namespace gb300
+
+namespace gb300 {
+// ---------------------------------------------------------------- 3-D TMA
+// The GEMM kernels' tensor maps are [batch][rows][cols] (a single matrix is
+// batch 1), so every tile copy names (x = column, y = row, z = batch entry).
+// Tiled load of the box at (x, y, z) into this block's shared memory,
+// completing its bytes on the mbarrier at `bar`.
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, int32_t x,
+                                            int32_t y, int32_t z, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(dst),
+      "l"(map), "r"(x), "r"(y), "r"(z), "r"(bar)
+      : "memory");
+}
+// The same box written to the same shared-memory offset of every block in
+// `mask`, each block's mbarrier at `bar` (same offset) receiving its bytes.
+__device__ __forceinline__ void tma_load_3d_mc(uint32_t dst, const CUtensorMap* map, int32_t x,
+                                               int32_t y, int32_t z, uint32_t bar, uint16_t mask) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes"
+      ".multicast::cluster [%0], [%1, {%2, %3, %4}], [%5], %6;" ::"r"(dst),
+      "l"(map), "r"(x), "r"(y), "r"(z), "r"(bar), "h"(mask)
+      : "memory");
+}
+// Load into this block's shared memory whose completion is signalled on the
+// mbarrier at cluster-window address `bar`, which may belong to the peer
+// block of the pair.
+__device__ __forceinline__ void tma_load_3d_pair(uint32_t dst, const CUtensorMap* map, int32_t x,
+                                                 int32_t y, int32_t z, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(dst),
+      "l"(map), "r"(x), "r"(y), "r"(z), "r"(bar)
+      : "memory");
+}
+// Tiled store of the shared-memory box at `src` to (x, y, z), clipped to the
+// tensor's extent in each dimension, in this thread's bulk group.
+__device__ __forceinline__ void tma_store_3d(const CUtensorMap* map, int32_t x, int32_t y,
+                                             int32_t z, uint32_t src) {
+  asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%1, %2, %3}], [%4];" ::"l"(map),
+               "r"(x), "r"(y), "r"(z), "r"(src)
+               : "memory");
 }
 }  // namespace gb300

@@ -360,9 +360,145 @@ int run_gemm(int transA, int transB, int64_t M64, int64_t N64, int64_t K64, int 
   return GEMM_OK;
 }
 
+// Strided batch (gemm_strided_batched): one launch over the whole batch when
+// the operands allow it, else entry by entry through run_gemm.  Arguments
+// already checked; batch >= 2, M, N > 0.
+int run_batched(int transA, int transB, int64_t M64, int64_t N64, int64_t K64, int dtype,
+                float alpha, float beta, const void* A, int64_t lda, int64_t sA, const void* B,
+                int64_t ldb, int64_t sB, void* C, int64_t ldc, int64_t sC, int64_t batch,
+                cudaStream_t stream, int64_t a_rows, int64_t a_cols, int64_t b_rows,
+                int64_t b_cols) {
+  int dev, sms;
+  unsigned int* status;
+  int rc = device_state(&dev, &status, &sms);
+  if (rc != GEMM_OK) return rc;
+  const int M = (int)M64, N = (int)N64, K = (int)K64;
+  const int64_t es = dtype == GEMM_F32 ? 4 : 2;
+  const char* Ab = static_cast<const char*>(A);
+  const char* Bb = static_cast<const char*>(B);
+  char* Cb = static_cast<char*>(C);
+  const bool tma_ok = dtype != GEMM_F32 && ((uintptr_t)A % 16) == 0 && ((uintptr_t)B % 16) == 0 &&
+                      (lda % 8) == 0 && (ldb % 8) == 0 && (sA % 8) == 0 && (sB % 8) == 0;
+  LaunchCtx ctx{stream, status, (uint64_t)g_timeout_ns.load(), 0};
+  int path = GEMM_PATH_NONE;
+  cudaError_t e = cudaSuccess;
+  bool per_entry = K > 0 && dtype != GEMM_F32 && !tma_ok;
+  if (!per_entry && K > 0 && dtype != GEMM_F32) {
+    // one persistent launch walks (entry, tile) units; the unit count stays
+    // below 2^31 by cutting very large batches into groups
+    path = GEMM_PATH_TC_BATCHED;
+    const int64_t tiles = (int64_t)((M + HG_BM - 1) / HG_BM) * ((N + 31) / 32);
+    const int64_t per_launch = tiles > 0 ? (int64_t)0x7fffffff / tiles : batch;
+    for (int64_t b0 = 0; b0 < batch && e == cudaSuccess; b0 += per_launch) {
+      const int nb = (int)(batch - b0 < per_launch ? batch - b0 : per_launch);
+      int bn = hgemm_pick_bn(M, N, transB, sms, nb);
+      const int forced = forced_bn();
+      if (forced == 32 ? (N <= 32 && transB) : (forced == 64 || forced == 128 || forced == 192 ||
+                                                forced == 256))
+        bn = forced;
+      HgemmArgs a{transA, transB, M, N, K, Ab + b0 * sA * es, lda, Bb + b0 * sB * es, ldb,
+                  Cb + b0 * sC * es, ldc, alpha, beta, 1, 0, nullptr, sms, bn, pair_enabled(),
+                  c_tma_enabled(), g_fault_injection.load()};
+      a.dtype = dtype;
+      a.batch = nb;
+      a.stride_a = sA; a.stride_b = sB; a.stride_c = sC;
+      e = launch_hgemm(a, ctx);
+      // the driver refused the 3-D description (e.g. batch pitches that
+      // interleave rows) before the first launch: run entry by entry
+      if (e == cudaErrorNotSupported && ctx.launches == 0) {
+        per_entry = true;
+        e = cudaSuccess;
+        break;
+      }
+    }
+  }
+  if (per_entry) {
+    // entry by entry: each one is a full gemm() (padded copies included)
+    int64_t launches = 0;
+    for (int64_t b = 0; b < batch; ++b) {
+      rc = run_gemm(transA, transB, M64, N64, K64, dtype, alpha, beta, Ab + b * sA * es, lda,
+                    Bb + b * sB * es, ldb, Cb + b * sC * es, ldc, stream, a_rows, a_cols, b_rows,
+                    b_cols);
+      launches += tl_last_launches;
+      if (rc != GEMM_OK) {
+        tl_last_launches = (int)launches;
+        return rc;
+      }
+    }
+    tl_last_path = GEMM_PATH_PER_ENTRY;
+    tl_last_launches = (int)launches;
+    return GEMM_OK;
+  }
+  if (path == GEMM_PATH_TC_BATCHED) {
+    // launched above
+  } else if (K == 0) {
+    path = GEMM_PATH_SCALE;
+    for (int64_t b = 0; b < batch && e == cudaSuccess; ++b)
+      e = launch_scale(dtype, M, N, Cb + b * sC * es, ldc, beta, ctx);
+  } else if (dtype == GEMM_F32) {
+    // the batch runs on grid.y, at most 65535 entries per launch
+    path = GEMM_PATH_FFMA_BATCHED;
+    for (int64_t b0 = 0; b0 < batch && e == cudaSuccess; b0 += 65535) {
+      const int nb = (int)(batch - b0 < 65535 ? batch - b0 : 65535);
+      SgemmArgs a{transA, transB, M, N, K, (const float*)(Ab + b0 * sA * es), lda,
+                  (const float*)(Bb + b0 * sB * es), ldb, (float*)(Cb + b0 * sC * es), ldc,
+                  alpha, beta, 1, K, nullptr};
+      a.batch = nb;
+      a.stride_a = sA; a.stride_b = sB; a.stride_c = sC;
+      e = launch_sgemm(a, ctx);
+    }
+  }
+  g_total_launches += ctx.launches;
+  tl_last_grid = ctx.grid;
+  tl_last_launches = ctx.launches;
+  if (e != cudaSuccess) {
+    tl_last_path = GEMM_PATH_NONE;
+    return cuda_fail(e);
+  }
+  tl_last_path = path;
+  return GEMM_OK;
+}
+
 }  // namespace
 
 extern "C" {
+
+int gemm_strided_batched(int transA, int transB, int64_t M, int64_t N, int64_t K, int dtype,
+                         float alpha, float beta, const void* A, int64_t lda, int64_t sA,
+                         const void* B, int64_t ldb, int64_t sB, void* C, int64_t ldc,
+                         int64_t sC, int64_t batch, gemm_stream_t stream) {
+  int64_t ar, ac, br, bc;
+  tl_last_path = GEMM_PATH_NONE;
+  tl_last_launches = 0;
+  if (batch < 0 || sA < 0 || sB < 0 || sC < 0) return GEMM_ERR_INVALID_ARG;
+  int rc = check_args(transA, transB, M, N, K, dtype, A, lda, B, ldb, C, ldc, &ar, &ac, &br, &bc);
+  if (rc != GEMM_OK) return rc;
+  if (batch == 0 || M == 0 || N == 0) return GEMM_OK;
+  if (batch >= ((int64_t)1 << 31)) return GEMM_ERR_UNSUPPORTED;
+  if (batch == 1)
+    return run_gemm(transA, transB, M, N, K, dtype, alpha, beta, A, lda, B, ldb, C, ldc,
+                    (cudaStream_t)stream, ar, ac, br, bc);
+  const int64_t es = dtype == GEMM_F32 ? 4 : 2;
+  const int64_t fc = footprint_bytes(M, N, ldc, 1);  // elements of one C
+  if (sC < fc) return GEMM_ERR_ALIAS;                 // C entries would overlap
+  // whole extents, in bytes, without overflow
+  const int64_t big = (int64_t)1 << 62;
+  auto span = [&](int64_t foot, int64_t stride, int64_t* out) {
+    if (stride > 0 && (batch - 1) > (big / es - foot) / stride) return false;
+    *out = ((batch - 1) * stride + foot) * es;
+    return true;
+  };
+  int64_t nC = 0, nA = 0, nB = 0;
+  if (!span(fc, sC, &nC)) return GEMM_ERR_UNSUPPORTED;
+  if (K > 0) {
+    if (!span(footprint_bytes(ar, ac, lda, 1), sA, &nA) ||
+        !span(footprint_bytes(br, bc, ldb, 1), sB, &nB))
+      return GEMM_ERR_UNSUPPORTED;
+    if (overlaps(C, nC, A, nA) || overlaps(C, nC, B, nB)) return GEMM_ERR_ALIAS;
+  }
+  return run_batched(transA, transB, M, N, K, dtype, alpha, beta, A, lda, sA, B, ldb, sB, C, ldc,
+                     sC, batch, (cudaStream_t)stream, ar, ac, br, bc);
+}
 
 int gemm(int transA, int transB, int64_t M, int64_t N, int64_t K, int dtype, float alpha,
          float beta, const void* A, int64_t lda, const void* B, int64_t ldb, void* C,

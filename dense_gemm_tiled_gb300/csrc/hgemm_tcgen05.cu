@@ -50,7 +50,7 @@ TailPlan hgemm_plan_tail(int M, int N, int K, int bn, bool pair, int workers) {
   return t;
 }
 
-int hgemm_pick_bn(int M, int N, int transB, int num_sms) {
+int hgemm_pick_bn(int M, int N, int transB, int num_sms, int batch) {
   // An MN-major B (transB == 0) is staged in 64-column swizzle atoms, so its
   // narrowest tile is 64 columns; a K-major B can go down to 32.
   if (N <= 32 && transB) return 32;
@@ -61,7 +61,8 @@ int hgemm_pick_bn(int M, int N, int transB, int num_sms) {
   // at 4096^3 with 2-SM pairs: 0.85 (BN 128), 0.92 (BN 192), 1.0 (BN 256) --
   // narrower tiles re-read A more often per flop.  Pick the cheapest; ties go
   // to the wider tile.
-  const int64_t tm = (M + BM - 1) / BM;
+  // (a strided batch multiplies the tile count: its entries share the rounds)
+  const int64_t tm = (int64_t)((M + BM - 1) / BM) * (batch > 1 ? batch : 1);
   const int widths[3] = {256, 192, 128};
   const double round_cost[3] = {1.0, 0.92, 0.85};
   int best = 256;

@@ -125,6 +125,11 @@ struct HParams {
   // writing fp32 partials to tail_ws; per 32-row strip the last slice to
   // arrive (tail_cnt) sums all slices in slice order and runs the epilogue.
   int dp_units, tail_splits, tail_k_slice;
+  // strided batch: units run over batch x tiles (no K split, no tail split);
+  // the tensor maps carry the batch as their third coordinate
+  int batch;
+  int64_t stride_c;  // elements between consecutive C matrices
+  int za_mask, zb_mask;  // -1: operand batched; 0: one matrix shared by all (pitch 0)
   float* tail_ws;          // [tail tiles][pair ? 2 : 1][tail_splits][4 warps][32 x BN]
   unsigned int* tail_cnt;  // [tail tiles][pair ? 2 : 1][4], zero on entry and on exit
 };
@@ -162,7 +167,7 @@ __device__ __forceinline__ constexpr uint32_t make_idesc() {
 //  * otherwise: unit = whole tile.
 template <bool PAIR>
 __device__ __forceinline__ void unit_coords(int u, const HParams& p, int rank, int& m0, int& tn,
-                                            int& kbeg, int& nkb, int& z, int& tail) {
+                                            int& kbeg, int& nkb, int& z, int& tail, int& bz) {
   const int rows = PAIR ? (p.tiles_m + 1) / 2 : p.tiles_m;
   const int tiles = rows * p.tiles_n;
   int t, ks;
@@ -179,6 +184,12 @@ __device__ __forceinline__ void unit_coords(int u, const HParams& p, int rank, i
     t = u - z * tiles;
     ks = p.k_slice;
   }
+  // a batched launch has no K split: the outer index is the batch entry
+  bz = 0;
+  if (p.batch > 1) {
+    bz = z;
+    z = 0;
+  }
   const int per_group = GROUP_M * p.tiles_n;
   const int first_m = (t / per_group) * GROUP_M;
   const int gsize = min(rows - first_m, GROUP_M);
@@ -194,14 +205,15 @@ __device__ __forceinline__ void unit_coords(int u, const HParams& p, int rank, i
 __device__ __forceinline__ int total_units(const HParams& p, bool pair) {
   const int tiles = (pair ? (p.tiles_m + 1) / 2 : p.tiles_m) * p.tiles_n;
   if (p.tail_splits > 0) return p.dp_units + (tiles - p.dp_units) * p.tail_splits;
-  return tiles * p.splits;
+  return tiles * p.splits * (p.batch > 1 ? p.batch : 1);
 }
 
 // alpha * v + beta * C_old -> T (RN-even) -> C, for 32 columns of one row
 template <typename T>
-__device__ __forceinline__ void store_c32(const HParams& p, int gm, int gn0, float (&v)[32]) {
+__device__ __forceinline__ void store_c32(const HParams& p, int bz, int gm, int gn0,
+                                          float (&v)[32]) {
   using E = Elem<T>;
-  T* dst = static_cast<T*>(p.C) + (int64_t)gm * p.ldc + gn0;
+  T* dst = static_cast<T*>(p.C) + (int64_t)bz * p.stride_c + (int64_t)gm * p.ldc + gn0;
 #pragma unroll
   for (int j = 0; j < 32; ++j) v[j] = p.alpha * v[j];
   const bool full = (gn0 + 31 < p.N) && p.c_vec_ok;
@@ -324,8 +336,9 @@ __global__ void __launch_bounds__(THREADS, 1)
       bool first = true;
       bool ok = true;
       for (int u = worker; u < n_units && ok; u += workers) {
-        int m0, tn, kbeg, nkb, z, tail;
-        unit_coords<PAIR>(u, p, rank, m0, tn, kbeg, nkb, z, tail);
+        int m0, tn, kbeg, nkb, z, tail, bz;
+        unit_coords<PAIR>(u, p, rank, m0, tn, kbeg, nkb, z, tail, bz);
+        const int za = bz & p.za_mask, zb = bz & p.zb_mask;
         const int n0 = tn * BN;
         for (int kb = 0; kb < nkb; ++kb) {
           if (!mbar_wait(empty_bar(stage), phase ^ 1u, wc)) { ok = false; break; }
@@ -340,18 +353,18 @@ __global__ void __launch_bounds__(THREADS, 1)
             const uint32_t fb = mapa_shared(full_bar(stage), 0u);
             if (rank == 0) mbar_arrive_expect_tx(full_bar(stage), STAGE_TX);
             if constexpr (A_MN) {
-              tma_load_2d_pair(sa, &tmA, m0, k0, fb);
-              tma_load_2d_pair(sa + 8192u, &tmA, m0 + 64, k0, fb);
+              tma_load_3d_pair(sa, &tmA, m0, k0, za, fb);
+              tma_load_3d_pair(sa + 8192u, &tmA, m0 + 64, k0, za, fb);
             } else {
-              tma_load_2d_pair(sa, &tmA, k0, m0, fb);
+              tma_load_3d_pair(sa, &tmA, k0, m0, za, fb);
             }
             if constexpr (B_MN) {
               constexpr int MINE = (C_::B_COLS / 64) / 2;
 #pragma unroll
               for (int h = 0; h < MINE; ++h)
-                tma_load_2d_pair(sb + (uint32_t)h * 8192u, &tmB, n0 + 64 * (rank * MINE + h), k0, fb);
+                tma_load_3d_pair(sb + (uint32_t)h * 8192u, &tmB, n0 + 64 * (rank * MINE + h), k0, zb, fb);
             } else {
-              tma_load_2d_pair(sb, &tmB, k0, n0 + rank * (BN / 2), fb);
+              tma_load_3d_pair(sb, &tmB, k0, n0 + rank * (BN / 2), zb, fb);
             }
             if (rank == 0) {
               pending |= 1u << stage;
@@ -362,10 +375,10 @@ __global__ void __launch_bounds__(THREADS, 1)
             const uint32_t sb = sa + (uint32_t)A_TILE_BYTES;
             mbar_arrive_expect_tx(full_bar(stage), STAGE_TX);
             if constexpr (A_MN) {
-              tma_load_2d(sa, &tmA, m0, k0, full_bar(stage));
-              tma_load_2d(sa + 8192u, &tmA, m0 + 64, k0, full_bar(stage));
+              tma_load_3d(sa, &tmA, m0, k0, za, full_bar(stage));
+              tma_load_3d(sa + 8192u, &tmA, m0 + 64, k0, za, full_bar(stage));
             } else {
-              tma_load_2d(sa, &tmA, k0, m0, full_bar(stage));
+              tma_load_3d(sa, &tmA, k0, m0, za, full_bar(stage));
             }
             if constexpr (MODE == 1) {
               // this block's half of B, written into both blocks of the pair
@@ -373,18 +386,18 @@ __global__ void __launch_bounds__(THREADS, 1)
                 constexpr int ATOMS = C_::B_COLS / 64, MINE = ATOMS / 2;
 #pragma unroll
                 for (int h = rank * MINE; h < (rank + 1) * MINE; ++h)
-                  tma_load_2d_mc(sb + (uint32_t)h * 8192u, &tmB, n0 + 64 * h, k0,
+                  tma_load_3d_mc(sb + (uint32_t)h * 8192u, &tmB, n0 + 64 * h, k0, zb,
                                  full_bar(stage), (uint16_t)3u);
               } else {
-                tma_load_2d_mc(sb + (uint32_t)(rank * (BN / 2) * 128), &tmB, k0,
-                               n0 + rank * (BN / 2), full_bar(stage), (uint16_t)3u);
+                tma_load_3d_mc(sb + (uint32_t)(rank * (BN / 2) * 128), &tmB, k0,
+                               n0 + rank * (BN / 2), zb, full_bar(stage), (uint16_t)3u);
               }
             } else if constexpr (B_MN) {
 #pragma unroll
               for (int h = 0; h < C_::B_COLS / 64; ++h)
-                tma_load_2d(sb + (uint32_t)h * 8192u, &tmB, n0 + 64 * h, k0, full_bar(stage));
+                tma_load_3d(sb + (uint32_t)h * 8192u, &tmB, n0 + 64 * h, k0, zb, full_bar(stage));
             } else {
-              tma_load_2d(sb, &tmB, k0, n0, full_bar(stage));
+              tma_load_3d(sb, &tmB, k0, n0, zb, full_bar(stage));
             }
             pending |= 1u << stage;
             pend_phase = (pend_phase & ~(1u << stage)) | (phase << stage);
@@ -408,8 +421,8 @@ __global__ void __launch_bounds__(THREADS, 1)
       int it = 0;
       bool ok = true;
       for (int u = worker; u < n_units && ok; u += workers, ++it) {
-        int m0, tn, kbeg, nkb, z, tail;
-        unit_coords<PAIR>(u, p, rank, m0, tn, kbeg, nkb, z, tail);
+        int m0, tn, kbeg, nkb, z, tail, bz;
+        unit_coords<PAIR>(u, p, rank, m0, tn, kbeg, nkb, z, tail, bz);
         const int buf = it & 1;
         const uint32_t acc_phase = (uint32_t)(it >> 1) & 1u;
         if (!mbar_wait(acce_bar(buf), acc_phase ^ 1u, wc)) { ok = false; break; }
@@ -452,8 +465,8 @@ __global__ void __launch_bounds__(THREADS, 1)
     const int row = q * 32 + lane;
     int it = 0;
     for (int u = worker; u < n_units; u += workers, ++it) {
-      int m0, tn, kbeg, nkb, z, tail;
-      unit_coords<PAIR>(u, p, rank, m0, tn, kbeg, nkb, z, tail);
+      int m0, tn, kbeg, nkb, z, tail, bz;
+      unit_coords<PAIR>(u, p, rank, m0, tn, kbeg, nkb, z, tail, bz);
       const int n0 = tn * BN;
       const int buf = it & 1;
       const uint32_t acc_phase = (uint32_t)(it >> 1) & 1u;
@@ -538,14 +551,14 @@ __global__ void __launch_bounds__(THREADS, 1)
           // (a block wholly past M or N -- the second tile of a pair on an odd
           // tile-row count -- is not stored at all)
           if (lane == 0 && m0 + q * 32 < p.M && gn0 < p.N) {
-            tma_store_2d(&tmC, gn0, m0 + q * 32, sbuf);
+            tma_store_3d(&tmC, gn0, m0 + q * 32, bz, sbuf);
             bulk_commit();
           }
         } else {
           float v[32];
 #pragma unroll
           for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
-          store_c32<T>(p, gm, gn0, v);
+          store_c32<T>(p, bz, gm, gn0, v);
         }
       }
       if (tail >= 0) {
@@ -578,7 +591,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                 v[4 * w] += f.x; v[4 * w + 1] += f.y; v[4 * w + 2] += f.z; v[4 * w + 3] += f.w;
               }
             }
-            if (gm < p.M) store_c32<T>(p, gm, n0 + c * 32, v);
+            if (gm < p.M) store_c32<T>(p, bz, gm, n0 + c * 32, v);
           }
           if (lane == 0) atomicExch(cnt, 0u);
         }
@@ -616,19 +629,24 @@ PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
   return fn;
 }
 
-// 2-D fp16 tensor map over a row-major [rows, cols] array with row pitch
-// `ld` elements; box = box_cols (inner) x box_rows, 128-byte swizzle,
-// out-of-range elements read as zero.
+// 3-D tensor map over `batch` row-major [rows, cols] 16-bit matrices with row
+// pitch `ld` and batch pitch `stride` elements; box = box_cols (inner) x
+// box_rows x 1, 128-byte swizzle by default, out-of-range elements read as
+// zero.  Returns false when the driver rejects the description (the launch
+// then reports cudaErrorNotSupported and nothing runs).
 bool make_map(CUtensorMap* map, CUtensorMapDataType type, const void* base, int64_t rows,
               int64_t cols, int64_t ld, int box_cols, int box_rows,
-              CUtensorMapSwizzle swizzle = CU_TENSOR_MAP_SWIZZLE_128B) {
+              CUtensorMapSwizzle swizzle = CU_TENSOR_MAP_SWIZZLE_128B, int64_t batch = 1,
+              int64_t stride = 0) {
   auto enc = get_encode();
   if (!enc) return false;
-  cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
-  cuuint64_t strides[1] = {(cuuint64_t)(ld * 2)};
-  cuuint32_t box[2] = {(cuuint32_t)box_cols, (cuuint32_t)box_rows};
-  cuuint32_t estr[2] = {1, 1};
-  CUresult r = enc(map, type, 2, const_cast<void*>(base), dims,
+  // [batch][rows][cols]; a single matrix is batch 1 with a nominal pitch
+  if (batch <= 1) stride = ld * (rows > 0 ? rows : 1);
+  cuuint64_t dims[3] = {(cuuint64_t)cols, (cuuint64_t)rows, (cuuint64_t)(batch > 1 ? batch : 1)};
+  cuuint64_t strides[2] = {(cuuint64_t)(ld * 2), (cuuint64_t)(stride * 2)};
+  cuuint32_t box[3] = {(cuuint32_t)box_cols, (cuuint32_t)box_rows, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = enc(map, type, 3, const_cast<void*>(base), dims,
                    strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                    swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
@@ -668,7 +686,7 @@ int pair_slots(int num_sms) {
 int host_total_units(const HParams& p, bool pair) {
   const int tiles = (pair ? (p.tiles_m + 1) / 2 : p.tiles_m) * p.tiles_n;
   if (p.tail_splits > 0) return p.dp_units + (tiles - p.dp_units) * p.tail_splits;
-  return tiles * p.splits;
+  return tiles * p.splits * (p.batch > 1 ? p.batch : 1);
 }
 
 template <typename T, int BN, bool A_MN, bool B_MN, bool SPLIT, int MODE>
@@ -678,17 +696,22 @@ cudaError_t launch_cfg(const HgemmArgs& a, const HParams& p, LaunchCtx& ctx) {
   using C_ = Cfg<BN, B_MN, MODE>;
   CUtensorMap mA, mB;
   bool ok;
-  if (A_MN) ok = make_map(&mA, TY, a.A, a.K, a.M, a.lda, 64, 64);     // stored [K, M]
-  else ok = make_map(&mA, TY, a.A, a.M, a.K, a.lda, 64, BM);          // stored [M, K]
-  if (!ok) return cudaErrorInvalidValue;
-  if (B_MN) ok = make_map(&mB, TY, a.B, a.K, a.N, a.ldb, 64, 64);     // stored [K, N]
-  else ok = make_map(&mB, TY, a.B, a.N, a.K, a.ldb, 64, PAIR ? BN / 2 : BN);  // stored [N, K]
-  if (!ok) return cudaErrorInvalidValue;
+  const CUtensorMapSwizzle SW = CU_TENSOR_MAP_SWIZZLE_128B;
+  // a pitch-0 operand is one matrix shared by every batch entry (z stays 0)
+  const int64_t nba = p.za_mask ? a.batch : 1, nbb = p.zb_mask ? a.batch : 1;
+  if (A_MN) ok = make_map(&mA, TY, a.A, a.K, a.M, a.lda, 64, 64, SW, nba, a.stride_a);  // [K, M]
+  else ok = make_map(&mA, TY, a.A, a.M, a.K, a.lda, 64, BM, SW, nba, a.stride_a);       // [M, K]
+  if (!ok) return cudaErrorNotSupported;
+  if (B_MN) ok = make_map(&mB, TY, a.B, a.K, a.N, a.ldb, 64, 64, SW, nbb, a.stride_b);  // [K, N]
+  else ok = make_map(&mB, TY, a.B, a.N, a.K, a.ldb, 64, PAIR ? BN / 2 : BN, SW, nbb,
+                     a.stride_b);                                                          // [N, K]
+  if (!ok) return cudaErrorNotSupported;
   // C: row-major [M, N], 32 x 32 boxes, 64-byte swizzle (used only when p.c_tma)
   CUtensorMap mC;
   memset(&mC, 0, sizeof(mC));
-  if (p.c_tma && !make_map(&mC, TY, a.C, a.M, a.N, a.ldc, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B))
-    return cudaErrorInvalidValue;
+  if (p.c_tma && !make_map(&mC, TY, a.C, a.M, a.N, a.ldc, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B,
+                           p.batch, p.stride_c))
+    return cudaErrorNotSupported;
   auto kern = hgemm_tc_kernel<T, BN, A_MN, B_MN, SPLIT, MODE>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        C_::SMEM_BYTES);
@@ -761,7 +784,8 @@ cudaError_t launch_hgemm_t(const HgemmArgs& a, LaunchCtx& ctx) {
   p.status = ctx.status;
   p.timeout_ns = ctx.timeout_ns;
   p.fault_injection = a.fault_injection;
-  p.c_vec_ok = ((reinterpret_cast<uintptr_t>(a.C) & 15u) == 0 && (a.ldc % 8) == 0) ? 1 : 0;
+  p.c_vec_ok = ((reinterpret_cast<uintptr_t>(a.C) & 15u) == 0 && (a.ldc % 8) == 0 &&
+                (a.batch <= 1 || (a.stride_c % 8) == 0)) ? 1 : 0;
   p.c_tma = (p.c_vec_ok && a.beta == 0.f && a.splits <= 1 && a.c_tma) ? 1 : 0;
   p.pair = hgemm_use_pair(bn, a.M, p.splits, a.pair) ? a.pair : 0;
   p.dp_units = a.dp_units;
@@ -769,7 +793,12 @@ cudaError_t launch_hgemm_t(const HgemmArgs& a, LaunchCtx& ctx) {
   p.tail_k_slice = a.tail_k_slice;
   p.tail_ws = a.tail_ws;
   p.tail_cnt = a.tail_cnt;
+  p.batch = a.batch > 1 ? a.batch : 1;
+  p.stride_c = p.batch > 1 ? a.stride_c : 0;
+  p.za_mask = (p.batch > 1 && a.stride_a != 0) ? -1 : 0;
+  p.zb_mask = (p.batch > 1 && a.stride_b != 0) ? -1 : 0;
   if (p.tail_splits > 0 && (p.splits != 1 || !p.tail_ws || !p.tail_cnt)) return cudaErrorInvalidValue;
+  if (p.batch > 1 && (p.splits != 1 || p.tail_splits > 0)) return cudaErrorInvalidValue;
   switch (bn) {
     case 32: return launch_bn<T, 32>(a, p, ctx);
     case 64: return launch_bn<T, 64>(a, p, ctx);

@@ -23,6 +23,10 @@ struct SgemmArgs {
   int splits;
   int k_slice;
   float* partial;
+  // strided batch (batch > 1, at most 65535, no split): matrix y of the batch
+  // is A + y*stride_a, B + y*stride_b, C + y*stride_c (elements)
+  int batch = 1;
+  int64_t stride_a = 0, stride_b = 0, stride_c = 0;
 };
 
 // One tcgen05 GEMM launch (fp16 or bf16 operands and output).
@@ -45,6 +49,10 @@ struct HgemmArgs {
   int c_tma;            // allow TMA stores of C (used when beta == 0 and C is aligned)
   int fault_injection;  // test hook: 1 = producer skips its first stage
   int dtype = 1;        // 1 fp16, 2 bf16 (gemm_dtype_t)
+  // strided batch (batch > 1: no split, no tail): element pitches between
+  // consecutive matrices; 16-bit TMA needs them (and ld) multiples of 8
+  int batch = 1;
+  int64_t stride_a = 0, stride_b = 0, stride_c = 0;
   // tail split (see hgemm_plan_tail); tail_splits == 0 disables it
   int dp_units = 0, tail_splits = 0, tail_k_slice = 0;
   float* tail_ws = nullptr;
@@ -93,7 +101,7 @@ constexpr int SG_WARPS_M = GB300_SG_WARPS_M;
 #endif
 constexpr int SG_BM = 64 * SG_WARPS_M, SG_BN = 128, SG_BK = GB300_SG_BK;
 constexpr int HG_BM = 128, HG_BK = 64;
-int hgemm_pick_bn(int M, int N, int transB, int num_sms);
+int hgemm_pick_bn(int M, int N, int transB, int num_sms, int batch = 1);
 bool hgemm_use_pair(int bn, int M, int splits, int allowed);
 int hgemm_pair_slots(int bn, int transA, int transB, int mode, int num_sms);
 TailPlan hgemm_plan_tail(int M, int N, int K, int bn, bool pair, int workers);

@@ -85,6 +85,9 @@ struct Params {
   int tiles_m, tiles_n;
   int group_m;  // tile-rows per rasterisation group
   float alpha, beta;
+  // strided batch: blockIdx.y selects matrices A + y*stride_a, B + y*stride_b,
+  // C + y*stride_c (all zero for a single GEMM)
+  int64_t stride_a, stride_b, stride_c;
 };
 
 // ---------------------------------------------------------------- staging
@@ -244,6 +247,8 @@ __global__ void __launch_bounds__(THREADS, GB300_SG_MIN_BLOCKS) sgemm_ffma_kerne
   const int tn = (bid % per_group) / gsize;
   const int m0 = tm * BM, n0 = tn * BN;
 
+  const float* const Ag = p.A + (int64_t)blockIdx.y * p.stride_a;
+  const float* const Bg = p.B + (int64_t)blockIdx.y * p.stride_b;
   const int kbeg = blockIdx.z * p.k_slice;
   const int kend = min(p.K, kbeg + p.k_slice);
   const int nk = (kend - kbeg + BK - 1) / BK;
@@ -251,11 +256,11 @@ __global__ void __launch_bounds__(THREADS, GB300_SG_MIN_BLOCKS) sgemm_ffma_kerne
   const uint32_t sbase = smem_u32(smem);
   auto stage_load = [&](int s, int k0) {
     const uint32_t st = sbase + (uint32_t)(s * STAGE_FLOATS) * 4u;
-    if constexpr (A_K) load_rows<VEC>(st, p.A, p.lda, m0, p.M, k0, kend, tid);
-    else load_kmajor<VEC, BM, APAD>(st, p.A, p.lda, m0, p.M, k0, kend, tid);
+    if constexpr (A_K) load_rows<VEC>(st, Ag, p.lda, m0, p.M, k0, kend, tid);
+    else load_kmajor<VEC, BM, APAD>(st, Ag, p.lda, m0, p.M, k0, kend, tid);
     const uint32_t sb = st + A_FLOATS * 4u;
-    if constexpr (B_K) load_transpose<BN, BPAD>(sb, p.B, p.ldb, n0, p.N, k0, kend, tid);
-    else load_kmajor<VEC, BN, BPAD>(sb, p.B, p.ldb, n0, p.N, k0, kend, tid);
+    if constexpr (B_K) load_transpose<BN, BPAD>(sb, Bg, p.ldb, n0, p.N, k0, kend, tid);
+    else load_kmajor<VEC, BN, BPAD>(sb, Bg, p.ldb, n0, p.N, k0, kend, tid);
   };
 
   // acc[i][jp] holds the outputs (row i, columns 2jp and 2jp+1) as a pair
@@ -341,7 +346,7 @@ __global__ void __launch_bounds__(THREADS, GB300_SG_MIN_BLOCKS) sgemm_ffma_kerne
             if (gn + j < p.N) dst[j] = v[j];
         }
       } else {
-        float* dst = p.C + (int64_t)gm * p.ldc + gn;
+        float* dst = p.C + (int64_t)blockIdx.y * p.stride_c + (int64_t)gm * p.ldc + gn;
         const bool vec_ok = VEC && (gn + 3 < p.N);
         if (vec_ok) {
           float4 o;
@@ -407,13 +412,19 @@ cudaError_t launch_sgemm(const SgemmArgs& a, LaunchCtx& ctx) {
     p.group_m = (int)g;
   }
   p.alpha = a.alpha; p.beta = a.beta;
-  // 16-byte staging needs 16-byte aligned rows in every operand (C too: the
-  // epilogue's float4 accesses share the flag).
+  const int batch = a.batch > 1 ? a.batch : 1;
+  if (batch > 1 && (a.splits > 1 || batch > 65535)) return cudaErrorInvalidValue;
+  p.stride_a = batch > 1 ? a.stride_a : 0;
+  p.stride_b = batch > 1 ? a.stride_b : 0;
+  p.stride_c = batch > 1 ? a.stride_c : 0;
+  // 16-byte staging needs 16-byte aligned rows in every operand and every
+  // batch entry (C too: the epilogue's float4 accesses share the flag).
   const bool vec = ((reinterpret_cast<uintptr_t>(a.A) | reinterpret_cast<uintptr_t>(a.B) |
                      reinterpret_cast<uintptr_t>(a.C)) & 15u) == 0 &&
-                   (a.lda % 4) == 0 && (a.ldb % 4) == 0 && (a.ldc % 4) == 0;
+                   (a.lda % 4) == 0 && (a.ldb % 4) == 0 && (a.ldc % 4) == 0 &&
+                   (p.stride_a % 4) == 0 && (p.stride_b % 4) == 0 && (p.stride_c % 4) == 0;
   const bool split = a.splits > 1;
-  dim3 grid(p.tiles_m * p.tiles_n, 1, split ? a.splits : 1);
+  dim3 grid(p.tiles_m * p.tiles_n, batch, split ? a.splits : 1);
   const bool A_K = !a.transA, B_K = a.transB;
   cudaError_t e;
   if (A_K && !B_K) e = launch_vs<true, false>(p, vec, split, grid, ctx.stream);

@@ -2,7 +2,11 @@
 
 This module only draws random numbers; it holds none of the GEMM arithmetic.
 Every draw happens on the CPU with a torch.Generator seeded explicitly, so the
-same (shape, seed) gives the same bits on every machine.
+same (shape, seed) gives the same bits within one PyTorch build.  Across builds
+(another version or CPU architecture) the vectorised normal transform may
+differ in the last bit, so a test draws its inputs in the process that runs
+both the GPU path and the oracle, and no stored expected value depends on
+these draws.
 
 Distributions (the workloads' own descriptions; the pages name no generator,
 so torch's CPU generator is the reading taken):
@@ -168,3 +172,70 @@ def sweep_problem(M, N, K, variant, dtype, beta, seed) -> Problem:
     tA, tB = VARIANTS[variant]
     return make_problem(M, N, K, tA, tB, dtype=dtype, seed=seed, beta=beta,
                         alpha=1.0, name=f"{dtype}_{variant}_{M}x{N}x{K}_b{beta}")
+
+
+# ---------------------------------------------------------------------------
+# Strided batches and the attention products ("Metal GEMM Kernels for LoRA
+# Training on Apple Silicon", section 8: Q, K, V head-major [H, N, d_h]).
+# ---------------------------------------------------------------------------
+@dataclass
+class BatchedProblem:
+    """batch entries of one shape: A [batch, *stored A], B [batch, *stored B],
+    C_in [batch, M, N] (None when beta == 0); CPU tensors, contiguous unless a
+    test re-lays them out."""
+    M: int
+    N: int
+    K: int
+    batch: int
+    transA: bool
+    transB: bool
+    dtype: str
+    alpha: float
+    beta: float
+    A: torch.Tensor
+    B: torch.Tensor
+    C_in: Optional[torch.Tensor]
+    name: str = ""
+
+
+def batched_problem(M, N, K, batch, variant="nn", dtype="f32", dist="uniform", seed=0, alpha=1.0,
+                    beta=0.0, name="") -> BatchedProblem:
+    tA, tB = VARIANTS[variant]
+    A = draw(dist, (batch,) + stored_shape(tA, M, K), seed * 3 + 0, dtype)
+    B = draw(dist, (batch,) + stored_shape(tB, K, N), seed * 3 + 1, dtype)
+    C_in = draw(dist, (batch, M, N), seed * 3 + 2, dtype) if beta != 0.0 else None
+    return BatchedProblem(M, N, K, batch, tA, tB, dtype, float(alpha), float(beta), A, B, C_in,
+                          name or f"{dtype}_{variant}_{batch}x{M}x{N}x{K}")
+
+
+def causal_probabilities(H, N, seed, dtype="f16") -> torch.Tensor:
+    """A synthetic P of the attention forward pass: [H, N, N], row i
+    non-negative on columns 0..i, exactly zero above the diagonal (the masked
+    half is written as hard zeros), each row scaled to sum to ~1 before
+    rounding to the operand type."""
+    u = torch.rand((H, N, N), generator=_gen(seed), dtype=torch.float32).double()
+    u = torch.tril(u)
+    u = u / u.sum(dim=-1, keepdim=True)
+    return u.to(DTYPES[dtype])
+
+
+ATTENTION_PRODUCTS = [
+    # (name, variant, left operand, right operand, M, N, K) with n = sequence
+    # length and d = head dimension; operands are [H, rows, cols] head-major
+    ("S=QK^T", "nt", "Q", "K", "n", "n", "d"),
+    ("O=PV", "nn", "P", "V", "n", "d", "n"),
+    ("dV=P^T dO", "tn", "P", "dO", "n", "d", "n"),
+    ("dP=dO V^T", "nt", "dO", "V", "n", "n", "d"),
+    ("dQ=dS K", "nn", "dS", "K", "n", "d", "n"),
+    ("dK=dS^T Q", "tn", "dS", "Q", "n", "d", "n"),
+]
+
+
+def attention_tensors(H, n, d, seed, dtype="f16") -> dict:
+    """Q, K, V, dO ~ N(0, 1) as [H, n, d]; P a causal row-stochastic [H, n, n];
+    dS ~ N(0, 1/n) as [H, n, n] (a stand-in for the softmax backward output,
+    which the GEMMs only consume)."""
+    t = {nm: normal((H, n, d), seed * 7 + i, 1.0, dtype) for i, nm in enumerate(("Q", "K", "V", "dO"))}
+    t["P"] = causal_probabilities(H, n, seed * 7 + 4, dtype)
+    t["dS"] = normal((H, n, n), seed * 7 + 5, float(n) ** -0.5, dtype)
+    return t

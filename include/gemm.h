@@ -136,6 +136,39 @@ int gemm_splitk_noalloc(int transA, int transB, int64_t M, int64_t N, int64_t K,
                         int64_t ldb, void* C, int64_t ldc, gemm_stream_t stream);
 
 /*
+ * gemm_strided_batched -- `batch` independent products of one shape,
+ *
+ *     C_b = alpha * op(A_b) * op(B_b) + beta * C_b,   b = 0 .. batch-1,
+ *
+ * with A_b = A + b*strideA, B_b = B + b*strideB, C_b = C + b*strideC (pitches
+ * in ELEMENTS).  This is the per-head GEMM of "Metal GEMM Kernels for LoRA
+ * Training on Apple Silicon", section 8 (Attention): Q, K, V stored head-major
+ * [H, N, d_h], so head h is a contiguous matrix at offset h*N*d_h and the six
+ * attention products are the nn/tn/nt variants entered at a head offset.  The
+ * page issues one GEMM per head; here the whole batch is one launch.
+ *
+ * Arguments as gemm(), plus:
+ *   strideA, strideB, strideC >= 0.  A pitch of 0 shares one matrix across
+ *     the batch (A or B only).  The C matrices must not overlap one another
+ *     (strideC >= (M-1)*ldc + N when batch > 1), else GEMM_ERR_ALIAS.
+ *   batch >= 0 and < 2^31; batch == 0 returns GEMM_OK without touching the
+ *     GPU.  batch == 1 is gemm().
+ * Aliasing is checked over whole extents: the span C .. C_{batch-1} must not
+ * overlap the span of A's or B's matrices (GEMM_ERR_ALIAS), even where the
+ * entries themselves would interleave without touching.
+ * One launch covers the batch (gemm_last_path() GEMM_PATH_FFMA_BATCHED or
+ * GEMM_PATH_TC_BATCHED) when the operands allow: fp32 always, in groups of
+ * 65535 entries; fp16/bf16 when A and B have 16-byte aligned bases, row
+ * pitches and batch pitches (lda, ldb, strideA, strideB multiples of 8).
+ * Otherwise each entry runs as its own gemm() in stream order
+ * (GEMM_PATH_PER_ENTRY).  No split-K within a batch.
+ */
+int gemm_strided_batched(int transA, int transB, int64_t M, int64_t N, int64_t K, int dtype,
+                         float alpha, float beta, const void* A, int64_t lda, int64_t strideA,
+                         const void* B, int64_t ldb, int64_t strideB, void* C, int64_t ldc,
+                         int64_t strideC, int64_t batch, gemm_stream_t stream);
+
+/*
  * gemm_check_device_status -- synchronises `stream`, then reads and clears
  * the current device's status word.  Returns GEMM_ERR_TIMEOUT if a kernel
  * gave up on a wait since the last check, GEMM_ERR_CUDA if the stream
@@ -161,7 +194,10 @@ typedef enum {
     GEMM_PATH_FFMA = 2,        /* fp32 FFMA tiled kernel */
     GEMM_PATH_FFMA_SPLITK = 3, /* fp32 FFMA kernel over K slices + reduction */
     GEMM_PATH_TC = 4,          /* fp16/bf16 tcgen05 kernel, fused epilogue */
-    GEMM_PATH_TC_SPLITK = 5    /* fp16/bf16 tcgen05 kernel over K slices + reduction */
+    GEMM_PATH_TC_SPLITK = 5,   /* fp16/bf16 tcgen05 kernel over K slices + reduction */
+    GEMM_PATH_FFMA_BATCHED = 6, /* strided batch: fp32 FFMA kernel, batch on the grid */
+    GEMM_PATH_TC_BATCHED = 7,  /* strided batch: one persistent tcgen05 launch */
+    GEMM_PATH_PER_ENTRY = 8    /* strided batch run entry by entry (unaligned operands) */
 } gemm_path_t;
 
 int gemm_last_path(void);

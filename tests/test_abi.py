@@ -75,3 +75,31 @@ def test_empty_output_returns_ok_without_gpu(b):
     assert b.gemm_raw(0, 0, 5, 0, 3, 1, 1.0, 0.0, PA, 3, PB, 1, PC, 1) == 0
     assert b.gemm_raw(0, 0, 0, 0, 0, 0, 1.0, 0.0, 0, 1, 0, 1, 0, 1) == 0
     assert b.last_path() == "none"
+
+
+@pytest.mark.parametrize("args,code", [
+    # (M, N, K, dtype, A, lda, sA, B, ldb, sB, C, ldc, sC, batch), nn
+    ((4, 4, 4, 0, PA, 4, 16, PB, 4, 16, PC, 4, 16, -1), 1),        # negative batch
+    ((4, 4, 4, 0, PA, 4, -16, PB, 4, 16, PC, 4, 16, 2), 1),        # negative A pitch
+    ((4, 4, 4, 0, PA, 4, 16, PB, 4, 16, PC, 4, -1, 2), 1),         # negative C pitch
+    ((4, 4, 4, 0, PA, 4, 16, PB, 4, 16, PC, 4, 15, 2), 3),         # C entries overlap
+    ((4, 4, 4, 0, PA, 4, 16, PB, 4, 16, PC, 4, 0, 3), 3),          # C pitch 0 (shared C)
+    ((4, 4, 4, 0, PA, 4, 16, PB, 4, 16, PA + 64, 4, 16, 2), 3),    # C span meets A's 2nd entry
+    ((4, 4, 4, 0, PA, 4, 0, PB, 4, 1 << 20, PB + 64, 4, 16, 2), 3),  # C inside B's span
+    ((4, 4, 4, 0, PA, 3, 16, PB, 4, 16, PC, 4, 16, 2), 1),         # lda < K
+    ((4, 4, 4, 0, PA, 4, 16, PB, 4, 16, PC, 4, 16, 1 << 31), 2),   # batch too large
+    ((4, 4, 4, 0, PA, 4, 1 << 60, PB, 4, 16, PC, 4, 16, 64), 2),   # extent overflows
+])
+def test_batched_invalid_arguments(b, args, code):
+    M, N, K, dt, A, lda, sA, B, ldb, sB, C, ldc, sC, batch = args
+    assert b.gemm_strided_batched_raw(0, 0, M, N, K, dt, 1.0, 0.0, A, lda, sA, B, ldb, sB, C, ldc,
+                                      sC, batch) == code
+    assert b.last_path() == "none"
+
+
+def test_batched_empty_returns_ok_without_gpu(b):
+    assert b.gemm_strided_batched_raw(0, 0, 4, 4, 4, 0, 1.0, 0.0, PA, 4, 16, PB, 4, 16, PC, 4, 16,
+                                      0) == 0
+    assert b.gemm_strided_batched_raw(0, 0, 0, 4, 4, 1, 1.0, 0.0, PA, 4, 16, PB, 4, 16, PC, 4, 16,
+                                      5) == 0
+    assert b.last_path() == "none"

@@ -302,6 +302,27 @@ def test_checker_tolerances():
     assert ex["ok"]
 
 
+def test_checker_subnormal_outputs():
+    """A result below 2^-14 lands on fp16's subnormal grid (spacing 2^-24), so
+    the correctly rounded value may sit up to 2^-25 from ref however small
+    |ref| is; one whole quantum off must still fail.  Same for bfloat16 at its
+    own subnormal spacing 2^-133."""
+    q16 = 2.0 ** -24
+    ref = np.array([1.0e-5 + 0.49 * q16, -3.0e-6 - 0.49 * q16])  # tiny single-term results
+    mag = np.abs(ref)
+    got = ref.astype(np.float16)  # numpy's RN-even cast onto the subnormal grid
+    assert np.all(np.abs(got.astype(np.float64)) < 2.0 ** -14)
+    assert compare.check(got, ref, mag, "f16")["ok"]
+    off = (got.astype(np.float64) + np.array([q16, -q16])).astype(np.float16)
+    assert compare.check(off, ref, mag, "f16")["bad"] == 2
+    # bfloat16: values near 2^-130 (subnormal), given as uint16 bit patterns
+    qb = 2.0 ** -133
+    refb = np.array([37.1 * qb, -5.3 * qb])
+    want = oracle.round_bf16_rne(refb)
+    assert compare.check(want, refb, np.abs(refb), "bf16")["ok"]
+    assert compare.check(want + np.uint16(1), refb, np.abs(refb), "bf16")["bad"] == 2
+
+
 # ---------------------------------------------------------------------------
 # planted mistakes: every one must trip at least one pin
 # ---------------------------------------------------------------------------
