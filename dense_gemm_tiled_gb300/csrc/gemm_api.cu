@@ -105,6 +105,15 @@ int check_args(int transA, int transB, int64_t M, int64_t N, int64_t K, int dtyp
   return GEMM_OK;
 }
 
+// fp32 stream-K persistent launch (env GEMM_GB300_SG_SK=0 turns it off).
+int sg_sk_enabled() {
+  static const int v = [] {
+    const char* s = getenv("GEMM_GB300_SG_SK");
+    return (s && s[0] == '0') ? 0 : 1;
+  }();
+  return v;
+}
+
 // fp32 packing pre-pass (env GEMM_GB300_SG_PACK=0 turns it off).
 int sg_pack_enabled() {
   static const int v = [] {
@@ -258,12 +267,27 @@ int run_gemm(int transA, int transB, int64_t M64, int64_t N64, int64_t K64, int 
     const size_t bytes_A = pack && !transA ? ((size_t)K * ldA_p * 4 + 255) / 256 * 256 : 0;
     const size_t bytes_B = pack && transB ? ((size_t)K * ldB_p * 4 + 255) / 256 * 256 : 0;
     const size_t bytes_P = splits > 1 ? (size_t)splits * M * N * sizeof(float) : 0;
+    // Stream-K: without a split, a tile count that is not a whole number of
+    // rounds of the SMs leaves the last round part-empty (4096^3: 1024 tiles,
+    // 6.7 rounds of 152).  The persistent launch gives whole tiles to all but
+    // the last one to two rounds and shares those rounds' K steps evenly.
+    const bool sk = splits == 1 && sg_sk_enabled() && tiles >= sms && tiles % sms != 0;
+    const int64_t sk_tiles = sk ? (tiles >= 2 * sms ? tiles % sms + sms : tiles) : 0;
+    const size_t bytes_S = sk ? (size_t)sms * 2 * SG_BM * SG_BN * sizeof(float) : 0;
+    const size_t bytes_N = sk ? ((size_t)sk_tiles * sizeof(unsigned int) + 255) / 256 * 256 : 0;
     Scratch ws;
-    if (bytes_A + bytes_B + bytes_P > 0) {
-      e = ws.get(bytes_A + bytes_B + bytes_P, stream);
+    if (bytes_A + bytes_B + bytes_P + bytes_S + bytes_N > 0) {
+      e = ws.get(bytes_A + bytes_B + bytes_P + bytes_S + bytes_N, stream);
       if (e != cudaSuccess) return cuda_fail(e);
     }
-    if (splits > 1) a.partial = (float*)ws.ptr;
+    if (splits > 1) a.partial = (float*)((char*)ws.ptr + bytes_A + bytes_B);
+    if (sk) {
+      a.sk_blocks = sms;
+      a.sk_ws = (float*)((char*)ws.ptr + bytes_A + bytes_B + bytes_P);
+      a.sk_cnt = (unsigned int*)((char*)a.sk_ws + bytes_S);
+      e = cudaMemsetAsync(a.sk_cnt, 0, (size_t)sk_tiles * sizeof(unsigned int), stream);
+      if (e != cudaSuccess) return cuda_fail(e);
+    }
     if (pack && !transA) {  // A [M,K] -> [K,M]
       float* At = (float*)ws.ptr;
       e = launch_transpose_f32(M, K, (const float*)A, lda, At, ldA_p, ctx);

@@ -27,6 +27,13 @@ struct SgemmArgs {
   // is A + y*stride_a, B + y*stride_b, C + y*stride_c (elements)
   int batch = 1;
   int64_t stride_a = 0, stride_b = 0, stride_c = 0;
+  // persistent stream-K launch (sk_blocks > 0, no split, no batch, at least
+  // sk_blocks tiles): sk_blocks blocks, partial tiles in sk_ws
+  // (sk_blocks * 2 * SG_BM * SG_BN floats), arrival counters in sk_cnt (one per
+  // tile, zero at launch)
+  int sk_blocks = 0;
+  float* sk_ws = nullptr;
+  unsigned int* sk_cnt = nullptr;
 };
 
 // One tcgen05 GEMM launch (fp16 or bf16 operands and output).

@@ -88,7 +88,22 @@ struct Params {
   // strided batch: blockIdx.y selects matrices A + y*stride_a, B + y*stride_b,
   // C + y*stride_c (all zero for a single GEMM)
   int64_t stride_a, stride_b, stride_c;
+  // persistent launches (KIND_PERSIST): gridDim.x blocks first take whole
+  // tiles t = blockIdx.x + i * gridDim.x below dp_tiles, then share the
+  // remaining tiles' K steps evenly (block b owns steps [b*I/G, (b+1)*I/G) of
+  // the I = sk_iters steps, G = gridDim.x, tiles in order, kiters steps
+  // each).  A tile cut between blocks is finished by the last block to
+  // arrive: partials in sk_ws[block][slot], arrivals counted in sk_cnt.
+  int dp_tiles, kiters;
+  int64_t sk_iters;
+  float* sk_ws;
+  unsigned int* sk_cnt;
 };
+
+// Kernel kinds: one output tile per block (C), one K slice of a tile per
+// block (raw partials, reduced by a second kernel), or persistent blocks over
+// whole tiles and then shared K steps (C, with in-kernel fix-up).
+constexpr int KIND_TILE = 0, KIND_SPLIT = 1, KIND_PERSIST = 2;
 
 // ---------------------------------------------------------------- staging
 // Tile layouts per operand and stage:
@@ -215,6 +230,11 @@ __device__ __forceinline__ uint64_t splat2(float x) {
   asm("mov.b64 %0, {%1, %1};" : "=l"(r) : "f"(x));
   return r;
 }
+__device__ __forceinline__ uint64_t pack2(float x, float y) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(x), "f"(y));
+  return r;
+}
 __device__ __forceinline__ float2 unpack2(uint64_t v) {
   float2 f;
   asm("mov.b64 {%0, %1}, %2;" : "=f"(f.x), "=f"(f.y) : "l"(v));
@@ -225,9 +245,17 @@ __device__ __forceinline__ float4 lds128(const float* p) {
   return *reinterpret_cast<const float4*>(p);
 }
 
-template <bool A_K, bool B_K, bool VEC, bool SPLIT>
+// Stream-K bookkeeping: the block whose step range contains step x, and the
+// first step of block b (G blocks over I steps).
+__device__ __forceinline__ int sk_owner(int64_t x, int G, int64_t I) {
+  return (int)(((x + 1) * G - 1) / I);
+}
+__device__ __forceinline__ int64_t sk_start(int b, int G, int64_t I) { return (int64_t)b * I / G; }
+
+template <bool A_K, bool B_K, bool VEC, int KIND>
 __global__ void __launch_bounds__(THREADS, GB300_SG_MIN_BLOCKS) sgemm_ffma_kernel(const Params p) {
   extern __shared__ __align__(16) float smem[];
+  __shared__ int s_last;
   const int tid = threadIdx.x;
   const int warp = tid >> 5, lane = tid & 31;
   const int wm = (warp >> 2) * 64;  // warp's first row in the tile
@@ -237,135 +265,236 @@ __global__ void __launch_bounds__(THREADS, GB300_SG_MIN_BLOCKS) sgemm_ffma_kerne
   const int bcol = wn + tx * 4;     // lane cols: bcol + {0..3}, bcol + 16 + {0..3}
   const int aswz = (arow >> 2) & SWZ_MASK;  // row-tile chunk permutation, same for all 8 lane rows
 
-  // grouped rasterisation of the tile grid (consecutive blocks share B panels
-  // within a group of group_m tile-rows)
-  const int bid = blockIdx.x;
-  const int per_group = p.group_m * p.tiles_n;
-  const int first_m = (bid / per_group) * p.group_m;
-  const int gsize = min(p.tiles_m - first_m, p.group_m);
-  const int tm = first_m + (bid % per_group) % gsize;
-  const int tn = (bid % per_group) / gsize;
-  const int m0 = tm * BM, n0 = tn * BN;
-
   const float* const Ag = p.A + (int64_t)blockIdx.y * p.stride_a;
   const float* const Bg = p.B + (int64_t)blockIdx.y * p.stride_b;
-  const int kbeg = blockIdx.z * p.k_slice;
-  const int kend = min(p.K, kbeg + p.k_slice);
-  const int nk = (kend - kbeg + BK - 1) / BK;
-
+  float* const Cg = p.C + (int64_t)blockIdx.y * p.stride_c;
   const uint32_t sbase = smem_u32(smem);
-  auto stage_load = [&](int s, int k0) {
-    const uint32_t st = sbase + (uint32_t)(s * STAGE_FLOATS) * 4u;
-    if constexpr (A_K) load_rows<VEC>(st, Ag, p.lda, m0, p.M, k0, kend, tid);
-    else load_kmajor<VEC, BM, APAD>(st, Ag, p.lda, m0, p.M, k0, kend, tid);
-    const uint32_t sb = st + A_FLOATS * 4u;
-    if constexpr (B_K) load_transpose<BN, BPAD>(sb, Bg, p.ldb, n0, p.N, k0, kend, tid);
-    else load_kmajor<VEC, BN, BPAD>(sb, Bg, p.ldb, n0, p.N, k0, kend, tid);
-  };
+
+  // work state: non-persistent blocks do one item; persistent blocks walk
+  // their whole tiles, then their stream-K step range
+  const int G = gridDim.x;
+  int dp_next = blockIdx.x;
+  int64_t sk_it = 0, sk_end = 0, sk_first = 0;
+  if constexpr (KIND == KIND_PERSIST) {
+    sk_first = sk_it = sk_start(blockIdx.x, G, p.sk_iters);
+    sk_end = sk_start(blockIdx.x + 1, G, p.sk_iters);
+  }
+  bool first_item = true;
 
   // acc[i][jp] holds the outputs (row i, columns 2jp and 2jp+1) as a pair
   uint64_t acc[8][4];
-#pragma unroll
-  for (int i = 0; i < 8; ++i)
-#pragma unroll
-    for (int j = 0; j < 4; ++j) acc[i][j] = 0ull;
+
+  for (;;) {
+    // ---- next work item: tile t, K range [kbeg, kend)
+    int t, kbeg, kend;
+    int64_t seg0 = 0;  // stream-K: first step of this segment
+    bool whole = true;
+    if constexpr (KIND != KIND_PERSIST) {
+      if (!first_item) break;
+      t = blockIdx.x;
+      kbeg = blockIdx.z * p.k_slice;
+      kend = min(p.K, kbeg + p.k_slice);
+    } else {
+      if (dp_next < p.dp_tiles) {
+        t = dp_next;
+        dp_next += G;
+        kbeg = 0;
+        kend = p.K;
+      } else if (sk_it < sk_end) {
+        const int64_t ts = sk_it / p.kiters;
+        const int s0 = (int)(sk_it - ts * p.kiters);
+        const int64_t left = sk_end - sk_it;
+        const int s1 = left < (int64_t)(p.kiters - s0) ? s0 + (int)left : p.kiters;
+        t = p.dp_tiles + (int)ts;
+        seg0 = sk_it;
+        sk_it += s1 - s0;
+        kbeg = s0 * BK;
+        kend = min(p.K, s1 * BK);
+        whole = s0 == 0 && s1 == p.kiters;
+      } else {
+        break;
+      }
+    }
+    first_item = false;
+
+    // grouped rasterisation of the tile grid (consecutive tiles share B panels
+    // within a group of group_m tile-rows)
+    const int per_group = p.group_m * p.tiles_n;
+    const int first_m = (t / per_group) * p.group_m;
+    const int gsize = min(p.tiles_m - first_m, p.group_m);
+    const int tm = first_m + (t % per_group) % gsize;
+    const int tn = (t % per_group) / gsize;
+    const int m0 = tm * BM, n0 = tn * BN;
+    const int nk = (kend - kbeg + BK - 1) / BK;
+
+    auto stage_load = [&](int s, int k0) {
+      const uint32_t st = sbase + (uint32_t)(s * STAGE_FLOATS) * 4u;
+      if constexpr (A_K) load_rows<VEC>(st, Ag, p.lda, m0, p.M, k0, kend, tid);
+      else load_kmajor<VEC, BM, APAD>(st, Ag, p.lda, m0, p.M, k0, kend, tid);
+      const uint32_t sb = st + A_FLOATS * 4u;
+      if constexpr (B_K) load_transpose<BN, BPAD>(sb, Bg, p.ldb, n0, p.N, k0, kend, tid);
+      else load_kmajor<VEC, BN, BPAD>(sb, Bg, p.ldb, n0, p.N, k0, kend, tid);
+    };
 
 #pragma unroll
-  for (int s = 0; s < STAGES - 1; ++s) {
-    if (s < nk) stage_load(s, kbeg + s * BK);
-    cp_async_commit();
-  }
+    for (int i = 0; i < 8; ++i)
+#pragma unroll
+      for (int j = 0; j < 4; ++j) acc[i][j] = 0ull;
 
-  for (int kt = 0; kt < nk; ++kt) {
-    cp_async_wait<STAGES - 2>();
-    __syncthreads();  // stage kt visible to all; stage kt-1 fully consumed
-    {
-      const int nxt = kt + STAGES - 1;
-      if (nxt < nk) stage_load(nxt % STAGES, kbeg + nxt * BK);
+    if constexpr (KIND == KIND_PERSIST) __syncthreads();  // the previous item's stages are free
+#pragma unroll
+    for (int s = 0; s < STAGES - 1; ++s) {
+      if (s < nk) stage_load(s, kbeg + s * BK);
       cp_async_commit();
     }
-    const float* As = smem + (kt % STAGES) * STAGE_FLOATS;
-    const float* Bs = As + A_FLOATS;
+
+    for (int kt = 0; kt < nk; ++kt) {
+      cp_async_wait<STAGES - 2>();
+      __syncthreads();  // stage kt visible to all; stage kt-1 fully consumed
+      {
+        const int nxt = kt + STAGES - 1;
+        if (nxt < nk) stage_load(nxt % STAGES, kbeg + nxt * BK);
+        cp_async_commit();
+      }
+      const float* As = smem + (kt % STAGES) * STAGE_FLOATS;
+      const float* Bs = As + A_FLOATS;
 #pragma unroll KC_UNROLL
-    for (int kc = 0; kc < BK / 4; ++kc) {
-      float a[8][4];  // a[i][kk]: row i, k = 4kc + kk (row-tile A)
+      for (int kc = 0; kc < BK / 4; ++kc) {
+        float a[8][4];  // a[i][kk]: row i, k = 4kc + kk (row-tile A)
 #pragma unroll
-      for (int kk = 0; kk < 4; ++kk) {
-        const int k = kc * 4 + kk;
-        float av[8];
-        if constexpr (A_K) {
-          // two k at a time (64-bit loads) keeps 16 rather than 32 A values live
-          if ((kk & 1) == 0) {
-            const float* base = As + arow * BK + ((kc ^ aswz) * 4) + kk;
+        for (int kk = 0; kk < 4; ++kk) {
+          const int k = kc * 4 + kk;
+          float av[8];
+          if constexpr (A_K) {
+            // two k at a time (64-bit loads) keeps 16 rather than 32 A values live
+            if ((kk & 1) == 0) {
+              const float* base = As + arow * BK + ((kc ^ aswz) * 4) + kk;
 #pragma unroll
-            for (int i = 0; i < 8; ++i) {
-              const float2 v = *reinterpret_cast<const float2*>(base + (i < 4 ? i : 32 + i - 4) * BK);
-              a[i][kk] = v.x; a[i][kk + 1] = v.y;
+              for (int i = 0; i < 8; ++i) {
+                const float2 v =
+                    *reinterpret_cast<const float2*>(base + (i < 4 ? i : 32 + i - 4) * BK);
+                a[i][kk] = v.x; a[i][kk + 1] = v.y;
+              }
             }
+#pragma unroll
+            for (int i = 0; i < 8; ++i) av[i] = a[i][kk];
+          } else {
+            const float4 lo = lds128(As + k * APAD + arow);
+            const float4 hi = lds128(As + k * APAD + arow + 32);
+            av[0] = lo.x; av[1] = lo.y; av[2] = lo.z; av[3] = lo.w;
+            av[4] = hi.x; av[5] = hi.y; av[6] = hi.z; av[7] = hi.w;
           }
+          const float* brow = Bs + k * BPAD + bcol;
+          const ulonglong2 b01 = *reinterpret_cast<const ulonglong2*>(brow);
+          const ulonglong2 b23 = *reinterpret_cast<const ulonglong2*>(brow + 16);
+          const uint64_t bp[4] = {b01.x, b01.y, b23.x, b23.y};
 #pragma unroll
-          for (int i = 0; i < 8; ++i) av[i] = a[i][kk];
-        } else {
-          const float4 lo = lds128(As + k * APAD + arow);
-          const float4 hi = lds128(As + k * APAD + arow + 32);
-          av[0] = lo.x; av[1] = lo.y; av[2] = lo.z; av[3] = lo.w;
-          av[4] = hi.x; av[5] = hi.y; av[6] = hi.z; av[7] = hi.w;
-        }
-        const float* brow = Bs + k * BPAD + bcol;
-        const ulonglong2 b01 = *reinterpret_cast<const ulonglong2*>(brow);
-        const ulonglong2 b23 = *reinterpret_cast<const ulonglong2*>(brow + 16);
-        const uint64_t bp[4] = {b01.x, b01.y, b23.x, b23.y};
+          for (int i = 0; i < 8; ++i) {
+            const uint64_t ap = splat2(av[i]);
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          const uint64_t ap = splat2(av[i]);
-#pragma unroll
-          for (int j = 0; j < 4; ++j) acc[i][j] = ffma2(ap, bp[j], acc[i][j]);
+            for (int j = 0; j < 4; ++j) acc[i][j] = ffma2(ap, bp[j], acc[i][j]);
+          }
         }
       }
     }
-  }
-  cp_async_wait<0>();
+    cp_async_wait<0>();
 
-  // epilogue: lane columns bcol + {0..3} (pairs 0, 1) and bcol + 16 + {0..3} (pairs 2, 3)
+    if constexpr (KIND == KIND_PERSIST) {
+      if (!whole) {
+        // A tile shared between blocks.  Every contributor stores its partial
+        // sums (warp-coalesced: float4 j of thread tid at [j][tid]) in its
+        // slot -- 0 for the segment a block starts with, 1 for the one it
+        // ends with -- then counts itself in.  The last to arrive adds all
+        // segments in K order (so the result does not depend on arrival
+        // order) and stores the tile.
+        const int slot = seg0 == sk_first ? 0 : 1;
+        float4* mine = reinterpret_cast<float4*>(p.sk_ws) +
+                       (int64_t)(blockIdx.x * 2 + slot) * (BM * BN / 4);
 #pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    const int gm = m0 + arow + (i < 4 ? i : 32 + i - 4);
-    if (gm >= p.M) continue;
+        for (int i = 0; i < 8; ++i)
 #pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      const int gn = n0 + bcol + h * 16;
-      const float2 lo = unpack2(acc[i][2 * h]), hi = unpack2(acc[i][2 * h + 1]);
-      const float v[4] = {lo.x, lo.y, hi.x, hi.y};
-      if constexpr (SPLIT) {
-        float* dst = p.partial + ((int64_t)blockIdx.z * p.M + gm) * p.N + gn;
-        if (gn + 3 < p.N && (p.N & 3) == 0) {
-          *reinterpret_cast<float4*>(dst) = make_float4(v[0], v[1], v[2], v[3]);
-        } else {
-#pragma unroll
-          for (int j = 0; j < 4; ++j)
-            if (gn + j < p.N) dst[j] = v[j];
-        }
-      } else {
-        float* dst = p.C + (int64_t)blockIdx.y * p.stride_c + (int64_t)gm * p.ldc + gn;
-        const bool vec_ok = VEC && (gn + 3 < p.N);
-        if (vec_ok) {
-          float4 o;
-          if (p.beta != 0.f) {
-            const float4 c = *reinterpret_cast<const float4*>(dst);
-            o = make_float4(__fmaf_rn(p.alpha, v[0], p.beta * c.x),
-                            __fmaf_rn(p.alpha, v[1], p.beta * c.y),
-                            __fmaf_rn(p.alpha, v[2], p.beta * c.z),
-                            __fmaf_rn(p.alpha, v[3], p.beta * c.w));
-          } else {
-            o = make_float4(p.alpha * v[0], p.alpha * v[1], p.alpha * v[2], p.alpha * v[3]);
+          for (int h = 0; h < 2; ++h) {
+            const float2 lo = unpack2(acc[i][2 * h]), hi = unpack2(acc[i][2 * h + 1]);
+            mine[(i * 2 + h) * THREADS + tid] = make_float4(lo.x, lo.y, hi.x, hi.y);
           }
-          *reinterpret_cast<float4*>(dst) = o;
-        } else {
+        __threadfence();
+        __syncthreads();
+        const int64_t x0 = (int64_t)(t - p.dp_tiles) * p.kiters;
+        const int c_lo = sk_owner(x0, G, p.sk_iters);
+        const int c_hi = sk_owner(x0 + p.kiters - 1, G, p.sk_iters);
+        if (tid == 0) {
+          const unsigned int before = atomicAdd(p.sk_cnt + (t - p.dp_tiles), 1u);
+          s_last = before == (unsigned int)(c_hi - c_lo);
+        }
+        __syncthreads();
+        if (!s_last) continue;
+        __threadfence();
+        float sum[8][4][2];
 #pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            if (gn + j < p.N) {
-              dst[j] = (p.beta != 0.f) ? __fmaf_rn(p.alpha, v[j], p.beta * dst[j])
-                                       : p.alpha * v[j];
+        for (int i = 0; i < 8; ++i)
+#pragma unroll
+          for (int j = 0; j < 4; ++j) sum[i][j][0] = sum[i][j][1] = 0.f;
+        for (int c = c_lo; c <= c_hi; ++c) {
+          const int cs = sk_start(c, G, p.sk_iters) >= x0 ? 0 : 1;
+          const float4* part = reinterpret_cast<const float4*>(p.sk_ws) +
+                               (int64_t)(c * 2 + cs) * (BM * BN / 4);
+#pragma unroll
+          for (int i = 0; i < 8; ++i)
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+              const float4 v = __ldcg(part + (i * 2 + h) * THREADS + tid);
+              sum[i][2 * h][0] += v.x; sum[i][2 * h][1] += v.y;
+              sum[i][2 * h + 1][0] += v.z; sum[i][2 * h + 1][1] += v.w;
+            }
+        }
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+#pragma unroll
+          for (int j = 0; j < 4; ++j) acc[i][j] = pack2(sum[i][j][0], sum[i][j][1]);
+      }
+    }
+
+    // epilogue: lane columns bcol + {0..3} (pairs 0, 1) and bcol + 16 + {0..3} (pairs 2, 3)
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int gm = m0 + arow + (i < 4 ? i : 32 + i - 4);
+      if (gm >= p.M) continue;
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int gn = n0 + bcol + h * 16;
+        const float2 lo = unpack2(acc[i][2 * h]), hi = unpack2(acc[i][2 * h + 1]);
+        const float v[4] = {lo.x, lo.y, hi.x, hi.y};
+        if constexpr (KIND == KIND_SPLIT) {
+          float* dst = p.partial + ((int64_t)blockIdx.z * p.M + gm) * p.N + gn;
+          if (gn + 3 < p.N && (p.N & 3) == 0) {
+            *reinterpret_cast<float4*>(dst) = make_float4(v[0], v[1], v[2], v[3]);
+          } else {
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+              if (gn + j < p.N) dst[j] = v[j];
+          }
+        } else {
+          float* dst = Cg + (int64_t)gm * p.ldc + gn;
+          const bool vec_ok = VEC && (gn + 3 < p.N);
+          if (vec_ok) {
+            float4 o;
+            if (p.beta != 0.f) {
+              const float4 c = *reinterpret_cast<const float4*>(dst);
+              o = make_float4(__fmaf_rn(p.alpha, v[0], p.beta * c.x),
+                              __fmaf_rn(p.alpha, v[1], p.beta * c.y),
+                              __fmaf_rn(p.alpha, v[2], p.beta * c.z),
+                              __fmaf_rn(p.alpha, v[3], p.beta * c.w));
+            } else {
+              o = make_float4(p.alpha * v[0], p.alpha * v[1], p.alpha * v[2], p.alpha * v[3]);
+            }
+            *reinterpret_cast<float4*>(dst) = o;
+          } else {
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              if (gn + j < p.N) {
+                dst[j] = (p.beta != 0.f) ? __fmaf_rn(p.alpha, v[j], p.beta * dst[j])
+                                         : p.alpha * v[j];
+              }
             }
           }
         }
@@ -374,9 +503,9 @@ __global__ void __launch_bounds__(THREADS, GB300_SG_MIN_BLOCKS) sgemm_ffma_kerne
   }
 }
 
-template <bool A_K, bool B_K, bool VEC, bool SPLIT>
+template <bool A_K, bool B_K, bool VEC, int KIND>
 cudaError_t launch_one(const Params& p, dim3 grid, cudaStream_t stream) {
-  auto kern = sgemm_ffma_kernel<A_K, B_K, VEC, SPLIT>;
+  auto kern = sgemm_ffma_kernel<A_K, B_K, VEC, KIND>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        SMEM_BYTES);
   if (e != cudaSuccess) return e;
@@ -385,13 +514,15 @@ cudaError_t launch_one(const Params& p, dim3 grid, cudaStream_t stream) {
 }
 
 template <bool A_K, bool B_K>
-cudaError_t launch_vs(const Params& p, bool vec, bool split, dim3 grid, cudaStream_t s) {
+cudaError_t launch_vs(const Params& p, bool vec, int kind, dim3 grid, cudaStream_t s) {
   if (vec) {
-    return split ? launch_one<A_K, B_K, true, true>(p, grid, s)
-                 : launch_one<A_K, B_K, true, false>(p, grid, s);
+    if (kind == KIND_SPLIT) return launch_one<A_K, B_K, true, KIND_SPLIT>(p, grid, s);
+    if (kind == KIND_PERSIST) return launch_one<A_K, B_K, true, KIND_PERSIST>(p, grid, s);
+    return launch_one<A_K, B_K, true, KIND_TILE>(p, grid, s);
   }
-  return split ? launch_one<A_K, B_K, false, true>(p, grid, s)
-               : launch_one<A_K, B_K, false, false>(p, grid, s);
+  if (kind == KIND_SPLIT) return launch_one<A_K, B_K, false, KIND_SPLIT>(p, grid, s);
+  if (kind == KIND_PERSIST) return launch_one<A_K, B_K, false, KIND_PERSIST>(p, grid, s);
+  return launch_one<A_K, B_K, false, KIND_TILE>(p, grid, s);
 }
 
 }  // namespace
@@ -424,13 +555,30 @@ cudaError_t launch_sgemm(const SgemmArgs& a, LaunchCtx& ctx) {
                    (a.lda % 4) == 0 && (a.ldb % 4) == 0 && (a.ldc % 4) == 0 &&
                    (p.stride_a % 4) == 0 && (p.stride_b % 4) == 0 && (p.stride_c % 4) == 0;
   const bool split = a.splits > 1;
-  dim3 grid(p.tiles_m * p.tiles_n, batch, split ? a.splits : 1);
+  const int tiles = p.tiles_m * p.tiles_n;
+  int kind = split ? KIND_SPLIT : KIND_TILE;
+  dim3 grid(tiles, batch, split ? a.splits : 1);
+  p.dp_tiles = 0; p.kiters = 0; p.sk_iters = 0; p.sk_ws = nullptr; p.sk_cnt = nullptr;
+  if (a.sk_blocks > 0) {
+    // persistent: all but the last one to two rounds of whole tiles go to
+    // blocks in turn; the rest are shared out by K steps
+    const int G = a.sk_blocks;
+    if (split || batch > 1 || tiles < G || !a.sk_ws || !a.sk_cnt) return cudaErrorInvalidValue;
+    kind = KIND_PERSIST;
+    p.kiters = (a.K + BK - 1) / BK;
+    p.dp_tiles = tiles >= 2 * G ? (tiles / G - 1) * G : 0;
+    p.sk_iters = (int64_t)(tiles - p.dp_tiles) * p.kiters;
+    p.sk_ws = a.sk_ws;
+    p.sk_cnt = a.sk_cnt;
+    grid = dim3(G, 1, 1);
+  }
   const bool A_K = !a.transA, B_K = a.transB;
   cudaError_t e;
-  if (A_K && !B_K) e = launch_vs<true, false>(p, vec, split, grid, ctx.stream);
-  else if (!A_K && !B_K) e = launch_vs<false, false>(p, vec, split, grid, ctx.stream);
-  else if (A_K && B_K) e = launch_vs<true, true>(p, vec, split, grid, ctx.stream);
-  else e = launch_vs<false, true>(p, vec, split, grid, ctx.stream);
+  if (A_K && !B_K) e = launch_vs<true, false>(p, vec, kind, grid, ctx.stream);
+  else if (!A_K && !B_K) e = launch_vs<false, false>(p, vec, kind, grid, ctx.stream);
+  else if (A_K && B_K) e = launch_vs<true, true>(p, vec, kind, grid, ctx.stream);
+  else e = launch_vs<false, true>(p, vec, kind, grid, ctx.stream);
+  ctx.grid = (int)(grid.x * grid.y * grid.z);
   if (e == cudaSuccess) ctx.launches++;
   return e;
 }

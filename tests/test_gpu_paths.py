@@ -52,3 +52,36 @@ def test_forced_kernel_configuration(lib_path, gpu, pair, bn, tail):
     r = subprocess.run([sys.executable, "-c", code], env=env, capture_output=True, text=True,
                        timeout=900)
     assert r.returncode == 0 and r.stdout.strip().endswith("ok"), r.stdout[-3000:] + r.stderr[-3000:]
+
+
+SCRIPT_F32 = r"""
+import sys
+sys.path.insert(0, {root!r}); sys.path.insert(0, {tests!r})
+from dense_gemm_tiled_gb300 import binding, inputs
+from helpers import check_problem
+for v in ("nn", "tn", "nt", "tt"):
+    tA, tB = inputs.VARIANTS[v]
+    # above the packing threshold (M*N*K >= 2^30) with more output tiles
+    # than the split-K rule splits (> 152), ragged in every dimension
+    p = inputs.make_problem(1000, 2600, 620, tA, tB, "f32", "uniform", seed=610, beta=0.5)
+    r = check_problem(p)
+    assert r["path"] == "ffma", r
+    p = inputs.make_problem(2048, 1408, 384, tA, tB, "f32", "integer", seed=611)
+    r = check_problem(p, exact=True)
+    assert r["path"] == "ffma", r
+print("ok")
+"""
+
+
+@pytest.mark.parametrize("pack,sk", [("1", "1"), ("0", "1"), ("1", "0")])
+def test_forced_fp32_configuration(lib_path, gpu, pack, sk):
+    """The fp32 transposing pre-pass (default on large problems) or the kernel
+    reading every layout directly (GEMM_GB300_SG_PACK=0); the persistent
+    stream-K launch (default when the tiles are not a whole number of rounds
+    of the SMs; both shapes here have 168 and 176 tiles) or one block per
+    tile (GEMM_GB300_SG_SK=0)."""
+    env = dict(os.environ, GEMM_GB300_SG_PACK=pack, GEMM_GB300_SG_SK=sk)
+    code = SCRIPT_F32.format(root=ROOT, tests=os.path.join(ROOT, "tests"))
+    r = subprocess.run([sys.executable, "-c", code], env=env, capture_output=True, text=True,
+                       timeout=900)
+    assert r.returncode == 0 and r.stdout.strip().endswith("ok"), r.stdout[-3000:] + r.stderr[-3000:]
