@@ -10,7 +10,11 @@ HBM.  The same line carries, measured in the same run:
              section 2), per-launch CUDA-event timing with L2 flushed before
              every launch;
   roofline   achieved / peak of the dominant kernel (FP32 FFMA pipe for the
-             SGEMM; the tensor pipe for the fp16 kernel);
+             SGEMM; the tensor pipe for the fp16 kernel), the kernel's own
+             device time taken by events the library records around it;
+  attention  the six GEMMs of one attention layer's forward and backward pass
+             ("Metal GEMM Kernels for LoRA Training", section 8), each one
+             strided-batched call over the heads, eager and as a CUDA graph;
   e2e        the SGEMM through gemm_host(): pinned host buffers, the copies to
              and from the GPU inside the timed region;
   cpu_baseline  the CPU oracle (double accumulation) on a bounded sample of
@@ -67,6 +71,7 @@ class ClockSampler:
         self.period = period_ms
         self.proc = None
         self.lines = []
+        self.first = 0
 
     def __enter__(self):
         try:
@@ -84,6 +89,15 @@ class ClockSampler:
         for line in self.proc.stdout:
             self.lines.append(line.strip())
 
+    def mark(self, wait_s: float = 3.0):
+        """Waits (up to wait_s) until nvidia-smi has produced a sample, so its
+        start-up is over; samples taken from then on are the ones summary()
+        reports."""
+        t_end = time.perf_counter() + wait_s
+        while self.proc is not None and not self.lines and time.perf_counter() < t_end:
+            time.sleep(0.01)
+        self.first = len(self.lines)
+
     def __exit__(self, *exc):
         if self.proc is not None:
             self.proc.terminate()
@@ -96,7 +110,7 @@ class ClockSampler:
     def summary(self):
         sm, mx, reasons = [], None, set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for ln in self.lines:
+        for ln in self.lines[self.first:]:
             parts = [p.strip() for p in ln.split(",")]
             if len(parts) < 9:
                 continue
@@ -268,6 +282,67 @@ def lora_step(dev, stream, reps: int = 20):
             "sum_of_gemms_ms": sum(v["us"] for v in per.values()) / 1e3, "per_gemm": per}
 
 
+def attention_step(dev, stream, reps: int = 20, H: int = 16, n: int = 2048, d: int = 128):
+    """The six GEMMs of one attention layer ("Metal GEMM Kernels for LoRA
+    Training", section 8: S = Q K^T, O = P V, dV = P^T dO, dP = dO V^T,
+    dQ = dS K, dK = dS^T Q over head-major [H, n, d] tensors), fp16 with fp32
+    accumulation, each one gemm_strided_batched() call over the H heads.
+    Model width H * d = 2048 (the LoRA page's d), sequence n = 2048.  Reported:
+    per-product device time (events around the call, median), their sum, and
+    the six replayed as one CUDA graph."""
+    import torch
+    from dense_gemm_tiled_gb300 import binding, inputs
+    t = {k: v.to(dev) for k, v in inputs.attention_tensors(H, n, d, seed=900).items()}
+    size = {"n": n, "d": d}
+    ops = []
+    for name, variant, left, right, Ms, Ns, Ks in inputs.ATTENTION_PRODUCTS:
+        tA, tB = inputs.VARIANTS[variant]
+        C = torch.empty((H, size[Ms], size[Ns]), dtype=torch.float16, device=dev)
+        ops.append((name, variant, tA, tB, t[left], t[right], C, size[Ms], size[Ns], size[Ks]))
+
+    def one(op):
+        name, variant, tA, tB, L, R, C = op[:7]
+        binding.gemm_strided_batched(L, R, C, tA, tB, stream=stream)
+
+    for op in ops:
+        one(op)
+    torch.cuda.synchronize()
+    per = {}
+    for op in ops:
+        ts = []
+        for _ in range(reps):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            one(op)
+            e1.record(stream)
+            e1.synchronize()
+            ts.append(e0.elapsed_time(e1))
+        Mo, No, Ko = op[7:]
+        med = statistics.median(ts)
+        per[op[0]] = {"us": med * 1e3, "variant": op[1], "shape": [H, Mo, No, Ko],
+                      "tflops": 2.0 * H * Mo * No * Ko / (med * 1e-3) / 1e12,
+                      "path": binding.last_path()}
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        for op in ops:
+            one(op)
+    for _ in range(3):
+        graph.replay()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(reps):
+        graph.replay()
+    e1.record()
+    e1.synchronize()
+    graph_ms = e0.elapsed_time(e1) / reps
+    flops = sum(2.0 * H * o[7] * o[8] * o[9] for o in ops)
+    assert binding.check_device_status(stream) == binding.OK
+    return {"heads": H, "seq": n, "head_dim": d, "gflop": flops / 1e9, "graph_ms": graph_ms,
+            "graph_tflops": flops / (graph_ms * 1e-3) / 1e12,
+            "sum_of_products_ms": sum(v["us"] for v in per.values()) / 1e3, "per_product": per}
+
+
 def run_case(args, local):
     """One GEMM, `warmup` untimed launches then `steps` timed ones (CUDA events
     per launch on the launching stream)."""
@@ -308,6 +383,7 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-fp16", action="store_true")
     ap.add_argument("--no-lora", action="store_true")
+    ap.add_argument("--no-attention", action="store_true")
     ap.add_argument("--case", default=None,
                     help="run only one GEMM (e.g. f32_nn_4096, f16_tn_4096, f16_nn_8192): "
                          "warm-up + steps, one short JSON line; used for profiling")
@@ -341,31 +417,49 @@ def main():
     def step():
         binding.gemm(A, B, C, stream=stream)
 
-    with torch.cuda.stream(stream):
-        for _ in range(args.warmup):
-            step()
-    torch.cuda.synchronize()
-    assert binding.check_device_status(stream) == binding.OK
-
     starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    barrier(world)
-    torch.cuda.synchronize()
-    launches0 = binding.total_launches()
+    # The library brackets the SGEMM kernel itself (not its packing pre-pass)
+    # with a pair of these on every KEV_EVERY-th timed step (recording foreign
+    # events costs the host ~0.5 ms while the stream is busy).
+    KEV_EVERY = 4
+    n_kev = (args.steps + KEV_EVERY - 1) // KEV_EVERY
+    kstarts = [torch.cuda.Event(enable_timing=True) for _ in range(n_kev)]
+    kends = [torch.cuda.Event(enable_timing=True) for _ in range(n_kev)]
+    for ev in kstarts + kends:
+        ev.record(stream)
+    # the clock sampler starts before the warm-up, so that nvidia-smi is
+    # already polling when the timed region begins
     with ClockSampler(local) as clk:
+        with torch.cuda.stream(stream):
+            for _ in range(args.warmup):
+                step()
+        torch.cuda.synchronize()
+        assert binding.check_device_status(stream) == binding.OK
+        clk.mark()
+        barrier(world)
+        torch.cuda.synchronize()
+        launches0 = binding.total_launches()
         t0 = time.perf_counter()
         for i in range(args.steps):
+            if i % KEV_EVERY == 0:
+                binding.set_kernel_events(kstarts[i // KEV_EVERY], kends[i // KEV_EVERY])
+            elif i % KEV_EVERY == 1:
+                binding.set_kernel_events()
             starts[i].record(stream)
             step()
             ends[i].record(stream)
         torch.cuda.synchronize()
         t1 = time.perf_counter()
+    binding.set_kernel_events()
     barrier(world)
     launches = binding.total_launches() - launches0
     path = binding.last_path()
     wall = max_over_ranks(t1 - t0, world, dev)
     ms_step = wall / args.steps * 1e3
-    kernel_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    avg_step_ms = sum(step_ms) / len(step_ms)
+    kernel_ms = [s.elapsed_time(e) for s, e in zip(kstarts, kends)]  # every KEV_EVERY-th step
     avg_kernel_ms = sum(kernel_ms) / len(kernel_ms)
     value = world * flops / (wall / args.steps) / 1e12
     clocks = clk.summary()
@@ -377,7 +471,10 @@ def main():
     achieved = flops / (avg_kernel_ms * 1e-3) / 1e12
     roofline = {"bound": "alu", "achieved": achieved, "peak": ffma_peak, "unit": "TFLOP/s",
                 "frac": achieved / ffma_peak, "traffic": None,
-                "kernel": "sgemm_ffma_kernel (fp32 nn, 128x128x16 tiles)",
+                "kernel": "sgemm_ffma_kernel (fp32, 128x128 tiles, K step 64, paired FMA; "
+                          "persistent stream-K launch: 1024 tiles over 152 SMs)",
+                "timing": "CUDA events recorded by the library around the kernel launch "
+                          "(gemm_set_kernel_events) on every 4th timed step, average",
                 "peak_basis": f"{sms} SMs x {FP32_LANES_PER_SM} FP32 lanes x 2 x {sm_max:.0f} MHz",
                 "frac_at_median_clock": (achieved / (sms * FP32_LANES_PER_SM * 2 *
                                                      clocks["sm_mhz"] * 1e6 / 1e12)
@@ -434,6 +531,7 @@ def main():
         assert binding.check_device_status(stream) == binding.OK
 
     lora = None if args.no_lora else lora_step(dev, stream)
+    attn = None if args.no_attention else attention_step(dev, stream)
 
     # end to end through gemm_host(): pinned host inputs, result read back
     Ah = inputs.uniform((M, K), 60, "f32").pin_memory()
@@ -468,9 +566,11 @@ def main():
                        "gpu": props.name, "sms": sms},
             "path": path,
             "kernel_ms_avg": avg_kernel_ms,
+            "step_device_ms_avg": avg_step_ms,
             "roofline": roofline,
             "fp16_4096": fp16,
             "lora_step": lora,
+            "attention": attn,
             "e2e": e2e,
             "cpu_baseline": cpu,
             "gpu_launches": launches,

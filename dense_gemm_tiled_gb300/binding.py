@@ -41,6 +41,8 @@ _lib.gemm_set_wait_timeout_ns.argtypes = [_i64]
 _lib.gemm_set_wait_timeout_ns.restype = None
 _lib.gemm_set_fault_injection.argtypes = [_int]
 _lib.gemm_set_fault_injection.restype = None
+_lib.gemm_set_kernel_events.argtypes = [_vp, _vp]
+_lib.gemm_set_kernel_events.restype = None
 
 F32 = 0
 F16_F32ACC = 1
@@ -88,6 +90,19 @@ def set_fault_injection(mode: int) -> None:
     _lib.gemm_set_fault_injection(int(mode))
 
 
+def set_kernel_events(start=None, end=None) -> None:
+    """Brackets the main GEMM kernel of later calls on this thread with two
+    torch.cuda.Event objects (each recorded once beforehand, so that its CUDA
+    event exists); no arguments turns it off."""
+    if start is None or end is None:
+        _lib.gemm_set_kernel_events(None, None)
+        return
+    s, e = int(start.cuda_event), int(end.cuda_event)
+    if not s or not e:
+        raise ValueError("record each event once before passing it")
+    _lib.gemm_set_kernel_events(s, e)
+
+
 def gemm_raw(transA, transB, M, N, K, dtype, alpha, beta, A, lda, B, ldb, C, ldc,
              stream=0) -> int:
     """The C entry point with plain integers (device addresses, stream handle)."""
@@ -114,12 +129,13 @@ def gemm_strided_batched_raw(transA, transB, M, N, K, dtype, alpha, beta, A, lda
                                      int(strideC), int(batch), stream or None)
 
 
-def _batch_pitch(t) -> int:
-    """Element pitch between the matrices of a [batch, rows, cols] tensor (0
-    for a broadcast operand made with expand())."""
-    if t.dim() != 3:
-        raise ValueError("batched operands are 3-D [batch, rows, cols]")
-    return int(t.stride(0)) if t.shape[0] > 1 else 0
+def _ld3(t) -> int:
+    """Row pitch of a [batch, rows, cols] tensor (the _ld rule per matrix)."""
+    if t.shape[2] > 1 and t.stride(2) != 1:
+        raise ValueError("rows must be contiguous (stride(2) == 1)")
+    if t.shape[1] <= 1:
+        return max(int(t.stride(1)), int(t.shape[2]), 1)
+    return int(t.stride(1))
 
 
 def gemm_strided_batched(A, B, C, transA=False, transB=False, alpha=1.0, beta=0.0, stream=None):
@@ -135,16 +151,25 @@ def gemm_strided_batched(A, B, C, transA=False, transB=False, alpha=1.0, beta=0.
     batch = int(C.shape[0])
     if A.shape[0] != batch or B.shape[0] != batch:
         raise ValueError("A, B and C must have the same batch size")
-    dtype, M, N, K = _dims(A[0], B[0], C[0], transA, transB)
-    for t in (A, B, C):
-        if not t.is_cuda:
-            raise ValueError("gemm_strided_batched() takes CUDA tensors")
+    if A.dtype != B.dtype or A.dtype != C.dtype:
+        raise TypeError("A, B and C must share a dtype")
+    dtype = _DTYPES.get(A.dtype)
+    if dtype is None:
+        raise TypeError(f"unsupported dtype {A.dtype}")
+    M, K = (A.shape[2], A.shape[1]) if transA else (A.shape[1], A.shape[2])
+    Kb, N = (B.shape[2], B.shape[1]) if transB else (B.shape[1], B.shape[2])
+    if K != Kb:
+        raise ValueError(f"inner dimensions differ: {K} vs {Kb}")
+    if C.shape[1] != M or C.shape[2] != N:
+        raise ValueError(f"C is {tuple(C.shape)}, expected {(batch, M, N)}")
+    if not (A.is_cuda and B.is_cuda and C.is_cuda):
+        raise ValueError("gemm_strided_batched() takes CUDA tensors")
     s = stream if stream is not None else torch.cuda.current_stream(C.device)
+    pitch = (lambda t: int(t.stride(0)) if batch > 1 else 0)
     rc = _lib.gemm_strided_batched(
-        int(transA), int(transB), M, N, K, dtype, float(alpha), float(beta),
-        A.data_ptr() or None, _ld(A[0]), _batch_pitch(A), B.data_ptr() or None, _ld(B[0]),
-        _batch_pitch(B), C.data_ptr() or None, _ld(C[0]), _batch_pitch(C), batch,
-        s.cuda_stream or None)
+        int(transA), int(transB), int(M), int(N), int(K), dtype, float(alpha), float(beta),
+        A.data_ptr() or None, _ld3(A), pitch(A), B.data_ptr() or None, _ld3(B), pitch(B),
+        C.data_ptr() or None, _ld3(C), pitch(C), batch, s.cuda_stream or None)
     if rc != OK:
         raise GemmError(rc)
     return C
@@ -160,17 +185,19 @@ def _ld(t) -> int:
     return int(t.stride(0))
 
 
-def _dims(A, B, C, transA, transB):
+_DTYPES = {}
+
+
+def _dtype_codes():
     import torch
+    _DTYPES.update({torch.float32: F32, torch.float16: F16_F32ACC, torch.bfloat16: BF16_F32ACC})
+
+
+def _dims(A, B, C, transA, transB):
     if A.dtype != B.dtype or A.dtype != C.dtype:
         raise TypeError("A, B and C must share a dtype")
-    if A.dtype == torch.float32:
-        dtype = F32
-    elif A.dtype == torch.float16:
-        dtype = F16_F32ACC
-    elif A.dtype == torch.bfloat16:
-        dtype = BF16_F32ACC
-    else:
+    dtype = _DTYPES.get(A.dtype)
+    if dtype is None:
         raise TypeError(f"unsupported dtype {A.dtype}")
     M, K = (A.shape[1], A.shape[0]) if transA else (A.shape[0], A.shape[1])
     Kb, N = (B.shape[1], B.shape[0]) if transB else (B.shape[0], B.shape[1])
@@ -226,3 +253,9 @@ def check_device_status(stream=None) -> int:
     import torch
     s = stream if stream is not None else torch.cuda.current_stream()
     return _lib.gemm_check_device_status(s.cuda_stream or None)
+
+
+try:
+    _dtype_codes()
+except ImportError:  # pragma: no cover - torch is needed only by the tensor wrappers
+    pass

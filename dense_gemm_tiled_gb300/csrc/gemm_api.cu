@@ -38,6 +38,31 @@ std::atomic<int> g_fault_injection{0};
 thread_local int tl_last_path = GEMM_PATH_NONE;
 thread_local int tl_last_launches = 0;
 thread_local int tl_last_grid = 0;
+// gemm_set_kernel_events: recorded around the main GEMM kernel of each call
+thread_local cudaEvent_t tl_ev_start = nullptr, tl_ev_end = nullptr;
+
+// The main GEMM kernel launch, bracketed by the caller's timing events when
+// set.
+cudaError_t timed_sgemm(const SgemmArgs& a, LaunchCtx& ctx) {
+  if (tl_ev_start && tl_ev_end) {
+    cudaError_t e = cudaEventRecord(tl_ev_start, ctx.stream);
+    if (e != cudaSuccess) return e;
+    e = launch_sgemm(a, ctx);
+    if (e != cudaSuccess) return e;
+    return cudaEventRecord(tl_ev_end, ctx.stream);
+  }
+  return launch_sgemm(a, ctx);
+}
+cudaError_t timed_hgemm(const HgemmArgs& a, LaunchCtx& ctx) {
+  if (tl_ev_start && tl_ev_end) {
+    cudaError_t e = cudaEventRecord(tl_ev_start, ctx.stream);
+    if (e != cudaSuccess) return e;
+    e = launch_hgemm(a, ctx);
+    if (e != cudaSuccess) return e;
+    return cudaEventRecord(tl_ev_end, ctx.stream);
+  }
+  return launch_hgemm(a, ctx);
+}
 
 // Per-device set-up, done once with that device current: the status word's
 // device address and the SM count.
@@ -299,7 +324,7 @@ int run_gemm(int transA, int transB, int64_t M64, int64_t N64, int64_t K64, int 
       a.B = Bt; a.ldb = ldB_p; a.transB = 0;
     }
     path = splits > 1 ? GEMM_PATH_FFMA_SPLITK : GEMM_PATH_FFMA;
-    if (e == cudaSuccess) e = launch_sgemm(a, ctx);
+    if (e == cudaSuccess) e = timed_sgemm(a, ctx);
     if (e == cudaSuccess && splits > 1)
       e = launch_splitk_reduce(0, M, N, splits, a.partial, C, ldc, alpha, beta, ctx);
   } else {
@@ -367,7 +392,7 @@ int run_gemm(int transA, int transB, int64_t M64, int64_t N64, int64_t K64, int 
         a.tail_cnt = tail_cnt;
       }
       path = splits > 1 ? GEMM_PATH_TC_SPLITK : GEMM_PATH_TC;
-      e = launch_hgemm(a, ctx);
+      e = timed_hgemm(a, ctx);
       if (e == cudaSuccess && splits > 1)
         e = launch_splitk_reduce(dtype, M, N, splits, a.partial, C, ldc, alpha, beta, ctx);
     }
@@ -426,7 +451,7 @@ int run_batched(int transA, int transB, int64_t M64, int64_t N64, int64_t K64, i
       a.dtype = dtype;
       a.batch = nb;
       a.stride_a = sA; a.stride_b = sB; a.stride_c = sC;
-      e = launch_hgemm(a, ctx);
+      e = timed_hgemm(a, ctx);
       // the driver refused the 3-D description (e.g. batch pitches that
       // interleave rows) before the first launch: run entry by entry
       if (e == cudaErrorNotSupported && ctx.launches == 0) {
@@ -469,7 +494,7 @@ int run_batched(int transA, int transB, int64_t M64, int64_t N64, int64_t K64, i
                   alpha, beta, 1, K, nullptr};
       a.batch = nb;
       a.stride_a = sA; a.stride_b = sB; a.stride_c = sC;
-      e = launch_sgemm(a, ctx);
+      e = timed_sgemm(a, ctx);
     }
   }
   g_total_launches += ctx.launches;
@@ -628,6 +653,11 @@ void gemm_set_wait_timeout_ns(int64_t ns) {
 
 void gemm_set_fault_injection(int mode) { g_fault_injection.store(mode); }
 
+void gemm_set_kernel_events(void* start, void* end) {
+  tl_ev_start = (start && end) ? static_cast<cudaEvent_t>(start) : nullptr;
+  tl_ev_end = (start && end) ? static_cast<cudaEvent_t>(end) : nullptr;
+}
+
 }  // extern "C"
 
 // ---------------------------------------------------------------------------
@@ -705,7 +735,7 @@ extern "C" int gemm_splitk_noalloc(int transA, int transB, int64_t M, int64_t N,
     SgemmArgs a{transA, transB, Mi, Ni, Ki, (const float*)A, lda, (const float*)B, ldb,
                 (float*)C, ldc, alpha, beta, splits, k_slice, splits > 1 ? scratch : nullptr};
     path = splits > 1 ? GEMM_PATH_FFMA_SPLITK : GEMM_PATH_FFMA;
-    e = launch_sgemm(a, ctx);
+    e = timed_sgemm(a, ctx);
     if (e == cudaSuccess && splits > 1)
       e = launch_splitk_reduce(0, Mi, Ni, splits, scratch, C, ldc, alpha, beta, ctx);
   } else {
@@ -729,7 +759,7 @@ extern "C" int gemm_splitk_noalloc(int transA, int transB, int64_t M, int64_t N,
                 c_tma_enabled(), g_fault_injection.load()};
     a.dtype = dtype;
     path = splits > 1 ? GEMM_PATH_TC_SPLITK : GEMM_PATH_TC;
-    e = launch_hgemm(a, ctx);
+    e = timed_hgemm(a, ctx);
     if (e == cudaSuccess && splits > 1)
       e = launch_splitk_reduce(dtype, Mi, Ni, splits, scratch, C, ldc, alpha, beta, ctx);
   }

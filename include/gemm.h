@@ -208,6 +208,18 @@ int64_t gemm_total_launches(void);
 int gemm_last_grid(void);
 
 /*
+ * Diagnostics: kernel timing.  With two CUDA events (cudaEvent_t, created by
+ * the caller), every later gemm(), gemm_splitk_noalloc() and
+ * gemm_strided_batched() call made from this host thread records `start` on
+ * its stream immediately before its main GEMM kernel and `end` immediately
+ * after it -- not around pre-passes (operand packing or padding) or the
+ * split-K reduction -- so cudaEventElapsedTime(start, end) is that kernel's
+ * device time for the latest call.  Passing NULL for either turns it off.  The
+ * events stay owned by the caller and must outlive their use.
+ */
+void gemm_set_kernel_events(void* start, void* end);
+
+/*
  * Test hook: the time limit, in nanoseconds, of every bounded wait inside the
  * kernels launched afterwards by this process (default 2e9, i.e. 2 s; values
  * <= 0 restore the default).  A wait that runs out sets the device status

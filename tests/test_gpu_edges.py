@@ -135,3 +135,34 @@ def test_bounded_wait_reports_timeout_and_context_survives():
     assert b.check_device_status() == b.OK
     ref, mag = oracle.gemm_ref(to_np(p.A), to_np(p.B))
     assert compare.check(to_np(C.cpu()), ref, mag, "f16", exact=True)["ok"]
+
+
+def test_kernel_events_bracket_the_gemm_kernel():
+    """gemm_set_kernel_events: the library records the caller's events around
+    its main kernel only, so on a problem with a packing pre-pass (fp32 nn
+    above the packing threshold) the kernel's time is positive and below the
+    whole call's."""
+    import torch
+    from dense_gemm_tiled_gb300 import binding
+    p = inputs.sweep_problem(2048, 2048, 2048, "nn", "f32", 0.0, seed=140)
+    A, B = p.A.cuda(), p.B.cuda()
+    C = torch.empty((2048, 2048), dtype=torch.float32, device="cuda")
+    ks, ke = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ks.record(); ke.record()
+    s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    binding.set_kernel_events(ks, ke)
+    try:
+        for _ in range(3):
+            s0.record()
+            binding.gemm(A, B, C)
+            s1.record()
+            s1.synchronize()
+    finally:
+        binding.set_kernel_events()
+    call_ms, kernel_ms = s0.elapsed_time(s1), ks.elapsed_time(ke)
+    assert 0.0 < kernel_ms < call_ms, (kernel_ms, call_ms)
+    # turned off: the events are no longer re-recorded
+    before = ks.elapsed_time(ke)
+    binding.gemm(A, B, C)
+    torch.cuda.synchronize()
+    assert ks.elapsed_time(ke) == before
