@@ -296,9 +296,10 @@ int run_gemm(int transA, int transB, int64_t M64, int64_t N64, int64_t K64, int 
     // rounds of the SMs leaves the last round part-empty (4096^3: 1024 tiles,
     // 6.7 rounds of 152).  The persistent launch gives whole tiles to all but
     // the last one to two rounds and shares those rounds' K steps evenly.
-    const bool sk = splits == 1 && sg_sk_enabled() && tiles >= sms && tiles % sms != 0;
-    const int64_t sk_tiles = sk ? (tiles >= 2 * sms ? tiles % sms + sms : tiles) : 0;
-    const size_t bytes_S = sk ? (size_t)sms * 2 * SG_BM * SG_BN * sizeof(float) : 0;
+    const int64_t G = (int64_t)sms * SG_BLOCKS_PER_SM;  // resident blocks
+    const bool sk = splits == 1 && sg_sk_enabled() && tiles >= G && tiles % G != 0;
+    const int64_t sk_tiles = sk ? (tiles >= 2 * G ? tiles % G + G : tiles) : 0;
+    const size_t bytes_S = sk ? (size_t)G * 2 * SG_BM * SG_BN * sizeof(float) : 0;
     const size_t bytes_N = sk ? ((size_t)sk_tiles * sizeof(unsigned int) + 255) / 256 * 256 : 0;
     Scratch ws;
     if (bytes_A + bytes_B + bytes_P + bytes_S + bytes_N > 0) {
@@ -307,7 +308,7 @@ int run_gemm(int transA, int transB, int64_t M64, int64_t N64, int64_t K64, int 
     }
     if (splits > 1) a.partial = (float*)((char*)ws.ptr + bytes_A + bytes_B);
     if (sk) {
-      a.sk_blocks = sms;
+      a.sk_blocks = (int)G;
       a.sk_ws = (float*)((char*)ws.ptr + bytes_A + bytes_B + bytes_P);
       a.sk_cnt = (unsigned int*)((char*)a.sk_ws + bytes_S);
       e = cudaMemsetAsync(a.sk_cnt, 0, (size_t)sk_tiles * sizeof(unsigned int), stream);

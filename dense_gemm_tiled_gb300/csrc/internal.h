@@ -98,7 +98,8 @@ cudaError_t launch_repack_16(int rows, int cols, const void* src, int64_t ld_src
                              int64_t ld_dst, LaunchCtx& ctx);
 
 // Tile sizes the dispatcher needs.
-// fp32 block tile: (64 * SG_WARPS_M) x 128, K step 32
+// fp32 block tile: (64 * SG_WARPS_M) x SG_BN, K step SG_BK, SG_BLOCKS_PER_SM
+// resident blocks per SM (compile-time knobs; the defaults measured fastest)
 #ifndef GB300_SG_WARPS_M
 #define GB300_SG_WARPS_M 2
 #endif
@@ -106,7 +107,14 @@ constexpr int SG_WARPS_M = GB300_SG_WARPS_M;
 #ifndef GB300_SG_BK
 #define GB300_SG_BK 64
 #endif
-constexpr int SG_BM = 64 * SG_WARPS_M, SG_BN = 128, SG_BK = GB300_SG_BK;
+#ifndef GB300_SG_BN
+#define GB300_SG_BN 128
+#endif
+#ifndef GB300_SG_MIN_BLOCKS
+#define GB300_SG_MIN_BLOCKS 1
+#endif
+constexpr int SG_BM = 64 * SG_WARPS_M, SG_BN = GB300_SG_BN, SG_BK = GB300_SG_BK;
+constexpr int SG_BLOCKS_PER_SM = GB300_SG_MIN_BLOCKS;
 constexpr int HG_BM = 128, HG_BK = 64;
 int hgemm_pick_bn(int M, int N, int transB, int num_sms, int batch = 1);
 bool hgemm_use_pair(int bn, int M, int splits, int allowed);

@@ -40,8 +40,9 @@ namespace gb300 {
 namespace {
 
 constexpr int BM = SG_BM, BN = SG_BN, BK = SG_BK;
-constexpr int WARPS_M = SG_WARPS_M;          // warps along m (each 64 rows); 4 along n
-constexpr int THREADS = 128 * WARPS_M;
+constexpr int WARPS_M = SG_WARPS_M;  // warps along m (each 64 rows)
+constexpr int WARPS_N = BN / 32;     // warps along n (each 32 columns)
+constexpr int THREADS = 32 * WARPS_M * WARPS_N;
 #ifndef GB300_SG_STAGES
 #define GB300_SG_STAGES 3
 #endif
@@ -58,17 +59,18 @@ constexpr int SMEM_BYTES = STAGES * STAGE_FLOATS * 4;  // 195 KiB at BK 64, 3 st
 // (32 MB): measured at 4096^3, 8-row groups read 352 MB from DRAM and 32-row
 // groups (64 MB of A panels) 520 MB -- the L2 is split between the two dies.
 constexpr int64_t RASTER_L2_BYTES = 32ll << 20;
-static_assert(BM == 64 * WARPS_M && BN == 128 && (BK == 16 || BK == 32 || BK == 64),
+static_assert(BM == 64 * WARPS_M && (BN == 64 || BN == 128) &&
+                  (BK == 16 || BK == 32 || BK == 64),
               "tile shape");
 
 // Compile-time tuning knobs (measured on GB300 at 4096^3; the defaults won;
 // K step and stage count are GB300_SG_BK in internal.h and GB300_SG_STAGES:
-// 64 x 3 beat 32 x 3, 32 x 4, 64 x 2 and 16 x 6 by 0.4-5 %):
+// 64 x 3 beat 32 x 3, 32 x 4, 64 x 2 and 16 x 6 by 0.4-5 %; 128 x 64 tiles
+// at two blocks per SM (GB300_SG_BN=64, GB300_SG_MIN_BLOCKS=2) were 1-3 %
+// slower; loading the next K step's fragments into a second register set
+// gained nothing):
 //  GB300_SG_MIN_BLOCKS  blocks per SM the register budget is sized for
 //  GB300_SG_KC_UNROLL   unrolling of the 4-k chunk loop
-#ifndef GB300_SG_MIN_BLOCKS
-#define GB300_SG_MIN_BLOCKS 1
-#endif
 #ifndef GB300_SG_KC_UNROLL
 #define GB300_SG_KC_UNROLL 8
 #endif
@@ -258,8 +260,8 @@ __global__ void __launch_bounds__(THREADS, GB300_SG_MIN_BLOCKS) sgemm_ffma_kerne
   __shared__ int s_last;
   const int tid = threadIdx.x;
   const int warp = tid >> 5, lane = tid & 31;
-  const int wm = (warp >> 2) * 64;  // warp's first row in the tile
-  const int wn = (warp & 3) * 32;   // warp's first column
+  const int wm = (warp / WARPS_N) * 64;  // warp's first row in the tile
+  const int wn = (warp % WARPS_N) * 32;  // warp's first column
   const int ty = lane >> 2, tx = lane & 3;
   const int arow = wm + ty * 4;     // lane rows: arow + {0..3}, arow + 32 + {0..3}
   const int bcol = wn + tx * 4;     // lane cols: bcol + {0..3}, bcol + 16 + {0..3}
@@ -508,6 +510,10 @@ cudaError_t launch_one(const Params& p, dim3 grid, cudaStream_t stream) {
   auto kern = sgemm_ffma_kernel<A_K, B_K, VEC, KIND>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        SMEM_BYTES);
+  // several resident blocks need the largest shared-memory carve-out
+  if (e == cudaSuccess && SG_BLOCKS_PER_SM > 1)
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout,
+                             (int)cudaSharedmemCarveoutMaxShared);
   if (e != cudaSuccess) return e;
   kern<<<grid, THREADS, SMEM_BYTES, stream>>>(p);
   return cudaGetLastError();
