@@ -83,7 +83,7 @@ constexpr int UMMA_K = 16;    // K per tcgen05.mma kind::f16
 constexpr int THREADS = 192;
 constexpr int GROUP_M = 8;
 constexpr int A_TILE_BYTES = BM * BK * 2;  // 16 KiB
-constexpr int SMEM_BUDGET = 200 * 1024;
+constexpr int SMEM_LIMIT = 227 * 1024;  // opt-in shared memory per block
 
 // MODE: 0 = single blocks; 1 = pairs of blocks sharing each B tile by TMA
 // multicast (each block still holds the whole B tile); 2 = pairs running
@@ -96,12 +96,17 @@ struct Cfg {
   static constexpr int B_COLS = B_MN ? (BN < 64 ? 64 : BN) : BN;
   static constexpr int B_TILE_BYTES = (MODE == 2 ? B_COLS / 2 : B_COLS) * BK * 2;
   static constexpr int STAGE_BYTES = A_TILE_BYTES + B_TILE_BYTES;
-  static constexpr int STAGES_RAW = SMEM_BUDGET / STAGE_BYTES;
+  // C staging for TMA stores: per epilogue warp NBUF buffers of a 32 x 64
+  // 16-bit box (4 KiB); two buffers unless that would cost a stage
+  static constexpr int FIXED_BYTES = 1024 /*align*/ + 256 /*barriers*/;
+  static constexpr int STAGES2 = (SMEM_LIMIT - FIXED_BYTES - 4 * 2 * 4096) / STAGE_BYTES;
+  static constexpr int STAGES1 = (SMEM_LIMIT - FIXED_BYTES - 4 * 1 * 4096) / STAGE_BYTES;
+  static constexpr int NBUF = (STAGES2 >= 8 || STAGES2 == STAGES1) ? 2 : 1;
+  static constexpr int STAGES_RAW = NBUF == 2 ? STAGES2 : STAGES1;
   static constexpr int STAGES = STAGES_RAW > 8 ? 8 : STAGES_RAW;
   // two accumulator buffers of BN fp32 columns, rounded up to a power of two
   static constexpr int TMEM_COLS = 2 * BN <= 64 ? 64 : 2 * BN <= 128 ? 128 : 2 * BN <= 256 ? 256 : 512;
-  // + 4 epilogue warps x 2 buffers x (32 x 32 fp16) staging for TMA stores of C
-  static constexpr int STAGING_BYTES = 4 * 2 * 2048;
+  static constexpr int STAGING_BYTES = 4 * NBUF * 4096;
   static constexpr int SMEM_BYTES =
       STAGES * STAGE_BYTES + STAGING_BYTES + 1024 /*align*/ + 256 /*barriers*/;
 };
@@ -275,7 +280,7 @@ __global__ void __launch_bounds__(THREADS, 1)
   const uint32_t raw_addr = smem_u32(smem_raw);
   const uint32_t tiles_addr = (raw_addr + 1023u) & ~1023u;  // swizzle atoms need 1 KiB alignment
   uint8_t* const tiles_ptr = smem_raw + (tiles_addr - raw_addr);
-  // C staging (1 KiB aligned: the 64-byte swizzle pattern repeats every 512 B)
+  // C staging (1 KiB aligned: the 128-byte swizzle pattern repeats every 1 KiB)
   const uint32_t staging_addr = tiles_addr + (uint32_t)(STAGES * C_::STAGE_BYTES);
   uint8_t* const staging_ptr = tiles_ptr + STAGES * C_::STAGE_BYTES;
   uint64_t* const bars = reinterpret_cast<uint64_t*>(staging_ptr + C_::STAGING_BYTES);
@@ -488,6 +493,54 @@ __global__ void __launch_bounds__(THREADS, 1)
       float* const tail_strip =
           tail >= 0 ? p.tail_ws + ((((int64_t)(tail * P + rank) * p.tail_splits + z) * 4 + q) * STRIP)
                     : nullptr;
+      if (!SPLIT && tail < 0 && p.c_tma) {
+        // C through TMA stores, 64 columns at a time: two tensor-memory loads
+        // in flight, the 32 x 64 16-bit block packed into this warp's staging
+        // buffer in the 128-byte swizzle (16-byte chunk w of row l at chunk
+        // w ^ (l & 7): the 8 lanes of each store phase hit distinct banks),
+        // then one TMA store clipped by the unit at M and N
+        constexpr int NB = C_::NBUF;
+#pragma unroll 1
+        for (int c = 0; c < BN / 32; c += 2) {
+          uint32_t r0[32], r1[32];
+          __syncwarp();
+          tmem_ld_32x32b_x32(t_row + (uint32_t)(c * 32), r0);
+          tmem_ld_32x32b_x32(t_row + (uint32_t)(c * 32 + 32), r1);
+          tmem_ld_wait();
+          if (c + 2 >= BN / 32) {
+            tc_fence_before();
+            if constexpr (TWO_SM) mbar_arrive_cluster(mapa_shared(acce_bar(buf), 0u));
+            else mbar_arrive(acce_bar(buf));
+          }
+          const int gn0 = n0 + c * 32;
+          const uint32_t sbuf = staging_addr + (uint32_t)((q * NB + (c / 2) % NB) * 4096);
+          if (lane == 0) bulk_wait_read<NB - 1>();  // this buffer's previous store has read it
+          __syncwarp();
+#pragma unroll
+          for (int w = 0; w < 8; ++w) {
+            const uint32_t* rr = w < 4 ? r0 + 8 * w : r1 + 8 * (w - 4);
+            uint4 o;
+            typename Elem<T>::T2* oh = reinterpret_cast<typename Elem<T>::T2*>(&o);
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+              oh[e] = Elem<T>::pack(p.alpha * __uint_as_float(rr[2 * e]),
+                                    p.alpha * __uint_as_float(rr[2 * e + 1]));
+            const uint32_t dst = sbuf + (uint32_t)(lane * 128 + ((w ^ (lane & 7)) * 16));
+            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(dst), "r"(o.x),
+                         "r"(o.y), "r"(o.z), "r"(o.w)
+                         : "memory");
+          }
+          fence_proxy_async_smem();
+          __syncwarp();
+          // (a block wholly past M or N -- the second tile of a pair on an odd
+          // tile-row count -- is not stored at all)
+          if (lane == 0 && m0 + q * 32 < p.M && gn0 < p.N) {
+            tma_store_3d(&tmC, gn0, m0 + q * 32, bz, sbuf);
+            bulk_commit();
+          }
+        }
+        continue;
+      }
 #pragma unroll 1
       for (int c = 0; c < BN / 32; ++c) {
         uint32_t r[32];
@@ -510,9 +563,8 @@ __global__ void __launch_bounds__(THREADS, 1)
           continue;
         }
         const int gn0 = n0 + c * 32;
-        // rows past M: loaded (warp-collective) but not stored; the TMA path
-        // stays warp-uniform and lets the unit clip them
-        if (gm >= p.M && !(p.c_tma && !SPLIT)) continue;
+        // rows past M: loaded (warp-collective) but not stored
+        if (gm >= p.M) continue;
         if constexpr (SPLIT) {
           float* dst = p.partial + ((int64_t)z * p.M + gm) * p.N + gn0;
           if (gn0 + 31 < p.N && (p.N & 3) == 0) {
@@ -524,35 +576,6 @@ __global__ void __launch_bounds__(THREADS, 1)
           } else {
             for (int j = 0; j < 32; ++j)
               if (gn0 + j < p.N) dst[j] = __uint_as_float(r[j]);
-          }
-        } else if (p.c_tma) {
-          // fp16 row segment -> this warp's staging buffer (64-byte swizzle:
-          // 16-byte chunk w of row l sits at chunk w ^ ((l >> 1) & 3), so the
-          // 8 lanes of each store phase hit distinct banks) -> TMA store of the
-          // 32 x 32 block, clipped by the unit at M and N
-          const uint32_t sbuf = staging_addr + (uint32_t)((q * 2 + (c & 1)) * 2048);
-          if (lane == 0) bulk_wait_read<1>();  // this buffer's previous store has read it
-          __syncwarp();
-#pragma unroll
-          for (int w = 0; w < 4; ++w) {
-            uint4 o;
-            typename Elem<T>::T2* oh = reinterpret_cast<typename Elem<T>::T2*>(&o);
-#pragma unroll
-            for (int e = 0; e < 4; ++e)
-              oh[e] = Elem<T>::pack(p.alpha * __uint_as_float(r[8 * w + 2 * e]),
-                                    p.alpha * __uint_as_float(r[8 * w + 2 * e + 1]));
-            const uint32_t dst = sbuf + (uint32_t)(lane * 64 + ((w ^ ((lane >> 1) & 3)) * 16));
-            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(dst), "r"(o.x),
-                         "r"(o.y), "r"(o.z), "r"(o.w)
-                         : "memory");
-          }
-          fence_proxy_async_smem();
-          __syncwarp();
-          // (a block wholly past M or N -- the second tile of a pair on an odd
-          // tile-row count -- is not stored at all)
-          if (lane == 0 && m0 + q * 32 < p.M && gn0 < p.N) {
-            tma_store_3d(&tmC, gn0, m0 + q * 32, bz, sbuf);
-            bulk_commit();
           }
         } else {
           float v[32];
@@ -706,10 +729,10 @@ cudaError_t launch_cfg(const HgemmArgs& a, const HParams& p, LaunchCtx& ctx) {
   else ok = make_map(&mB, TY, a.B, a.N, a.K, a.ldb, 64, PAIR ? BN / 2 : BN, SW, nbb,
                      a.stride_b);                                                          // [N, K]
   if (!ok) return cudaErrorNotSupported;
-  // C: row-major [M, N], 32 x 32 boxes, 64-byte swizzle (used only when p.c_tma)
+  // C: row-major [M, N], 64 x 32 boxes, 128-byte swizzle (used only when p.c_tma)
   CUtensorMap mC;
   memset(&mC, 0, sizeof(mC));
-  if (p.c_tma && !make_map(&mC, TY, a.C, a.M, a.N, a.ldc, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B,
+  if (p.c_tma && !make_map(&mC, TY, a.C, a.M, a.N, a.ldc, 64, 32, CU_TENSOR_MAP_SWIZZLE_128B,
                            p.batch, p.stride_c))
     return cudaErrorNotSupported;
   auto kern = hgemm_tc_kernel<T, BN, A_MN, B_MN, SPLIT, MODE>;
@@ -786,7 +809,7 @@ cudaError_t launch_hgemm_t(const HgemmArgs& a, LaunchCtx& ctx) {
   p.fault_injection = a.fault_injection;
   p.c_vec_ok = ((reinterpret_cast<uintptr_t>(a.C) & 15u) == 0 && (a.ldc % 8) == 0 &&
                 (a.batch <= 1 || (a.stride_c % 8) == 0)) ? 1 : 0;
-  p.c_tma = (p.c_vec_ok && a.beta == 0.f && a.splits <= 1 && a.c_tma) ? 1 : 0;
+  p.c_tma = (p.c_vec_ok && a.beta == 0.f && a.splits <= 1 && a.c_tma && bn >= 64) ? 1 : 0;
   p.pair = hgemm_use_pair(bn, a.M, p.splits, a.pair) ? a.pair : 0;
   p.dp_units = a.dp_units;
   p.tail_splits = a.tail_splits;
