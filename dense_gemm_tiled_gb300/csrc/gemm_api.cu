@@ -130,6 +130,16 @@ int check_args(int transA, int transB, int64_t M, int64_t N, int64_t K, int dtyp
   return GEMM_OK;
 }
 
+// gemm_host's copy/compute overlap (env GEMM_GB300_HOST_PIPELINE=0 turns it
+// off).
+int host_pipeline_enabled() {
+  static const int v = [] {
+    const char* s = getenv("GEMM_GB300_HOST_PIPELINE");
+    return (s && s[0] == '0') ? 0 : 1;
+  }();
+  return v;
+}
+
 // fp32 stream-K persistent launch (env GEMM_GB300_SG_SK=0 turns it off).
 int sg_sk_enabled() {
   static const int v = [] {
@@ -410,6 +420,124 @@ int run_gemm(int transA, int transB, int64_t M64, int64_t N64, int64_t K64, int 
   return GEMM_OK;
 }
 
+// gemm_host on large problems: row panels of C, so that the copies of later
+// panels' A rows in and earlier panels' C rows out overlap the GEMMs.  One
+// copy stream each way per device, created once; ordering by events.
+cudaStream_t g_side[MAX_DEVICES][2];
+
+cudaError_t side_streams(cudaStream_t* in, cudaStream_t* out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= MAX_DEVICES) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lk(g_mu);
+  for (int i = 0; i < 2; ++i)
+    if (!g_side[dev][i]) {
+      e = cudaStreamCreateWithFlags(&g_side[dev][i], cudaStreamNonBlocking);
+      if (e != cudaSuccess) return e;
+    }
+  *in = g_side[dev][0];
+  *out = g_side[dev][1];
+  return cudaSuccess;
+}
+
+struct EventSet {
+  cudaEvent_t ev[2 * 8 + 2] = {};
+  int n = 0;
+  ~EventSet() {
+    for (int i = 0; i < n; ++i) cudaEventDestroy(ev[i]);
+  }
+  cudaError_t make(int count) {
+    for (; n < count; ++n) {
+      cudaError_t e = cudaEventCreateWithFlags(&ev[n], cudaEventDisableTiming);
+      if (e != cudaSuccess) return e;
+    }
+    return cudaSuccess;
+  }
+};
+
+// Host buffers in, `panels` row panels of C computed and copied out as each
+// finishes; returns after the caller's stream has synchronised.
+int host_pipelined(int transA, int transB, int64_t M, int64_t N, int64_t K, int dtype,
+                   float alpha, float beta, const void* A, int64_t lda, const void* B,
+                   int64_t ldb, void* C, int64_t ldc, cudaStream_t stream, int64_t ar,
+                   int64_t ac, int64_t br, int64_t bc, int panels) {
+  const int64_t e = dtype == GEMM_F32 ? 4 : 2;
+  const int64_t align = 16 / e;
+  const int64_t lda_d = (ac + align - 1) / align * align;
+  const int64_t ldb_d = (bc + align - 1) / align * align;
+  const int64_t ldc_d = (N + align - 1) / align * align;
+  const size_t nA = (size_t)(ar * lda_d * e + 255) / 256 * 256;
+  const size_t nB = (size_t)(br * ldb_d * e + 255) / 256 * 256;
+  const size_t nC = (size_t)(M * ldc_d * e + 255) / 256 * 256;
+  cudaStream_t sin, sout;
+  cudaError_t ce = side_streams(&sin, &sout);
+  if (ce != cudaSuccess) return cuda_fail(ce);
+  EventSet evs;
+  ce = evs.make(2 * panels + 2);
+  if (ce != cudaSuccess) return cuda_fail(ce);
+  Scratch buf;
+  ce = buf.get(nA + nB + nC, stream);
+  if (ce != cudaSuccess) return cuda_fail(ce);
+  char* dA = (char*)buf.ptr;
+  char* dB = dA + nA;
+  char* dC = dB + nB;
+  cudaEvent_t ev_alloc = evs.ev[2 * panels], ev_out = evs.ev[2 * panels + 1];
+  // rows per panel: a whole number of 128-row tiles
+  const int64_t pr = ((M + panels - 1) / panels + 127) / 128 * 128;
+  int path = GEMM_PATH_NONE, launches = 0;
+  ce = cudaEventRecord(ev_alloc, stream);
+  if (ce == cudaSuccess) ce = cudaStreamWaitEvent(sin, ev_alloc, 0);
+  if (ce == cudaSuccess) ce = cudaStreamWaitEvent(sout, ev_alloc, 0);
+  if (ce == cudaSuccess)
+    ce = cudaMemcpy2DAsync(dB, ldb_d * e, B, ldb * e, bc * e, br, cudaMemcpyHostToDevice, sin);
+  int rc = GEMM_OK;
+  for (int p = 0; p < panels && ce == cudaSuccess && rc == GEMM_OK; ++p) {
+    const int64_t r0 = p * pr, r1 = r0 + pr < M ? r0 + pr : M;
+    if (r0 >= M) break;
+    const int64_t mp = r1 - r0;
+    // A rows r0..r1 of op(A): rows of A[M,K], or columns of A[K,M]
+    const char* srcA = static_cast<const char*>(A) + (transA ? r0 * e : r0 * lda * e);
+    char* dstA = dA + (transA ? r0 * e : r0 * lda_d * e);
+    ce = transA ? cudaMemcpy2DAsync(dstA, lda_d * e, srcA, lda * e, mp * e, ar,
+                                    cudaMemcpyHostToDevice, sin)
+                : cudaMemcpy2DAsync(dstA, lda_d * e, srcA, lda * e, ac * e, mp,
+                                    cudaMemcpyHostToDevice, sin);
+    char* dCp = dC + r0 * ldc_d * e;
+    char* hCp = static_cast<char*>(C) + r0 * ldc * e;
+    if (ce == cudaSuccess && beta != 0.f)
+      ce = cudaMemcpy2DAsync(dCp, ldc_d * e, hCp, ldc * e, N * e, mp, cudaMemcpyHostToDevice, sin);
+    if (ce == cudaSuccess) ce = cudaEventRecord(evs.ev[2 * p], sin);
+    if (ce == cudaSuccess) ce = cudaStreamWaitEvent(stream, evs.ev[2 * p], 0);
+    if (ce != cudaSuccess) break;
+    rc = run_gemm(transA, transB, mp, N, K, dtype, alpha, beta, dstA, lda_d, dB, ldb_d, dCp,
+                  ldc_d, stream, transA ? K : mp, transA ? mp : K, br, bc);
+    if (rc != GEMM_OK) break;
+    path = tl_last_path;
+    launches += tl_last_launches;
+    ce = cudaEventRecord(evs.ev[2 * p + 1], stream);
+    if (ce == cudaSuccess) ce = cudaStreamWaitEvent(sout, evs.ev[2 * p + 1], 0);
+    if (ce == cudaSuccess)
+      ce = cudaMemcpy2DAsync(hCp, ldc * e, dCp, ldc_d * e, N * e, mp, cudaMemcpyDeviceToHost,
+                             sout);
+  }
+  // the caller's stream takes over both copy streams' work before the buffer
+  // is released on it
+  cudaError_t ce2 = cudaEventRecord(ev_out, sout);
+  if (ce2 == cudaSuccess) ce2 = cudaStreamWaitEvent(stream, ev_out, 0);
+  cudaError_t ce3 = cudaEventRecord(ev_alloc, sin);
+  if (ce3 == cudaSuccess) ce3 = cudaStreamWaitEvent(stream, ev_alloc, 0);
+  cudaFreeAsync(buf.ptr, stream);
+  buf.ptr = nullptr;
+  cudaError_t ce4 = cudaStreamSynchronize(stream);
+  if (rc != GEMM_OK) return rc;
+  if (ce != cudaSuccess) return cuda_fail(ce);
+  if (ce2 != cudaSuccess || ce3 != cudaSuccess || ce4 != cudaSuccess) return GEMM_ERR_CUDA;
+  tl_last_path = path;
+  tl_last_launches = launches;
+  return GEMM_OK;
+}
+
 // Strided batch (gemm_strided_batched): one launch over the whole batch when
 // the operands allow it, else entry by entry through run_gemm.  Arguments
 // already checked; batch >= 2, M, N > 0.
@@ -573,6 +701,10 @@ int gemm_host(int transA, int transB, int64_t M, int64_t N, int64_t K, int dtype
   if (rc != GEMM_OK) return rc;
   if (M == 0 || N == 0) return GEMM_OK;
   cudaStream_t stream = (cudaStream_t)stream_;
+  // large problems: copies overlapped with the GEMMs of row panels
+  if (K > 0 && M >= 256 && (double)M * N * K >= (double)(1ll << 30) && host_pipeline_enabled())
+    return host_pipelined(transA, transB, M, N, K, dtype, alpha, beta, A, lda, B, ldb, C, ldc,
+                          stream, ar, ac, br, bc, M >= 4096 ? 4 : 2);
   const int64_t e = dtype == GEMM_F32 ? 4 : 2;
   const int64_t align = 16 / e;  // device pitch: whole 16-byte units
   const int64_t lda_d = (ac + align - 1) / align * align;

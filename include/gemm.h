@@ -98,7 +98,11 @@ int gemm(int transA, int transB, int64_t M, int64_t N, int64_t K, int dtype, flo
  * gemm_host -- the same product on HOST buffers: copies A, B (and C when
  * beta != 0) to device memory taken from the stream-ordered allocator, runs
  * gemm() on `stream`, copies C back and synchronises `stream` before it
- * returns.  A, B, C are host pointers with the same layout rules as gemm();
+ * returns.  Problems of at least 2^30 multiply-adds are cut into 2 to 4 row
+ * panels of C whose copies run on two library-owned copy streams (one per
+ * direction, per device), ordered by events against the GEMMs on `stream`, so
+ * that copies overlap computation; the call still returns only when C is
+ * complete in host memory.  A, B, C are host pointers with the same layout rules as gemm();
  * page-locked (pinned) memory gives asynchronous DMA copies, pageable memory
  * works but is staged by the driver.  The device copies are packed (ld equal
  * to the row length) and freed before return.

@@ -166,3 +166,27 @@ def test_kernel_events_bracket_the_gemm_kernel():
     binding.gemm(A, B, C)
     torch.cuda.synchronize()
     assert ks.elapsed_time(ke) == before
+
+
+@pytest.mark.parametrize("dtype,variant,M", [("f32", "nn", 1024), ("f32", "tn", 1000),
+                                             ("f32", "nt", 4096), ("f16", "tn", 1000),
+                                             ("bf16", "nn", 2048)])
+def test_gemm_host_pipelined(dtype, variant, M):
+    """gemm_host on problems of at least 2^30 multiply-adds runs row panels of
+    C on the device while later panels' A rows are still arriving and earlier
+    panels' C rows are leaving (two copy streams); every panel must match the
+    oracle, beta included."""
+    b = _b()
+    N, K = 1536, 1024 if M < 4096 else 256
+    p = inputs.sweep_problem(M, N, K, variant, dtype, 0.5, seed=345)
+    A, B = p.A.pin_memory(), p.B.pin_memory()
+    C = p.C_in.clone().pin_memory()
+    b.gemm_host(A, B, C, p.transA, p.transB, p.alpha, p.beta)
+    full = M * N * K <= (1 << 31)
+    from helpers import oracle_for
+    ref, mag, idx = oracle_for(p, full=full, seed=3)
+    got = to_np(C)
+    if idx is not None:
+        got = got[idx[0], idx[1]]
+    res = compare.check(got, ref, mag, dtype)
+    assert res["ok"], res
