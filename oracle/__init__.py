@@ -37,6 +37,10 @@ def bind(path: str):
     lib.oracle_gemm_points.argtypes = [ci, ci, i64, i64, i64, ci, dbl, dbl, vp, i64, vp, i64,
                                        vp, i64, vp, vp, i64, vp, vp, ci]
     lib.oracle_gemm_points.restype = ci
+    lib.oracle_bias_act.argtypes = [vp, i64, i64, i64, vp, ci]
+    lib.oracle_bias_act.restype = ci
+    lib.oracle_gelu.argtypes = [dbl]
+    lib.oracle_gelu.restype = dbl
     lib.oracle_half_to_double.argtypes = [ctypes.c_uint16]
     lib.oracle_half_to_double.restype = dbl
     lib.oracle_double_to_half_rne.argtypes = [dbl]
@@ -152,6 +156,40 @@ def gemm_ref_points(A, B, rows, cols, C=None, transA=False, transB=False, alpha=
     if rc != 0:
         raise RuntimeError(f"oracle_gemm_points failed with code {rc}")
     return ref, mag
+
+
+ACTS = {"none": 0, "relu": 1, "gelu": 2}
+
+
+def bias_act(x, bias=None, act="none", cols_index=None):
+    """act(x + bias[j]) elementwise in double ("From a C loop to a GPU kernel",
+    section "Fusion": per-output bias, then the activation).  x: float64 [M, N]
+    (or [npts] with cols_index giving each point's column); bias: None or a
+    length-N array of any oracle dtype (bfloat16 as uint16 with fmt handled by
+    the caller: pass float64 values); act: 'none', 'relu' or 'gelu' (exact,
+    v * Phi(v)).  Returns a new float64 array."""
+    x = np.array(x, dtype=np.float64, copy=True)
+    b = None if bias is None else np.ascontiguousarray(bias, dtype=np.float64)
+    if x.ndim == 1:
+        # points: one row whose k-th entry takes the bias of its own column
+        if b is not None:
+            b = np.ascontiguousarray(b[np.asarray(cols_index, dtype=np.int64)])
+        x2 = x.reshape(1, -1)
+    else:
+        x2 = x
+    rows, cols = x2.shape
+    rc = _load().oracle_bias_act(x2.ctypes.data, rows, cols, cols,
+                                 None if b is None else b.ctypes.data, ACTS[act])
+    if rc != 0:
+        raise RuntimeError("oracle_bias_act failed")
+    return x2.reshape(x.shape)
+
+
+def gelu(v):
+    """The oracle's exact gelu, elementwise (float64)."""
+    v = np.ascontiguousarray(v, dtype=np.float64)
+    f = _load().oracle_gelu
+    return np.vectorize(lambda t: f(float(t)))(v)
 
 
 def half_to_double(h) -> np.ndarray:

@@ -84,3 +84,56 @@ def check(C, ref, mag, dtype: str, exact: bool = False) -> dict:
         "max_abs_err": float(np.nanmax(err)) if err.size and not np.all(np.isnan(err)) else
         (float("nan") if err.size else 0.0),
     }
+
+
+GELU_LIPSCHITZ = 1.13  # max |d/dv v*Phi(v)| = 1.1289 (at v = sqrt(2))
+EPI_ARITH = 2.0 ** -22  # the fp32 additions of alpha*acc, beta*C and the bias
+GELU_EVAL = 2.0 ** -20  # fp32 evaluation of v/2 * (1 + erf(v / sqrt(2)))
+
+
+def check_epilogue(C, ref_pre, mag, dtype: str, bias=None, act: str = "none", exact=False,
+                   cols_index=None) -> dict:
+    """Compare a fused-epilogue result C = act(alpha*AB + beta*C_in + bias[j])
+    with the oracle ("From a C loop to a GPU kernel", section "Fusion").
+
+    ref_pre, mag: the oracle's GEMM result and magnitude (before bias and
+    activation); bias: float64 values per column or None; act: none, relu or
+    gelu.  The bound propagates the GEMM bound through the activation (relu
+    and identity are 1-Lipschitz, gelu 1.13-Lipschitz), adds the fp32
+    rounding of the epilogue's additions and, for gelu, of its evaluation,
+    then the output rounding of 16-bit results as check() does:
+      bound = L * (rel(dtype) * mag + 2^-22 * (mag + |bias_j|))
+              + [gelu] 2^-20 * (|x| + |out|) + out_rounding(dtype, |out|)
+    with x = ref_pre + bias_j and out = act(x).  exact=True (small-integer
+    inputs, identity or relu): C must equal out (fp32) or RNE(out)."""
+    from . import bias_act
+    ref_pre = np.asarray(ref_pre, dtype=np.float64)
+    mag = np.asarray(mag, dtype=np.float64)
+    out = bias_act(ref_pre, bias, act, cols_index=cols_index)
+    if exact:
+        return check(C, out, mag, dtype, exact=True)
+    if bias is None:
+        bj = np.zeros_like(ref_pre)
+    else:
+        b = np.asarray(bias, dtype=np.float64)
+        bj = b[np.asarray(cols_index)] if ref_pre.ndim == 1 else np.broadcast_to(b, ref_pre.shape)
+    x = ref_pre + bj
+    rel = F32_REL if dtype == "f32" else F16_REL
+    lip = GELU_LIPSCHITZ if act == "gelu" else 1.0
+    bound = lip * (rel * mag + EPI_ARITH * (mag + np.abs(bj)))
+    if act == "gelu":
+        bound = bound + GELU_EVAL * (np.abs(x) + np.abs(out))
+    if dtype == "f16":
+        bound = bound + F16_OUT * np.abs(out) + F16_SUB
+    elif dtype == "bf16":
+        bound = bound + BF16_OUT * np.abs(out) + BF16_SUB
+    Cd = as_double(C, dtype).reshape(out.shape)
+    err = np.abs(Cd - out)
+    bad = ~(err <= bound)
+    nbad = int(np.count_nonzero(bad))
+    with np.errstate(divide="ignore", invalid="ignore"):
+        ratio = np.where(bound > 0, err / bound, np.where(err == 0, 0.0, np.inf))
+    ratio = np.where(np.isnan(err), np.inf, ratio)
+    return {"ok": nbad == 0, "n": int(out.size), "bad": nbad,
+            "worst_ratio": float(ratio.max()) if ratio.size else 0.0,
+            "max_abs_err": float(np.nanmax(err)) if err.size else 0.0}

@@ -253,6 +253,41 @@ int oracle_gemm(int transA, int transB, int64_t M, int64_t N, int64_t K, int dty
 }
 
 /* ------------------------------------------------------------------------- */
+/* Fused epilogue: bias and activation.                                       */
+/* ------------------------------------------------------------------------- */
+/*
+ * "From a C loop to a GPU kernel", section "Fusion": after C = A @ B the fused
+ * kernel adds a learned per-output offset (bias) and applies gelu before the
+ * single write.  Per output column j (the output feature):
+ *     out[i][j] = act(x[i][j] + bias[j])
+ * with act one of
+ *     ORACLE_ACT_NONE  identity
+ *     ORACLE_ACT_RELU  max(v, 0)
+ *     ORACLE_ACT_GELU  v * Phi(v) = v/2 * (1 + erf(v / sqrt(2))), the exact
+ *                      form (the page names gelu without a formula; the
+ *                      defining expression is taken, not a tanh fit).
+ * x is rows x cols, row pitch ldx, rewritten in place; bias (cols doubles) may
+ * be NULL for no bias.  erf is the C library's.
+ */
+enum { ORACLE_ACT_NONE = 0, ORACLE_ACT_RELU = 1, ORACLE_ACT_GELU = 2 };
+
+double oracle_gelu(double v) { return 0.5 * v * (1.0 + erf(v / sqrt(2.0))); }
+
+int oracle_bias_act(double* x, int64_t rows, int64_t cols, int64_t ldx, const double* bias,
+                    int act) {
+    if (rows < 0 || cols < 0 || (rows > 0 && !x) || ldx < cols) return 1;
+    if (act != ORACLE_ACT_NONE && act != ORACLE_ACT_RELU && act != ORACLE_ACT_GELU) return 1;
+    for (int64_t i = 0; i < rows; ++i)
+        for (int64_t j = 0; j < cols; ++j) {
+            double v = x[i * ldx + j] + (bias ? bias[j] : 0.0);
+            if (act == ORACLE_ACT_RELU) v = v > 0.0 ? v : 0.0;
+            else if (act == ORACLE_ACT_GELU) v = oracle_gelu(v);
+            x[i * ldx + j] = v;
+        }
+    return 0;
+}
+
+/* ------------------------------------------------------------------------- */
 /* Selected elements only (for products too large to form in full).          */
 /* ------------------------------------------------------------------------- */
 typedef struct {

@@ -173,8 +173,49 @@ def pin_bf16_integer_exact(lib=None):
         assert np.array_equal(ref, want.astype(np.float64)), v
 
 
+EPI_GOLDEN = os.path.join(os.path.dirname(GOLDEN), "epilogue_values.json")
+
+
+def _bias_act(lib, x, bias, act):
+    l = lib or oracle._load()
+    x = np.array(x, dtype=np.float64)
+    b = np.ascontiguousarray(bias, dtype=np.float64) if bias is not None else None
+    assert l.oracle_bias_act(x.ctypes.data, x.shape[0], x.shape[1], x.shape[1],
+                             None if b is None else b.ctypes.data, oracle.ACTS[act]) == 0
+    return x
+
+
+def pin_gelu_table(lib=None):
+    """gelu(v) = v * Phi(v) against tabulated standard normal values, and the
+    identity gelu(v) - gelu(-v) = v (Phi(v) + Phi(-v) = 1)."""
+    l = lib or oracle._load()
+    for v, want in json.load(open(EPI_GOLDEN))["gelu"]:
+        got = l.oracle_gelu(v)
+        assert abs(got - want) <= 1e-15 * max(1.0, abs(want)), (v, got, want)
+    for v in np.linspace(-6, 6, 97):
+        assert abs((l.oracle_gelu(v) - l.oracle_gelu(-v)) - v) <= 1e-14 * max(1.0, abs(v))
+    # through the epilogue entry, with and without a bias
+    x = np.array([[1.0, -1.0, 2.0]])
+    got = _bias_act(lib, x, None, "gelu")
+    assert np.allclose(got, [[0.8413447460685429, -0.15865525393145707, 1.9544997361036416]],
+                       rtol=1e-15, atol=0)
+    got = _bias_act(lib, x - 1.0, np.ones(3), "gelu")
+    assert np.allclose(got, [[0.8413447460685429, -0.15865525393145707, 1.9544997361036416]],
+                       rtol=1e-15, atol=0)
+
+
+def pin_bias_per_column(lib=None):
+    """The bias is a per-output (per-column) offset, added before the
+    activation; relu is max(v, 0)."""
+    g = json.load(open(EPI_GOLDEN))["bias_act"]
+    for act in ("none", "relu"):
+        got = _bias_act(lib, g["x"], g["bias"], act)
+        assert np.array_equal(got, np.array(g[act])), (act, got)
+
+
 PINS = [pin_hand_products, pin_integer_exact, pin_transpose_identity, pin_fp16_exhaustive,
-        pin_fp16_ties_to_even, pin_bf16_exhaustive, pin_bf16_ties_to_even, pin_bf16_integer_exact]
+        pin_fp16_ties_to_even, pin_bf16_exhaustive, pin_bf16_ties_to_even, pin_bf16_integer_exact,
+        pin_gelu_table, pin_bias_per_column]
 
 
 # ---------------------------------------------------------------------------
@@ -348,6 +389,16 @@ MUTATIONS = {
                              "double r = rne_integer(ldexp(a, 132));"),
     "bf16_bias": ("return (uint16_t)(s | (uint16_t)((e + 127) << 7) | (uint16_t)((int)r - 128));",
                   "return (uint16_t)(s | (uint16_t)((e + 126) << 7) | (uint16_t)((int)r - 128));"),
+    "bias_ignored": ("double v = x[i * ldx + j] + (bias ? bias[j] : 0.0);",
+                     "double v = x[i * ldx + j];"),
+    "bias_by_row": ("double v = x[i * ldx + j] + (bias ? bias[j] : 0.0);",
+                    "double v = x[i * ldx + j] + (bias ? bias[i < cols ? i : 0] : 0.0);"),
+    "relu_keeps_negatives": ("if (act == ORACLE_ACT_RELU) v = v > 0.0 ? v : 0.0;",
+                             "if (act == ORACLE_ACT_RELU) v = v > 0.0 ? v : -v;"),
+    "gelu_tanh_fit": ("double oracle_gelu(double v) { return 0.5 * v * (1.0 + erf(v / sqrt(2.0))); }",
+                      "double oracle_gelu(double v) { return 0.5 * v * (1.0 + tanh(0.7978845608028654 * (v + 0.044715 * v * v * v))); }"),
+    "gelu_missing_sqrt2": ("double oracle_gelu(double v) { return 0.5 * v * (1.0 + erf(v / sqrt(2.0))); }",
+                           "double oracle_gelu(double v) { return 0.5 * v * (1.0 + erf(v / 2.0)); }"),
     "bf16_read_as_fp16": ("if (dtype == ORACLE_BF16) return oracle_bf16_to_double(((const uint16_t*)p)[idx]);",
                           "if (dtype == ORACLE_BF16) return oracle_half_to_double(((const uint16_t*)p)[idx]);"),
 }
@@ -371,3 +422,23 @@ def test_pins_catch_planted_mistakes(name, tmp_path):
         except AssertionError:
             failed.append(pin.__name__)
     assert failed, f"planted mistake {name} passed every pin"
+
+
+def test_checker_epilogue():
+    """check_epilogue: the oracle's own bias/activation result, rounded to the
+    output type, passes; a relative 1e-3 slip or a bias on the wrong axis
+    fails."""
+    r = _rng(9)
+    ref = r.normal(0, 2, (6, 5))
+    mag = np.abs(ref) * 4 + 1.0
+    b = r.normal(0, 1, 5)
+    for act in ("none", "relu", "gelu"):
+        out = oracle.bias_act(ref, b, act)
+        for dt, cast in (("f32", np.float32), ("f16", np.float16)):
+            assert compare.check_epilogue(out.astype(cast), ref, mag, dt, b, act)["ok"], (act, dt)
+        assert not compare.check_epilogue((out * 1.001 + 1e-3).astype(np.float32), ref, mag,
+                                          "f32", b, act)["ok"]
+    sq, msq = ref[:5], mag[:5]
+    wrong_axis = oracle.bias_act(np.ascontiguousarray(sq.T), b, "none").T  # bias along rows
+    assert not compare.check_epilogue(wrong_axis.astype(np.float32), sq, msq, "f32", b,
+                                      "none")["ok"]
