@@ -23,6 +23,8 @@ _GEMM_ARGS = [_int, _int, _i64, _i64, _i64, _int, _flt, _flt, _vp, _i64, _vp, _i
               _vp]
 _lib.gemm.argtypes = _GEMM_ARGS
 _lib.gemm.restype = _int
+_lib.gemm_ex.argtypes = _GEMM_ARGS[:-1] + [_vp, _int, _vp]
+_lib.gemm_ex.restype = _int
 _lib.gemm_host.argtypes = _GEMM_ARGS
 _lib.gemm_host.restype = _int
 _lib.gemm_strided_batched.argtypes = [_int, _int, _i64, _i64, _i64, _int, _flt, _flt, _vp, _i64,
@@ -109,6 +111,14 @@ def gemm_raw(transA, transB, M, N, K, dtype, alpha, beta, A, lda, B, ldb, C, ldc
     return _lib.gemm(int(transA), int(transB), int(M), int(N), int(K), int(dtype), float(alpha),
                      float(beta), A or None, int(lda), B or None, int(ldb), C or None, int(ldc),
                      stream or None)
+
+
+def gemm_ex_raw(transA, transB, M, N, K, dtype, alpha, beta, A, lda, B, ldb, C, ldc, bias, act,
+                stream=0) -> int:
+    """gemm_ex with plain integers (device addresses, act code)."""
+    return _lib.gemm_ex(int(transA), int(transB), int(M), int(N), int(K), int(dtype),
+                        float(alpha), float(beta), A or None, int(lda), B or None, int(ldb),
+                        C or None, int(ldc), bias or None, int(act), stream or None)
 
 
 def gemm_host_raw(transA, transB, M, N, K, dtype, alpha, beta, A, lda, B, ldb, C, ldc,
@@ -208,13 +218,20 @@ def _dims(A, B, C, transA, transB):
     return dtype, int(M), int(N), int(K)
 
 
-def gemm(A, B, C, transA=False, transB=False, alpha=1.0, beta=0.0, stream=None):
-    """C = alpha * op(A) @ op(B) + beta * C in place, on torch CUDA tensors.
+ACTS = {"none": 0, "relu": 1, "gelu": 2}
+
+
+def gemm(A, B, C, transA=False, transB=False, alpha=1.0, beta=0.0, stream=None, bias=None,
+         act="none"):
+    """C = act(alpha * op(A) @ op(B) + beta * C + bias) in place, on torch CUDA
+    tensors.
 
     A is [M,K] (or [K,M] with transA), B is [K,N] (or [N,K] with transB),
     C is [M,N]; all float32, all float16 or all bfloat16 (fp32 accumulation), rows
-    contiguous, any leading dimension.  Runs on `stream` (a torch.cuda.Stream)
-    or the current stream.  Returns C.
+    contiguous, any leading dimension.  bias: None or a contiguous CUDA tensor
+    of N elements of C's dtype (per output column); act: 'none', 'relu' or
+    'gelu'.  Runs on `stream` (a torch.cuda.Stream) or the current stream.
+    Returns C.
     """
     import torch
     dtype, M, N, K = _dims(A, B, C, transA, transB)
@@ -222,6 +239,19 @@ def gemm(A, B, C, transA=False, transB=False, alpha=1.0, beta=0.0, stream=None):
         if not t.is_cuda:
             raise ValueError("gemm() takes CUDA tensors; use gemm_host() for host memory")
     s = stream if stream is not None else torch.cuda.current_stream(C.device)
+    if bias is not None or act != "none":
+        if bias is not None:
+            if not bias.is_cuda or bias.dtype != C.dtype or bias.numel() != N or \
+                    not bias.is_contiguous():
+                raise ValueError("bias: a contiguous CUDA tensor of N elements of C's dtype")
+        rc = _lib.gemm_ex(int(transA), int(transB), M, N, K, dtype, float(alpha), float(beta),
+                          A.data_ptr() or None, _ld(A), B.data_ptr() or None, _ld(B),
+                          C.data_ptr() or None, _ld(C),
+                          (bias.data_ptr() or None) if bias is not None else None, ACTS[act],
+                          s.cuda_stream or None)
+        if rc != OK:
+            raise GemmError(rc)
+        return C
     rc = _lib.gemm(int(transA), int(transB), M, N, K, dtype, float(alpha), float(beta),
                    A.data_ptr() or None, _ld(A), B.data_ptr() or None, _ld(B),
                    C.data_ptr() or None, _ld(C), s.cuda_stream or None)

@@ -62,7 +62,7 @@ __device__ __forceinline__ float load_out(const __nv_bfloat16* C, int64_t i) {
 // float4); the general path handles one element per thread.
 template <typename T>
 __global__ void splitk_reduce_vec4(int M, int N, int splits, const float* __restrict__ P, T* C,
-                                   int64_t ldc, float alpha, float beta) {
+                                   int64_t ldc, float alpha, float beta, Epilogue ep) {
   const int64_t quads = (int64_t)M * (N / 4);
   const int64_t slice = (int64_t)M * N;
   for (int64_t q = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; q < quads;
@@ -81,14 +81,14 @@ __global__ void splitk_reduce_vec4(int M, int N, int splits, const float* __rest
     for (int j = 0; j < 4; ++j) {
       float o = alpha * v[j];
       if (beta != 0.f) o = __fmaf_rn(beta, load_out(C, base + j), o);
-      store_out(C, base + j, o);
+      store_out(C, base + j, apply_epilogue<T>(o, ep, (int)n + j));
     }
   }
 }
 
 template <typename T>
 __global__ void splitk_reduce_scalar(int M, int N, int splits, const float* __restrict__ P, T* C,
-                                     int64_t ldc, float alpha, float beta) {
+                                     int64_t ldc, float alpha, float beta, Epilogue ep) {
   const int64_t total = (int64_t)M * N;
   for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < total;
        i += (int64_t)gridDim.x * blockDim.x) {
@@ -97,18 +97,19 @@ __global__ void splitk_reduce_scalar(int M, int N, int splits, const float* __re
     for (int z = 1; z < splits; ++z) s += P[i + z * total];
     float o = alpha * s;
     if (beta != 0.f) o = __fmaf_rn(beta, load_out(C, m * ldc + n), o);
-    store_out(C, m * ldc + n, o);
+    store_out(C, m * ldc + n, apply_epilogue<T>(o, ep, (int)n));
   }
 }
 
 template <typename T>
-__global__ void scale_kernel(int M, int N, T* C, int64_t ldc, float beta) {
+__global__ void scale_kernel(int M, int N, T* C, int64_t ldc, float beta, Epilogue ep) {
   const int64_t total = (int64_t)M * N;
   for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < total;
        i += (int64_t)gridDim.x * blockDim.x) {
     const int64_t m = i / N, n = i - m * N;
     const int64_t off = m * ldc + n;
-    store_out(C, off, beta != 0.f ? beta * load_out(C, off) : 0.f);
+    const float o = beta != 0.f ? beta * load_out(C, off) : 0.f;
+    store_out(C, off, apply_epilogue<T>(o, ep, (int)n));
   }
 }
 
@@ -190,20 +191,21 @@ cudaError_t launch_transpose_f32(int rows, int cols, const float* src, int64_t l
 }
 
 cudaError_t launch_splitk_reduce(int dtype, int M, int N, int splits, const float* P, void* C,
-                                 int64_t ldc, float alpha, float beta, LaunchCtx& ctx) {
+                                 int64_t ldc, float alpha, float beta, LaunchCtx& ctx,
+                                 Epilogue ep) {
   const int threads = 256;
   const bool vec = (N % 4) == 0;
   const int64_t items = vec ? (int64_t)M * (N / 4) : (int64_t)M * N;
   const int grid = grid_for(items, threads);
   if (dtype == 0) {
-    if (vec) splitk_reduce_vec4<float><<<grid, threads, 0, ctx.stream>>>(M, N, splits, P, (float*)C, ldc, alpha, beta);
-    else splitk_reduce_scalar<float><<<grid, threads, 0, ctx.stream>>>(M, N, splits, P, (float*)C, ldc, alpha, beta);
+    if (vec) splitk_reduce_vec4<float><<<grid, threads, 0, ctx.stream>>>(M, N, splits, P, (float*)C, ldc, alpha, beta, ep);
+    else splitk_reduce_scalar<float><<<grid, threads, 0, ctx.stream>>>(M, N, splits, P, (float*)C, ldc, alpha, beta, ep);
   } else if (dtype == 1) {
-    if (vec) splitk_reduce_vec4<__half><<<grid, threads, 0, ctx.stream>>>(M, N, splits, P, (__half*)C, ldc, alpha, beta);
-    else splitk_reduce_scalar<__half><<<grid, threads, 0, ctx.stream>>>(M, N, splits, P, (__half*)C, ldc, alpha, beta);
+    if (vec) splitk_reduce_vec4<__half><<<grid, threads, 0, ctx.stream>>>(M, N, splits, P, (__half*)C, ldc, alpha, beta, ep);
+    else splitk_reduce_scalar<__half><<<grid, threads, 0, ctx.stream>>>(M, N, splits, P, (__half*)C, ldc, alpha, beta, ep);
   } else {
-    if (vec) splitk_reduce_vec4<__nv_bfloat16><<<grid, threads, 0, ctx.stream>>>(M, N, splits, P, (__nv_bfloat16*)C, ldc, alpha, beta);
-    else splitk_reduce_scalar<__nv_bfloat16><<<grid, threads, 0, ctx.stream>>>(M, N, splits, P, (__nv_bfloat16*)C, ldc, alpha, beta);
+    if (vec) splitk_reduce_vec4<__nv_bfloat16><<<grid, threads, 0, ctx.stream>>>(M, N, splits, P, (__nv_bfloat16*)C, ldc, alpha, beta, ep);
+    else splitk_reduce_scalar<__nv_bfloat16><<<grid, threads, 0, ctx.stream>>>(M, N, splits, P, (__nv_bfloat16*)C, ldc, alpha, beta, ep);
   }
   cudaError_t e = cudaGetLastError();
   if (e == cudaSuccess) ctx.launches++;
@@ -211,12 +213,12 @@ cudaError_t launch_splitk_reduce(int dtype, int M, int N, int splits, const floa
 }
 
 cudaError_t launch_scale(int dtype, int M, int N, void* C, int64_t ldc, float beta,
-                         LaunchCtx& ctx) {
+                         LaunchCtx& ctx, Epilogue ep) {
   const int threads = 256;
   const int grid = grid_for((int64_t)M * N, threads);
-  if (dtype == 0) scale_kernel<float><<<grid, threads, 0, ctx.stream>>>(M, N, (float*)C, ldc, beta);
-  else if (dtype == 1) scale_kernel<__half><<<grid, threads, 0, ctx.stream>>>(M, N, (__half*)C, ldc, beta);
-  else scale_kernel<__nv_bfloat16><<<grid, threads, 0, ctx.stream>>>(M, N, (__nv_bfloat16*)C, ldc, beta);
+  if (dtype == 0) scale_kernel<float><<<grid, threads, 0, ctx.stream>>>(M, N, (float*)C, ldc, beta, ep);
+  else if (dtype == 1) scale_kernel<__half><<<grid, threads, 0, ctx.stream>>>(M, N, (__half*)C, ldc, beta, ep);
+  else scale_kernel<__nv_bfloat16><<<grid, threads, 0, ctx.stream>>>(M, N, (__nv_bfloat16*)C, ldc, beta, ep);
   cudaError_t e = cudaGetLastError();
   if (e == cudaSuccess) ctx.launches++;
   return e;

@@ -8,9 +8,12 @@
 #pragma once
 
 #include <cuda.h>
+#include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
+
+#include "internal.h"
 
 namespace gb300 {
 
@@ -269,6 +272,29 @@ __device__ __forceinline__ void tc_commit_pair_mc(uint32_t bar, uint16_t mask) {
       " [%0], %1;" ::"r"(bar),
       "h"(mask)
       : "memory");
+}
+}  // namespace gb300
+
+namespace gb300 {
+// ---------------------------------------------------------------- fused epilogue
+// "From a C loop to a GPU kernel", section "Fusion": the per-output bias and
+// the activation are applied to the fp32 value alpha*acc + beta*C_old before
+// the single store.  act: 0 none, 1 relu (max(v, 0)), 2 gelu (v * Phi(v) =
+// v/2 * (1 + erf(v / sqrt 2)), CUDA's erff).
+__device__ __forceinline__ float bias_value(const float* b, int j) { return __ldg(b + j); }
+__device__ __forceinline__ float bias_value(const __half* b, int j) { return __half2float(b[j]); }
+__device__ __forceinline__ float bias_value(const __nv_bfloat16* b, int j) {
+  return __bfloat162float(b[j]);
+}
+__device__ __forceinline__ float apply_act(float v, int act) {
+  if (act == 1) return v > 0.f ? v : 0.f;
+  if (act == 2) return 0.5f * v * (1.f + erff(v * 0.70710678118654752f));
+  return v;
+}
+template <typename T>
+__device__ __forceinline__ float apply_epilogue(float v, const Epilogue& e, int col) {
+  if (e.bias) v += bias_value(static_cast<const T*>(e.bias), col);
+  return apply_act(v, e.act);
 }
 }  // namespace gb300
 

@@ -273,7 +273,7 @@ struct Scratch {
 int run_gemm(int transA, int transB, int64_t M64, int64_t N64, int64_t K64, int dtype,
              float alpha, float beta, const void* A, int64_t lda, const void* B, int64_t ldb,
              void* C, int64_t ldc, cudaStream_t stream, int64_t a_rows, int64_t a_cols,
-             int64_t b_rows, int64_t b_cols) {
+             int64_t b_rows, int64_t b_cols, Epilogue ep = Epilogue()) {
   int dev, sms;
   unsigned int* status;
   int rc = device_state(&dev, &status, &sms);
@@ -285,13 +285,14 @@ int run_gemm(int transA, int transB, int64_t M64, int64_t N64, int64_t K64, int 
 
   if (K == 0) {
     path = GEMM_PATH_SCALE;
-    e = launch_scale(dtype, M, N, C, ldc, beta, ctx);
+    e = launch_scale(dtype, M, N, C, ldc, beta, ctx, ep);
   } else if (dtype == GEMM_F32) {
     const int64_t tiles = (int64_t)((M + SG_BM - 1) / SG_BM) * ((N + SG_BN - 1) / SG_BN);
     int splits, k_slice;
     plan_splits(tiles, K, SG_BK, 2 * sms, 4, 16, &splits, &k_slice);
     SgemmArgs a{transA, transB, M, N, K, (const float*)A, lda, (const float*)B, ldb, (float*)C,
                 ldc, alpha, beta, splits, k_slice, nullptr};
+    if (splits == 1) a.ep = ep;  // split-K: the reduction applies it
     // Packing: the kernel reads A stored [K,M] and B stored [K,N] fastest
     // (measured at 4096^3: tn 56.4 TF/s, nn 53.7, nt 46.9), so on large
     // problems an operand stored with k contiguous is first transposed into
@@ -337,7 +338,7 @@ int run_gemm(int transA, int transB, int64_t M64, int64_t N64, int64_t K64, int 
     path = splits > 1 ? GEMM_PATH_FFMA_SPLITK : GEMM_PATH_FFMA;
     if (e == cudaSuccess) e = timed_sgemm(a, ctx);
     if (e == cudaSuccess && splits > 1)
-      e = launch_splitk_reduce(0, M, N, splits, a.partial, C, ldc, alpha, beta, ctx);
+      e = launch_splitk_reduce(0, M, N, splits, a.partial, C, ldc, alpha, beta, ctx, ep);
   } else {
     int bn = hgemm_pick_bn(M, N, transB, sms);
     const int forced = forced_bn();
@@ -395,6 +396,7 @@ int run_gemm(int transA, int transB, int64_t M64, int64_t N64, int64_t K64, int 
                   splits, k_slice, splits > 1 ? (float*)wp : nullptr, sms, bn, pair,
                   c_tma_enabled(), g_fault_injection.load()};
       a.dtype = dtype;
+      if (splits == 1) a.ep = ep;  // split-K: the reduction applies it
       if (tail.splits > 0) {
         a.dp_units = tail.dp_units;
         a.tail_splits = tail.splits;
@@ -405,7 +407,7 @@ int run_gemm(int transA, int transB, int64_t M64, int64_t N64, int64_t K64, int 
       path = splits > 1 ? GEMM_PATH_TC_SPLITK : GEMM_PATH_TC;
       e = timed_hgemm(a, ctx);
       if (e == cudaSuccess && splits > 1)
-        e = launch_splitk_reduce(dtype, M, N, splits, a.partial, C, ldc, alpha, beta, ctx);
+        e = launch_splitk_reduce(dtype, M, N, splits, a.partial, C, ldc, alpha, beta, ctx, ep);
     }
   }
   g_total_launches += ctx.launches;
@@ -676,6 +678,29 @@ int gemm_strided_batched(int transA, int transB, int64_t M, int64_t N, int64_t K
   }
   return run_batched(transA, transB, M, N, K, dtype, alpha, beta, A, lda, sA, B, ldb, sB, C, ldc,
                      sC, batch, (cudaStream_t)stream, ar, ac, br, bc);
+}
+
+int gemm_ex(int transA, int transB, int64_t M, int64_t N, int64_t K, int dtype, float alpha,
+            float beta, const void* A, int64_t lda, const void* B, int64_t ldb, void* C,
+            int64_t ldc, const void* bias, int act, gemm_stream_t stream) {
+  int64_t ar, ac, br, bc;
+  tl_last_path = GEMM_PATH_NONE;
+  tl_last_launches = 0;
+  if (act != GEMM_ACT_NONE && act != GEMM_ACT_RELU && act != GEMM_ACT_GELU)
+    return GEMM_ERR_INVALID_ARG;
+  int rc = check_args(transA, transB, M, N, K, dtype, A, lda, B, ldb, C, ldc, &ar, &ac, &br, &bc);
+  if (rc != GEMM_OK) return rc;
+  if (M == 0 || N == 0) return GEMM_OK;
+  const int64_t e = dtype == GEMM_F32 ? 4 : 2;
+  if (bias) {
+    if (((uintptr_t)bias % (uintptr_t)e) != 0) return GEMM_ERR_INVALID_ARG;
+    if (overlaps(C, footprint_bytes(M, N, ldc, e), bias, N * e)) return GEMM_ERR_ALIAS;
+  }
+  Epilogue ep;
+  ep.bias = bias;
+  ep.act = act;
+  return run_gemm(transA, transB, M, N, K, dtype, alpha, beta, A, lda, B, ldb, C, ldc,
+                  (cudaStream_t)stream, ar, ac, br, bc, ep);
 }
 
 int gemm(int transA, int transB, int64_t M, int64_t N, int64_t K, int dtype, float alpha,

@@ -135,6 +135,7 @@ struct HParams {
   int batch;
   int64_t stride_c;  // elements between consecutive C matrices
   int za_mask, zb_mask;  // -1: operand batched; 0: one matrix shared by all (pitch 0)
+  Epilogue ep;           // bias (output type, per column) and activation
   float* tail_ws;          // [tail tiles][pair ? 2 : 1][tail_splits][4 warps][32 x BN]
   unsigned int* tail_cnt;  // [tail tiles][pair ? 2 : 1][4], zero on entry and on exit
 };
@@ -222,6 +223,7 @@ __device__ __forceinline__ void store_c32(const HParams& p, int bz, int gm, int 
 #pragma unroll
   for (int j = 0; j < 32; ++j) v[j] = p.alpha * v[j];
   const bool full = (gn0 + 31 < p.N) && p.c_vec_ok;
+  const bool epi = p.ep.bias != nullptr || p.ep.act != 0;
   if (full) {
     if (p.beta != 0.f) {
 #pragma unroll
@@ -236,6 +238,10 @@ __device__ __forceinline__ void store_c32(const HParams& p, int bz, int gm, int 
         }
       }
     }
+    if (epi) {
+#pragma unroll
+      for (int j = 0; j < 32; ++j) v[j] = apply_epilogue<T>(v[j], p.ep, gn0 + j);
+    }
 #pragma unroll
     for (int w = 0; w < 4; ++w) {
       uint4 o;
@@ -249,6 +255,7 @@ __device__ __forceinline__ void store_c32(const HParams& p, int bz, int gm, int 
       if (gn0 + j < p.N) {
         float o = v[j];
         if (p.beta != 0.f) o = __fmaf_rn(p.beta, E::to(dst[j]), o);
+        if (epi) o = apply_epilogue<T>(o, p.ep, gn0 + j);
         dst[j] = E::from(o);
       }
     }
@@ -500,6 +507,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         // w ^ (l & 7): the 8 lanes of each store phase hit distinct banks),
         // then one TMA store clipped by the unit at M and N
         constexpr int NB = C_::NBUF;
+        const bool epi = p.ep.bias != nullptr || p.ep.act != 0;
 #pragma unroll 1
         for (int c = 0; c < BN / 32; c += 2) {
           uint32_t r0[32], r1[32];
@@ -522,9 +530,15 @@ __global__ void __launch_bounds__(THREADS, 1)
             uint4 o;
             typename Elem<T>::T2* oh = reinterpret_cast<typename Elem<T>::T2*>(&o);
 #pragma unroll
-            for (int e = 0; e < 4; ++e)
-              oh[e] = Elem<T>::pack(p.alpha * __uint_as_float(rr[2 * e]),
-                                    p.alpha * __uint_as_float(rr[2 * e + 1]));
+            for (int e = 0; e < 4; ++e) {
+              float x0 = p.alpha * __uint_as_float(rr[2 * e]);
+              float x1 = p.alpha * __uint_as_float(rr[2 * e + 1]);
+              // (columns past N are clipped by the store; their bias is not read)
+              const int col = gn0 + 8 * w + 2 * e;
+              if (epi && col < p.N) x0 = apply_epilogue<T>(x0, p.ep, col);
+              if (epi && col + 1 < p.N) x1 = apply_epilogue<T>(x1, p.ep, col + 1);
+              oh[e] = Elem<T>::pack(x0, x1);
+            }
             const uint32_t dst = sbuf + (uint32_t)(lane * 128 + ((w ^ (lane & 7)) * 16));
             asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(dst), "r"(o.x),
                          "r"(o.y), "r"(o.z), "r"(o.w)
@@ -819,6 +833,7 @@ cudaError_t launch_hgemm_t(const HgemmArgs& a, LaunchCtx& ctx) {
   p.batch = a.batch > 1 ? a.batch : 1;
   p.stride_c = p.batch > 1 ? a.stride_c : 0;
   p.za_mask = (p.batch > 1 && a.stride_a != 0) ? -1 : 0;
+  p.ep = a.ep;
   p.zb_mask = (p.batch > 1 && a.stride_b != 0) ? -1 : 0;
   if (p.tail_splits > 0 && (p.splits != 1 || !p.tail_ws || !p.tail_cnt)) return cudaErrorInvalidValue;
   if (p.batch > 1 && (p.splits != 1 || p.tail_splits > 0)) return cudaErrorInvalidValue;

@@ -8,6 +8,14 @@
 namespace gb300 {
 
 // One fp32 GEMM launch over a K range per grid z-slice.
+// Fused epilogue of a GEMM: C = act(alpha * AB + beta * C + bias[j]).
+// bias: N elements of the output type (device), or null; act: 0 none, 1 relu,
+// 2 gelu.
+struct Epilogue {
+  const void* bias = nullptr;
+  int act = 0;
+};
+
 struct SgemmArgs {
   int transA, transB;
   int M, N, K;
@@ -34,6 +42,7 @@ struct SgemmArgs {
   int sk_blocks = 0;
   float* sk_ws = nullptr;
   unsigned int* sk_cnt = nullptr;
+  Epilogue ep;  // fused bias / activation (not with splits > 1: the reduction applies it)
 };
 
 // One tcgen05 GEMM launch (fp16 or bf16 operands and output).
@@ -64,6 +73,7 @@ struct HgemmArgs {
   int dp_units = 0, tail_splits = 0, tail_k_slice = 0;
   float* tail_ws = nullptr;
   unsigned int* tail_cnt = nullptr;
+  Epilogue ep;  // fused bias / activation (not with splits > 1: the reduction applies it)
 };
 
 struct TailPlan {
@@ -85,10 +95,11 @@ cudaError_t launch_hgemm(const HgemmArgs& a, LaunchCtx& ctx);
 cudaError_t launch_hgemm_bf16(const HgemmArgs& a, LaunchCtx& ctx);
 // C[M,N] = alpha * sum_z P[z] + beta * C; dtype 0 = fp32 C, 1 = fp16 C, 2 = bf16 C.
 cudaError_t launch_splitk_reduce(int dtype, int M, int N, int splits, const float* P, void* C,
-                                 int64_t ldc, float alpha, float beta, LaunchCtx& ctx);
-// C = beta * C (K == 0); beta == 0 writes zeros.
+                                 int64_t ldc, float alpha, float beta, LaunchCtx& ctx,
+                                 Epilogue ep = Epilogue());
+// C = act(beta * C + bias) (K == 0); beta == 0 reads no C.
 cudaError_t launch_scale(int dtype, int M, int N, void* C, int64_t ldc, float beta,
-                         LaunchCtx& ctx);
+                         LaunchCtx& ctx, Epilogue ep = Epilogue());
 // dst[c][r] = src[r][c] (fp32 rows x cols).
 cudaError_t launch_transpose_f32(int rows, int cols, const float* src, int64_t ld_src,
                                  float* dst, int64_t ld_dst, LaunchCtx& ctx);

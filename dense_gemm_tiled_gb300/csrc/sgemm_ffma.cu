@@ -100,6 +100,7 @@ struct Params {
   int64_t sk_iters;
   float* sk_ws;
   unsigned int* sk_cnt;
+  Epilogue ep;  // bias (fp32, per column) and activation, applied before the store
 };
 
 // Kernel kinds: one output tile per block (C), one K slice of a tile per
@@ -478,6 +479,7 @@ __global__ void __launch_bounds__(THREADS, GB300_SG_MIN_BLOCKS) sgemm_ffma_kerne
         } else {
           float* dst = Cg + (int64_t)gm * p.ldc + gn;
           const bool vec_ok = VEC && (gn + 3 < p.N);
+          const bool epi = p.ep.bias != nullptr || p.ep.act != 0;
           if (vec_ok) {
             float4 o;
             if (p.beta != 0.f) {
@@ -489,13 +491,21 @@ __global__ void __launch_bounds__(THREADS, GB300_SG_MIN_BLOCKS) sgemm_ffma_kerne
             } else {
               o = make_float4(p.alpha * v[0], p.alpha * v[1], p.alpha * v[2], p.alpha * v[3]);
             }
+            if (epi) {
+              o.x = apply_epilogue<float>(o.x, p.ep, gn);
+              o.y = apply_epilogue<float>(o.y, p.ep, gn + 1);
+              o.z = apply_epilogue<float>(o.z, p.ep, gn + 2);
+              o.w = apply_epilogue<float>(o.w, p.ep, gn + 3);
+            }
             *reinterpret_cast<float4*>(dst) = o;
           } else {
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
               if (gn + j < p.N) {
-                dst[j] = (p.beta != 0.f) ? __fmaf_rn(p.alpha, v[j], p.beta * dst[j])
-                                         : p.alpha * v[j];
+                float o = (p.beta != 0.f) ? __fmaf_rn(p.alpha, v[j], p.beta * dst[j])
+                                          : p.alpha * v[j];
+                if (epi) o = apply_epilogue<float>(o, p.ep, gn + j);
+                dst[j] = o;
               }
             }
           }
@@ -549,6 +559,7 @@ cudaError_t launch_sgemm(const SgemmArgs& a, LaunchCtx& ctx) {
     p.group_m = (int)g;
   }
   p.alpha = a.alpha; p.beta = a.beta;
+  p.ep = a.ep;
   const int batch = a.batch > 1 ? a.batch : 1;
   if (batch > 1 && (a.splits > 1 || batch > 65535)) return cudaErrorInvalidValue;
   p.stride_a = batch > 1 ? a.stride_a : 0;

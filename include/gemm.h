@@ -95,6 +95,32 @@ int gemm(int transA, int transB, int64_t M, int64_t N, int64_t K, int dtype, flo
          int64_t ldc, gemm_stream_t stream);
 
 /*
+ * gemm_ex -- gemm() with a fused epilogue ("From a C loop to a GPU kernel",
+ * section "Fusion": add the bias and apply the activation while the tile is
+ * still in registers, write the result once):
+ *
+ *     C = act(alpha * op(A) * op(B) + beta * C + bias[j])
+ *
+ * bias: DEVICE pointer to N elements of the output type (fp32 for GEMM_F32,
+ *   fp16 / bf16 otherwise), one per output column (the per-output offset), or
+ *   NULL for none; element-aligned; must not overlap C (GEMM_ERR_ALIAS).
+ * act: a gemm_act_t.  GEMM_ACT_GELU is the exact v * Phi(v) =
+ *   v/2 * (1 + erf(v / sqrt 2)), evaluated in fp32 with CUDA's erff.
+ * Everything else as gemm(); with bias == NULL and GEMM_ACT_NONE it is gemm().
+ * The bias and activation are applied in fp32 before the output rounding, in
+ * every path (split-K: by the reduction; K == 0: act(beta * C + bias)).
+ */
+typedef enum {
+    GEMM_ACT_NONE = 0,
+    GEMM_ACT_RELU = 1,  /* max(v, 0) */
+    GEMM_ACT_GELU = 2   /* v * Phi(v), Phi the standard normal distribution function */
+} gemm_act_t;
+
+int gemm_ex(int transA, int transB, int64_t M, int64_t N, int64_t K, int dtype, float alpha,
+            float beta, const void* A, int64_t lda, const void* B, int64_t ldb, void* C,
+            int64_t ldc, const void* bias, int act, gemm_stream_t stream);
+
+/*
  * gemm_host -- the same product on HOST buffers: copies A, B (and C when
  * beta != 0) to device memory taken from the stream-ordered allocator, runs
  * gemm() on `stream`, copies C back and synchronises `stream` before it

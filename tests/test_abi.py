@@ -103,3 +103,12 @@ def test_batched_empty_returns_ok_without_gpu(b):
     assert b.gemm_strided_batched_raw(0, 0, 0, 4, 4, 1, 1.0, 0.0, PA, 4, 16, PB, 4, 16, PC, 4, 16,
                                       5) == 0
     assert b.last_path() == "none"
+
+
+def test_gemm_ex_invalid_arguments(b):
+    # (..., bias, act): bad act code, misaligned bias, bias overlapping C
+    assert b.gemm_ex_raw(0, 0, 4, 4, 4, 0, 1.0, 0.0, PA, 4, PB, 4, PC, 4, 0, 3) == 1
+    assert b.gemm_ex_raw(0, 0, 4, 4, 4, 0, 1.0, 0.0, PA, 4, PB, 4, PC, 4, PC + 4096 + 2, 1) == 1
+    assert b.gemm_ex_raw(0, 0, 4, 4, 4, 0, 1.0, 0.0, PA, 4, PB, 4, PC, 4, PC + 16, 2) == 3
+    assert b.gemm_ex_raw(0, 0, 0, 4, 4, 0, 1.0, 0.0, PA, 4, PB, 4, PC, 4, 0, 2) == 0
+    assert b.last_path() == "none"
