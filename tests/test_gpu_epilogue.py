@@ -80,7 +80,8 @@ def test_activation_without_bias(dtype, act):
 @pytest.mark.parametrize("dtype", ["f32", "f16", "bf16"])
 def test_relu_bias_integer_exact(dtype):
     """Small-integer operands and an integer bias: relu(AB + bias) is exact."""
-    prob = inputs.make_problem(256, 384, 192, False, True, dtype, "integer", seed=730, beta=1.0)
+    prob = inputs.make_problem(256, 384, 192, False, True, dtype, "integer", seed=730, beta=1.0,
+                               c_fill="integer")
     bias = _bias(384, dtype, 731, integer=True)
     _check(prob, bias, "relu", exact=True)
 
