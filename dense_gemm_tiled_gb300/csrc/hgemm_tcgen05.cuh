@@ -214,18 +214,18 @@ __device__ __forceinline__ int total_units(const HParams& p, bool pair) {
   return tiles * p.splits * (p.batch > 1 ? p.batch : 1);
 }
 
-// alpha * v + beta * C_old -> T (RN-even) -> C, for 32 columns of one row
+// act(alpha * v + beta * C + bias) -> T (RN-even) -> C, for 32 columns of one
+// row (every loop fully unrolled, so v stays in registers)
 template <typename T>
 __device__ __forceinline__ void store_c32(const HParams& p, int bz, int gm, int gn0,
                                           float (&v)[32]) {
   using E = Elem<T>;
   T* dst = static_cast<T*>(p.C) + (int64_t)bz * p.stride_c + (int64_t)gm * p.ldc + gn0;
+  const bool full = (gn0 + 31 < p.N) && p.c_vec_ok;
 #pragma unroll
   for (int j = 0; j < 32; ++j) v[j] = p.alpha * v[j];
-  const bool full = (gn0 + 31 < p.N) && p.c_vec_ok;
-  const bool epi = p.ep.bias != nullptr || p.ep.act != 0;
-  if (full) {
-    if (p.beta != 0.f) {
+  if (p.beta != 0.f) {
+    if (full) {
 #pragma unroll
       for (int w = 0; w < 4; ++w) {
         const uint4 cv = reinterpret_cast<const uint4*>(dst)[w];
@@ -237,11 +237,18 @@ __device__ __forceinline__ void store_c32(const HParams& p, int bz, int gm, int 
           v[8 * w + 2 * e + 1] = __fmaf_rn(p.beta, f.y, v[8 * w + 2 * e + 1]);
         }
       }
-    }
-    if (epi) {
+    } else {
 #pragma unroll
-      for (int j = 0; j < 32; ++j) v[j] = apply_epilogue<T>(v[j], p.ep, gn0 + j);
+      for (int j = 0; j < 32; ++j)
+        if (gn0 + j < p.N) v[j] = __fmaf_rn(p.beta, E::to(dst[j]), v[j]);
     }
+  }
+  if (p.ep.bias != nullptr || p.ep.act != 0) {
+#pragma unroll
+    for (int j = 0; j < 32; ++j)
+      if (gn0 + j < p.N) v[j] = apply_epilogue<T>(v[j], p.ep, gn0 + j);
+  }
+  if (full) {
 #pragma unroll
     for (int w = 0; w < 4; ++w) {
       uint4 o;
@@ -251,14 +258,9 @@ __device__ __forceinline__ void store_c32(const HParams& p, int bz, int gm, int 
       reinterpret_cast<uint4*>(dst)[w] = o;
     }
   } else {
-    for (int j = 0; j < 32; ++j) {
-      if (gn0 + j < p.N) {
-        float o = v[j];
-        if (p.beta != 0.f) o = __fmaf_rn(p.beta, E::to(dst[j]), o);
-        if (epi) o = apply_epilogue<T>(o, p.ep, gn0 + j);
-        dst[j] = E::from(o);
-      }
-    }
+#pragma unroll
+    for (int j = 0; j < 32; ++j)
+      if (gn0 + j < p.N) dst[j] = E::from(v[j]);
   }
 }
 
@@ -524,26 +526,34 @@ __global__ void __launch_bounds__(THREADS, 1)
           const uint32_t sbuf = staging_addr + (uint32_t)((q * NB + (c / 2) % NB) * 4096);
           if (lane == 0) bulk_wait_read<NB - 1>();  // this buffer's previous store has read it
           __syncwarp();
+          // 16-byte chunk w (columns 8w .. 8w+7 of the 64) of this lane's row;
+          // r holds columns 32h .. 32h+31 (constant indices after unrolling)
+          auto pack_half = [&](const uint32_t (&r)[32], int h) {
 #pragma unroll
-          for (int w = 0; w < 8; ++w) {
-            const uint32_t* rr = w < 4 ? r0 + 8 * w : r1 + 8 * (w - 4);
-            uint4 o;
-            typename Elem<T>::T2* oh = reinterpret_cast<typename Elem<T>::T2*>(&o);
+            for (int ww = 0; ww < 4; ++ww) {
+              const int w = 4 * h + ww;
+              uint4 o;
+              typename Elem<T>::T2* oh = reinterpret_cast<typename Elem<T>::T2*>(&o);
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              float x0 = p.alpha * __uint_as_float(rr[2 * e]);
-              float x1 = p.alpha * __uint_as_float(rr[2 * e + 1]);
-              // (columns past N are clipped by the store; their bias is not read)
-              const int col = gn0 + 8 * w + 2 * e;
-              if (epi && col < p.N) x0 = apply_epilogue<T>(x0, p.ep, col);
-              if (epi && col + 1 < p.N) x1 = apply_epilogue<T>(x1, p.ep, col + 1);
-              oh[e] = Elem<T>::pack(x0, x1);
+              for (int e = 0; e < 4; ++e) {
+                float x0 = p.alpha * __uint_as_float(r[8 * ww + 2 * e]);
+                float x1 = p.alpha * __uint_as_float(r[8 * ww + 2 * e + 1]);
+                if (epi) {
+                  // (columns past N are clipped by the store; their bias is not read)
+                  const int col = gn0 + 8 * w + 2 * e;
+                  if (col < p.N) x0 = apply_epilogue<T>(x0, p.ep, col);
+                  if (col + 1 < p.N) x1 = apply_epilogue<T>(x1, p.ep, col + 1);
+                }
+                oh[e] = Elem<T>::pack(x0, x1);
+              }
+              const uint32_t dst = sbuf + (uint32_t)(lane * 128 + ((w ^ (lane & 7)) * 16));
+              asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(dst), "r"(o.x),
+                           "r"(o.y), "r"(o.z), "r"(o.w)
+                           : "memory");
             }
-            const uint32_t dst = sbuf + (uint32_t)(lane * 128 + ((w ^ (lane & 7)) * 16));
-            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(dst), "r"(o.x),
-                         "r"(o.y), "r"(o.z), "r"(o.w)
-                         : "memory");
-          }
+          };
+          pack_half(r0, 0);
+          pack_half(r1, 1);
           fence_proxy_async_smem();
           __syncwarp();
           // (a block wholly past M or N -- the second tile of a pair on an odd
