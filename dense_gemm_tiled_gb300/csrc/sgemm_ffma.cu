@@ -391,12 +391,20 @@ __global__ void __launch_bounds__(THREADS, GB300_SG_MIN_BLOCKS) sgemm_ffma_kerne
           const ulonglong2 b01 = *reinterpret_cast<const ulonglong2*>(brow);
           const ulonglong2 b23 = *reinterpret_cast<const ulonglong2*>(brow + 16);
           const uint64_t bp[4] = {b01.x, b01.y, b23.x, b23.y};
+          // All eight (a, a) pairs first, then column pair by column pair, the
+          // rows alternating between the two 4-row halves: the eight paired
+          // FMAs sharing bp[j] follow each other and none waits on the register
+          // move that builds its splatted operand.  Measured at 4096^3 against
+          // row by row (i outer, j inner): +5 %; rows in order 0..7: -0.1 %;
+          // other interleavings: -0.5 to -2.6 %.
+          uint64_t ap[8];
 #pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            const uint64_t ap = splat2(av[i]);
+          for (int i = 0; i < 8; ++i) ap[i] = splat2(av[i]);
+          constexpr int ORD[8] = {0, 4, 1, 5, 2, 6, 3, 7};
 #pragma unroll
-            for (int j = 0; j < 4; ++j) acc[i][j] = ffma2(ap, bp[j], acc[i][j]);
-          }
+          for (int j = 0; j < 4; ++j)
+#pragma unroll
+            for (int ii = 0; ii < 8; ++ii) acc[ORD[ii]][j] = ffma2(ap[ORD[ii]], bp[j], acc[ORD[ii]][j]);
         }
       }
     }
