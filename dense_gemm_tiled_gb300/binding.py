@@ -49,6 +49,7 @@ _lib.gemm_set_kernel_events.restype = None
 F32 = 0
 F16_F32ACC = 1
 BF16_F32ACC = 2
+F32_TF32 = 3
 OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_ALIAS, ERR_CUDA, ERR_NO_MEMORY, ERR_TIMEOUT = range(7)
 PATHS = {0: "none", 1: "scale", 2: "ffma", 3: "ffma_splitk", 4: "tc", 5: "tc_splitk",
          6: "ffma_batched", 7: "tc_batched", 8: "per_entry"}
@@ -222,7 +223,7 @@ ACTS = {"none": 0, "relu": 1, "gelu": 2}
 
 
 def gemm(A, B, C, transA=False, transB=False, alpha=1.0, beta=0.0, stream=None, bias=None,
-         act="none"):
+         act="none", tf32=False):
     """C = act(alpha * op(A) @ op(B) + beta * C + bias) in place, on torch CUDA
     tensors.
 
@@ -230,11 +231,16 @@ def gemm(A, B, C, transA=False, transB=False, alpha=1.0, beta=0.0, stream=None, 
     C is [M,N]; all float32, all float16 or all bfloat16 (fp32 accumulation), rows
     contiguous, any leading dimension.  bias: None or a contiguous CUDA tensor
     of N elements of C's dtype (per output column); act: 'none', 'relu' or
-    'gelu'.  Runs on `stream` (a torch.cuda.Stream) or the current stream.
-    Returns C.
+    'gelu'.  tf32=True (float32 tensors only) opts into the reduced-precision
+    TF32 tensor-core path.  Runs on `stream` (a torch.cuda.Stream) or the
+    current stream.  Returns C.
     """
     import torch
     dtype, M, N, K = _dims(A, B, C, transA, transB)
+    if tf32:
+        if dtype != F32:
+            raise TypeError("tf32=True takes float32 tensors")
+        dtype = F32_TF32
     for t in (A, B, C):
         if not t.is_cuda:
             raise ValueError("gemm() takes CUDA tensors; use gemm_host() for host memory")

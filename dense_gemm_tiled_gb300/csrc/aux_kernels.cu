@@ -124,6 +124,18 @@ __global__ void repack_16_kernel(int rows, int cols, const uint16_t* __restrict_
   }
 }
 
+// 32-bit elements copied row by row into a new row pitch (the columns past
+// `cols` are left as they are: the tensor maps bound every read at cols)
+__global__ void repack_32_kernel(int rows, int cols, const uint32_t* __restrict__ src,
+                                 int64_t ld_src, uint32_t* __restrict__ dst, int64_t ld_dst) {
+  const int64_t total = (int64_t)rows * cols;
+  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < total;
+       i += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t r = i / cols, c = i - r * cols;
+    dst[r * ld_dst + c] = src[r * ld_src + c];
+  }
+}
+
 // dst[c][r] = src[r][c] for a rows x cols fp32 matrix: 64 x 64 tiles staged
 // through shared memory (one padding column), 128-bit global loads and stores
 // where rows are 16-byte aligned, scalar accesses at ragged edges.
@@ -175,6 +187,16 @@ __global__ void __launch_bounds__(256) transpose_f32_kernel(int rows, int cols,
 }
 
 }  // namespace
+
+cudaError_t launch_repack_32(int rows, int cols, const void* src, int64_t ld_src, void* dst,
+                             int64_t ld_dst, LaunchCtx& ctx) {
+  const int grid = grid_for((int64_t)rows * cols, 256);
+  repack_32_kernel<<<grid, 256, 0, ctx.stream>>>(rows, cols, static_cast<const uint32_t*>(src),
+                                                  ld_src, static_cast<uint32_t*>(dst), ld_dst);
+  cudaError_t e = cudaGetLastError();
+  if (e == cudaSuccess) ctx.launches++;
+  return e;
+}
 
 cudaError_t launch_transpose_f32(int rows, int cols, const float* src, int64_t ld_src,
                                  float* dst, int64_t ld_dst, LaunchCtx& ctx) {

@@ -86,6 +86,11 @@ int device_state(int* dev_out, unsigned int** status, int* sms) {
   return GEMM_OK;
 }
 
+// Bytes per element of a gemm_dtype_t, and the output kind the auxiliary
+// kernels take (0 fp32, 1 fp16, 2 bf16).
+inline int64_t esize(int dtype) { return (dtype == GEMM_F32 || dtype == GEMM_F32_TF32) ? 4 : 2; }
+inline int out_kind(int dtype) { return dtype == GEMM_F32_TF32 ? 0 : dtype; }
+
 inline int64_t footprint_bytes(int64_t rows, int64_t cols, int64_t ld, int64_t e) {
   if (rows <= 0 || cols <= 0) return 0;
   return ((rows - 1) * ld + cols) * e;
@@ -103,7 +108,8 @@ int check_args(int transA, int transB, int64_t M, int64_t N, int64_t K, int dtyp
                int64_t ldc, int64_t* a_rows, int64_t* a_cols, int64_t* b_rows,
                int64_t* b_cols) {
   if ((transA != 0 && transA != 1) || (transB != 0 && transB != 1)) return GEMM_ERR_INVALID_ARG;
-  if (dtype != GEMM_F32 && dtype != GEMM_F16_F32ACC && dtype != GEMM_BF16_F32ACC)
+  if (dtype != GEMM_F32 && dtype != GEMM_F16_F32ACC && dtype != GEMM_BF16_F32ACC &&
+      dtype != GEMM_F32_TF32)
     return GEMM_ERR_INVALID_ARG;
   if (M < 0 || N < 0 || K < 0) return GEMM_ERR_INVALID_ARG;
   const int64_t lim = (int64_t)1 << 31;
@@ -116,7 +122,7 @@ int check_args(int transA, int transB, int64_t M, int64_t N, int64_t K, int dtyp
   if (lda < (*a_cols > 1 ? *a_cols : 1)) return GEMM_ERR_INVALID_ARG;
   if (ldb < (*b_cols > 1 ? *b_cols : 1)) return GEMM_ERR_INVALID_ARG;
   if (M == 0 || N == 0) return GEMM_OK;
-  const int64_t e = dtype == GEMM_F32 ? 4 : 2;
+  const int64_t e = esize(dtype);
   if (!C || ((uintptr_t)C % (uintptr_t)e) != 0) return GEMM_ERR_INVALID_ARG;
   if (K > 0) {
     if (!A || !B) return GEMM_ERR_INVALID_ARG;
@@ -285,7 +291,54 @@ int run_gemm(int transA, int transB, int64_t M64, int64_t N64, int64_t K64, int 
 
   if (K == 0) {
     path = GEMM_PATH_SCALE;
-    e = launch_scale(dtype, M, N, C, ldc, beta, ctx, ep);
+    e = launch_scale(out_kind(dtype), M, N, C, ldc, beta, ctx, ep);
+  } else if (dtype == GEMM_F32_TF32) {
+    // Opt-in TF32: the tcgen05 kernel on kind::tf32 reads K-major fp32
+    // operands in 16-byte aligned rows, A [M, K] and B [N, K]; others are
+    // transposed or re-pitched into scratch first.
+    int bn = hgemm_pick_bn(M, N, 1, sms);
+    const int64_t tiles = (int64_t)((M + HG_BM - 1) / HG_BM) * ((N + bn - 1) / bn);
+    int splits, k_slice;
+    plan_splits(tiles, K, 32, sms, 4, 32, &splits, &k_slice);
+    const bool a_ok = !transA && ((uintptr_t)A % 16) == 0 && (lda % 4) == 0;
+    const bool b_ok = transB && ((uintptr_t)B % 16) == 0 && (ldb % 4) == 0;
+    const int64_t ldk = (K + 3) / 4 * 4;
+    const size_t bytes_a = a_ok ? 0 : ((size_t)M * ldk * 4 + 255) / 256 * 256;
+    const size_t bytes_b = b_ok ? 0 : ((size_t)N * ldk * 4 + 255) / 256 * 256;
+    const size_t bytes_p = splits > 1 ? (size_t)splits * M * N * sizeof(float) : 0;
+    Scratch ws;
+    if (bytes_a + bytes_b + bytes_p > 0) {
+      e = ws.get(bytes_a + bytes_b + bytes_p, stream);
+      if (e != cudaSuccess) return cuda_fail(e);
+    }
+    const void* Ad = A;
+    const void* Bd = B;
+    int64_t ldad = lda, ldbd = ldb;
+    char* wp = (char*)ws.ptr;
+    if (!a_ok) {
+      float* dst = (float*)wp;
+      e = transA ? launch_transpose_f32(K, M, (const float*)A, lda, dst, ldk, ctx)
+                 : launch_repack_32(M, K, A, lda, dst, ldk, ctx);
+      Ad = dst; ldad = ldk; wp += bytes_a;
+    }
+    if (e == cudaSuccess && !b_ok) {
+      float* dst = (float*)wp;
+      e = !transB ? launch_transpose_f32(K, N, (const float*)B, ldb, dst, ldk, ctx)
+                  : launch_repack_32(N, K, B, ldb, dst, ldk, ctx);
+      Bd = dst; ldbd = ldk; wp += bytes_b;
+    }
+    if (e == cudaSuccess) {
+      const int pair = pair_enabled();
+      HgemmArgs a{0, 1, M, N, K, Ad, ldad, Bd, ldbd, C, ldc, alpha, beta,
+                  splits, k_slice, splits > 1 ? (float*)wp : nullptr, sms, bn, pair,
+                  c_tma_enabled(), g_fault_injection.load()};
+      a.dtype = GEMM_F32_TF32;
+      if (splits == 1) a.ep = ep;  // split-K: the reduction applies it
+      path = splits > 1 ? GEMM_PATH_TC_SPLITK : GEMM_PATH_TC;
+      e = timed_hgemm(a, ctx);
+      if (e == cudaSuccess && splits > 1)
+        e = launch_splitk_reduce(0, M, N, splits, a.partial, C, ldc, alpha, beta, ctx, ep);
+    }
   } else if (dtype == GEMM_F32) {
     const int64_t tiles = (int64_t)((M + SG_BM - 1) / SG_BM) * ((N + SG_BN - 1) / SG_BN);
     int splits, k_slice;
@@ -464,7 +517,7 @@ int host_pipelined(int transA, int transB, int64_t M, int64_t N, int64_t K, int 
                    float alpha, float beta, const void* A, int64_t lda, const void* B,
                    int64_t ldb, void* C, int64_t ldc, cudaStream_t stream, int64_t ar,
                    int64_t ac, int64_t br, int64_t bc, int panels) {
-  const int64_t e = dtype == GEMM_F32 ? 4 : 2;
+  const int64_t e = esize(dtype);
   const int64_t align = 16 / e;
   const int64_t lda_d = (ac + align - 1) / align * align;
   const int64_t ldb_d = (bc + align - 1) / align * align;
@@ -553,11 +606,13 @@ int run_batched(int transA, int transB, int64_t M64, int64_t N64, int64_t K64, i
   int rc = device_state(&dev, &status, &sms);
   if (rc != GEMM_OK) return rc;
   const int M = (int)M64, N = (int)N64, K = (int)K64;
-  const int64_t es = dtype == GEMM_F32 ? 4 : 2;
+  const int64_t es = esize(dtype);
   const char* Ab = static_cast<const char*>(A);
   const char* Bb = static_cast<const char*>(B);
   char* Cb = static_cast<char*>(C);
-  const bool tma_ok = dtype != GEMM_F32 && ((uintptr_t)A % 16) == 0 && ((uintptr_t)B % 16) == 0 &&
+  // (TF32 runs entry by entry: its operands may need packing into K-major rows)
+  const bool tma_ok = dtype != GEMM_F32 && dtype != GEMM_F32_TF32 && ((uintptr_t)A % 16) == 0 &&
+                      ((uintptr_t)B % 16) == 0 &&
                       (lda % 8) == 0 && (ldb % 8) == 0 && (sA % 8) == 0 && (sB % 8) == 0;
   LaunchCtx ctx{stream, status, (uint64_t)g_timeout_ns.load(), 0};
   int path = GEMM_PATH_NONE;
@@ -614,7 +669,7 @@ int run_batched(int transA, int transB, int64_t M64, int64_t N64, int64_t K64, i
   } else if (K == 0) {
     path = GEMM_PATH_SCALE;
     for (int64_t b = 0; b < batch && e == cudaSuccess; ++b)
-      e = launch_scale(dtype, M, N, Cb + b * sC * es, ldc, beta, ctx);
+      e = launch_scale(out_kind(dtype), M, N, Cb + b * sC * es, ldc, beta, ctx);
   } else if (dtype == GEMM_F32) {
     // the batch runs on grid.y, at most 65535 entries per launch
     path = GEMM_PATH_FFMA_BATCHED;
@@ -658,7 +713,7 @@ int gemm_strided_batched(int transA, int transB, int64_t M, int64_t N, int64_t K
   if (batch == 1)
     return run_gemm(transA, transB, M, N, K, dtype, alpha, beta, A, lda, B, ldb, C, ldc,
                     (cudaStream_t)stream, ar, ac, br, bc);
-  const int64_t es = dtype == GEMM_F32 ? 4 : 2;
+  const int64_t es = esize(dtype);
   const int64_t fc = footprint_bytes(M, N, ldc, 1);  // elements of one C
   if (sC < fc) return GEMM_ERR_ALIAS;                 // C entries would overlap
   // whole extents, in bytes, without overflow
@@ -691,7 +746,7 @@ int gemm_ex(int transA, int transB, int64_t M, int64_t N, int64_t K, int dtype, 
   int rc = check_args(transA, transB, M, N, K, dtype, A, lda, B, ldb, C, ldc, &ar, &ac, &br, &bc);
   if (rc != GEMM_OK) return rc;
   if (M == 0 || N == 0) return GEMM_OK;
-  const int64_t e = dtype == GEMM_F32 ? 4 : 2;
+  const int64_t e = esize(dtype);
   if (bias) {
     if (((uintptr_t)bias % (uintptr_t)e) != 0) return GEMM_ERR_INVALID_ARG;
     if (overlaps(C, footprint_bytes(M, N, ldc, e), bias, N * e)) return GEMM_ERR_ALIAS;
@@ -730,7 +785,7 @@ int gemm_host(int transA, int transB, int64_t M, int64_t N, int64_t K, int dtype
   if (K > 0 && M >= 256 && (double)M * N * K >= (double)(1ll << 30) && host_pipeline_enabled())
     return host_pipelined(transA, transB, M, N, K, dtype, alpha, beta, A, lda, B, ldb, C, ldc,
                           stream, ar, ac, br, bc, M >= 4096 ? 4 : 2);
-  const int64_t e = dtype == GEMM_F32 ? 4 : 2;
+  const int64_t e = esize(dtype);
   const int64_t align = 16 / e;  // device pitch: whole 16-byte units
   const int64_t lda_d = (ac + align - 1) / align * align;
   const int64_t ldb_d = (bc + align - 1) / align * align;
@@ -867,6 +922,7 @@ extern "C" int gemm_splitk_noalloc(int transA, int transB, int64_t M, int64_t N,
   tl_last_launches = 0;
   int rc = check_args(transA, transB, M, N, K, dtype, A, lda, B, ldb, C, ldc, &ar, &ac, &br, &bc);
   if (rc != GEMM_OK) return rc;
+  if (dtype == GEMM_F32_TF32) return GEMM_ERR_UNSUPPORTED;  // its packing would need scratch
   if (M == 0 || N == 0) return GEMM_OK;
   cudaStream_t stream = (cudaStream_t)stream_;
   int dev, sms;

@@ -78,6 +78,7 @@ int hgemm_pick_bn(int M, int N, int transB, int num_sms, int batch) {
 
 cudaError_t launch_hgemm(const HgemmArgs& a, LaunchCtx& ctx) {
   if (a.dtype == 2) return launch_hgemm_bf16(a, ctx);
+  if (a.dtype == 3) return launch_hgemm_tf32(a, ctx);
   return launch_hgemm_t<__half>(a, ctx);
 }
 

@@ -77,9 +77,27 @@ struct Elem<__nv_bfloat16> {
   static __device__ __forceinline__ float to(__nv_bfloat16 v) { return __bfloat162float(v); }
 };
 
+// fp32 operands for the opt-in TF32 path (kind::tf32; output fp32)
+template <>
+struct Elem<float> {
+  using T2 = float2;
+  static constexpr uint32_t FMT = 2;  // kind::tf32 A/B format: TF32
+  static constexpr CUtensorMapDataType TMA = CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
+  static __device__ __forceinline__ T2 pack(float a, float b) { return make_float2(a, b); }
+  static __device__ __forceinline__ float2 unpack(T2 v) { return v; }
+  static __device__ __forceinline__ float from(float f) { return f; }
+  static __device__ __forceinline__ float to(float v) { return v; }
+};
+
+// Elements of T in one 128-byte swizzle-atom row: the K depth of a stage (64
+// for 16-bit operands, 32 for fp32), and the K of one MMA (32 bytes: 16 or 8).
+template <typename T>
+__host__ __device__ constexpr int kblk() { return 128 / (int)sizeof(T); }
+template <typename T>
+__host__ __device__ constexpr int kmma() { return 32 / (int)sizeof(T); }
+
 constexpr int BM = HG_BM;     // 128 accumulator rows = 128 TMEM lanes
-constexpr int BK = HG_BK;     // 64 fp16 = 128 bytes = one swizzle atom row
-constexpr int UMMA_K = 16;    // K per tcgen05.mma kind::f16
+constexpr int BK = HG_BK;     // 64 fp16 = 128 bytes = one swizzle atom row (16-bit types)
 constexpr int THREADS = 192;
 constexpr int GROUP_M = 8;
 constexpr int A_TILE_BYTES = BM * BK * 2;  // 16 KiB
@@ -171,7 +189,7 @@ __device__ __forceinline__ constexpr uint32_t make_idesc() {
 //  * tail split: units below dp_units are whole tiles; unit dp_units + v is
 //    slice v / tail_tiles of tail tile v % tail_tiles (`tail` >= 0);
 //  * otherwise: unit = whole tile.
-template <bool PAIR>
+template <bool PAIR, int KB = BK>
 __device__ __forceinline__ void unit_coords(int u, const HParams& p, int rank, int& m0, int& tn,
                                             int& kbeg, int& nkb, int& z, int& tail, int& bz) {
   const int rows = PAIR ? (p.tiles_m + 1) / 2 : p.tiles_m;
@@ -205,7 +223,7 @@ __device__ __forceinline__ void unit_coords(int u, const HParams& p, int rank, i
   m0 = tm * BM;
   kbeg = z * ks;
   const int kend = min(p.K, kbeg + ks);
-  nkb = (kend - kbeg + BK - 1) / BK;
+  nkb = (kend - kbeg + KB - 1) / KB;
 }
 
 __device__ __forceinline__ int total_units(const HParams& p, bool pair) {
@@ -225,7 +243,20 @@ __device__ __forceinline__ void store_c32(const HParams& p, int bz, int gm, int 
 #pragma unroll
   for (int j = 0; j < 32; ++j) v[j] = p.alpha * v[j];
   if (p.beta != 0.f) {
-    if (full) {
+    if (!full) {
+#pragma unroll
+      for (int j = 0; j < 32; ++j)
+        if (gn0 + j < p.N) v[j] = __fmaf_rn(p.beta, E::to(dst[j]), v[j]);
+    } else if constexpr (sizeof(T) == 4) {
+#pragma unroll
+      for (int w = 0; w < 8; ++w) {
+        const float4 cv = reinterpret_cast<const float4*>(dst)[w];
+        v[4 * w] = __fmaf_rn(p.beta, cv.x, v[4 * w]);
+        v[4 * w + 1] = __fmaf_rn(p.beta, cv.y, v[4 * w + 1]);
+        v[4 * w + 2] = __fmaf_rn(p.beta, cv.z, v[4 * w + 2]);
+        v[4 * w + 3] = __fmaf_rn(p.beta, cv.w, v[4 * w + 3]);
+      }
+    } else {
 #pragma unroll
       for (int w = 0; w < 4; ++w) {
         const uint4 cv = reinterpret_cast<const uint4*>(dst)[w];
@@ -237,10 +268,6 @@ __device__ __forceinline__ void store_c32(const HParams& p, int bz, int gm, int 
           v[8 * w + 2 * e + 1] = __fmaf_rn(p.beta, f.y, v[8 * w + 2 * e + 1]);
         }
       }
-    } else {
-#pragma unroll
-      for (int j = 0; j < 32; ++j)
-        if (gn0 + j < p.N) v[j] = __fmaf_rn(p.beta, E::to(dst[j]), v[j]);
     }
   }
   if (p.ep.bias != nullptr || p.ep.act != 0) {
@@ -248,7 +275,16 @@ __device__ __forceinline__ void store_c32(const HParams& p, int bz, int gm, int 
     for (int j = 0; j < 32; ++j)
       if (gn0 + j < p.N) v[j] = apply_epilogue<T>(v[j], p.ep, gn0 + j);
   }
-  if (full) {
+  if (!full) {
+#pragma unroll
+    for (int j = 0; j < 32; ++j)
+      if (gn0 + j < p.N) dst[j] = E::from(v[j]);
+  } else if constexpr (sizeof(T) == 4) {
+#pragma unroll
+    for (int w = 0; w < 8; ++w)
+      reinterpret_cast<float4*>(dst)[w] =
+          make_float4(v[4 * w], v[4 * w + 1], v[4 * w + 2], v[4 * w + 3]);
+  } else {
 #pragma unroll
     for (int w = 0; w < 4; ++w) {
       uint4 o;
@@ -257,10 +293,6 @@ __device__ __forceinline__ void store_c32(const HParams& p, int bz, int gm, int 
       for (int e = 0; e < 4; ++e) oh[e] = E::pack(v[8 * w + 2 * e], v[8 * w + 2 * e + 1]);
       reinterpret_cast<uint4*>(dst)[w] = o;
     }
-  } else {
-#pragma unroll
-    for (int j = 0; j < 32; ++j)
-      if (gn0 + j < p.N) dst[j] = E::from(v[j]);
   }
 }
 
@@ -351,12 +383,12 @@ __global__ void __launch_bounds__(THREADS, 1)
       bool ok = true;
       for (int u = worker; u < n_units && ok; u += workers) {
         int m0, tn, kbeg, nkb, z, tail, bz;
-        unit_coords<PAIR>(u, p, rank, m0, tn, kbeg, nkb, z, tail, bz);
+        unit_coords<PAIR, kblk<T>()>(u, p, rank, m0, tn, kbeg, nkb, z, tail, bz);
         const int za = bz & p.za_mask, zb = bz & p.zb_mask;
         const int n0 = tn * BN;
         for (int kb = 0; kb < nkb; ++kb) {
           if (!mbar_wait(empty_bar(stage), phase ^ 1u, wc)) { ok = false; break; }
-          const int k0 = kbeg + kb * BK;
+          const int k0 = kbeg + kb * kblk<T>();
           const bool skip = first && p.fault_injection == 1;
           first = false;
           if (!skip && TWO_SM) {
@@ -436,7 +468,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       bool ok = true;
       for (int u = worker; u < n_units && ok; u += workers, ++it) {
         int m0, tn, kbeg, nkb, z, tail, bz;
-        unit_coords<PAIR>(u, p, rank, m0, tn, kbeg, nkb, z, tail, bz);
+        unit_coords<PAIR, kblk<T>()>(u, p, rank, m0, tn, kbeg, nkb, z, tail, bz);
         const int buf = it & 1;
         const uint32_t acc_phase = (uint32_t)(it >> 1) & 1u;
         if (!mbar_wait(acce_bar(buf), acc_phase ^ 1u, wc)) { ok = false; break; }
@@ -448,14 +480,20 @@ __global__ void __launch_bounds__(THREADS, 1)
           const uint32_t sa = tiles_addr + (uint32_t)(stage * C_::STAGE_BYTES);
           const uint32_t sb = sa + (uint32_t)A_TILE_BYTES;
 #pragma unroll
-          for (int kk = 0; kk < BK / UMMA_K; ++kk) {
+          for (int kk = 0; kk < kblk<T>() / kmma<T>(); ++kk) {
             uint64_t ad, bd;
             if constexpr (A_MN) ad = make_sdesc(sa + (uint32_t)kk * 2048u, 8192u, 1024u);
             else ad = make_sdesc(sa + (uint32_t)kk * 32u, 16u, 1024u);
             if constexpr (B_MN) bd = make_sdesc(sb + (uint32_t)kk * 2048u, 8192u, 1024u);
             else bd = make_sdesc(sb + (uint32_t)kk * 32u, 16u, 1024u);
-            if constexpr (TWO_SM) tc_mma_f16_pair(d_tmem, ad, bd, idesc, (kb | kk) != 0 ? 1u : 0u);
-            else tc_mma_f16(d_tmem, ad, bd, idesc, (kb | kk) != 0 ? 1u : 0u);
+            const uint32_t acc = (kb | kk) != 0 ? 1u : 0u;
+            if constexpr (sizeof(T) == 4) {
+              if constexpr (TWO_SM) tc_mma_tf32_pair(d_tmem, ad, bd, idesc, acc);
+              else tc_mma_tf32(d_tmem, ad, bd, idesc, acc);
+            } else {
+              if constexpr (TWO_SM) tc_mma_f16_pair(d_tmem, ad, bd, idesc, acc);
+              else tc_mma_f16(d_tmem, ad, bd, idesc, acc);
+            }
           }
           // buffer free once these MMAs finish (in both blocks of a pair)
           if constexpr (TWO_SM) tc_commit_pair_mc(empty_bar(stage), (uint16_t)3u);
@@ -480,7 +518,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     int it = 0;
     for (int u = worker; u < n_units; u += workers, ++it) {
       int m0, tn, kbeg, nkb, z, tail, bz;
-      unit_coords<PAIR>(u, p, rank, m0, tn, kbeg, nkb, z, tail, bz);
+      unit_coords<PAIR, kblk<T>()>(u, p, rank, m0, tn, kbeg, nkb, z, tail, bz);
       const int n0 = tn * BN;
       const int buf = it & 1;
       const uint32_t acc_phase = (uint32_t)(it >> 1) & 1u;
@@ -502,7 +540,50 @@ __global__ void __launch_bounds__(THREADS, 1)
       float* const tail_strip =
           tail >= 0 ? p.tail_ws + ((((int64_t)(tail * P + rank) * p.tail_splits + z) * 4 + q) * STRIP)
                     : nullptr;
-      if (!SPLIT && tail < 0 && p.c_tma) {
+      if constexpr (sizeof(T) == 4) if (!SPLIT && tail < 0 && p.c_tma) {
+        // fp32 C through TMA stores, 32 columns (128 bytes a row) at a time,
+        // in the same 128-byte swizzle as the 16-bit path below
+        constexpr int NB = C_::NBUF;
+        const bool epi = p.ep.bias != nullptr || p.ep.act != 0;
+#pragma unroll 1
+        for (int c = 0; c < BN / 32; ++c) {
+          uint32_t r[32];
+          __syncwarp();
+          tmem_ld_32x32b_x32(t_row + (uint32_t)(c * 32), r);
+          tmem_ld_wait();
+          if (c == BN / 32 - 1) {
+            tc_fence_before();
+            if constexpr (TWO_SM) mbar_arrive_cluster(mapa_shared(acce_bar(buf), 0u));
+            else mbar_arrive(acce_bar(buf));
+          }
+          const int gn0 = n0 + c * 32;
+          const uint32_t sbuf = staging_addr + (uint32_t)((q * NB + c % NB) * 4096);
+          if (lane == 0) bulk_wait_read<NB - 1>();
+          __syncwarp();
+#pragma unroll
+          for (int w = 0; w < 8; ++w) {
+            float x[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              x[e] = p.alpha * __uint_as_float(r[4 * w + e]);
+              const int col = gn0 + 4 * w + e;
+              if (epi && col < p.N) x[e] = apply_epilogue<T>(x[e], p.ep, col);
+            }
+            const uint32_t dst = sbuf + (uint32_t)(lane * 128 + ((w ^ (lane & 7)) * 16));
+            asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(dst), "f"(x[0]),
+                         "f"(x[1]), "f"(x[2]), "f"(x[3])
+                         : "memory");
+          }
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0 && m0 + q * 32 < p.M && gn0 < p.N) {
+            tma_store_3d(&tmC, gn0, m0 + q * 32, bz, sbuf);
+            bulk_commit();
+          }
+        }
+        continue;
+      }
+      if constexpr (sizeof(T) == 2) if (!SPLIT && tail < 0 && p.c_tma) {
         // C through TMA stores, 64 columns at a time: two tensor-memory loads
         // in flight, the 32 x 64 16-bit block packed into this warp's staging
         // buffer in the 128-byte swizzle (16-byte chunk w of row l at chunk
@@ -676,21 +757,21 @@ PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
   return fn;
 }
 
-// 3-D tensor map over `batch` row-major [rows, cols] 16-bit matrices with row
-// pitch `ld` and batch pitch `stride` elements; box = box_cols (inner) x
+// 3-D tensor map over `batch` row-major [rows, cols] matrices of `esize`-byte
+// elements with row pitch `ld` and batch pitch `stride` elements; box = box_cols (inner) x
 // box_rows x 1, 128-byte swizzle by default, out-of-range elements read as
 // zero.  Returns false when the driver rejects the description (the launch
 // then reports cudaErrorNotSupported and nothing runs).
 bool make_map(CUtensorMap* map, CUtensorMapDataType type, const void* base, int64_t rows,
               int64_t cols, int64_t ld, int box_cols, int box_rows,
               CUtensorMapSwizzle swizzle = CU_TENSOR_MAP_SWIZZLE_128B, int64_t batch = 1,
-              int64_t stride = 0) {
+              int64_t stride = 0, int esize = 2) {
   auto enc = get_encode();
   if (!enc) return false;
   // [batch][rows][cols]; a single matrix is batch 1 with a nominal pitch
   if (batch <= 1) stride = ld * (rows > 0 ? rows : 1);
   cuuint64_t dims[3] = {(cuuint64_t)cols, (cuuint64_t)rows, (cuuint64_t)(batch > 1 ? batch : 1)};
-  cuuint64_t strides[2] = {(cuuint64_t)(ld * 2), (cuuint64_t)(stride * 2)};
+  cuuint64_t strides[2] = {(cuuint64_t)(ld * esize), (cuuint64_t)(stride * esize)};
   cuuint32_t box[3] = {(cuuint32_t)box_cols, (cuuint32_t)box_rows, 1};
   cuuint32_t estr[3] = {1, 1, 1};
   CUresult r = enc(map, type, 3, const_cast<void*>(base), dims,
@@ -746,18 +827,22 @@ cudaError_t launch_cfg(const HgemmArgs& a, const HParams& p, LaunchCtx& ctx) {
   const CUtensorMapSwizzle SW = CU_TENSOR_MAP_SWIZZLE_128B;
   // a pitch-0 operand is one matrix shared by every batch entry (z stays 0)
   const int64_t nba = p.za_mask ? a.batch : 1, nbb = p.zb_mask ? a.batch : 1;
-  if (A_MN) ok = make_map(&mA, TY, a.A, a.K, a.M, a.lda, 64, 64, SW, nba, a.stride_a);  // [K, M]
-  else ok = make_map(&mA, TY, a.A, a.M, a.K, a.lda, 64, BM, SW, nba, a.stride_a);       // [M, K]
+  // K-major boxes are one 128-byte swizzle row deep in K (64 16-bit or 32
+  // fp32 elements); MN-major boxes (16-bit types only) are 64 x 64
+  constexpr int KB = kblk<T>(), ES = (int)sizeof(T);
+  if (A_MN) ok = make_map(&mA, TY, a.A, a.K, a.M, a.lda, 64, 64, SW, nba, a.stride_a, ES);  // [K, M]
+  else ok = make_map(&mA, TY, a.A, a.M, a.K, a.lda, KB, BM, SW, nba, a.stride_a, ES);       // [M, K]
   if (!ok) return cudaErrorNotSupported;
-  if (B_MN) ok = make_map(&mB, TY, a.B, a.K, a.N, a.ldb, 64, 64, SW, nbb, a.stride_b);  // [K, N]
-  else ok = make_map(&mB, TY, a.B, a.N, a.K, a.ldb, 64, PAIR ? BN / 2 : BN, SW, nbb,
-                     a.stride_b);                                                          // [N, K]
+  if (B_MN) ok = make_map(&mB, TY, a.B, a.K, a.N, a.ldb, 64, 64, SW, nbb, a.stride_b, ES);  // [K, N]
+  else ok = make_map(&mB, TY, a.B, a.N, a.K, a.ldb, KB, PAIR ? BN / 2 : BN, SW, nbb,
+                     a.stride_b, ES);                                                          // [N, K]
   if (!ok) return cudaErrorNotSupported;
-  // C: row-major [M, N], 64 x 32 boxes, 128-byte swizzle (used only when p.c_tma)
+  // C: row-major [M, N], 128-byte x 32-row boxes (64 x 32 16-bit, 32 x 32 fp32),
+  // 128-byte swizzle (used only when p.c_tma)
   CUtensorMap mC;
   memset(&mC, 0, sizeof(mC));
-  if (p.c_tma && !make_map(&mC, TY, a.C, a.M, a.N, a.ldc, 64, 32, CU_TENSOR_MAP_SWIZZLE_128B,
-                           p.batch, p.stride_c))
+  if (p.c_tma && !make_map(&mC, TY, a.C, a.M, a.N, a.ldc, KB, 32, CU_TENSOR_MAP_SWIZZLE_128B,
+                           p.batch, p.stride_c, ES))
     return cudaErrorNotSupported;
   auto kern = hgemm_tc_kernel<T, BN, A_MN, B_MN, SPLIT, MODE>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -798,6 +883,14 @@ cudaError_t launch_bn(const HgemmArgs& a, const HParams& p, LaunchCtx& ctx) {
   const bool A_MN = a.transA != 0, B_MN = a.transB == 0, split = a.splits > 1;
   constexpr bool CAN_PAIR = BN == 128 || BN == 256;
   constexpr int M1 = CAN_PAIR ? 1 : 0, M2 = CAN_PAIR ? 2 : 0;
+  if constexpr (sizeof(T) == 4) {
+    // TF32 operands are staged K-major only (the dispatcher packs them so)
+    if (A_MN || B_MN) return cudaErrorInvalidValue;
+    if (split) return launch_cfg<T, BN, false, false, true, 0>(a, p, ctx);
+    if (CAN_PAIR && p.pair == 2) return launch_cfg<T, BN, false, false, false, M2>(a, p, ctx);
+    if (CAN_PAIR && p.pair == 1) return launch_cfg<T, BN, false, false, false, M1>(a, p, ctx);
+    return launch_cfg<T, BN, false, false, false, 0>(a, p, ctx);
+  } else {
 #define GB300_HG(AM, BMN)                                                   \
   if (A_MN == AM && B_MN == BMN) {                                          \
     if (split) return launch_cfg<T, BN, AM, BMN, true, 0>(a, p, ctx);       \
@@ -810,6 +903,7 @@ cudaError_t launch_bn(const HgemmArgs& a, const HParams& p, LaunchCtx& ctx) {
   GB300_HG(false, false)
   GB300_HG(true, false)
 #undef GB300_HG
+  }
   return cudaErrorInvalidValue;
 }
 
@@ -823,7 +917,7 @@ cudaError_t launch_hgemm_t(const HgemmArgs& a, LaunchCtx& ctx) {
   p.ldc = a.ldc;
   p.M = a.M; p.N = a.N; p.K = a.K;
   p.splits = a.splits > 1 ? a.splits : 1;
-  p.k_slice = a.splits > 1 ? a.k_slice : ((a.K + BK - 1) / BK) * BK;
+  p.k_slice = a.splits > 1 ? a.k_slice : ((a.K + kblk<T>() - 1) / kblk<T>()) * kblk<T>();
   const int bn = a.bn;
   p.tiles_m = (a.M + BM - 1) / BM;
   p.tiles_n = (a.N + bn - 1) / bn;
@@ -831,9 +925,11 @@ cudaError_t launch_hgemm_t(const HgemmArgs& a, LaunchCtx& ctx) {
   p.status = ctx.status;
   p.timeout_ns = ctx.timeout_ns;
   p.fault_injection = a.fault_injection;
-  p.c_vec_ok = ((reinterpret_cast<uintptr_t>(a.C) & 15u) == 0 && (a.ldc % 8) == 0 &&
-                (a.batch <= 1 || (a.stride_c % 8) == 0)) ? 1 : 0;
-  p.c_tma = (p.c_vec_ok && a.beta == 0.f && a.splits <= 1 && a.c_tma && bn >= 64) ? 1 : 0;
+  constexpr int VEC = 16 / (int)sizeof(T);  // elements per 16 bytes
+  p.c_vec_ok = ((reinterpret_cast<uintptr_t>(a.C) & 15u) == 0 && (a.ldc % VEC) == 0 &&
+                (a.batch <= 1 || (a.stride_c % VEC) == 0)) ? 1 : 0;
+  p.c_tma = (p.c_vec_ok && a.beta == 0.f && a.splits <= 1 && a.c_tma &&
+             bn >= (sizeof(T) == 4 ? 32 : 64)) ? 1 : 0;
   p.pair = hgemm_use_pair(bn, a.M, p.splits, a.pair) ? a.pair : 0;
   p.dp_units = a.dp_units;
   p.tail_splits = a.tail_splits;

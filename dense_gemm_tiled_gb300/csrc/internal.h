@@ -64,7 +64,7 @@ struct HgemmArgs {
   int pair;             // block pairs allowed: 0 none, 1 multicast B, 2 2-SM MMAs
   int c_tma;            // allow TMA stores of C (used when beta == 0 and C is aligned)
   int fault_injection;  // test hook: 1 = producer skips its first stage
-  int dtype = 1;        // 1 fp16, 2 bf16 (gemm_dtype_t)
+  int dtype = 1;        // 1 fp16, 2 bf16, 3 fp32 on TF32 MMAs (gemm_dtype_t)
   // strided batch (batch > 1: no split, no tail): element pitches between
   // consecutive matrices; 16-bit TMA needs them (and ld) multiples of 8
   int batch = 1;
@@ -93,6 +93,8 @@ struct LaunchCtx {
 cudaError_t launch_sgemm(const SgemmArgs& a, LaunchCtx& ctx);
 cudaError_t launch_hgemm(const HgemmArgs& a, LaunchCtx& ctx);
 cudaError_t launch_hgemm_bf16(const HgemmArgs& a, LaunchCtx& ctx);
+// fp32 operands and output on kind::tf32 MMAs (HgemmArgs.dtype 3; K-major A and B)
+cudaError_t launch_hgemm_tf32(const HgemmArgs& a, LaunchCtx& ctx);
 // C[M,N] = alpha * sum_z P[z] + beta * C; dtype 0 = fp32 C, 1 = fp16 C, 2 = bf16 C.
 cudaError_t launch_splitk_reduce(int dtype, int M, int N, int splits, const float* P, void* C,
                                  int64_t ldc, float alpha, float beta, LaunchCtx& ctx,
@@ -103,6 +105,10 @@ cudaError_t launch_scale(int dtype, int M, int N, void* C, int64_t ldc, float be
 // dst[c][r] = src[r][c] (fp32 rows x cols).
 cudaError_t launch_transpose_f32(int rows, int cols, const float* src, int64_t ld_src,
                                  float* dst, int64_t ld_dst, LaunchCtx& ctx);
+// dst[r][c] = src[r][c] for c < cols (32-bit elements; dst columns past cols
+// untouched).
+cudaError_t launch_repack_32(int rows, int cols, const void* src, int64_t ld_src, void* dst,
+                             int64_t ld_dst, LaunchCtx& ctx);
 // dst[r][c] = src[r][c] for c < cols, 0 for cols <= c < ld_dst (16-bit elements,
 // fp16 or bf16: +0 is the zero bit pattern in both).
 cudaError_t launch_repack_16(int rows, int cols, const void* src, int64_t ld_src, void* dst,

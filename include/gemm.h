@@ -65,10 +65,19 @@ typedef enum {
     GEMM_F32 = 0,         /* A, B, C fp32; fp32 FMA accumulation */
     GEMM_F16_F32ACC = 1,  /* A, B, C fp16 (IEEE binary16); fp32 accumulation;
                              result rounded to fp16 round-to-nearest-even */
-    GEMM_BF16_F32ACC = 2  /* A, B, C bfloat16; fp32 accumulation; result
+    GEMM_BF16_F32ACC = 2, /* A, B, C bfloat16; fp32 accumulation; result
                              rounded to bfloat16 round-to-nearest-even (the
                              bfloat16 row of the LoRA page's section 1 type
                              table, native on these tensor cores) */
+    GEMM_F32_TF32 = 3     /* OPT-IN reduced precision: A, B, C fp32, but the
+                             products use only the TF32 part of each operand
+                             (sign, 8 exponent and the top 10 fraction bits)
+                             on the tensor cores; fp32 accumulation.  Error up
+                             to ~2^-9 * sum|a*b|, against ~K * 2^-24 for
+                             GEMM_F32.  The counterpart of the relaxed-
+                             precision switch of "Optimizing GEMM on Apple's
+                             M5 from scratch, Part 2"; never chosen for you.
+                             Not accepted by gemm_splitk_noalloc. */
 } gemm_dtype_t;
 
 typedef enum {

@@ -11,6 +11,9 @@ Tolerances, elementwise, with ref and mag from the oracle
          (bf16 keeps 8 significant bits: rounding the fp32 result moves it by
          at most 2^-9 |ref|, and the bound allows twice that; its subnormal
          spacing is 2^-133)
+  tf32:  |C - ref| <= (2^-9 + 1e-5) * mag   (the opt-in TF32 path keeps 10 of
+         the 23 fraction bits of each operand: relative error below 2^-10 per
+         operand, 2^-9 per product, plus the fp32 accumulation of fp32)
   small-integer inputs: bit-exact -- fp32 C == ref, fp16/bf16 C == RNE(ref).
 The fp32 bound is the one the pages' observations support: reassociating an
 fp32 sum moves low bits by ~1e-5 at 512^3 ("From a C loop to a GPU kernel",
@@ -22,6 +25,7 @@ import numpy as np
 from . import bf16_to_double, half_to_double, round_bf16_rne, round_half_rne
 
 F32_REL = 1e-5
+TF32_REL = 2.0 ** -9 + 1e-5
 F16_REL = 1e-4
 F16_OUT = 1e-3
 BF16_OUT = 4e-3
@@ -67,6 +71,8 @@ def check(C, ref, mag, dtype: str, exact: bool = False) -> dict:
             bound = F16_REL * mag + F16_OUT * np.abs(ref) + F16_SUB
         elif dtype == "bf16":
             bound = F16_REL * mag + BF16_OUT * np.abs(ref) + BF16_SUB
+        elif dtype == "tf32":
+            bound = TF32_REL * mag
         else:
             bound = F32_REL * mag
         ok = err <= bound
@@ -118,7 +124,7 @@ def check_epilogue(C, ref_pre, mag, dtype: str, bias=None, act: str = "none", ex
         b = np.asarray(bias, dtype=np.float64)
         bj = b[np.asarray(cols_index)] if ref_pre.ndim == 1 else np.broadcast_to(b, ref_pre.shape)
     x = ref_pre + bj
-    rel = F32_REL if dtype == "f32" else F16_REL
+    rel = {"f32": F32_REL, "tf32": TF32_REL}.get(dtype, F16_REL)
     lip = GELU_LIPSCHITZ if act == "gelu" else 1.0
     bound = lip * (rel * mag + EPI_ARITH * (mag + np.abs(bj)))
     if act == "gelu":

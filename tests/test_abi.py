@@ -112,3 +112,14 @@ def test_gemm_ex_invalid_arguments(b):
     assert b.gemm_ex_raw(0, 0, 4, 4, 4, 0, 1.0, 0.0, PA, 4, PB, 4, PC, 4, PC + 16, 2) == 3
     assert b.gemm_ex_raw(0, 0, 0, 4, 4, 0, 1.0, 0.0, PA, 4, PB, 4, PC, 4, 0, 2) == 0
     assert b.last_path() == "none"
+
+
+def test_tf32_not_accepted_without_scratch(b, lib_path):
+    import ctypes
+    lib = ctypes.CDLL(lib_path)
+    f = lib.gemm_splitk_noalloc
+    i64, ci, cf, vp = ctypes.c_int64, ctypes.c_int, ctypes.c_float, ctypes.c_void_p
+    f.argtypes = [ci, ci, i64, i64, i64, ci, cf, cf, vp, i64, vp, i64, vp, i64, vp]
+    f.restype = ci
+    assert f(0, 0, 4, 4, 4, 3, 1.0, 0.0, PA, 4, PB, 4, PC, 4, None) == 2
+    assert b.gemm_raw(0, 0, 4, 4, 4, 4, 1.0, 0.0, PA, 4, PB, 4, PC, 4) == 1  # dtype 4 unknown

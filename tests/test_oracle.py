@@ -442,3 +442,38 @@ def test_checker_epilogue():
     wrong_axis = oracle.bias_act(np.ascontiguousarray(sq.T), b, "none").T  # bias along rows
     assert not compare.check_epilogue(wrong_axis.astype(np.float32), sq, msq, "f32", b,
                                       "none")["ok"]
+
+
+def _tf32(x, mode):
+    """fp32 values reduced to TF32 (10 fraction bits) by truncation or by
+    round-to-nearest-even of the low 13 bits, on the bit patterns."""
+    b = np.ascontiguousarray(x, dtype=np.float32).view(np.uint32).astype(np.uint64)
+    if mode == "rne":
+        lsb = (b >> 13) & 1
+        b = b + 0xFFF + lsb
+    b = (b & 0xFFFFE000) & 0xFFFFFFFF
+    return b.astype(np.uint32).view(np.float32)
+
+
+def test_tf32_bound_covers_operand_reduction():
+    """The opt-in TF32 tolerance, (2^-9 + 1e-5) * mag, holds for a product of
+    TF32-reduced operands -- truncated or rounded -- accumulated exactly, and
+    is violated by a coarser (8 fraction bits) reduction; fp32's own bound is
+    violated by TF32, so the tf32 check is the looser one it must be."""
+    r = _rng(12)
+    A = _f32(r.uniform(-1, 1, (64, 300)))
+    B = _f32(r.uniform(-1, 1, (300, 48)))
+    ref, mag = oracle.gemm_ref(A, B)
+    for mode in ("trunc", "rne"):
+        got = _tf32(A, mode).astype(np.float64) @ _tf32(B, mode).astype(np.float64)
+        assert compare.check(got.astype(np.float32), ref, mag, "tf32")["ok"], mode
+        assert not compare.check(got.astype(np.float32), ref, mag, "f32")["ok"], mode
+    # same-signed operands make truncation errors add up: 10 kept fraction
+    # bits stay inside the bound, 8 do not
+    Ap, Bp = np.abs(A), np.abs(B)
+    refp, magp = oracle.gemm_ref(Ap, Bp)
+    got = _tf32(Ap, "trunc").astype(np.float64) @ _tf32(Bp, "trunc").astype(np.float64)
+    assert compare.check(got.astype(np.float32), refp, magp, "tf32")["ok"]
+    coarse = lambda x: (np.ascontiguousarray(x).view(np.uint32) & 0xFFFF8000).view(np.float32)
+    got = coarse(Ap).astype(np.float64) @ coarse(Bp).astype(np.float64)
+    assert not compare.check(got.astype(np.float32), refp, magp, "tf32")["ok"]
