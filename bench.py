@@ -282,6 +282,56 @@ def lora_step(dev, stream, reps: int = 20):
             "sum_of_gemms_ms": sum(v["us"] for v in per.values()) / 1e3, "per_gemm": per}
 
 
+TF32_PER_BF16 = 1.1 / 2.25  # nominal dense TF32 / BF16 tensor rates
+
+
+def tf32_4096(dev, stream, flops, peaks, args):
+    """The opt-in TF32 path (fp32 operands on kind::tf32 MMAs) at 4096^3, nt
+    (operands already K-major) and nn (B packed first): per-launch medians
+    with L2 flushed, the whole call and the MMA kernel alone (events the
+    library records around it), against the measured bf16 peak scaled by the
+    nominal TF32/BF16 ratio."""
+    import torch
+    from dense_gemm_tiled_gb300 import binding, inputs
+    peak = peaks["bf16_tflops"] * TF32_PER_BF16
+    flush = torch.empty(int(2.5 * L2_BYTES) // 4, dtype=torch.float32, device=dev)
+    out = {}
+    for var in ("nt", "nn"):
+        tA, tB = inputs.VARIANTS[var]
+        p = inputs.make_problem(M, N, K, tA, tB, "f32", seed=75)
+        A, B = p.A.to(dev), p.B.to(dev)
+        C = torch.empty((M, N), dtype=torch.float32, device=dev)
+        for _ in range(args.warmup):
+            binding.gemm(A, B, C, tA, tB, stream=stream, tf32=True)
+        ks, ke = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        ks.record(stream); ke.record(stream)
+        call, kern = [], []
+        for _ in range(max(10, min(30, args.steps))):
+            with torch.cuda.stream(stream):
+                flush.fill_(1.0)
+            s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            binding.set_kernel_events(ks, ke)
+            s.record(stream)
+            binding.gemm(A, B, C, tA, tB, stream=stream, tf32=True)
+            e.record(stream)
+            binding.set_kernel_events()
+            e.synchronize()
+            call.append(s.elapsed_time(e))
+            kern.append(ks.elapsed_time(ke))
+        kmed = statistics.median(kern)
+        ach = flops / (kmed * 1e-3) / 1e12
+        out[var] = {"tflops_call": flops / (statistics.median(call) * 1e-3) / 1e12,
+                    "tflops_kernel": ach, "path": binding.last_path(),
+                    "roofline": {"bound": "tensor", "achieved": ach, "peak": peak,
+                                 "unit": "TFLOP/s", "frac": ach / peak,
+                                 "peak_basis": f"{peaks['source']} bf16 dense burst x "
+                                               f"{TF32_PER_BF16:.4f} (nominal TF32/BF16)"}}
+        del A, B, C
+    del flush
+    assert binding.check_device_status(stream) == binding.OK
+    return out
+
+
 def attention_step(dev, stream, reps: int = 20, H: int = 16, n: int = 2048, d: int = 128):
     """The six GEMMs of one attention layer ("Metal GEMM Kernels for LoRA
     Training", section 8: S = Q K^T, O = P V, dV = P^T dO, dP = dO V^T,
@@ -530,6 +580,7 @@ def main():
         del flush
         assert binding.check_device_status(stream) == binding.OK
 
+    tf32 = None if args.no_fp16 else tf32_4096(dev, stream, flops, peaks, args)
     lora = None if args.no_lora else lora_step(dev, stream)
     attn = None if args.no_attention else attention_step(dev, stream)
 
@@ -569,6 +620,7 @@ def main():
             "step_device_ms_avg": avg_step_ms,
             "roofline": roofline,
             "fp16_4096": fp16,
+            "tf32_4096": tf32,
             "lora_step": lora,
             "attention": attn,
             "e2e": e2e,
