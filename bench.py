@@ -400,20 +400,21 @@ def run_case(args, local):
     from dense_gemm_tiled_gb300 import binding, inputs
     dt, var, size = args.case.split("_")
     n = int(size)
+    tf32 = dt == "tf32"  # the opt-in TF32 path on fp32 data
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
     tA, tB = inputs.VARIANTS[var]
-    p = inputs.make_problem(n, n, n, tA, tB, dtype=dt, seed=80)
+    p = inputs.make_problem(n, n, n, tA, tB, dtype="f32" if tf32 else dt, seed=80)
     A, B = p.A.to(dev), p.B.to(dev)
     C = torch.empty((n, n), dtype=A.dtype, device=dev)
     s = torch.cuda.Stream(dev)
     for _ in range(args.warmup):
-        binding.gemm(A, B, C, tA, tB, stream=s)
+        binding.gemm(A, B, C, tA, tB, stream=s, tf32=tf32)
     ts = []
     for _ in range(args.steps):
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record(s)
-        binding.gemm(A, B, C, tA, tB, stream=s)
+        binding.gemm(A, B, C, tA, tB, stream=s, tf32=tf32)
         e1.record(s)
         e1.synchronize()
         ts.append(e0.elapsed_time(e1))
@@ -435,7 +436,7 @@ def main():
     ap.add_argument("--no-lora", action="store_true")
     ap.add_argument("--no-attention", action="store_true")
     ap.add_argument("--case", default=None,
-                    help="run only one GEMM (e.g. f32_nn_4096, f16_tn_4096, f16_nn_8192): "
+                    help="run only one GEMM (e.g. f32_nn_4096, f16_tn_4096, f16_nn_8192, tf32_nt_4096): "
                          "warm-up + steps, one short JSON line; used for profiling")
     args = ap.parse_args()
     if args.warmup < 3:
