@@ -46,7 +46,8 @@ TailPlan hgemm_plan_tail(int M, int N, int K, int bn, bool pair, int workers) {
   t.dp_units = full * workers;
   const int halves = pair ? 2 : 1;
   t.ws_bytes = (size_t)rem * halves * t.splits * BM * bn * sizeof(float);
-  t.cnt_bytes = (size_t)rem * halves * 4 * sizeof(unsigned int);
+  // one counter per 32-row strip and epilogue column share (at most two)
+  t.cnt_bytes = (size_t)rem * halves * 4 * 2 * sizeof(unsigned int);
   return t;
 }
 

@@ -98,7 +98,15 @@ __host__ __device__ constexpr int kmma() { return 32 / (int)sizeof(T); }
 
 constexpr int BM = HG_BM;     // 128 accumulator rows = 128 TMEM lanes
 constexpr int BK = HG_BK;     // 64 fp16 = 128 bytes = one swizzle atom row (16-bit types)
-constexpr int THREADS = 192;
+// Epilogue warps: 4 (one per 32-lane quarter of the accumulator) or 8 (two per
+// quarter, each draining half of the tile's columns)
+#ifndef GB300_HG_EPI_WARPS
+#define GB300_HG_EPI_WARPS 8
+#endif
+constexpr int EPI_WARPS = GB300_HG_EPI_WARPS;
+constexpr int EPI_HALVES = EPI_WARPS / 4;
+static_assert(EPI_WARPS == 4 || EPI_WARPS == 8, "epilogue warps");
+constexpr int THREADS = 64 + 32 * EPI_WARPS;
 constexpr int GROUP_M = 8;
 constexpr int A_TILE_BYTES = BM * BK * 2;  // 16 KiB
 constexpr int SMEM_LIMIT = 227 * 1024;  // opt-in shared memory per block
@@ -114,17 +122,22 @@ struct Cfg {
   static constexpr int B_COLS = B_MN ? (BN < 64 ? 64 : BN) : BN;
   static constexpr int B_TILE_BYTES = (MODE == 2 ? B_COLS / 2 : B_COLS) * BK * 2;
   static constexpr int STAGE_BYTES = A_TILE_BYTES + B_TILE_BYTES;
-  // C staging for TMA stores: per epilogue warp NBUF buffers of a 32 x 64
-  // 16-bit box (4 KiB); two buffers unless that would cost a stage
+  // C staging for TMA stores: 4 KiB buffers (one 32-row box of 128-byte rows).
+  // Four epilogue warps take two each when that costs no pipeline stage, else
+  // one; eight warps (both column shares, for short-K tiles) take one each and
+  // are allowed only where that costs no stage either (EPI2).
   static constexpr int FIXED_BYTES = 1024 /*align*/ + 256 /*barriers*/;
-  static constexpr int STAGES2 = (SMEM_LIMIT - FIXED_BYTES - 4 * 2 * 4096) / STAGE_BYTES;
-  static constexpr int STAGES1 = (SMEM_LIMIT - FIXED_BYTES - 4 * 1 * 4096) / STAGE_BYTES;
-  static constexpr int NBUF = (STAGES2 >= 8 || STAGES2 == STAGES1) ? 2 : 1;
-  static constexpr int STAGES_RAW = NBUF == 2 ? STAGES2 : STAGES1;
+  static constexpr int STAGES_OF(int staging) {
+    return (SMEM_LIMIT - FIXED_BYTES - staging) / STAGE_BYTES;
+  }
+  static constexpr int NBUF4 = (STAGES_OF(8 * 4096) >= 8 || STAGES_OF(8 * 4096) == STAGES_OF(4 * 4096)) ? 2 : 1;
+  static constexpr int STAGING4 = 4 * NBUF4 * 4096;
+  static constexpr bool EPI2 = EPI_WARPS == 8 && STAGES_OF(8 * 4096) >= (STAGES_OF(STAGING4) < 8 ? STAGES_OF(STAGING4) : 8);
+  static constexpr int STAGING_BYTES = (EPI2 && STAGING4 < 8 * 4096) ? 8 * 4096 : STAGING4;
+  static constexpr int STAGES_RAW = STAGES_OF(STAGING_BYTES);
   static constexpr int STAGES = STAGES_RAW > 8 ? 8 : STAGES_RAW;
   // two accumulator buffers of BN fp32 columns, rounded up to a power of two
   static constexpr int TMEM_COLS = 2 * BN <= 64 ? 64 : 2 * BN <= 128 ? 128 : 2 * BN <= 256 ? 256 : 512;
-  static constexpr int STAGING_BYTES = 4 * NBUF * 4096;
   static constexpr int SMEM_BYTES =
       STAGES * STAGE_BYTES + STAGING_BYTES + 1024 /*align*/ + 256 /*barriers*/;
 };
@@ -154,6 +167,7 @@ struct HParams {
   int64_t stride_c;  // elements between consecutive C matrices
   int za_mask, zb_mask;  // -1: operand batched; 0: one matrix shared by all (pitch 0)
   Epilogue ep;           // bias (output type, per column) and activation
+  int epi_halves;        // epilogue warps in use per accumulator quarter: 1 or EPI_HALVES
   float* tail_ws;          // [tail tiles][pair ? 2 : 1][tail_splits][4 warps][32 x BN]
   unsigned int* tail_cnt;  // [tail tiles][pair ? 2 : 1][4], zero on entry and on exit
 };
@@ -347,7 +361,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       mbar_init(accf_bar(b), 1);
       // 2-SM pairs: both blocks' epilogues release the accumulator to the
       // even block's MMA issuer
-      mbar_init(acce_bar(b), TWO_SM ? 256 : 128);
+      mbar_init(acce_bar(b), (TWO_SM ? 2 : 1) * 32 * 4 * p.epi_halves);
     }
     mbar_init(drain_bar, 1);
     *abort_flag = 0u;
@@ -515,8 +529,32 @@ __global__ void __launch_bounds__(THREADS, 1)
     // ------------------------------------------------------------ epilogue
     const int q = warp & 3;  // this warp may access TMEM lanes 32q .. 32q+31
     const int row = q * 32 + lane;
+    const int ew = warp - 2;                 // epilogue warp index, 0 .. EPI_WARPS-1
+    const int hh = ew / 4;                   // which share of the columns it drains
+    const int nh = p.epi_halves;             // shares in use (long-K tiles use one)
+    // this warp's 32-column chunks [c_lo, c_hi) and 64-column groups [g_lo, g_hi)
+    const int c_lo = (BN / 32) * hh / nh, c_hi = (BN / 32) * (hh + 1) / nh;
+    const int g_lo = (BN / 64) * hh / nh, g_hi = (BN / 64) * (hh + 1) / nh;
+    // staging buffers of this warp (the block's 4 KiB buffers split over the
+    // warps in use)
+    const int nbw = (C_::STAGING_BYTES / 4096) / (4 * nh);
+    auto wait_staging = [&]() {  // this warp's oldest store has read its buffer
+      if (lane == 0) {
+        if (nbw >= 2) bulk_wait_read<1>();
+        else bulk_wait_read<0>();
+      }
+      __syncwarp();
+    };
+    // the accumulator buffer is released by every epilogue thread once its
+    // last tensor-memory load of the unit is done
+    auto release_acc = [&](int buf) {
+      tc_fence_before();
+      if constexpr (TWO_SM) mbar_arrive_cluster(mapa_shared(acce_bar(buf), 0u));
+      else mbar_arrive(acce_bar(buf));
+    };
     int it = 0;
-    for (int u = worker; u < n_units; u += workers, ++it) {
+    // (warps of an unused share take no unit; they wait at the final barrier)
+    for (int u = hh < nh ? worker : n_units; u < n_units; u += workers, ++it) {
       int m0, tn, kbeg, nkb, z, tail, bz;
       unit_coords<PAIR, kblk<T>()>(u, p, rank, m0, tn, kbeg, nkb, z, tail, bz);
       const int n0 = tn * BN;
@@ -543,23 +581,18 @@ __global__ void __launch_bounds__(THREADS, 1)
       if constexpr (sizeof(T) == 4) if (!SPLIT && tail < 0 && p.c_tma) {
         // fp32 C through TMA stores, 32 columns (128 bytes a row) at a time,
         // in the same 128-byte swizzle as the 16-bit path below
-        constexpr int NB = C_::NBUF;
         const bool epi = p.ep.bias != nullptr || p.ep.act != 0;
+        if (c_lo == c_hi) release_acc(buf);
 #pragma unroll 1
-        for (int c = 0; c < BN / 32; ++c) {
+        for (int c = c_lo; c < c_hi; ++c) {
           uint32_t r[32];
           __syncwarp();
           tmem_ld_32x32b_x32(t_row + (uint32_t)(c * 32), r);
           tmem_ld_wait();
-          if (c == BN / 32 - 1) {
-            tc_fence_before();
-            if constexpr (TWO_SM) mbar_arrive_cluster(mapa_shared(acce_bar(buf), 0u));
-            else mbar_arrive(acce_bar(buf));
-          }
+          if (c == c_hi - 1) release_acc(buf);
           const int gn0 = n0 + c * 32;
-          const uint32_t sbuf = staging_addr + (uint32_t)((q * NB + c % NB) * 4096);
-          if (lane == 0) bulk_wait_read<NB - 1>();
-          __syncwarp();
+          const uint32_t sbuf = staging_addr + (uint32_t)((ew * nbw + c % nbw) * 4096);
+          wait_staging();
 #pragma unroll
           for (int w = 0; w < 8; ++w) {
             float x[4];
@@ -589,24 +622,20 @@ __global__ void __launch_bounds__(THREADS, 1)
         // buffer in the 128-byte swizzle (16-byte chunk w of row l at chunk
         // w ^ (l & 7): the 8 lanes of each store phase hit distinct banks),
         // then one TMA store clipped by the unit at M and N
-        constexpr int NB = C_::NBUF;
         const bool epi = p.ep.bias != nullptr || p.ep.act != 0;
+        if (g_lo == g_hi) release_acc(buf);
 #pragma unroll 1
-        for (int c = 0; c < BN / 32; c += 2) {
+        for (int g = g_lo; g < g_hi; ++g) {
+          const int c = 2 * g;
           uint32_t r0[32], r1[32];
           __syncwarp();
           tmem_ld_32x32b_x32(t_row + (uint32_t)(c * 32), r0);
           tmem_ld_32x32b_x32(t_row + (uint32_t)(c * 32 + 32), r1);
           tmem_ld_wait();
-          if (c + 2 >= BN / 32) {
-            tc_fence_before();
-            if constexpr (TWO_SM) mbar_arrive_cluster(mapa_shared(acce_bar(buf), 0u));
-            else mbar_arrive(acce_bar(buf));
-          }
+          if (g == g_hi - 1) release_acc(buf);
           const int gn0 = n0 + c * 32;
-          const uint32_t sbuf = staging_addr + (uint32_t)((q * NB + (c / 2) % NB) * 4096);
-          if (lane == 0) bulk_wait_read<NB - 1>();  // this buffer's previous store has read it
-          __syncwarp();
+          const uint32_t sbuf = staging_addr + (uint32_t)((ew * nbw + g % nbw) * 4096);
+          wait_staging();
           // 16-byte chunk w (columns 8w .. 8w+7 of the 64) of this lane's row;
           // r holds columns 32h .. 32h+31 (constant indices after unrolling)
           auto pack_half = [&](const uint32_t (&r)[32], int h) {
@@ -646,19 +675,16 @@ __global__ void __launch_bounds__(THREADS, 1)
         }
         continue;
       }
+      // (2-SM pairs: the even block's MMAs write both blocks' tensor memory,
+      // so the release goes to its barrier)
+      if (c_lo == c_hi) release_acc(buf);
 #pragma unroll 1
-      for (int c = 0; c < BN / 32; ++c) {
+      for (int c = c_lo; c < c_hi; ++c) {
         uint32_t r[32];
         __syncwarp();
         tmem_ld_32x32b_x32(t_row + (uint32_t)(c * 32), r);
         tmem_ld_wait();
-        if (c == BN / 32 - 1) {
-          tc_fence_before();
-          // accumulator buffer may be overwritten (2-SM pairs: tell the even
-          // block, whose MMAs write both blocks' tensor memory)
-          if constexpr (TWO_SM) mbar_arrive_cluster(mapa_shared(acce_bar(buf), 0u));
-          else mbar_arrive(acce_bar(buf));
-        }
+        if (c == c_hi - 1) release_acc(buf);
         if (tail >= 0) {
           float4* dst = reinterpret_cast<float4*>(tail_strip) + (c * 8) * 32 + lane;
 #pragma unroll
@@ -689,15 +715,17 @@ __global__ void __launch_bounds__(THREADS, 1)
           store_c32<T>(p, bz, gm, gn0, v);
         }
       }
-      if (tail >= 0) {
-        // Last slice to arrive for this 32-row strip finishes it: partial
+      if (tail >= 0 && c_lo < c_hi) {
+        // Last slice to arrive for this 32-row strip (and column share)
+        // finishes it: partial
         // writes are fenced before the arrival, the slices are summed in slice
         // order (so the result does not depend on which slice came last), and
         // the counter is left at zero for the next launch.  No waiting on
         // other blocks is involved.
         __threadfence();
         unsigned int old = 0;
-        unsigned int* cnt = p.tail_cnt + (tail * P + rank) * 4 + q;
+        // one counter per 32-row strip and column share
+        unsigned int* cnt = p.tail_cnt + ((tail * P + rank) * 4 + q) * EPI_HALVES + hh;
         if (lane == 0) old = atomicAdd(cnt, 1u);
         old = __shfl_sync(0xffffffffu, old, 0);
         if (old == (unsigned int)(p.tail_splits - 1)) {
@@ -706,7 +734,7 @@ __global__ void __launch_bounds__(THREADS, 1)
               p.tail_ws + (((int64_t)(tail * P + rank) * p.tail_splits * 4 + q) * STRIP);
           const int64_t slice_stride = 4 * (int64_t)STRIP;
 #pragma unroll 1
-          for (int c = 0; c < BN / 32; ++c) {
+          for (int c = c_lo; c < c_hi; ++c) {
             float v[32];
 #pragma unroll
             for (int j = 0; j < 32; ++j) v[j] = 0.f;
@@ -848,6 +876,9 @@ cudaError_t launch_cfg(const HgemmArgs& a, const HParams& p, LaunchCtx& ctx) {
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        C_::SMEM_BYTES);
   if (e != cudaSuccess) return e;
+  // both epilogue shares only where this configuration's staging has room
+  HParams pp = p;
+  if (!C_::EPI2) pp.epi_halves = 1;
   if constexpr (PAIR) {
     // persistent grid of as many pairs as can be resident at once
     const int max_pairs = pair_slots<T, BN, A_MN, B_MN, MODE>(a.num_sms);
@@ -866,12 +897,12 @@ cudaError_t launch_cfg(const HgemmArgs& a, const HParams& p, LaunchCtx& ctx) {
     const int pairs = units < max_pairs ? units : max_pairs;
     cfg.gridDim = dim3(2 * pairs);
     ctx.grid = 2 * pairs;
-    e = cudaLaunchKernelEx(&cfg, kern, mA, mB, mC, p);
+    e = cudaLaunchKernelEx(&cfg, kern, mA, mB, mC, pp);
   } else {
     const int units = host_total_units(p, false);
     const int grid = units < a.num_sms ? units : a.num_sms;
     ctx.grid = grid;
-    kern<<<grid, THREADS, C_::SMEM_BYTES, ctx.stream>>>(mA, mB, mC, p);
+    kern<<<grid, THREADS, C_::SMEM_BYTES, ctx.stream>>>(mA, mB, mC, pp);
     e = cudaGetLastError();
   }
   if (e == cudaSuccess) ctx.launches++;
@@ -940,6 +971,14 @@ cudaError_t launch_hgemm_t(const HgemmArgs& a, LaunchCtx& ctx) {
   p.stride_c = p.batch > 1 ? a.stride_c : 0;
   p.za_mask = (p.batch > 1 && a.stride_a != 0) ? -1 : 0;
   p.ep = a.ep;
+  // Short-K tiles are epilogue-bound: both shares of epilogue warps drain them
+  // (measured: 4096 x 4096 x 128 fp16 23.2 -> 19-21 us); long-K tiles keep one
+  // share, which leaves the main loop's warps more issue slots (4096^3 and
+  // 8192^3 were 2 % slower with two).
+  {
+    const int steps = (p.k_slice + kblk<T>() - 1) / kblk<T>();
+    p.epi_halves = (EPI_HALVES > 1 && steps <= 8) ? EPI_HALVES : 1;
+  }
   p.zb_mask = (p.batch > 1 && a.stride_b != 0) ? -1 : 0;
   if (p.tail_splits > 0 && (p.splits != 1 || !p.tail_ws || !p.tail_cnt)) return cudaErrorInvalidValue;
   if (p.batch > 1 && (p.splits != 1 || p.tail_splits > 0)) return cudaErrorInvalidValue;
