@@ -7,9 +7,12 @@
 //                  are added in increasing z, so the result does not depend on
 //                  scheduling.
 //  scale         : C = beta * C, the K == 0 case of C = alpha*A*B + beta*C.
-//  repack_16     : copies an fp16/bf16 operand whose rows are not 16-byte aligned
-//                  into a zero-padded buffer with a 16-byte row pitch, so the
-//                  tensor-memory-access unit can read it.
+//  repack        : copies an operand whose rows are not 16-byte aligned into a
+//                  zero-padded buffer with a 16-byte row pitch, so that the
+//                  tensor-memory-access unit (16-bit) or 16-byte copies (fp32)
+//                  can read it.
+//  copy_rows     : the way back: C computed into an aligned scratch copy is
+//                  copied into the caller's unaligned rows.
 //  transpose_f32 : packs an fp32 operand stored with k contiguous into the
 //                  k-major layout the FP32 kernel reads fastest (the "packing"
 //                  step of a tuned BLAS, "From a C loop to a GPU kernel", "What
@@ -17,6 +20,8 @@
 //
 // All are HBM-bound; they use grid-stride loops over 128-bit accesses
 // where the layout allows, with grids sized to a multiple of the SM count.
+#include <algorithm>
+
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
@@ -28,7 +33,7 @@
 namespace gb300 {
 namespace {
 
-int grid_for(int64_t work_items, int threads) {
+int sm_count() {
   static int sms = 0;
   if (sms == 0) {
     int dev = 0;
@@ -36,8 +41,12 @@ int grid_for(int64_t work_items, int threads) {
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     if (sms <= 0) sms = 1;
   }
+  return sms;
+}
+
+int grid_for(int64_t work_items, int threads) {
   int64_t blocks = (work_items + threads - 1) / threads;
-  const int64_t cap = (int64_t)sms * 8;
+  const int64_t cap = (int64_t)sm_count() * 8;
   if (blocks > cap) blocks = cap;
   if (blocks < 1) blocks = 1;
   return (int)blocks;
@@ -113,26 +122,62 @@ __global__ void scale_kernel(int M, int N, T* C, int64_t ldc, float beta, Epilog
   }
 }
 
-// 16-bit elements copied as bit patterns (fp16 and bf16 alike; padding is +0)
-__global__ void repack_16_kernel(int rows, int cols, const uint16_t* __restrict__ src,
-                                 int64_t ld_src, uint16_t* __restrict__ dst, int64_t ld_dst) {
-  const int64_t total = (int64_t)rows * ld_dst;
-  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < total;
-       i += (int64_t)gridDim.x * blockDim.x) {
-    const int64_t r = i / ld_dst, c = i - r * ld_dst;
-    dst[i] = (c < cols) ? src[r * ld_src + c] : (uint16_t)0;
+// Row pitch change: element bit patterns (fp16, bf16 or fp32 alike) copied
+// from rows of any alignment into rows of ld_dst elements, ld_dst a multiple
+// of one 16-byte chunk; a thread writes one chunk with a 128-bit store and
+// reads its elements one by one (coalesced across the warp); zeros past cols.
+// Blocks run over (chunk range, row) pairs: no per-element division.
+template <typename W>
+__global__ void __launch_bounds__(256) repack_kernel(int rows, int cols, const W* __restrict__ src,
+                                                     int64_t ld_src, W* __restrict__ dst,
+                                                     int64_t ld_dst) {
+  constexpr int V = 16 / sizeof(W);
+  const int chunks = (int)(ld_dst / V);
+  for (int r = blockIdx.y; r < rows; r += gridDim.y) {
+    const W* s = src + (int64_t)r * ld_src;
+    for (int q = blockIdx.x * blockDim.x + threadIdx.x; q < chunks; q += gridDim.x * blockDim.x) {
+      const int c0 = q * V;
+      uint32_t w[4];
+      if constexpr (sizeof(W) == 4) {
+#pragma unroll
+        for (int e = 0; e < 4; ++e) w[e] = (c0 + e < cols) ? (uint32_t)__ldg(s + c0 + e) : 0u;
+      } else {
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const uint32_t lo = (c0 + 2 * e < cols) ? (uint32_t)__ldg(s + c0 + 2 * e) : 0u;
+          const uint32_t hi = (c0 + 2 * e + 1 < cols) ? (uint32_t)__ldg(s + c0 + 2 * e + 1) : 0u;
+          w[e] = lo | (hi << 16);
+        }
+      }
+      *reinterpret_cast<uint4*>(dst + (int64_t)r * ld_dst + c0) = make_uint4(w[0], w[1], w[2], w[3]);
+    }
   }
 }
 
-// 32-bit elements copied row by row into a new row pitch (the columns past
-// `cols` are left as they are: the tensor maps bound every read at cols)
-__global__ void repack_32_kernel(int rows, int cols, const uint32_t* __restrict__ src,
-                                 int64_t ld_src, uint32_t* __restrict__ dst, int64_t ld_dst) {
-  const int64_t total = (int64_t)rows * cols;
-  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < total;
-       i += (int64_t)gridDim.x * blockDim.x) {
-    const int64_t r = i / cols, c = i - r * cols;
-    dst[r * ld_dst + c] = src[r * ld_src + c];
+// Plain row copy for rows of any alignment: element-wise on both sides
+// (coalesced across the warp), eight elements a thread in flight.
+template <typename W>
+__global__ void __launch_bounds__(256) copy_rows_kernel(int rows, int cols,
+                                                        const W* __restrict__ src, int64_t ld_src,
+                                                        W* __restrict__ dst, int64_t ld_dst) {
+  constexpr int U = 8;
+  for (int r = blockIdx.y; r < rows; r += gridDim.y) {
+    const W* s = src + (int64_t)r * ld_src;
+    W* d = dst + (int64_t)r * ld_dst;
+    for (int c0 = blockIdx.x * blockDim.x * U + threadIdx.x; c0 < cols;
+         c0 += gridDim.x * blockDim.x * U) {
+      W v[U];
+#pragma unroll
+      for (int e = 0; e < U; ++e) {
+        const int c = c0 + e * (int)blockDim.x;
+        v[e] = c < cols ? __ldg(s + c) : W(0);
+      }
+#pragma unroll
+      for (int e = 0; e < U; ++e) {
+        const int c = c0 + e * (int)blockDim.x;
+        if (c < cols) d[c] = v[e];
+      }
+    }
   }
 }
 
@@ -186,16 +231,48 @@ __global__ void __launch_bounds__(256) transpose_f32_kernel(int rows, int cols,
   }
 }
 
-}  // namespace
-
-cudaError_t launch_repack_32(int rows, int cols, const void* src, int64_t ld_src, void* dst,
-                             int64_t ld_dst, LaunchCtx& ctx) {
-  const int grid = grid_for((int64_t)rows * cols, 256);
-  repack_32_kernel<<<grid, 256, 0, ctx.stream>>>(rows, cols, static_cast<const uint32_t*>(src),
-                                                  ld_src, static_cast<uint32_t*>(dst), ld_dst);
+template <typename W>
+cudaError_t launch_repack(int rows, int cols, const void* src, int64_t ld_src, void* dst,
+                          int64_t ld_dst, LaunchCtx& ctx) {
+  constexpr int V = 16 / sizeof(W);
+  if (ld_dst % V != 0 || ld_dst < cols || (reinterpret_cast<uintptr_t>(dst) & 15u) != 0)
+    return cudaErrorInvalidValue;
+  if (rows <= 0 || cols <= 0) return cudaSuccess;
+  const int64_t chunks = ld_dst / V;
+  const int gx = (int)std::min<int64_t>((chunks + 255) / 256, 64);
+  const int gy = (int)std::min<int64_t>(std::min<int64_t>(rows, 65535),
+                                        std::max<int64_t>(1, (int64_t)sm_count() * 8 / gx));
+  repack_kernel<W><<<dim3(gx, gy), 256, 0, ctx.stream>>>(
+      rows, cols, static_cast<const W*>(src), ld_src, static_cast<W*>(dst), ld_dst);
   cudaError_t e = cudaGetLastError();
   if (e == cudaSuccess) ctx.launches++;
   return e;
+}
+
+}  // namespace
+
+cudaError_t launch_copy_rows(int esize, int rows, int cols, const void* src, int64_t ld_src,
+                             void* dst, int64_t ld_dst, LaunchCtx& ctx) {
+  if (esize != 2 && esize != 4) return cudaErrorInvalidValue;
+  if (rows <= 0 || cols <= 0) return cudaSuccess;
+  const int64_t per_block = 256 * 8;
+  const int gx = (int)std::min<int64_t>((cols + per_block - 1) / per_block, 64);
+  const int gy = (int)std::min<int64_t>(std::min<int64_t>(rows, 65535),
+                                        std::max<int64_t>(1, (int64_t)sm_count() * 8 / gx));
+  if (esize == 2)
+    copy_rows_kernel<uint16_t><<<dim3(gx, gy), 256, 0, ctx.stream>>>(
+        rows, cols, static_cast<const uint16_t*>(src), ld_src, static_cast<uint16_t*>(dst), ld_dst);
+  else
+    copy_rows_kernel<uint32_t><<<dim3(gx, gy), 256, 0, ctx.stream>>>(
+        rows, cols, static_cast<const uint32_t*>(src), ld_src, static_cast<uint32_t*>(dst), ld_dst);
+  cudaError_t e = cudaGetLastError();
+  if (e == cudaSuccess) ctx.launches++;
+  return e;
+}
+
+cudaError_t launch_repack_32(int rows, int cols, const void* src, int64_t ld_src, void* dst,
+                             int64_t ld_dst, LaunchCtx& ctx) {
+  return launch_repack<uint32_t>(rows, cols, src, ld_src, dst, ld_dst, ctx);
 }
 
 cudaError_t launch_transpose_f32(int rows, int cols, const float* src, int64_t ld_src,
@@ -248,13 +325,7 @@ cudaError_t launch_scale(int dtype, int M, int N, void* C, int64_t ldc, float be
 
 cudaError_t launch_repack_16(int rows, int cols, const void* src, int64_t ld_src, void* dst,
                              int64_t ld_dst, LaunchCtx& ctx) {
-  const int threads = 256;
-  const int grid = grid_for((int64_t)rows * ld_dst, threads);
-  repack_16_kernel<<<grid, threads, 0, ctx.stream>>>(rows, cols, (const uint16_t*)src, ld_src,
-                                                     (uint16_t*)dst, ld_dst);
-  cudaError_t e = cudaGetLastError();
-  if (e == cudaSuccess) ctx.launches++;
-  return e;
+  return launch_repack<uint16_t>(rows, cols, src, ld_src, dst, ld_dst, ctx);
 }
 
 }  // namespace gb300

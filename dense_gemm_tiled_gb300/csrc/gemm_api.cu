@@ -186,6 +186,18 @@ int c_tma_enabled() {
   return v;
 }
 
+// A C whose rows are not 16-byte aligned cannot go through the tensor-memory-
+// access unit; the tensor-core kernel then stores it row by row through its
+// staging buffers, which on large problems costs more than computing into an
+// aligned scratch copy (TMA stores, and TMA loads when beta != 0) and moving
+// that into place with a copy kernel (measured 4095^3 fp16, whole call:
+// 170 us row by row against 155 us through the copy with beta = 0, 335 us
+// against 177 us with beta = 1).
+bool c_scratch_wanted(const void* C, int64_t ldc, int64_t es, int M, int N) {
+  const bool aligned = ((uintptr_t)C % 16) == 0 && (ldc * es) % 16 == 0;
+  return !aligned && c_tma_enabled() && (int64_t)M * N >= (1ll << 21);
+}
+
 // Switch for the fp16 tail split (env GEMM_GB300_HG_TAIL=1 turns it on).  Off
 // by default: measured on GB300 at 4096^3 and 8192^3 it was within noise of
 // the plain persistent grid (the last, partly idle round of tiles runs faster
@@ -306,9 +318,20 @@ int run_gemm(int transA, int transB, int64_t M64, int64_t N64, int64_t K64, int 
     const size_t bytes_a = a_ok ? 0 : ((size_t)M * ldk * 4 + 255) / 256 * 256;
     const size_t bytes_b = b_ok ? 0 : ((size_t)N * ldk * 4 + 255) / 256 * 256;
     const size_t bytes_p = splits > 1 ? (size_t)splits * M * N * sizeof(float) : 0;
+    const bool c_scr = splits == 1 && c_scratch_wanted(C, ldc, 4, M, N);
+    const int64_t ldc_p = (N + 3) / 4 * 4;
+    const size_t bytes_c = c_scr ? ((size_t)M * ldc_p * 4 + 255) / 256 * 256 : 0;
     Scratch ws;
-    if (bytes_a + bytes_b + bytes_p > 0) {
-      e = ws.get(bytes_a + bytes_b + bytes_p, stream);
+    if (bytes_a + bytes_b + bytes_p + bytes_c > 0) {
+      e = ws.get(bytes_a + bytes_b + bytes_p + bytes_c, stream);
+      if (e != cudaSuccess) return cuda_fail(e);
+    }
+    void* Cd = C;
+    int64_t ldcd = ldc;
+    if (c_scr) {
+      Cd = (char*)ws.ptr + bytes_a + bytes_b + bytes_p;
+      ldcd = ldc_p;
+      if (beta != 0.f) e = launch_repack_32(M, N, C, ldc, Cd, ldc_p, ctx);
       if (e != cudaSuccess) return cuda_fail(e);
     }
     const void* Ad = A;
@@ -329,7 +352,7 @@ int run_gemm(int transA, int transB, int64_t M64, int64_t N64, int64_t K64, int 
     }
     if (e == cudaSuccess) {
       const int pair = pair_enabled();
-      HgemmArgs a{0, 1, M, N, K, Ad, ldad, Bd, ldbd, C, ldc, alpha, beta,
+      HgemmArgs a{0, 1, M, N, K, Ad, ldad, Bd, ldbd, Cd, ldcd, alpha, beta,
                   splits, k_slice, splits > 1 ? (float*)wp : nullptr, sms, bn, pair,
                   c_tma_enabled(), g_fault_injection.load()};
       a.dtype = GEMM_F32_TF32;
@@ -338,6 +361,7 @@ int run_gemm(int transA, int transB, int64_t M64, int64_t N64, int64_t K64, int 
       e = timed_hgemm(a, ctx);
       if (e == cudaSuccess && splits > 1)
         e = launch_splitk_reduce(0, M, N, splits, a.partial, C, ldc, alpha, beta, ctx, ep);
+      if (e == cudaSuccess && c_scr) e = launch_copy_rows(4, M, N, Cd, ldc_p, C, ldc, ctx);
     }
   } else if (dtype == GEMM_F32) {
     const int64_t tiles = (int64_t)((M + SG_BM - 1) / SG_BM) * ((N + SG_BN - 1) / SG_BN);
@@ -350,11 +374,16 @@ int run_gemm(int transA, int transB, int64_t M64, int64_t N64, int64_t K64, int 
     // (measured at 4096^3: tn 56.4 TF/s, nn 53.7, nt 46.9), so on large
     // problems an operand stored with k contiguous is first transposed into
     // that layout (HBM-bound, ~1 % of the GEMM's time at 4096^3).
-    const bool pack = splits == 1 && sg_pack_enabled() &&
-                      (double)M * N * K >= (double)(1ll << 30) && (!transA || transB);
+    // An operand whose rows are not 16-byte aligned is read with 4-byte
+    // copies (measured 4095^3: 42 TF/s); on large problems it is copied into
+    // a padded row pitch first, so the kernel takes 16-byte copies throughout.
+    const bool big = splits == 1 && sg_pack_enabled() && (double)M * N * K >= (double)(1ll << 30);
+    auto misaligned = [](const void* p, int64_t ld) { return ((uintptr_t)p % 16) != 0 || ld % 4 != 0; };
+    const bool packA = big && (!transA || misaligned(A, lda));
+    const bool packB = big && (transB || misaligned(B, ldb));
     const int64_t ldA_p = (M + 3) / 4 * 4, ldB_p = (N + 3) / 4 * 4;
-    const size_t bytes_A = pack && !transA ? ((size_t)K * ldA_p * 4 + 255) / 256 * 256 : 0;
-    const size_t bytes_B = pack && transB ? ((size_t)K * ldB_p * 4 + 255) / 256 * 256 : 0;
+    const size_t bytes_A = packA ? ((size_t)K * ldA_p * 4 + 255) / 256 * 256 : 0;
+    const size_t bytes_B = packB ? ((size_t)K * ldB_p * 4 + 255) / 256 * 256 : 0;
     const size_t bytes_P = splits > 1 ? (size_t)splits * M * N * sizeof(float) : 0;
     // Stream-K: without a split, a tile count that is not a whole number of
     // rounds of the SMs leaves the last round part-empty (4096^3: 1024 tiles,
@@ -378,14 +407,16 @@ int run_gemm(int transA, int transB, int64_t M64, int64_t N64, int64_t K64, int 
       e = cudaMemsetAsync(a.sk_cnt, 0, (size_t)sk_tiles * sizeof(unsigned int), stream);
       if (e != cudaSuccess) return cuda_fail(e);
     }
-    if (pack && !transA) {  // A [M,K] -> [K,M]
+    if (packA) {  // A [M,K] -> [K,M], or A [K,M] into an aligned pitch
       float* At = (float*)ws.ptr;
-      e = launch_transpose_f32(M, K, (const float*)A, lda, At, ldA_p, ctx);
+      e = transA ? launch_repack_32(K, M, A, lda, At, ldA_p, ctx)
+                 : launch_transpose_f32(M, K, (const float*)A, lda, At, ldA_p, ctx);
       a.A = At; a.lda = ldA_p; a.transA = 1;
     }
-    if (e == cudaSuccess && pack && transB) {  // B [N,K] -> [K,N]
+    if (e == cudaSuccess && packB) {  // B [N,K] -> [K,N], or B [K,N] into an aligned pitch
       float* Bt = (float*)((char*)ws.ptr + bytes_A);
-      e = launch_transpose_f32(N, K, (const float*)B, ldb, Bt, ldB_p, ctx);
+      e = transB ? launch_transpose_f32(N, K, (const float*)B, ldb, Bt, ldB_p, ctx)
+                 : launch_repack_32(K, N, B, ldb, Bt, ldB_p, ctx);
       a.B = Bt; a.ldb = ldB_p; a.transB = 0;
     }
     path = splits > 1 ? GEMM_PATH_FFMA_SPLITK : GEMM_PATH_FFMA;
@@ -420,12 +451,24 @@ int run_gemm(int transA, int transB, int64_t M64, int64_t N64, int64_t K64, int 
       tail = hgemm_plan_tail(M, N, K, bn, use_pair,
                              use_pair ? hgemm_pair_slots(bn, transA, transB, pair, sms) : sms);
     const size_t bytes_t = tail.splits > 0 ? (tail.ws_bytes + 255) / 256 * 256 + tail.cnt_bytes : 0;
+    // C rows not 16-byte aligned: see c_scratch_wanted
+    const bool c_scr = splits == 1 && tail.splits == 0 && c_scratch_wanted(C, ldc, 2, M, N);
+    const int64_t ldc_p = (N + 7) / 8 * 8;
+    const size_t bytes_c = c_scr ? ((size_t)M * ldc_p * 2 + 255) / 256 * 256 : 0;
     Scratch ws;
-    if (bytes_a + bytes_b + bytes_p + bytes_t > 0) {
-      e = ws.get(bytes_a + bytes_b + bytes_p + bytes_t, stream);
+    if (bytes_a + bytes_b + bytes_p + bytes_t + bytes_c > 0) {
+      e = ws.get(bytes_a + bytes_b + bytes_p + bytes_t + bytes_c, stream);
       if (e != cudaSuccess) return cuda_fail(e);
     }
     char* wp = (char*)ws.ptr;
+    void* Cd = C;
+    int64_t ldcd = ldc;
+    if (c_scr) {
+      Cd = wp + bytes_a + bytes_b + bytes_p + bytes_t;
+      ldcd = ldc_p;
+      if (beta != 0.f) e = launch_repack_16(M, N, C, ldc, Cd, ldc_p, ctx);
+      if (e != cudaSuccess) return cuda_fail(e);
+    }
     float* tail_ws = nullptr;
     unsigned int* tail_cnt = nullptr;
     if (tail.splits > 0) {
@@ -445,7 +488,7 @@ int run_gemm(int transA, int transB, int64_t M64, int64_t N64, int64_t K64, int 
       Bd = dst; ldbd = ldb_p; wp += bytes_b;
     }
     if (e == cudaSuccess) {
-      HgemmArgs a{transA, transB, M, N, K, Ad, ldad, Bd, ldbd, C, ldc, alpha, beta,
+      HgemmArgs a{transA, transB, M, N, K, Ad, ldad, Bd, ldbd, Cd, ldcd, alpha, beta,
                   splits, k_slice, splits > 1 ? (float*)wp : nullptr, sms, bn, pair,
                   c_tma_enabled(), g_fault_injection.load()};
       a.dtype = dtype;
@@ -461,6 +504,7 @@ int run_gemm(int transA, int transB, int64_t M64, int64_t N64, int64_t K64, int 
       e = timed_hgemm(a, ctx);
       if (e == cudaSuccess && splits > 1)
         e = launch_splitk_reduce(dtype, M, N, splits, a.partial, C, ldc, alpha, beta, ctx, ep);
+      if (e == cudaSuccess && c_scr) e = launch_copy_rows(2, M, N, Cd, ldc_p, C, ldc, ctx);
     }
   }
   g_total_launches += ctx.launches;

@@ -45,6 +45,8 @@
 #include <stdint.h>
 #include <string.h>
 
+#include <type_traits>
+
 #include "common.cuh"
 #include "internal.h"
 
@@ -154,7 +156,7 @@ struct HParams {
   uint64_t timeout_ns;
   int fault_injection;
   int c_vec_ok;  // C base 16-byte aligned and ldc % 8 == 0
-  int c_tma;     // beta == 0 and C aligned: C leaves through TMA stores
+  int c_tma;     // C aligned: C leaves through TMA stores (and comes in by TMA loads)
   int pair;      // 1: clusters of two blocks share each B tile (TMA multicast)
   // Tail split (only when splits == 1): units [0, dp_units) are whole tiles;
   // the remaining tiles are cut into tail_splits K slices of tail_k_slice, each
@@ -310,6 +312,55 @@ __device__ __forceinline__ void store_c32(const HParams& p, int bz, int gm, int 
   }
 }
 
+// The same for a 32 x 32 block of C (rows gm0 .., columns gn0 ..; lane l holds
+// row gm0 + l in r) whose rows are not 16-byte aligned, through this warp's
+// 4 KiB staging buffer: row by row from lane-owned rows, every global access
+// of the warp touches 32 rows (measured 4095^3 fp16: the kernel at 2.3x the
+// time of 4096^3); staged, the block is written in row = lane order (16-byte
+// chunk w of row l at chunk w ^ (l & 7), conflict-free) and read back one
+// column a lane, so each access covers one row.  C is loaded sixteen rows at
+// a time ahead of use.
+template <typename T>
+__device__ __forceinline__ void store_c32_staged(const HParams& p, int bz, int gm0, int gn0,
+                                                 uint32_t sbuf, const uint32_t (&r)[32],
+                                                 int lane) {
+  using E = Elem<T>;
+#pragma unroll
+  for (int w = 0; w < 8; ++w) {
+    const uint32_t a = sbuf + (uint32_t)(lane * 128 + ((w ^ (lane & 7)) * 16));
+    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(a), "r"(r[4 * w]),
+                 "r"(r[4 * w + 1]), "r"(r[4 * w + 2]), "r"(r[4 * w + 3])
+                 : "memory");
+  }
+  __syncwarp();
+  const bool epi = p.ep.bias != nullptr || p.ep.act != 0;
+  const int col = gn0 + lane;
+  T* const Cc = static_cast<T*>(p.C) + (int64_t)bz * p.stride_c + (int64_t)gm0 * p.ldc + col;
+  const int rows = min(32, p.M - gm0);
+#pragma unroll 1
+  for (int r0 = 0; r0 < rows; r0 += 16) {
+    float cv[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i)
+      cv[i] = (p.beta != 0.f && col < p.N && r0 + i < rows) ? E::to(Cc[(int64_t)(r0 + i) * p.ldc])
+                                                             : 0.f;
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      const int rr = r0 + i;
+      if (rr >= rows || col >= p.N) continue;
+      float x;
+      const uint32_t a =
+          sbuf + (uint32_t)(rr * 128 + (((lane >> 2) ^ (rr & 7)) * 16) + (lane & 3) * 4);
+      asm volatile("ld.shared.f32 %0, [%1];" : "=f"(x) : "r"(a) : "memory");
+      float o = p.alpha * x;
+      if (p.beta != 0.f) o = __fmaf_rn(p.beta, cv[i], o);
+      if (epi) o = apply_epilogue<T>(o, p.ep, col);
+      Cc[(int64_t)rr * p.ldc] = E::from(o);
+    }
+  }
+  __syncwarp();  // the buffer is rewritten by the next block
+}
+
 template <typename T, int BN, bool A_MN, bool B_MN, bool SPLIT, int MODE>
 __global__ void __launch_bounds__(THREADS, 1)
     hgemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
@@ -339,7 +390,8 @@ __global__ void __launch_bounds__(THREADS, 1)
   const uint32_t staging_addr = tiles_addr + (uint32_t)(STAGES * C_::STAGE_BYTES);
   uint8_t* const staging_ptr = tiles_ptr + STAGES * C_::STAGE_BYTES;
   uint64_t* const bars = reinterpret_cast<uint64_t*>(staging_ptr + C_::STAGING_BYTES);
-  // barrier layout: full[STAGES], empty[STAGES], acc_full[2], acc_empty[2], drain
+  // barrier layout: full[STAGES], empty[STAGES], acc_full[2], acc_empty[2], drain,
+  // the tensor-memory address slot (and abort flag) ...
   const uint32_t bar0 = smem_u32(bars);
   auto full_bar = [&](int s) { return bar0 + 8u * (uint32_t)s; };
   auto empty_bar = [&](int s) { return bar0 + 8u * (uint32_t)(STAGES + s); };
@@ -347,6 +399,10 @@ __global__ void __launch_bounds__(THREADS, 1)
   auto acce_bar = [&](int b) { return bar0 + 8u * (uint32_t)(2 * STAGES + 2 + b); };
   const uint32_t drain_bar = bar0 + 8u * (uint32_t)(2 * STAGES + 4);
   uint32_t* const tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * STAGES + 5);
+  // ... then one per C staging buffer: its TMA load of C (beta != 0) completed
+  constexpr int NSTAGING = C_::STAGING_BYTES / 4096;
+  static_assert(8 * (2 * STAGES + 6 + NSTAGING) <= 256, "barrier area");
+  auto cload_bar = [&](int b) { return bar0 + 8u * (uint32_t)(2 * STAGES + 6 + b); };
   volatile uint32_t* const abort_flag = tmem_slot + 1;
 
   const int warp = threadIdx.x >> 5;
@@ -364,6 +420,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       mbar_init(acce_bar(b), (TWO_SM ? 2 : 1) * 32 * 4 * p.epi_halves);
     }
     mbar_init(drain_bar, 1);
+    for (int b = 0; b < NSTAGING; ++b) mbar_init(cload_bar(b), 1);
     *abort_flag = 0u;
     fence_mbar_init();
   }
@@ -552,14 +609,54 @@ __global__ void __launch_bounds__(THREADS, 1)
       if constexpr (TWO_SM) mbar_arrive_cluster(mapa_shared(acce_bar(buf), 0u));
       else mbar_arrive(acce_bar(buf));
     };
+    // TMA stores: C boxes of 32 rows (64 columns of 16-bit C, 32 of fp32),
+    // numbered i in [i_lo, i_hi) within a unit, take this warp's buffers in
+    // turn across units (box i at buffer (nb0 + i - i_lo) % nbw, nb0 the
+    // boxes of earlier units), so the buffer written next is always the
+    // least recently stored from.  With beta != 0, C comes in by TMA loads of
+    // the same boxes into the buffers, ahead of use; lane 0 alone tracks which
+    // buffers have a load in flight (cpend) and their barriers' phases (cph).
+    // (fp32 C with one buffer a warp: the load of each 32-column box would be
+    // waited for in turn -- measured slower than the direct path, which keeps
+    // eight 16-byte loads a thread in flight -- so that case takes the latter)
+    constexpr int KBOX = 128 / (int)sizeof(T);
+    const bool tma_c = p.c_tma && (p.beta == 0.f || sizeof(T) == 2 || nbw >= 2);
+    const bool c_in = !SPLIT && tma_c && p.beta != 0.f;
+    const int i_lo = sizeof(T) == 4 ? c_lo : g_lo, i_hi = sizeof(T) == 4 ? c_hi : g_hi;
+    int nb = 0;
+    uint32_t cpend = 0u, cph = 0u;
+    auto c_load = [&](int lb, int gx, int gy, int bz_) {  // lane 0
+      const int bi = ew * nbw + lb;
+      bulk_wait_read<0>();  // earlier stores from the buffer have read it
+      mbar_arrive_expect_tx(cload_bar(bi), 4096u);
+      tma_load_3d(staging_addr + (uint32_t)(bi * 4096), &tmC, gx, gy, bz_, cload_bar(bi));
+      cpend |= 1u << lb;
+    };
+    auto c_wait = [&](int lb) -> bool {  // whole warp
+      bool ok = true;
+      if (lane == 0 && ((cpend >> lb) & 1u)) {
+        ok = mbar_wait(cload_bar(ew * nbw + lb), (cph >> lb) & 1u, wc);
+        if (ok) { cph ^= 1u << lb; cpend &= ~(1u << lb); }
+      }
+      return __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+    };
     int it = 0;
+    bool dead = false;
     // (warps of an unused share take no unit; they wait at the final barrier)
-    for (int u = hh < nh ? worker : n_units; u < n_units; u += workers, ++it) {
+    for (int u = hh < nh ? worker : n_units; u < n_units && !dead; u += workers, ++it) {
       int m0, tn, kbeg, nkb, z, tail, bz;
       unit_coords<PAIR, kblk<T>()>(u, p, rank, m0, tn, kbeg, nkb, z, tail, bz);
       const int n0 = tn * BN;
       const int buf = it & 1;
       const uint32_t acc_phase = (uint32_t)(it >> 1) & 1u;
+      // C of the first boxes is requested before the accumulator is ready (a
+      // box wholly past M or N is neither loaded nor stored)
+      const bool c_rows = m0 + q * 32 < p.M;
+      const int nb0 = nb;
+      auto box_buf = [&](int i) { return (nb0 + i - i_lo) % nbw; };
+      if (c_in && tail < 0 && c_rows && lane == 0)
+        for (int i = i_lo; i < i_hi && i < i_lo + nbw; ++i)
+          if (n0 + KBOX * i < p.N) c_load(box_buf(i), n0 + KBOX * i, m0 + q * 32, bz);
       // one lane waits, the warp follows: the TMEM loads below are
       // warp-collective, so the whole warp must take the same branch
       bool got = false;
@@ -578,101 +675,150 @@ __global__ void __launch_bounds__(THREADS, 1)
       float* const tail_strip =
           tail >= 0 ? p.tail_ws + ((((int64_t)(tail * P + rank) * p.tail_splits + z) * 4 + q) * STRIP)
                     : nullptr;
-      if constexpr (sizeof(T) == 4) if (!SPLIT && tail < 0 && p.c_tma) {
+      if constexpr (sizeof(T) == 4) if (!SPLIT && tail < 0 && tma_c) {
         // fp32 C through TMA stores, 32 columns (128 bytes a row) at a time,
         // in the same 128-byte swizzle as the 16-bit path below
-        const bool epi = p.ep.bias != nullptr || p.ep.act != 0;
-        if (c_lo == c_hi) release_acc(buf);
+        // (two copies of the loop: with C loads (beta != 0) and without)
+        auto boxes = [&](auto cin_tag) {
+          constexpr bool CIN = decltype(cin_tag)::value;
+          const bool epi = p.ep.bias != nullptr || p.ep.act != 0;
+          if (c_lo == c_hi) release_acc(buf);
 #pragma unroll 1
-        for (int c = c_lo; c < c_hi; ++c) {
-          uint32_t r[32];
-          __syncwarp();
-          tmem_ld_32x32b_x32(t_row + (uint32_t)(c * 32), r);
-          tmem_ld_wait();
-          if (c == c_hi - 1) release_acc(buf);
-          const int gn0 = n0 + c * 32;
-          const uint32_t sbuf = staging_addr + (uint32_t)((ew * nbw + c % nbw) * 4096);
-          wait_staging();
-#pragma unroll
-          for (int w = 0; w < 8; ++w) {
-            float x[4];
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              x[e] = p.alpha * __uint_as_float(r[4 * w + e]);
-              const int col = gn0 + 4 * w + e;
-              if (epi && col < p.N) x[e] = apply_epilogue<T>(x[e], p.ep, col);
+          for (int c = c_lo; c < c_hi; ++c) {
+            // request C of box c + nbw - 1 into the buffer box c - 1 used
+            if (CIN && c > c_lo && lane == 0 && c_rows && c + nbw - 1 < c_hi &&
+                n0 + 32 * (c + nbw - 1) < p.N)
+              c_load(box_buf(c + nbw - 1), n0 + 32 * (c + nbw - 1), m0 + q * 32, bz);
+            uint32_t r[32];
+            __syncwarp();
+            tmem_ld_32x32b_x32(t_row + (uint32_t)(c * 32), r);
+            tmem_ld_wait();
+            if (c == c_hi - 1) release_acc(buf);
+            const int gn0 = n0 + c * 32;
+            const uint32_t sbuf = staging_addr + (uint32_t)((ew * nbw + box_buf(c)) * 4096);
+            if (CIN) {
+              if (!c_wait(box_buf(c))) { dead = true; break; }
+            } else {
+              wait_staging();
             }
-            const uint32_t dst = sbuf + (uint32_t)(lane * 128 + ((w ^ (lane & 7)) * 16));
-            asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(dst), "f"(x[0]),
-                         "f"(x[1]), "f"(x[2]), "f"(x[3])
-                         : "memory");
+#pragma unroll
+            for (int w = 0; w < 8; ++w) {
+              const uint32_t dst = sbuf + (uint32_t)(lane * 128 + ((w ^ (lane & 7)) * 16));
+              float cv[4] = {0.f, 0.f, 0.f, 0.f};
+              if (CIN)
+                asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
+                             : "=f"(cv[0]), "=f"(cv[1]), "=f"(cv[2]), "=f"(cv[3])
+                             : "r"(dst)
+                             : "memory");
+              float x[4];
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                x[e] = p.alpha * __uint_as_float(r[4 * w + e]);
+                if (CIN) x[e] = __fmaf_rn(p.beta, cv[e], x[e]);
+                const int col = gn0 + 4 * w + e;
+                if (epi && col < p.N) x[e] = apply_epilogue<T>(x[e], p.ep, col);
+              }
+              asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(dst), "f"(x[0]),
+                           "f"(x[1]), "f"(x[2]), "f"(x[3])
+                           : "memory");
+            }
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0 && c_rows && gn0 < p.N) {
+              tma_store_3d(&tmC, gn0, m0 + q * 32, bz, sbuf);
+              bulk_commit();
+            }
           }
-          fence_proxy_async_smem();
-          __syncwarp();
-          if (lane == 0 && m0 + q * 32 < p.M && gn0 < p.N) {
-            tma_store_3d(&tmC, gn0, m0 + q * 32, bz, sbuf);
-            bulk_commit();
-          }
-        }
+        };
+        if (c_in) boxes(std::true_type{});
+        else boxes(std::false_type{});
+        nb += i_hi - i_lo;
         continue;
       }
-      if constexpr (sizeof(T) == 2) if (!SPLIT && tail < 0 && p.c_tma) {
+      if constexpr (sizeof(T) == 2) if (!SPLIT && tail < 0 && tma_c) {
         // C through TMA stores, 64 columns at a time: two tensor-memory loads
         // in flight, the 32 x 64 16-bit block packed into this warp's staging
         // buffer in the 128-byte swizzle (16-byte chunk w of row l at chunk
         // w ^ (l & 7): the 8 lanes of each store phase hit distinct banks),
         // then one TMA store clipped by the unit at M and N
-        const bool epi = p.ep.bias != nullptr || p.ep.act != 0;
-        if (g_lo == g_hi) release_acc(buf);
+        // (two copies of the loop: with C loads (beta != 0) and without)
+        auto boxes = [&](auto cin_tag) {
+          constexpr bool CIN = decltype(cin_tag)::value;
+          const bool epi = p.ep.bias != nullptr || p.ep.act != 0;
+          if (g_lo == g_hi) release_acc(buf);
 #pragma unroll 1
-        for (int g = g_lo; g < g_hi; ++g) {
-          const int c = 2 * g;
-          uint32_t r0[32], r1[32];
-          __syncwarp();
-          tmem_ld_32x32b_x32(t_row + (uint32_t)(c * 32), r0);
-          tmem_ld_32x32b_x32(t_row + (uint32_t)(c * 32 + 32), r1);
-          tmem_ld_wait();
-          if (g == g_hi - 1) release_acc(buf);
-          const int gn0 = n0 + c * 32;
-          const uint32_t sbuf = staging_addr + (uint32_t)((ew * nbw + g % nbw) * 4096);
-          wait_staging();
-          // 16-byte chunk w (columns 8w .. 8w+7 of the 64) of this lane's row;
-          // r holds columns 32h .. 32h+31 (constant indices after unrolling)
-          auto pack_half = [&](const uint32_t (&r)[32], int h) {
-#pragma unroll
-            for (int ww = 0; ww < 4; ++ww) {
-              const int w = 4 * h + ww;
-              uint4 o;
-              typename Elem<T>::T2* oh = reinterpret_cast<typename Elem<T>::T2*>(&o);
-#pragma unroll
-              for (int e = 0; e < 4; ++e) {
-                float x0 = p.alpha * __uint_as_float(r[8 * ww + 2 * e]);
-                float x1 = p.alpha * __uint_as_float(r[8 * ww + 2 * e + 1]);
-                if (epi) {
-                  // (columns past N are clipped by the store; their bias is not read)
-                  const int col = gn0 + 8 * w + 2 * e;
-                  if (col < p.N) x0 = apply_epilogue<T>(x0, p.ep, col);
-                  if (col + 1 < p.N) x1 = apply_epilogue<T>(x1, p.ep, col + 1);
-                }
-                oh[e] = Elem<T>::pack(x0, x1);
-              }
-              const uint32_t dst = sbuf + (uint32_t)(lane * 128 + ((w ^ (lane & 7)) * 16));
-              asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(dst), "r"(o.x),
-                           "r"(o.y), "r"(o.z), "r"(o.w)
-                           : "memory");
+          for (int g = g_lo; g < g_hi; ++g) {
+            // request C of box g + nbw - 1 into the buffer box g - 1 used
+            if (CIN && g > g_lo && lane == 0 && c_rows && g + nbw - 1 < g_hi &&
+                n0 + 64 * (g + nbw - 1) < p.N)
+              c_load(box_buf(g + nbw - 1), n0 + 64 * (g + nbw - 1), m0 + q * 32, bz);
+            const int c = 2 * g;
+            uint32_t r0[32], r1[32];
+            __syncwarp();
+            tmem_ld_32x32b_x32(t_row + (uint32_t)(c * 32), r0);
+            tmem_ld_32x32b_x32(t_row + (uint32_t)(c * 32 + 32), r1);
+            tmem_ld_wait();
+            if (g == g_hi - 1) release_acc(buf);
+            const int gn0 = n0 + c * 32;
+            const uint32_t sbuf = staging_addr + (uint32_t)((ew * nbw + box_buf(g)) * 4096);
+            if (CIN) {
+              if (!c_wait(box_buf(g))) { dead = true; break; }
+            } else {
+              wait_staging();
             }
-          };
-          pack_half(r0, 0);
-          pack_half(r1, 1);
-          fence_proxy_async_smem();
-          __syncwarp();
-          // (a block wholly past M or N -- the second tile of a pair on an odd
-          // tile-row count -- is not stored at all)
-          if (lane == 0 && m0 + q * 32 < p.M && gn0 < p.N) {
-            tma_store_3d(&tmC, gn0, m0 + q * 32, bz, sbuf);
-            bulk_commit();
+            // 16-byte chunk w (columns 8w .. 8w+7 of the 64) of this lane's row;
+            // r holds columns 32h .. 32h+31 (constant indices after unrolling)
+            auto pack_half = [&](const uint32_t (&r)[32], int h) {
+#pragma unroll
+              for (int ww = 0; ww < 4; ++ww) {
+                const int w = 4 * h + ww;
+                const uint32_t dst = sbuf + (uint32_t)(lane * 128 + ((w ^ (lane & 7)) * 16));
+                uint4 ci = make_uint4(0u, 0u, 0u, 0u);
+                if (CIN)
+                  asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                               : "=r"(ci.x), "=r"(ci.y), "=r"(ci.z), "=r"(ci.w)
+                               : "r"(dst)
+                               : "memory");
+                const typename Elem<T>::T2* ch = reinterpret_cast<const typename Elem<T>::T2*>(&ci);
+                uint4 o;
+                typename Elem<T>::T2* oh = reinterpret_cast<typename Elem<T>::T2*>(&o);
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                  float x0 = p.alpha * __uint_as_float(r[8 * ww + 2 * e]);
+                  float x1 = p.alpha * __uint_as_float(r[8 * ww + 2 * e + 1]);
+                  if (CIN) {
+                    const float2 cf = Elem<T>::unpack(ch[e]);
+                    x0 = __fmaf_rn(p.beta, cf.x, x0);
+                    x1 = __fmaf_rn(p.beta, cf.y, x1);
+                  }
+                  if (epi) {
+                    // (columns past N are clipped by the store; their bias is not read)
+                    const int col = gn0 + 8 * w + 2 * e;
+                    if (col < p.N) x0 = apply_epilogue<T>(x0, p.ep, col);
+                    if (col + 1 < p.N) x1 = apply_epilogue<T>(x1, p.ep, col + 1);
+                  }
+                  oh[e] = Elem<T>::pack(x0, x1);
+                }
+                asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(dst), "r"(o.x),
+                             "r"(o.y), "r"(o.z), "r"(o.w)
+                             : "memory");
+              }
+            };
+            pack_half(r0, 0);
+            pack_half(r1, 1);
+            fence_proxy_async_smem();
+            __syncwarp();
+            // (a block wholly past M or N -- the second tile of a pair on an odd
+            // tile-row count -- is not stored at all)
+            if (lane == 0 && c_rows && gn0 < p.N) {
+              tma_store_3d(&tmC, gn0, m0 + q * 32, bz, sbuf);
+              bulk_commit();
+            }
           }
-        }
+        };
+        if (c_in) boxes(std::true_type{});
+        else boxes(std::false_type{});
+        nb += i_hi - i_lo;
         continue;
       }
       // (2-SM pairs: the even block's MMAs write both blocks' tensor memory,
@@ -694,6 +840,15 @@ __global__ void __launch_bounds__(THREADS, 1)
           continue;
         }
         const int gn0 = n0 + c * 32;
+        if (!SPLIT && !p.c_vec_ok) {
+          // through this warp's first staging buffer (no TMA store uses the
+          // buffers in a launch that takes this path); the whole warp takes
+          // part, rows past M are skipped inside
+          if (m0 + q * 32 < p.M)
+            store_c32_staged<T>(p, bz, m0 + q * 32, gn0,
+                                staging_addr + (uint32_t)(ew * nbw * 4096), r, lane);
+          continue;
+        }
         // rows past M: loaded (warp-collective) but not stored
         if (gm >= p.M) continue;
         if constexpr (SPLIT) {
@@ -753,7 +908,14 @@ __global__ void __launch_bounds__(THREADS, 1)
         }
       }
     }
-    if (lane == 0) bulk_wait_all();  // C stores complete before the block ends
+    if (lane == 0) {
+      bulk_wait_all();  // C stores complete before the block ends
+      // (after an abort: C loads still in flight land before shared memory
+      // is released)
+      for (int lb = 0; lb < nbw; ++lb)
+        if ((cpend >> lb) & 1u)
+          mbar_wait_drain(cload_bar(ew * nbw + lb), (cph >> lb) & 1u, p.timeout_ns);
+    }
   }
 
   tc_fence_before();
@@ -959,7 +1121,7 @@ cudaError_t launch_hgemm_t(const HgemmArgs& a, LaunchCtx& ctx) {
   constexpr int VEC = 16 / (int)sizeof(T);  // elements per 16 bytes
   p.c_vec_ok = ((reinterpret_cast<uintptr_t>(a.C) & 15u) == 0 && (a.ldc % VEC) == 0 &&
                 (a.batch <= 1 || (a.stride_c % VEC) == 0)) ? 1 : 0;
-  p.c_tma = (p.c_vec_ok && a.beta == 0.f && a.splits <= 1 && a.c_tma &&
+  p.c_tma = (p.c_vec_ok && a.splits <= 1 && a.c_tma &&
              bn >= (sizeof(T) == 4 ? 32 : 64)) ? 1 : 0;
   p.pair = hgemm_use_pair(bn, a.M, p.splits, a.pair) ? a.pair : 0;
   p.dp_units = a.dp_units;

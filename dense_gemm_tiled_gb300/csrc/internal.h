@@ -62,7 +62,7 @@ struct HgemmArgs {
   int num_sms;
   int bn;               // tile width: 32, 64, 128, 192 or 256
   int pair;             // block pairs allowed: 0 none, 1 multicast B, 2 2-SM MMAs
-  int c_tma;            // allow TMA stores of C (used when beta == 0 and C is aligned)
+  int c_tma;            // allow TMA stores (and, beta != 0, TMA loads) of C when C is aligned
   int fault_injection;  // test hook: 1 = producer skips its first stage
   int dtype = 1;        // 1 fp16, 2 bf16, 3 fp32 on TF32 MMAs (gemm_dtype_t)
   // strided batch (batch > 1: no split, no tail): element pitches between
@@ -105,14 +105,18 @@ cudaError_t launch_scale(int dtype, int M, int N, void* C, int64_t ldc, float be
 // dst[c][r] = src[r][c] (fp32 rows x cols).
 cudaError_t launch_transpose_f32(int rows, int cols, const float* src, int64_t ld_src,
                                  float* dst, int64_t ld_dst, LaunchCtx& ctx);
-// dst[r][c] = src[r][c] for c < cols (32-bit elements; dst columns past cols
-// untouched).
+// dst[r][c] = src[r][c] for c < cols, 0 for cols <= c < ld_dst, into a dst
+// with 16-byte aligned rows (base 16-byte aligned, ld_dst a multiple of 4
+// elements for repack_32 or 8 for repack_16; else cudaErrorInvalidValue).
+// 32-bit or 16-bit elements (fp16 or bf16: +0 is the zero bit pattern in both).
 cudaError_t launch_repack_32(int rows, int cols, const void* src, int64_t ld_src, void* dst,
                              int64_t ld_dst, LaunchCtx& ctx);
-// dst[r][c] = src[r][c] for c < cols, 0 for cols <= c < ld_dst (16-bit elements,
-// fp16 or bf16: +0 is the zero bit pattern in both).
 cudaError_t launch_repack_16(int rows, int cols, const void* src, int64_t ld_src, void* dst,
                              int64_t ld_dst, LaunchCtx& ctx);
+// dst[r][c] = src[r][c] for c < cols, any alignment on either side (element
+// size 2 or 4 bytes): the way back from an aligned scratch copy of C.
+cudaError_t launch_copy_rows(int esize, int rows, int cols, const void* src, int64_t ld_src,
+                             void* dst, int64_t ld_dst, LaunchCtx& ctx);
 
 // Tile sizes the dispatcher needs.
 // fp32 block tile: (64 * SG_WARPS_M) x SG_BN, K step SG_BK, SG_BLOCKS_PER_SM

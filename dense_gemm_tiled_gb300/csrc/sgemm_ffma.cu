@@ -101,6 +101,7 @@ struct Params {
   float* sk_ws;
   unsigned int* sk_cnt;
   Epilogue ep;  // bias (fp32, per column) and activation, applied before the store
+  int c_vec;    // C rows (and batch entries) 16-byte aligned: float4 epilogue accesses
 };
 
 // Kernel kinds: one output tile per block (C), one K slice of a tile per
@@ -486,7 +487,7 @@ __global__ void __launch_bounds__(THREADS, GB300_SG_MIN_BLOCKS) sgemm_ffma_kerne
           }
         } else {
           float* dst = Cg + (int64_t)gm * p.ldc + gn;
-          const bool vec_ok = VEC && (gn + 3 < p.N);
+          const bool vec_ok = p.c_vec && (gn + 3 < p.N);
           const bool epi = p.ep.bias != nullptr || p.ep.act != 0;
           if (vec_ok) {
             float4 o;
@@ -573,12 +574,14 @@ cudaError_t launch_sgemm(const SgemmArgs& a, LaunchCtx& ctx) {
   p.stride_a = batch > 1 ? a.stride_a : 0;
   p.stride_b = batch > 1 ? a.stride_b : 0;
   p.stride_c = batch > 1 ? a.stride_c : 0;
-  // 16-byte staging needs 16-byte aligned rows in every operand and every
-  // batch entry (C too: the epilogue's float4 accesses share the flag).
-  const bool vec = ((reinterpret_cast<uintptr_t>(a.A) | reinterpret_cast<uintptr_t>(a.B) |
-                     reinterpret_cast<uintptr_t>(a.C)) & 15u) == 0 &&
-                   (a.lda % 4) == 0 && (a.ldb % 4) == 0 && (a.ldc % 4) == 0 &&
-                   (p.stride_a % 4) == 0 && (p.stride_b % 4) == 0 && (p.stride_c % 4) == 0;
+  // 16-byte staging needs 16-byte aligned rows in both operands and every
+  // batch entry; the epilogue's float4 accesses need the same of C.
+  const bool vec = ((reinterpret_cast<uintptr_t>(a.A) | reinterpret_cast<uintptr_t>(a.B)) &
+                    15u) == 0 &&
+                   (a.lda % 4) == 0 && (a.ldb % 4) == 0 && (p.stride_a % 4) == 0 &&
+                   (p.stride_b % 4) == 0;
+  p.c_vec = (reinterpret_cast<uintptr_t>(a.C) & 15u) == 0 && (a.ldc % 4) == 0 &&
+            (p.stride_c % 4) == 0;
   const bool split = a.splits > 1;
   const int tiles = p.tiles_m * p.tiles_n;
   int kind = split ? KIND_SPLIT : KIND_TILE;

@@ -31,6 +31,9 @@ for v in ("nn", "tn", "nt", "tt"):
     check_problem(p, exact=True)
     p = inputs.make_problem(300, 520, 264, tA, tB, "f16", "uniform", seed=601, beta=0.5)
     check_problem(p)
+    # odd N: C rows off 16-byte alignment
+    p = inputs.make_problem(300, 523, 264, tA, tB, "f16", "uniform", seed=604, beta=0.5)
+    check_problem(p)
     p = inputs.make_problem(1024, 768, 1000, tA, tB, "f16", "uniform", seed=602)
     check_problem(p)
     # 2048 x 3072 with 256-wide tiles: 96 pair units (192 single tiles) over
@@ -68,6 +71,10 @@ for v in ("nn", "tn", "nt", "tt"):
     assert r["path"] == "ffma", r
     p = inputs.make_problem(2048, 1408, 384, tA, tB, "f32", "integer", seed=611)
     r = check_problem(p, exact=True)
+    assert r["path"] == "ffma", r
+    # odd leading dimensions everywhere (rows off 16-byte alignment)
+    p = inputs.make_problem(1001, 2601, 621, tA, tB, "f32", "uniform", seed=612, beta=0.5)
+    r = check_problem(p)
     assert r["path"] == "ffma", r
 print("ok")
 """
