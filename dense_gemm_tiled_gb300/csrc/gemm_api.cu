@@ -164,6 +164,15 @@ int sg_pack_enabled() {
   return v;
 }
 
+// fp32 narrow tile for N <= 32 (env GEMM_GB300_SG_NARROW=0 turns it off).
+int sg_narrow_enabled() {
+  static const int v = [] {
+    const char* e = getenv("GEMM_GB300_SG_NARROW");
+    return e ? atoi(e) : 1;
+  }();
+  return v;
+}
+
 // fp16 block pairs (env GEMM_GB300_HG_PAIR): 0 off, 1 pairs sharing B tiles by
 // TMA multicast, 2 (default) pairs running 2-SM (cta_group::2) MMAs -- measured
 // on GB300 at 4096^3 and 8192^3: mode 2 +6..9 % over mode 1 (nn, nt).
@@ -364,11 +373,19 @@ int run_gemm(int transA, int transB, int64_t M64, int64_t N64, int64_t K64, int 
       if (e == cudaSuccess && c_scr) e = launch_copy_rows(4, M, N, Cd, ldc_p, C, ldc, ctx);
     }
   } else if (dtype == GEMM_F32) {
-    const int64_t tiles = (int64_t)((M + SG_BM - 1) / SG_BM) * ((N + SG_BN - 1) / SG_BN);
+    // N <= 32: the narrow tile (256 x 32, two blocks per SM), split over K
+    // until one round of resident blocks is full
+    const bool narrow = N <= SGN_BN && sg_narrow_enabled();
+    const int bm = narrow ? SGN_BM : SG_BM, bn = narrow ? SGN_BN : SG_BN;
+    const int64_t tiles = (int64_t)((M + bm - 1) / bm) * ((N + bn - 1) / bn);
     int splits, k_slice;
-    plan_splits(tiles, K, SG_BK, 2 * sms, 4, 16, &splits, &k_slice);
+    if (narrow)
+      plan_splits(tiles, K, SGN_BK, sms * SGN_BLOCKS_PER_SM, 8, 16, &splits, &k_slice);
+    else
+      plan_splits(tiles, K, SG_BK, 2 * sms, 4, 16, &splits, &k_slice);
     SgemmArgs a{transA, transB, M, N, K, (const float*)A, lda, (const float*)B, ldb, (float*)C,
                 ldc, alpha, beta, splits, k_slice, nullptr};
+    a.narrow = narrow ? 1 : 0;
     if (splits == 1) a.ep = ep;  // split-K: the reduction applies it
     // Packing: the kernel reads A stored [K,M] and B stored [K,N] fastest
     // (measured at 4096^3: tn 56.4 TF/s, nn 53.7, nt 46.9), so on large
@@ -377,12 +394,18 @@ int run_gemm(int transA, int transB, int64_t M64, int64_t N64, int64_t K64, int 
     // An operand whose rows are not 16-byte aligned is read with 4-byte
     // copies (measured 4095^3: 42 TF/s); on large problems it is copied into
     // a padded row pitch first, so the kernel takes 16-byte copies throughout.
-    const bool big = splits == 1 && sg_pack_enabled() && (double)M * N * K >= (double)(1ll << 30);
+    // (The narrow tile streams A once with no reuse across tile columns, so
+    // transposing A would double its traffic: only a misaligned operand is
+    // copied there, and it splits over K, so the test is on the problem size.)
+    const bool big = (splits == 1 || narrow) && sg_pack_enabled() &&
+                     (double)M * N * K >= (double)(1ll << 30);
     auto misaligned = [](const void* p, int64_t ld) { return ((uintptr_t)p % 16) != 0 || ld % 4 != 0; };
-    const bool packA = big && (!transA || misaligned(A, lda));
+    const bool packA = big && ((!transA && !narrow) || misaligned(A, lda));
     const bool packB = big && (transB || misaligned(B, ldb));
-    const int64_t ldA_p = (M + 3) / 4 * 4, ldB_p = (N + 3) / 4 * 4;
-    const size_t bytes_A = packA ? ((size_t)K * ldA_p * 4 + 255) / 256 * 256 : 0;
+    const int64_t ldA_p = (M + 3) / 4 * 4, ldB_p = (N + 3) / 4 * 4, ldK_p = (K + 3) / 4 * 4;
+    const bool a_rows = narrow && !transA;  // A copied as [M,K] rows, not transposed
+    const size_t bytes_A =
+        packA ? ((size_t)(a_rows ? M * ldK_p : K * ldA_p) * 4 + 255) / 256 * 256 : 0;
     const size_t bytes_B = packB ? ((size_t)K * ldB_p * 4 + 255) / 256 * 256 : 0;
     const size_t bytes_P = splits > 1 ? (size_t)splits * M * N * sizeof(float) : 0;
     // Stream-K: without a split, a tile count that is not a whole number of
@@ -390,7 +413,7 @@ int run_gemm(int transA, int transB, int64_t M64, int64_t N64, int64_t K64, int 
     // 6.7 rounds of 152).  The persistent launch gives whole tiles to all but
     // the last one to two rounds and shares those rounds' K steps evenly.
     const int64_t G = (int64_t)sms * SG_BLOCKS_PER_SM;  // resident blocks
-    const bool sk = splits == 1 && sg_sk_enabled() && tiles >= G && tiles % G != 0;
+    const bool sk = splits == 1 && !narrow && sg_sk_enabled() && tiles >= G && tiles % G != 0;
     const int64_t sk_tiles = sk ? (tiles >= 2 * G ? tiles % G + G : tiles) : 0;
     const size_t bytes_S = sk ? (size_t)G * 2 * SG_BM * SG_BN * sizeof(float) : 0;
     const size_t bytes_N = sk ? ((size_t)sk_tiles * sizeof(unsigned int) + 255) / 256 * 256 : 0;
@@ -407,7 +430,11 @@ int run_gemm(int transA, int transB, int64_t M64, int64_t N64, int64_t K64, int 
       e = cudaMemsetAsync(a.sk_cnt, 0, (size_t)sk_tiles * sizeof(unsigned int), stream);
       if (e != cudaSuccess) return cuda_fail(e);
     }
-    if (packA) {  // A [M,K] -> [K,M], or A [K,M] into an aligned pitch
+    if (packA && a_rows) {  // A [M,K] into an aligned pitch
+      float* At = (float*)ws.ptr;
+      e = launch_repack_32(M, K, A, lda, At, ldK_p, ctx);
+      a.A = At; a.lda = ldK_p;
+    } else if (packA) {  // A [M,K] -> [K,M], or A [K,M] into an aligned pitch
       float* At = (float*)ws.ptr;
       e = transA ? launch_repack_32(K, M, A, lda, At, ldA_p, ctx)
                  : launch_transpose_f32(M, K, (const float*)A, lda, At, ldA_p, ctx);
@@ -724,6 +751,7 @@ int run_batched(int transA, int transB, int64_t M64, int64_t N64, int64_t K64, i
                   alpha, beta, 1, K, nullptr};
       a.batch = nb;
       a.stride_a = sA; a.stride_b = sB; a.stride_c = sC;
+      a.narrow = N <= SGN_BN && sg_narrow_enabled() ? 1 : 0;
       e = timed_sgemm(a, ctx);
     }
   }

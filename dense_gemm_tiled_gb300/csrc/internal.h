@@ -42,6 +42,9 @@ struct SgemmArgs {
   int sk_blocks = 0;
   float* sk_ws = nullptr;
   unsigned int* sk_cnt = nullptr;
+  // block tile: 0 the general SG_BM x SG_BN tile, 1 the narrow SGN_BM x SGN_BN
+  // tile for N <= SGN_BN (no stream-K launch)
+  int narrow = 0;
   Epilogue ep;  // fused bias / activation (not with splits > 1: the reduction applies it)
 };
 
@@ -91,6 +94,7 @@ struct LaunchCtx {
 
 // Launchers (return cudaSuccess or the launch error).
 cudaError_t launch_sgemm(const SgemmArgs& a, LaunchCtx& ctx);
+cudaError_t launch_sgemm_narrow(const SgemmArgs& a, LaunchCtx& ctx);  // a.narrow tiles
 cudaError_t launch_hgemm(const HgemmArgs& a, LaunchCtx& ctx);
 cudaError_t launch_hgemm_bf16(const HgemmArgs& a, LaunchCtx& ctx);
 // fp32 operands and output on kind::tf32 MMAs (HgemmArgs.dtype 3; K-major A and B)
@@ -136,6 +140,19 @@ constexpr int SG_WARPS_M = GB300_SG_WARPS_M;
 #endif
 constexpr int SG_BM = 64 * SG_WARPS_M, SG_BN = GB300_SG_BN, SG_BK = GB300_SG_BK;
 constexpr int SG_BLOCKS_PER_SM = GB300_SG_MIN_BLOCKS;
+// fp32 narrow tile for N <= 32: a 128 x 128 tile would leave 3/4 of its
+// columns idle (the rank-32 output of a LoRA projection, M=8192 N=32 K=8192)
+#ifndef GB300_SGN_WARPS_M
+#define GB300_SGN_WARPS_M 4
+#endif
+#ifndef GB300_SGN_BK
+#define GB300_SGN_BK 32
+#endif
+#ifndef GB300_SGN_MIN_BLOCKS
+#define GB300_SGN_MIN_BLOCKS 2
+#endif
+constexpr int SGN_BM = 64 * GB300_SGN_WARPS_M, SGN_BN = 32, SGN_BK = GB300_SGN_BK;
+constexpr int SGN_BLOCKS_PER_SM = GB300_SGN_MIN_BLOCKS;
 constexpr int HG_BM = 128, HG_BK = 64;
 int hgemm_pick_bn(int M, int N, int transB, int num_sms, int batch = 1);
 bool hgemm_use_pair(int bn, int M, int splits, int allowed);

@@ -1,614 +1,11 @@
-// FP32 SGEMM on the CUDA cores: C = alpha * op(A) * op(B) + beta * C.
-//
-// What the pages contribute (design ideas, not code):
-//  - "Optimizing GEMM on Apple's M5 from scratch, Part 1": shared-memory
-//    tiling ("Kernels 2 and 3: Shared Memory Tiling": every input tile is
-//    loaded once per block and reused by all its threads) and thread
-//    coarsening ("Kernel 4: 1D Thread Coarsening": one thread owns several
-//    outputs so an operand value held in a register feeds several FMAs).  Here
-//    the coarsening is two-dimensional, an 8 x 8 register block per thread, the
-//    register blocking of "From a C loop to a GPU kernel" ("One thread, four
-//    outputs", 2x2 there, with 4x4 and 8x8 named as the next steps).
-//  - "From a C loop to a GPU kernel", "The bubble between tiles": the next K
-//    tile is fetched while the current one is consumed.  Here a 3-stage
-//    cp.async ring.
-//  - "Metal GEMM Kernels for LoRA Training", section 3: the transposed
-//    operand cost instruction count, not memory traffic.  Here no operand is
-//    transposed in memory at all: each operand is staged in the orientation it
-//    is stored in, and the inner loop reads it with 128-bit shared loads along
-//    whichever dimension is contiguous (k for A[M,K] / B[N,K]; m or n for
-//    A[K,M] / B[K,N]).
-//  - "Part 1", "Kernel 1: Naive Implementation" (and "Coalescing" in the C-loop
-//    post): consecutive threads own consecutive columns, so global loads are
-//    coalesced; here every global load is a 16-byte cp.async and a warp's loads
-//    cover whole 64- or 512-byte row segments.
-//
-// Tile: (64 * WARPS_M) x 128 outputs per block, K step 64, 128 * WARPS_M threads
-// (warps WARPS_M x 4, each warp 64 x 32, each lane 8 x 8 outputs split into
-// 4-wide groups), one block per SM.  The inner product runs on Blackwell's
-// paired FP32 FMA (fma.rn.f32x2): one instruction updates two adjacent outputs
-// of a lane, halving the issue slots the FMAs take (the scalar-FMA version of
-// this kernel was bound by instruction issue).  Each half of the pair is an
-// IEEE fp32 FMA (round to nearest even); no fast-math, denormals kept.
-#include <cuda_runtime.h>
-#include <stdint.h>
-
-#include "common.cuh"
-#include "internal.h"
+// FP32 SGEMM on the CUDA cores, general tile (the kernel is in sgemm_ffma.cuh).
+#include "sgemm_ffma.cuh"
 
 namespace gb300 {
-namespace {
-
-constexpr int BM = SG_BM, BN = SG_BN, BK = SG_BK;
-constexpr int WARPS_M = SG_WARPS_M;  // warps along m (each 64 rows)
-constexpr int WARPS_N = BN / 32;     // warps along n (each 32 columns)
-constexpr int THREADS = 32 * WARPS_M * WARPS_N;
-#ifndef GB300_SG_STAGES
-#define GB300_SG_STAGES 3
-#endif
-constexpr int STAGES = GB300_SG_STAGES;
-constexpr int APAD = BM + 4;  // k-major tile rows padded: conflict-free transposing writes
-constexpr int BPAD = BN + 4;
-constexpr int A_FLOATS = (BM * BK > BK * APAD) ? BM * BK : BK * APAD;
-constexpr int B_FLOATS = BK * BPAD;
-constexpr int STAGE_FLOATS = A_FLOATS + B_FLOATS;
-constexpr int SMEM_BYTES = STAGES * STAGE_FLOATS * 4;  // 195 KiB at BK 64, 3 stages
-// Tile rasterisation: blocks walk GROUP tile-rows column by column, so each B
-// panel is fetched from DRAM once per group while the group's A panels stay in
-// L2.  The host picks GROUP so those A panels take about a quarter of L2
-// (32 MB): measured at 4096^3, 8-row groups read 352 MB from DRAM and 32-row
-// groups (64 MB of A panels) 520 MB -- the L2 is split between the two dies.
-constexpr int64_t RASTER_L2_BYTES = 32ll << 20;
-static_assert(BM == 64 * WARPS_M && (BN == 64 || BN == 128) &&
-                  (BK == 16 || BK == 32 || BK == 64),
-              "tile shape");
-
-// Compile-time tuning knobs (measured on GB300 at 4096^3; the defaults won;
-// K step and stage count are GB300_SG_BK in internal.h and GB300_SG_STAGES:
-// 64 x 3 beat 32 x 3, 32 x 4, 64 x 2 and 16 x 6 by 0.4-5 %; 128 x 64 tiles
-// at two blocks per SM (GB300_SG_BN=64, GB300_SG_MIN_BLOCKS=2) were 1-3 %
-// slower; loading the next K step's fragments into a second register set
-// gained nothing):
-//  GB300_SG_MIN_BLOCKS  blocks per SM the register budget is sized for
-//  GB300_SG_KC_UNROLL   unrolling of the 4-k chunk loop
-#ifndef GB300_SG_KC_UNROLL
-#define GB300_SG_KC_UNROLL 8
-#endif
-constexpr int KC_UNROLL = GB300_SG_KC_UNROLL;
-
-struct Params {
-  const float* A;
-  const float* B;
-  float* C;
-  float* partial;
-  int64_t lda, ldb, ldc;
-  int M, N, K;
-  int k_slice;
-  int tiles_m, tiles_n;
-  int group_m;  // tile-rows per rasterisation group
-  float alpha, beta;
-  // strided batch: blockIdx.y selects matrices A + y*stride_a, B + y*stride_b,
-  // C + y*stride_c (all zero for a single GEMM)
-  int64_t stride_a, stride_b, stride_c;
-  // persistent launches (KIND_PERSIST): gridDim.x blocks first take whole
-  // tiles t = blockIdx.x + i * gridDim.x below dp_tiles, then share the
-  // remaining tiles' K steps evenly (block b owns steps [b*I/G, (b+1)*I/G) of
-  // the I = sk_iters steps, G = gridDim.x, tiles in order, kiters steps
-  // each).  A tile cut between blocks is finished by the last block to
-  // arrive: partials in sk_ws[block][slot], arrivals counted in sk_cnt.
-  int dp_tiles, kiters;
-  int64_t sk_iters;
-  float* sk_ws;
-  unsigned int* sk_cnt;
-  Epilogue ep;  // bias (fp32, per column) and activation, applied before the store
-  int c_vec;    // C rows (and batch entries) 16-byte aligned: float4 epilogue accesses
-};
-
-// Kernel kinds: one output tile per block (C), one K slice of a tile per
-// block (raw partials, reduced by a second kernel), or persistent blocks over
-// whole tiles and then shared K steps (C, with in-kernel fix-up).
-constexpr int KIND_TILE = 0, KIND_SPLIT = 1, KIND_PERSIST = 2;
-
-// ---------------------------------------------------------------- staging
-// Tile layouts per operand and stage:
-//  "k-major" tile : 32 rows (k) x BM or BN (m or n), rows padded by 4 floats.
-//                   An operand stored with m/n contiguous (A[K,M], B[K,N]) is
-//                   copied row by row with 16-byte copies.  B stored [N,K] is
-//                   transposed into it on the way in with 4-byte copies -- the
-//                   transposing write of "Metal GEMM Kernels for LoRA Training",
-//                   section 3, done by the async-copy unit: a warp reads 4 rows
-//                   x 32 bytes of global memory and, thanks to the padding,
-//                   writes 32 distinct banks.  B must be k-major because the
-//                   paired FMA needs column pairs (n, n+1) in adjacent registers.
-//  "row" tile     : BM rows (m) x 32 k, 128-byte rows whose eight 16-byte chunks
-//                   are permuted by chunk ^ ((row >> 2) & 7) so that the lanes
-//                   reading the same k of rows r and r+4 hit distinct banks;
-//                   A stored [M,K] stays in this layout (measured faster than
-//                   transposing it, by copies or through registers).
-// chunk permutation within a row tile row (BK/4 chunks): XOR with (row / 4)
-// modulo the chunk count, at most 8
-constexpr int SWZ_MASK = (BK / 4 < 8 ? BK / 4 : 8) - 1;
-__device__ __forceinline__ int a_swz(int row, int chunk) { return chunk ^ ((row >> 2) & SWZ_MASK); }
-
-// source [R rows][K] (k contiguous) -> row tile of BM rows
-template <bool VEC>
-__device__ __forceinline__ void load_rows(uint32_t dst, const float* __restrict__ g, int64_t ld,
-                                          int r0, int R, int k0, int K, int tid) {
-  if constexpr (VEC) {
-    constexpr int CPR = BK / 4;  // 16-byte chunks per row
-    constexpr int CHUNKS = BM * CPR;
-#pragma unroll
-    for (int it = 0; it < (CHUNKS + THREADS - 1) / THREADS; ++it) {
-      const int q = tid + it * THREADS;
-      if (CHUNKS % THREADS != 0 && q >= CHUNKS) break;
-      const int row = q / CPR, c = q % CPR;
-      const int gr = r0 + row, gk = k0 + c * 4;
-      const bool ok = (gr < R) && (gk < K);
-      const uint32_t bytes = ok ? (uint32_t)min(4, K - gk) * 4u : 0u;
-      const float* src = ok ? g + (int64_t)gr * ld + gk : g;
-      cp_async_16(dst + (uint32_t)(row * BK + a_swz(row, c) * 4) * 4u, src, bytes);
-    }
-  } else {
-    constexpr int ELEMS = BM * BK;
-#pragma unroll 4
-    for (int it = 0; it < (ELEMS + THREADS - 1) / THREADS; ++it) {
-      const int e = tid + it * THREADS;
-      if (ELEMS % THREADS != 0 && e >= ELEMS) break;
-      const int row = e / BK, kk = e % BK;
-      const int gr = r0 + row, gk = k0 + kk;
-      const bool ok = (gr < R) && (gk < K);
-      const float* src = ok ? g + (int64_t)gr * ld + gk : g;
-      const int col = a_swz(row, kk >> 2) * 4 + (kk & 3);
-      cp_async_4(dst + (uint32_t)(row * BK + col) * 4u, src, ok ? 4u : 0u);
-    }
-  }
-}
-
-// source [K][R] (m/n contiguous) -> k-major tile of W columns, row pitch PITCH
-template <bool VEC, int W, int PITCH>
-__device__ __forceinline__ void load_kmajor(uint32_t dst, const float* __restrict__ g, int64_t ld,
-                                            int r0, int R, int k0, int K, int tid) {
-  if constexpr (VEC) {
-    constexpr int CPR = W / 4;  // 16-byte chunks per k row
-    constexpr int CHUNKS = BK * CPR;
-#pragma unroll
-    for (int it = 0; it < (CHUNKS + THREADS - 1) / THREADS; ++it) {
-      const int q = tid + it * THREADS;
-      if (CHUNKS % THREADS != 0 && q >= CHUNKS) break;
-      const int krow = q / CPR, c = q - krow * CPR;
-      const int gk = k0 + krow, gr = r0 + c * 4;
-      const bool ok = (gk < K) && (gr < R);
-      const uint32_t bytes = ok ? (uint32_t)min(4, R - gr) * 4u : 0u;
-      const float* src = ok ? g + (int64_t)gk * ld + gr : g;
-      cp_async_16(dst + (uint32_t)(krow * PITCH + c * 4) * 4u, src, bytes);
-    }
-  } else {
-    constexpr int ELEMS = BK * W;
-#pragma unroll 4
-    for (int it = 0; it < (ELEMS + THREADS - 1) / THREADS; ++it) {
-      const int e = tid + it * THREADS;
-      if (ELEMS % THREADS != 0 && e >= ELEMS) break;
-      const int krow = e / W, rr = e - krow * W;
-      const int gk = k0 + krow, gr = r0 + rr;
-      const bool ok = (gk < K) && (gr < R);
-      const float* src = ok ? g + (int64_t)gk * ld + gr : g;
-      cp_async_4(dst + (uint32_t)(krow * PITCH + rr) * 4u, src, ok ? 4u : 0u);
-    }
-  }
-}
-
-// source [R rows][K] (k contiguous) -> k-major tile of W columns, transposed by
-// 4-byte copies: lane l reads k = l & 7 of row (l >> 3) of a 4-row group
-template <int W, int PITCH>
-__device__ __forceinline__ void load_transpose(uint32_t dst, const float* __restrict__ g,
-                                               int64_t ld, int r0, int R, int k0, int K,
-                                               int tid) {
-  const int warp = tid >> 5, lane = tid & 31;
-  const int kl = lane & 7, rl = lane >> 3;
-  constexpr int GROUPS = (W / 4) * (BK / 8);  // 4-row x 8-k groups
-  constexpr int WARPS = THREADS / 32;
-#pragma unroll 4
-  for (int it = 0; it < (GROUPS + WARPS - 1) / WARPS; ++it) {
-    const int grp = warp + it * WARPS;
-    if (GROUPS % WARPS != 0 && grp >= GROUPS) break;
-    const int rg = grp % (W / 4), kg = grp / (W / 4);
-    const int row = rg * 4 + rl, k = kg * 8 + kl;
-    const int gr = r0 + row, gk = k0 + k;
-    const bool ok = (gr < R) && (gk < K);
-    const float* src = ok ? g + (int64_t)gr * ld + gk : g;
-    cp_async_4(dst + (uint32_t)(k * PITCH + row) * 4u, src, ok ? 4u : 0u);
-  }
-}
-
-// ---------------------------------------------------------------- paired FMA
-// fma.rn.f32x2: two IEEE fp32 fused multiply-adds (round to nearest even) in
-// one instruction on a pair of registers; each half is exactly an fp32 FMA,
-// so results keep fp32 semantics.
-__device__ __forceinline__ uint64_t ffma2(uint64_t a, uint64_t b, uint64_t c) {
-  uint64_t d;
-  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
-  return d;
-}
-__device__ __forceinline__ uint64_t splat2(float x) {
-  uint64_t r;
-  asm("mov.b64 %0, {%1, %1};" : "=l"(r) : "f"(x));
-  return r;
-}
-__device__ __forceinline__ uint64_t pack2(float x, float y) {
-  uint64_t r;
-  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(x), "f"(y));
-  return r;
-}
-__device__ __forceinline__ float2 unpack2(uint64_t v) {
-  float2 f;
-  asm("mov.b64 {%0, %1}, %2;" : "=f"(f.x), "=f"(f.y) : "l"(v));
-  return f;
-}
-
-__device__ __forceinline__ float4 lds128(const float* p) {
-  return *reinterpret_cast<const float4*>(p);
-}
-
-// Stream-K bookkeeping: the block whose step range contains step x, and the
-// first step of block b (G blocks over I steps).
-__device__ __forceinline__ int sk_owner(int64_t x, int G, int64_t I) {
-  return (int)(((x + 1) * G - 1) / I);
-}
-__device__ __forceinline__ int64_t sk_start(int b, int G, int64_t I) { return (int64_t)b * I / G; }
-
-template <bool A_K, bool B_K, bool VEC, int KIND>
-__global__ void __launch_bounds__(THREADS, GB300_SG_MIN_BLOCKS) sgemm_ffma_kernel(const Params p) {
-  extern __shared__ __align__(16) float smem[];
-  __shared__ int s_last;
-  const int tid = threadIdx.x;
-  const int warp = tid >> 5, lane = tid & 31;
-  const int wm = (warp / WARPS_N) * 64;  // warp's first row in the tile
-  const int wn = (warp % WARPS_N) * 32;  // warp's first column
-  const int ty = lane >> 2, tx = lane & 3;
-  const int arow = wm + ty * 4;     // lane rows: arow + {0..3}, arow + 32 + {0..3}
-  const int bcol = wn + tx * 4;     // lane cols: bcol + {0..3}, bcol + 16 + {0..3}
-  const int aswz = (arow >> 2) & SWZ_MASK;  // row-tile chunk permutation, same for all 8 lane rows
-
-  const float* const Ag = p.A + (int64_t)blockIdx.y * p.stride_a;
-  const float* const Bg = p.B + (int64_t)blockIdx.y * p.stride_b;
-  float* const Cg = p.C + (int64_t)blockIdx.y * p.stride_c;
-  const uint32_t sbase = smem_u32(smem);
-
-  // work state: non-persistent blocks do one item; persistent blocks walk
-  // their whole tiles, then their stream-K step range
-  const int G = gridDim.x;
-  int dp_next = blockIdx.x;
-  int64_t sk_it = 0, sk_end = 0, sk_first = 0;
-  if constexpr (KIND == KIND_PERSIST) {
-    sk_first = sk_it = sk_start(blockIdx.x, G, p.sk_iters);
-    sk_end = sk_start(blockIdx.x + 1, G, p.sk_iters);
-  }
-  bool first_item = true;
-
-  // acc[i][jp] holds the outputs (row i, columns 2jp and 2jp+1) as a pair
-  uint64_t acc[8][4];
-
-  for (;;) {
-    // ---- next work item: tile t, K range [kbeg, kend)
-    int t, kbeg, kend;
-    int64_t seg0 = 0;  // stream-K: first step of this segment
-    bool whole = true;
-    if constexpr (KIND != KIND_PERSIST) {
-      if (!first_item) break;
-      t = blockIdx.x;
-      kbeg = blockIdx.z * p.k_slice;
-      kend = min(p.K, kbeg + p.k_slice);
-    } else {
-      if (dp_next < p.dp_tiles) {
-        t = dp_next;
-        dp_next += G;
-        kbeg = 0;
-        kend = p.K;
-      } else if (sk_it < sk_end) {
-        const int64_t ts = sk_it / p.kiters;
-        const int s0 = (int)(sk_it - ts * p.kiters);
-        const int64_t left = sk_end - sk_it;
-        const int s1 = left < (int64_t)(p.kiters - s0) ? s0 + (int)left : p.kiters;
-        t = p.dp_tiles + (int)ts;
-        seg0 = sk_it;
-        sk_it += s1 - s0;
-        kbeg = s0 * BK;
-        kend = min(p.K, s1 * BK);
-        whole = s0 == 0 && s1 == p.kiters;
-      } else {
-        break;
-      }
-    }
-    first_item = false;
-
-    // grouped rasterisation of the tile grid (consecutive tiles share B panels
-    // within a group of group_m tile-rows)
-    const int per_group = p.group_m * p.tiles_n;
-    const int first_m = (t / per_group) * p.group_m;
-    const int gsize = min(p.tiles_m - first_m, p.group_m);
-    const int tm = first_m + (t % per_group) % gsize;
-    const int tn = (t % per_group) / gsize;
-    const int m0 = tm * BM, n0 = tn * BN;
-    const int nk = (kend - kbeg + BK - 1) / BK;
-
-    auto stage_load = [&](int s, int k0) {
-      const uint32_t st = sbase + (uint32_t)(s * STAGE_FLOATS) * 4u;
-      if constexpr (A_K) load_rows<VEC>(st, Ag, p.lda, m0, p.M, k0, kend, tid);
-      else load_kmajor<VEC, BM, APAD>(st, Ag, p.lda, m0, p.M, k0, kend, tid);
-      const uint32_t sb = st + A_FLOATS * 4u;
-      if constexpr (B_K) load_transpose<BN, BPAD>(sb, Bg, p.ldb, n0, p.N, k0, kend, tid);
-      else load_kmajor<VEC, BN, BPAD>(sb, Bg, p.ldb, n0, p.N, k0, kend, tid);
-    };
-
-#pragma unroll
-    for (int i = 0; i < 8; ++i)
-#pragma unroll
-      for (int j = 0; j < 4; ++j) acc[i][j] = 0ull;
-
-    if constexpr (KIND == KIND_PERSIST) __syncthreads();  // the previous item's stages are free
-#pragma unroll
-    for (int s = 0; s < STAGES - 1; ++s) {
-      if (s < nk) stage_load(s, kbeg + s * BK);
-      cp_async_commit();
-    }
-
-    for (int kt = 0; kt < nk; ++kt) {
-      cp_async_wait<STAGES - 2>();
-      __syncthreads();  // stage kt visible to all; stage kt-1 fully consumed
-      {
-        const int nxt = kt + STAGES - 1;
-        if (nxt < nk) stage_load(nxt % STAGES, kbeg + nxt * BK);
-        cp_async_commit();
-      }
-      const float* As = smem + (kt % STAGES) * STAGE_FLOATS;
-      const float* Bs = As + A_FLOATS;
-#pragma unroll KC_UNROLL
-      for (int kc = 0; kc < BK / 4; ++kc) {
-        float a[8][4];  // a[i][kk]: row i, k = 4kc + kk (row-tile A)
-#pragma unroll
-        for (int kk = 0; kk < 4; ++kk) {
-          const int k = kc * 4 + kk;
-          float av[8];
-          if constexpr (A_K) {
-            // two k at a time (64-bit loads) keeps 16 rather than 32 A values live
-            if ((kk & 1) == 0) {
-              const float* base = As + arow * BK + ((kc ^ aswz) * 4) + kk;
-#pragma unroll
-              for (int i = 0; i < 8; ++i) {
-                const float2 v =
-                    *reinterpret_cast<const float2*>(base + (i < 4 ? i : 32 + i - 4) * BK);
-                a[i][kk] = v.x; a[i][kk + 1] = v.y;
-              }
-            }
-#pragma unroll
-            for (int i = 0; i < 8; ++i) av[i] = a[i][kk];
-          } else {
-            const float4 lo = lds128(As + k * APAD + arow);
-            const float4 hi = lds128(As + k * APAD + arow + 32);
-            av[0] = lo.x; av[1] = lo.y; av[2] = lo.z; av[3] = lo.w;
-            av[4] = hi.x; av[5] = hi.y; av[6] = hi.z; av[7] = hi.w;
-          }
-          const float* brow = Bs + k * BPAD + bcol;
-          const ulonglong2 b01 = *reinterpret_cast<const ulonglong2*>(brow);
-          const ulonglong2 b23 = *reinterpret_cast<const ulonglong2*>(brow + 16);
-          const uint64_t bp[4] = {b01.x, b01.y, b23.x, b23.y};
-          // All eight (a, a) pairs first, then column pair by column pair, the
-          // rows alternating between the two 4-row halves: the eight paired
-          // FMAs sharing bp[j] follow each other and none waits on the register
-          // move that builds its splatted operand.  Measured at 4096^3 against
-          // row by row (i outer, j inner): +5 %; rows in order 0..7: -0.1 %;
-          // other interleavings: -0.5 to -2.6 %.
-          uint64_t ap[8];
-#pragma unroll
-          for (int i = 0; i < 8; ++i) ap[i] = splat2(av[i]);
-          constexpr int ORD[8] = {0, 4, 1, 5, 2, 6, 3, 7};
-#pragma unroll
-          for (int j = 0; j < 4; ++j)
-#pragma unroll
-            for (int ii = 0; ii < 8; ++ii) acc[ORD[ii]][j] = ffma2(ap[ORD[ii]], bp[j], acc[ORD[ii]][j]);
-        }
-      }
-    }
-    cp_async_wait<0>();
-
-    if constexpr (KIND == KIND_PERSIST) {
-      if (!whole) {
-        // A tile shared between blocks.  Every contributor stores its partial
-        // sums (warp-coalesced: float4 j of thread tid at [j][tid]) in its
-        // slot -- 0 for the segment a block starts with, 1 for the one it
-        // ends with -- then counts itself in.  The last to arrive adds all
-        // segments in K order (so the result does not depend on arrival
-        // order) and stores the tile.
-        const int slot = seg0 == sk_first ? 0 : 1;
-        float4* mine = reinterpret_cast<float4*>(p.sk_ws) +
-                       (int64_t)(blockIdx.x * 2 + slot) * (BM * BN / 4);
-#pragma unroll
-        for (int i = 0; i < 8; ++i)
-#pragma unroll
-          for (int h = 0; h < 2; ++h) {
-            const float2 lo = unpack2(acc[i][2 * h]), hi = unpack2(acc[i][2 * h + 1]);
-            mine[(i * 2 + h) * THREADS + tid] = make_float4(lo.x, lo.y, hi.x, hi.y);
-          }
-        __threadfence();
-        __syncthreads();
-        const int64_t x0 = (int64_t)(t - p.dp_tiles) * p.kiters;
-        const int c_lo = sk_owner(x0, G, p.sk_iters);
-        const int c_hi = sk_owner(x0 + p.kiters - 1, G, p.sk_iters);
-        if (tid == 0) {
-          const unsigned int before = atomicAdd(p.sk_cnt + (t - p.dp_tiles), 1u);
-          s_last = before == (unsigned int)(c_hi - c_lo);
-        }
-        __syncthreads();
-        if (!s_last) continue;
-        __threadfence();
-        float sum[8][4][2];
-#pragma unroll
-        for (int i = 0; i < 8; ++i)
-#pragma unroll
-          for (int j = 0; j < 4; ++j) sum[i][j][0] = sum[i][j][1] = 0.f;
-        for (int c = c_lo; c <= c_hi; ++c) {
-          const int cs = sk_start(c, G, p.sk_iters) >= x0 ? 0 : 1;
-          const float4* part = reinterpret_cast<const float4*>(p.sk_ws) +
-                               (int64_t)(c * 2 + cs) * (BM * BN / 4);
-#pragma unroll
-          for (int i = 0; i < 8; ++i)
-#pragma unroll
-            for (int h = 0; h < 2; ++h) {
-              const float4 v = __ldcg(part + (i * 2 + h) * THREADS + tid);
-              sum[i][2 * h][0] += v.x; sum[i][2 * h][1] += v.y;
-              sum[i][2 * h + 1][0] += v.z; sum[i][2 * h + 1][1] += v.w;
-            }
-        }
-#pragma unroll
-        for (int i = 0; i < 8; ++i)
-#pragma unroll
-          for (int j = 0; j < 4; ++j) acc[i][j] = pack2(sum[i][j][0], sum[i][j][1]);
-      }
-    }
-
-    // epilogue: lane columns bcol + {0..3} (pairs 0, 1) and bcol + 16 + {0..3} (pairs 2, 3)
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      const int gm = m0 + arow + (i < 4 ? i : 32 + i - 4);
-      if (gm >= p.M) continue;
-#pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        const int gn = n0 + bcol + h * 16;
-        const float2 lo = unpack2(acc[i][2 * h]), hi = unpack2(acc[i][2 * h + 1]);
-        const float v[4] = {lo.x, lo.y, hi.x, hi.y};
-        if constexpr (KIND == KIND_SPLIT) {
-          float* dst = p.partial + ((int64_t)blockIdx.z * p.M + gm) * p.N + gn;
-          if (gn + 3 < p.N && (p.N & 3) == 0) {
-            *reinterpret_cast<float4*>(dst) = make_float4(v[0], v[1], v[2], v[3]);
-          } else {
-#pragma unroll
-            for (int j = 0; j < 4; ++j)
-              if (gn + j < p.N) dst[j] = v[j];
-          }
-        } else {
-          float* dst = Cg + (int64_t)gm * p.ldc + gn;
-          const bool vec_ok = p.c_vec && (gn + 3 < p.N);
-          const bool epi = p.ep.bias != nullptr || p.ep.act != 0;
-          if (vec_ok) {
-            float4 o;
-            if (p.beta != 0.f) {
-              const float4 c = *reinterpret_cast<const float4*>(dst);
-              o = make_float4(__fmaf_rn(p.alpha, v[0], p.beta * c.x),
-                              __fmaf_rn(p.alpha, v[1], p.beta * c.y),
-                              __fmaf_rn(p.alpha, v[2], p.beta * c.z),
-                              __fmaf_rn(p.alpha, v[3], p.beta * c.w));
-            } else {
-              o = make_float4(p.alpha * v[0], p.alpha * v[1], p.alpha * v[2], p.alpha * v[3]);
-            }
-            if (epi) {
-              o.x = apply_epilogue<float>(o.x, p.ep, gn);
-              o.y = apply_epilogue<float>(o.y, p.ep, gn + 1);
-              o.z = apply_epilogue<float>(o.z, p.ep, gn + 2);
-              o.w = apply_epilogue<float>(o.w, p.ep, gn + 3);
-            }
-            *reinterpret_cast<float4*>(dst) = o;
-          } else {
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-              if (gn + j < p.N) {
-                float o = (p.beta != 0.f) ? __fmaf_rn(p.alpha, v[j], p.beta * dst[j])
-                                          : p.alpha * v[j];
-                if (epi) o = apply_epilogue<float>(o, p.ep, gn + j);
-                dst[j] = o;
-              }
-            }
-          }
-        }
-      }
-    }
-  }
-}
-
-template <bool A_K, bool B_K, bool VEC, int KIND>
-cudaError_t launch_one(const Params& p, dim3 grid, cudaStream_t stream) {
-  auto kern = sgemm_ffma_kernel<A_K, B_K, VEC, KIND>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       SMEM_BYTES);
-  // several resident blocks need the largest shared-memory carve-out
-  if (e == cudaSuccess && SG_BLOCKS_PER_SM > 1)
-    e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout,
-                             (int)cudaSharedmemCarveoutMaxShared);
-  if (e != cudaSuccess) return e;
-  kern<<<grid, THREADS, SMEM_BYTES, stream>>>(p);
-  return cudaGetLastError();
-}
-
-template <bool A_K, bool B_K>
-cudaError_t launch_vs(const Params& p, bool vec, int kind, dim3 grid, cudaStream_t s) {
-  if (vec) {
-    if (kind == KIND_SPLIT) return launch_one<A_K, B_K, true, KIND_SPLIT>(p, grid, s);
-    if (kind == KIND_PERSIST) return launch_one<A_K, B_K, true, KIND_PERSIST>(p, grid, s);
-    return launch_one<A_K, B_K, true, KIND_TILE>(p, grid, s);
-  }
-  if (kind == KIND_SPLIT) return launch_one<A_K, B_K, false, KIND_SPLIT>(p, grid, s);
-  if (kind == KIND_PERSIST) return launch_one<A_K, B_K, false, KIND_PERSIST>(p, grid, s);
-  return launch_one<A_K, B_K, false, KIND_TILE>(p, grid, s);
-}
-
-}  // namespace
 
 cudaError_t launch_sgemm(const SgemmArgs& a, LaunchCtx& ctx) {
-  Params p;
-  p.A = a.A; p.B = a.B; p.C = a.C; p.partial = a.partial;
-  p.lda = a.lda; p.ldb = a.ldb; p.ldc = a.ldc;
-  p.M = a.M; p.N = a.N; p.K = a.K;
-  p.k_slice = a.splits > 1 ? a.k_slice : a.K;
-  p.tiles_m = (a.M + BM - 1) / BM;
-  p.tiles_n = (a.N + BN - 1) / BN;
-  {
-    const int64_t panel = (int64_t)BM * (a.splits > 1 ? a.k_slice : a.K) * 4;
-    int64_t g = panel > 0 ? RASTER_L2_BYTES / panel : p.tiles_m;
-    if (g < 1) g = 1;
-    if (g > p.tiles_m) g = p.tiles_m;
-    p.group_m = (int)g;
-  }
-  p.alpha = a.alpha; p.beta = a.beta;
-  p.ep = a.ep;
-  const int batch = a.batch > 1 ? a.batch : 1;
-  if (batch > 1 && (a.splits > 1 || batch > 65535)) return cudaErrorInvalidValue;
-  p.stride_a = batch > 1 ? a.stride_a : 0;
-  p.stride_b = batch > 1 ? a.stride_b : 0;
-  p.stride_c = batch > 1 ? a.stride_c : 0;
-  // 16-byte staging needs 16-byte aligned rows in both operands and every
-  // batch entry; the epilogue's float4 accesses need the same of C.
-  const bool vec = ((reinterpret_cast<uintptr_t>(a.A) | reinterpret_cast<uintptr_t>(a.B)) &
-                    15u) == 0 &&
-                   (a.lda % 4) == 0 && (a.ldb % 4) == 0 && (p.stride_a % 4) == 0 &&
-                   (p.stride_b % 4) == 0;
-  p.c_vec = (reinterpret_cast<uintptr_t>(a.C) & 15u) == 0 && (a.ldc % 4) == 0 &&
-            (p.stride_c % 4) == 0;
-  const bool split = a.splits > 1;
-  const int tiles = p.tiles_m * p.tiles_n;
-  int kind = split ? KIND_SPLIT : KIND_TILE;
-  dim3 grid(tiles, batch, split ? a.splits : 1);
-  p.dp_tiles = 0; p.kiters = 0; p.sk_iters = 0; p.sk_ws = nullptr; p.sk_cnt = nullptr;
-  if (a.sk_blocks > 0) {
-    // persistent: all but the last one to two rounds of whole tiles go to
-    // blocks in turn; the rest are shared out by K steps
-    const int G = a.sk_blocks;
-    if (split || batch > 1 || tiles < G || !a.sk_ws || !a.sk_cnt) return cudaErrorInvalidValue;
-    kind = KIND_PERSIST;
-    p.kiters = (a.K + BK - 1) / BK;
-    p.dp_tiles = tiles >= 2 * G ? (tiles / G - 1) * G : 0;
-    p.sk_iters = (int64_t)(tiles - p.dp_tiles) * p.kiters;
-    p.sk_ws = a.sk_ws;
-    p.sk_cnt = a.sk_cnt;
-    grid = dim3(G, 1, 1);
-  }
-  const bool A_K = !a.transA, B_K = a.transB;
-  cudaError_t e;
-  if (A_K && !B_K) e = launch_vs<true, false>(p, vec, kind, grid, ctx.stream);
-  else if (!A_K && !B_K) e = launch_vs<false, false>(p, vec, kind, grid, ctx.stream);
-  else if (A_K && B_K) e = launch_vs<true, true>(p, vec, kind, grid, ctx.stream);
-  else e = launch_vs<false, true>(p, vec, kind, grid, ctx.stream);
-  ctx.grid = (int)(grid.x * grid.y * grid.z);
-  if (e == cudaSuccess) ctx.launches++;
-  return e;
+  if (a.narrow) return launch_sgemm_narrow(a, ctx);
+  return launch_sgemm_t<TileWide, true>(a, ctx);
 }
 
 }  // namespace gb300

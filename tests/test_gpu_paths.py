@@ -92,3 +92,37 @@ def test_forced_fp32_configuration(lib_path, gpu, pack, sk):
     r = subprocess.run([sys.executable, "-c", code], env=env, capture_output=True, text=True,
                        timeout=900)
     assert r.returncode == 0 and r.stdout.strip().endswith("ok"), r.stdout[-3000:] + r.stderr[-3000:]
+
+
+SCRIPT_NARROW = r"""
+import sys
+sys.path.insert(0, {root!r}); sys.path.insert(0, {tests!r})
+from dense_gemm_tiled_gb300 import binding, inputs
+from helpers import check_problem
+for v in ("nn", "tn", "nt", "tt"):
+    tA, tB = inputs.VARIANTS[v]
+    # rank-32 output with a long K (split over K), a ragged N below 32 with
+    # beta, every dimension ragged, and odd leading dimensions on a problem
+    # large enough for the pre-pass copies
+    p = inputs.make_problem(4096, 32, 2048, tA, tB, "f32", "uniform", seed=620)
+    check_problem(p)
+    p = inputs.make_problem(300, 17, 5000, tA, tB, "f32", "uniform", seed=621, beta=0.5)
+    check_problem(p)
+    p = inputs.make_problem(777, 31, 333, tA, tB, "f32", "integer", seed=622, beta=1.0,
+                            c_fill="integer")
+    check_problem(p, exact=True)
+    p = inputs.make_problem(8191, 29, 4601, tA, tB, "f32", "uniform", seed=623)
+    check_problem(p)
+print("ok")
+"""
+
+
+@pytest.mark.parametrize("narrow", ["1", "0"])
+def test_fp32_narrow_tile(lib_path, gpu, narrow):
+    """N <= 32 on the fp32 path: the 256 x 32 tile (default) or the general
+    128 x 128 tile (GEMM_GB300_SG_NARROW=0), split over K or not."""
+    env = dict(os.environ, GEMM_GB300_SG_NARROW=narrow)
+    code = SCRIPT_NARROW.format(root=ROOT, tests=os.path.join(ROOT, "tests"))
+    r = subprocess.run([sys.executable, "-c", code], env=env, capture_output=True, text=True,
+                       timeout=900)
+    assert r.returncode == 0 and r.stdout.strip().endswith("ok"), r.stdout[-3000:] + r.stderr[-3000:]
