@@ -72,6 +72,8 @@ __device__ __forceinline__ float load_out(const __nv_bfloat16* C, int64_t i) {
 template <typename T>
 __global__ void splitk_reduce_vec4(int M, int N, int splits, const float* __restrict__ P, T* C,
                                    int64_t ldc, float alpha, float beta, Epilogue ep) {
+  pdl_wait();
+  pdl_trigger();
   const int64_t quads = (int64_t)M * (N / 4);
   const int64_t slice = (int64_t)M * N;
   for (int64_t q = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; q < quads;
@@ -98,6 +100,8 @@ __global__ void splitk_reduce_vec4(int M, int N, int splits, const float* __rest
 template <typename T>
 __global__ void splitk_reduce_scalar(int M, int N, int splits, const float* __restrict__ P, T* C,
                                      int64_t ldc, float alpha, float beta, Epilogue ep) {
+  pdl_wait();
+  pdl_trigger();
   const int64_t total = (int64_t)M * N;
   for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < total;
        i += (int64_t)gridDim.x * blockDim.x) {
@@ -112,6 +116,8 @@ __global__ void splitk_reduce_scalar(int M, int N, int splits, const float* __re
 
 template <typename T>
 __global__ void scale_kernel(int M, int N, T* C, int64_t ldc, float beta, Epilogue ep) {
+  pdl_wait();
+  pdl_trigger();
   const int64_t total = (int64_t)M * N;
   for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < total;
        i += (int64_t)gridDim.x * blockDim.x) {
@@ -131,6 +137,8 @@ template <typename W>
 __global__ void __launch_bounds__(256) repack_kernel(int rows, int cols, const W* __restrict__ src,
                                                      int64_t ld_src, W* __restrict__ dst,
                                                      int64_t ld_dst) {
+  pdl_wait();
+  pdl_trigger();
   constexpr int V = 16 / sizeof(W);
   const int chunks = (int)(ld_dst / V);
   for (int r = blockIdx.y; r < rows; r += gridDim.y) {
@@ -160,6 +168,8 @@ template <typename W>
 __global__ void __launch_bounds__(256) copy_rows_kernel(int rows, int cols,
                                                         const W* __restrict__ src, int64_t ld_src,
                                                         W* __restrict__ dst, int64_t ld_dst) {
+  pdl_wait();
+  pdl_trigger();
   constexpr int U = 8;
   for (int r = blockIdx.y; r < rows; r += gridDim.y) {
     const W* s = src + (int64_t)r * ld_src;
@@ -189,6 +199,8 @@ __global__ void __launch_bounds__(256) transpose_f32_kernel(int rows, int cols,
                                                             const float* __restrict__ src,
                                                             int64_t ld_src, float* __restrict__ dst,
                                                             int64_t ld_dst) {
+  pdl_wait();
+  pdl_trigger();
   __shared__ float tile[64][65];
   const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;  // 16 float4 columns x 16 rows
   const int tiles_c = (cols + 63) / 64;
@@ -242,9 +254,9 @@ cudaError_t launch_repack(int rows, int cols, const void* src, int64_t ld_src, v
   const int gx = (int)std::min<int64_t>((chunks + 255) / 256, 64);
   const int gy = (int)std::min<int64_t>(std::min<int64_t>(rows, 65535),
                                         std::max<int64_t>(1, (int64_t)sm_count() * 8 / gx));
-  repack_kernel<W><<<dim3(gx, gy), 256, 0, ctx.stream>>>(
-      rows, cols, static_cast<const W*>(src), ld_src, static_cast<W*>(dst), ld_dst);
-  cudaError_t e = cudaGetLastError();
+  cudaError_t e = launch_kernel(repack_kernel<W>, dim3(gx, gy), dim3(256), 0, ctx.stream, 1, rows,
+                                cols, static_cast<const W*>(src), ld_src, static_cast<W*>(dst),
+                                ld_dst);
   if (e == cudaSuccess) ctx.launches++;
   return e;
 }
@@ -259,13 +271,14 @@ cudaError_t launch_copy_rows(int esize, int rows, int cols, const void* src, int
   const int gx = (int)std::min<int64_t>((cols + per_block - 1) / per_block, 64);
   const int gy = (int)std::min<int64_t>(std::min<int64_t>(rows, 65535),
                                         std::max<int64_t>(1, (int64_t)sm_count() * 8 / gx));
-  if (esize == 2)
-    copy_rows_kernel<uint16_t><<<dim3(gx, gy), 256, 0, ctx.stream>>>(
-        rows, cols, static_cast<const uint16_t*>(src), ld_src, static_cast<uint16_t*>(dst), ld_dst);
-  else
-    copy_rows_kernel<uint32_t><<<dim3(gx, gy), 256, 0, ctx.stream>>>(
-        rows, cols, static_cast<const uint32_t*>(src), ld_src, static_cast<uint32_t*>(dst), ld_dst);
-  cudaError_t e = cudaGetLastError();
+  cudaError_t e =
+      esize == 2
+          ? launch_kernel(copy_rows_kernel<uint16_t>, dim3(gx, gy), dim3(256), 0, ctx.stream, 1,
+                          rows, cols, static_cast<const uint16_t*>(src), ld_src,
+                          static_cast<uint16_t*>(dst), ld_dst)
+          : launch_kernel(copy_rows_kernel<uint32_t>, dim3(gx, gy), dim3(256), 0, ctx.stream, 1,
+                          rows, cols, static_cast<const uint32_t*>(src), ld_src,
+                          static_cast<uint32_t*>(dst), ld_dst);
   if (e == cudaSuccess) ctx.launches++;
   return e;
 }
@@ -282,9 +295,10 @@ cudaError_t launch_transpose_f32(int rows, int cols, const float* src, int64_t l
   // 128-bit accesses need 16-byte aligned rows on both sides
   const bool vec = ((reinterpret_cast<uintptr_t>(src) | reinterpret_cast<uintptr_t>(dst)) & 15u) == 0 &&
                    (ld_src % 4) == 0 && (ld_dst % 4) == 0;
-  if (vec) transpose_f32_kernel<true><<<grid, 256, 0, ctx.stream>>>(rows, cols, src, ld_src, dst, ld_dst);
-  else transpose_f32_kernel<false><<<grid, 256, 0, ctx.stream>>>(rows, cols, src, ld_src, dst, ld_dst);
-  cudaError_t e = cudaGetLastError();
+  cudaError_t e = vec ? launch_kernel(transpose_f32_kernel<true>, dim3(grid), dim3(256), 0,
+                                      ctx.stream, 1, rows, cols, src, ld_src, dst, ld_dst)
+                       : launch_kernel(transpose_f32_kernel<false>, dim3(grid), dim3(256), 0,
+                                      ctx.stream, 1, rows, cols, src, ld_src, dst, ld_dst);
   if (e == cudaSuccess) ctx.launches++;
   return e;
 }
@@ -296,17 +310,24 @@ cudaError_t launch_splitk_reduce(int dtype, int M, int N, int splits, const floa
   const bool vec = (N % 4) == 0;
   const int64_t items = vec ? (int64_t)M * (N / 4) : (int64_t)M * N;
   const int grid = grid_for(items, threads);
+  const dim3 g(grid), b(threads);
+  cudaError_t e;
   if (dtype == 0) {
-    if (vec) splitk_reduce_vec4<float><<<grid, threads, 0, ctx.stream>>>(M, N, splits, P, (float*)C, ldc, alpha, beta, ep);
-    else splitk_reduce_scalar<float><<<grid, threads, 0, ctx.stream>>>(M, N, splits, P, (float*)C, ldc, alpha, beta, ep);
+    e = vec ? launch_kernel(splitk_reduce_vec4<float>, g, b, 0, ctx.stream, 1, M, N, splits, P,
+                            (float*)C, ldc, alpha, beta, ep)
+            : launch_kernel(splitk_reduce_scalar<float>, g, b, 0, ctx.stream, 1, M, N, splits, P,
+                            (float*)C, ldc, alpha, beta, ep);
   } else if (dtype == 1) {
-    if (vec) splitk_reduce_vec4<__half><<<grid, threads, 0, ctx.stream>>>(M, N, splits, P, (__half*)C, ldc, alpha, beta, ep);
-    else splitk_reduce_scalar<__half><<<grid, threads, 0, ctx.stream>>>(M, N, splits, P, (__half*)C, ldc, alpha, beta, ep);
+    e = vec ? launch_kernel(splitk_reduce_vec4<__half>, g, b, 0, ctx.stream, 1, M, N, splits, P,
+                            (__half*)C, ldc, alpha, beta, ep)
+            : launch_kernel(splitk_reduce_scalar<__half>, g, b, 0, ctx.stream, 1, M, N, splits, P,
+                            (__half*)C, ldc, alpha, beta, ep);
   } else {
-    if (vec) splitk_reduce_vec4<__nv_bfloat16><<<grid, threads, 0, ctx.stream>>>(M, N, splits, P, (__nv_bfloat16*)C, ldc, alpha, beta, ep);
-    else splitk_reduce_scalar<__nv_bfloat16><<<grid, threads, 0, ctx.stream>>>(M, N, splits, P, (__nv_bfloat16*)C, ldc, alpha, beta, ep);
+    e = vec ? launch_kernel(splitk_reduce_vec4<__nv_bfloat16>, g, b, 0, ctx.stream, 1, M, N, splits,
+                            P, (__nv_bfloat16*)C, ldc, alpha, beta, ep)
+            : launch_kernel(splitk_reduce_scalar<__nv_bfloat16>, g, b, 0, ctx.stream, 1, M, N,
+                            splits, P, (__nv_bfloat16*)C, ldc, alpha, beta, ep);
   }
-  cudaError_t e = cudaGetLastError();
   if (e == cudaSuccess) ctx.launches++;
   return e;
 }
@@ -315,10 +336,15 @@ cudaError_t launch_scale(int dtype, int M, int N, void* C, int64_t ldc, float be
                          LaunchCtx& ctx, Epilogue ep) {
   const int threads = 256;
   const int grid = grid_for((int64_t)M * N, threads);
-  if (dtype == 0) scale_kernel<float><<<grid, threads, 0, ctx.stream>>>(M, N, (float*)C, ldc, beta, ep);
-  else if (dtype == 1) scale_kernel<__half><<<grid, threads, 0, ctx.stream>>>(M, N, (__half*)C, ldc, beta, ep);
-  else scale_kernel<__nv_bfloat16><<<grid, threads, 0, ctx.stream>>>(M, N, (__nv_bfloat16*)C, ldc, beta, ep);
-  cudaError_t e = cudaGetLastError();
+  const dim3 g(grid), b(threads);
+  cudaError_t e;
+  if (dtype == 0)
+    e = launch_kernel(scale_kernel<float>, g, b, 0, ctx.stream, 1, M, N, (float*)C, ldc, beta, ep);
+  else if (dtype == 1)
+    e = launch_kernel(scale_kernel<__half>, g, b, 0, ctx.stream, 1, M, N, (__half*)C, ldc, beta, ep);
+  else
+    e = launch_kernel(scale_kernel<__nv_bfloat16>, g, b, 0, ctx.stream, 1, M, N,
+                      (__nv_bfloat16*)C, ldc, beta, ep);
   if (e == cudaSuccess) ctx.launches++;
   return e;
 }

@@ -32,6 +32,19 @@ __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
 
+// Programmatic dependent launch.  Every kernel of the library is launched with
+// programmatic stream serialization (launch_kernel below), so it may become
+// resident while the kernel before it in the stream is still running: its
+// set-up (barriers, tensor memory, descriptor prefetch) then overlaps that
+// kernel's tail.  Before its first global-memory access it waits for the
+// previous kernel to complete and its writes to be visible (pdl_wait), and it
+// lets the next kernel launch (pdl_trigger), whose blocks in turn wait for this
+// one to complete.  Both are no-ops in a launch without the attribute.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 __device__ __forceinline__ uint64_t globaltimer_ns() {
   uint64_t t;
   asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
@@ -362,4 +375,35 @@ __device__ __forceinline__ void tma_store_3d(const CUtensorMap* map, int32_t x, 
                "r"(x), "r"(y), "r"(z), "r"(src)
                : "memory");
 }
+
+// Launches `kern` on `stream` with programmatic stream serialization (unless
+// switched off: env GEMM_GB300_PDL=0) and, for cluster_x > 1, clusters of
+// cluster_x blocks along x.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_kernel(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                          cudaStream_t stream, int cluster_x, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[2];
+  int n = 0;
+  if (pdl_enabled()) {
+    attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[n].val.programmaticStreamSerializationAllowed = 1;
+    ++n;
+  }
+  if (cluster_x > 1) {
+    attr[n].id = cudaLaunchAttributeClusterDimension;
+    attr[n].val.clusterDim.x = (unsigned)cluster_x;
+    attr[n].val.clusterDim.y = 1;
+    attr[n].val.clusterDim.z = 1;
+    ++n;
+  }
+  cfg.attrs = attr;
+  cfg.numAttrs = n;
+  return cudaLaunchKernelEx(&cfg, kern, args...);
+}
+
 }  // namespace gb300

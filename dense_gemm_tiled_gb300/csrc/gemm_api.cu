@@ -24,6 +24,17 @@
 
 using namespace gb300;
 
+namespace gb300 {
+// Programmatic dependent launch switch (declared in internal.h).
+int pdl_enabled() {
+  static const int v = [] {
+    const char* e = getenv("GEMM_GB300_PDL");
+    return e ? atoi(e) : 1;
+  }();
+  return v;
+}
+}  // namespace gb300
+
 namespace {
 
 __device__ unsigned int g_status_word;  // per device: bits of STATUS_*

@@ -438,6 +438,10 @@ __global__ void __launch_bounds__(THREADS, 1)
   else __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
+  // (set-up above may overlap the previous kernel in the stream; it completes
+  // before any global access below)
+  pdl_wait();
+  pdl_trigger();
 
   const WaitCtl wc{p.status, abort_flag, p.timeout_ns};
   const int n_units = total_units(p, PAIR);
@@ -1044,28 +1048,17 @@ cudaError_t launch_cfg(const HgemmArgs& a, const HParams& p, LaunchCtx& ctx) {
   if constexpr (PAIR) {
     // persistent grid of as many pairs as can be resident at once
     const int max_pairs = pair_slots<T, BN, A_MN, B_MN, MODE>(a.num_sms);
-    cudaLaunchConfig_t cfg = {};
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = 2;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.blockDim = dim3(THREADS);
-    cfg.dynamicSmemBytes = C_::SMEM_BYTES;
-    cfg.stream = ctx.stream;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
     const int units = host_total_units(p, true);
     const int pairs = units < max_pairs ? units : max_pairs;
-    cfg.gridDim = dim3(2 * pairs);
     ctx.grid = 2 * pairs;
-    e = cudaLaunchKernelEx(&cfg, kern, mA, mB, mC, pp);
+    e = launch_kernel(kern, dim3(2 * pairs), dim3(THREADS), C_::SMEM_BYTES, ctx.stream, 2, mA, mB,
+                      mC, pp);
   } else {
     const int units = host_total_units(p, false);
     const int grid = units < a.num_sms ? units : a.num_sms;
     ctx.grid = grid;
-    kern<<<grid, THREADS, C_::SMEM_BYTES, ctx.stream>>>(mA, mB, mC, pp);
-    e = cudaGetLastError();
+    e = launch_kernel(kern, dim3(grid), dim3(THREADS), C_::SMEM_BYTES, ctx.stream, 1, mA, mB, mC,
+                      pp);
   }
   if (e == cudaSuccess) ctx.launches++;
   return e;

@@ -93,6 +93,10 @@ struct LaunchCtx {
 };
 
 // Launchers (return cudaSuccess or the launch error).
+// Programmatic dependent launch of the library's kernels (env GEMM_GB300_PDL=0
+// turns it off).
+int pdl_enabled();
+
 cudaError_t launch_sgemm(const SgemmArgs& a, LaunchCtx& ctx);
 cudaError_t launch_sgemm_narrow(const SgemmArgs& a, LaunchCtx& ctx);  // a.narrow tiles
 cudaError_t launch_hgemm(const HgemmArgs& a, LaunchCtx& ctx);

@@ -281,6 +281,9 @@ __global__ void __launch_bounds__(TL::THREADS, TL::MIN_BLOCKS) sgemm_ffma_kernel
   constexpr int BM = TL::BM, BN = TL::BN, BK = TL::BK, THREADS = TL::THREADS;
   constexpr int WARPS_N = TL::WARPS_N, APAD = TL::APAD, BPAD = TL::BPAD;
   constexpr int A_FLOATS = TL::A_FLOATS, STAGE_FLOATS = TL::STAGE_FLOATS;
+  // (the previous kernel in the stream completes before any global access)
+  pdl_wait();
+  pdl_trigger();
   extern __shared__ __align__(16) float smem[];
   __shared__ int s_last;
   const int tid = threadIdx.x;
@@ -557,8 +560,7 @@ cudaError_t launch_one(const Params& p, dim3 grid, cudaStream_t stream) {
     e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout,
                              (int)cudaSharedmemCarveoutMaxShared);
   if (e != cudaSuccess) return e;
-  kern<<<grid, TL::THREADS, TL::SMEM_BYTES, stream>>>(p);
-  return cudaGetLastError();
+  return launch_kernel(kern, grid, dim3(TL::THREADS), TL::SMEM_BYTES, stream, 1, p);
 }
 
 // (PERSIST: the stream-K launch, instantiated only for tiles that use it)

@@ -8,7 +8,7 @@ import torch
 import oracle
 from oracle import compare
 from dense_gemm_tiled_gb300 import inputs
-from helpers import check_problem, to_np
+from helpers import check_problem, fmt_of, to_np
 
 pytestmark = pytest.mark.gpu
 
@@ -190,3 +190,57 @@ def test_gemm_host_pipelined(dtype, variant, M):
         got = got[idx[0], idx[1]]
     res = compare.check(got, ref, mag, dtype)
     assert res["ok"], res
+
+
+@pytest.mark.parametrize("dtype", ["f32", "f16"])
+@pytest.mark.parametrize("shape", [(256, 256, 2048), (1024, 768, 512)], ids=["splitk", "whole"])
+@pytest.mark.parametrize("graph", [False, True], ids=["eager", "graph"])
+def test_dependent_calls_back_to_back(dtype, shape, graph):
+    """Calls queued on one stream with no synchronisation between them, each
+    reading what the one before wrote (Y2 = Y1 W2 after Y1 = X W1) or
+    overwriting what it read (Y1 = X' W1 after Y2 read Y1): the library's
+    kernels may start while the previous one runs, so each must wait for it
+    before touching memory.  Split-K shapes add the reduction kernel to the
+    chain.  Eager and captured in a CUDA graph, against the oracle."""
+    b = _b()
+    M, N, K = shape  # Y1 [M, K] feeds the second product, which is [M, K] x [K, N]
+    X = inputs.uniform((M, K), 900, dtype)
+    X2 = inputs.uniform((M, K), 901, dtype)
+    W1 = inputs.uniform((K, K), 902, dtype)
+    W2 = inputs.uniform((K, N), 903, dtype)
+    d = {k: v.cuda() for k, v in dict(X=X, X2=X2, W1=W1, W2=W2).items()}
+    Y1 = torch.empty((M, K), dtype=d["X"].dtype, device="cuda")
+    Y2 = torch.empty((M, N), dtype=d["X"].dtype, device="cuda")
+    s = torch.cuda.Stream()
+
+    def chain():
+        b.gemm(d["X"], d["W1"], Y1, stream=s)
+        b.gemm(Y1, d["W2"], Y2, stream=s)
+        b.gemm(d["X2"], d["W1"], Y1, stream=s)
+
+    with torch.cuda.stream(s):
+        chain()
+    s.synchronize()
+    if graph:
+        Y1.fill_(float("nan"))
+        Y2.fill_(float("nan"))
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=s):
+            chain()
+        g.replay()
+        torch.cuda.synchronize()
+    assert b.check_device_status() == b.OK
+    fmt = fmt_of(dtype)
+    ref1, mag1 = oracle.gemm_ref(to_np(X2), to_np(W1), None, False, False, 1.0, 0.0, fmt=fmt)
+    assert compare.check(to_np(Y1.cpu()), ref1, mag1, dtype)["ok"]
+    # the second product is checked on the operand it read: the first Y1,
+    # recomputed alone (the library is deterministic) and itself checked
+    Y1a = torch.empty_like(Y1)
+    b.gemm(d["X"], d["W1"], Y1a)
+    torch.cuda.synchronize()
+    r0, m0 = oracle.gemm_ref(to_np(X), to_np(W1), None, False, False, 1.0, 0.0, fmt=fmt)
+    assert compare.check(to_np(Y1a.cpu()), r0, m0, dtype)["ok"]
+    ref2, mag2 = oracle.gemm_ref(to_np(Y1a.cpu()), to_np(W2), None, False, False, 1.0, 0.0,
+                                 fmt=fmt)
+    assert compare.check(to_np(Y2.cpu()), ref2, mag2, dtype)["ok"]
