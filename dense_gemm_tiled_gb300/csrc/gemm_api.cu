@@ -243,6 +243,17 @@ int forced_bn() {
 int cuda_fail(cudaError_t e) { return e == cudaErrorMemoryAllocation ? GEMM_ERR_NO_MEMORY : GEMM_ERR_CUDA; }
 
 // Split-K plan: how many K slices, each a multiple of `kstep` long.
+// Fewest K steps a split-K slice gets (compile-time knobs).  fp32: one (a
+// 64-deep step of a 128 x 128 tile is ~1M FMAs), measured on small squares
+// against 2 and 4: 256^3 16 / 21 / 31 us, 512^3 18 / 23 / 33 us; fp16: four
+// (one or two measured 1-8 % slower from 256^3 to 1024^3).
+#ifndef GB300_SG_SLICE_STEPS
+#define GB300_SG_SLICE_STEPS 1
+#endif
+#ifndef GB300_HG_SLICE_STEPS
+#define GB300_HG_SLICE_STEPS 4
+#endif
+
 void plan_splits(int64_t tiles, int64_t K, int kstep, int capacity, int min_steps_per_slice,
                  int max_splits, int* splits, int* k_slice) {
   const int64_t steps = (K + kstep - 1) / kstep;
@@ -393,7 +404,7 @@ int run_gemm(int transA, int transB, int64_t M64, int64_t N64, int64_t K64, int 
     if (narrow)
       plan_splits(tiles, K, SGN_BK, sms * SGN_BLOCKS_PER_SM, 8, 16, &splits, &k_slice);
     else
-      plan_splits(tiles, K, SG_BK, 2 * sms, 4, 16, &splits, &k_slice);
+      plan_splits(tiles, K, SG_BK, 2 * sms, GB300_SG_SLICE_STEPS, 16, &splits, &k_slice);
     SgemmArgs a{transA, transB, M, N, K, (const float*)A, lda, (const float*)B, ldb, (float*)C,
                 ldc, alpha, beta, splits, k_slice, nullptr};
     a.narrow = narrow ? 1 : 0;
@@ -469,7 +480,7 @@ int run_gemm(int transA, int transB, int64_t M64, int64_t N64, int64_t K64, int 
       bn = forced;
     const int64_t tiles = (int64_t)((M + HG_BM - 1) / HG_BM) * ((N + bn - 1) / bn);
     int splits, k_slice;
-    plan_splits(tiles, K, HG_BK, sms, 4, 32, &splits, &k_slice);
+    plan_splits(tiles, K, HG_BK, sms, GB300_HG_SLICE_STEPS, 32, &splits, &k_slice);
     // The tensor-memory-access unit needs 16-byte aligned bases and row
     // pitches; an operand that has neither is copied into padded scratch.
     const void* Ad = A;

@@ -51,7 +51,7 @@ SHAPES = {
     # fp32: split-K (15 tiles), plain tiles, persistent stream-K with packing,
     # and rows of every operand off 16-byte alignment (odd leading dimensions:
     # operands copied to an aligned pitch first, C stored element-wise)
-    "f32": [((300, 520, 1024), "ffma_splitk"), ((640, 1280, 96), "ffma"),
+    "f32": [((300, 520, 1024), "ffma_splitk"), ((640, 1280, 64), "ffma"),
             ((1000, 2600, 620), "ffma"), ((1001, 2601, 621), "ffma")],
     # 16-bit: split-K, whole-K 2-SM pairs (C stored by TMA, and loaded by TMA
     # when beta != 0), and an odd N (C rows off 16-byte alignment: stored
