@@ -40,9 +40,16 @@
  *   - Calls are asynchronous on `stream` (0 = the legacy default stream) and
  *     may be made from several host threads.  Scratch space the library needs
  *     (split-K partial sums; zero-padded copies of operands whose rows are not
- *     16-byte aligned) is taken in stream order on `stream` from a memory pool
- *     the library creates once per device, and released on the same stream;
- *     the pool keeps released memory for reuse until the process exits.
+ *     16-byte aligned; on large problems an aligned working copy of a C whose
+ *     rows are not, copied into place at the end) is taken in stream order on
+ *     `stream` from a memory pool the library creates once per device, and
+ *     released on the same stream; the pool keeps released memory for reuse
+ *     until the process exits.
+ *   - The library's kernels are launched with programmatic stream
+ *     serialization: each may start its set-up while the previous work on the
+ *     stream is finishing, and waits for that work to complete before reading
+ *     or writing any buffer.  Stream order is therefore kept exactly as for
+ *     ordinary launches (environment GEMM_GB300_PDL=0 turns the overlap off).
  *   - Argument errors are returned synchronously, before anything is
  *     launched.  Launch failures return GEMM_ERR_CUDA.  A kernel whose
  *     internal wait exceeds its time limit records the fact in a per-device
