@@ -618,11 +618,17 @@ int host_pipelined(int transA, int transB, int64_t M, int64_t N, int64_t K, int 
   const size_t nA = (size_t)(ar * lda_d * e + 255) / 256 * 256;
   const size_t nB = (size_t)(br * ldb_d * e + 255) / 256 * 256;
   const size_t nC = (size_t)(M * ldc_d * e + 255) / 256 * 256;
+  // fp32 C: the first panel runs as NK products over K slices, each started
+  // once its slice of B (and of the panel's A rows) has arrived, accumulating
+  // in C (beta = 1 after the first); so the first GEMM waits for a quarter of
+  // B rather than all of it.  (16-bit C would be rounded between slices.)
+  const int NK = (dtype == GEMM_F32 || dtype == GEMM_F32_TF32) && K >= 1024 ? 4 : 1;
+  const int64_t kl = ((K + NK - 1) / NK + 63) / 64 * 64;  // K per slice
   cudaStream_t sin, sout;
   cudaError_t ce = side_streams(&sin, &sout);
   if (ce != cudaSuccess) return cuda_fail(ce);
   EventSet evs;
-  ce = evs.make(2 * panels + 2);
+  ce = evs.make(2 * panels + 2 + NK);
   if (ce != cudaSuccess) return cuda_fail(ce);
   Scratch buf;
   ce = buf.get(nA + nB + nC, stream);
@@ -637,13 +643,57 @@ int host_pipelined(int transA, int transB, int64_t M, int64_t N, int64_t K, int 
   ce = cudaEventRecord(ev_alloc, stream);
   if (ce == cudaSuccess) ce = cudaStreamWaitEvent(sin, ev_alloc, 0);
   if (ce == cudaSuccess) ce = cudaStreamWaitEvent(sout, ev_alloc, 0);
-  if (ce == cudaSuccess)
+  if (ce == cudaSuccess && NK == 1)
     ce = cudaMemcpy2DAsync(dB, ldb_d * e, B, ldb * e, bc * e, br, cudaMemcpyHostToDevice, sin);
   int rc = GEMM_OK;
   for (int p = 0; p < panels && ce == cudaSuccess && rc == GEMM_OK; ++p) {
     const int64_t r0 = p * pr, r1 = r0 + pr < M ? r0 + pr : M;
     if (r0 >= M) break;
     const int64_t mp = r1 - r0;
+    if (p == 0 && NK > 1) {
+      // panel 0 (rows 0 .. mp), slice by slice: B rows k0..k1 of B[K,N] or
+      // columns of B[N,K]; A columns k0..k1 of A[M,K] or rows of A[K,M]
+      char* dC0 = dC;
+      char* hC0 = static_cast<char*>(C);
+      for (int c = 0; c < NK && ce == cudaSuccess && rc == GEMM_OK; ++c) {
+        const int64_t k0 = c * kl, k1 = k0 + kl < K ? k0 + kl : K;
+        if (k0 >= K) break;
+        const int64_t kw = k1 - k0;
+        const char* hB = static_cast<const char*>(B) + (transB ? k0 * e : k0 * ldb * e);
+        char* dBk = dB + (transB ? k0 * e : k0 * ldb_d * e);
+        ce = transB ? cudaMemcpy2DAsync(dBk, ldb_d * e, hB, ldb * e, kw * e, br,
+                                        cudaMemcpyHostToDevice, sin)
+                    : cudaMemcpy2DAsync(dBk, ldb_d * e, hB, ldb * e, bc * e, kw,
+                                        cudaMemcpyHostToDevice, sin);
+        const char* hA = static_cast<const char*>(A) + (transA ? k0 * lda * e : k0 * e);
+        char* dAk = dA + (transA ? k0 * lda_d * e : k0 * e);
+        if (ce == cudaSuccess)
+          ce = transA ? cudaMemcpy2DAsync(dAk, lda_d * e, hA, lda * e, mp * e, kw,
+                                          cudaMemcpyHostToDevice, sin)
+                      : cudaMemcpy2DAsync(dAk, lda_d * e, hA, lda * e, kw * e, mp,
+                                          cudaMemcpyHostToDevice, sin);
+        if (ce == cudaSuccess && c == 0 && beta != 0.f)
+          ce = cudaMemcpy2DAsync(dC0, ldc_d * e, hC0, ldc * e, N * e, mp, cudaMemcpyHostToDevice,
+                                 sin);
+        cudaEvent_t evk = evs.ev[2 * panels + 2 + c];
+        if (ce == cudaSuccess) ce = cudaEventRecord(evk, sin);
+        if (ce == cudaSuccess) ce = cudaStreamWaitEvent(stream, evk, 0);
+        if (ce != cudaSuccess) break;
+        rc = run_gemm(transA, transB, mp, N, kw, dtype, alpha, c == 0 ? beta : 1.f, dAk, lda_d,
+                      dBk, ldb_d, dC0, ldc_d, stream, transA ? kw : mp, transA ? mp : kw,
+                      transB ? N : kw, transB ? kw : N);
+        if (rc != GEMM_OK) break;
+        path = tl_last_path;
+        launches += tl_last_launches;
+      }
+      if (ce != cudaSuccess || rc != GEMM_OK) break;
+      ce = cudaEventRecord(evs.ev[1], stream);
+      if (ce == cudaSuccess) ce = cudaStreamWaitEvent(sout, evs.ev[1], 0);
+      if (ce == cudaSuccess)
+        ce = cudaMemcpy2DAsync(hC0, ldc * e, dC0, ldc_d * e, N * e, mp, cudaMemcpyDeviceToHost,
+                               sout);
+      continue;
+    }
     // A rows r0..r1 of op(A): rows of A[M,K], or columns of A[K,M]
     const char* srcA = static_cast<const char*>(A) + (transA ? r0 * e : r0 * lda * e);
     char* dstA = dA + (transA ? r0 * e : r0 * lda_d * e);

@@ -169,12 +169,13 @@ def test_kernel_events_bracket_the_gemm_kernel():
 
 
 @pytest.mark.parametrize("dtype,variant,M", [("f32", "nn", 1024), ("f32", "tn", 1000),
-                                             ("f32", "nt", 4096), ("f16", "tn", 1000),
-                                             ("bf16", "nn", 2048)])
+                                             ("f32", "nt", 4096), ("f32", "nt", 2048),
+                                             ("f16", "tn", 1000), ("bf16", "nn", 2048)])
 def test_gemm_host_pipelined(dtype, variant, M):
     """gemm_host on problems of at least 2^30 multiply-adds runs row panels of
     C on the device while later panels' A rows are still arriving and earlier
-    panels' C rows are leaving (two copy streams); every panel must match the
+    panels' C rows are leaving (two copy streams); with fp32 and K >= 1024 the
+    first panel runs over K slices as B arrives.  Every panel must match the
     oracle, beta included."""
     b = _b()
     N, K = 1536, 1024 if M < 4096 else 256
