@@ -123,3 +123,16 @@ def test_tf32_not_accepted_without_scratch(b, lib_path):
     f.restype = ci
     assert f(0, 0, 4, 4, 4, 3, 1.0, 0.0, PA, 4, PB, 4, PC, 4, None) == 2
     assert b.gemm_raw(0, 0, 4, 4, 4, 4, 1.0, 0.0, PA, 4, PB, 4, PC, 4) == 1  # dtype 4 unknown
+
+
+@pytest.mark.parametrize("entry", ["gemm", "gemm_strided_batched"])
+def test_binding_refuses_host_tensors(lib_path, entry):
+    """No CPU fallback: the device entry points refuse host tensors outright
+    (host memory goes through gemm_host, whose copies are part of the call)."""
+    import torch
+    from dense_gemm_tiled_gb300 import binding
+    shape = (4, 8, 8) if entry == "gemm_strided_batched" else (8, 8)
+    A, B, C = torch.ones(shape), torch.ones(shape), torch.zeros(shape)
+    with pytest.raises(ValueError):
+        getattr(binding, entry)(A, B, C)
+    assert torch.count_nonzero(C) == 0
