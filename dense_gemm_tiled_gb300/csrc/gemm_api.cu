@@ -823,7 +823,6 @@ int run_batched(int transA, int transB, int64_t M64, int64_t N64, int64_t K64, i
                   alpha, beta, 1, K, nullptr};
       a.batch = nb;
       a.stride_a = sA; a.stride_b = sB; a.stride_c = sC;
-      a.narrow = N <= SGN_BN && sg_narrow_enabled() ? 1 : 0;
       e = timed_sgemm(a, ctx);
     }
   }
