@@ -222,14 +222,6 @@ __device__ __forceinline__ void cluster_sync() {
       "barrier.cluster.arrive.release.aligned;\n\t"
       "barrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
-// tcgen05.commit arriving on the mbarrier at `bar` in every block of `mask`.
-__device__ __forceinline__ void tc_commit_mc(uint32_t bar, uint16_t mask) {
-  asm volatile(
-      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
-      " [%0], %1;" ::"r"(bar),
-      "h"(mask)
-      : "memory");
-}
 }  // namespace gb300
 
 namespace gb300 {
@@ -344,16 +336,6 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map
       "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes"
       " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(dst),
       "l"(map), "r"(x), "r"(y), "r"(z), "r"(bar)
-      : "memory");
-}
-// The same box written to the same shared-memory offset of every block in
-// `mask`, each block's mbarrier at `bar` (same offset) receiving its bytes.
-__device__ __forceinline__ void tma_load_3d_mc(uint32_t dst, const CUtensorMap* map, int32_t x,
-                                               int32_t y, int32_t z, uint32_t bar, uint16_t mask) {
-  asm volatile(
-      "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes"
-      ".multicast::cluster [%0], [%1, {%2, %3, %4}], [%5], %6;" ::"r"(dst),
-      "l"(map), "r"(x), "r"(y), "r"(z), "r"(bar), "h"(mask)
       : "memory");
 }
 // Load into this block's shared memory whose completion is signalled on the

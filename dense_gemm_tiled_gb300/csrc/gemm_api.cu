@@ -184,14 +184,12 @@ int sg_narrow_enabled() {
   return v;
 }
 
-// fp16 block pairs (env GEMM_GB300_HG_PAIR): 0 off, 1 pairs sharing B tiles by
-// TMA multicast, 2 (default) pairs running 2-SM (cta_group::2) MMAs -- measured
-// on GB300 at 4096^3 and 8192^3: mode 2 +6..9 % over mode 1 (nn, nt).
+// fp16 block pairs (env GEMM_GB300_HG_PAIR): 0 single blocks, 2 (default)
+// pairs running 2-SM (cta_group::2) MMAs; any other value means 2.
 int pair_enabled() {
   static const int v = [] {
     const char* e = getenv("GEMM_GB300_HG_PAIR");
-    const int m = e ? atoi(e) : 2;
-    return (m >= 0 && m <= 2) ? m : 2;
+    return (e && atoi(e) == 0) ? 0 : 2;
   }();
   return v;
 }

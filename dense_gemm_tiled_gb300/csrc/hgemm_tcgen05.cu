@@ -8,8 +8,7 @@ int hgemm_pair_slots(int bn, int transA, int transB, int mode, int num_sms) {
   const bool A_MN = transA != 0, B_MN = transB == 0;
 #define GB300_SLOTS(W, AM, BMN)                                                              \
   if (bn == W && A_MN == AM && B_MN == BMN)                                                  \
-    return mode == 2 ? pair_slots<__half, W, AM, BMN, 2>(num_sms)                           \
-                     : pair_slots<__half, W, AM, BMN, 1>(num_sms);
+    return pair_slots<__half, W, AM, BMN, 2>(num_sms);
   GB300_SLOTS(128, false, true) GB300_SLOTS(128, true, true) GB300_SLOTS(128, false, false)
   GB300_SLOTS(128, true, false) GB300_SLOTS(256, false, true) GB300_SLOTS(256, true, true)
   GB300_SLOTS(256, false, false) GB300_SLOTS(256, true, false)

@@ -113,12 +113,12 @@ constexpr int GROUP_M = 8;
 constexpr int A_TILE_BYTES = BM * BK * 2;  // 16 KiB
 constexpr int SMEM_LIMIT = 227 * 1024;  // opt-in shared memory per block
 
-// MODE: 0 = single blocks; 1 = pairs of blocks sharing each B tile by TMA
-// multicast (each block still holds the whole B tile); 2 = pairs running
-// 256-row MMAs across both SMs (tcgen05 cta_group::2): each block holds its
-// 128 rows of A and half of the B tile.
+// MODE: 0 = single blocks; 2 = pairs running 256-row MMAs across both SMs
+// (tcgen05 cta_group::2): each block holds its 128 rows of A and half of the
+// B tile.
 template <int BN, bool B_MN, int MODE = 0>
 struct Cfg {
+  static_assert(MODE == 0 || MODE == 2, "kernel mode");
   // An MN-major B tile is stored as 64-wide swizzle atoms, so it is at least
   // one atom wide; the MMA reads only the first BN columns.
   static constexpr int B_COLS = B_MN ? (BN < 64 ? 64 : BN) : BN;
@@ -157,7 +157,7 @@ struct HParams {
   int fault_injection;
   int c_vec_ok;  // C base 16-byte aligned and ldc % 8 == 0
   int c_tma;     // C aligned: C leaves through TMA stores (and comes in by TMA loads)
-  int pair;      // 1: clusters of two blocks share each B tile (TMA multicast)
+  int pair;      // 2: clusters of two blocks run 2-SM (cta_group::2) MMAs; 0: single blocks
   // Tail split (only when splits == 1): units [0, dp_units) are whole tiles;
   // the remaining tiles are cut into tail_splits K slices of tail_k_slice, each
   // writing fp32 partials to tail_ws; per 32-row strip the last slice to
@@ -370,14 +370,11 @@ __global__ void __launch_bounds__(THREADS, 1)
   constexpr bool TWO_SM = MODE == 2;
   using C_ = Cfg<BN, B_MN, MODE>;
   constexpr int STAGES = C_::STAGES;
-  // bytes that complete one stage: this block's (single, multicast pair), or
-  // both blocks' (2-SM pair: all loads of the pair complete on the even
-  // block's barrier)
+  // bytes that complete one stage: this block's (single), or both blocks'
+  // (2-SM pair: all loads of the pair complete on the even block's barrier)
   constexpr uint32_t STAGE_TX = (uint32_t)C_::STAGE_BYTES * (TWO_SM ? 2u : 1u);
-  // Multicast pairs: each block of the cluster loads half of the B tile and
-  // multicasts it to both, so a stage is only free again once both blocks'
-  // MMAs have read it (two arrivals on `empty`).  2-SM pairs: the even block
-  // issues every MMA and its commits arrive on both blocks' barriers.
+  // 2-SM pairs: the even block issues every MMA and its commits arrive on
+  // both blocks' barriers.
   const int rank = PAIR ? (int)cluster_ctarank() : 0;
   const int worker = PAIR ? (int)(blockIdx.x >> 1) : (int)blockIdx.x;
   const int workers = PAIR ? (int)(gridDim.x >> 1) : (int)gridDim.x;
@@ -411,7 +408,7 @@ __global__ void __launch_bounds__(THREADS, 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(full_bar(s), 1);
-      mbar_init(empty_bar(s), MODE == 1 ? 2 : 1);
+      mbar_init(empty_bar(s), 1);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(accf_bar(b), 1);
@@ -434,7 +431,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     }
   }
   tc_fence_before();
-  if constexpr (PAIR) cluster_sync();  // the peer's barriers exist before any multicast
+  if constexpr (PAIR) cluster_sync();  // the peer's barriers exist before any remote arrive
   else __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
@@ -501,19 +498,7 @@ __global__ void __launch_bounds__(THREADS, 1)
             } else {
               tma_load_3d(sa, &tmA, k0, m0, za, full_bar(stage));
             }
-            if constexpr (MODE == 1) {
-              // this block's half of B, written into both blocks of the pair
-              if constexpr (B_MN) {
-                constexpr int ATOMS = C_::B_COLS / 64, MINE = ATOMS / 2;
-#pragma unroll
-                for (int h = rank * MINE; h < (rank + 1) * MINE; ++h)
-                  tma_load_3d_mc(sb + (uint32_t)h * 8192u, &tmB, n0 + 64 * h, k0, zb,
-                                 full_bar(stage), (uint16_t)3u);
-              } else {
-                tma_load_3d_mc(sb + (uint32_t)(rank * (BN / 2) * 128), &tmB, k0,
-                               n0 + rank * (BN / 2), zb, full_bar(stage), (uint16_t)3u);
-              }
-            } else if constexpr (B_MN) {
+            if constexpr (B_MN) {
 #pragma unroll
               for (int h = 0; h < C_::B_COLS / 64; ++h)
                 tma_load_3d(sb + (uint32_t)h * 8192u, &tmB, n0 + 64 * h, k0, zb, full_bar(stage));
@@ -572,7 +557,6 @@ __global__ void __launch_bounds__(THREADS, 1)
           }
           // buffer free once these MMAs finish (in both blocks of a pair)
           if constexpr (TWO_SM) tc_commit_pair_mc(empty_bar(stage), (uint16_t)3u);
-          else if constexpr (PAIR) tc_commit_mc(empty_bar(stage), (uint16_t)3u);
           else tc_commit(empty_bar(stage));
           if (++stage == STAGES) { stage = 0; phase ^= 1u; }
         }
@@ -923,8 +907,8 @@ __global__ void __launch_bounds__(THREADS, 1)
   }
 
   tc_fence_before();
-  // A pair leaves together: the peer's multicast copies and commit arrivals
-  // target this block's shared memory until both are done.
+  // A pair leaves together: the peer's copies and commit arrivals target
+  // this block's shared memory until both are done.
   if constexpr (PAIR) cluster_sync();
   else __syncthreads();
   if (warp == 1) {
@@ -1068,20 +1052,18 @@ template <typename T, int BN>
 cudaError_t launch_bn(const HgemmArgs& a, const HParams& p, LaunchCtx& ctx) {
   const bool A_MN = a.transA != 0, B_MN = a.transB == 0, split = a.splits > 1;
   constexpr bool CAN_PAIR = BN == 128 || BN == 256;
-  constexpr int M1 = CAN_PAIR ? 1 : 0, M2 = CAN_PAIR ? 2 : 0;
+  constexpr int M2 = CAN_PAIR ? 2 : 0;
   if constexpr (sizeof(T) == 4) {
     // TF32 operands are staged K-major only (the dispatcher packs them so)
     if (A_MN || B_MN) return cudaErrorInvalidValue;
     if (split) return launch_cfg<T, BN, false, false, true, 0>(a, p, ctx);
     if (CAN_PAIR && p.pair == 2) return launch_cfg<T, BN, false, false, false, M2>(a, p, ctx);
-    if (CAN_PAIR && p.pair == 1) return launch_cfg<T, BN, false, false, false, M1>(a, p, ctx);
     return launch_cfg<T, BN, false, false, false, 0>(a, p, ctx);
   } else {
 #define GB300_HG(AM, BMN)                                                   \
   if (A_MN == AM && B_MN == BMN) {                                          \
     if (split) return launch_cfg<T, BN, AM, BMN, true, 0>(a, p, ctx);       \
     if (CAN_PAIR && p.pair == 2) return launch_cfg<T, BN, AM, BMN, false, M2>(a, p, ctx); \
-    if (CAN_PAIR && p.pair == 1) return launch_cfg<T, BN, AM, BMN, false, M1>(a, p, ctx); \
     return launch_cfg<T, BN, AM, BMN, false, 0>(a, p, ctx);                 \
   }
   GB300_HG(false, true)

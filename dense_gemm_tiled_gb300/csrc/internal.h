@@ -64,7 +64,7 @@ struct HgemmArgs {
   float* partial;   // [splits][M][N] fp32 when splits > 1
   int num_sms;
   int bn;               // tile width: 32, 64, 128, 192 or 256
-  int pair;             // block pairs allowed: 0 none, 1 multicast B, 2 2-SM MMAs
+  int pair;             // block pairs allowed: 0 none, 2 2-SM (cta_group::2) MMAs
   int c_tma;            // allow TMA stores (and, beta != 0, TMA loads) of C when C is aligned
   int fault_injection;  // test hook: 1 = producer skips its first stage
   int dtype = 1;        // 1 fp16, 2 bf16, 3 fp32 on TF32 MMAs (gemm_dtype_t)
