@@ -45,6 +45,8 @@ _lib.gemm_set_fault_injection.argtypes = [_int]
 _lib.gemm_set_fault_injection.restype = None
 _lib.gemm_set_kernel_events.argtypes = [_vp, _vp]
 _lib.gemm_set_kernel_events.restype = None
+_lib.gemm_scratch_high_water.argtypes = [_int]
+_lib.gemm_scratch_high_water.restype = _i64
 
 F32 = 0
 F16_F32ACC = 1
@@ -91,6 +93,13 @@ def set_wait_timeout_ns(ns: int) -> None:
 
 def set_fault_injection(mode: int) -> None:
     _lib.gemm_set_fault_injection(int(mode))
+
+
+def scratch_high_water(reset: bool = False) -> int:
+    """Most bytes in use at once from the library's scratch pool on the
+    current device since the last reset (0: none taken); reset=True then
+    clears the mark."""
+    return _lib.gemm_scratch_high_water(1 if reset else 0)
 
 
 def set_kernel_events(start=None, end=None) -> None:

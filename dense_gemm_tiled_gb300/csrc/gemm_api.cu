@@ -216,14 +216,15 @@ bool c_scratch_wanted(const void* C, int64_t ldc, int64_t es, int M, int N) {
   return !aligned && c_tma_enabled() && (int64_t)M * N >= (1ll << 21);
 }
 
-// Switch for the fp16 tail split (env GEMM_GB300_HG_TAIL=1 turns it on).  Off
-// by default: measured on GB300 at 4096^3 and 8192^3 it was within noise of
-// the plain persistent grid (the last, partly idle round of tiles runs faster
-// per tile because fewer blocks share the L2-to-SM bandwidth).
-int tail_enabled() {
+// Stream-K schedule of the tensor-core kernel (env GEMM_GB300_HG_SK): 1
+// (default) shares out the K steps of a last, part-filled round of tiles when
+// that pays; 0 whole tiles only; 2 shares every tile (forces the shared-tile
+// path, for tests).
+int sk_mode() {
   static const int v = [] {
-    const char* e = getenv("GEMM_GB300_HG_TAIL");
-    return e ? atoi(e) : 0;
+    const char* e = getenv("GEMM_GB300_HG_SK");
+    const int m = e ? atoi(e) : 1;
+    return (m >= 0 && m <= 2) ? m : 1;
   }();
   return v;
 }
@@ -238,18 +239,26 @@ int forced_bn() {
   return v;
 }
 
+// Tile width of the tensor-core kernel for 16-bit operands: the dispatcher's
+// model, unless GEMM_GB300_HG_BN forces one (32 only for a K-major B with
+// N <= 32).
+int pick_bn16(int M, int N, int K, int transA, int transB, int sms, int batch, int skm) {
+  int bn = hgemm_pick_bn(M, N, K, transA, transB, HG_BK, batch, pair_enabled(), sms, skm);
+  const int forced = forced_bn();
+  if (forced == 32 ? (N <= 32 && transB)
+                   : (forced == 64 || forced == 128 || forced == 192 || forced == 256))
+    bn = forced;
+  return bn;
+}
+
 int cuda_fail(cudaError_t e) { return e == cudaErrorMemoryAllocation ? GEMM_ERR_NO_MEMORY : GEMM_ERR_CUDA; }
 
-// Split-K plan: how many K slices, each a multiple of `kstep` long.
-// Fewest K steps a split-K slice gets (compile-time knobs).  fp32: one (a
+// Split-K plan of the fp32 kernel: how many K slices, each a multiple of
+// `kstep` long.  Fewest K steps a slice gets (compile-time knob): one (a
 // 64-deep step of a 128 x 128 tile is ~1M FMAs), measured on small squares
-// against 2 and 4: 256^3 16 / 21 / 31 us, 512^3 18 / 23 / 33 us; fp16: four
-// (one or two measured 1-8 % slower from 256^3 to 1024^3).
+// against 2 and 4: 256^3 16 / 21 / 31 us, 512^3 18 / 23 / 33 us.
 #ifndef GB300_SG_SLICE_STEPS
 #define GB300_SG_SLICE_STEPS 1
-#endif
-#ifndef GB300_HG_SLICE_STEPS
-#define GB300_HG_SLICE_STEPS 4
 #endif
 
 void plan_splits(int64_t tiles, int64_t K, int kstep, int capacity, int min_steps_per_slice,
@@ -271,6 +280,21 @@ void plan_splits(int64_t tiles, int64_t K, int kstep, int capacity, int min_step
   const int64_t per = (steps + s - 1) / s;  // steps per slice
   *k_slice = (int)(per * kstep);
   *splits = (int)((steps + per - 1) / per);  // every slice non-empty
+}
+
+// fp32 tile and K split: N <= 32 takes the narrow tile (256 x 32, two blocks
+// per SM), split over K until one round of resident blocks is full; other
+// shapes the 128 x 128 tile, split when the tiles fill under half of two
+// rounds of the SMs.
+void plan_f32(int M, int N, int K, int sms, bool* narrow, int64_t* tiles, int* splits,
+              int* k_slice) {
+  *narrow = N <= SGN_BN && sg_narrow_enabled();
+  const int bm = *narrow ? SGN_BM : SG_BM, bn = *narrow ? SGN_BN : SG_BN;
+  *tiles = (int64_t)((M + bm - 1) / bm) * ((N + bn - 1) / bn);
+  if (*narrow)
+    plan_splits(*tiles, K, SGN_BK, sms * SGN_BLOCKS_PER_SM, 8, 16, splits, k_slice);
+  else
+    plan_splits(*tiles, K, SG_BK, 2 * sms, GB300_SG_SLICE_STEPS, 16, splits, k_slice);
 }
 
 // Scratch comes from a stream-ordered memory pool owned by the library, one
@@ -301,6 +325,8 @@ cudaError_t scratch_pool(cudaMemPool_t* out) {
   *out = g_pool[dev];
   return cudaSuccess;
 }
+
+inline size_t pad256(size_t n) { return (n + 255) / 256 * 256; }
 
 struct Scratch {
   void* ptr = nullptr;
@@ -337,72 +363,63 @@ int run_gemm(int transA, int transB, int64_t M64, int64_t N64, int64_t K64, int 
     // Opt-in TF32: the tcgen05 kernel on kind::tf32 reads K-major fp32
     // operands in 16-byte aligned rows, A [M, K] and B [N, K]; others are
     // transposed or re-pitched into scratch first.
-    int bn = hgemm_pick_bn(M, N, 1, sms);
-    const int64_t tiles = (int64_t)((M + HG_BM - 1) / HG_BM) * ((N + bn - 1) / bn);
-    int splits, k_slice;
-    plan_splits(tiles, K, 32, sms, 4, 32, &splits, &k_slice);
+    const int bn = hgemm_pick_bn(M, N, K, 0, 1, 32, 1, pair_enabled(), sms, sk_mode());
+    const HPlan pl = hgemm_plan(M, N, K, bn, 0, 1, 32, 1, pair_enabled(), sms, sk_mode());
     const bool a_ok = !transA && ((uintptr_t)A % 16) == 0 && (lda % 4) == 0;
     const bool b_ok = transB && ((uintptr_t)B % 16) == 0 && (ldb % 4) == 0;
     const int64_t ldk = (K + 3) / 4 * 4;
-    const size_t bytes_a = a_ok ? 0 : ((size_t)M * ldk * 4 + 255) / 256 * 256;
-    const size_t bytes_b = b_ok ? 0 : ((size_t)N * ldk * 4 + 255) / 256 * 256;
-    const size_t bytes_p = splits > 1 ? (size_t)splits * M * N * sizeof(float) : 0;
-    const bool c_scr = splits == 1 && c_scratch_wanted(C, ldc, 4, M, N);
+    const size_t bytes_a = a_ok ? 0 : pad256((size_t)M * ldk * 4);
+    const size_t bytes_b = b_ok ? 0 : pad256((size_t)N * ldk * 4);
+    const size_t bytes_w = pad256(pl.ws_bytes), bytes_n = pad256(pl.cnt_bytes);
+    const bool c_scr = c_scratch_wanted(C, ldc, 4, M, N);
     const int64_t ldc_p = (N + 3) / 4 * 4;
-    const size_t bytes_c = c_scr ? ((size_t)M * ldc_p * 4 + 255) / 256 * 256 : 0;
+    const size_t bytes_c = c_scr ? pad256((size_t)M * ldc_p * 4) : 0;
     Scratch ws;
-    if (bytes_a + bytes_b + bytes_p + bytes_c > 0) {
-      e = ws.get(bytes_a + bytes_b + bytes_p + bytes_c, stream);
+    const size_t total = bytes_a + bytes_b + bytes_w + bytes_n + bytes_c;
+    if (total > 0) {
+      e = ws.get(total, stream);
       if (e != cudaSuccess) return cuda_fail(e);
     }
-    void* Cd = C;
-    int64_t ldcd = ldc;
-    if (c_scr) {
-      Cd = (char*)ws.ptr + bytes_a + bytes_b + bytes_p;
-      ldcd = ldc_p;
-      if (beta != 0.f) e = launch_repack_32(M, N, C, ldc, Cd, ldc_p, ctx);
-      if (e != cudaSuccess) return cuda_fail(e);
-    }
+    char* wp = (char*)ws.ptr;
+    float* At = (float*)wp;
+    float* Bt = (float*)(wp + bytes_a);
+    float* sk_ws = (float*)(wp + bytes_a + bytes_b);
+    unsigned int* sk_cnt = (unsigned int*)(wp + bytes_a + bytes_b + bytes_w);
+    void* Cd = c_scr ? (void*)(wp + bytes_a + bytes_b + bytes_w + bytes_n) : C;
+    const int64_t ldcd = c_scr ? ldc_p : ldc;
+    if (c_scr && beta != 0.f) e = launch_repack_32(M, N, C, ldc, Cd, ldc_p, ctx);
+    if (e == cudaSuccess && pl.sk_workers > 0)
+      e = cudaMemsetAsync(sk_cnt, 0, pl.cnt_bytes, stream);
     const void* Ad = A;
     const void* Bd = B;
     int64_t ldad = lda, ldbd = ldb;
-    char* wp = (char*)ws.ptr;
-    if (!a_ok) {
-      float* dst = (float*)wp;
-      e = transA ? launch_transpose_f32(K, M, (const float*)A, lda, dst, ldk, ctx)
-                 : launch_repack_32(M, K, A, lda, dst, ldk, ctx);
-      Ad = dst; ldad = ldk; wp += bytes_a;
+    if (e == cudaSuccess && !a_ok) {
+      e = transA ? launch_transpose_f32(K, M, (const float*)A, lda, At, ldk, ctx)
+                 : launch_repack_32(M, K, A, lda, At, ldk, ctx);
+      Ad = At; ldad = ldk;
     }
     if (e == cudaSuccess && !b_ok) {
-      float* dst = (float*)wp;
-      e = !transB ? launch_transpose_f32(K, N, (const float*)B, ldb, dst, ldk, ctx)
-                  : launch_repack_32(N, K, B, ldb, dst, ldk, ctx);
-      Bd = dst; ldbd = ldk; wp += bytes_b;
+      e = !transB ? launch_transpose_f32(K, N, (const float*)B, ldb, Bt, ldk, ctx)
+                  : launch_repack_32(N, K, B, ldb, Bt, ldk, ctx);
+      Bd = Bt; ldbd = ldk;
     }
     if (e == cudaSuccess) {
-      const int pair = pair_enabled();
-      HgemmArgs a{0, 1, M, N, K, Ad, ldad, Bd, ldbd, Cd, ldcd, alpha, beta,
-                  splits, k_slice, splits > 1 ? (float*)wp : nullptr, sms, bn, pair,
+      HgemmArgs a{0, 1, M, N, K, Ad, ldad, Bd, ldbd, Cd, ldcd, alpha, beta, sms, bn,
                   c_tma_enabled(), g_fault_injection.load()};
       a.dtype = GEMM_F32_TF32;
-      if (splits == 1) a.ep = ep;  // split-K: the reduction applies it
-      path = splits > 1 ? GEMM_PATH_TC_SPLITK : GEMM_PATH_TC;
+      a.plan = pl;
+      a.sk_ws = sk_ws;
+      a.sk_cnt = sk_cnt;
+      a.ep = ep;
+      path = pl.sk_workers > 0 ? GEMM_PATH_TC_SPLITK : GEMM_PATH_TC;
       e = timed_hgemm(a, ctx);
-      if (e == cudaSuccess && splits > 1)
-        e = launch_splitk_reduce(0, M, N, splits, a.partial, C, ldc, alpha, beta, ctx, ep);
       if (e == cudaSuccess && c_scr) e = launch_copy_rows(4, M, N, Cd, ldc_p, C, ldc, ctx);
     }
   } else if (dtype == GEMM_F32) {
-    // N <= 32: the narrow tile (256 x 32, two blocks per SM), split over K
-    // until one round of resident blocks is full
-    const bool narrow = N <= SGN_BN && sg_narrow_enabled();
-    const int bm = narrow ? SGN_BM : SG_BM, bn = narrow ? SGN_BN : SG_BN;
-    const int64_t tiles = (int64_t)((M + bm - 1) / bm) * ((N + bn - 1) / bn);
+    bool narrow;
     int splits, k_slice;
-    if (narrow)
-      plan_splits(tiles, K, SGN_BK, sms * SGN_BLOCKS_PER_SM, 8, 16, &splits, &k_slice);
-    else
-      plan_splits(tiles, K, SG_BK, 2 * sms, GB300_SG_SLICE_STEPS, 16, &splits, &k_slice);
+    int64_t tiles;
+    plan_f32(M, N, K, sms, &narrow, &tiles, &splits, &k_slice);
     SgemmArgs a{transA, transB, M, N, K, (const float*)A, lda, (const float*)B, ldb, (float*)C,
                 ldc, alpha, beta, splits, k_slice, nullptr};
     a.narrow = narrow ? 1 : 0;
@@ -471,86 +488,56 @@ int run_gemm(int transA, int transB, int64_t M64, int64_t N64, int64_t K64, int 
     if (e == cudaSuccess && splits > 1)
       e = launch_splitk_reduce(0, M, N, splits, a.partial, C, ldc, alpha, beta, ctx, ep);
   } else {
-    int bn = hgemm_pick_bn(M, N, transB, sms);
-    const int forced = forced_bn();
-    if (forced == 32 ? (N <= 32 && transB) : (forced == 64 || forced == 128 || forced == 192 ||
-                                              forced == 256))
-      bn = forced;
-    const int64_t tiles = (int64_t)((M + HG_BM - 1) / HG_BM) * ((N + bn - 1) / bn);
-    int splits, k_slice;
-    plan_splits(tiles, K, HG_BK, sms, GB300_HG_SLICE_STEPS, 32, &splits, &k_slice);
+    const int bn = pick_bn16(M, N, K, transA, transB, sms, 1, sk_mode());
+    const HPlan pl = hgemm_plan(M, N, K, bn, transA, transB, HG_BK, 1, pair_enabled(), sms,
+                                sk_mode());
     // The tensor-memory-access unit needs 16-byte aligned bases and row
     // pitches; an operand that has neither is copied into padded scratch.
-    const void* Ad = A;
-    const void* Bd = B;
-    int64_t ldad = lda, ldbd = ldb;
     const bool a_ok = ((uintptr_t)A % 16) == 0 && (lda % 8) == 0;
     const bool b_ok = ((uintptr_t)B % 16) == 0 && (ldb % 8) == 0;
     const int64_t lda_p = (a_cols + 7) / 8 * 8, ldb_p = (b_cols + 7) / 8 * 8;
-    size_t bytes_a = a_ok ? 0 : (size_t)(a_rows * lda_p * 2 + 255) / 256 * 256;
-    size_t bytes_b = b_ok ? 0 : (size_t)(b_rows * ldb_p * 2 + 255) / 256 * 256;
-    size_t bytes_p = splits > 1 ? (size_t)splits * M * N * sizeof(float) : 0;
-    // tail split of the persistent grid's last round (needs its own partials)
-    const int pair = pair_enabled();
-    const bool use_pair = hgemm_use_pair(bn, M, splits, pair);
-    TailPlan tail{0, 0, 0, 0, 0};
-    if (splits == 1 && tail_enabled())
-      tail = hgemm_plan_tail(M, N, K, bn, use_pair,
-                             use_pair ? hgemm_pair_slots(bn, transA, transB, pair, sms) : sms);
-    const size_t bytes_t = tail.splits > 0 ? (tail.ws_bytes + 255) / 256 * 256 + tail.cnt_bytes : 0;
+    const size_t bytes_a = a_ok ? 0 : pad256((size_t)(a_rows * lda_p * 2));
+    const size_t bytes_b = b_ok ? 0 : pad256((size_t)(b_rows * ldb_p * 2));
+    const size_t bytes_w = pad256(pl.ws_bytes), bytes_n = pad256(pl.cnt_bytes);
     // C rows not 16-byte aligned: see c_scratch_wanted
-    const bool c_scr = splits == 1 && tail.splits == 0 && c_scratch_wanted(C, ldc, 2, M, N);
+    const bool c_scr = c_scratch_wanted(C, ldc, 2, M, N);
     const int64_t ldc_p = (N + 7) / 8 * 8;
-    const size_t bytes_c = c_scr ? ((size_t)M * ldc_p * 2 + 255) / 256 * 256 : 0;
+    const size_t bytes_c = c_scr ? pad256((size_t)M * ldc_p * 2) : 0;
     Scratch ws;
-    if (bytes_a + bytes_b + bytes_p + bytes_t + bytes_c > 0) {
-      e = ws.get(bytes_a + bytes_b + bytes_p + bytes_t + bytes_c, stream);
+    const size_t total = bytes_a + bytes_b + bytes_w + bytes_n + bytes_c;
+    if (total > 0) {
+      e = ws.get(total, stream);
       if (e != cudaSuccess) return cuda_fail(e);
     }
     char* wp = (char*)ws.ptr;
-    void* Cd = C;
-    int64_t ldcd = ldc;
-    if (c_scr) {
-      Cd = wp + bytes_a + bytes_b + bytes_p + bytes_t;
-      ldcd = ldc_p;
-      if (beta != 0.f) e = launch_repack_16(M, N, C, ldc, Cd, ldc_p, ctx);
-      if (e != cudaSuccess) return cuda_fail(e);
-    }
-    float* tail_ws = nullptr;
-    unsigned int* tail_cnt = nullptr;
-    if (tail.splits > 0) {
-      tail_ws = (float*)(wp + bytes_a + bytes_b + bytes_p);
-      tail_cnt = (unsigned int*)((char*)tail_ws + (tail.ws_bytes + 255) / 256 * 256);
-      e = cudaMemsetAsync(tail_cnt, 0, tail.cnt_bytes, stream);
-      if (e != cudaSuccess) return cuda_fail(e);
-    }
-    if (!a_ok) {
-      void* dst = wp;
-      e = launch_repack_16((int)a_rows, (int)a_cols, Ad, lda, dst, lda_p, ctx);
-      Ad = dst; ldad = lda_p; wp += bytes_a;
+    float* sk_ws = (float*)(wp + bytes_a + bytes_b);
+    unsigned int* sk_cnt = (unsigned int*)(wp + bytes_a + bytes_b + bytes_w);
+    void* Cd = c_scr ? (void*)(wp + bytes_a + bytes_b + bytes_w + bytes_n) : C;
+    const int64_t ldcd = c_scr ? ldc_p : ldc;
+    if (c_scr && beta != 0.f) e = launch_repack_16(M, N, C, ldc, Cd, ldc_p, ctx);
+    if (e == cudaSuccess && pl.sk_workers > 0)
+      e = cudaMemsetAsync(sk_cnt, 0, pl.cnt_bytes, stream);
+    const void* Ad = A;
+    const void* Bd = B;
+    int64_t ldad = lda, ldbd = ldb;
+    if (e == cudaSuccess && !a_ok) {
+      e = launch_repack_16((int)a_rows, (int)a_cols, A, lda, wp, lda_p, ctx);
+      Ad = wp; ldad = lda_p;
     }
     if (e == cudaSuccess && !b_ok) {
-      void* dst = wp;
-      e = launch_repack_16((int)b_rows, (int)b_cols, Bd, ldb, dst, ldb_p, ctx);
-      Bd = dst; ldbd = ldb_p; wp += bytes_b;
+      e = launch_repack_16((int)b_rows, (int)b_cols, B, ldb, wp + bytes_a, ldb_p, ctx);
+      Bd = wp + bytes_a; ldbd = ldb_p;
     }
     if (e == cudaSuccess) {
-      HgemmArgs a{transA, transB, M, N, K, Ad, ldad, Bd, ldbd, Cd, ldcd, alpha, beta,
-                  splits, k_slice, splits > 1 ? (float*)wp : nullptr, sms, bn, pair,
+      HgemmArgs a{transA, transB, M, N, K, Ad, ldad, Bd, ldbd, Cd, ldcd, alpha, beta, sms, bn,
                   c_tma_enabled(), g_fault_injection.load()};
       a.dtype = dtype;
-      if (splits == 1) a.ep = ep;  // split-K: the reduction applies it
-      if (tail.splits > 0) {
-        a.dp_units = tail.dp_units;
-        a.tail_splits = tail.splits;
-        a.tail_k_slice = tail.k_slice;
-        a.tail_ws = tail_ws;
-        a.tail_cnt = tail_cnt;
-      }
-      path = splits > 1 ? GEMM_PATH_TC_SPLITK : GEMM_PATH_TC;
+      a.plan = pl;
+      a.sk_ws = sk_ws;
+      a.sk_cnt = sk_cnt;
+      a.ep = ep;
+      path = pl.sk_workers > 0 ? GEMM_PATH_TC_SPLITK : GEMM_PATH_TC;
       e = timed_hgemm(a, ctx);
-      if (e == cudaSuccess && splits > 1)
-        e = launch_splitk_reduce(dtype, M, N, splits, a.partial, C, ldc, alpha, beta, ctx, ep);
       if (e == cudaSuccess && c_scr) e = launch_copy_rows(2, M, N, Cd, ldc_p, C, ldc, ctx);
     }
   }
@@ -767,16 +754,14 @@ int run_batched(int transA, int transB, int64_t M64, int64_t N64, int64_t K64, i
     const int64_t per_launch = tiles > 0 ? (int64_t)0x7fffffff / tiles : batch;
     for (int64_t b0 = 0; b0 < batch && e == cudaSuccess; b0 += per_launch) {
       const int nb = (int)(batch - b0 < per_launch ? batch - b0 : per_launch);
-      int bn = hgemm_pick_bn(M, N, transB, sms, nb);
-      const int forced = forced_bn();
-      if (forced == 32 ? (N <= 32 && transB) : (forced == 64 || forced == 128 || forced == 192 ||
-                                                forced == 256))
-        bn = forced;
+      const int bn = pick_bn16(M, N, K, transA, transB, sms, nb, 0);
       HgemmArgs a{transA, transB, M, N, K, Ab + b0 * sA * es, lda, Bb + b0 * sB * es, ldb,
-                  Cb + b0 * sC * es, ldc, alpha, beta, 1, 0, nullptr, sms, bn, pair_enabled(),
-                  c_tma_enabled(), g_fault_injection.load()};
+                  Cb + b0 * sC * es, ldc, alpha, beta, sms, bn, c_tma_enabled(),
+                  g_fault_injection.load()};
       a.dtype = dtype;
       a.batch = nb;
+      // whole tiles: the batch itself fills the grid
+      a.plan = hgemm_plan(M, N, K, bn, transA, transB, HG_BK, nb, pair_enabled(), sms, 0);
       a.stride_a = sA; a.stride_b = sB; a.stride_c = sC;
       e = timed_hgemm(a, ctx);
       // the driver refused the 3-D description (e.g. batch pitches that
@@ -996,6 +981,25 @@ const char* gemm_status_string(int status) {
 
 int gemm_version(void) { return (1 << 16) | 0; }
 
+int64_t gemm_scratch_high_water(int reset) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= MAX_DEVICES) return -1;
+  cudaMemPool_t pool;
+  {
+    std::lock_guard<std::mutex> lk(g_mu);
+    pool = g_pool[dev];
+  }
+  if (!pool) return 0;
+  cuuint64_t v = 0;
+  if (cudaMemPoolGetAttribute(pool, cudaMemPoolAttrUsedMemHigh, &v) != cudaSuccess) return -1;
+  if (reset) {
+    cuuint64_t zero = 0;
+    if (cudaMemPoolSetAttribute(pool, cudaMemPoolAttrUsedMemHigh, &zero) != cudaSuccess)
+      return -1;
+  }
+  return (int64_t)v;
+}
+
 int gemm_last_path(void) { return tl_last_path; }
 int gemm_last_launches(void) { return tl_last_launches; }
 int gemm_last_grid(void) { return tl_last_grid; }
@@ -1018,9 +1022,10 @@ void gemm_set_kernel_events(void* start, void* end) {
 // gemm_splitk_noalloc: the same product for callers that must not allocate
 // device memory, e.g. code running under an allocator that already owns the
 // whole device (a framework's caching allocator), or a host process whose
-// rules forbid runtime allocation once it is serving.  The split-K partial
-// sums, which gemm() takes from the stream-ordered allocator, live here in a
-// fixed array compiled into the library instead.
+// rules forbid runtime allocation once it is serving.  The partial sums that
+// gemm() keeps in memory from the stream-ordered allocator (the fp32 kernel's
+// K slices; the tensor-core kernel's shared tiles and their arrival counters)
+// live here in a fixed array compiled into the library instead.
 //
 // The array is a file-scope __device__ variable: every GPU that loads this
 // library holds it (GEMM_NOALLOC_SCRATCH_BYTES) until the process exits.  Host
@@ -1028,11 +1033,11 @@ void gemm_set_kernel_events(void* start, void* end) {
 // once per device with cudaGetSymbolAddress, with that device current, the
 // first time the entry point runs on it; that first call therefore makes a
 // runtime query and should come before any stream capture.  All calls share
-// the one array and it keeps whatever the last call left: every element a
-// call reads is written by the same call first (each K slice writes all of its
-// M x N partials before the reduction reads them), so nothing needs clearing,
-// but two calls that overlap on the GPU (different streams, no ordering
-// between them) race on it.
+// the one array and it keeps whatever the last call left: every partial sum a
+// call reads is written by the same call first, and the arrival counters,
+// which must start at zero, are cleared on the stream (cudaMemsetAsync, no
+// allocation) before each launch that uses them; two calls that overlap on
+// the GPU (different streams, no ordering between them) race on it.
 // ---------------------------------------------------------------------------
 #define GEMM_NOALLOC_SCRATCH_BYTES (8u << 20)
 
@@ -1081,14 +1086,18 @@ extern "C" int gemm_splitk_noalloc(int transA, int transB, int64_t M, int64_t N,
     path = GEMM_PATH_SCALE;
     e = launch_scale(dtype, Mi, Ni, C, ldc, beta, ctx);
   } else if (dtype == GEMM_F32) {
-    const int64_t tiles = (int64_t)((Mi + SG_BM - 1) / SG_BM) * ((Ni + SG_BN - 1) / SG_BN);
+    // gemm()'s tile and K split; without gemm()'s operand packing and
+    // stream-K launch on large problems, which take scratch
+    bool narrow;
     int splits, k_slice;
-    plan_splits(tiles, Ki, SG_BK, 2 * sms, 4, 16, &splits, &k_slice);
+    int64_t tiles;
+    plan_f32(Mi, Ni, Ki, sms, &narrow, &tiles, &splits, &k_slice);
     if (splits > 1 && (uint64_t)splits * (uint64_t)M * (uint64_t)N * sizeof(float) >
                           GEMM_NOALLOC_SCRATCH_BYTES)
       return GEMM_ERR_UNSUPPORTED;  // partial sums would not fit the fixed array
     SgemmArgs a{transA, transB, Mi, Ni, Ki, (const float*)A, lda, (const float*)B, ldb,
                 (float*)C, ldc, alpha, beta, splits, k_slice, splits > 1 ? scratch : nullptr};
+    a.narrow = narrow ? 1 : 0;
     path = splits > 1 ? GEMM_PATH_FFMA_SPLITK : GEMM_PATH_FFMA;
     e = timed_sgemm(a, ctx);
     if (e == cudaSuccess && splits > 1)
@@ -1098,28 +1107,28 @@ extern "C" int gemm_splitk_noalloc(int transA, int transB, int64_t M, int64_t N,
     // (16-byte aligned base and row pitch): padding them would need scratch.
     if (((uintptr_t)A % 16) != 0 || (lda % 8) != 0 || ((uintptr_t)B % 16) != 0 || (ldb % 8) != 0)
       return GEMM_ERR_UNSUPPORTED;
-    int bn = hgemm_pick_bn(Mi, Ni, transB, sms);
-    const int forced = forced_bn();
-    if (forced == 32 ? (Ni <= 32 && transB) : (forced == 64 || forced == 128 || forced == 192 ||
-                                               forced == 256))
-      bn = forced;
-    const int64_t tiles = (int64_t)((Mi + HG_BM - 1) / HG_BM) * ((Ni + bn - 1) / bn);
-    int splits, k_slice;
-    plan_splits(tiles, Ki, HG_BK, sms, 4, 32, &splits, &k_slice);
-    if (splits > 1 && (uint64_t)splits * (uint64_t)M * (uint64_t)N * sizeof(float) >
-                          GEMM_NOALLOC_SCRATCH_BYTES)
-      return GEMM_ERR_UNSUPPORTED;  // partial sums would not fit the fixed array
-    HgemmArgs a{transA, transB, Mi, Ni, Ki, A, lda, B, ldb, C, ldc, alpha, beta, splits,
-                k_slice, splits > 1 ? scratch : nullptr, sms, bn, pair_enabled(),
+    // gemm()'s tile width and schedule; shared tiles' partial sums and
+    // counters in the fixed array when they fit, else whole tiles only
+    const int bn = pick_bn16(Mi, Ni, Ki, transA, transB, sms, 1, sk_mode());
+    HPlan pl = hgemm_plan(Mi, Ni, Ki, bn, transA, transB, HG_BK, 1, pair_enabled(), sms,
+                          sk_mode());
+    if (pad256(pl.ws_bytes) + pl.cnt_bytes > GEMM_NOALLOC_SCRATCH_BYTES)
+      pl = hgemm_plan(Mi, Ni, Ki, bn, transA, transB, HG_BK, 1, pair_enabled(), sms, 0);
+    unsigned int* cnt = reinterpret_cast<unsigned int*>(
+        reinterpret_cast<char*>(scratch) + pad256(pl.ws_bytes));
+    if (pl.sk_workers > 0) e = cudaMemsetAsync(cnt, 0, pl.cnt_bytes, stream);
+    HgemmArgs a{transA, transB, Mi, Ni, Ki, A, lda, B, ldb, C, ldc, alpha, beta, sms, bn,
                 c_tma_enabled(), g_fault_injection.load()};
     a.dtype = dtype;
-    path = splits > 1 ? GEMM_PATH_TC_SPLITK : GEMM_PATH_TC;
-    e = timed_hgemm(a, ctx);
-    if (e == cudaSuccess && splits > 1)
-      e = launch_splitk_reduce(dtype, Mi, Ni, splits, scratch, C, ldc, alpha, beta, ctx);
+    a.plan = pl;
+    a.sk_ws = scratch;
+    a.sk_cnt = cnt;
+    path = pl.sk_workers > 0 ? GEMM_PATH_TC_SPLITK : GEMM_PATH_TC;
+    if (e == cudaSuccess) e = timed_hgemm(a, ctx);
   }
   g_total_launches += ctx.launches;
   tl_last_launches = ctx.launches;
+  tl_last_grid = ctx.grid;
   if (e != cudaSuccess) return cuda_fail(e);
   tl_last_path = path;
   return GEMM_OK;

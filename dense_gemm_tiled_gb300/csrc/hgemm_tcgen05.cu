@@ -1,10 +1,10 @@
 // fp16 instantiation of the tcgen05 GEMM (hgemm_tcgen05.cuh) and the
-// dispatcher's planning functions: tile width, block pairs, tail split.
+// dispatcher's planning functions: tile width, block pairs, schedule.
 #include "hgemm_tcgen05.cuh"
 
 namespace gb300 {
 
-int hgemm_pair_slots(int bn, int transA, int transB, int mode, int num_sms) {
+int hgemm_pair_slots(int bn, int transA, int transB, int num_sms) {
   const bool A_MN = transA != 0, B_MN = transB == 0;
 #define GB300_SLOTS(W, AM, BMN)                                                              \
   if (bn == W && A_MN == AM && B_MN == BMN)                                                  \
@@ -16,61 +16,137 @@ int hgemm_pair_slots(int bn, int transA, int transB, int mode, int num_sms) {
   return num_sms / 2;
 }
 
-// Pairs of blocks share B tiles when the tile is 128 or 256 wide, there are at
-// least two tile rows, and K is not split (the split-K path keeps single
-// blocks).
-bool hgemm_use_pair(int bn, int M, int splits, int allowed) {
-  return allowed && (bn == 128 || bn == 256) && (M + BM - 1) / BM >= 2 && splits == 1;
+// Pairs of blocks run 2-SM MMAs when the tile is 128 or 256 wide and there
+// are at least two tile rows.
+bool hgemm_use_pair(int bn, int M, int allowed) {
+  return allowed == 2 && (bn == 128 || bn == 256) && (M + BM - 1) / BM >= 2;
 }
 
-// Tail split for the persistent grid (no split-K): with `workers` blocks (or
-// pairs) taking units round-robin, the last round holds units % workers tiles.
-// When that is at most half the workers, those tiles are cut into K slices so
-// that the last round spreads over all workers.
-TailPlan hgemm_plan_tail(int M, int N, int K, int bn, bool pair, int workers) {
-  TailPlan t{0, 0, 0, 0, 0};
+// Fewest K steps a stream-K range gets; most ranges that share one tile; and
+// what finishing shared tiles costs, in K steps of the busiest worker:
+// publishing partial sums, and the last contributor reading them back and
+// adding them before its store (compile-time knobs).  Measured on GB300 with
+// fp16: for 2-SM pairs of 256-wide tiles, sharing that shortens the busiest
+// worker by 14 K steps loses (512 x 5632 x 2048: 21 -> 33 us), by 40 gains
+// nothing (4096^3), by 66 still loses a little (512 x 2048 x 5632: 35.5 ->
+// 36.5 us) and by 96 gains (1024 x 1024 x 8192: 45.7 -> 39.6 us); single
+// 64-wide tiles, whose partial sums are a quarter the size, gain from 24
+// steps up (512 x 32 x 2048: 17.0 -> 16.1 us; 512 x 32 x 5632: 31.4 -> 22.3
+// us).
+#ifndef GB300_HG_SK_MIN_STEPS
+#define GB300_HG_SK_MIN_STEPS 4
+#endif
+#ifndef GB300_HG_SK_MAX_CONTRIB
+#define GB300_HG_SK_MAX_CONTRIB 5
+#endif
+#ifndef GB300_HG_SK_COST_WIDE
+#define GB300_HG_SK_COST_WIDE 72
+#endif
+#ifndef GB300_HG_SK_COST_NARROW
+#define GB300_HG_SK_COST_NARROW 16
+#endif
+
+// K steps a stream-K plan adds for finishing shared tiles (0 without).
+int sk_cost_steps(const HPlan& pl) {
+  if (pl.sk_workers == 0) return 0;
+  return pl.bn <= 64 ? GB300_HG_SK_COST_NARROW : GB300_HG_SK_COST_WIDE;
+}
+
+// K steps the busiest worker of a plan runs.
+int64_t busiest_steps(const HPlan& pl) {
+  int64_t s = (int64_t)((pl.dp_tiles + pl.workers - 1) / pl.workers) * pl.steps;
+  if (pl.sk_workers > 0) s += (pl.sk_steps + pl.sk_workers - 1) / pl.sk_workers;
+  return s;
+}
+
+HPlan hgemm_plan(int M, int N, int K, int bn, int transA, int transB, int kstep, int batch,
+                 int pair_allowed, int num_sms, int sk_mode) {
+  HPlan pl;
+  pl.bn = bn;
   const int tiles_m = (M + BM - 1) / BM, tiles_n = (N + bn - 1) / bn;
-  const int units = (pair ? (tiles_m + 1) / 2 : tiles_m) * tiles_n;
-  const int full = units / workers, rem = units % workers;
-  const int nkb = (K + BK - 1) / BK;
-  if (workers <= 0 || full == 0 || rem == 0 || rem * 2 > workers || nkb < 8) return t;
-  int sp = workers / rem;
-  if (sp > nkb / 4) sp = nkb / 4;
-  if (sp > 8) sp = 8;
-  if (sp < 2) return t;
-  const int per = (nkb + sp - 1) / sp;
-  t.splits = (nkb + per - 1) / per;
-  if (t.splits < 2) { t.splits = 0; return t; }
-  t.k_slice = per * BK;
-  t.dp_units = full * workers;
-  const int halves = pair ? 2 : 1;
-  t.ws_bytes = (size_t)rem * halves * t.splits * BM * bn * sizeof(float);
-  // one counter per 32-row strip and epilogue column share (at most two)
-  t.cnt_bytes = (size_t)rem * halves * 4 * 2 * sizeof(unsigned int);
-  return t;
+  const bool pair = hgemm_use_pair(bn, M, pair_allowed);
+  pl.pair = pair ? 2 : 0;
+  const int64_t rows = pair ? (tiles_m + 1) / 2 : tiles_m;
+  const int64_t nb = batch > 1 ? batch : 1;
+  const int64_t tiles = rows * tiles_n * nb;
+  const int steps = (K + kstep - 1) / kstep;
+  const int wmax = pair ? hgemm_pair_slots(bn, transA, transB, num_sms) : num_sms;
+  pl.tiles = (int)tiles;
+  pl.steps = steps > 0 ? steps : 1;
+  pl.dp_tiles = (int)tiles;
+  pl.workers = (int)(tiles < wmax ? tiles : wmax);
+  if (sk_mode != 0 && nb == 1 && tiles > 0 && steps >= 2 * GB300_HG_SK_MIN_STEPS) {
+    // Tiles of the last, part-filled round are shared, together with the
+    // round before it when there is one: every range then spans at least a
+    // tile, so a shared tile has two contributors -- one range's first unit
+    // (early) and the previous range's last (late), which finds the other's
+    // partial sums waiting.  Mode 2 shares every tile.
+    const int64_t rem = tiles % wmax;
+    int64_t shared = rem == 0 ? 0 : (tiles >= 2 * (int64_t)wmax ? rem + wmax : tiles);
+    if (sk_mode == 2) shared = tiles;
+    const int64_t total = shared * steps;
+    int64_t skw = total / GB300_HG_SK_MIN_STEPS;
+    if (skw > wmax) skw = wmax;
+    // at most GB300_HG_SK_MAX_CONTRIB ranges meet in a tile
+    const int64_t cap = shared * (GB300_HG_SK_MAX_CONTRIB - 1);
+    if (skw > cap) skw = cap;
+    // (positions up to skw * total must fit 64 bits; every range non-empty)
+    if (shared > 0 && skw >= 2 && total < ((int64_t)1 << 40)) {
+      HPlan sk = pl;
+      sk.dp_tiles = (int)(tiles - shared);
+      sk.sk_workers = (int)skw;
+      sk.sk_steps = total;
+      sk.workers = sk.dp_tiles > 0 ? wmax : (int)skw;
+      const int P = pair ? 2 : 1;
+      sk.ws_bytes = (size_t)skw * 2 * P * BM * bn * sizeof(float);
+      sk.cnt_bytes = (size_t)shared * P * 4 * EPI_HALVES * sizeof(unsigned int);
+      // shared only where the busiest worker saves more than finishing the
+      // shared tiles costs
+      if (sk_mode == 2 || busiest_steps(sk) + sk_cost_steps(sk) < busiest_steps(pl)) pl = sk;
+    }
+  }
+  // Epilogue warps per accumulator quarter.  The epilogue of one unit is
+  // bound by its warps' issue latency (about 1 us per 32 x 64 block a warp
+  // stores, measured on GB300), which the next unit's main loop hides except
+  // after a worker's last unit, where it adds to the launch: both shares of
+  // warps drain it when units are short (<= GB300_HG_EPI2_STEPS K steps)
+  // (4096 x 4096 x 128 fp16: 23.2 -> 19-21 us with both).
+#ifndef GB300_HG_EPI2_STEPS
+#define GB300_HG_EPI2_STEPS 8
+#endif
+  int64_t unit_steps = pl.steps;
+  if (pl.sk_workers > 0) {
+    const int64_t per = (pl.sk_steps + pl.sk_workers - 1) / pl.sk_workers;
+    if (per < unit_steps) unit_steps = per;
+  }
+  // (a 32-wide tile is one 32-column chunk: nothing to share)
+  pl.epi_halves =
+      (EPI_HALVES > 1 && unit_steps <= GB300_HG_EPI2_STEPS && bn >= 64) ? EPI_HALVES : 1;
+  return pl;
 }
 
-int hgemm_pick_bn(int M, int N, int transB, int num_sms, int batch) {
+int hgemm_pick_bn(int M, int N, int K, int transA, int transB, int kstep, int batch,
+                  int pair_allowed, int num_sms, int sk_mode) {
   // An MN-major B (transB == 0) is staged in 64-column swizzle atoms, so its
   // narrowest tile is 64 columns; a K-major B can go down to 32.
   if (N <= 32 && transB) return 32;
   if (N <= 64) return 64;
   if (N <= 128) return 128;
-  // Wider N: the persistent grid runs ceil(tiles / SMs) rounds of tiles.  A
-  // round of 128 x BN tiles costs, relative to BN = 256 and measured on GB300
-  // at 4096^3 with 2-SM pairs: 0.85 (BN 128), 0.92 (BN 192), 1.0 (BN 256) --
-  // narrower tiles re-read A more often per flop.  Pick the cheapest; ties go
-  // to the wider tile.
-  // (a strided batch multiplies the tile count: its entries share the rounds)
-  const int64_t tm = (int64_t)((M + BM - 1) / BM) * (batch > 1 ? batch : 1);
+  // Wider N: the launch takes as long as its busiest worker, which runs
+  // ceil(whole tiles / workers) tiles of `steps` K steps plus its stream-K
+  // range (and the finishing of shared tiles).  A K step of a 128 x BN tile
+  // costs, relative to BN = 256 and measured on GB300 at 4096^3 with 2-SM
+  // pairs: 0.85 (BN 128), 0.92 (BN 192), 1.0 (BN 256) -- narrower tiles
+  // re-read A more often per flop.  Pick the cheapest; ties go to the wider
+  // tile.
   const int widths[3] = {256, 192, 128};
-  const double round_cost[3] = {1.0, 0.92, 0.85};
+  const double step_cost[3] = {1.0, 0.92, 0.85};
   int best = 256;
   double best_cost = -1.0;
   for (int w = 0; w < 3; ++w) {
-    const int64_t tiles = tm * ((N + widths[w] - 1) / widths[w]);
-    const int64_t rounds = (tiles + num_sms - 1) / num_sms;
-    const double cost = (double)rounds * round_cost[w];
+    const HPlan pl = hgemm_plan(M, N, K, widths[w], transA, transB, kstep, batch, pair_allowed,
+                                num_sms, sk_mode);
+    const double cost = (double)(busiest_steps(pl) + sk_cost_steps(pl)) * step_cost[w];
     if (best_cost < 0.0 || cost < best_cost - 1e-9) { best = widths[w]; best_cost = cost; }
   }
   return best;

@@ -32,7 +32,12 @@
 //  * The 128 x BN fp32 accumulator lives in tensor memory, double buffered,
 //    so the epilogue of one tile overlaps the main loop of the next.
 //  * Fused epilogue: tcgen05.ld -> alpha * acc + beta * C_old -> fp16
-//    (round to nearest even) -> global; or raw fp32 partial sums (split-K).
+//    (round to nearest even) -> TMA store through swizzled staging.
+//  * Schedule: whole tiles round-robin over the persistent grid, optionally
+//    followed by stream-K -- the K steps of the last tiles shared out in equal
+//    contiguous ranges, a tile shared by several ranges finished by its last
+//    contributor from the others' fp32 partial sums (section 5's split-K,
+//    with the reduction inside the GEMM kernel and no waiting between blocks).
 //
 // Every mbarrier wait is bounded (see common.cuh); on expiry the block stops
 // issuing work, drains its in-flight copies and MMAs, frees its tensor memory
@@ -128,7 +133,7 @@ struct Cfg {
   // Four epilogue warps take two each when that costs no pipeline stage, else
   // one; eight warps (both column shares, for short-K tiles) take one each and
   // are allowed only where that costs no stage either (EPI2).
-  static constexpr int FIXED_BYTES = 1024 /*align*/ + 256 /*barriers*/;
+  static constexpr int FIXED_BYTES = 1024 /*align*/ + 512 /*barriers*/;
   static constexpr int STAGES_OF(int staging) {
     return (SMEM_LIMIT - FIXED_BYTES - staging) / STAGE_BYTES;
   }
@@ -141,37 +146,52 @@ struct Cfg {
   // two accumulator buffers of BN fp32 columns, rounded up to a power of two
   static constexpr int TMEM_COLS = 2 * BN <= 64 ? 64 : 2 * BN <= 128 ? 128 : 2 * BN <= 256 ? 256 : 512;
   static constexpr int SMEM_BYTES =
-      STAGES * STAGE_BYTES + STAGING_BYTES + 1024 /*align*/ + 256 /*barriers*/;
+      STAGES * STAGE_BYTES + STAGING_BYTES + FIXED_BYTES;
 };
 
 struct HParams {
-  void* C;  // __half or __nv_bfloat16, per the kernel's element type
-  float* partial;
+  void* C;  // __half, __nv_bfloat16 or float, per the kernel's element type
   int64_t ldc;
   int M, N, K;
-  int k_slice;
-  int tiles_m, tiles_n, splits;
+  int tiles_m, tiles_n;  // 128-row tiles and BN-column tiles of one matrix
+  // Work tiles: one per (batch entry, row of tiles -- a row of tile pairs
+  // with pairs --, column of tiles), `steps` K steps of kblk each.
+  int tiles, steps;
+  // Schedule (a persistent grid of W workers: blocks, or block pairs):
+  //  * tiles [0, dp_tiles) are whole units, worker w taking w, w + W, ...;
+  //  * the K steps of the other tiles, (tiles - dp_tiles) * steps of them in
+  //    tile-major order, are cut into sk_workers contiguous ranges of (almost)
+  //    equal length, worker w < sk_workers taking range w (stream-K).  A range
+  //    covers the end of one tile, whole tiles, and the start of another; a
+  //    tile covered by one range is stored as usual, a tile shared by several
+  //    ranges is finished by whichever contributor arrives last (below).
+  int dp_tiles, sk_workers;
+  int64_t sk_steps;
+  // floor((2^64 - 1) / d) for d = sk_workers, sk_steps, steps (div_magic)
+  uint64_t m_skw, m_sks, m_steps;
+  // Shared tiles: each contributing range writes its fp32 partial sums to its
+  // slot of sk_ws -- [sk_workers][2: the range's first / last tile][pair ? 2 :
+  // 1][4 lane quarters][32 x BN], each quarter's strip laid out as one warp
+  // holds it ([32-column chunk][float4][lane]) -- then counts itself in
+  // sk_cnt[shared tile][pair ? 2 : 1][4][EPI_HALVES] (zero at launch); the
+  // last to count sums every contributor's slot in K order, runs the epilogue
+  // and puts the counter back to zero.  No block waits for another.
+  float* sk_ws;
+  unsigned int* sk_cnt;
   float alpha, beta;
   unsigned int* status;
   uint64_t timeout_ns;
   int fault_injection;
-  int c_vec_ok;  // C base 16-byte aligned and ldc % 8 == 0
+  int c_vec_ok;  // C base 16-byte aligned and ldc % (16 / element size) == 0
   int c_tma;     // C aligned: C leaves through TMA stores (and comes in by TMA loads)
   int pair;      // 2: clusters of two blocks run 2-SM (cta_group::2) MMAs; 0: single blocks
-  // Tail split (only when splits == 1): units [0, dp_units) are whole tiles;
-  // the remaining tiles are cut into tail_splits K slices of tail_k_slice, each
-  // writing fp32 partials to tail_ws; per 32-row strip the last slice to
-  // arrive (tail_cnt) sums all slices in slice order and runs the epilogue.
-  int dp_units, tail_splits, tail_k_slice;
-  // strided batch: units run over batch x tiles (no K split, no tail split);
-  // the tensor maps carry the batch as their third coordinate
+  // strided batch: the tensor maps carry the batch entry as their third
+  // coordinate
   int batch;
   int64_t stride_c;  // elements between consecutive C matrices
   int za_mask, zb_mask;  // -1: operand batched; 0: one matrix shared by all (pitch 0)
   Epilogue ep;           // bias (output type, per column) and activation
   int epi_halves;        // epilogue warps in use per accumulator quarter: 1 or EPI_HALVES
-  float* tail_ws;          // [tail tiles][pair ? 2 : 1][tail_splits][4 warps][32 x BN]
-  unsigned int* tail_cnt;  // [tail tiles][pair ? 2 : 1][4], zero on entry and on exit
 };
 
 // tcgen05 shared-memory matrix descriptor, 128-byte swizzle:
@@ -198,54 +218,76 @@ __device__ __forceinline__ constexpr uint32_t make_idesc() {
          ((B_MN ? 1u : 0u) << 16) | ((uint32_t)(BN >> 3) << 17) | ((uint32_t)(M_ROWS >> 4) << 24);
 }
 
-// Work unit u -> tile, K range, slice.  Without pairs a tile is 128 x BN;
-// with pairs (a cluster of two blocks sharing B) a unit covers two vertically
-// adjacent tiles and block `rank` of the pair takes tile row 2 * pair_row + rank.
-//  * split-K launches: unit = slice z of tile t, u = z * tiles + t;
-//  * tail split: units below dp_units are whole tiles; unit dp_units + v is
-//    slice v / tail_tiles of tail tile v % tail_tiles (`tail` >= 0);
-//  * otherwise: unit = whole tile.
-template <bool PAIR, int KB = BK>
-__device__ __forceinline__ void unit_coords(int u, const HParams& p, int rank, int& m0, int& tn,
-                                            int& kbeg, int& nkb, int& z, int& tail, int& bz) {
-  const int rows = PAIR ? (p.tiles_m + 1) / 2 : p.tiles_m;
-  const int tiles = rows * p.tiles_n;
-  int t, ks;
-  tail = -1;
-  if (p.tail_splits > 0 && u >= p.dp_units) {
-    const int tail_tiles = tiles - p.dp_units;
-    const int v = u - p.dp_units;
-    tail = v % tail_tiles;
-    z = v / tail_tiles;
-    t = p.dp_units + tail;
-    ks = p.tail_k_slice;
+// One unit of a worker's work: this block's 128 rows of a tile (from m0),
+// its columns from n0, batch entry bz, K steps [kb0, kb0 + nkb).  sk >= 0
+// marks a shared tile (stream-K tile sk, counted from dp_tiles) whose partial
+// sums from this range go to the range's slot `slot`.  Without pairs a tile is
+// 128 x BN; with pairs a tile is two vertically adjacent 128-row tiles and
+// block `rank` of the pair takes tile row 2 * pair_row + rank.
+struct Unit {
+  int m0, n0, bz, kb0, nkb, sk, slot;
+};
+
+// First stream-K step of range w (range w is [sk_begin(w), sk_begin(w + 1))).
+__device__ __forceinline__ int64_t sk_begin(const HParams& p, int w) {
+  return (int64_t)div_magic((uint64_t)w * (uint64_t)p.sk_steps, (uint64_t)p.sk_workers, p.m_skw);
+}
+// The range that holds stream-K step x: the largest w with sk_begin(w) <= x.
+__device__ __forceinline__ int sk_owner(const HParams& p, int64_t x) {
+  return (int)div_magic((uint64_t)(x + 1) * (uint64_t)p.sk_workers - 1u, (uint64_t)p.sk_steps,
+                        p.m_sks);
+}
+// Slot of range w in shared tile sk: 0 if the range starts in the tile (it is
+// the range's first tile), 1 if it started before (its last).
+// (sk_begin(w) >= s0 exactly when w * sk_steps >= s0 * sk_workers)
+__device__ __forceinline__ int sk_slot(const HParams& p, int w, int64_t s0) {
+  return (int64_t)w * p.sk_steps >= s0 * p.sk_workers ? 0 : 1;
+}
+
+// Unit i of worker w (of W); false when the worker has no unit i.  Every role
+// of the block walks the same sequence: the worker's whole tiles first, then
+// the tiles its stream-K range touches, in K order.
+template <bool PAIR, int TBN>
+__device__ __forceinline__ bool unit_at(const HParams& p, int w, int W, int i, int rank,
+                                        Unit& u) {
+  const int n_dp = w < p.dp_tiles ? (p.dp_tiles - 1 - w) / W + 1 : 0;
+  int t;
+  u.kb0 = 0;
+  u.nkb = p.steps;
+  u.sk = -1;
+  u.slot = 0;
+  if (i < n_dp) {
+    t = w + i * W;
   } else {
-    z = u / tiles;
-    t = u - z * tiles;
-    ks = p.k_slice;
+    if (w >= p.sk_workers) return false;
+    const int64_t b = sk_begin(p, w), e = sk_begin(p, w + 1);
+    const int64_t tr = (int64_t)div_magic((uint64_t)b, (uint64_t)p.steps, p.m_steps) + (i - n_dp);
+    const int64_t s0 = tr * p.steps;
+    const int64_t lo = b > s0 ? b : s0;
+    const int64_t hi = e < s0 + p.steps ? e : s0 + p.steps;
+    if (hi <= lo) return false;
+    u.kb0 = (int)(lo - s0);
+    u.nkb = (int)(hi - lo);
+    if (u.nkb < p.steps) {
+      u.sk = (int)tr;
+      u.slot = b >= s0 ? 0 : 1;  // the range's first tile, or its last
+    }
+    t = p.dp_tiles + (int)tr;
   }
-  // a batched launch has no K split: the outer index is the batch entry
-  bz = 0;
-  if (p.batch > 1) {
-    bz = z;
-    z = 0;
-  }
+  // tile t -> batch entry, then grouped rasterisation within the entry
+  const int rows = PAIR ? (p.tiles_m + 1) / 2 : p.tiles_m;
+  const int per_entry = rows * p.tiles_n;
+  u.bz = t / per_entry;
+  t -= u.bz * per_entry;
   const int per_group = GROUP_M * p.tiles_n;
   const int first_m = (t / per_group) * GROUP_M;
   const int gsize = min(rows - first_m, GROUP_M);
   const int tr = first_m + (t % per_group) % gsize;
-  tn = (t % per_group) / gsize;
+  const int tn = (t % per_group) / gsize;
   const int tm = PAIR ? 2 * tr + rank : tr;
-  m0 = tm * BM;
-  kbeg = z * ks;
-  const int kend = min(p.K, kbeg + ks);
-  nkb = (kend - kbeg + KB - 1) / KB;
-}
-
-__device__ __forceinline__ int total_units(const HParams& p, bool pair) {
-  const int tiles = (pair ? (p.tiles_m + 1) / 2 : p.tiles_m) * p.tiles_n;
-  if (p.tail_splits > 0) return p.dp_units + (tiles - p.dp_units) * p.tail_splits;
-  return tiles * p.splits * (p.batch > 1 ? p.batch : 1);
+  u.m0 = tm * BM;
+  u.n0 = tn * TBN;
+  return true;
 }
 
 // act(alpha * v + beta * C + bias) -> T (RN-even) -> C, for 32 columns of one
@@ -361,7 +403,7 @@ __device__ __forceinline__ void store_c32_staged(const HParams& p, int bz, int g
   __syncwarp();  // the buffer is rewritten by the next block
 }
 
-template <typename T, int BN, bool A_MN, bool B_MN, bool SPLIT, int MODE>
+template <typename T, int BN, bool A_MN, bool B_MN, int MODE>
 __global__ void __launch_bounds__(THREADS, 1)
     hgemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
                     const __grid_constant__ CUtensorMap tmB,
@@ -398,8 +440,11 @@ __global__ void __launch_bounds__(THREADS, 1)
   uint32_t* const tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * STAGES + 5);
   // ... then one per C staging buffer: its TMA load of C (beta != 0) completed
   constexpr int NSTAGING = C_::STAGING_BYTES / 4096;
-  static_assert(8 * (2 * STAGES + 6 + NSTAGING) <= 256, "barrier area");
+  static_assert(8 * (2 * STAGES + 6 + NSTAGING + EPI_WARPS) <= 512, "barrier area");
   auto cload_bar = [&](int b) { return bar0 + 8u * (uint32_t)(2 * STAGES + 6 + b); };
+  // ... then one per epilogue warp: its bulk loads of shared-tile partial
+  // sums (into the stage ring, once the ring is idle) completed
+  auto fix_bar = [&](int w) { return bar0 + 8u * (uint32_t)(2 * STAGES + 6 + NSTAGING + w); };
   volatile uint32_t* const abort_flag = tmem_slot + 1;
 
   const int warp = threadIdx.x >> 5;
@@ -418,6 +463,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     }
     mbar_init(drain_bar, 1);
     for (int b = 0; b < NSTAGING; ++b) mbar_init(cload_bar(b), 1);
+    for (int w = 0; w < EPI_WARPS; ++w) mbar_init(fix_bar(w), 1);
     *abort_flag = 0u;
     fence_mbar_init();
   }
@@ -441,7 +487,6 @@ __global__ void __launch_bounds__(THREADS, 1)
   pdl_trigger();
 
   const WaitCtl wc{p.status, abort_flag, p.timeout_ns};
-  const int n_units = total_units(p, PAIR);
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
@@ -453,14 +498,13 @@ __global__ void __launch_bounds__(THREADS, 1)
       uint32_t pending = 0, pend_phase = 0;  // per-stage: last load issued / its parity
       bool first = true;
       bool ok = true;
-      for (int u = worker; u < n_units && ok; u += workers) {
-        int m0, tn, kbeg, nkb, z, tail, bz;
-        unit_coords<PAIR, kblk<T>()>(u, p, rank, m0, tn, kbeg, nkb, z, tail, bz);
-        const int za = bz & p.za_mask, zb = bz & p.zb_mask;
-        const int n0 = tn * BN;
-        for (int kb = 0; kb < nkb; ++kb) {
+      Unit U;
+      for (int i = 0; ok && unit_at<PAIR, BN>(p, worker, workers, i, rank, U); ++i) {
+        const int m0 = U.m0, n0 = U.n0;
+        const int za = U.bz & p.za_mask, zb = U.bz & p.zb_mask;
+        for (int kb = 0; kb < U.nkb; ++kb) {
           if (!mbar_wait(empty_bar(stage), phase ^ 1u, wc)) { ok = false; break; }
-          const int k0 = kbeg + kb * kblk<T>();
+          const int k0 = (U.kb0 + kb) * kblk<T>();
           const bool skip = first && p.fault_injection == 1;
           first = false;
           if (!skip && TWO_SM) {
@@ -526,9 +570,9 @@ __global__ void __launch_bounds__(THREADS, 1)
       uint32_t phase = 0;
       int it = 0;
       bool ok = true;
-      for (int u = worker; u < n_units && ok; u += workers, ++it) {
-        int m0, tn, kbeg, nkb, z, tail, bz;
-        unit_coords<PAIR, kblk<T>()>(u, p, rank, m0, tn, kbeg, nkb, z, tail, bz);
+      Unit U;
+      for (; ok && unit_at<PAIR, BN>(p, worker, workers, it, rank, U); ++it) {
+        const int nkb = U.nkb;
         const int buf = it & 1;
         const uint32_t acc_phase = (uint32_t)(it >> 1) & 1u;
         if (!mbar_wait(acce_bar(buf), acc_phase ^ 1u, wc)) { ok = false; break; }
@@ -609,8 +653,14 @@ __global__ void __launch_bounds__(THREADS, 1)
     // eight 16-byte loads a thread in flight -- so that case takes the latter)
     constexpr int KBOX = 128 / (int)sizeof(T);
     const bool tma_c = p.c_tma && (p.beta == 0.f || sizeof(T) == 2 || nbw >= 2);
-    const bool c_in = !SPLIT && tma_c && p.beta != 0.f;
+    const bool c_in = tma_c && p.beta != 0.f;
     const int i_lo = sizeof(T) == 4 ? c_lo : g_lo, i_hi = sizeof(T) == 4 ? c_hi : g_hi;
+    // 32-column chunks of a shared tile this warp publishes, sums and
+    // counts: the chunks its store of the tile will cover (64-column groups
+    // for 16-bit C through TMA, 32-column chunks otherwise), so that a warp
+    // only ever stores columns whose sums it finished itself
+    const int s_lo = (sizeof(T) == 2 && tma_c) ? 2 * g_lo : c_lo;
+    const int s_hi = (sizeof(T) == 2 && tma_c) ? 2 * g_hi : c_hi;
     int nb = 0;
     uint32_t cpend = 0u, cph = 0u;
     auto c_load = [&](int lb, int gx, int gy, int bz_) {  // lane 0
@@ -630,21 +680,43 @@ __global__ void __launch_bounds__(THREADS, 1)
     };
     int it = 0;
     bool dead = false;
+    uint32_t fph = 0u;  // phase of this warp's fix_bar (lane 0)
+    Unit U;
     // (warps of an unused share take no unit; they wait at the final barrier)
-    for (int u = hh < nh ? worker : n_units; u < n_units && !dead; u += workers, ++it) {
-      int m0, tn, kbeg, nkb, z, tail, bz;
-      unit_coords<PAIR, kblk<T>()>(u, p, rank, m0, tn, kbeg, nkb, z, tail, bz);
-      const int n0 = tn * BN;
+    for (; hh < nh && !dead && unit_at<PAIR, BN>(p, worker, workers, it, rank, U); ++it) {
+      const int m0 = U.m0, n0 = U.n0, bz = U.bz;
       const int buf = it & 1;
       const uint32_t acc_phase = (uint32_t)(it >> 1) & 1u;
-      // C of the first boxes is requested before the accumulator is ready (a
-      // box wholly past M or N is neither loaded nor stored)
+      // C of the first boxes is requested ahead (a box wholly past M or N is
+      // neither loaded nor stored): for a whole tile before its accumulator
+      // is ready
       const bool c_rows = m0 + q * 32 < p.M;
       const int nb0 = nb;
       auto box_buf = [&](int i) { return (nb0 + i - i_lo) % nbw; };
-      if (c_in && tail < 0 && c_rows && lane == 0)
-        for (int i = i_lo; i < i_hi && i < i_lo + nbw; ++i)
-          if (n0 + KBOX * i < p.N) c_load(box_buf(i), n0 + KBOX * i, m0 + q * 32, bz);
+      auto prefetch_c = [&]() {
+        if (c_in && c_rows && lane == 0)
+          for (int i = i_lo; i < i_hi && i < i_lo + nbw; ++i)
+            if (n0 + KBOX * i < p.N) c_load(box_buf(i), n0 + KBOX * i, m0 + q * 32, bz);
+      };
+      if (U.sk < 0) prefetch_c();
+      // Shared tile: its contributors (ranges w_first .. w_last, in K order),
+      // this strip's arrival counter, and whether this is the worker's last
+      // unit -- which reads the counter before its accumulator is ready, so
+      // that the read's latency overlaps the main loop.
+      int64_t s0 = 0;
+      int w_first = 0, w_last = 0;
+      unsigned int* cnt = nullptr;
+      bool final = false;
+      unsigned int seen = 0;
+      if (U.sk >= 0) {
+        s0 = (int64_t)U.sk * p.steps;
+        w_first = sk_owner(p, s0);
+        w_last = sk_owner(p, s0 + p.steps - 1);
+        cnt = p.sk_cnt + (((int64_t)U.sk * (PAIR ? 2 : 1) + rank) * 4 + q) * EPI_HALVES + hh;
+        Unit U2;
+        final = !unit_at<PAIR, BN>(p, worker, workers, it + 1, rank, U2);
+        if (final && lane == 0 && s_lo < s_hi) seen = ld_acquire(cnt);
+      }
       // one lane waits, the warp follows: the TMEM loads below are
       // warp-collective, so the whole warp must take the same branch
       bool got = false;
@@ -654,16 +726,157 @@ __global__ void __launch_bounds__(THREADS, 1)
       tc_fence_after();
       const int gm = m0 + row;
       const uint32_t t_row = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(buf * BN);
-      // tail slice: this warp's 32 x BN partial sums for the tile live in a
-      // block of the workspace laid out as the warp holds them -- [chunk c]
-      // [float4 v][lane] -- so every store and load of a warp covers 512
-      // contiguous bytes
+      // shared tile: a warp's 32 x BN partial sums live in its strip of the
+      // range's slot, laid out as the warp holds them -- [chunk c][float4 v]
+      // [lane] -- so every store and load of a warp covers 512 contiguous
+      // bytes
       constexpr int P = PAIR ? 2 : 1;
       constexpr int STRIP = 32 * BN;  // floats per warp strip
-      float* const tail_strip =
-          tail >= 0 ? p.tail_ws + ((((int64_t)(tail * P + rank) * p.tail_splits + z) * 4 + q) * STRIP)
-                    : nullptr;
-      if constexpr (sizeof(T) == 4) if (!SPLIT && tail < 0 && tma_c) {
+      auto strip_of = [&](int w_, int slot_) {
+        return p.sk_ws + ((((int64_t)w_ * 2 + slot_) * P + rank) * 4 + q) * STRIP;
+      };
+      bool whole = U.sk < 0;
+      if (!whole) {
+        // ------------------------------------------------ shared tile
+        // The contributor that finds every other one counted in, and is on
+        // its last unit, adds their sums to its own accumulator (bulk copies
+        // into the stage ring, idle once the worker's last accumulator is
+        // complete) and stores the tile as a whole one.  Any other
+        // contributor publishes its sums in its slot and counts in; if that
+        // makes it the last, it finishes the strip the same way (on its last
+        // unit) or from the slots with plain loads (earlier units, rare).
+        if (s_lo == s_hi) { release_acc(buf); continue; }  // (no columns: not counted)
+        const int n_contrib = w_last - w_first + 1;
+        constexpr uint32_t RING = (uint32_t)(STAGES * C_::STAGE_BYTES);
+        const uint32_t region_bytes = (RING / (uint32_t)(4 * nh)) & ~4095u;
+        const int n_slots = (int)(region_bytes >> 12);
+        const uint32_t region = tiles_addr + (uint32_t)(hh * 4 + q) * region_bytes;
+        seen = __shfl_sync(0xffffffffu, seen, 0);
+        if (final && seen != (unsigned int)(n_contrib - 1)) {  // look again
+          if (lane == 0) seen = ld_acquire(cnt);
+          seen = __shfl_sync(0xffffffffu, seen, 0);
+        }
+        const bool ring_ok = n_contrib - 1 <= n_slots;
+        if (!(final && ring_ok && seen == (unsigned int)(n_contrib - 1))) {
+          // publish this range's sums in its slot, then count in
+          float* const mine = strip_of(worker, U.slot);
+#pragma unroll 1
+          for (int c = s_lo; c < s_hi; ++c) {
+            uint32_t r[32];
+            __syncwarp();
+            tmem_ld_32x32b_x32(t_row + (uint32_t)(c * 32), r);
+            tmem_ld_wait();
+            if (!final && c == s_hi - 1) release_acc(buf);
+            float4* dst = reinterpret_cast<float4*>(mine) + c * 256 + lane;
+#pragma unroll
+            for (int v = 0; v < 8; ++v)
+              dst[v * 32] = make_float4(__uint_as_float(r[4 * v]), __uint_as_float(r[4 * v + 1]),
+                                        __uint_as_float(r[4 * v + 2]), __uint_as_float(r[4 * v + 3]));
+          }
+          __threadfence();
+          __syncwarp();
+          unsigned int old = 0;
+          if (lane == 0) old = atomicAdd(cnt, 1u);
+          old = __shfl_sync(0xffffffffu, old, 0);
+          if (old != (unsigned int)(n_contrib - 1)) {  // another contributor finishes it
+            if (final) release_acc(buf);
+            continue;
+          }
+          __threadfence();  // every contributor's sums are visible
+          if (!final || !ring_ok) {
+            // every slot (this range's own included), plain loads, K order
+#pragma unroll 1
+            for (int c = s_lo; c < s_hi; ++c) {
+              float v[32];
+#pragma unroll
+              for (int j = 0; j < 32; ++j) v[j] = 0.f;
+              for (int w2 = w_first; w2 <= w_last; ++w2) {
+                const float4* src =
+                    reinterpret_cast<const float4*>(strip_of(w2, sk_slot(p, w2, s0))) + c * 256 + lane;
+#pragma unroll
+                for (int w = 0; w < 8; ++w) {
+                  const float4 f = __ldcg(src + w * 32);
+                  v[4 * w] += f.x; v[4 * w + 1] += f.y; v[4 * w + 2] += f.z; v[4 * w + 3] += f.w;
+                }
+              }
+              if (gm < p.M) store_c32<T>(p, bz, gm, n0 + c * 32, v);
+            }
+            if (final) release_acc(buf);
+            __syncwarp();
+            if (lane == 0) atomicExch(cnt, 0u);
+            continue;
+          }
+        }
+        // Add the other contributors' sums to this accumulator strip, in K
+        // order, through this warp's share of the ring (4 KiB slots, one
+        // 32-column chunk of one contributor each).
+        {
+          const int per = n_contrib - 1;
+          const int cpb = n_slots / per > 0 ? n_slots / per : 1;
+          bool ok = true;
+          for (int c0 = s_lo; c0 < s_hi && ok; c0 += cpb) {
+            const int c1 = min(s_hi, c0 + cpb);
+            if (lane == 0) {
+              fence_proxy_async_global();
+              mbar_arrive_expect_tx(fix_bar(ew), (uint32_t)((c1 - c0) * per) * 4096u);
+              int sl = 0;
+              for (int c = c0; c < c1; ++c)
+                for (int w2 = w_first; w2 <= w_last; ++w2) {
+                  if (w2 == worker) continue;
+                  bulk_load(region + (uint32_t)sl * 4096u,
+                            strip_of(w2, sk_slot(p, w2, s0)) + c * 1024, 4096u, fix_bar(ew));
+                  ++sl;
+                }
+              ok = mbar_wait(fix_bar(ew), fph, wc);
+              // (given up: the copies in flight land before the block's
+              // shared memory is released)
+              if (!ok) mbar_wait_drain(fix_bar(ew), fph, p.timeout_ns);
+              fph ^= 1u;
+            }
+            ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+            if (!ok) break;
+            int sl = 0;
+#pragma unroll 1
+            for (int c = c0; c < c1; ++c) {
+              uint32_t r[32];
+              __syncwarp();
+              tmem_ld_32x32b_x32(t_row + (uint32_t)(c * 32), r);
+              tmem_ld_wait();
+              float v[32];
+#pragma unroll
+              for (int j = 0; j < 32; ++j) v[j] = 0.f;
+              for (int w2 = w_first; w2 <= w_last; ++w2) {
+                if (w2 == worker) {
+#pragma unroll
+                  for (int j = 0; j < 32; ++j) v[j] += __uint_as_float(r[j]);
+                  continue;
+                }
+                const uint32_t a = region + (uint32_t)sl * 4096u + (uint32_t)lane * 16u;
+#pragma unroll
+                for (int w = 0; w < 8; ++w) {
+                  float f0, f1, f2, f3;
+                  asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
+                               : "=f"(f0), "=f"(f1), "=f"(f2), "=f"(f3)
+                               : "r"(a + (uint32_t)w * 512u)
+                               : "memory");
+                  v[4 * w] += f0; v[4 * w + 1] += f1; v[4 * w + 2] += f2; v[4 * w + 3] += f3;
+                }
+                ++sl;
+              }
+#pragma unroll
+              for (int j = 0; j < 32; ++j) r[j] = __float_as_uint(v[j]);
+              tmem_st_32x32b_x32(t_row + (uint32_t)(c * 32), r);
+            }
+            tmem_st_wait();
+            __syncwarp();  // every lane has read the slots before they are refilled
+          }
+          if (!ok) { dead = true; break; }
+        }
+        if (lane == 0) atomicExch(cnt, 0u);
+        whole = true;
+        prefetch_c();
+      }
+      if constexpr (sizeof(T) == 4) if (whole && tma_c) {
         // fp32 C through TMA stores, 32 columns (128 bytes a row) at a time,
         // in the same 128-byte swizzle as the 16-bit path below
         // (two copies of the loop: with C loads (beta != 0) and without)
@@ -723,7 +936,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         nb += i_hi - i_lo;
         continue;
       }
-      if constexpr (sizeof(T) == 2) if (!SPLIT && tail < 0 && tma_c) {
+      if constexpr (sizeof(T) == 2) if (whole && tma_c) {
         // C through TMA stores, 64 columns at a time: two tensor-memory loads
         // in flight, the 32 x 64 16-bit block packed into this warp's staging
         // buffer in the 128-byte swizzle (16-byte chunk w of row l at chunk
@@ -819,16 +1032,8 @@ __global__ void __launch_bounds__(THREADS, 1)
         tmem_ld_32x32b_x32(t_row + (uint32_t)(c * 32), r);
         tmem_ld_wait();
         if (c == c_hi - 1) release_acc(buf);
-        if (tail >= 0) {
-          float4* dst = reinterpret_cast<float4*>(tail_strip) + (c * 8) * 32 + lane;
-#pragma unroll
-          for (int v = 0; v < 8; ++v)
-            dst[v * 32] = make_float4(__uint_as_float(r[4 * v]), __uint_as_float(r[4 * v + 1]),
-                                      __uint_as_float(r[4 * v + 2]), __uint_as_float(r[4 * v + 3]));
-          continue;
-        }
         const int gn0 = n0 + c * 32;
-        if (!SPLIT && !p.c_vec_ok) {
+        if (!p.c_vec_ok) {
           // through this warp's first staging buffer (no TMA store uses the
           // buffers in a launch that takes this path); the whole warp takes
           // part, rows past M are skipped inside
@@ -839,61 +1044,10 @@ __global__ void __launch_bounds__(THREADS, 1)
         }
         // rows past M: loaded (warp-collective) but not stored
         if (gm >= p.M) continue;
-        if constexpr (SPLIT) {
-          float* dst = p.partial + ((int64_t)z * p.M + gm) * p.N + gn0;
-          if (gn0 + 31 < p.N && (p.N & 3) == 0) {
+        float v[32];
 #pragma unroll
-            for (int v = 0; v < 8; ++v)
-              reinterpret_cast<float4*>(dst)[v] =
-                  make_float4(__uint_as_float(r[4 * v]), __uint_as_float(r[4 * v + 1]),
-                              __uint_as_float(r[4 * v + 2]), __uint_as_float(r[4 * v + 3]));
-          } else {
-            for (int j = 0; j < 32; ++j)
-              if (gn0 + j < p.N) dst[j] = __uint_as_float(r[j]);
-          }
-        } else {
-          float v[32];
-#pragma unroll
-          for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
-          store_c32<T>(p, bz, gm, gn0, v);
-        }
-      }
-      if (tail >= 0 && c_lo < c_hi) {
-        // Last slice to arrive for this 32-row strip (and column share)
-        // finishes it: partial
-        // writes are fenced before the arrival, the slices are summed in slice
-        // order (so the result does not depend on which slice came last), and
-        // the counter is left at zero for the next launch.  No waiting on
-        // other blocks is involved.
-        __threadfence();
-        unsigned int old = 0;
-        // one counter per 32-row strip and column share
-        unsigned int* cnt = p.tail_cnt + ((tail * P + rank) * 4 + q) * EPI_HALVES + hh;
-        if (lane == 0) old = atomicAdd(cnt, 1u);
-        old = __shfl_sync(0xffffffffu, old, 0);
-        if (old == (unsigned int)(p.tail_splits - 1)) {
-          __threadfence();
-          const float* strip0 =
-              p.tail_ws + (((int64_t)(tail * P + rank) * p.tail_splits * 4 + q) * STRIP);
-          const int64_t slice_stride = 4 * (int64_t)STRIP;
-#pragma unroll 1
-          for (int c = c_lo; c < c_hi; ++c) {
-            float v[32];
-#pragma unroll
-            for (int j = 0; j < 32; ++j) v[j] = 0.f;
-            for (int zz = 0; zz < p.tail_splits; ++zz) {
-              const float4* src =
-                  reinterpret_cast<const float4*>(strip0 + zz * slice_stride) + (c * 8) * 32 + lane;
-#pragma unroll
-              for (int w = 0; w < 8; ++w) {
-                const float4 f = __ldcg(src + w * 32);
-                v[4 * w] += f.x; v[4 * w + 1] += f.y; v[4 * w + 2] += f.z; v[4 * w + 3] += f.w;
-              }
-            }
-            if (gm < p.M) store_c32<T>(p, bz, gm, n0 + c * 32, v);
-          }
-          if (lane == 0) atomicExch(cnt, 0u);
-        }
+        for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
+        store_c32<T>(p, bz, gm, gn0, v);
       }
     }
     if (lane == 0) {
@@ -921,17 +1075,15 @@ __global__ void __launch_bounds__(THREADS, 1)
 
 // ---------------------------------------------------------------- host side
 PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-  static bool tried = false;
-  if (!tried) {
-    tried = true;
+  static const PFN_cuTensorMapEncodeTiled_v12000 fn = [] {
     void* ptr = nullptr;
     cudaDriverEntryPointQueryResult q;
     if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000,
                                          cudaEnableDefault, &q) == cudaSuccess &&
         q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
-  }
+      return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+    return (PFN_cuTensorMapEncodeTiled_v12000) nullptr;
+  }();
   return fn;
 }
 
@@ -940,14 +1092,52 @@ PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
 // box_rows x 1, 128-byte swizzle by default, out-of-range elements read as
 // zero.  Returns false when the driver rejects the description (the launch
 // then reports cudaErrorNotSupported and nothing runs).
+//
+// Encoded maps are kept in a small per-thread cache keyed by everything the
+// description holds (address, element type and size, extents, pitches, box,
+// swizzle): a map only describes a layout, so it stays valid for whatever
+// memory lies at that address; a repeated call skips the encoding.
+struct MapKey {
+  const void* base;
+  int64_t rows, cols, ld, batch, stride;
+  int box_cols, box_rows, type, swizzle, esize;
+  bool operator==(const MapKey& o) const {
+    return base == o.base && rows == o.rows && cols == o.cols && ld == o.ld &&
+           batch == o.batch && stride == o.stride && box_cols == o.box_cols &&
+           box_rows == o.box_rows && type == o.type && swizzle == o.swizzle && esize == o.esize;
+  }
+};
+struct MapEntry {
+  MapKey key;
+  CUtensorMap map;
+  bool used;
+};
+constexpr int MAP_CACHE = 64;
+
+inline uint64_t map_hash(const MapKey& k) {
+  uint64_t h = (uint64_t)(uintptr_t)k.base * 0x9E3779B97F4A7C15ull;
+  const int64_t v[9] = {k.rows, k.cols, k.ld, k.batch, k.stride, k.box_cols, k.box_rows,
+                        k.type * 16 + k.swizzle, k.esize};
+  for (int i = 0; i < 9; ++i) h = (h ^ (uint64_t)v[i]) * 0x100000001B3ull;
+  return h ^ (h >> 29);
+}
+
 bool make_map(CUtensorMap* map, CUtensorMapDataType type, const void* base, int64_t rows,
               int64_t cols, int64_t ld, int box_cols, int box_rows,
               CUtensorMapSwizzle swizzle = CU_TENSOR_MAP_SWIZZLE_128B, int64_t batch = 1,
               int64_t stride = 0, int esize = 2) {
-  auto enc = get_encode();
-  if (!enc) return false;
   // [batch][rows][cols]; a single matrix is batch 1 with a nominal pitch
   if (batch <= 1) stride = ld * (rows > 0 ? rows : 1);
+  const MapKey key{base, rows, cols, ld, batch > 1 ? batch : 1, stride, box_cols, box_rows,
+                   (int)type, (int)swizzle, esize};
+  thread_local MapEntry cache[MAP_CACHE];
+  MapEntry& slot = cache[map_hash(key) % MAP_CACHE];
+  if (slot.used && slot.key == key) {
+    *map = slot.map;
+    return true;
+  }
+  auto enc = get_encode();
+  if (!enc) return false;
   cuuint64_t dims[3] = {(cuuint64_t)cols, (cuuint64_t)rows, (cuuint64_t)(batch > 1 ? batch : 1)};
   cuuint64_t strides[2] = {(cuuint64_t)(ld * esize), (cuuint64_t)(stride * esize)};
   cuuint32_t box[3] = {(cuuint32_t)box_cols, (cuuint32_t)box_rows, 1};
@@ -956,7 +1146,11 @@ bool make_map(CUtensorMap* map, CUtensorMapDataType type, const void* base, int6
                    strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                    swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS;
+  if (r != CUDA_SUCCESS) return false;
+  slot.key = key;
+  slot.map = *map;
+  slot.used = true;
+  return true;
 }
 
 // How many two-block clusters of the pair kernel can be resident at once
@@ -967,7 +1161,7 @@ int pair_slots(int num_sms) {
   static int n = 0;
   if (n == 0) {
     using C_ = Cfg<BN, B_MN, MODE>;
-    auto kern = hgemm_tc_kernel<T, BN, A_MN, B_MN, false, MODE>;
+    auto kern = hgemm_tc_kernel<T, BN, A_MN, B_MN, MODE>;
     int q = 0;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              C_::SMEM_BYTES) == cudaSuccess) {
@@ -989,13 +1183,17 @@ int pair_slots(int num_sms) {
   return n;
 }
 
-int host_total_units(const HParams& p, bool pair) {
-  const int tiles = (pair ? (p.tiles_m + 1) / 2 : p.tiles_m) * p.tiles_n;
-  if (p.tail_splits > 0) return p.dp_units + (tiles - p.dp_units) * p.tail_splits;
-  return tiles * p.splits * (p.batch > 1 ? p.batch : 1);
+// cudaFuncSetAttribute for the kernel's shared memory, once per
+// configuration (a driver call per GEMM otherwise).
+template <typename T, int BN, bool A_MN, bool B_MN, int MODE>
+cudaError_t kernel_attributes() {
+  static const cudaError_t e = cudaFuncSetAttribute(
+      hgemm_tc_kernel<T, BN, A_MN, B_MN, MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+      Cfg<BN, B_MN, MODE>::SMEM_BYTES);
+  return e;
 }
 
-template <typename T, int BN, bool A_MN, bool B_MN, bool SPLIT, int MODE>
+template <typename T, int BN, bool A_MN, bool B_MN, int MODE>
 cudaError_t launch_cfg(const HgemmArgs& a, const HParams& p, LaunchCtx& ctx) {
   constexpr CUtensorMapDataType TY = Elem<T>::TMA;
   constexpr bool PAIR = MODE != 0;
@@ -1022,49 +1220,36 @@ cudaError_t launch_cfg(const HgemmArgs& a, const HParams& p, LaunchCtx& ctx) {
   if (p.c_tma && !make_map(&mC, TY, a.C, a.M, a.N, a.ldc, KB, 32, CU_TENSOR_MAP_SWIZZLE_128B,
                            p.batch, p.stride_c, ES))
     return cudaErrorNotSupported;
-  auto kern = hgemm_tc_kernel<T, BN, A_MN, B_MN, SPLIT, MODE>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       C_::SMEM_BYTES);
+  auto kern = hgemm_tc_kernel<T, BN, A_MN, B_MN, MODE>;
+  cudaError_t e = kernel_attributes<T, BN, A_MN, B_MN, MODE>();
   if (e != cudaSuccess) return e;
   // both epilogue shares only where this configuration's staging has room
   HParams pp = p;
   if (!C_::EPI2) pp.epi_halves = 1;
-  if constexpr (PAIR) {
-    // persistent grid of as many pairs as can be resident at once
-    const int max_pairs = pair_slots<T, BN, A_MN, B_MN, MODE>(a.num_sms);
-    const int units = host_total_units(p, true);
-    const int pairs = units < max_pairs ? units : max_pairs;
-    ctx.grid = 2 * pairs;
-    e = launch_kernel(kern, dim3(2 * pairs), dim3(THREADS), C_::SMEM_BYTES, ctx.stream, 2, mA, mB,
-                      mC, pp);
-  } else {
-    const int units = host_total_units(p, false);
-    const int grid = units < a.num_sms ? units : a.num_sms;
-    ctx.grid = grid;
-    e = launch_kernel(kern, dim3(grid), dim3(THREADS), C_::SMEM_BYTES, ctx.stream, 1, mA, mB, mC,
-                      pp);
-  }
+  const int workers = a.plan.workers;
+  ctx.grid = PAIR ? 2 * workers : workers;
+  e = launch_kernel(kern, dim3(ctx.grid), dim3(THREADS), C_::SMEM_BYTES, ctx.stream, PAIR ? 2 : 1,
+                    mA, mB, mC, pp);
   if (e == cudaSuccess) ctx.launches++;
   return e;
 }
 
 template <typename T, int BN>
 cudaError_t launch_bn(const HgemmArgs& a, const HParams& p, LaunchCtx& ctx) {
-  const bool A_MN = a.transA != 0, B_MN = a.transB == 0, split = a.splits > 1;
+  const bool A_MN = a.transA != 0, B_MN = a.transB == 0;
   constexpr bool CAN_PAIR = BN == 128 || BN == 256;
   constexpr int M2 = CAN_PAIR ? 2 : 0;
+  const bool pair = CAN_PAIR && p.pair == 2;
   if constexpr (sizeof(T) == 4) {
     // TF32 operands are staged K-major only (the dispatcher packs them so)
     if (A_MN || B_MN) return cudaErrorInvalidValue;
-    if (split) return launch_cfg<T, BN, false, false, true, 0>(a, p, ctx);
-    if (CAN_PAIR && p.pair == 2) return launch_cfg<T, BN, false, false, false, M2>(a, p, ctx);
-    return launch_cfg<T, BN, false, false, false, 0>(a, p, ctx);
+    if (pair) return launch_cfg<T, BN, false, false, M2>(a, p, ctx);
+    return launch_cfg<T, BN, false, false, 0>(a, p, ctx);
   } else {
 #define GB300_HG(AM, BMN)                                                   \
   if (A_MN == AM && B_MN == BMN) {                                          \
-    if (split) return launch_cfg<T, BN, AM, BMN, true, 0>(a, p, ctx);       \
-    if (CAN_PAIR && p.pair == 2) return launch_cfg<T, BN, AM, BMN, false, M2>(a, p, ctx); \
-    return launch_cfg<T, BN, AM, BMN, false, 0>(a, p, ctx);                 \
+    if (pair) return launch_cfg<T, BN, AM, BMN, M2>(a, p, ctx);             \
+    return launch_cfg<T, BN, AM, BMN, 0>(a, p, ctx);                        \
   }
   GB300_HG(false, true)
   GB300_HG(true, true)
@@ -1075,20 +1260,29 @@ cudaError_t launch_bn(const HgemmArgs& a, const HParams& p, LaunchCtx& ctx) {
   return cudaErrorInvalidValue;
 }
 
-// One launch of the kernel for element type T (HgemmArgs already planned by the
-// dispatcher: tile width, split, pairs, tail).
+// One launch of the kernel for element type T, as planned by hgemm_plan
+// (tile width, pairs, schedule, scratch for shared tiles).
 template <typename T>
 cudaError_t launch_hgemm_t(const HgemmArgs& a, LaunchCtx& ctx) {
+  const HPlan& pl = a.plan;
   HParams p;
   p.C = a.C;
-  p.partial = a.partial;
   p.ldc = a.ldc;
   p.M = a.M; p.N = a.N; p.K = a.K;
-  p.splits = a.splits > 1 ? a.splits : 1;
-  p.k_slice = a.splits > 1 ? a.k_slice : ((a.K + kblk<T>() - 1) / kblk<T>()) * kblk<T>();
   const int bn = a.bn;
   p.tiles_m = (a.M + BM - 1) / BM;
   p.tiles_n = (a.N + bn - 1) / bn;
+  p.tiles = pl.tiles;
+  p.steps = pl.steps;
+  p.dp_tiles = pl.dp_tiles;
+  p.sk_workers = pl.sk_workers;
+  p.sk_steps = pl.sk_steps;
+  auto magic = [](uint64_t d) { return d > 0 ? ~0ull / d : 0ull; };
+  p.m_skw = magic((uint64_t)pl.sk_workers);
+  p.m_sks = magic((uint64_t)pl.sk_steps);
+  p.m_steps = magic((uint64_t)pl.steps);
+  p.sk_ws = a.sk_ws;
+  p.sk_cnt = a.sk_cnt;
   p.alpha = a.alpha; p.beta = a.beta;
   p.status = ctx.status;
   p.timeout_ns = ctx.timeout_ns;
@@ -1096,29 +1290,16 @@ cudaError_t launch_hgemm_t(const HgemmArgs& a, LaunchCtx& ctx) {
   constexpr int VEC = 16 / (int)sizeof(T);  // elements per 16 bytes
   p.c_vec_ok = ((reinterpret_cast<uintptr_t>(a.C) & 15u) == 0 && (a.ldc % VEC) == 0 &&
                 (a.batch <= 1 || (a.stride_c % VEC) == 0)) ? 1 : 0;
-  p.c_tma = (p.c_vec_ok && a.splits <= 1 && a.c_tma &&
-             bn >= (sizeof(T) == 4 ? 32 : 64)) ? 1 : 0;
-  p.pair = hgemm_use_pair(bn, a.M, p.splits, a.pair) ? a.pair : 0;
-  p.dp_units = a.dp_units;
-  p.tail_splits = a.tail_splits;
-  p.tail_k_slice = a.tail_k_slice;
-  p.tail_ws = a.tail_ws;
-  p.tail_cnt = a.tail_cnt;
+  p.c_tma = (p.c_vec_ok && a.c_tma && bn >= (sizeof(T) == 4 ? 32 : 64)) ? 1 : 0;
+  p.pair = pl.pair;
   p.batch = a.batch > 1 ? a.batch : 1;
   p.stride_c = p.batch > 1 ? a.stride_c : 0;
   p.za_mask = (p.batch > 1 && a.stride_a != 0) ? -1 : 0;
-  p.ep = a.ep;
-  // Short-K tiles are epilogue-bound: both shares of epilogue warps drain them
-  // (measured: 4096 x 4096 x 128 fp16 23.2 -> 19-21 us); long-K tiles keep one
-  // share, which leaves the main loop's warps more issue slots (4096^3 and
-  // 8192^3 were 2 % slower with two).
-  {
-    const int steps = (p.k_slice + kblk<T>() - 1) / kblk<T>();
-    p.epi_halves = (EPI_HALVES > 1 && steps <= 8) ? EPI_HALVES : 1;
-  }
   p.zb_mask = (p.batch > 1 && a.stride_b != 0) ? -1 : 0;
-  if (p.tail_splits > 0 && (p.splits != 1 || !p.tail_ws || !p.tail_cnt)) return cudaErrorInvalidValue;
-  if (p.batch > 1 && (p.splits != 1 || p.tail_splits > 0)) return cudaErrorInvalidValue;
+  p.ep = a.ep;
+  p.epi_halves = pl.epi_halves;
+  if (pl.workers <= 0 || pl.steps <= 0 || pl.bn != bn) return cudaErrorInvalidValue;
+  if (pl.sk_workers > 0 && (!a.sk_ws || !a.sk_cnt)) return cudaErrorInvalidValue;
   switch (bn) {
     case 32: return launch_bn<T, 32>(a, p, ctx);
     case 64: return launch_bn<T, 64>(a, p, ctx);

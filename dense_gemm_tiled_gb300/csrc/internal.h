@@ -48,40 +48,49 @@ struct SgemmArgs {
   Epilogue ep;  // fused bias / activation (not with splits > 1: the reduction applies it)
 };
 
-// One tcgen05 GEMM launch (fp16 or bf16 operands and output).
+// Schedule of one tcgen05 GEMM launch (hgemm_plan): a persistent grid of
+// `workers` blocks, or block pairs with pair == 2, over `tiles` output tiles
+// of `steps` K steps each.  Tiles [0, dp_tiles) are whole units handed out
+// round-robin; the K steps of the others are shared out in sk_workers equal
+// contiguous ranges (stream-K), a tile shared by several ranges being summed
+// from fp32 partials by its last contributor.
+struct HPlan {
+  int bn = 0;                 // tile width
+  int pair = 0;               // 0 single blocks, 2 two-SM pairs
+  int workers = 0;            // blocks (or pairs) in the grid
+  int tiles = 0, steps = 0;   // work tiles (batch included), K steps per tile
+  int dp_tiles = 0;           // whole tiles
+  int sk_workers = 0;         // ranges of the shared steps (0: no sharing)
+  int64_t sk_steps = 0;       // (tiles - dp_tiles) * steps
+  int epi_halves = 1;         // epilogue warps per accumulator quarter
+  size_t ws_bytes = 0;        // fp32 partial slots: sk_workers x 2 x (pair ? 2 : 1) x 128 x bn
+  size_t cnt_bytes = 0;       // arrival counters, zero before the launch
+};
+
+// One tcgen05 GEMM launch (fp16, bf16, or fp32 on TF32 MMAs).
 struct HgemmArgs {
   int transA, transB;
   int M, N, K;
-  const void* A;  // 16-byte aligned base, lda * 2 a multiple of 16
+  const void* A;  // 16-byte aligned base, row pitch a multiple of 16 bytes
   int64_t lda;
   const void* B;
   int64_t ldb;
   void* C;
   int64_t ldc;
   float alpha, beta;
-  int splits;
-  int k_slice;      // multiple of the kernel's K block
-  float* partial;   // [splits][M][N] fp32 when splits > 1
   int num_sms;
   int bn;               // tile width: 32, 64, 128, 192 or 256
-  int pair;             // block pairs allowed: 0 none, 2 2-SM (cta_group::2) MMAs
   int c_tma;            // allow TMA stores (and, beta != 0, TMA loads) of C when C is aligned
   int fault_injection;  // test hook: 1 = producer skips its first stage
   int dtype = 1;        // 1 fp16, 2 bf16, 3 fp32 on TF32 MMAs (gemm_dtype_t)
-  // strided batch (batch > 1: no split, no tail): element pitches between
-  // consecutive matrices; 16-bit TMA needs them (and ld) multiples of 8
+  // strided batch (batch > 1): element pitches between consecutive matrices;
+  // 16-bit TMA needs them (and ld) multiples of 8
   int batch = 1;
   int64_t stride_a = 0, stride_b = 0, stride_c = 0;
-  // tail split (see hgemm_plan_tail); tail_splits == 0 disables it
-  int dp_units = 0, tail_splits = 0, tail_k_slice = 0;
-  float* tail_ws = nullptr;
-  unsigned int* tail_cnt = nullptr;
-  Epilogue ep;  // fused bias / activation (not with splits > 1: the reduction applies it)
-};
-
-struct TailPlan {
-  int dp_units, splits, k_slice;
-  size_t ws_bytes, cnt_bytes;
+  HPlan plan;                      // from hgemm_plan
+  float* sk_ws = nullptr;          // plan.ws_bytes of scratch when plan.sk_workers > 0
+  unsigned int* sk_cnt = nullptr;  // plan.cnt_bytes, zeroed before the launch
+  Epilogue ep;  // fused bias / activation
 };
 
 struct LaunchCtx {
@@ -158,9 +167,17 @@ constexpr int SG_BLOCKS_PER_SM = GB300_SG_MIN_BLOCKS;
 constexpr int SGN_BM = 64 * GB300_SGN_WARPS_M, SGN_BN = 32, SGN_BK = GB300_SGN_BK;
 constexpr int SGN_BLOCKS_PER_SM = GB300_SGN_MIN_BLOCKS;
 constexpr int HG_BM = 128, HG_BK = 64;
-int hgemm_pick_bn(int M, int N, int transB, int num_sms, int batch = 1);
-bool hgemm_use_pair(int bn, int M, int splits, int allowed);
-int hgemm_pair_slots(int bn, int transA, int transB, int mode, int num_sms);
-TailPlan hgemm_plan_tail(int M, int N, int K, int bn, bool pair, int workers);
+// Tile width of the tcgen05 kernel (32 to 256 columns) for this problem and
+// schedule (arguments as hgemm_plan).
+int hgemm_pick_bn(int M, int N, int K, int transA, int transB, int kstep, int batch,
+                  int pair_allowed, int num_sms, int sk_mode);
+bool hgemm_use_pair(int bn, int M, int allowed);
+int hgemm_pair_slots(int bn, int transA, int transB, int num_sms);
+// Schedule of a tcgen05 launch.  kstep: K elements per step (64 for 16-bit
+// operands, 32 for TF32); pair_allowed: 0 or 2; sk_mode: 0 whole tiles only,
+// 1 share the steps of a last, part-filled round of tiles when that pays, 2
+// share every tile (a test setting).
+HPlan hgemm_plan(int M, int N, int K, int bn, int transA, int transB, int kstep, int batch,
+                 int pair_allowed, int num_sms, int sk_mode);
 
 }  // namespace gb300

@@ -161,21 +161,30 @@ int gemm_host(int transA, int transB, int64_t M, int64_t N, int64_t K, int dtype
  * other allocating routine.  (No page of the method describes this entry
  * point; it is a property of this library.)
  *
- * Same arguments, rules and results as gemm(), same kernels.  The split-K
- * partial sums that gemm() takes from the stream-ordered allocator live in one
- * fixed array of 8 MiB compiled into the library, which every GPU that loads
- * the library holds until the process exits.  Limits:
- *   - a problem whose split-K partials (splits x M x N x 4 bytes) exceed
- *     8 MiB returns GEMM_ERR_UNSUPPORTED without launching anything;
+ * Same arguments, rules and results as gemm(), with gemm()'s kernels and
+ * choice of tile and schedule.  The partial sums that gemm() keeps in scratch
+ * from the stream-ordered allocator -- the fp32 kernel's K slices, and the
+ * tensor-core kernel's shared (stream-K) tiles with their arrival counters --
+ * live in one fixed array of 8 MiB compiled into the library, which every
+ * GPU that loads the library holds until the process exits.  Differences and
+ * limits:
+ *   - an fp32 problem whose K slices (splits x M x N x 4 bytes) exceed 8 MiB
+ *     returns GEMM_ERR_UNSUPPORTED without launching anything;
+ *   - a tensor-core problem whose shared tiles would not fit the array runs
+ *     with whole tiles only (no scratch needed);
+ *   - gemm()'s scratch-based steps are left out: the fp32 operand packing and
+ *     persistent stream-K launch on large problems, and the aligned working
+ *     copy of an unaligned fp16 C (the kernel stores such a C row by row);
  *   - fp16/bf16 operands must have 16-byte aligned bases and row pitches (lda,
  *     ldb multiples of 8), else GEMM_ERR_UNSUPPORTED (padding them would need
- *     scratch).
+ *     scratch); GEMM_F32_TF32 is not accepted.
  * The first call on a device looks up the array's device address (a CUDA
  * runtime query, done once per device with that device current); make that
  * first call before any stream capture.  All calls share the array: calls
  * whose kernels can overlap on the GPU (e.g. on two unordered streams) race
- * on it, so order them on one stream or with events.  Nothing in it needs
- * clearing between calls: a call writes every partial it reads.
+ * on it, so order them on one stream or with events.  A call writes every
+ * partial sum it reads, and clears the counters that must start at zero
+ * (cudaMemsetAsync on `stream`, which allocates nothing) before its launch.
  */
 int gemm_splitk_noalloc(int transA, int transB, int64_t M, int64_t N, int64_t K, int dtype,
                         float alpha, float beta, const void* A, int64_t lda, const void* B,
@@ -240,7 +249,9 @@ typedef enum {
     GEMM_PATH_FFMA = 2,        /* fp32 FFMA tiled kernel */
     GEMM_PATH_FFMA_SPLITK = 3, /* fp32 FFMA kernel over K slices + reduction */
     GEMM_PATH_TC = 4,          /* fp16/bf16 tcgen05 kernel, fused epilogue */
-    GEMM_PATH_TC_SPLITK = 5,   /* fp16/bf16 tcgen05 kernel over K slices + reduction */
+    GEMM_PATH_TC_SPLITK = 5,   /* tcgen05 kernel whose persistent grid shares the K steps
+                                  of some tiles (stream-K); partial sums combined inside
+                                  the kernel */
     GEMM_PATH_FFMA_BATCHED = 6, /* strided batch: fp32 FFMA kernel, batch on the grid */
     GEMM_PATH_TC_BATCHED = 7,  /* strided batch: one persistent tcgen05 launch */
     GEMM_PATH_PER_ENTRY = 8    /* strided batch run entry by entry (unaligned operands) */
@@ -264,6 +275,16 @@ int gemm_last_grid(void);
  * events stay owned by the caller and must outlive their use.
  */
 void gemm_set_kernel_events(void* start, void* end);
+
+/*
+ * Diagnostics: scratch use.  Returns the largest number of bytes that were in
+ * use at once, on the current device, from the stream-ordered memory pool the
+ * library takes its scratch from, since the previous reset (0 if the pool has
+ * not been created yet, -1 on a CUDA error); a nonzero `reset` then sets the
+ * mark back to zero.  A stretch of calls that leaves the mark at zero took no
+ * scratch from the pool.
+ */
+int64_t gemm_scratch_high_water(int reset);
 
 /*
  * Test hook: the time limit, in nanoseconds, of every bounded wait inside the

@@ -53,13 +53,14 @@ SHAPES = {
     # operands copied to an aligned pitch first, C stored element-wise)
     "f32": [((300, 520, 1024), "ffma_splitk"), ((640, 1280, 64), "ffma"),
             ((1000, 2600, 620), "ffma"), ((1001, 2601, 621), "ffma")],
-    # 16-bit: split-K, whole-K 2-SM pairs (C stored by TMA, and loaded by TMA
-    # when beta != 0), and an odd N (C rows off 16-byte alignment: stored
-    # through the staging buffers a row at a time, or on a larger problem
-    # computed into an aligned copy that is then copied into place)
-    "f16": [((300, 520, 1024), "tc_splitk"), ((2048, 1536, 512), "tc"), ((2000, 1003, 512), None),
+    # 16-bit: shared tiles (stream-K: 10 tiles, K = 6144), whole-K 2-SM pairs
+    # (C stored by TMA, and loaded by TMA when beta != 0), and an odd N (C rows
+    # off 16-byte alignment: stored through the staging buffers a row at a
+    # time, or on a larger problem computed into an aligned copy that is then
+    # copied into place)
+    "f16": [((300, 520, 6144), "tc_splitk"), ((2048, 1536, 512), "tc"), ((2000, 1003, 512), None),
             ((2100, 1003, 512), None)],
-    "bf16": [((300, 520, 1024), "tc_splitk"), ((2048, 1536, 512), "tc"),
+    "bf16": [((300, 520, 6144), "tc_splitk"), ((2048, 1536, 512), "tc"),
              ((2000, 1003, 512), None)],
 }
 

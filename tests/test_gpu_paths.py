@@ -1,12 +1,14 @@
 """Every fp16 kernel configuration against the oracle.
 
 The dispatcher picks one tile width (64/128/192/256 columns); for 128 and 256,
-pairs of blocks running 2-SM MMAs across the pair; and a K split of the
-persistent grid's last round when it would run under half full.  Each
-configuration is forced here in its own process (the switches are read once per process from
-GEMM_GB300_HG_PAIR, GEMM_GB300_HG_BN and GEMM_GB300_HG_TAIL) and checked on
-ragged, multi-tile problems in all four variants, exact on small-integer
-inputs.
+pairs of blocks running 2-SM MMAs across the pair; and a schedule: whole tiles,
+or the K steps of a last, part-filled round of tiles shared out over the
+persistent grid (stream-K, shared tiles finished by their last contributor).
+Each configuration is forced here in its own process (the switches are read
+once per process from GEMM_GB300_HG_PAIR, GEMM_GB300_HG_BN and
+GEMM_GB300_HG_SK; SK=2 shares every tile, so every tile goes through the
+partial-sum path) and checked on ragged, multi-tile problems in all four
+variants, exact on small-integer inputs.
 """
 import os
 import subprocess
@@ -36,19 +38,25 @@ for v in ("nn", "tn", "nt", "tt"):
     p = inputs.make_problem(1024, 768, 1000, tA, tB, "f16", "uniform", seed=602)
     check_problem(p)
     # 2048 x 3072 with 256-wide tiles: 96 pair units (192 single tiles) over
-    # 76 pairs (152 blocks) leaves a last round under half full, which the
-    # tail split cuts into K slices
+    # 76 pairs (152 blocks) leaves a last round part-filled, whose K steps
+    # stream-K shares out
     p = inputs.make_problem(2048, 3072, 512, tA, tB, "f16", "uniform", seed=603, beta=0.5)
+    check_problem(p)
+    # few tiles, long K: shared tiles with many contributors each
+    p = inputs.make_problem(260, 96, 3000, tA, tB, "f16", "integer", seed=605)
+    check_problem(p, exact=True)
+    p = inputs.make_problem(130, 200, 2056, tA, tB, "f16", "uniform", seed=606, beta=0.5)
     check_problem(p)
 print("ok")
 """
 
 
-@pytest.mark.parametrize("pair,bn,tail", [("2", "256", "0"), ("2", "256", "1"), ("2", "128", "0"),
-                                          ("2", "128", "1"), ("0", "256", "1"), ("0", "256", "0"),
-                                          ("0", "128", "1"), ("0", "192", "1"), ("0", "64", "1")])
-def test_forced_kernel_configuration(lib_path, gpu, pair, bn, tail):
-    env = dict(os.environ, GEMM_GB300_HG_PAIR=pair, GEMM_GB300_HG_BN=bn, GEMM_GB300_HG_TAIL=tail)
+@pytest.mark.parametrize("pair,bn,sk", [("2", "256", "1"), ("2", "256", "2"), ("2", "256", "0"),
+                                        ("2", "128", "1"), ("2", "128", "2"), ("0", "256", "2"),
+                                        ("0", "256", "0"), ("0", "128", "2"), ("0", "192", "2"),
+                                        ("0", "64", "2"), ("0", "64", "1")])
+def test_forced_kernel_configuration(lib_path, gpu, pair, bn, sk):
+    env = dict(os.environ, GEMM_GB300_HG_PAIR=pair, GEMM_GB300_HG_BN=bn, GEMM_GB300_HG_SK=sk)
     code = SCRIPT.format(root=ROOT, tests=os.path.join(ROOT, "tests"))
     r = subprocess.run([sys.executable, "-c", code], env=env, capture_output=True, text=True,
                        timeout=900)

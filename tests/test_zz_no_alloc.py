@@ -2,24 +2,29 @@
 
 Some callers cannot allocate device memory at call time -- their allocator
 already owns the GPU, or their process forbids allocation while serving.  For
-them the library keeps the split-K partial sums in a fixed 8 MiB array.  This
-test calls that entry point through the C ABI and checks that it gives the
-same results as gemm() (within the tolerances the other tests use), on two
-calls in a row so that whatever the first call left in the shared array cannot
-leak into the second, and that a problem too large for the array is refused
-before anything is launched.
+them the library keeps the partial sums it would otherwise take from its
+scratch pool in a fixed 8 MiB array.  This test calls that entry point through
+the C ABI and checks, on two calls in a row (so that whatever the first call
+left in the shared array cannot leak into the second):
+  - each result against the oracle, at the tolerances the other tests use, or
+    bit for bit on small-integer inputs;
+  - that the shapes meant to split K did take a split path;
+  - that the second call allocated nothing: the device's free memory, torch's
+    allocator and the library's scratch pool are unchanged across it (the
+    first call, made before any gemm() on the shape, has loaded the kernels);
+  - that a problem too large for the array is refused before anything runs.
+gemm() on the same inputs is checked against the oracle as a second check.
 
 The file name makes pytest collect it last.
 """
 import ctypes
 
-import numpy as np
 import pytest
 import torch
 
-import oracle
-from oracle import compare
 from dense_gemm_tiled_gb300 import inputs
+from helpers import oracle_for, to_np
+from oracle import compare
 
 pytestmark = pytest.mark.gpu
 
@@ -42,44 +47,74 @@ def _call(L, p, A, B, C, stream):
                                  C.data_ptr(), C.stride(0), stream)
 
 
-@pytest.mark.parametrize("dtype,variant,shape", [
-    ("f16", "nt", (512, 32, 5632)),   # LoRA adapter shapes: split-K path
-    ("f16", "nn", (512, 32, 2048)),
-    ("f32", "tn", (512, 32, 5632)),
-    ("f16", "nt", (300, 520, 256)),   # no split: nothing in the array is used
-])
-def test_noalloc_matches_gemm_on_two_calls(lib, dtype, variant, shape):
-    L, binding = lib
+def _problem(dtype, variant, shape, dist, seed):
     M, N, K = shape
+    tA, tB = inputs.VARIANTS[variant]
+    if dist == "integer":
+        return inputs.make_problem(M, N, K, tA, tB, dtype, "integer", seed=seed)
+    return inputs.make_problem(M, N, K, tA, tB, dtype, "uniform", seed=seed, beta=0.5)
+
+
+SPLIT_PATHS = ("tc_splitk", "ffma_splitk")
+
+
+@pytest.mark.parametrize("dtype,variant,shape,dist,split", [
+    ("f16", "nt", (512, 32, 5632), "uniform", True),   # LoRA adapter shapes: shared K
+    ("f16", "nn", (512, 32, 2048), "uniform", True),
+    ("f16", "nt", (512, 32, 5632), "integer", True),   # bit-exact through the shared tiles
+    ("f32", "tn", (512, 32, 5632), "uniform", True),   # narrow fp32 tile, split K
+    ("f32", "nn", (1000, 32, 3000), "integer", True),
+    ("f16", "nt", (300, 520, 256), "uniform", False),  # whole tiles: the array is not used
+])
+def test_noalloc_matches_oracle_on_two_calls(lib, dtype, variant, shape, dist, split):
+    L, binding = lib
     dev = torch.device("cuda:0")
     stream = torch.cuda.current_stream().cuda_stream
-    for call, seed in enumerate((900, 901)):
-        p = inputs.sweep_problem(M, N, K, variant, dtype, 0.5, seed=seed + 10 * M)
-        A, B = p.A.to(dev), p.B.to(dev)
-        C_ref = p.C_in.to(dev).clone()
-        C_new = p.C_in.to(dev).clone()
-        binding.gemm(A, B, C_ref, p.transA, p.transB, p.alpha, p.beta)
-        rc = _call(L, p, A, B, C_new, stream)
+    probs = [_problem(dtype, variant, shape, dist, seed=900 + 10 * call + shape[0])
+             for call in range(2)]
+    # every tensor exists before the first call, so nothing below allocates
+    # through torch
+    dev_in = [(p.A.to(dev), p.B.to(dev), p.C_in.to(dev).clone() if p.C_in is not None else
+               torch.zeros((p.M, p.N), dtype=p.A.dtype, device=dev)) for p in probs]
+    C_gemm = [c.clone() for (_, _, c) in dev_in]
+    torch.cuda.synchronize()
+    for call, (p, (A, B, C)) in enumerate(zip(probs, dev_in)):
+        if call == 1:
+            free0 = torch.cuda.mem_get_info()[0]
+            torch0 = torch.cuda.memory_allocated()
+            assert binding.scratch_high_water(reset=True) >= 0
+        rc = _call(L, p, A, B, C, stream)
         assert rc == 0, binding.status_string(rc)
+        path = binding.last_path()
         torch.cuda.synchronize()
         assert binding.check_device_status() == binding.OK
-        # tolerance of the other tests, with gemm()'s output as the reference
-        _, mag = oracle.gemm_ref(p.A.numpy(), p.B.numpy(), p.C_in.numpy(), p.transA, p.transB,
-                                 p.alpha, p.beta)
-        got = C_new.cpu().numpy()
-        want = compare.as_double(C_ref.cpu().numpy())
-        res = compare.check(got, want, mag, dtype)
+        if call == 1:
+            assert torch.cuda.mem_get_info()[0] == free0
+            assert torch.cuda.memory_allocated() == torch0
+            assert binding.scratch_high_water() == 0
+        assert (path in SPLIT_PATHS) == split, path
+        ref, mag, _ = oracle_for(p, full=True)
+        res = compare.check(to_np(C.cpu()), ref, mag, dtype, exact=(dist == "integer"))
         assert res["ok"], (call, res)
+    # second check: gemm() on the same inputs, after the no-alloc calls
+    for p, (A, B, _), C in zip(probs, dev_in, C_gemm):
+        binding.gemm(A, B, C, p.transA, p.transB, p.alpha, p.beta)
+        torch.cuda.synchronize()
+        ref, mag, _ = oracle_for(p, full=True)
+        res = compare.check(to_np(C.cpu()), ref, mag, dtype, exact=(dist == "integer"))
+        assert res["ok"], res
 
 
 def test_noalloc_refuses_problems_larger_than_its_array(lib):
     L, binding = lib
     dev = torch.device("cuda:0")
-    # a 512 x 512 fp16 output is 16 tiles of 128 x 128; with K = 8192 it is
-    # split 9 ways: 9 MiB of fp32 partial sums, more than the 8 MiB array
-    p = inputs.make_problem(512, 512, 8192, False, False, "f16", "uniform", seed=950)
+    # a 1152 x 1152 fp32 output is 81 tiles of 128 x 128, split over K (4096)
+    # on any GPU with at least 81 SMs; one slice of partial sums is already
+    # 1152 * 1152 * 4 bytes = 5.3 MB, so two or more exceed the 8 MiB array
+    p = inputs.make_problem(1152, 1152, 4096, False, False, "f32", "uniform", seed=950)
     A, B = p.A.to(dev), p.B.to(dev)
-    C = torch.full((512, 512), 7.0, dtype=torch.float16, device=dev)
+    C = torch.full((1152, 1152), 7.0, dtype=torch.float32, device=dev)
+    torch.cuda.synchronize()
     rc = _call(L, p, A, B, C, torch.cuda.current_stream().cuda_stream)
     assert rc == binding.ERR_UNSUPPORTED
     torch.cuda.synchronize()
