@@ -4,21 +4,29 @@ Headline (the JSON line's `value`): fp32 SGEMM, nn, row-major, M = N = K = 4096,
 alpha = 1, beta = 0, A and B i.i.d. U[-1, 1) -- the problem of "Optimizing GEMM
 on Apple's M5 from scratch" (Parts 1 and 2) -- in TFLOP/s (2*M*N*K flops per
 step).  One step is one gemm() call through the C ABI on inputs resident in
-HBM.  The same line carries, measured in the same run:
-  fp16       fp16-operand / fp32-accumulate / fp16-output GEMM at 4096^3 in the
-             nn, tn and nt variants ("Metal GEMM Kernels for LoRA Training",
-             section 2), per-launch CUDA-event timing with L2 flushed before
-             every launch;
-  roofline   achieved / peak of the dominant kernel (FP32 FFMA pipe for the
-             SGEMM; the tensor pipe for the fp16 kernel), the kernel's own
-             device time taken by events the library records around it;
-  attention  the six GEMMs of one attention layer's forward and backward pass
-             ("Metal GEMM Kernels for LoRA Training", section 8), each one
-             strided-batched call over the heads, eager and as a CUDA graph;
+HBM; `step_ms` gives the per-step device-time median, min and p90.  The same
+line carries, measured in the same run:
+  roofline   achieved / peak of the headline kernel (the FP32 FFMA pipe), from
+             its own device time (events the library records around it);
+  clocks     SM clock and throttle reasons sampled (NVML, every 2 ms) during
+             the timed region, and over the whole run;
+  control    a bf16 cuBLAS matmul before and after, against the measured peak
+             ("Metal GEMM Kernels for LoRA Training", section 9);
+  fp16       fp16-operand / fp32-accumulate / fp16-output GEMM at 2048^3 and
+             4096^3 in the nn, tn and nt variants ("Metal GEMM Kernels for
+             LoRA Training", section 2), L2 flushed before every launch,
+             against the measured tensor peak;
+  tf32_4096  the opt-in TF32 path at 4096^3;
+  skinny_hbm_frac  the rank-32 LoRA adapter products and M=8192, N=32,
+             K=8192 against the measured HBM bandwidth: [us, frac, b2b_us];
+  lora_step, attention  the LoRA MLP-block step's 18 GEMMs and one attention
+             layer's six products (section 8) as CUDA graphs;
   e2e        the SGEMM through gemm_host(): pinned host buffers, the copies to
              and from the GPU inside the timed region;
   cpu_baseline  the CPU oracle (double accumulation) on a bounded sample of
              rows of the same problem, on this host's cores.
+Per-item details (each LoRA GEMM, each attention product, each skinny
+product) go to stderr as JSON lines.
 
 Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
 For N > 1 run under torch.distributed.run: every rank runs its own replica of
@@ -61,71 +69,127 @@ def load_peaks():
 
 
 class ClockSampler:
-    """nvidia-smi clocks and throttle reasons sampled during the timed region."""
-    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
-              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
-              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    """SM clocks and clock-event (throttle) reasons sampled during a timed
+    region: NVML through ctypes every `period_ms` (read-only queries), else
+    nvidia-smi at its own pace.  mark() starts a region, summary() reports the
+    samples taken since the mark."""
+    # NVML clock-event reason bits
+    REASONS = {0x8: "hw_slowdown", 0x40: "hw_thermal_slowdown", 0x20: "sw_thermal_slowdown",
+               0x4: "sw_power_cap"}
 
-    def __init__(self, gpu_index: int, period_ms: int = 100):
-        self.gpu = gpu_index
-        self.period = period_ms
-        self.proc = None
-        self.lines = []
+    def __init__(self, device_index: int, period_ms: float = 2.0, uuid: str = None,
+                 pci_bus_id: str = None):
+        self.index = device_index
+        self.period = period_ms / 1000.0
+        self.uuid, self.pci = uuid, pci_bus_id
+        self.samples = []  # (sm_mhz, max_mhz, reasons bitmask)
         self.first = 0
+        self.source = None
+        self._stop = threading.Event()
+        self.thread = None
+        self.proc = None
+
+    # -- NVML
+    def _nvml(self):
+        import ctypes
+        lib = ctypes.CDLL("libnvidia-ml.so.1")
+        if lib.nvmlInit_v2() != 0:
+            return None
+        h = ctypes.c_void_p()
+        ok = False
+        if self.uuid:
+            ok = lib.nvmlDeviceGetHandleByUUID(self.uuid.encode(), ctypes.byref(h)) == 0
+        if not ok and self.pci:
+            ok = lib.nvmlDeviceGetHandleByPciBusId_v2(self.pci.encode(), ctypes.byref(h)) == 0
+        if not ok:
+            ok = lib.nvmlDeviceGetHandleByIndex_v2(self.index, ctypes.byref(h)) == 0
+        return (lib, h) if ok else None
+
+    def _loop_nvml(self, lib, h):
+        import ctypes
+        clk, mx, rs = ctypes.c_uint(), ctypes.c_uint(), ctypes.c_ulonglong()
+        lib.nvmlDeviceGetMaxClockInfo(h, 1, ctypes.byref(mx))  # NVML_CLOCK_SM
+        reasons_fn = (getattr(lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or
+                      getattr(lib, "nvmlDeviceGetCurrentClocksThrottleReasons", None))
+        while not self._stop.is_set():
+            if lib.nvmlDeviceGetClockInfo(h, 1, ctypes.byref(clk)) == 0:
+                r = 0
+                if reasons_fn is not None and reasons_fn(h, ctypes.byref(rs)) == 0:
+                    r = rs.value
+                self.samples.append((float(clk.value), float(mx.value), int(r)))
+            time.sleep(self.period)
+
+    # -- nvidia-smi fallback
+    FIELDS = ("index,clocks.sm,clocks.max.sm,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def _loop_smi(self):
+        bits = [0x8, 0x40, 0x20, 0x4]
+        for line in self.proc.stdout:
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 7:
+                continue
+            try:
+                sm, mx = float(parts[1]), float(parts[2])
+            except ValueError:
+                continue
+            r = sum(b for b, v in zip(bits, parts[3:7]) if v.lower() == "active")
+            self.samples.append((sm, mx, r))
 
     def __enter__(self):
         try:
+            nv = self._nvml()
+        except (OSError, AttributeError):
+            nv = None
+        if nv is not None:
+            self.source = "nvml"
+            self.thread = threading.Thread(target=self._loop_nvml, args=nv, daemon=True)
+            self.thread.start()
+            return self
+        try:
             self.proc = subprocess.Popen(
-                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", f"-lms={self.period}"],
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms=50"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
-            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.source = "nvidia-smi"
+            self.thread = threading.Thread(target=self._loop_smi, daemon=True)
             self.thread.start()
         except (OSError, FileNotFoundError):
             self.proc = None
         return self
 
-    def _read(self):
-        for line in self.proc.stdout:
-            self.lines.append(line.strip())
-
     def mark(self, wait_s: float = 3.0):
-        """Waits (up to wait_s) until nvidia-smi has produced a sample, so its
-        start-up is over; samples taken from then on are the ones summary()
-        reports."""
+        """Waits (up to wait_s) for a first sample, then starts a region."""
         t_end = time.perf_counter() + wait_s
-        while self.proc is not None and not self.lines and time.perf_counter() < t_end:
-            time.sleep(0.01)
-        self.first = len(self.lines)
+        while self.thread is not None and not self.samples and time.perf_counter() < t_end:
+            time.sleep(0.005)
+        self.first = len(self.samples)
 
     def __exit__(self, *exc):
+        self._stop.set()
         if self.proc is not None:
             self.proc.terminate()
             try:
                 self.proc.wait(timeout=5)
             except subprocess.TimeoutExpired:
                 self.proc.kill()
+        if self.thread is not None:
             self.thread.join(timeout=2)
 
-    def summary(self):
-        sm, mx, reasons = [], None, set()
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for ln in self.lines[self.first:]:
-            parts = [p.strip() for p in ln.split(",")]
-            if len(parts) < 9:
-                continue
-            try:
-                sm.append(float(parts[1]))
-                mx = float(parts[2])
-            except ValueError:
-                continue
-            for name, val in zip(names, parts[5:9]):
-                if val.lower() == "active":
+    def summary(self, start: int = None, end: int = None):
+        sel = self.samples[self.first if start is None else start:end]
+        if not sel:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0,
+                    "source": self.source}
+        reasons = set()
+        for _, _, r in sel:
+            for bit, name in self.REASONS.items():
+                if r & bit:
                     reasons.add(name)
-        if not sm:
-            return {"sm_mhz": None, "sm_max_mhz": mx, "reasons": [], "samples": 0}
-        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
-                "samples": len(sm)}
+        sm = [x[0] for x in sel]
+        return {"sm_mhz": statistics.median(sm), "sm_min_mhz": min(sm), "sm_max_mhz": sel[-1][1],
+                "reasons": sorted(reasons), "samples": len(sel), "source": self.source}
 
 
 def dist_setup():
@@ -227,11 +291,158 @@ def run_reference(args, world, rank):
 
 
 # ------------------------------------------------------------------ GPU legs
+def detail(name: str, obj) -> None:
+    """Per-item measurements that do not belong on the JSON line go to stderr,
+    one JSON object per line."""
+    print(json.dumps({"detail": name, **obj}), file=sys.stderr, flush=True)
+
+
+class Flush:
+    """Writes a buffer of 2.5x the L2 size on `stream` (the L2 flush between
+    timed launches)."""
+
+    def __init__(self, dev, stream):
+        import torch
+        self.buf = torch.empty(int(2.5 * L2_BYTES) // 4, dtype=torch.float32, device=dev)
+        self.stream = stream
+
+    def __call__(self):
+        import torch
+        with torch.cuda.stream(self.stream):
+            self.buf.fill_(1.0)
+
+
+def time_launches(fn, stream, reps: int, flush=None):
+    """Per-call device times (ms) of fn() on `stream`, CUDA events around each
+    call, L2 flushed before each when `flush` is given."""
+    import torch
+    ts = []
+    for _ in range(reps):
+        if flush is not None:
+            flush()
+        s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s.record(stream)
+        fn()
+        e.record(stream)
+        e.synchronize()
+        ts.append(s.elapsed_time(e))
+    return ts
+
+
+def spread(ts):
+    """median / min / p90 of a list of times."""
+    v = sorted(ts)
+    return statistics.median(v), v[0], v[min(len(v) - 1, int(0.9 * len(v)))]
+
+
+def fp16_squares(dev, stream, peaks, args, sizes=(2048, 4096)):
+    """fp16 operands / fp32 accumulation / fp16 output at n^3 in the nn, tn
+    and nt variants ("Metal GEMM Kernels for LoRA Training", section 2):
+    per-launch median with L2 flushed before every launch, against the
+    measured tensor peak."""
+    import torch
+    from dense_gemm_tiled_gb300 import binding, inputs
+    flush = Flush(dev, stream)
+    out = {}
+    for n in sizes:
+        fl = 2.0 * n ** 3
+        row = {}
+        for var in ("nn", "tn", "nt"):
+            tA, tB = inputs.VARIANTS[var]
+            p = inputs.hgemm_square(n, var, seed=70)
+            A, B = p.A.to(dev), p.B.to(dev)
+            C = torch.empty((n, n), dtype=torch.float16, device=dev)
+            call = lambda: binding.gemm(A, B, C, tA, tB, stream=stream)
+            for _ in range(args.warmup):
+                call()
+            med, mn, p90 = spread(time_launches(call, stream, max(10, min(50, args.steps)), flush))
+            ach = fl / (med * 1e-3) / 1e12
+            row[var] = {"tflops": round(ach, 1), "frac": round(ach / peaks["bf16_tflops"], 4),
+                        "us": round(med * 1e3, 2), "us_min": round(mn * 1e3, 2),
+                        "us_p90": round(p90 * 1e3, 2), "path": binding.last_path()}
+            del A, B, C
+        out[str(n)] = row
+    assert binding.check_device_status(stream) == binding.OK
+    return out
+
+
+SKINNY = [  # (name, M, N, K, variant, dtype): the rank-32 LoRA adapter products
+    ("xA", 512, 32, 2048, "nt", "f16"),        # X @ A^T (forward, down to rank 32)
+    ("xAB", 512, 5632, 32, "nt", "f16"),       # (X A^T) @ B^T (forward, back up)
+    ("dGB", 512, 32, 5632, "nn", "f16"),       # dG @ B (backward)
+    ("dGBA", 512, 2048, 32, "nn", "f16"),      # (dG B) @ A
+    ("dA", 32, 2048, 512, "tn", "f16"),        # (dG B)^T X (weight gradient)
+    ("dB", 5632, 32, 512, "tn", "f16"),        # dG^T (X A^T)
+    ("n32_f16", 8192, 32, 8192, "nn", "f16"),  # the sweep's M=8192, N=32, K=8192
+    ("n32_f32", 8192, 32, 8192, "nn", "f32"),
+]
+
+
+def skinny_hbm(dev, stream, peaks, reps: int = 30):
+    """The skinny rank-32 products, bound by HBM bandwidth: algorithmic bytes
+    e * (MK + KN + MN) per call against the measured copy bandwidth.  `us`:
+    one call with L2 flushed before it (median); `b2b_us`: calls issued back
+    to back, device time per call (host-bound when the host issues slower
+    than the GPU runs); `host_us`: the host's time per call; `graph_us`: the
+    call replayed from a CUDA graph, back to back."""
+    import torch
+    from dense_gemm_tiled_gb300 import binding, inputs
+    flush = Flush(dev, stream)
+    out = {}
+    for name, M, N, K, var, dt in SKINNY:
+        tA, tB = inputs.VARIANTS[var]
+        p = inputs.make_problem(M, N, K, tA, tB, dt, "normal", seed=77, std_a=1.0, std_b=0.02)
+        A, B = p.A.to(dev), p.B.to(dev)
+        C = torch.empty((M, N), dtype=p.A.dtype, device=dev)
+        call = lambda: binding.gemm(A, B, C, tA, tB, stream=stream)
+        for _ in range(5):
+            call()
+        torch.cuda.synchronize()
+        med, mn, p90 = spread(time_launches(call, stream, reps, flush))
+        launches = binding.last_launches()
+        # back to back
+        n_b2b = 200
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        e0.record(stream)
+        for _ in range(n_b2b):
+            call()
+        e1.record(stream)
+        t1 = time.perf_counter()
+        e1.synchronize()
+        b2b = e0.elapsed_time(e1) / n_b2b
+        # one call captured in a graph, replayed back to back
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            call()
+        for _ in range(3):
+            g.replay()
+        torch.cuda.synchronize()
+        e0.record()
+        for _ in range(n_b2b):
+            g.replay()
+        e1.record()
+        e1.synchronize()
+        gus = e0.elapsed_time(e1) / n_b2b
+        e = 4 if dt == "f32" else 2
+        nbytes = e * (M * K + K * N + M * N)
+        gbs = nbytes / (med * 1e-3) / 1e9
+        out[name] = {"mnk": f"{M}x{N}x{K} {var} {dt}", "bytes": nbytes, "us": round(med * 1e3, 2),
+                     "gbs": round(gbs, 1), "frac": round(gbs / peaks["hbm_gbs"], 4),
+                     "b2b_us": round(b2b * 1e3, 2), "host_us": round((t1 - t0) / n_b2b * 1e6, 2),
+                     "graph_us": round(gus * 1e3, 2), "launches": launches,
+                     "path": binding.last_path()}
+        del A, B, C, g
+    assert binding.check_device_status(stream) == binding.OK
+    return out
+
+
 def lora_step(dev, stream, reps: int = 20):
     """The 18 GEMMs of one LoRA MLP-block training step ("Metal GEMM Kernels for
     LoRA Training", section 5: T=512, d=2048, FFN=5632, rank 32), fp16 with fp32
-    accumulation: per-GEMM device time (CUDA events, median) and the whole set
-    replayed as one CUDA graph."""
+    accumulation: per-GEMM device time (CUDA events, median; details on
+    stderr) and the whole set replayed as one CUDA graph."""
     import torch
     from dense_gemm_tiled_gb300 import binding, inputs
     gemms = inputs.lora_step_gemms()
@@ -252,15 +463,8 @@ def lora_step(dev, stream, reps: int = 20):
     torch.cuda.synchronize()
     per = {}
     for op in ops:
-        ts = []
-        for _ in range(reps):
-            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            e0.record(stream)
-            one(op)
-            e1.record(stream)
-            e1.synchronize()
-            ts.append(e0.elapsed_time(e1))
-        per[op[0].name] = {"us": statistics.median(ts) * 1e3, "path": binding.last_path(),
+        med, _, _ = spread(time_launches(lambda: one(op), stream, reps))
+        per[op[0].name] = {"us": round(med * 1e3, 2), "path": binding.last_path(),
                            "shape": [op[0].M, op[0].N, op[0].K], "variant": op[0].variant}
     graph = torch.cuda.CUDAGraph()
     with torch.cuda.graph(graph, stream=stream):
@@ -277,9 +481,35 @@ def lora_step(dev, stream, reps: int = 20):
     e1.synchronize()
     graph_ms = e0.elapsed_time(e1) / reps
     flops = sum(2.0 * g.M * g.N * g.K for g in gemms)
-    return {"gemms": len(gemms), "gflop": flops / 1e9, "graph_ms": graph_ms,
-            "graph_tflops": flops / (graph_ms * 1e-3) / 1e12,
-            "sum_of_gemms_ms": sum(v["us"] for v in per.values()) / 1e3, "per_gemm": per}
+    detail("lora_step_per_gemm", per)
+    return {"gemms": len(gemms), "gflop": round(flops / 1e9, 2), "graph_ms": round(graph_ms, 4),
+            "graph_tflops": round(flops / (graph_ms * 1e-3) / 1e12, 1),
+            "sum_of_gemms_ms": round(sum(v["us"] for v in per.values()) / 1e3, 4)}
+
+
+def control(dev, peaks):
+    """Measurement control ("Metal GEMM Kernels for LoRA Training", section
+    9): a bf16 8192^3 torch.matmul (cuBLAS) timed the same way as the
+    driver's measured peak, best of 10 after 3 warm-up calls, compared with
+    that peak; within 10 % means the GPU runs as it did when the peak was
+    taken.  Context only: no product path uses it."""
+    import torch
+    a = torch.randn(8192, 8192, device=dev, dtype=torch.bfloat16)
+    b = torch.randn(8192, 8192, device=dev, dtype=torch.bfloat16)
+    for _ in range(3):
+        torch.matmul(a, b)
+    ts = []
+    for _ in range(10):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        torch.matmul(a, b)
+        e1.record()
+        e1.synchronize()
+        ts.append(e0.elapsed_time(e1))
+    tf = 2.0 * 8192 ** 3 / (min(ts) * 1e-3) / 1e12
+    del a, b
+    return {"bf16_tflops": round(tf, 1), "ratio": round(tf / peaks["bf16_tflops"], 3),
+            "ok": abs(tf / peaks["bf16_tflops"] - 1.0) <= 0.10}
 
 
 TF32_PER_BF16 = 1.1 / 2.25  # nominal dense TF32 / BF16 tensor rates
@@ -320,13 +550,12 @@ def tf32_4096(dev, stream, flops, peaks, args):
             kern.append(ks.elapsed_time(ke))
         kmed = statistics.median(kern)
         ach = flops / (kmed * 1e-3) / 1e12
-        out[var] = {"tflops_call": flops / (statistics.median(call) * 1e-3) / 1e12,
-                    "tflops_kernel": ach, "path": binding.last_path(),
-                    "roofline": {"bound": "tensor", "achieved": ach, "peak": peak,
-                                 "unit": "TFLOP/s", "frac": ach / peak,
-                                 "peak_basis": f"{peaks['source']} bf16 dense burst x "
-                                               f"{TF32_PER_BF16:.4f} (nominal TF32/BF16)"}}
+        out[var] = {"tflops_call": round(flops / (statistics.median(call) * 1e-3) / 1e12, 1),
+                    "tflops_kernel": round(ach, 1), "frac": round(ach / peak, 4),
+                    "path": binding.last_path()}
         del A, B, C
+    out["peak"] = round(peak, 1)
+    out["peak_basis"] = f"{peaks['source']} bf16 burst x {TF32_PER_BF16:.4f} (nominal TF32/BF16)"
     del flush
     assert binding.check_device_status(stream) == binding.OK
     return out
@@ -388,9 +617,11 @@ def attention_step(dev, stream, reps: int = 20, H: int = 16, n: int = 2048, d: i
     graph_ms = e0.elapsed_time(e1) / reps
     flops = sum(2.0 * H * o[7] * o[8] * o[9] for o in ops)
     assert binding.check_device_status(stream) == binding.OK
-    return {"heads": H, "seq": n, "head_dim": d, "gflop": flops / 1e9, "graph_ms": graph_ms,
-            "graph_tflops": flops / (graph_ms * 1e-3) / 1e12,
-            "sum_of_products_ms": sum(v["us"] for v in per.values()) / 1e3, "per_product": per}
+    detail("attention_per_product", per)
+    return {"heads": H, "seq": n, "head_dim": d, "gflop": round(flops / 1e9, 2),
+            "graph_ms": round(graph_ms, 4),
+            "graph_tflops": round(flops / (graph_ms * 1e-3) / 1e12, 1),
+            "sum_of_products_ms": round(sum(v["us"] for v in per.values()) / 1e3, 4)}
 
 
 def run_case(args, local):
@@ -435,6 +666,7 @@ def main():
     ap.add_argument("--no-fp16", action="store_true")
     ap.add_argument("--no-lora", action="store_true")
     ap.add_argument("--no-attention", action="store_true")
+    ap.add_argument("--no-control", action="store_true")
     ap.add_argument("--case", default=None,
                     help="run only one GEMM (e.g. f32_nn_4096, f16_tn_4096, f16_nn_8192, tf32_nt_4096): "
                          "warm-up + steps, one short JSON line; used for profiling")
@@ -458,6 +690,10 @@ def main():
     sms = props.multi_processor_count
     peaks = load_peaks()
     stream = torch.cuda.Stream(dev)
+    uuid = getattr(props, "uuid", None)
+    uuid = f"GPU-{uuid}" if uuid is not None else None
+    pci = (f"{props.pci_domain_id:08x}:{props.pci_bus_id:02x}:{props.pci_device_id:02x}.0"
+           if hasattr(props, "pci_bus_id") else None)
 
     # headline problem, resident in HBM
     A = inputs.uniform((M, K), 60, "f32").to(dev)
@@ -479,9 +715,10 @@ def main():
     kends = [torch.cuda.Event(enable_timing=True) for _ in range(n_kev)]
     for ev in kstarts + kends:
         ev.record(stream)
-    # the clock sampler starts before the warm-up, so that nvidia-smi is
-    # already polling when the timed region begins
-    with ClockSampler(local) as clk:
+    ctl_before = control(dev, peaks) if not args.no_control else None
+    # the clock sampler runs from before the warm-up to the end of the run;
+    # the headline's clocks are the samples of its timed region
+    with ClockSampler(local, uuid=uuid, pci_bus_id=pci) as clk:
         with torch.cuda.stream(stream):
             for _ in range(args.warmup):
                 step()
@@ -502,33 +739,42 @@ def main():
             ends[i].record(stream)
         torch.cuda.synchronize()
         t1 = time.perf_counter()
-    binding.set_kernel_events()
-    barrier(world)
-    launches = binding.total_launches() - launches0
-    path = binding.last_path()
-    wall = max_over_ranks(t1 - t0, world, dev)
-    ms_step = wall / args.steps * 1e3
-    step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
-    avg_step_ms = sum(step_ms) / len(step_ms)
-    kernel_ms = [s.elapsed_time(e) for s, e in zip(kstarts, kends)]  # every KEV_EVERY-th step
-    avg_kernel_ms = sum(kernel_ms) / len(kernel_ms)
-    value = world * flops / (wall / args.steps) / 1e12
-    clocks = clk.summary()
-    assert binding.check_device_status(stream) == binding.OK
+        head_samples = len(clk.samples)
+        binding.set_kernel_events()
+        barrier(world)
+        launches = binding.total_launches() - launches0
+        path = binding.last_path()
+        wall = max_over_ranks(t1 - t0, world, dev)
+        ms_step = wall / args.steps * 1e3
+        step_ms = [s_.elapsed_time(e_) for s_, e_ in zip(starts, ends)]
+        kernel_ms = [s_.elapsed_time(e_) for s_, e_ in zip(kstarts, kends)]  # every KEV_EVERY-th step
+        avg_kernel_ms = sum(kernel_ms) / len(kernel_ms)
+        value = world * flops / (wall / args.steps) / 1e12
+        clocks = clk.summary(end=head_samples)
+        assert binding.check_device_status(stream) == binding.OK
+
+        fp16 = None if args.no_fp16 else fp16_squares(dev, stream, peaks, args)
+        tf32 = None if args.no_fp16 else tf32_4096(dev, stream, flops, peaks, args)
+        skinny = None if args.no_lora else skinny_hbm(dev, stream, peaks)
+        lora = None if args.no_lora else lora_step(dev, stream)
+        attn = None if args.no_attention else attention_step(dev, stream)
+        clocks_run = clk.summary(start=0)
+    ctl_after = control(dev, peaks) if not args.no_control else None
 
     # FP32 FFMA peak from unit counts and clocks: SMs x 128 lanes x 2 flops
     sm_max = clocks.get("sm_max_mhz") or peaks["sm_max_mhz"]
     ffma_peak = sms * FP32_LANES_PER_SM * 2 * sm_max * 1e6 / 1e12
     achieved = flops / (avg_kernel_ms * 1e-3) / 1e12
-    roofline = {"bound": "alu", "achieved": achieved, "peak": ffma_peak, "unit": "TFLOP/s",
-                "frac": achieved / ffma_peak, "traffic": None,
+    med_step, min_step, p90_step = spread(step_ms)
+    roofline = {"bound": "alu", "achieved": round(achieved, 3), "peak": round(ffma_peak, 3),
+                "unit": "TFLOP/s", "frac": round(achieved / ffma_peak, 4), "traffic": None,
                 "kernel": "sgemm_ffma_kernel (fp32, 128x128 tiles, K step 64, paired FMA; "
                           "persistent stream-K launch: 1024 tiles over 152 SMs)",
                 "timing": "CUDA events recorded by the library around the kernel launch "
                           "(gemm_set_kernel_events) on every 4th timed step, average",
                 "peak_basis": f"{sms} SMs x {FP32_LANES_PER_SM} FP32 lanes x 2 x {sm_max:.0f} MHz",
-                "frac_at_median_clock": (achieved / (sms * FP32_LANES_PER_SM * 2 *
-                                                     clocks["sm_mhz"] * 1e6 / 1e12)
+                "frac_at_median_clock": (round(achieved / (sms * FP32_LANES_PER_SM * 2 *
+                                                           clocks["sm_mhz"] * 1e6 / 1e12), 4)
                                          if clocks.get("sm_mhz") else None)}
     # DRAM bytes per launch of this kernel from the committed ncu capture
     tpath = os.path.join(ROOT, "profiles", "traffic.json")
@@ -540,50 +786,7 @@ def main():
             traffic = {}
     if "sgemm_f32_nn_4096" in traffic:
         roofline["traffic"] = traffic["sgemm_f32_nn_4096"]["bytes"]
-        roofline["traffic_unit"] = "bytes per launch (ncu dram read + write)"
         roofline["algorithmic_bytes"] = 4 * (M * K + K * N + M * N)
-
-    # fp16 variants, per-launch timing, L2 flushed before each launch
-    fp16 = None
-    if not args.no_fp16:
-        fp16 = {}
-        flush = torch.empty(int(2.5 * L2_BYTES) // 4, dtype=torch.float32, device=dev)
-        for var in ("nn", "tn", "nt"):
-            tA, tB = inputs.VARIANTS[var]
-            p = inputs.hgemm_square(4096, var, seed=70)
-            Ah, Bh = p.A.to(dev), p.B.to(dev)
-            Ch = torch.empty((M, N), dtype=torch.float16, device=dev)
-            with torch.cuda.stream(stream):
-                for _ in range(args.warmup):
-                    binding.gemm(Ah, Bh, Ch, tA, tB, stream=stream)
-            ts = []
-            reps = max(10, min(50, args.steps))
-            for _ in range(reps):
-                with torch.cuda.stream(stream):
-                    flush.fill_(1.0)
-                s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-                s.record(stream)
-                binding.gemm(Ah, Bh, Ch, tA, tB, stream=stream)
-                e.record(stream)
-                e.synchronize()
-                ts.append(s.elapsed_time(e))
-            hpath = binding.last_path()
-            med = statistics.median(ts)
-            ach = flops / (med * 1e-3) / 1e12
-            fp16[var] = {"tflops": ach, "ms_median": med, "ms_min": min(ts), "path": hpath,
-                         "traffic": (traffic.get(f"hgemm_f16_{var}_4096") or {}).get("bytes"),
-                         "roofline": {"bound": "tensor", "achieved": ach,
-                                      "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
-                                      "frac": ach / peaks["bf16_tflops"],
-                                      "peak_basis": f"{peaks['source']} bf16 dense burst "
-                                                    "(cuBLAS 8192^3) x 1 (fp16 rate = bf16 rate)"}}
-            del Ah, Bh, Ch
-        del flush
-        assert binding.check_device_status(stream) == binding.OK
-
-    tf32 = None if args.no_fp16 else tf32_4096(dev, stream, flops, peaks, args)
-    lora = None if args.no_lora else lora_step(dev, stream)
-    attn = None if args.no_attention else attention_step(dev, stream)
 
     # end to end through gemm_host(): pinned host inputs, result read back
     Ah = inputs.uniform((M, K), 60, "f32").pin_memory()
@@ -606,29 +809,34 @@ def main():
         cpu = cpu_baseline()
 
     if rank == 0:
+        if skinny is not None:
+            detail("skinny_hbm", skinny)
         line = {
             "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
             "data": "synthetic",
             "config": {"workload": WORKLOAD,
-                       "l2": "inputs larger than L2: A, B, C are 192 MiB against a 129 MB L2; "
-                             "fp16 sub-results flush L2 (323 MB write) before each launch",
-                       "parallelism": "replicas" if world > 1 else "single GPU",
-                       "gpu": props.name, "sms": sms},
+                       "l2": "inputs larger than L2 (A, B, C: 192 MiB vs 129 MB); fp16, TF32 "
+                             "and skinny sub-results flush L2 (323 MB write) before each launch",
+                       "parallelism": "replicas" if world > 1 else "single GPU", "sms": sms},
             "path": path,
-            "kernel_ms_avg": avg_kernel_ms,
-            "step_device_ms_avg": avg_step_ms,
+            "step_ms": {"median": round(med_step, 4), "min": round(min_step, 4),
+                        "p90": round(p90_step, 4), "kernel_avg": round(avg_kernel_ms, 4)},
             "roofline": roofline,
-            "fp16_4096": fp16,
-            "tf32_4096": tf32,
-            "lora_step": lora,
-            "attention": attn,
             "e2e": e2e,
             "cpu_baseline": cpu,
             "gpu_launches": launches,
             "clocks": clocks,
-            "peaks": peaks,
+            "clocks_whole_run": clocks_run,
+            "control": {"before": ctl_before, "after": ctl_after},
+            "peaks": {k: peaks[k] for k in ("hbm_gbs", "bf16_tflops", "source")},
+            "attention": attn,
+            "lora_step": lora,
+            "tf32_4096": tf32,
+            "skinny_hbm_frac": ({k: [v["us"], v["frac"], v["b2b_us"]] for k, v in skinny.items()}
+                                if skinny else None),
+            "fp16": fp16,
         }
         print(json.dumps(line), flush=True)
     if world > 1:

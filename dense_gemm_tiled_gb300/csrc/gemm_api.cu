@@ -217,14 +217,14 @@ bool c_scratch_wanted(const void* C, int64_t ldc, int64_t es, int M, int N) {
 }
 
 // Stream-K schedule of the tensor-core kernel (env GEMM_GB300_HG_SK): 1
-// (default) shares out the K steps of a last, part-filled round of tiles when
-// that pays; 0 whole tiles only; 2 shares every tile (forces the shared-tile
-// path, for tests).
+// (default) shares out K steps when that pays; 0 whole tiles only; 2 and 3
+// share every tile, finished inside the kernel (2) or by the reduction kernel
+// (3) -- test settings that force those paths.
 int sk_mode() {
   static const int v = [] {
     const char* e = getenv("GEMM_GB300_HG_SK");
     const int m = e ? atoi(e) : 1;
-    return (m >= 0 && m <= 2) ? m : 1;
+    return (m >= 0 && m <= 3) ? m : 1;
   }();
   return v;
 }
@@ -388,7 +388,7 @@ int run_gemm(int transA, int transB, int64_t M64, int64_t N64, int64_t K64, int 
     void* Cd = c_scr ? (void*)(wp + bytes_a + bytes_b + bytes_w + bytes_n) : C;
     const int64_t ldcd = c_scr ? ldc_p : ldc;
     if (c_scr && beta != 0.f) e = launch_repack_32(M, N, C, ldc, Cd, ldc_p, ctx);
-    if (e == cudaSuccess && pl.sk_workers > 0)
+    if (e == cudaSuccess && pl.cnt_bytes > 0)
       e = cudaMemsetAsync(sk_cnt, 0, pl.cnt_bytes, stream);
     const void* Ad = A;
     const void* Bd = B;
@@ -515,7 +515,7 @@ int run_gemm(int transA, int transB, int64_t M64, int64_t N64, int64_t K64, int 
     void* Cd = c_scr ? (void*)(wp + bytes_a + bytes_b + bytes_w + bytes_n) : C;
     const int64_t ldcd = c_scr ? ldc_p : ldc;
     if (c_scr && beta != 0.f) e = launch_repack_16(M, N, C, ldc, Cd, ldc_p, ctx);
-    if (e == cudaSuccess && pl.sk_workers > 0)
+    if (e == cudaSuccess && pl.cnt_bytes > 0)
       e = cudaMemsetAsync(sk_cnt, 0, pl.cnt_bytes, stream);
     const void* Ad = A;
     const void* Bd = B;
@@ -1116,7 +1116,7 @@ extern "C" int gemm_splitk_noalloc(int transA, int transB, int64_t M, int64_t N,
       pl = hgemm_plan(Mi, Ni, Ki, bn, transA, transB, HG_BK, 1, pair_enabled(), sms, 0);
     unsigned int* cnt = reinterpret_cast<unsigned int*>(
         reinterpret_cast<char*>(scratch) + pad256(pl.ws_bytes));
-    if (pl.sk_workers > 0) e = cudaMemsetAsync(cnt, 0, pl.cnt_bytes, stream);
+    if (pl.cnt_bytes > 0) e = cudaMemsetAsync(cnt, 0, pl.cnt_bytes, stream);
     HgemmArgs a{transA, transB, Mi, Ni, Ki, A, lda, B, ldb, C, ldc, alpha, beta, sms, bn,
                 c_tma_enabled(), g_fault_injection.load()};
     a.dtype = dtype;

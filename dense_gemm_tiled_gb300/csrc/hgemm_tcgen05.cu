@@ -45,10 +45,15 @@ bool hgemm_use_pair(int bn, int M, int allowed) {
 #ifndef GB300_HG_SK_COST_NARROW
 #define GB300_HG_SK_COST_NARROW 16
 #endif
+// ... and when every contributor publishes and a reduction kernel finishes
+#ifndef GB300_HG_SK_COST_PUBLISH
+#define GB300_HG_SK_COST_PUBLISH 24
+#endif
 
 // K steps a stream-K plan adds for finishing shared tiles (0 without).
 int sk_cost_steps(const HPlan& pl) {
   if (pl.sk_workers == 0) return 0;
+  if (pl.sk_publish) return GB300_HG_SK_COST_PUBLISH;
   return pl.bn <= 64 ? GB300_HG_SK_COST_NARROW : GB300_HG_SK_COST_WIDE;
 }
 
@@ -83,7 +88,11 @@ HPlan hgemm_plan(int M, int N, int K, int bn, int transA, int transB, int kstep,
     // partial sums waiting.  Mode 2 shares every tile.
     const int64_t rem = tiles % wmax;
     int64_t shared = rem == 0 ? 0 : (tiles >= 2 * (int64_t)wmax ? rem + wmax : tiles);
-    if (sk_mode == 2) shared = tiles;
+    if (sk_mode >= 2) shared = tiles;
+    // With every tile shared, all ranges end together and race to finish
+    // their tiles; there a reduction kernel over the published sums (every
+    // SM taking part) beats the last contributor's finish (one block or block
+    // pair a tile).
     const int64_t total = shared * steps;
     int64_t skw = total / GB300_HG_SK_MIN_STEPS;
     if (skw > wmax) skw = wmax;
@@ -99,10 +108,12 @@ HPlan hgemm_plan(int M, int N, int K, int bn, int transA, int transB, int kstep,
       sk.workers = sk.dp_tiles > 0 ? wmax : (int)skw;
       const int P = pair ? 2 : 1;
       sk.ws_bytes = (size_t)skw * 2 * P * BM * bn * sizeof(float);
-      sk.cnt_bytes = (size_t)shared * P * 4 * EPI_HALVES * sizeof(unsigned int);
+      sk.sk_publish = sk_mode == 3 || (sk_mode == 1 && sk.dp_tiles == 0);
+      sk.cnt_bytes =
+          sk.sk_publish ? 0 : (size_t)shared * P * 4 * EPI_HALVES * sizeof(unsigned int);
       // shared only where the busiest worker saves more than finishing the
       // shared tiles costs
-      if (sk_mode == 2 || busiest_steps(sk) + sk_cost_steps(sk) < busiest_steps(pl)) pl = sk;
+      if (sk_mode >= 2 || busiest_steps(sk) + sk_cost_steps(sk) < busiest_steps(pl)) pl = sk;
     }
   }
   // Epilogue warps per accumulator quarter.  The epilogue of one unit is

@@ -178,6 +178,9 @@ struct HParams {
   // and puts the counter back to zero.  No block waits for another.
   float* sk_ws;
   unsigned int* sk_cnt;
+  // 1: every contributor only publishes its partial sums and a separate
+  // reduction kernel (hgemm_sk_reduce) finishes the shared tiles; sk_cnt unused
+  int sk_publish;
   float alpha, beta;
   unsigned int* status;
   uint64_t timeout_ns;
@@ -244,6 +247,25 @@ __device__ __forceinline__ int sk_slot(const HParams& p, int w, int64_t s0) {
   return (int64_t)w * p.sk_steps >= s0 * p.sk_workers ? 0 : 1;
 }
 
+// Work tile t -> batch entry bz, then grouped rasterisation within the
+// entry: block `rank`'s first row m0 and the tile's first column n0.
+template <bool PAIR, int TBN>
+__device__ __forceinline__ void tile_origin(const HParams& p, int t, int rank, int& m0, int& n0,
+                                            int& bz) {
+  const int rows = PAIR ? (p.tiles_m + 1) / 2 : p.tiles_m;
+  const int per_entry = rows * p.tiles_n;
+  bz = t / per_entry;
+  t -= bz * per_entry;
+  const int per_group = GROUP_M * p.tiles_n;
+  const int first_m = (t / per_group) * GROUP_M;
+  const int gsize = min(rows - first_m, GROUP_M);
+  const int tr = first_m + (t % per_group) % gsize;
+  const int tn = (t % per_group) / gsize;
+  const int tm = PAIR ? 2 * tr + rank : tr;
+  m0 = tm * BM;
+  n0 = tn * TBN;
+}
+
 // Unit i of worker w (of W); false when the worker has no unit i.  Every role
 // of the block walks the same sequence: the worker's whole tiles first, then
 // the tiles its stream-K range touches, in K order.
@@ -274,19 +296,7 @@ __device__ __forceinline__ bool unit_at(const HParams& p, int w, int W, int i, i
     }
     t = p.dp_tiles + (int)tr;
   }
-  // tile t -> batch entry, then grouped rasterisation within the entry
-  const int rows = PAIR ? (p.tiles_m + 1) / 2 : p.tiles_m;
-  const int per_entry = rows * p.tiles_n;
-  u.bz = t / per_entry;
-  t -= u.bz * per_entry;
-  const int per_group = GROUP_M * p.tiles_n;
-  const int first_m = (t / per_group) * GROUP_M;
-  const int gsize = min(rows - first_m, GROUP_M);
-  const int tr = first_m + (t % per_group) % gsize;
-  const int tn = (t % per_group) / gsize;
-  const int tm = PAIR ? 2 * tr + rank : tr;
-  u.m0 = tm * BM;
-  u.n0 = tn * TBN;
+  tile_origin<PAIR, TBN>(p, t, rank, u.m0, u.n0, u.bz);
   return true;
 }
 
@@ -715,7 +725,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         cnt = p.sk_cnt + (((int64_t)U.sk * (PAIR ? 2 : 1) + rank) * 4 + q) * EPI_HALVES + hh;
         Unit U2;
         final = !unit_at<PAIR, BN>(p, worker, workers, it + 1, rank, U2);
-        if (final && lane == 0 && s_lo < s_hi) seen = ld_acquire(cnt);
+        if (!p.sk_publish && final && lane == 0 && s_lo < s_hi) seen = ld_acquire(cnt);
       }
       // one lane waits, the warp follows: the TMEM loads below are
       // warp-collective, so the whole warp must take the same branch
@@ -747,6 +757,24 @@ __global__ void __launch_bounds__(THREADS, 1)
         // unit) or from the slots with plain loads (earlier units, rare).
         if (s_lo == s_hi) { release_acc(buf); continue; }  // (no columns: not counted)
         const int n_contrib = w_last - w_first + 1;
+        if (p.sk_publish) {
+          // publish only: the reduction kernel finishes every shared tile
+          float* const mine = strip_of(worker, U.slot);
+#pragma unroll 1
+          for (int c = s_lo; c < s_hi; ++c) {
+            uint32_t r[32];
+            __syncwarp();
+            tmem_ld_32x32b_x32(t_row + (uint32_t)(c * 32), r);
+            tmem_ld_wait();
+            if (c == s_hi - 1) release_acc(buf);
+            float4* dst = reinterpret_cast<float4*>(mine) + c * 256 + lane;
+#pragma unroll
+            for (int v = 0; v < 8; ++v)
+              dst[v * 32] = make_float4(__uint_as_float(r[4 * v]), __uint_as_float(r[4 * v + 1]),
+                                        __uint_as_float(r[4 * v + 2]), __uint_as_float(r[4 * v + 3]));
+          }
+          continue;
+        }
         constexpr uint32_t RING = (uint32_t)(STAGES * C_::STAGE_BYTES);
         const uint32_t region_bytes = (RING / (uint32_t)(4 * nh)) & ~4095u;
         const int n_slots = (int)(region_bytes >> 12);
@@ -1073,6 +1101,49 @@ __global__ void __launch_bounds__(THREADS, 1)
   }
 }
 
+// Reduction of shared tiles published by every contributor (sk_publish):
+// one warp per (shared tile, block of the pair, 32-row quarter, 32-column
+// chunk) sums the contributors' chunks in K order -- every load of the warp
+// covers 512 contiguous bytes -- and stores act(alpha * sum + beta * C +
+// bias) for its rows.  Blocks of 8 warps; launched after the GEMM kernel in
+// stream order.
+template <typename T, bool PAIR, int TBN>
+__global__ void __launch_bounds__(256) hgemm_sk_reduce(const HParams p) {
+  pdl_wait();
+  pdl_trigger();
+  constexpr int P = PAIR ? 2 : 1;
+  constexpr int CH = TBN / 32;
+  constexpr int STRIP = 32 * TBN;
+  const int lane = threadIdx.x & 31;
+  const int64_t wid = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
+  const int64_t shared = (int64_t)p.tiles - p.dp_tiles;
+  if (wid >= shared * P * 4 * CH) return;
+  const int c = (int)(wid % CH);
+  const int q = (int)((wid / CH) % 4);
+  const int rank = (int)((wid / (CH * 4)) % P);
+  const int64_t tr = wid / (CH * 4 * P);
+  int m0, n0, bz;
+  tile_origin<PAIR, TBN>(p, p.dp_tiles + (int)tr, rank, m0, n0, bz);
+  const int64_t s0 = tr * p.steps;
+  const int w_first = sk_owner(p, s0), w_last = sk_owner(p, s0 + p.steps - 1);
+  if (w_first == w_last) return;  // one range covered the tile: stored as a whole one
+  float v[32];
+#pragma unroll
+  for (int j = 0; j < 32; ++j) v[j] = 0.f;
+  for (int w2 = w_first; w2 <= w_last; ++w2) {
+    const float4* src =
+        reinterpret_cast<const float4*>(p.sk_ws + ((((int64_t)w2 * 2 + sk_slot(p, w2, s0)) * P +
+                                                    rank) * 4 + q) * STRIP) + c * 256 + lane;
+#pragma unroll
+    for (int w = 0; w < 8; ++w) {
+      const float4 f = __ldcg(src + w * 32);
+      v[4 * w] += f.x; v[4 * w + 1] += f.y; v[4 * w + 2] += f.z; v[4 * w + 3] += f.w;
+    }
+  }
+  const int gm = m0 + q * 32 + lane, gn0 = n0 + c * 32;
+  if (gm < p.M && gn0 < p.N) store_c32<T>(p, bz, gm, gn0, v);
+}
+
 // ---------------------------------------------------------------- host side
 PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
   static const PFN_cuTensorMapEncodeTiled_v12000 fn = [] {
@@ -1230,7 +1301,14 @@ cudaError_t launch_cfg(const HgemmArgs& a, const HParams& p, LaunchCtx& ctx) {
   ctx.grid = PAIR ? 2 * workers : workers;
   e = launch_kernel(kern, dim3(ctx.grid), dim3(THREADS), C_::SMEM_BYTES, ctx.stream, PAIR ? 2 : 1,
                     mA, mB, mC, pp);
-  if (e == cudaSuccess) ctx.launches++;
+  if (e != cudaSuccess) return e;
+  ctx.launches++;
+  if (pp.sk_workers > 0 && pp.sk_publish) {
+    const int64_t warps = ((int64_t)pp.tiles - pp.dp_tiles) * (PAIR ? 2 : 1) * 4 * (BN / 32);
+    e = launch_kernel(hgemm_sk_reduce<T, PAIR, BN>, dim3((unsigned)((warps + 7) / 8)), dim3(256),
+                      0, ctx.stream, 1, pp);
+    if (e == cudaSuccess) ctx.launches++;
+  }
   return e;
 }
 
@@ -1283,6 +1361,7 @@ cudaError_t launch_hgemm_t(const HgemmArgs& a, LaunchCtx& ctx) {
   p.m_steps = magic((uint64_t)pl.steps);
   p.sk_ws = a.sk_ws;
   p.sk_cnt = a.sk_cnt;
+  p.sk_publish = pl.sk_publish;
   p.alpha = a.alpha; p.beta = a.beta;
   p.status = ctx.status;
   p.timeout_ns = ctx.timeout_ns;
@@ -1299,7 +1378,7 @@ cudaError_t launch_hgemm_t(const HgemmArgs& a, LaunchCtx& ctx) {
   p.ep = a.ep;
   p.epi_halves = pl.epi_halves;
   if (pl.workers <= 0 || pl.steps <= 0 || pl.bn != bn) return cudaErrorInvalidValue;
-  if (pl.sk_workers > 0 && (!a.sk_ws || !a.sk_cnt)) return cudaErrorInvalidValue;
+  if (pl.sk_workers > 0 && (!a.sk_ws || (!pl.sk_publish && !a.sk_cnt))) return cudaErrorInvalidValue;
   switch (bn) {
     case 32: return launch_bn<T, 32>(a, p, ctx);
     case 64: return launch_bn<T, 64>(a, p, ctx);

@@ -62,6 +62,7 @@ struct HPlan {
   int dp_tiles = 0;           // whole tiles
   int sk_workers = 0;         // ranges of the shared steps (0: no sharing)
   int64_t sk_steps = 0;       // (tiles - dp_tiles) * steps
+  int sk_publish = 0;         // 1: every contributor publishes; a reduction kernel finishes
   int epi_halves = 1;         // epilogue warps per accumulator quarter
   size_t ws_bytes = 0;        // fp32 partial slots: sk_workers x 2 x (pair ? 2 : 1) x 128 x bn
   size_t cnt_bytes = 0;       // arrival counters, zero before the launch
@@ -175,8 +176,11 @@ bool hgemm_use_pair(int bn, int M, int allowed);
 int hgemm_pair_slots(int bn, int transA, int transB, int num_sms);
 // Schedule of a tcgen05 launch.  kstep: K elements per step (64 for 16-bit
 // operands, 32 for TF32); pair_allowed: 0 or 2; sk_mode: 0 whole tiles only,
-// 1 share the steps of a last, part-filled round of tiles when that pays, 2
-// share every tile (a test setting).
+// 1 share K steps when that pays (the last one or two rounds of tiles,
+// finished inside the kernel; or, with fewer tiles than workers, every tile,
+// finished by a reduction kernel), 2 share every tile and finish inside the
+// kernel, 3 share every tile and finish with the reduction kernel (2 and 3
+// are test settings).
 HPlan hgemm_plan(int M, int N, int K, int bn, int transA, int transB, int kstep, int batch,
                  int pair_allowed, int num_sms, int sk_mode);
 

@@ -6,9 +6,10 @@ or the K steps of a last, part-filled round of tiles shared out over the
 persistent grid (stream-K, shared tiles finished by their last contributor).
 Each configuration is forced here in its own process (the switches are read
 once per process from GEMM_GB300_HG_PAIR, GEMM_GB300_HG_BN and
-GEMM_GB300_HG_SK; SK=2 shares every tile, so every tile goes through the
-partial-sum path) and checked on ragged, multi-tile problems in all four
-variants, exact on small-integer inputs.
+GEMM_GB300_HG_SK; SK=2 and SK=3 share every tile, so every tile goes through
+the partial-sum path, finished inside the kernel (2) or by the reduction
+kernel (3)) and checked on ragged, multi-tile problems in all four variants,
+exact on small-integer inputs.
 """
 import os
 import subprocess
@@ -51,10 +52,11 @@ print("ok")
 """
 
 
-@pytest.mark.parametrize("pair,bn,sk", [("2", "256", "1"), ("2", "256", "2"), ("2", "256", "0"),
-                                        ("2", "128", "1"), ("2", "128", "2"), ("0", "256", "2"),
+@pytest.mark.parametrize("pair,bn,sk", [("2", "256", "1"), ("2", "256", "2"), ("2", "256", "3"),
+                                        ("2", "256", "0"), ("2", "128", "1"), ("2", "128", "2"),
+                                        ("2", "128", "3"), ("0", "256", "2"), ("0", "256", "3"),
                                         ("0", "256", "0"), ("0", "128", "2"), ("0", "192", "2"),
-                                        ("0", "64", "2"), ("0", "64", "1")])
+                                        ("0", "64", "2"), ("0", "64", "3"), ("0", "64", "1")])
 def test_forced_kernel_configuration(lib_path, gpu, pair, bn, sk):
     env = dict(os.environ, GEMM_GB300_HG_PAIR=pair, GEMM_GB300_HG_BN=bn, GEMM_GB300_HG_SK=sk)
     code = SCRIPT.format(root=ROOT, tests=os.path.join(ROOT, "tests"))
@@ -132,3 +134,29 @@ def test_fp32_narrow_tile(lib_path, gpu, narrow):
     r = subprocess.run([sys.executable, "-c", code], env=env, capture_output=True, text=True,
                        timeout=900)
     assert r.returncode == 0 and r.stdout.strip().endswith("ok"), r.stdout[-3000:] + r.stderr[-3000:]
+
+
+SCRIPT_LAUNCHES = r"""
+import sys
+sys.path.insert(0, {root!r}); sys.path.insert(0, {tests!r})
+from dense_gemm_tiled_gb300 import binding, inputs
+from helpers import check_problem
+# a LoRA adapter product (rank-32 output, K = 2048): 4 tiles shared by 16 ranges
+p = inputs.make_problem(512, 32, 2048, False, True, "f16", "uniform", seed=242)
+r = check_problem(p)
+print(r["path"], binding.last_launches())
+"""
+
+
+@pytest.mark.parametrize("sk,launches", [("2", 1), ("3", 2)])
+def test_shared_tile_finishing_launches(lib_path, gpu, sk, launches):
+    """Shared tiles finished inside the GEMM kernel by each tile's last
+    contributor take one launch (GEMM_GB300_HG_SK=2); finished by the
+    reduction kernel over every contributor's published sums, two
+    (GEMM_GB300_HG_SK=3)."""
+    env = dict(os.environ, GEMM_GB300_HG_SK=sk)
+    code = SCRIPT_LAUNCHES.format(root=ROOT, tests=os.path.join(ROOT, "tests"))
+    r = subprocess.run([sys.executable, "-c", code], env=env, capture_output=True, text=True,
+                       timeout=600)
+    assert r.returncode == 0, r.stdout[-3000:] + r.stderr[-3000:]
+    assert r.stdout.split()[-2:] == ["tc_splitk", str(launches)], r.stdout

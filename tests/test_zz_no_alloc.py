@@ -60,7 +60,7 @@ SPLIT_PATHS = ("tc_splitk", "ffma_splitk")
 
 @pytest.mark.parametrize("dtype,variant,shape,dist,split", [
     ("f16", "nt", (512, 32, 5632), "uniform", True),   # LoRA adapter shapes: shared K
-    ("f16", "nn", (512, 32, 2048), "uniform", True),
+    ("f16", "nn", (512, 32, 4096), "uniform", True),
     ("f16", "nt", (512, 32, 5632), "integer", True),   # bit-exact through the shared tiles
     ("f32", "tn", (512, 32, 5632), "uniform", True),   # narrow fp32 tile, split K
     ("f32", "nn", (1000, 32, 3000), "integer", True),
