@@ -17,6 +17,8 @@ line carries, measured in the same run:
              LoRA Training", section 2), L2 flushed before every launch,
              against the measured tensor peak;
   tf32_4096  the opt-in TF32 path at 4096^3;
+  tf32x3_4096  the opt-in 3xTF32 path (fp32 accuracy on the tensor cores) on
+             the headline problem;
   skinny_hbm_frac  the rank-32 LoRA adapter products and M=8192, N=32,
              K=8192 against the measured HBM bandwidth: [us, frac, b2b_us];
   lora_step, attention  the LoRA MLP-block step's 18 GEMMs and one attention
@@ -515,6 +517,46 @@ def control(dev, peaks):
 TF32_PER_BF16 = 1.1 / 2.25  # nominal dense TF32 / BF16 tensor rates
 
 
+def tf32x3_4096(dev, stream, flops, peaks, args):
+    """The opt-in 3xTF32 path (fp32 operands split into TF32 hi and lo parts,
+    hi*hi + hi*lo + lo*hi on kind::tf32 MMAs: fp32 accuracy on the tensor
+    cores) at the headline problem, fp32 nn 4096^3: the whole call (split
+    pre-pass included) and the MMA kernel alone, L2 flushed before each call.
+    Throughput in fp32 flops (2*M*N*K); the kernel's own roof is the TF32
+    peak over 3 (three MMAs per product)."""
+    import torch
+    from dense_gemm_tiled_gb300 import binding
+    from dense_gemm_tiled_gb300 import inputs
+    flush = Flush(dev, stream)
+    A = inputs.uniform((M, K), 60, "f32").to(dev)
+    B = inputs.uniform((K, N), 61, "f32").to(dev)
+    C = torch.empty((M, N), dtype=torch.float32, device=dev)
+    call = lambda: binding.gemm(A, B, C, stream=stream, tf32x3=True)
+    for _ in range(args.warmup):
+        call()
+    ks, ke = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ks.record(stream); ke.record(stream)
+    calls, kern = [], []
+    for _ in range(max(10, min(30, args.steps))):
+        flush()
+        s_, e_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        binding.set_kernel_events(ks, ke)
+        s_.record(stream)
+        call()
+        e_.record(stream)
+        binding.set_kernel_events()
+        e_.synchronize()
+        calls.append(s_.elapsed_time(e_))
+        kern.append(ks.elapsed_time(ke))
+    peak = peaks["bf16_tflops"] * TF32_PER_BF16 / 3.0
+    kmed = statistics.median(kern)
+    ach = flops / (kmed * 1e-3) / 1e12
+    assert binding.check_device_status(stream) == binding.OK
+    return {"tflops_call": round(flops / (statistics.median(calls) * 1e-3) / 1e12, 1),
+            "tflops_kernel": round(ach, 1), "frac": round(ach / peak, 4), "peak": round(peak, 1),
+            "path": binding.last_path()}
+
+
 def tf32_4096(dev, stream, flops, peaks, args):
     """The opt-in TF32 path (fp32 operands on kind::tf32 MMAs) at 4096^3, nt
     (operands already K-major) and nn (B packed first): per-launch medians
@@ -755,6 +797,7 @@ def main():
 
         fp16 = None if args.no_fp16 else fp16_squares(dev, stream, peaks, args)
         tf32 = None if args.no_fp16 else tf32_4096(dev, stream, flops, peaks, args)
+        tf32x3 = None if args.no_fp16 else tf32x3_4096(dev, stream, flops, peaks, args)
         skinny = None if args.no_lora else skinny_hbm(dev, stream, peaks)
         lora = None if args.no_lora else lora_step(dev, stream)
         attn = None if args.no_attention else attention_step(dev, stream)
@@ -834,6 +877,7 @@ def main():
             "attention": attn,
             "lora_step": lora,
             "tf32_4096": tf32,
+            "tf32x3_4096": tf32x3,
             "skinny_hbm_frac": ({k: [v["us"], v["frac"], v["b2b_us"]] for k, v in skinny.items()}
                                 if skinny else None),
             "fp16": fp16,

@@ -52,6 +52,7 @@ F32 = 0
 F16_F32ACC = 1
 BF16_F32ACC = 2
 F32_TF32 = 3
+F32_3XTF32 = 4
 OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_ALIAS, ERR_CUDA, ERR_NO_MEMORY, ERR_TIMEOUT = range(7)
 PATHS = {0: "none", 1: "scale", 2: "ffma", 3: "ffma_splitk", 4: "tc", 5: "tc_splitk",
          6: "ffma_batched", 7: "tc_batched", 8: "per_entry"}
@@ -231,8 +232,26 @@ def _dims(A, B, C, transA, transB):
 ACTS = {"none": 0, "relu": 1, "gelu": 2}
 
 
+def _current_stream(device_index: int) -> int:
+    """Raw handle of the current CUDA stream of a device."""
+    import torch
+    get_raw = getattr(torch._C, "_cuda_getCurrentRawStream", None)
+    if get_raw is not None:
+        return get_raw(device_index)
+    return torch.cuda.current_stream(device_index).cuda_stream
+
+
+def _ld_of(shape, stride) -> int:
+    """_ld from a 2-D shape and stride already fetched."""
+    if shape[1] > 1 and stride[1] != 1:
+        raise ValueError("rows must be contiguous (stride(1) == 1)")
+    if shape[0] <= 1:
+        return max(stride[0], shape[1], 1)
+    return stride[0]
+
+
 def gemm(A, B, C, transA=False, transB=False, alpha=1.0, beta=0.0, stream=None, bias=None,
-         act="none", tf32=False):
+         act="none", tf32=False, tf32x3=False):
     """C = act(alpha * op(A) @ op(B) + beta * C + bias) in place, on torch CUDA
     tensors.
 
@@ -241,38 +260,55 @@ def gemm(A, B, C, transA=False, transB=False, alpha=1.0, beta=0.0, stream=None, 
     contiguous, any leading dimension.  bias: None or a contiguous CUDA tensor
     of N elements of C's dtype (per output column); act: 'none', 'relu' or
     'gelu'.  tf32=True (float32 tensors only) opts into the reduced-precision
-    TF32 tensor-core path.  Runs on `stream` (a torch.cuda.Stream) or the
-    current stream.  Returns C.
+    TF32 tensor-core path; tf32x3=True into the 3xTF32 tensor-core path (about
+    fp32 accuracy, finite inputs).  Runs on `stream` (a torch.cuda.Stream) or
+    the current stream.  Returns C.
     """
-    import torch
-    dtype, M, N, K = _dims(A, B, C, transA, transB)
-    if tf32:
-        if dtype != F32:
-            raise TypeError("tf32=True takes float32 tensors")
-        dtype = F32_TF32
-    for t in (A, B, C):
-        if not t.is_cuda:
-            raise ValueError("gemm() takes CUDA tensors; use gemm_host() for host memory")
-    s = stream if stream is not None else torch.cuda.current_stream(C.device)
+    dt = A.dtype
+    dtype = _DTYPES.get(dt)
+    if dtype is None or B.dtype != dt or C.dtype != dt:
+        if B.dtype != dt or C.dtype != dt:
+            raise TypeError("A, B and C must share a dtype")
+        raise TypeError(f"unsupported dtype {dt}")
+    sa, sb, sc = A.shape, B.shape, C.shape
+    if len(sa) != 2 or len(sb) != 2 or len(sc) != 2:
+        raise ValueError("matrices are 2-D")
+    M, K = (sa[1], sa[0]) if transA else (sa[0], sa[1])
+    Kb, N = (sb[1], sb[0]) if transB else (sb[0], sb[1])
+    if K != Kb:
+        raise ValueError(f"inner dimensions differ: {K} vs {Kb}")
+    if sc[0] != M or sc[1] != N:
+        raise ValueError(f"C is {tuple(sc)}, expected {(M, N)}")
+    if tf32 or tf32x3:
+        if dtype != F32 or (tf32 and tf32x3):
+            raise TypeError("tf32=True or tf32x3=True (one of them) takes float32 tensors")
+        dtype = F32_TF32 if tf32 else F32_3XTF32
+    if not (A.is_cuda and B.is_cuda and C.is_cuda):
+        raise ValueError("gemm() takes CUDA tensors; use gemm_host() for host memory")
+    s = stream.cuda_stream if stream is not None else _current_stream(C.get_device())
+    lda, ldb, ldc = _ld_of(sa, A.stride()), _ld_of(sb, B.stride()), _ld_of(sc, C.stride())
     if bias is not None or act != "none":
         if bias is not None:
             if not bias.is_cuda or bias.dtype != C.dtype or bias.numel() != N or \
                     not bias.is_contiguous():
                 raise ValueError("bias: a contiguous CUDA tensor of N elements of C's dtype")
         rc = _lib.gemm_ex(int(transA), int(transB), M, N, K, dtype, float(alpha), float(beta),
-                          A.data_ptr() or None, _ld(A), B.data_ptr() or None, _ld(B),
-                          C.data_ptr() or None, _ld(C),
+                          A.data_ptr() or None, lda, B.data_ptr() or None, ldb,
+                          C.data_ptr() or None, ldc,
                           (bias.data_ptr() or None) if bias is not None else None, ACTS[act],
-                          s.cuda_stream or None)
+                          s or None)
         if rc != OK:
             raise GemmError(rc)
         return C
-    rc = _lib.gemm(int(transA), int(transB), M, N, K, dtype, float(alpha), float(beta),
-                   A.data_ptr() or None, _ld(A), B.data_ptr() or None, _ld(B),
-                   C.data_ptr() or None, _ld(C), s.cuda_stream or None)
+    rc = _gemm_fn(int(transA), int(transB), M, N, K, dtype, float(alpha), float(beta),
+                  A.data_ptr() or None, lda, B.data_ptr() or None, ldb, C.data_ptr() or None,
+                  ldc, s or None)
     if rc != OK:
         raise GemmError(rc)
     return C
+
+
+_gemm_fn = _lib.gemm
 
 
 def gemm_host(A, B, C, transA=False, transB=False, alpha=1.0, beta=0.0, stream=None):

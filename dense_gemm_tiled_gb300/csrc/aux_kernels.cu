@@ -283,6 +283,113 @@ cudaError_t launch_copy_rows(int esize, int rows, int cols, const void* src, int
   return e;
 }
 
+// ---------------------------------------------------------------- 3xTF32 split
+// An fp32 value x as hi + lo with hi its TF32 part (sign, exponent and the
+// top 10 fraction bits: x with the low 13 fraction bits cleared, i.e.
+// truncated toward zero) and lo = x - hi, which is exact in fp32 (hi and x
+// share their leading bits) and below 2^-10 |x|.  A tensor core fed hi and lo
+// as TF32 operands recovers x * y, to about 2^-20 relative, as hi(x) hi(y) +
+// hi(x) lo(y) + lo(x) hi(y).  Infinities and NaNs are kept in hi (lo = 0).
+__device__ __forceinline__ void tf32_split(float x, float& hi, float& lo) {
+  if (!isfinite(x)) {
+    hi = x;
+    lo = 0.f;
+    return;
+  }
+  hi = __uint_as_float(__float_as_uint(x) & 0xffffe000u);
+  lo = x - hi;
+}
+
+// dst_hi[r][c], dst_lo[r][c] (row pitch ld_dst, 16-byte aligned rows) from
+// src[r][c] for c < cols, zero for cols <= c < ld_dst.  One thread per 4
+// destination columns.
+__global__ void __launch_bounds__(256) split_rows_kernel(int rows, int cols,
+                                                         const float* __restrict__ src,
+                                                         int64_t ld_src, float* __restrict__ hi,
+                                                         float* __restrict__ lo, int64_t ld_dst) {
+  pdl_wait();
+  pdl_trigger();
+  const int q = (int)(ld_dst / 4);
+  const int64_t total = (int64_t)rows * q;
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total;
+       i += (int64_t)gridDim.x * blockDim.x) {
+    const int r = (int)(i / q), c = (int)(i - (int64_t)r * q) * 4;
+    float h[4], l[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const float x = c + e < cols ? src[(int64_t)r * ld_src + c + e] : 0.f;
+      tf32_split(x, h[e], l[e]);
+    }
+    *reinterpret_cast<float4*>(hi + (int64_t)r * ld_dst + c) = make_float4(h[0], h[1], h[2], h[3]);
+    *reinterpret_cast<float4*>(lo + (int64_t)r * ld_dst + c) = make_float4(l[0], l[1], l[2], l[3]);
+  }
+}
+
+// The transposing counterpart: dst[c][r] from src[r][c] (src rows x cols,
+// dst cols x rows), 64 x 64 tiles through shared memory as in
+// transpose_f32_kernel, split on the way out.  Destination columns r in
+// [rows, ld_dst) are not written (the caller zeroes them or never reads them).
+__global__ void __launch_bounds__(256) split_transpose_kernel(int rows, int cols,
+                                                              const float* __restrict__ src,
+                                                              int64_t ld_src, float* __restrict__ hi,
+                                                              float* __restrict__ lo,
+                                                              int64_t ld_dst) {
+  pdl_wait();
+  pdl_trigger();
+  __shared__ float tile[64][65];
+  const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
+  const int tiles_c = (cols + 63) / 64;
+  const int64_t tiles = (int64_t)((rows + 63) / 64) * tiles_c;
+  for (int64_t t = blockIdx.x; t < tiles; t += gridDim.x) {
+    const int r0 = (int)(t / tiles_c) * 64, c0 = (int)(t % tiles_c) * 64;
+#pragma unroll
+    for (int p = 0; p < 4; ++p) {
+      const int rr = ty + 16 * p, r = r0 + rr;
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int c = c0 + 4 * tx + e;
+        tile[rr][4 * tx + e] = (r < rows && c < cols) ? src[(int64_t)r * ld_src + c] : 0.f;
+      }
+    }
+    __syncthreads();
+#pragma unroll
+    for (int p = 0; p < 4; ++p) {
+      const int cc = ty + 16 * p, c = c0 + cc, r = r0 + 4 * tx;
+      if (c < cols) {
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          if (r + e >= rows) continue;
+          float h, l;
+          tf32_split(tile[4 * tx + e][cc], h, l);
+          hi[(int64_t)c * ld_dst + r + e] = h;
+          lo[(int64_t)c * ld_dst + r + e] = l;
+        }
+      }
+    }
+    __syncthreads();
+  }
+}
+
+cudaError_t launch_split_tf32(bool transpose, int rows, int cols, const float* src,
+                              int64_t ld_src, float* hi, float* lo, int64_t ld_dst,
+                              LaunchCtx& ctx) {
+  cudaError_t e;
+  if (!transpose) {
+    if ((ld_dst % 4) != 0 || ((reinterpret_cast<uintptr_t>(hi) | reinterpret_cast<uintptr_t>(lo)) & 15u))
+      return cudaErrorInvalidValue;
+    const int grid = grid_for((int64_t)rows * (ld_dst / 4), 256);
+    e = launch_kernel(split_rows_kernel, dim3(grid), dim3(256), 0, ctx.stream, 1, rows, cols, src,
+                      ld_src, hi, lo, ld_dst);
+  } else {
+    const int64_t tiles = (int64_t)((rows + 63) / 64) * ((cols + 63) / 64);
+    const int grid = grid_for(tiles * 256, 256);
+    e = launch_kernel(split_transpose_kernel, dim3(grid), dim3(256), 0, ctx.stream, 1, rows, cols,
+                      src, ld_src, hi, lo, ld_dst);
+  }
+  if (e == cudaSuccess) ctx.launches++;
+  return e;
+}
+
 cudaError_t launch_repack_32(int rows, int cols, const void* src, int64_t ld_src, void* dst,
                              int64_t ld_dst, LaunchCtx& ctx) {
   return launch_repack<uint32_t>(rows, cols, src, ld_src, dst, ld_dst, ctx);

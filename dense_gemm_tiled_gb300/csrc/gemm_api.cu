@@ -99,8 +99,11 @@ int device_state(int* dev_out, unsigned int** status, int* sms) {
 
 // Bytes per element of a gemm_dtype_t, and the output kind the auxiliary
 // kernels take (0 fp32, 1 fp16, 2 bf16).
-inline int64_t esize(int dtype) { return (dtype == GEMM_F32 || dtype == GEMM_F32_TF32) ? 4 : 2; }
-inline int out_kind(int dtype) { return dtype == GEMM_F32_TF32 ? 0 : dtype; }
+inline bool is_f32(int dtype) {
+  return dtype == GEMM_F32 || dtype == GEMM_F32_TF32 || dtype == GEMM_F32_3XTF32;
+}
+inline int64_t esize(int dtype) { return is_f32(dtype) ? 4 : 2; }
+inline int out_kind(int dtype) { return is_f32(dtype) ? 0 : dtype; }
 
 inline int64_t footprint_bytes(int64_t rows, int64_t cols, int64_t ld, int64_t e) {
   if (rows <= 0 || cols <= 0) return 0;
@@ -120,7 +123,7 @@ int check_args(int transA, int transB, int64_t M, int64_t N, int64_t K, int dtyp
                int64_t* b_cols) {
   if ((transA != 0 && transA != 1) || (transB != 0 && transB != 1)) return GEMM_ERR_INVALID_ARG;
   if (dtype != GEMM_F32 && dtype != GEMM_F16_F32ACC && dtype != GEMM_BF16_F32ACC &&
-      dtype != GEMM_F32_TF32)
+      dtype != GEMM_F32_TF32 && dtype != GEMM_F32_3XTF32)
     return GEMM_ERR_INVALID_ARG;
   if (M < 0 || N < 0 || K < 0) return GEMM_ERR_INVALID_ARG;
   const int64_t lim = (int64_t)1 << 31;
@@ -359,17 +362,23 @@ int run_gemm(int transA, int transB, int64_t M64, int64_t N64, int64_t K64, int 
   if (K == 0) {
     path = GEMM_PATH_SCALE;
     e = launch_scale(out_kind(dtype), M, N, C, ldc, beta, ctx, ep);
-  } else if (dtype == GEMM_F32_TF32) {
+  } else if (dtype == GEMM_F32_TF32 || dtype == GEMM_F32_3XTF32) {
     // Opt-in TF32: the tcgen05 kernel on kind::tf32 reads K-major fp32
     // operands in 16-byte aligned rows, A [M, K] and B [N, K]; others are
-    // transposed or re-pitched into scratch first.
-    const int bn = hgemm_pick_bn(M, N, K, 0, 1, 32, 1, pair_enabled(), sms, sk_mode());
-    const HPlan pl = hgemm_plan(M, N, K, bn, 0, 1, 32, 1, pair_enabled(), sms, sk_mode());
-    const bool a_ok = !transA && ((uintptr_t)A % 16) == 0 && (lda % 4) == 0;
-    const bool b_ok = transB && ((uintptr_t)B % 16) == 0 && (ldb % 4) == 0;
+    // transposed or re-pitched into scratch first.  3xTF32: every operand is
+    // split into TF32 hi and lo planes (K-major, in scratch) and the kernel
+    // runs hi*hi + hi*lo + lo*hi over one K loop of three segments.
+    const bool x3 = dtype == GEMM_F32_3XTF32;
     const int64_t ldk = (K + 3) / 4 * 4;
-    const size_t bytes_a = a_ok ? 0 : pad256((size_t)M * ldk * 4);
-    const size_t bytes_b = b_ok ? 0 : pad256((size_t)N * ldk * 4);
+    const int steps_k = (K + 31) / 32;
+    const int K_eff = x3 ? 3 * steps_k * 32 : K;
+    const int bn = hgemm_pick_bn(M, N, K_eff, 0, 1, 32, 1, pair_enabled(), sms, sk_mode());
+    const HPlan pl = hgemm_plan(M, N, K_eff, bn, 0, 1, 32, 1, pair_enabled(), sms, sk_mode());
+    const bool a_ok = !x3 && !transA && ((uintptr_t)A % 16) == 0 && (lda % 4) == 0;
+    const bool b_ok = !x3 && transB && ((uintptr_t)B % 16) == 0 && (ldb % 4) == 0;
+    const int planes = x3 ? 2 : 1;
+    const size_t bytes_a = a_ok ? 0 : pad256((size_t)planes * M * ldk * 4);
+    const size_t bytes_b = b_ok ? 0 : pad256((size_t)planes * N * ldk * 4);
     const size_t bytes_w = pad256(pl.ws_bytes), bytes_n = pad256(pl.cnt_bytes);
     const bool c_scr = c_scratch_wanted(C, ldc, 4, M, N);
     const int64_t ldc_p = (N + 3) / 4 * 4;
@@ -393,15 +402,26 @@ int run_gemm(int transA, int transB, int64_t M64, int64_t N64, int64_t K64, int 
     const void* Ad = A;
     const void* Bd = B;
     int64_t ldad = lda, ldbd = ldb;
-    if (e == cudaSuccess && !a_ok) {
-      e = transA ? launch_transpose_f32(K, M, (const float*)A, lda, At, ldk, ctx)
-                 : launch_repack_32(M, K, A, lda, At, ldk, ctx);
+    if (e == cudaSuccess && x3) {
+      // A [M,K] rows, or A [K,M] transposed; B [N,K] rows, or B [K,N] transposed
+      e = launch_split_tf32(transA != 0, transA ? K : M, transA ? M : K, (const float*)A, lda, At,
+                            At + (int64_t)M * ldk, ldk, ctx);
+      if (e == cudaSuccess)
+        e = launch_split_tf32(transB == 0, transB ? N : K, transB ? K : N, (const float*)B, ldb,
+                              Bt, Bt + (int64_t)N * ldk, ldk, ctx);
       Ad = At; ldad = ldk;
-    }
-    if (e == cudaSuccess && !b_ok) {
-      e = !transB ? launch_transpose_f32(K, N, (const float*)B, ldb, Bt, ldk, ctx)
-                  : launch_repack_32(N, K, B, ldb, Bt, ldk, ctx);
       Bd = Bt; ldbd = ldk;
+    } else {
+      if (e == cudaSuccess && !a_ok) {
+        e = transA ? launch_transpose_f32(K, M, (const float*)A, lda, At, ldk, ctx)
+                   : launch_repack_32(M, K, A, lda, At, ldk, ctx);
+        Ad = At; ldad = ldk;
+      }
+      if (e == cudaSuccess && !b_ok) {
+        e = !transB ? launch_transpose_f32(K, N, (const float*)B, ldb, Bt, ldk, ctx)
+                    : launch_repack_32(N, K, B, ldb, Bt, ldk, ctx);
+        Bd = Bt; ldbd = ldk;
+      }
     }
     if (e == cudaSuccess) {
       HgemmArgs a{0, 1, M, N, K, Ad, ldad, Bd, ldbd, Cd, ldcd, alpha, beta, sms, bn,
@@ -411,6 +431,11 @@ int run_gemm(int transA, int transB, int64_t M64, int64_t N64, int64_t K64, int 
       a.sk_ws = sk_ws;
       a.sk_cnt = sk_cnt;
       a.ep = ep;
+      if (x3) {
+        a.split3 = 1;
+        a.stride_a = (int64_t)M * ldk;  // plane pitches
+        a.stride_b = (int64_t)N * ldk;
+      }
       path = pl.sk_workers > 0 ? GEMM_PATH_TC_SPLITK : GEMM_PATH_TC;
       e = timed_hgemm(a, ctx);
       if (e == cudaSuccess && c_scr) e = launch_copy_rows(4, M, N, Cd, ldc_p, C, ldc, ctx);
@@ -607,7 +632,7 @@ int host_pipelined(int transA, int transB, int64_t M, int64_t N, int64_t K, int 
   // once its slice of B (and of the panel's A rows) has arrived, accumulating
   // in C (beta = 1 after the first); so the first GEMM waits for a quarter of
   // B rather than all of it.  (16-bit C would be rounded between slices.)
-  const int NK = (dtype == GEMM_F32 || dtype == GEMM_F32_TF32) && K >= 1024 ? 4 : 1;
+  const int NK = is_f32(dtype) && K >= 1024 ? 4 : 1;
   const int64_t kl = ((K + NK - 1) / NK + 63) / 64 * 64;  // K per slice
   cudaStream_t sin, sout;
   cudaError_t ce = side_streams(&sin, &sout);
@@ -739,7 +764,7 @@ int run_batched(int transA, int transB, int64_t M64, int64_t N64, int64_t K64, i
   const char* Bb = static_cast<const char*>(B);
   char* Cb = static_cast<char*>(C);
   // (TF32 runs entry by entry: its operands may need packing into K-major rows)
-  const bool tma_ok = dtype != GEMM_F32 && dtype != GEMM_F32_TF32 && ((uintptr_t)A % 16) == 0 &&
+  const bool tma_ok = !is_f32(dtype) && ((uintptr_t)A % 16) == 0 &&
                       ((uintptr_t)B % 16) == 0 &&
                       (lda % 8) == 0 && (ldb % 8) == 0 && (sA % 8) == 0 && (sB % 8) == 0;
   LaunchCtx ctx{stream, status, (uint64_t)g_timeout_ns.load(), 0};
@@ -1068,7 +1093,8 @@ extern "C" int gemm_splitk_noalloc(int transA, int transB, int64_t M, int64_t N,
   tl_last_launches = 0;
   int rc = check_args(transA, transB, M, N, K, dtype, A, lda, B, ldb, C, ldc, &ar, &ac, &br, &bc);
   if (rc != GEMM_OK) return rc;
-  if (dtype == GEMM_F32_TF32) return GEMM_ERR_UNSUPPORTED;  // its packing would need scratch
+  if (dtype == GEMM_F32_TF32 || dtype == GEMM_F32_3XTF32)
+    return GEMM_ERR_UNSUPPORTED;  // their packing would need scratch
   if (M == 0 || N == 0) return GEMM_OK;
   cudaStream_t stream = (cudaStream_t)stream_;
   int dev, sms;

@@ -169,6 +169,10 @@ struct HParams {
   int64_t sk_steps;
   // floor((2^64 - 1) / d) for d = sk_workers, sk_steps, steps (div_magic)
   uint64_t m_skw, m_sks, m_steps;
+  // 3xTF32: a tile's steps run over three segments of steps_k K steps each,
+  // reading (A plane, B plane) = (hi, hi), (hi, lo), (lo, hi); the planes are
+  // the operand maps' third coordinate
+  int split3, steps_k;
   // Shared tiles: each contributing range writes its fp32 partial sums to its
   // slot of sk_ws -- [sk_workers][2: the range's first / last tile][pair ? 2 :
   // 1][4 lane quarters][32 x BN], each quarter's strip laid out as one warp
@@ -511,10 +515,16 @@ __global__ void __launch_bounds__(THREADS, 1)
       Unit U;
       for (int i = 0; ok && unit_at<PAIR, BN>(p, worker, workers, i, rank, U); ++i) {
         const int m0 = U.m0, n0 = U.n0;
-        const int za = U.bz & p.za_mask, zb = U.bz & p.zb_mask;
+        int za = U.bz & p.za_mask, zb = U.bz & p.zb_mask;
         for (int kb = 0; kb < U.nkb; ++kb) {
           if (!mbar_wait(empty_bar(stage), phase ^ 1u, wc)) { ok = false; break; }
-          const int k0 = (U.kb0 + kb) * kblk<T>();
+          int k0 = (U.kb0 + kb) * kblk<T>();
+          if (p.split3) {
+            const int g = U.kb0 + kb, seg = g / p.steps_k;
+            k0 = (g - seg * p.steps_k) * kblk<T>();
+            za = seg == 2 ? 1 : 0;
+            zb = seg == 1 ? 1 : 0;
+          }
           const bool skip = first && p.fault_injection == 1;
           first = false;
           if (!skip && TWO_SM) {
@@ -1272,8 +1282,10 @@ cudaError_t launch_cfg(const HgemmArgs& a, const HParams& p, LaunchCtx& ctx) {
   CUtensorMap mA, mB;
   bool ok;
   const CUtensorMapSwizzle SW = CU_TENSOR_MAP_SWIZZLE_128B;
-  // a pitch-0 operand is one matrix shared by every batch entry (z stays 0)
-  const int64_t nba = p.za_mask ? a.batch : 1, nbb = p.zb_mask ? a.batch : 1;
+  // a pitch-0 operand is one matrix shared by every batch entry (z stays 0);
+  // 3xTF32 operands are two planes each (hi, lo)
+  const int64_t nba = a.split3 ? 2 : (p.za_mask ? a.batch : 1);
+  const int64_t nbb = a.split3 ? 2 : (p.zb_mask ? a.batch : 1);
   // K-major boxes are one 128-byte swizzle row deep in K (64 16-bit or 32
   // fp32 elements); MN-major boxes (16-bit types only) are 64 x 64
   constexpr int KB = kblk<T>(), ES = (int)sizeof(T);
@@ -1377,6 +1389,10 @@ cudaError_t launch_hgemm_t(const HgemmArgs& a, LaunchCtx& ctx) {
   p.zb_mask = (p.batch > 1 && a.stride_b != 0) ? -1 : 0;
   p.ep = a.ep;
   p.epi_halves = pl.epi_halves;
+  p.split3 = a.split3;
+  p.steps_k = a.split3 ? (a.K + kblk<T>() - 1) / kblk<T>() : 0;
+  if (a.split3 && (sizeof(T) != 4 || p.batch > 1 || pl.steps != 3 * p.steps_k))
+    return cudaErrorInvalidValue;
   if (pl.workers <= 0 || pl.steps <= 0 || pl.bn != bn) return cudaErrorInvalidValue;
   if (pl.sk_workers > 0 && (!a.sk_ws || (!pl.sk_publish && !a.sk_cnt))) return cudaErrorInvalidValue;
   switch (bn) {

@@ -84,6 +84,10 @@ struct HgemmArgs {
   int c_tma;            // allow TMA stores (and, beta != 0, TMA loads) of C when C is aligned
   int fault_injection;  // test hook: 1 = producer skips its first stage
   int dtype = 1;        // 1 fp16, 2 bf16, 3 fp32 on TF32 MMAs (gemm_dtype_t)
+  // 3xTF32 (fp32 operands only): A and B are two planes each, hi and lo, a
+  // plane pitch stride_a / stride_b apart; the K loop runs three segments of
+  // K each: hi(A) hi(B), hi(A) lo(B), lo(A) hi(B)
+  int split3 = 0;
   // strided batch (batch > 1): element pitches between consecutive matrices;
   // 16-bit TMA needs them (and ld) multiples of 8
   int batch = 1;
@@ -120,6 +124,14 @@ cudaError_t launch_splitk_reduce(int dtype, int M, int N, int splits, const floa
 // C = act(beta * C + bias) (K == 0); beta == 0 reads no C.
 cudaError_t launch_scale(int dtype, int M, int N, void* C, int64_t ldc, float beta,
                          LaunchCtx& ctx, Epilogue ep = Epilogue());
+// 3xTF32 operand split: hi = the TF32 part of each fp32 value (low 13
+// fraction bits cleared), lo = x - hi (exact), into two planes of row pitch
+// ld_dst (a multiple of 4, 16-byte aligned).  transpose == false: planes
+// [rows][cols] from src [rows][cols], padding columns zeroed; true: planes
+// [cols][rows] from src [rows][cols], padding not written.
+cudaError_t launch_split_tf32(bool transpose, int rows, int cols, const float* src,
+                              int64_t ld_src, float* hi, float* lo, int64_t ld_dst,
+                              LaunchCtx& ctx);
 // dst[c][r] = src[r][c] (fp32 rows x cols).
 cudaError_t launch_transpose_f32(int rows, int cols, const float* src, int64_t ld_src,
                                  float* dst, int64_t ld_dst, LaunchCtx& ctx);

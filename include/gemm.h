@@ -76,7 +76,7 @@ typedef enum {
                              rounded to bfloat16 round-to-nearest-even (the
                              bfloat16 row of the LoRA page's section 1 type
                              table, native on these tensor cores) */
-    GEMM_F32_TF32 = 3     /* OPT-IN reduced precision: A, B, C fp32, but the
+    GEMM_F32_TF32 = 3,    /* OPT-IN reduced precision: A, B, C fp32, but the
                              products use only the TF32 part of each operand
                              (sign, 8 exponent and the top 10 fraction bits)
                              on the tensor cores; fp32 accumulation.  Error up
@@ -85,6 +85,18 @@ typedef enum {
                              precision switch of "Optimizing GEMM on Apple's
                              M5 from scratch, Part 2"; never chosen for you.
                              Not accepted by gemm_splitk_noalloc. */
+    GEMM_F32_3XTF32 = 4   /* OPT-IN: A, B, C fp32 on the tensor cores at about
+                             fp32 accuracy.  Each operand is split into its
+                             TF32 part hi (low 13 fraction bits cleared) and
+                             the rest lo = x - hi (exact), and the products are
+                             formed as hi*hi + hi*lo + lo*hi in one fp32
+                             accumulation: the dropped lo*lo term and the TF32
+                             reading of lo leave an error of about 2^-19 *
+                             sum|a*b|, within GEMM_F32's tolerance.  Inputs
+                             must be finite (an infinity in one operand meets a
+                             zero lo of the other).  Takes scratch for the
+                             split planes (2 x 4 bytes x (M + N) x K); not
+                             accepted by gemm_splitk_noalloc. */
 } gemm_dtype_t;
 
 typedef enum {
@@ -177,7 +189,7 @@ int gemm_host(int transA, int transB, int64_t M, int64_t N, int64_t K, int dtype
  *     copy of an unaligned fp16 C (the kernel stores such a C row by row);
  *   - fp16/bf16 operands must have 16-byte aligned bases and row pitches (lda,
  *     ldb multiples of 8), else GEMM_ERR_UNSUPPORTED (padding them would need
- *     scratch); GEMM_F32_TF32 is not accepted.
+ *     scratch); GEMM_F32_TF32 and GEMM_F32_3XTF32 are not accepted.
  * The first call on a device looks up the array's device address (a CUDA
  * runtime query, done once per device with that device current); make that
  * first call before any stream capture.  All calls share the array: calls

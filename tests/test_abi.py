@@ -121,8 +121,9 @@ def test_tf32_not_accepted_without_scratch(b, lib_path):
     i64, ci, cf, vp = ctypes.c_int64, ctypes.c_int, ctypes.c_float, ctypes.c_void_p
     f.argtypes = [ci, ci, i64, i64, i64, ci, cf, cf, vp, i64, vp, i64, vp, i64, vp]
     f.restype = ci
-    assert f(0, 0, 4, 4, 4, 3, 1.0, 0.0, PA, 4, PB, 4, PC, 4, None) == 2
-    assert b.gemm_raw(0, 0, 4, 4, 4, 4, 1.0, 0.0, PA, 4, PB, 4, PC, 4) == 1  # dtype 4 unknown
+    assert f(0, 0, 4, 4, 4, 3, 1.0, 0.0, PA, 4, PB, 4, PC, 4, None) == 2  # TF32
+    assert f(0, 0, 4, 4, 4, 4, 1.0, 0.0, PA, 4, PB, 4, PC, 4, None) == 2  # 3xTF32
+    assert b.gemm_raw(0, 0, 4, 4, 4, 5, 1.0, 0.0, PA, 4, PB, 4, PC, 4) == 1  # dtype 5 unknown
 
 
 @pytest.mark.parametrize("entry", ["gemm", "gemm_strided_batched"])
