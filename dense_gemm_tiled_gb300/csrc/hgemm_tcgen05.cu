@@ -130,9 +130,11 @@ HPlan hgemm_plan(int M, int N, int K, int bn, int transA, int transB, int kstep,
     const int64_t per = (pl.sk_steps + pl.sk_workers - 1) / pl.sk_workers;
     if (per < unit_steps) unit_steps = per;
   }
-  // (a 32-wide tile is one 32-column chunk: nothing to share)
-  pl.epi_halves =
-      (EPI_HALVES > 1 && unit_steps <= GB300_HG_EPI2_STEPS && bn >= 64) ? EPI_HALVES : 1;
+  // (a 32-wide tile is one 32-column chunk: nothing to share; with every
+  // tile shared, every worker's epilogue is the publishing of its partial
+  // sums at the end of the launch: both shares)
+  pl.epi_halves = (EPI_HALVES > 1 && bn >= 64 &&
+                   (unit_steps <= GB300_HG_EPI2_STEPS || pl.sk_publish)) ? EPI_HALVES : 1;
   return pl;
 }
 

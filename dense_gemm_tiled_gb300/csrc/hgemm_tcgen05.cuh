@@ -1112,46 +1112,95 @@ __global__ void __launch_bounds__(THREADS, 1)
 }
 
 // Reduction of shared tiles published by every contributor (sk_publish):
-// one warp per (shared tile, block of the pair, 32-row quarter, 32-column
-// chunk) sums the contributors' chunks in K order -- every load of the warp
-// covers 512 contiguous bytes -- and stores act(alpha * sum + beta * C +
-// bias) for its rows.  Blocks of 8 warps; launched after the GEMM kernel in
+// one block of 256 threads per (shared tile, block of the pair, 32-row
+// quarter, 32-column chunk).  Thread (v, lane) loads float4 v of row lane
+// from every contributor (all loads in flight together; every load of a warp
+// covers 512 contiguous bytes) and adds them in K order; the 32 x 32 sums go
+// through shared memory so that the output is written 4 columns a thread,
+// 8 threads a row -- 64-byte (16-bit C) or 128-byte (fp32 C) row segments --
+// as act(alpha * sum + beta * C + bias).  Launched after the GEMM kernel in
 // stream order.
 template <typename T, bool PAIR, int TBN>
 __global__ void __launch_bounds__(256) hgemm_sk_reduce(const HParams p) {
+  using E = Elem<T>;
   pdl_wait();
   pdl_trigger();
   constexpr int P = PAIR ? 2 : 1;
   constexpr int CH = TBN / 32;
   constexpr int STRIP = 32 * TBN;
-  const int lane = threadIdx.x & 31;
-  const int64_t wid = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
-  const int64_t shared = (int64_t)p.tiles - p.dp_tiles;
-  if (wid >= shared * P * 4 * CH) return;
-  const int c = (int)(wid % CH);
-  const int q = (int)((wid / CH) % 4);
-  const int rank = (int)((wid / (CH * 4)) % P);
-  const int64_t tr = wid / (CH * 4 * P);
+  constexpr int MAXC = 8;  // contributors a tile can have (the planner allows at most 5)
+  __shared__ float sum[32][33];
+  const int lane = threadIdx.x & 31, v = threadIdx.x >> 5;
+  const int64_t unit = blockIdx.x;
+  const int c = (int)(unit % CH);
+  const int q = (int)((unit / CH) % 4);
+  const int rank = (int)((unit / (CH * 4)) % P);
+  const int64_t tr = unit / (CH * 4 * P);
+  if (tr >= (int64_t)p.tiles - p.dp_tiles) return;
   int m0, n0, bz;
   tile_origin<PAIR, TBN>(p, p.dp_tiles + (int)tr, rank, m0, n0, bz);
   const int64_t s0 = tr * p.steps;
   const int w_first = sk_owner(p, s0), w_last = sk_owner(p, s0 + p.steps - 1);
   if (w_first == w_last) return;  // one range covered the tile: stored as a whole one
-  float v[32];
+  float4 f[MAXC];
 #pragma unroll
-  for (int j = 0; j < 32; ++j) v[j] = 0.f;
-  for (int w2 = w_first; w2 <= w_last; ++w2) {
-    const float4* src =
-        reinterpret_cast<const float4*>(p.sk_ws + ((((int64_t)w2 * 2 + sk_slot(p, w2, s0)) * P +
-                                                    rank) * 4 + q) * STRIP) + c * 256 + lane;
+  for (int i = 0; i < MAXC; ++i) {
+    const int w2 = w_first + i;
+    f[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (w2 <= w_last)
+      f[i] = __ldcg(reinterpret_cast<const float4*>(
+                        p.sk_ws + ((((int64_t)w2 * 2 + sk_slot(p, w2, s0)) * P + rank) * 4 + q) *
+                                      STRIP) +
+                    c * 256 + v * 32 + lane);
+  }
+  float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
 #pragma unroll
-    for (int w = 0; w < 8; ++w) {
-      const float4 f = __ldcg(src + w * 32);
-      v[4 * w] += f.x; v[4 * w + 1] += f.y; v[4 * w + 2] += f.z; v[4 * w + 3] += f.w;
+  for (int i = 0; i < MAXC; ++i) {
+    if (w_first + i > w_last) break;
+    a0 += f[i].x; a1 += f[i].y; a2 += f[i].z; a3 += f[i].w;
+  }
+  sum[lane][4 * v] = a0; sum[lane][4 * v + 1] = a1;
+  sum[lane][4 * v + 2] = a2; sum[lane][4 * v + 3] = a3;
+  __syncthreads();
+  // thread t: row t / 8 of the chunk, columns 4 (t % 8) .. +3
+  const int r = threadIdx.x >> 3, cc = (threadIdx.x & 7) * 4;
+  const int gm = m0 + q * 32 + r, gn0 = n0 + c * 32 + cc;
+  if (gm >= p.M || gn0 >= p.N) return;
+  T* dst = static_cast<T*>(p.C) + (int64_t)bz * p.stride_c + (int64_t)gm * p.ldc + gn0;
+  const bool epi = p.ep.bias != nullptr || p.ep.act != 0;
+  float x[4];
+#pragma unroll
+  for (int j = 0; j < 4; ++j) x[j] = p.alpha * sum[r][cc + j];
+  // 16 (fp32) or 8 (16-bit) aligned bytes when C rows are 16-byte aligned
+  const bool vec = p.c_vec_ok && gn0 + 3 < p.N;
+  if (p.beta != 0.f) {
+    if (vec && sizeof(T) == 4) {
+      const float4 cv = *reinterpret_cast<const float4*>(dst);
+      x[0] = __fmaf_rn(p.beta, cv.x, x[0]); x[1] = __fmaf_rn(p.beta, cv.y, x[1]);
+      x[2] = __fmaf_rn(p.beta, cv.z, x[2]); x[3] = __fmaf_rn(p.beta, cv.w, x[3]);
+    } else {
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+        if (gn0 + j < p.N) x[j] = __fmaf_rn(p.beta, E::to(dst[j]), x[j]);
     }
   }
-  const int gm = m0 + q * 32 + lane, gn0 = n0 + c * 32;
-  if (gm < p.M && gn0 < p.N) store_c32<T>(p, bz, gm, gn0, v);
+  if (epi) {
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+      if (gn0 + j < p.N) x[j] = apply_epilogue<T>(x[j], p.ep, gn0 + j);
+  }
+  if (vec) {
+    if constexpr (sizeof(T) == 4) {
+      *reinterpret_cast<float4*>(dst) = make_float4(x[0], x[1], x[2], x[3]);
+    } else {
+      typename E::T2 h[2] = {E::pack(x[0], x[1]), E::pack(x[2], x[3])};
+      *reinterpret_cast<uint2*>(dst) = *reinterpret_cast<const uint2*>(h);
+    }
+  } else {
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+      if (gn0 + j < p.N) dst[j] = E::from(x[j]);
+  }
 }
 
 // ---------------------------------------------------------------- host side
@@ -1316,9 +1365,9 @@ cudaError_t launch_cfg(const HgemmArgs& a, const HParams& p, LaunchCtx& ctx) {
   if (e != cudaSuccess) return e;
   ctx.launches++;
   if (pp.sk_workers > 0 && pp.sk_publish) {
-    const int64_t warps = ((int64_t)pp.tiles - pp.dp_tiles) * (PAIR ? 2 : 1) * 4 * (BN / 32);
-    e = launch_kernel(hgemm_sk_reduce<T, PAIR, BN>, dim3((unsigned)((warps + 7) / 8)), dim3(256),
-                      0, ctx.stream, 1, pp);
+    const int64_t units = ((int64_t)pp.tiles - pp.dp_tiles) * (PAIR ? 2 : 1) * 4 * (BN / 32);
+    e = launch_kernel(hgemm_sk_reduce<T, PAIR, BN>, dim3((unsigned)units), dim3(256), 0,
+                      ctx.stream, 1, pp);
     if (e == cudaSuccess) ctx.launches++;
   }
   return e;
