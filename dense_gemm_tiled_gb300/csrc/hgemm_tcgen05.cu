@@ -46,14 +46,29 @@ bool hgemm_use_pair(int bn, int M, int allowed) {
 #define GB300_HG_SK_COST_NARROW 16
 #endif
 // ... and when every contributor publishes and a reduction kernel finishes
+// (wide tiles; 64-wide or narrower: 512 x 32 x 2048 fp16, 16 ranges of 8
+// steps against 4 tiles of 32: 17.0 -> 15.0 us)
 #ifndef GB300_HG_SK_COST_PUBLISH
 #define GB300_HG_SK_COST_PUBLISH 24
+#endif
+#ifndef GB300_HG_SK_COST_PUBLISH_NARROW
+#define GB300_HG_SK_COST_PUBLISH_NARROW 12
+#endif
+// Most ranges that share one tile of 64 columns or fewer when a reduction
+// kernel finishes it (its threads load every contributor's partial sums at
+// once): 512 x 32 x 5632 fp16, 16 ranges of 22 steps against 28 of 12.6:
+// 14.9 -> 12.4 us.  Wider tiles keep GB300_HG_SK_MAX_CONTRIB: 512 x 2048 x
+// 5632 on 2-SM pairs, 64 ranges of 22 steps (four to a tile, none straddling
+// two) against 76 of 18.5: 24.7 against 30.9 us.
+#ifndef GB300_HG_SK_MAX_CONTRIB_PUBLISH
+#define GB300_HG_SK_MAX_CONTRIB_PUBLISH 16
 #endif
 
 // K steps a stream-K plan adds for finishing shared tiles (0 without).
 int sk_cost_steps(const HPlan& pl) {
   if (pl.sk_workers == 0) return 0;
-  if (pl.sk_publish) return GB300_HG_SK_COST_PUBLISH;
+  if (pl.sk_publish)
+    return pl.bn <= 64 ? GB300_HG_SK_COST_PUBLISH_NARROW : GB300_HG_SK_COST_PUBLISH;
   return pl.bn <= 64 ? GB300_HG_SK_COST_NARROW : GB300_HG_SK_COST_WIDE;
 }
 
@@ -94,10 +109,12 @@ HPlan hgemm_plan(int M, int N, int K, int bn, int transA, int transB, int kstep,
     // SM taking part) beats the last contributor's finish (one block or block
     // pair a tile).
     const int64_t total = shared * steps;
+    const bool publish = sk_mode == 3 || (sk_mode == 1 && tiles == shared);
     int64_t skw = total / GB300_HG_SK_MIN_STEPS;
     if (skw > wmax) skw = wmax;
-    // at most GB300_HG_SK_MAX_CONTRIB ranges meet in a tile
-    const int64_t cap = shared * (GB300_HG_SK_MAX_CONTRIB - 1);
+    // at most GB300_HG_SK_MAX_CONTRIB(_PUBLISH) ranges meet in a tile
+    const int64_t cap = shared * ((publish && bn <= 64 ? GB300_HG_SK_MAX_CONTRIB_PUBLISH
+                                                       : GB300_HG_SK_MAX_CONTRIB) - 1);
     if (skw > cap) skw = cap;
     // (positions up to skw * total must fit 64 bits; every range non-empty)
     if (shared > 0 && skw >= 2 && total < ((int64_t)1 << 40)) {
@@ -108,7 +125,7 @@ HPlan hgemm_plan(int M, int N, int K, int bn, int transA, int transB, int kstep,
       sk.workers = sk.dp_tiles > 0 ? wmax : (int)skw;
       const int P = pair ? 2 : 1;
       sk.ws_bytes = (size_t)skw * 2 * P * BM * bn * sizeof(float);
-      sk.sk_publish = sk_mode == 3 || (sk_mode == 1 && sk.dp_tiles == 0);
+      sk.sk_publish = publish;
       sk.cnt_bytes =
           sk.sk_publish ? 0 : (size_t)shared * P * 4 * EPI_HALVES * sizeof(unsigned int);
       // shared only where the busiest worker saves more than finishing the

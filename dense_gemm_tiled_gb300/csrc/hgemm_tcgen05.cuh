@@ -1128,7 +1128,9 @@ __global__ void __launch_bounds__(256) hgemm_sk_reduce(const HParams p) {
   constexpr int P = PAIR ? 2 : 1;
   constexpr int CH = TBN / 32;
   constexpr int STRIP = 32 * TBN;
-  constexpr int MAXC = 8;  // contributors a tile can have (the planner allows at most 5)
+  // contributors a tile can have: the planner allows at most 5 to tiles wider
+  // than 64 columns, 16 to narrower ones
+  constexpr int MAXC = TBN > 64 ? 5 : 16;
   __shared__ float sum[32][33];
   const int lane = threadIdx.x & 31, v = threadIdx.x >> 5;
   const int64_t unit = blockIdx.x;
@@ -1142,6 +1144,8 @@ __global__ void __launch_bounds__(256) hgemm_sk_reduce(const HParams p) {
   const int64_t s0 = tr * p.steps;
   const int w_first = sk_owner(p, s0), w_last = sk_owner(p, s0 + p.steps - 1);
   if (w_first == w_last) return;  // one range covered the tile: stored as a whole one
+  // (only the first contributor can have started before the tile: slot 1)
+  const int slot0 = sk_slot(p, w_first, s0);
   float4 f[MAXC];
 #pragma unroll
   for (int i = 0; i < MAXC; ++i) {
@@ -1149,7 +1153,7 @@ __global__ void __launch_bounds__(256) hgemm_sk_reduce(const HParams p) {
     f[i] = make_float4(0.f, 0.f, 0.f, 0.f);
     if (w2 <= w_last)
       f[i] = __ldcg(reinterpret_cast<const float4*>(
-                        p.sk_ws + ((((int64_t)w2 * 2 + sk_slot(p, w2, s0)) * P + rank) * 4 + q) *
+                        p.sk_ws + ((((int64_t)w2 * 2 + (i == 0 ? slot0 : 0)) * P + rank) * 4 + q) *
                                       STRIP) +
                     c * 256 + v * 32 + lane);
   }
