@@ -668,33 +668,37 @@ def attention_step(dev, stream, reps: int = 20, H: int = 16, n: int = 2048, d: i
 
 def run_case(args, local):
     """One GEMM, `warmup` untimed launches then `steps` timed ones (CUDA events
-    per launch on the launching stream)."""
+    per launch on the launching stream).  The case is <dtype>_<variant>_<size>
+    with dtype f32, f16, bf16, tf32 or tf32x3 (the last two: the opt-in paths
+    on fp32 data) and size n (n^3) or MxNxK."""
     import torch
     from dense_gemm_tiled_gb300 import binding, inputs
     dt, var, size = args.case.split("_")
-    n = int(size)
-    tf32 = dt == "tf32"  # the opt-in TF32 path on fp32 data
+    M, N, K = (int(x) for x in size.split("x")) if "x" in size else (int(size),) * 3
+    tf32, tf32x3 = dt == "tf32", dt == "tf32x3"
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
     tA, tB = inputs.VARIANTS[var]
-    p = inputs.make_problem(n, n, n, tA, tB, dtype="f32" if tf32 else dt, seed=80)
+    p = inputs.make_problem(M, N, K, tA, tB, dtype="f32" if (tf32 or tf32x3) else dt, seed=80)
     A, B = p.A.to(dev), p.B.to(dev)
-    C = torch.empty((n, n), dtype=A.dtype, device=dev)
+    C = torch.empty((M, N), dtype=A.dtype, device=dev)
     s = torch.cuda.Stream(dev)
+    call = lambda: binding.gemm(A, B, C, tA, tB, stream=s, tf32=tf32, tf32x3=tf32x3)
     for _ in range(args.warmup):
-        binding.gemm(A, B, C, tA, tB, stream=s, tf32=tf32)
+        call()
     ts = []
     for _ in range(args.steps):
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record(s)
-        binding.gemm(A, B, C, tA, tB, stream=s, tf32=tf32)
+        call()
         e1.record(s)
         e1.synchronize()
         ts.append(e0.elapsed_time(e1))
     assert binding.check_device_status(s) == binding.OK
     med = statistics.median(ts)
-    print(json.dumps({"case": args.case, "path": binding.last_path(), "ms_median": med,
-                      "tflops": 2.0 * n ** 3 / (med * 1e-3) / 1e12, "steps": args.steps}),
+    print(json.dumps({"case": args.case, "path": binding.last_path(),
+                      "launches": binding.last_launches(), "ms_median": med,
+                      "tflops": 2.0 * M * N * K / (med * 1e-3) / 1e12, "steps": args.steps}),
           flush=True)
 
 
@@ -710,8 +714,9 @@ def main():
     ap.add_argument("--no-attention", action="store_true")
     ap.add_argument("--no-control", action="store_true")
     ap.add_argument("--case", default=None,
-                    help="run only one GEMM (e.g. f32_nn_4096, f16_tn_4096, f16_nn_8192, tf32_nt_4096): "
-                         "warm-up + steps, one short JSON line; used for profiling")
+                    help="run only one GEMM (e.g. f32_nn_4096, f16_tn_4096, f16_nn_512x32x5632, "
+                         "tf32_nt_4096, tf32x3_nn_4096): warm-up + steps, one short JSON line; "
+                         "used for profiling")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

@@ -169,9 +169,10 @@ struct HParams {
   int64_t sk_steps;
   // floor((2^64 - 1) / d) for d = sk_workers, sk_steps, steps (div_magic)
   uint64_t m_skw, m_sks, m_steps;
-  // 3xTF32: a tile's steps run over three segments of steps_k K steps each,
-  // reading (A plane, B plane) = (hi, hi), (hi, lo), (lo, hi); the planes are
-  // the operand maps' third coordinate
+  // 3xTF32: a tile's steps are its steps_k K steps three times over, step g
+  // reading K step g / 3 of the (A plane, B plane) pair (hi, hi), (hi, lo),
+  // (lo, hi) for g % 3 = 0, 1, 2; the planes are the operand maps' third
+  // coordinate
   int split3, steps_k;
   // Shared tiles: each contributing range writes its fp32 partial sums to its
   // slot of sk_ws -- [sk_workers][2: the range's first / last tile][pair ? 2 :
@@ -520,8 +521,12 @@ __global__ void __launch_bounds__(THREADS, 1)
           if (!mbar_wait(empty_bar(stage), phase ^ 1u, wc)) { ok = false; break; }
           int k0 = (U.kb0 + kb) * kblk<T>();
           if (p.split3) {
-            const int g = U.kb0 + kb, seg = g / p.steps_k;
-            k0 = (g - seg * p.steps_k) * kblk<T>();
+            // step g is segment g % 3 of K step g / 3: the three products of a
+            // K step follow each other, so each plane tile's second use finds
+            // it in L2 (segment after segment re-read the planes from DRAM:
+            // 2.3 GB a launch at 4096^3)
+            const int g = U.kb0 + kb, seg = g % 3;
+            k0 = (g / 3) * kblk<T>();
             za = seg == 2 ? 1 : 0;
             zb = seg == 1 ? 1 : 0;
           }

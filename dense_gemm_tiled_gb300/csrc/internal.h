@@ -85,8 +85,8 @@ struct HgemmArgs {
   int fault_injection;  // test hook: 1 = producer skips its first stage
   int dtype = 1;        // 1 fp16, 2 bf16, 3 fp32 on TF32 MMAs (gemm_dtype_t)
   // 3xTF32 (fp32 operands only): A and B are two planes each, hi and lo, a
-  // plane pitch stride_a / stride_b apart; the K loop runs three segments of
-  // K each: hi(A) hi(B), hi(A) lo(B), lo(A) hi(B)
+  // plane pitch stride_a / stride_b apart; every K step is run three times:
+  // hi(A) hi(B), hi(A) lo(B), lo(A) hi(B)
   int split3 = 0;
   // strided batch (batch > 1): element pitches between consecutive matrices;
   // 16-bit TMA needs them (and ld) multiples of 8
