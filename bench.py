@@ -816,8 +816,9 @@ def main():
     med_step, min_step, p90_step = spread(step_ms)
     roofline = {"bound": "alu", "achieved": round(achieved, 3), "peak": round(ffma_peak, 3),
                 "unit": "TFLOP/s", "frac": round(achieved / ffma_peak, 4), "traffic": None,
-                "kernel": "sgemm_ffma_kernel (fp32, 128x128 tiles, K step 64, paired FMA; "
-                          "persistent stream-K launch: 1024 tiles over 152 SMs)",
+                "kernel": "sgemm_ws_kernel (fp32, 128x128 tiles, K step 64, paired FMA; "
+                          "operand tiles staged by TMA from a producer warp into a 3-stage "
+                          "mbarrier ring; persistent stream-K launch: 1024 tiles over 152 SMs)",
                 "timing": "CUDA events recorded by the library around the kernel launch "
                           "(gemm_set_kernel_events) on every 4th timed step, average",
                 "peak_basis": f"{sms} SMs x {FP32_LANES_PER_SM} FP32 lanes x 2 x {sm_max:.0f} MHz",

@@ -187,6 +187,28 @@ int sg_narrow_enabled() {
   return v;
 }
 
+// fp32 tile for N > 32 (env GEMM_GB300_SG_TILE): 0 the 128 x 128 tile, 2 the
+// 128 x 256 one, 3 the 128 x 64 one; unset or any other value: the
+// dispatcher's choice.
+int sg_tile_forced() {
+  static const int v = [] {
+    const char* e = getenv("GEMM_GB300_SG_TILE");
+    const int t = e ? atoi(e) : -1;
+    return (t == SG_TILE_WIDE || t == SG_TILE_BIG || t == SG_TILE_HALF) ? t : -1;
+  }();
+  return v;
+}
+
+// fp32 warp-specialised TMA staging for k-major aligned operands (env
+// GEMM_GB300_SG_WS=0 turns it off).
+int sg_ws_enabled() {
+  static const int v = [] {
+    const char* e = getenv("GEMM_GB300_SG_WS");
+    return (e && e[0] == '0') ? 0 : 1;
+  }();
+  return v;
+}
+
 // fp16 block pairs (env GEMM_GB300_HG_PAIR): 0 single blocks, 2 (default)
 // pairs running 2-SM (cta_group::2) MMAs; any other value means 2.
 int pair_enabled() {
@@ -289,15 +311,18 @@ void plan_splits(int64_t tiles, int64_t K, int kstep, int capacity, int min_step
 // per SM), split over K until one round of resident blocks is full; other
 // shapes the 128 x 128 tile, split when the tiles fill under half of two
 // rounds of the SMs.
-void plan_f32(int M, int N, int K, int sms, bool* narrow, int64_t* tiles, int* splits,
+void plan_f32(int M, int N, int K, int sms, int* tile, int64_t* tiles, int* splits,
               int* k_slice) {
-  *narrow = N <= SGN_BN && sg_narrow_enabled();
-  const int bm = *narrow ? SGN_BM : SG_BM, bn = *narrow ? SGN_BN : SG_BN;
-  *tiles = (int64_t)((M + bm - 1) / bm) * ((N + bn - 1) / bn);
-  if (*narrow)
+  if (N <= SGN_BN && sg_narrow_enabled()) *tile = SG_TILE_NARROW;
+  else if (sg_tile_forced() >= 0) *tile = sg_tile_forced();
+  else *tile = SG_TILE_WIDE;
+  const SgTileShape ts = sg_tile_shape(*tile);
+  *tiles = (int64_t)((M + ts.bm - 1) / ts.bm) * ((N + ts.bn - 1) / ts.bn);
+  if (*tile == SG_TILE_NARROW)
     plan_splits(*tiles, K, SGN_BK, sms * SGN_BLOCKS_PER_SM, 8, 16, splits, k_slice);
   else
-    plan_splits(*tiles, K, SG_BK, 2 * sms, GB300_SG_SLICE_STEPS, 16, splits, k_slice);
+    plan_splits(*tiles, K, ts.bk, 2 * sms * ts.blocks_per_sm, GB300_SG_SLICE_STEPS, 16, splits,
+                k_slice);
 }
 
 // Scratch comes from a stream-ordered memory pool owned by the library, one
@@ -441,13 +466,16 @@ int run_gemm(int transA, int transB, int64_t M64, int64_t N64, int64_t K64, int 
       if (e == cudaSuccess && c_scr) e = launch_copy_rows(4, M, N, Cd, ldc_p, C, ldc, ctx);
     }
   } else if (dtype == GEMM_F32) {
-    bool narrow;
-    int splits, k_slice;
+    int tile, splits, k_slice;
     int64_t tiles;
-    plan_f32(M, N, K, sms, &narrow, &tiles, &splits, &k_slice);
+    plan_f32(M, N, K, sms, &tile, &tiles, &splits, &k_slice);
+    const bool narrow = tile == SG_TILE_NARROW;
+    const SgTileShape ts = sg_tile_shape(tile);
     SgemmArgs a{transA, transB, M, N, K, (const float*)A, lda, (const float*)B, ldb, (float*)C,
                 ldc, alpha, beta, splits, k_slice, nullptr};
-    a.narrow = narrow ? 1 : 0;
+    a.tile = tile;
+    a.ws = sg_ws_enabled();
+    a.fault_injection = g_fault_injection.load();
     if (splits == 1) a.ep = ep;  // split-K: the reduction applies it
     // Packing: the kernel reads A stored [K,M] and B stored [K,N] fastest
     // (measured at 4096^3: tn 56.4 TF/s, nn 53.7, nt 46.9), so on large
@@ -474,10 +502,10 @@ int run_gemm(int transA, int transB, int64_t M64, int64_t N64, int64_t K64, int 
     // rounds of the SMs leaves the last round part-empty (4096^3: 1024 tiles,
     // 6.7 rounds of 152).  The persistent launch gives whole tiles to all but
     // the last one to two rounds and shares those rounds' K steps evenly.
-    const int64_t G = (int64_t)sms * SG_BLOCKS_PER_SM;  // resident blocks
+    const int64_t G = (int64_t)sms * ts.blocks_per_sm;  // resident blocks
     const bool sk = splits == 1 && !narrow && sg_sk_enabled() && tiles >= G && tiles % G != 0;
     const int64_t sk_tiles = sk ? (tiles >= 2 * G ? tiles % G + G : tiles) : 0;
-    const size_t bytes_S = sk ? (size_t)G * 2 * SG_BM * SG_BN * sizeof(float) : 0;
+    const size_t bytes_S = sk ? (size_t)G * 2 * ts.bm * ts.bn * sizeof(float) : 0;
     const size_t bytes_N = sk ? ((size_t)sk_tiles * sizeof(unsigned int) + 255) / 256 * 256 : 0;
     Scratch ws;
     if (bytes_A + bytes_B + bytes_P + bytes_S + bytes_N > 0) {
@@ -1114,16 +1142,15 @@ extern "C" int gemm_splitk_noalloc(int transA, int transB, int64_t M, int64_t N,
   } else if (dtype == GEMM_F32) {
     // gemm()'s tile and K split; without gemm()'s operand packing and
     // stream-K launch on large problems, which take scratch
-    bool narrow;
-    int splits, k_slice;
+    int tile, splits, k_slice;
     int64_t tiles;
-    plan_f32(Mi, Ni, Ki, sms, &narrow, &tiles, &splits, &k_slice);
+    plan_f32(Mi, Ni, Ki, sms, &tile, &tiles, &splits, &k_slice);
     if (splits > 1 && (uint64_t)splits * (uint64_t)M * (uint64_t)N * sizeof(float) >
                           GEMM_NOALLOC_SCRATCH_BYTES)
       return GEMM_ERR_UNSUPPORTED;  // partial sums would not fit the fixed array
     SgemmArgs a{transA, transB, Mi, Ni, Ki, (const float*)A, lda, (const float*)B, ldb,
                 (float*)C, ldc, alpha, beta, splits, k_slice, splits > 1 ? scratch : nullptr};
-    a.narrow = narrow ? 1 : 0;
+    a.tile = tile;
     path = splits > 1 ? GEMM_PATH_FFMA_SPLITK : GEMM_PATH_FFMA;
     e = timed_sgemm(a, ctx);
     if (e == cudaSuccess && splits > 1)

@@ -36,15 +36,19 @@ struct SgemmArgs {
   int batch = 1;
   int64_t stride_a = 0, stride_b = 0, stride_c = 0;
   // persistent stream-K launch (sk_blocks > 0, no split, no batch, at least
-  // sk_blocks tiles): sk_blocks blocks, partial tiles in sk_ws
-  // (sk_blocks * 2 * SG_BM * SG_BN floats), arrival counters in sk_cnt (one per
-  // tile, zero at launch)
+  // sk_blocks tiles; not the narrow tile): sk_blocks blocks, partial tiles in
+  // sk_ws (sk_blocks * 2 * bm * bn floats of the tile's shape), arrival
+  // counters in sk_cnt (one per tile, zero at launch)
   int sk_blocks = 0;
   float* sk_ws = nullptr;
   unsigned int* sk_cnt = nullptr;
-  // block tile: 0 the general SG_BM x SG_BN tile, 1 the narrow SGN_BM x SGN_BN
-  // tile for N <= SGN_BN (no stream-K launch)
-  int narrow = 0;
+  // block tile (SG_TILE_*): the general 128 x 128 tile, the narrow one for
+  // N <= SGN_BN, the big 128 x 256 or the half 128 x 64
+  int tile = 0;
+  // operands k-major (A [K,M], B [K,N]) with 16-byte aligned rows, one GEMM,
+  // no split: stage them with the warp-specialised TMA kernel (ws = 1)
+  int ws = 0;
+  int fault_injection = 0;  // test hook of that kernel (see sgemm_ffma.cuh)
   Epilogue ep;  // fused bias / activation (not with splits > 1: the reduction applies it)
 };
 
@@ -112,7 +116,9 @@ struct LaunchCtx {
 int pdl_enabled();
 
 cudaError_t launch_sgemm(const SgemmArgs& a, LaunchCtx& ctx);
-cudaError_t launch_sgemm_narrow(const SgemmArgs& a, LaunchCtx& ctx);  // a.narrow tiles
+cudaError_t launch_sgemm_narrow(const SgemmArgs& a, LaunchCtx& ctx);  // SG_TILE_NARROW
+cudaError_t launch_sgemm_big(const SgemmArgs& a, LaunchCtx& ctx);     // SG_TILE_BIG
+cudaError_t launch_sgemm_half(const SgemmArgs& a, LaunchCtx& ctx);    // SG_TILE_HALF
 cudaError_t launch_hgemm(const HgemmArgs& a, LaunchCtx& ctx);
 cudaError_t launch_hgemm_bf16(const HgemmArgs& a, LaunchCtx& ctx);
 // fp32 operands and output on kind::tf32 MMAs (HgemmArgs.dtype 3; K-major A and B)
@@ -179,6 +185,27 @@ constexpr int SG_BLOCKS_PER_SM = GB300_SG_MIN_BLOCKS;
 #endif
 constexpr int SGN_BM = 64 * GB300_SGN_WARPS_M, SGN_BN = 32, SGN_BK = GB300_SGN_BK;
 constexpr int SGN_BLOCKS_PER_SM = GB300_SGN_MIN_BLOCKS;
+// fp32 big tile: 128 x 256 at K step 32 in a 4-stage ring, one block of 8
+// warps per SM, each lane 8 rows x 16 columns -- per K a lane builds its 8
+// splatted A pairs once for 64 paired FMAs (32 with 8 x 8), and the block
+// reads 3/8 rather than 1/2 a float from shared memory per FMA pair
+constexpr int SGB_BM = 128, SGB_BN = 256, SGB_BK = 32, SGB_STAGES = 4;
+// fp32 half tile: 128 x 64 at K step 32 in a 4-stage ring, 4 warps, two
+// blocks per SM: twice the tiles of 128 x 128 for grids that leave SMs idle
+constexpr int SGH_BM = 128, SGH_BN = 64, SGH_BK = 32, SGH_STAGES = 4, SGH_BLOCKS_PER_SM = 2;
+// fp32 tile ids (SgemmArgs::tile) and their shapes
+enum { SG_TILE_WIDE = 0, SG_TILE_NARROW = 1, SG_TILE_BIG = 2, SG_TILE_HALF = 3 };
+struct SgTileShape {
+  int bm, bn, bk, blocks_per_sm;
+};
+inline SgTileShape sg_tile_shape(int tile) {
+  switch (tile) {
+    case SG_TILE_NARROW: return {SGN_BM, SGN_BN, SGN_BK, SGN_BLOCKS_PER_SM};
+    case SG_TILE_BIG: return {SGB_BM, SGB_BN, SGB_BK, 1};
+    case SG_TILE_HALF: return {SGH_BM, SGH_BN, SGH_BK, SGH_BLOCKS_PER_SM};
+    default: return {SG_BM, SG_BN, SG_BK, SG_BLOCKS_PER_SM};
+  }
+}
 constexpr int HG_BM = 128, HG_BK = 64;
 // Tile width of the tcgen05 kernel (32 to 256 columns) for this problem and
 // schedule (arguments as hgemm_plan).

@@ -23,11 +23,20 @@
 //    coalesced; here every global load is a 16-byte cp.async and a warp's loads
 //    cover whole 64- or 512-byte row segments.
 //
-// Tile: (64 * WARPS_M) x (32 * WARPS_N) outputs per block (warps of 64 x 32,
-// each lane 8 x 8 outputs split into 4-wide groups): 128 x 128 at K step 64,
-// one block per SM, in general; 256 x 32 at K step 32, two blocks per SM, for
-// N <= 32.  This header is instantiated once per tile shape, each in its own
-// translation unit.  The inner product runs on Blackwell's
+// Tile: (64 * WARPS_M) x (4 * LN * WARPS_N) outputs per block (warps of
+// 64 x 4 LN, each lane 8 x LN outputs split into 4-wide groups): 128 x 128 at
+// K step 64, one block per SM, in general; 256 x 32 at K step 32, two blocks
+// per SM, for N <= 32; 128 x 256 (LN = 16) and 128 x 64 as opt-in shapes.
+// This header is instantiated once per tile shape, each in its own
+// translation unit.
+//
+// Two kernels share the inner product and the epilogue: sgemm_ffma_kernel,
+// whose warps stage every layout themselves with cp.async copies and a block
+// barrier per K step, and sgemm_ws_kernel, for operands stored k-major with
+// aligned rows (what the packing pre-pass writes), where a producer warp
+// feeds the ring by TMA and the math warps synchronise only through the
+// stages' mbarriers (measured at 4096^3: 2.22 -> 1.92 ms, the FMA pipe 80 ->
+// 90 % busy).  The inner product runs on Blackwell's
 // paired FP32 FMA (fma.rn.f32x2): one instruction updates two adjacent outputs
 // of a lane, halving the issue slots the FMAs take (the scalar-FMA version of
 // this kernel was bound by instruction issue).  Each half of the pair is an
@@ -39,6 +48,7 @@
 
 #include "common.cuh"
 #include "internal.h"
+#include "tensor_map.h"
 
 namespace gb300 {
 namespace {
@@ -47,12 +57,18 @@ namespace {
 #define GB300_SG_STAGES 3
 #endif
 constexpr int STAGES = GB300_SG_STAGES;
-// Block tile: (64 * WM) x (32 * WN) outputs, WM x WN warps of 64 x 32, K step
-// BK_, sized for MINB resident blocks per SM.
-template <int WM, int WN, int BK_, int MINB>
+// Block tile: (64 * WM) x (4 * LN * WN) outputs, WM x WN warps of 64 x 4 LN
+// (each lane 8 rows x LN columns, LN = 8 or 16), K step BK_, NST-stage ring,
+// sized for MINB resident blocks per SM.
+template <int WM, int WN, int BK_, int MINB, int LN_ = 8, int NST = STAGES>
 struct Tile {
   static constexpr int WARPS_M = WM, WARPS_N = WN;
-  static constexpr int BM = 64 * WM, BN = 32 * WN, BK = BK_;
+  static constexpr int LN = LN_;         // columns a lane owns
+  static constexpr int JP = LN / 2;      // ... as column pairs
+  static constexpr int HB = LN / 4;      // ... as 4-column groups, 16 columns apart
+  static constexpr int WARP_N = 4 * LN;  // columns a warp owns
+  static constexpr int BM = 64 * WM, BN = WARP_N * WN, BK = BK_;
+  static constexpr int NSTAGES = NST;
   static constexpr int THREADS = 32 * WM * WN;
   static constexpr int MIN_BLOCKS = MINB;
   static constexpr int APAD = BM + 4;  // k-major tile rows padded: conflict-free transposing writes
@@ -60,18 +76,24 @@ struct Tile {
   static constexpr int A_FLOATS = (BM * BK > BK * APAD) ? BM * BK : BK * APAD;
   static constexpr int B_FLOATS = BK * BPAD;
   static constexpr int STAGE_FLOATS = A_FLOATS + B_FLOATS;
-  static constexpr int SMEM_BYTES = STAGES * STAGE_FLOATS * 4;
+  static constexpr int SMEM_BYTES = NSTAGES * STAGE_FLOATS * 4;
   // chunk permutation within a row tile row (BK/4 chunks): XOR with (row / 4)
   // modulo the chunk count, at most 8
   static constexpr int SWZ_MASK = (BK / 4 < 8 ? BK / 4 : 8) - 1;
   static_assert(BK == 16 || BK == 32 || BK == 64, "K step");
+  static_assert(LN == 8 || LN == 16, "lane columns");
+  static_assert(NSTAGES >= 2, "stages");
 };
 // the general tile (128 x 128 at the defaults: 195 KiB at BK 64, 3 stages) and
 // the narrow one for N <= 32 (256 x 32, BK 32, two blocks per SM)
 using TileWide = Tile<SG_WARPS_M, SG_BN / 32, SG_BK, SG_BLOCKS_PER_SM>;
 using TileNarrow = Tile<SGN_BM / 64, SGN_BN / 32, SGN_BK, SGN_BLOCKS_PER_SM>;
+using TileBig = Tile<SGB_BM / 64, SGB_BN / 64, SGB_BK, 1, 16, SGB_STAGES>;
+using TileHalf = Tile<SGH_BM / 64, SGH_BN / 32, SGH_BK, SGH_BLOCKS_PER_SM, 8, SGH_STAGES>;
 static_assert(TileWide::BM == SG_BM && TileWide::BN == SG_BN, "tile shape");
 static_assert(TileNarrow::BM == SGN_BM && TileNarrow::BN == SGN_BN, "tile shape");
+static_assert(TileBig::BM == SGB_BM && TileBig::BN == SGB_BN, "tile shape");
+static_assert(TileHalf::BM == SGH_BM && TileHalf::BN == SGH_BN, "tile shape");
 
 // Tile rasterisation: blocks walk GROUP tile-rows column by column, so each B
 // panel is fetched from DRAM once per group while the group's A panels stay in
@@ -119,6 +141,12 @@ struct Params {
   unsigned int* sk_cnt;
   Epilogue ep;  // bias (fp32, per column) and activation, applied before the store
   int c_vec;    // C rows (and batch entries) 16-byte aligned: float4 epilogue accesses
+  // warp-specialised variant: the device status word its bounded waits flag
+  // their expiry in, their limit, and a test hook (1: the first stage's loads
+  // are never issued, so the first wait expires)
+  unsigned int* status;
+  uint64_t timeout_ns;
+  int fault_injection;
 };
 
 // Kernel kinds: one output tile per block (C), one K slice of a tile per
@@ -276,11 +304,232 @@ __device__ __forceinline__ int sk_owner(int64_t x, int G, int64_t I) {
 }
 __device__ __forceinline__ int64_t sk_start(int b, int G, int64_t I) { return (int64_t)b * I / G; }
 
+// One work item of a block: tile t over K range [kbeg, kend).  seg0 is the
+// first step of a stream-K segment; whole marks an item covering all of K.
+struct Item {
+  int t, kbeg, kend;
+  int64_t seg0;
+  bool whole;
+};
+
+// The persistent walk of block b of G: whole tiles b, b + G, ... below
+// dp_tiles, then the block's stream-K step range, one segment per tile it
+// touches.
+struct Walk {
+  int dp_next;
+  int64_t sk_it, sk_end, sk_first;
+  __device__ __forceinline__ void init(const Params& p, int b, int G) {
+    dp_next = b;
+    sk_first = sk_it = sk_start(b, G, p.sk_iters);
+    sk_end = sk_start(b + 1, G, p.sk_iters);
+  }
+  template <int BK>
+  __device__ __forceinline__ bool next(const Params& p, int G, Item& w) {
+    if (dp_next < p.dp_tiles) {
+      w.t = dp_next;
+      dp_next += G;
+      w.kbeg = 0;
+      w.kend = p.K;
+      w.seg0 = 0;
+      w.whole = true;
+      return true;
+    }
+    if (sk_it >= sk_end) return false;
+    const int64_t ts = sk_it / p.kiters;
+    const int s0 = (int)(sk_it - ts * p.kiters);
+    const int64_t left = sk_end - sk_it;
+    const int s1 = left < (int64_t)(p.kiters - s0) ? s0 + (int)left : p.kiters;
+    w.t = p.dp_tiles + (int)ts;
+    w.seg0 = sk_it;
+    sk_it += s1 - s0;
+    w.kbeg = s0 * BK;
+    w.kend = min(p.K, s1 * BK);
+    w.whole = s0 == 0 && s1 == p.kiters;
+    return true;
+  }
+};
+
+// Grouped rasterisation of the tile grid (consecutive tiles share B panels
+// within a group of group_m tile-rows): the first row and column of tile t.
+template <class TL>
+__device__ __forceinline__ void tile_origin(const Params& p, int t, int& m0, int& n0) {
+  const int per_group = p.group_m * p.tiles_n;
+  const int first_m = (t / per_group) * p.group_m;
+  const int gsize = min(p.tiles_m - first_m, p.group_m);
+  m0 = (first_m + (t % per_group) % gsize) * TL::BM;
+  n0 = ((t % per_group) / gsize) * TL::BN;
+}
+
+// One k of a lane's 8 x LN block: av holds its 8 A values (rows arow + {0..3},
+// arow + 32 + {0..3}); brow points at its B values in the stage's k row
+// (columns bcol + 16 h + {0..3}).
+template <class TL>
+__device__ __forceinline__ void fma_k(uint64_t (&acc)[8][TL::JP], const float (&av)[8],
+                                      const float* brow) {
+  constexpr int JP = TL::JP, HB = TL::HB;
+  uint64_t bp[JP];
+#pragma unroll
+  for (int h = 0; h < HB; ++h) {
+    const ulonglong2 b = *reinterpret_cast<const ulonglong2*>(brow + 16 * h);
+    bp[2 * h] = b.x;
+    bp[2 * h + 1] = b.y;
+  }
+  // All eight (a, a) pairs first, then column pair by column pair, the rows
+  // alternating between the two 4-row halves: the eight paired FMAs sharing
+  // bp[j] follow each other and none waits on the register move that builds
+  // its splatted operand.  Measured at 4096^3 against row by row (i outer, j
+  // inner): +5 %; rows in order 0..7: -0.1 %; other interleavings: -0.5 to
+  // -2.6 %.
+  uint64_t ap[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) ap[i] = splat2(av[i]);
+  constexpr int ORD[8] = {0, 4, 1, 5, 2, 6, 3, 7};
+#pragma unroll
+  for (int j = 0; j < JP; ++j)
+#pragma unroll
+    for (int ii = 0; ii < 8; ++ii) acc[ORD[ii]][j] = ffma2(ap[ORD[ii]], bp[j], acc[ORD[ii]][j]);
+}
+
+// Barrier over the threads that compute (N = 0: the whole block; else the
+// first N threads, named barrier 1, the other warps not taking part).
+template <int N>
+__device__ __forceinline__ void compute_sync() {
+  if constexpr (N == 0) __syncthreads();
+  else asm volatile("bar.sync 1, %0;" ::"n"(N) : "memory");
+}
+
+// The end of a work item.  A tile shared between blocks (not `whole`, a
+// persistent launch) has its partial sums published; only its last
+// contributor goes on, with the sum of all contributions.  Then the epilogue
+// (alpha, beta, bias, activation) stores the lane's block of C, or, in a
+// split launch, its raw sums in slice blockIdx.z of `partial`.  SYNC: the
+// barrier over the computing threads (compute_sync).
+template <class TL, int KIND, int SYNC>
+__device__ __forceinline__ void finish_item(const Params& p, uint64_t (&acc)[8][TL::JP],
+                                            const Item& w, int64_t sk_first, int m0, int n0,
+                                            float* Cg, int tid, int arow, int bcol, int& s_last) {
+  constexpr int BM = TL::BM, BN = TL::BN, THREADS = TL::THREADS, JP = TL::JP, HB = TL::HB;
+  if constexpr (KIND == KIND_PERSIST) {
+    if (!w.whole) {
+      // Every contributor stores its partial sums (warp-coalesced: float4 j
+      // of thread tid at [j][tid]) in its slot -- 0 for the segment a block
+      // starts with, 1 for the one it ends with -- then counts itself in.
+      // The last to arrive adds all segments in K order (so the result does
+      // not depend on arrival order) and stores the tile.
+      const int G = gridDim.x;
+      const int slot = w.seg0 == sk_first ? 0 : 1;
+      float4* mine = reinterpret_cast<float4*>(p.sk_ws) +
+                     (int64_t)(blockIdx.x * 2 + slot) * (BM * BN / 4);
+#pragma unroll
+      for (int i = 0; i < 8; ++i)
+#pragma unroll
+        for (int h = 0; h < HB; ++h) {
+          const float2 lo = unpack2(acc[i][2 * h]), hi = unpack2(acc[i][2 * h + 1]);
+          mine[(i * HB + h) * THREADS + tid] = make_float4(lo.x, lo.y, hi.x, hi.y);
+        }
+      __threadfence();
+      compute_sync<SYNC>();
+      const int64_t x0 = (int64_t)(w.t - p.dp_tiles) * p.kiters;
+      const int c_lo = sk_owner(x0, G, p.sk_iters);
+      const int c_hi = sk_owner(x0 + p.kiters - 1, G, p.sk_iters);
+      if (tid == 0) {
+        const unsigned int before = atomicAdd(p.sk_cnt + (w.t - p.dp_tiles), 1u);
+        s_last = before == (unsigned int)(c_hi - c_lo);
+      }
+      compute_sync<SYNC>();
+      const bool last = s_last != 0;
+      // (tid 0 writes s_last again only past the first barrier of the next
+      // shared tile, which every computing thread reaches after this read)
+      if (!last) return;
+      __threadfence();
+      float sum[8][JP][2];
+#pragma unroll
+      for (int i = 0; i < 8; ++i)
+#pragma unroll
+        for (int j = 0; j < JP; ++j) sum[i][j][0] = sum[i][j][1] = 0.f;
+      for (int c = c_lo; c <= c_hi; ++c) {
+        const int cs = sk_start(c, G, p.sk_iters) >= x0 ? 0 : 1;
+        const float4* part = reinterpret_cast<const float4*>(p.sk_ws) +
+                             (int64_t)(c * 2 + cs) * (BM * BN / 4);
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+#pragma unroll
+          for (int h = 0; h < HB; ++h) {
+            const float4 v = __ldcg(part + (i * HB + h) * THREADS + tid);
+            sum[i][2 * h][0] += v.x; sum[i][2 * h][1] += v.y;
+            sum[i][2 * h + 1][0] += v.z; sum[i][2 * h + 1][1] += v.w;
+          }
+      }
+#pragma unroll
+      for (int i = 0; i < 8; ++i)
+#pragma unroll
+        for (int j = 0; j < JP; ++j) acc[i][j] = pack2(sum[i][j][0], sum[i][j][1]);
+    }
+  }
+
+  // epilogue: lane columns bcol + 16 h + {0..3} (pairs 2h, 2h + 1)
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const int gm = m0 + arow + (i < 4 ? i : 32 + i - 4);
+    if (gm >= p.M) continue;
+#pragma unroll
+    for (int h = 0; h < HB; ++h) {
+      const int gn = n0 + bcol + h * 16;
+      const float2 lo = unpack2(acc[i][2 * h]), hi = unpack2(acc[i][2 * h + 1]);
+      const float v[4] = {lo.x, lo.y, hi.x, hi.y};
+      if constexpr (KIND == KIND_SPLIT) {
+        float* dst = p.partial + ((int64_t)blockIdx.z * p.M + gm) * p.N + gn;
+        if (gn + 3 < p.N && (p.N & 3) == 0) {
+          *reinterpret_cast<float4*>(dst) = make_float4(v[0], v[1], v[2], v[3]);
+        } else {
+#pragma unroll
+          for (int j = 0; j < 4; ++j)
+            if (gn + j < p.N) dst[j] = v[j];
+        }
+      } else {
+        float* dst = Cg + (int64_t)gm * p.ldc + gn;
+        const bool vec_ok = p.c_vec && (gn + 3 < p.N);
+        const bool epi = p.ep.bias != nullptr || p.ep.act != 0;
+        if (vec_ok) {
+          float4 o;
+          if (p.beta != 0.f) {
+            const float4 c = *reinterpret_cast<const float4*>(dst);
+            o = make_float4(__fmaf_rn(p.alpha, v[0], p.beta * c.x),
+                            __fmaf_rn(p.alpha, v[1], p.beta * c.y),
+                            __fmaf_rn(p.alpha, v[2], p.beta * c.z),
+                            __fmaf_rn(p.alpha, v[3], p.beta * c.w));
+          } else {
+            o = make_float4(p.alpha * v[0], p.alpha * v[1], p.alpha * v[2], p.alpha * v[3]);
+          }
+          if (epi) {
+            o.x = apply_epilogue<float>(o.x, p.ep, gn);
+            o.y = apply_epilogue<float>(o.y, p.ep, gn + 1);
+            o.z = apply_epilogue<float>(o.z, p.ep, gn + 2);
+            o.w = apply_epilogue<float>(o.w, p.ep, gn + 3);
+          }
+          *reinterpret_cast<float4*>(dst) = o;
+        } else {
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            if (gn + j < p.N) {
+              float o = (p.beta != 0.f) ? __fmaf_rn(p.alpha, v[j], p.beta * dst[j])
+                                        : p.alpha * v[j];
+              if (epi) o = apply_epilogue<float>(o, p.ep, gn + j);
+              dst[j] = o;
+            }
+          }
+        }
+      }
+    }
+  }
+}
+
 template <class TL, bool A_K, bool B_K, bool VEC, int KIND>
 __global__ void __launch_bounds__(TL::THREADS, TL::MIN_BLOCKS) sgemm_ffma_kernel(const Params p) {
-  constexpr int BM = TL::BM, BN = TL::BN, BK = TL::BK, THREADS = TL::THREADS;
+  constexpr int BM = TL::BM, BK = TL::BK;
   constexpr int WARPS_N = TL::WARPS_N, APAD = TL::APAD, BPAD = TL::BPAD;
   constexpr int A_FLOATS = TL::A_FLOATS, STAGE_FLOATS = TL::STAGE_FLOATS;
+  constexpr int JP = TL::JP, NST = TL::NSTAGES;
   // (the previous kernel in the stream completes before any global access)
   pdl_wait();
   pdl_trigger();
@@ -288,11 +537,11 @@ __global__ void __launch_bounds__(TL::THREADS, TL::MIN_BLOCKS) sgemm_ffma_kernel
   __shared__ int s_last;
   const int tid = threadIdx.x;
   const int warp = tid >> 5, lane = tid & 31;
-  const int wm = (warp / WARPS_N) * 64;  // warp's first row in the tile
-  const int wn = (warp % WARPS_N) * 32;  // warp's first column
+  const int wm = (warp / WARPS_N) * 64;          // warp's first row in the tile
+  const int wn = (warp % WARPS_N) * TL::WARP_N;  // warp's first column
   const int ty = lane >> 2, tx = lane & 3;
   const int arow = wm + ty * 4;     // lane rows: arow + {0..3}, arow + 32 + {0..3}
-  const int bcol = wn + tx * 4;     // lane cols: bcol + {0..3}, bcol + 16 + {0..3}
+  const int bcol = wn + tx * 4;     // lane cols: bcol + 16 h + {0..3}, h < HB
   const int aswz = (arow >> 2) & TL::SWZ_MASK;  // row-tile chunk permutation, same for all 8 lane rows
 
   const float* const Ag = p.A + (int64_t)blockIdx.y * p.stride_a;
@@ -303,58 +552,29 @@ __global__ void __launch_bounds__(TL::THREADS, TL::MIN_BLOCKS) sgemm_ffma_kernel
   // work state: non-persistent blocks do one item; persistent blocks walk
   // their whole tiles, then their stream-K step range
   const int G = gridDim.x;
-  int dp_next = blockIdx.x;
-  int64_t sk_it = 0, sk_end = 0, sk_first = 0;
-  if constexpr (KIND == KIND_PERSIST) {
-    sk_first = sk_it = sk_start(blockIdx.x, G, p.sk_iters);
-    sk_end = sk_start(blockIdx.x + 1, G, p.sk_iters);
-  }
+  Walk walk = {};
+  if constexpr (KIND == KIND_PERSIST) walk.init(p, blockIdx.x, G);
   bool first_item = true;
 
-  // acc[i][jp] holds the outputs (row i, columns 2jp and 2jp+1) as a pair
-  uint64_t acc[8][4];
+  // acc[i][jp] holds the outputs (row i, lane columns 2jp and 2jp+1) as a pair
+  uint64_t acc[8][JP];
 
   for (;;) {
-    // ---- next work item: tile t, K range [kbeg, kend)
-    int t, kbeg, kend;
-    int64_t seg0 = 0;  // stream-K: first step of this segment
-    bool whole = true;
+    Item w;
     if constexpr (KIND != KIND_PERSIST) {
       if (!first_item) break;
-      t = blockIdx.x;
-      kbeg = blockIdx.z * p.k_slice;
-      kend = min(p.K, kbeg + p.k_slice);
+      w.t = blockIdx.x;
+      w.kbeg = blockIdx.z * p.k_slice;
+      w.kend = min(p.K, w.kbeg + p.k_slice);
+      w.seg0 = 0;
+      w.whole = true;
     } else {
-      if (dp_next < p.dp_tiles) {
-        t = dp_next;
-        dp_next += G;
-        kbeg = 0;
-        kend = p.K;
-      } else if (sk_it < sk_end) {
-        const int64_t ts = sk_it / p.kiters;
-        const int s0 = (int)(sk_it - ts * p.kiters);
-        const int64_t left = sk_end - sk_it;
-        const int s1 = left < (int64_t)(p.kiters - s0) ? s0 + (int)left : p.kiters;
-        t = p.dp_tiles + (int)ts;
-        seg0 = sk_it;
-        sk_it += s1 - s0;
-        kbeg = s0 * BK;
-        kend = min(p.K, s1 * BK);
-        whole = s0 == 0 && s1 == p.kiters;
-      } else {
-        break;
-      }
+      if (!walk.next<BK>(p, G, w)) break;
     }
     first_item = false;
-
-    // grouped rasterisation of the tile grid (consecutive tiles share B panels
-    // within a group of group_m tile-rows)
-    const int per_group = p.group_m * p.tiles_n;
-    const int first_m = (t / per_group) * p.group_m;
-    const int gsize = min(p.tiles_m - first_m, p.group_m);
-    const int tm = first_m + (t % per_group) % gsize;
-    const int tn = (t % per_group) / gsize;
-    const int m0 = tm * BM, n0 = tn * BN;
+    int m0, n0;
+    tile_origin<TL>(p, w.t, m0, n0);
+    const int kbeg = w.kbeg, kend = w.kend;
     const int nk = (kend - kbeg + BK - 1) / BK;
 
     auto stage_load = [&](int s, int k0) {
@@ -362,31 +582,31 @@ __global__ void __launch_bounds__(TL::THREADS, TL::MIN_BLOCKS) sgemm_ffma_kernel
       if constexpr (A_K) load_rows<TL, VEC>(st, Ag, p.lda, m0, p.M, k0, kend, tid);
       else load_kmajor<TL, VEC, BM, APAD>(st, Ag, p.lda, m0, p.M, k0, kend, tid);
       const uint32_t sb = st + A_FLOATS * 4u;
-      if constexpr (B_K) load_transpose<TL, BN, BPAD>(sb, Bg, p.ldb, n0, p.N, k0, kend, tid);
-      else load_kmajor<TL, VEC, BN, BPAD>(sb, Bg, p.ldb, n0, p.N, k0, kend, tid);
+      if constexpr (B_K) load_transpose<TL, TL::BN, BPAD>(sb, Bg, p.ldb, n0, p.N, k0, kend, tid);
+      else load_kmajor<TL, VEC, TL::BN, BPAD>(sb, Bg, p.ldb, n0, p.N, k0, kend, tid);
     };
 
 #pragma unroll
     for (int i = 0; i < 8; ++i)
 #pragma unroll
-      for (int j = 0; j < 4; ++j) acc[i][j] = 0ull;
+      for (int j = 0; j < JP; ++j) acc[i][j] = 0ull;
 
     if constexpr (KIND == KIND_PERSIST) __syncthreads();  // the previous item's stages are free
 #pragma unroll
-    for (int s = 0; s < STAGES - 1; ++s) {
+    for (int s = 0; s < NST - 1; ++s) {
       if (s < nk) stage_load(s, kbeg + s * BK);
       cp_async_commit();
     }
 
     for (int kt = 0; kt < nk; ++kt) {
-      cp_async_wait<STAGES - 2>();
+      cp_async_wait<NST - 2>();
       __syncthreads();  // stage kt visible to all; stage kt-1 fully consumed
       {
-        const int nxt = kt + STAGES - 1;
-        if (nxt < nk) stage_load(nxt % STAGES, kbeg + nxt * BK);
+        const int nxt = kt + NST - 1;
+        if (nxt < nk) stage_load(nxt % NST, kbeg + nxt * BK);
         cp_async_commit();
       }
-      const float* As = smem + (kt % STAGES) * STAGE_FLOATS;
+      const float* As = smem + (kt % NST) * STAGE_FLOATS;
       const float* Bs = As + A_FLOATS;
 #pragma unroll KC_UNROLL
       for (int kc = 0; kc < BK / 4; ++kc) {
@@ -414,139 +634,149 @@ __global__ void __launch_bounds__(TL::THREADS, TL::MIN_BLOCKS) sgemm_ffma_kernel
             av[0] = lo.x; av[1] = lo.y; av[2] = lo.z; av[3] = lo.w;
             av[4] = hi.x; av[5] = hi.y; av[6] = hi.z; av[7] = hi.w;
           }
-          const float* brow = Bs + k * BPAD + bcol;
-          const ulonglong2 b01 = *reinterpret_cast<const ulonglong2*>(brow);
-          const ulonglong2 b23 = *reinterpret_cast<const ulonglong2*>(brow + 16);
-          const uint64_t bp[4] = {b01.x, b01.y, b23.x, b23.y};
-          // All eight (a, a) pairs first, then column pair by column pair, the
-          // rows alternating between the two 4-row halves: the eight paired
-          // FMAs sharing bp[j] follow each other and none waits on the register
-          // move that builds its splatted operand.  Measured at 4096^3 against
-          // row by row (i outer, j inner): +5 %; rows in order 0..7: -0.1 %;
-          // other interleavings: -0.5 to -2.6 %.
-          uint64_t ap[8];
-#pragma unroll
-          for (int i = 0; i < 8; ++i) ap[i] = splat2(av[i]);
-          constexpr int ORD[8] = {0, 4, 1, 5, 2, 6, 3, 7};
-#pragma unroll
-          for (int j = 0; j < 4; ++j)
-#pragma unroll
-            for (int ii = 0; ii < 8; ++ii) acc[ORD[ii]][j] = ffma2(ap[ORD[ii]], bp[j], acc[ORD[ii]][j]);
+          fma_k<TL>(acc, av, Bs + k * BPAD + bcol);
         }
       }
     }
     cp_async_wait<0>();
 
-    if constexpr (KIND == KIND_PERSIST) {
-      if (!whole) {
-        // A tile shared between blocks.  Every contributor stores its partial
-        // sums (warp-coalesced: float4 j of thread tid at [j][tid]) in its
-        // slot -- 0 for the segment a block starts with, 1 for the one it
-        // ends with -- then counts itself in.  The last to arrive adds all
-        // segments in K order (so the result does not depend on arrival
-        // order) and stores the tile.
-        const int slot = seg0 == sk_first ? 0 : 1;
-        float4* mine = reinterpret_cast<float4*>(p.sk_ws) +
-                       (int64_t)(blockIdx.x * 2 + slot) * (BM * BN / 4);
-#pragma unroll
-        for (int i = 0; i < 8; ++i)
-#pragma unroll
-          for (int h = 0; h < 2; ++h) {
-            const float2 lo = unpack2(acc[i][2 * h]), hi = unpack2(acc[i][2 * h + 1]);
-            mine[(i * 2 + h) * THREADS + tid] = make_float4(lo.x, lo.y, hi.x, hi.y);
-          }
-        __threadfence();
-        __syncthreads();
-        const int64_t x0 = (int64_t)(t - p.dp_tiles) * p.kiters;
-        const int c_lo = sk_owner(x0, G, p.sk_iters);
-        const int c_hi = sk_owner(x0 + p.kiters - 1, G, p.sk_iters);
-        if (tid == 0) {
-          const unsigned int before = atomicAdd(p.sk_cnt + (t - p.dp_tiles), 1u);
-          s_last = before == (unsigned int)(c_hi - c_lo);
-        }
-        __syncthreads();
-        if (!s_last) continue;
-        __threadfence();
-        float sum[8][4][2];
-#pragma unroll
-        for (int i = 0; i < 8; ++i)
-#pragma unroll
-          for (int j = 0; j < 4; ++j) sum[i][j][0] = sum[i][j][1] = 0.f;
-        for (int c = c_lo; c <= c_hi; ++c) {
-          const int cs = sk_start(c, G, p.sk_iters) >= x0 ? 0 : 1;
-          const float4* part = reinterpret_cast<const float4*>(p.sk_ws) +
-                               (int64_t)(c * 2 + cs) * (BM * BN / 4);
-#pragma unroll
-          for (int i = 0; i < 8; ++i)
-#pragma unroll
-            for (int h = 0; h < 2; ++h) {
-              const float4 v = __ldcg(part + (i * 2 + h) * THREADS + tid);
-              sum[i][2 * h][0] += v.x; sum[i][2 * h][1] += v.y;
-              sum[i][2 * h + 1][0] += v.z; sum[i][2 * h + 1][1] += v.w;
-            }
-        }
-#pragma unroll
-        for (int i = 0; i < 8; ++i)
-#pragma unroll
-          for (int j = 0; j < 4; ++j) acc[i][j] = pack2(sum[i][j][0], sum[i][j][1]);
-      }
-    }
+    finish_item<TL, KIND, 0>(p, acc, w, walk.sk_first, m0, n0, Cg, tid, arow, bcol, s_last);
+  }
+}
 
-    // epilogue: lane columns bcol + {0..3} (pairs 0, 1) and bcol + 16 + {0..3} (pairs 2, 3)
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      const int gm = m0 + arow + (i < 4 ? i : 32 + i - 4);
-      if (gm >= p.M) continue;
-#pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        const int gn = n0 + bcol + h * 16;
-        const float2 lo = unpack2(acc[i][2 * h]), hi = unpack2(acc[i][2 * h + 1]);
-        const float v[4] = {lo.x, lo.y, hi.x, hi.y};
-        if constexpr (KIND == KIND_SPLIT) {
-          float* dst = p.partial + ((int64_t)blockIdx.z * p.M + gm) * p.N + gn;
-          if (gn + 3 < p.N && (p.N & 3) == 0) {
-            *reinterpret_cast<float4*>(dst) = make_float4(v[0], v[1], v[2], v[3]);
-          } else {
-#pragma unroll
-            for (int j = 0; j < 4; ++j)
-              if (gn + j < p.N) dst[j] = v[j];
+// ---------------------------------------------------------------- warp-specialised
+// Persistent variant for operands stored k-major with 16-byte aligned rows
+// (A as [K, M], B as [K, N]: the layouts the packing pre-pass writes).  One
+// extra warp streams both operand tiles of every K step into the NST-stage
+// ring by TMA, each stage's arrival counted on its `full` mbarrier; the
+// computing warps wait only for the stage they need and release it with one
+// arrival per warp on its `empty` mbarrier.  No block-wide barrier and no
+// copy instruction sits in the main loop, and the loads of the next item's
+// first stages overlap the current item's epilogue.  Tile parts past M, N or
+// K read as zeros (the tensor maps' out-of-range fill).  Every wait is
+// bounded: a warp whose wait expires stops computing (the status word then
+// holds GEMM_ERR_TIMEOUT) but still walks its items, so the computing warps'
+// barriers stay matched; the producer drains its copies in flight.
+template <class TL>
+struct WsCfg {
+  static constexpr int A_BYTES = TL::BM * TL::BK * 4;  // [BK][BM], dense rows
+  static constexpr int B_BYTES = TL::BN * TL::BK * 4;  // [BK][BN]
+  static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+  static constexpr int THREADS = TL::THREADS + 32;
+  static constexpr int SMEM_BYTES = TL::NSTAGES * STAGE_BYTES + 1024;  // + alignment slack
+  static_assert(A_BYTES % 1024 == 0 && B_BYTES % 1024 == 0, "stage alignment");
+};
+
+template <class TL>
+__global__ void __launch_bounds__(TL::THREADS + 32, TL::MIN_BLOCKS)
+    sgemm_ws_kernel(const __grid_constant__ CUtensorMap tmA,
+                    const __grid_constant__ CUtensorMap tmB, const Params p) {
+  constexpr int BM = TL::BM, BN = TL::BN, BK = TL::BK, NST = TL::NSTAGES, JP = TL::JP;
+  constexpr int WARPS = TL::THREADS / 32;
+  using WC = WsCfg<TL>;
+  extern __shared__ __align__(1024) uint8_t ws_smem[];
+  __shared__ __align__(8) uint64_t bars[2 * NST];
+  __shared__ uint32_t s_abort;
+  __shared__ int s_last;
+  const uint32_t raw = smem_u32(ws_smem);
+  const uint32_t ring = (raw + 1023u) & ~1023u;
+  const float* const ring_f = reinterpret_cast<const float*>(ws_smem + (ring - raw));
+  const uint32_t bar0 = smem_u32(bars);
+  auto full_bar = [&](int s) { return bar0 + 8u * (uint32_t)s; };
+  auto empty_bar = [&](int s) { return bar0 + 8u * (uint32_t)(NST + s); };
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  if (tid == 0) {
+    for (int s = 0; s < NST; ++s) {
+      mbar_init(full_bar(s), 1);
+      mbar_init(empty_bar(s), WARPS);
+    }
+    s_abort = 0u;
+    fence_mbar_init();
+  }
+  __syncthreads();
+  // (the previous kernel in the stream completes before any global access)
+  pdl_wait();
+  pdl_trigger();
+  const WaitCtl wc{p.status, &s_abort, p.timeout_ns};
+  const int G = gridDim.x;
+  Walk walk = {};
+  walk.init(p, blockIdx.x, G);
+  Item w;
+
+  if (warp == WARPS) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      tma_prefetch_desc(&tmA);
+      tma_prefetch_desc(&tmB);
+      int stage = 0;
+      uint32_t phase = 0, pending = 0, pend_phase = 0;  // per stage: last load issued / its parity
+      bool ok = true, first = true;
+      while (ok && walk.next<BK>(p, G, w)) {
+        int m0, n0;
+        tile_origin<TL>(p, w.t, m0, n0);
+        for (int k0 = w.kbeg; k0 < w.kend; k0 += BK) {
+          if (!mbar_wait(empty_bar(stage), phase ^ 1u, wc)) { ok = false; break; }
+          // (test hook: the first stage's loads are never issued)
+          const bool skip = first && p.fault_injection == 1;
+          first = false;
+          if (!skip) {
+            const uint32_t sa = ring + (uint32_t)(stage * WC::STAGE_BYTES);
+            mbar_arrive_expect_tx(full_bar(stage), WC::STAGE_BYTES);
+            tma_load_3d(sa, &tmA, m0, k0, 0, full_bar(stage));
+            tma_load_3d(sa + WC::A_BYTES, &tmB, n0, k0, 0, full_bar(stage));
+            pending |= 1u << stage;
+            pend_phase = (pend_phase & ~(1u << stage)) | (phase << stage);
           }
-        } else {
-          float* dst = Cg + (int64_t)gm * p.ldc + gn;
-          const bool vec_ok = p.c_vec && (gn + 3 < p.N);
-          const bool epi = p.ep.bias != nullptr || p.ep.act != 0;
-          if (vec_ok) {
-            float4 o;
-            if (p.beta != 0.f) {
-              const float4 c = *reinterpret_cast<const float4*>(dst);
-              o = make_float4(__fmaf_rn(p.alpha, v[0], p.beta * c.x),
-                              __fmaf_rn(p.alpha, v[1], p.beta * c.y),
-                              __fmaf_rn(p.alpha, v[2], p.beta * c.z),
-                              __fmaf_rn(p.alpha, v[3], p.beta * c.w));
-            } else {
-              o = make_float4(p.alpha * v[0], p.alpha * v[1], p.alpha * v[2], p.alpha * v[3]);
-            }
-            if (epi) {
-              o.x = apply_epilogue<float>(o.x, p.ep, gn);
-              o.y = apply_epilogue<float>(o.y, p.ep, gn + 1);
-              o.z = apply_epilogue<float>(o.z, p.ep, gn + 2);
-              o.w = apply_epilogue<float>(o.w, p.ep, gn + 3);
-            }
-            *reinterpret_cast<float4*>(dst) = o;
-          } else {
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-              if (gn + j < p.N) {
-                float o = (p.beta != 0.f) ? __fmaf_rn(p.alpha, v[j], p.beta * dst[j])
-                                          : p.alpha * v[j];
-                if (epi) o = apply_epilogue<float>(o, p.ep, gn + j);
-                dst[j] = o;
-              }
-            }
-          }
+          if (++stage == NST) { stage = 0; phase ^= 1u; }
         }
       }
+      // every load issued lands before the block's shared memory is released
+      for (int s = 0; s < NST; ++s)
+        if (pending & (1u << s)) mbar_wait_drain(full_bar(s), (pend_phase >> s) & 1u, p.timeout_ns);
     }
+    return;
+  }
+
+  // -------------------------------------------------------------- computing warps
+  const int wm = (warp / TL::WARPS_N) * 64;          // warp's first row in the tile
+  const int wn = (warp % TL::WARPS_N) * TL::WARP_N;  // warp's first column
+  const int ty = lane >> 2, tx = lane & 3;
+  const int arow = wm + ty * 4;  // lane rows: arow + {0..3}, arow + 32 + {0..3}
+  const int bcol = wn + tx * 4;  // lane cols: bcol + 16 h + {0..3}, h < HB
+  uint64_t acc[8][JP];
+  int stage = 0;
+  uint32_t phase = 0;
+  bool failed = false;
+  while (walk.next<BK>(p, G, w)) {
+    int m0, n0;
+    tile_origin<TL>(p, w.t, m0, n0);
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+#pragma unroll
+      for (int j = 0; j < JP; ++j) acc[i][j] = 0ull;
+    for (int k0 = w.kbeg; k0 < w.kend; k0 += BK) {
+      if (!failed) failed = !__all_sync(0xffffffffu, mbar_wait(full_bar(stage), phase, wc));
+      if (!failed) {
+        const float* As = ring_f + stage * (WC::STAGE_BYTES / 4);
+        const float* Bs = As + BM * BK;
+#pragma unroll KC_UNROLL
+        for (int kc = 0; kc < BK / 4; ++kc) {
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk) {
+            const int k = kc * 4 + kk;
+            const float4 lo = lds128(As + k * BM + arow);
+            const float4 hi = lds128(As + k * BM + arow + 32);
+            const float av[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
+            fma_k<TL>(acc, av, Bs + k * BN + bcol);
+          }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(empty_bar(stage));
+      }
+      if (++stage == NST) { stage = 0; phase ^= 1u; }
+    }
+    finish_item<TL, KIND_PERSIST, TL::THREADS>(p, acc, w, walk.sk_first, m0, n0, p.C, tid, arow,
+                                               bcol, s_last);
   }
 }
 
@@ -582,6 +812,27 @@ cudaError_t launch_vs(const Params& p, bool vec, int kind, dim3 grid, cudaStream
   return launch_one<TL, A_K, B_K, false, KIND_TILE>(p, grid, s);
 }
 
+// The warp-specialised launch: grid blocks over the persistent plan in p.
+template <class TL>
+cudaError_t launch_ws(const Params& p, const SgemmArgs& a, dim3 grid, cudaStream_t stream) {
+  using WC = WsCfg<TL>;
+  // A as [K, M] and B as [K, N], fp32, boxes of BK rows of the block tile's width
+  CUtensorMap mA, mB;
+  if (!make_map(&mA, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, a.A, a.K, a.M, a.lda, TL::BM, TL::BK,
+                CU_TENSOR_MAP_SWIZZLE_NONE, 1, 0, 4) ||
+      !make_map(&mB, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, a.B, a.K, a.N, a.ldb, TL::BN, TL::BK,
+                CU_TENSOR_MAP_SWIZZLE_NONE, 1, 0, 4))
+    return cudaErrorNotSupported;
+  auto kern = sgemm_ws_kernel<TL>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       WC::SMEM_BYTES);
+  if (e == cudaSuccess && TL::MIN_BLOCKS > 1)
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout,
+                             (int)cudaSharedmemCarveoutMaxShared);
+  if (e != cudaSuccess) return e;
+  return launch_kernel(kern, grid, dim3(WC::THREADS), WC::SMEM_BYTES, stream, 1, mA, mB, p);
+}
+
 // The whole launch for tile TL (host side of launch_sgemm).
 template <class TL, bool PERSIST>
 cudaError_t launch_sgemm_t(const SgemmArgs& a, LaunchCtx& ctx) {
@@ -602,6 +853,9 @@ cudaError_t launch_sgemm_t(const SgemmArgs& a, LaunchCtx& ctx) {
   }
   p.alpha = a.alpha; p.beta = a.beta;
   p.ep = a.ep;
+  p.status = ctx.status;
+  p.timeout_ns = ctx.timeout_ns;
+  p.fault_injection = a.fault_injection;
   const int batch = a.batch > 1 ? a.batch : 1;
   if (batch > 1 && (a.splits > 1 || batch > 65535)) return cudaErrorInvalidValue;
   p.stride_a = batch > 1 ? a.stride_a : 0;
@@ -634,8 +888,21 @@ cudaError_t launch_sgemm_t(const SgemmArgs& a, LaunchCtx& ctx) {
     grid = dim3(G, 1, 1);
   }
   const bool A_K = !a.transA, B_K = a.transB;
-  cudaError_t e;
-  if (A_K && !B_K) e = launch_vs<TL, true, false, PERSIST>(p, vec, kind, grid, ctx.stream);
+  cudaError_t e = cudaErrorInvalidValue;
+  // warp-specialised TMA staging (tiles with 8 x 8 lane blocks: with the
+  // extra warp ptxas holds a thread to 168 registers, where the 8 x 16 block
+  // spills): persistent over the stream-K plan, or one block per tile
+  // without one
+  constexpr bool WS = PERSIST && TL::LN == 8;
+  const bool ws = WS && a.ws && !split && batch == 1 && vec && !A_K && !B_K;
+  if (ws) {
+    if (kind != KIND_PERSIST) {
+      p.kiters = (a.K + BK - 1) / BK;
+      p.dp_tiles = tiles;
+      grid = dim3(tiles, 1, 1);
+    }
+    if constexpr (WS) e = launch_ws<TL>(p, a, grid, ctx.stream);
+  } else if (A_K && !B_K) e = launch_vs<TL, true, false, PERSIST>(p, vec, kind, grid, ctx.stream);
   else if (!A_K && !B_K) e = launch_vs<TL, false, false, PERSIST>(p, vec, kind, grid, ctx.stream);
   else if (A_K && B_K) e = launch_vs<TL, true, true, PERSIST>(p, vec, kind, grid, ctx.stream);
   else e = launch_vs<TL, false, true, PERSIST>(p, vec, kind, grid, ctx.stream);

@@ -137,6 +137,30 @@ def test_bounded_wait_reports_timeout_and_context_survives():
     assert compare.check(to_np(C.cpu()), ref, mag, "f16", exact=True)["ok"]
 
 
+def test_bounded_wait_reports_timeout_fp32_tma_staging():
+    """The same for the fp32 kernel whose operand tiles arrive by TMA (tn:
+    both operands stored k-major; 192 output tiles, no K split)."""
+    b = _b()
+    p = inputs.make_problem(2048, 1536, 256, True, False, "f32", "integer", seed=351)
+    A, B = p.A.cuda(), p.B.cuda()
+    C = torch.zeros((2048, 1536), dtype=torch.float32, device="cuda")
+    assert b.check_device_status() == b.OK
+    b.set_wait_timeout_ns(100_000_000)  # 0.1 s
+    b.set_fault_injection(1)
+    try:
+        b.gemm(A, B, C, True, False)
+        assert b.last_path() == "ffma"
+        assert b.check_device_status() == b.ERR_TIMEOUT
+    finally:
+        b.set_fault_injection(0)
+        b.set_wait_timeout_ns(0)
+    assert b.check_device_status() == b.OK
+    b.gemm(A, B, C, True, False)
+    assert b.check_device_status() == b.OK
+    ref, mag = oracle.gemm_ref(to_np(p.A), to_np(p.B), None, True, False)
+    assert compare.check(to_np(C.cpu()), ref, mag, "f32", exact=True)["ok"]
+
+
 def test_kernel_events_bracket_the_gemm_kernel():
     """gemm_set_kernel_events: the library records the caller's events around
     its main kernel only, so on a problem with a packing pre-pass (fp32 nn

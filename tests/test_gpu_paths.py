@@ -70,33 +70,52 @@ import sys
 sys.path.insert(0, {root!r}); sys.path.insert(0, {tests!r})
 from dense_gemm_tiled_gb300 import binding, inputs
 from helpers import check_problem
+# (the 128 x 128 tile's counts; the 128 x 256 tile splits the first three
+# shapes over K instead)
+want = ("ffma",) if {tile!r} == "0" else ("ffma", "ffma_splitk")
 for v in ("nn", "tn", "nt", "tt"):
     tA, tB = inputs.VARIANTS[v]
     # above the packing threshold (M*N*K >= 2^30) with more output tiles
     # than the split-K rule splits (> 152), ragged in every dimension
     p = inputs.make_problem(1000, 2600, 620, tA, tB, "f32", "uniform", seed=610, beta=0.5)
     r = check_problem(p)
-    assert r["path"] == "ffma", r
+    assert r["path"] in want, r
     p = inputs.make_problem(2048, 1408, 384, tA, tB, "f32", "integer", seed=611)
     r = check_problem(p, exact=True)
-    assert r["path"] == "ffma", r
+    assert r["path"] in want, r
     # odd leading dimensions everywhere (rows off 16-byte alignment)
     p = inputs.make_problem(1001, 2601, 621, tA, tB, "f32", "uniform", seed=612, beta=0.5)
     r = check_problem(p)
+    assert r["path"] in want, r
+    # 176 tiles of 128 x 256 (stream-K for that tile too), integer: exact
+    p = inputs.make_problem(2048, 2600, 400, tA, tB, "f32", "integer", seed=613, beta=1.0,
+                            c_fill="integer")
+    r = check_problem(p, exact=True)
     assert r["path"] == "ffma", r
 print("ok")
 """
 
 
-@pytest.mark.parametrize("pack,sk", [("1", "1"), ("0", "1"), ("1", "0")])
-def test_forced_fp32_configuration(lib_path, gpu, pack, sk):
+@pytest.mark.parametrize("pack,sk,tile,ws", [("1", "1", "0", "1"), ("0", "1", "0", "1"),
+                                             ("1", "0", "0", "1"), ("1", "1", "0", "0"),
+                                             ("1", "0", "0", "0"), ("1", "1", "2", "1"),
+                                             ("0", "1", "2", "1"), ("1", "0", "2", "1"),
+                                             ("1", "1", "3", "1"), ("0", "1", "3", "1"),
+                                             ("1", "1", "3", "0")])
+def test_forced_fp32_configuration(lib_path, gpu, pack, sk, tile, ws):
     """The fp32 transposing pre-pass (default on large problems) or the kernel
     reading every layout directly (GEMM_GB300_SG_PACK=0); the persistent
     stream-K launch (default when the tiles are not a whole number of rounds
-    of the SMs; both shapes here have 168 and 176 tiles) or one block per
-    tile (GEMM_GB300_SG_SK=0)."""
-    env = dict(os.environ, GEMM_GB300_SG_PACK=pack, GEMM_GB300_SG_SK=sk)
-    code = SCRIPT_F32.format(root=ROOT, tests=os.path.join(ROOT, "tests"))
+    of the SMs; the shapes here have 168 and 176 tiles of 128 x 128, 84 and 88
+    of 128 x 256, 336 and 352 of 128 x 64 against 304 resident blocks) or one
+    block per tile (GEMM_GB300_SG_SK=0); the 128 x 128 tile, the 128 x 256
+    one (lanes of 8 x 16 outputs) or the 128 x 64 one (GEMM_GB300_SG_TILE 0,
+    2, 3); operands stored k-major (packed, or tn as given) staged by the
+    warp-specialised TMA kernel (default for the 128 x 128 and 128 x 64
+    tiles) or by every warp's cp.async copies (GEMM_GB300_SG_WS=0)."""
+    env = dict(os.environ, GEMM_GB300_SG_PACK=pack, GEMM_GB300_SG_SK=sk, GEMM_GB300_SG_TILE=tile,
+               GEMM_GB300_SG_WS=ws)
+    code = SCRIPT_F32.format(root=ROOT, tests=os.path.join(ROOT, "tests"), tile=tile)
     r = subprocess.run([sys.executable, "-c", code], env=env, capture_output=True, text=True,
                        timeout=900)
     assert r.returncode == 0 and r.stdout.strip().endswith("ok"), r.stdout[-3000:] + r.stderr[-3000:]
