@@ -471,6 +471,21 @@ int run_gemm(int transA, int transB, int64_t M64, int64_t N64, int64_t K64, int 
     plan_f32(M, N, K, sms, &tile, &tiles, &splits, &k_slice);
     const bool narrow = tile == SG_TILE_NARROW;
     const SgTileShape ts = sg_tile_shape(tile);
+    const int64_t G = (int64_t)sms * ts.blocks_per_sm;  // resident blocks
+    // Fewer tiles than resident blocks on a large problem: rather than K
+    // slices and a reduction kernel, the warp-specialised kernel (operands
+    // packed k-major) shares every tile's K steps evenly over all blocks in
+    // one launch, the last contributor to a tile adding the others' partial
+    // sums -- while a tile has at most about four contributors (its fix-up is
+    // one block's reads).  Every block's step range must be non-empty.
+    const int64_t kiters = (K + ts.bk - 1) / ts.bk;
+    const bool sk_all = splits > 1 && !narrow && sg_ws_enabled() && sg_sk_enabled() &&
+                        sg_pack_enabled() && (double)M * N * K >= (double)(1ll << 30) &&
+                        tiles * 4 >= G && tiles * kiters >= G;
+    if (sk_all) {
+      splits = 1;
+      k_slice = K;
+    }
     SgemmArgs a{transA, transB, M, N, K, (const float*)A, lda, (const float*)B, ldb, (float*)C,
                 ldc, alpha, beta, splits, k_slice, nullptr};
     a.tile = tile;
@@ -502,8 +517,8 @@ int run_gemm(int transA, int transB, int64_t M64, int64_t N64, int64_t K64, int 
     // rounds of the SMs leaves the last round part-empty (4096^3: 1024 tiles,
     // 6.7 rounds of 152).  The persistent launch gives whole tiles to all but
     // the last one to two rounds and shares those rounds' K steps evenly.
-    const int64_t G = (int64_t)sms * ts.blocks_per_sm;  // resident blocks
-    const bool sk = splits == 1 && !narrow && sg_sk_enabled() && tiles >= G && tiles % G != 0;
+    const bool sk = splits == 1 && !narrow && sg_sk_enabled() && tiles % G != 0 &&
+                    (tiles >= G || sk_all);
     const int64_t sk_tiles = sk ? (tiles >= 2 * G ? tiles % G + G : tiles) : 0;
     const size_t bytes_S = sk ? (size_t)G * 2 * ts.bm * ts.bn * sizeof(float) : 0;
     const size_t bytes_N = sk ? ((size_t)sk_tiles * sizeof(unsigned int) + 255) / 256 * 256 : 0;

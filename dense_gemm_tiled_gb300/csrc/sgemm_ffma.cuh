@@ -876,11 +876,13 @@ cudaError_t launch_sgemm_t(const SgemmArgs& a, LaunchCtx& ctx) {
   p.dp_tiles = 0; p.kiters = 0; p.sk_iters = 0; p.sk_ws = nullptr; p.sk_cnt = nullptr;
   if (a.sk_blocks > 0) {
     // persistent: all but the last one to two rounds of whole tiles go to
-    // blocks in turn; the rest are shared out by K steps
+    // blocks in turn; the rest (every tile, with fewer tiles than blocks) are
+    // shared out by K steps, each block's range non-empty
     const int G = a.sk_blocks;
-    if (split || batch > 1 || tiles < G || !a.sk_ws || !a.sk_cnt) return cudaErrorInvalidValue;
-    kind = KIND_PERSIST;
     p.kiters = (a.K + BK - 1) / BK;
+    if (split || batch > 1 || (int64_t)tiles * p.kiters < G || !a.sk_ws || !a.sk_cnt)
+      return cudaErrorInvalidValue;
+    kind = KIND_PERSIST;
     p.dp_tiles = tiles >= 2 * G ? (tiles / G - 1) * G : 0;
     p.sk_iters = (int64_t)(tiles - p.dp_tiles) * p.kiters;
     p.sk_ws = a.sk_ws;

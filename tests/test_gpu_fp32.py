@@ -62,10 +62,12 @@ def test_skinny_split_k_beta():
     check_problem(p)
 
 
-@pytest.mark.parametrize("shape", [(2048, 2048, 2048), (1000, 3000, 777), (1536, 1664, 4100)])
+@pytest.mark.parametrize("shape", [(2048, 2048, 2048), (1000, 3000, 777), (1536, 1664, 4100),
+                                   (1024, 1152, 4096)])
 def test_stream_k_deterministic(shape):
     """Shapes whose tile count is not a whole number of rounds of the SMs run
-    as one persistent launch whose last rounds share K steps between blocks;
+    as one persistent launch whose last rounds share K steps between blocks
+    (with fewer tiles than SMs, as 72 tiles at 1024 x 1152, every tile's);
     the block that finishes a shared tile adds the pieces in K order, so two
     runs agree bit for bit whichever block arrives last."""
     import torch
