@@ -278,6 +278,22 @@ int pick_bn16(int M, int N, int K, int transA, int transB, int sms, int batch, i
 
 int cuda_fail(cudaError_t e) { return e == cudaErrorMemoryAllocation ? GEMM_ERR_NO_MEMORY : GEMM_ERR_CUDA; }
 
+// fp32 problem size (M*N*K, as a power of two) from which operands are packed
+// into the layout the kernels read fastest, and the most contributors a tile
+// gets when every tile's K steps are shared (resident blocks / tiles), as
+// compile-time knobs.  Measured on GB300 (whole calls, L2 flushed): packing
+// from 2^27 lost where it changed the path (1024 x 1024 x 512 38.6 -> 41.7 us,
+// 768 x 1024 x 768 nt 41.7 -> 46.1 us); up to 8 contributors against 4 gained
+// on 30 to 37 tiles (640 x 640 x 16384 265 -> 226 us, 768 x 768 x 8192 196 ->
+// 169 us, 640 x 768 x 4096 95 -> 85 us).
+#ifndef GB300_SG_PACK_MIN_LOG2
+#define GB300_SG_PACK_MIN_LOG2 30
+#endif
+#ifndef GB300_SG_SKALL_MAX_SHARE
+#define GB300_SG_SKALL_MAX_SHARE 8
+#endif
+constexpr double SG_PACK_MIN = (double)(1ll << GB300_SG_PACK_MIN_LOG2);
+
 // Split-K plan of the fp32 kernel: how many K slices, each a multiple of
 // `kstep` long.  Fewest K steps a slice gets (compile-time knob): one (a
 // 64-deep step of a 128 x 128 tile is ~1M FMAs), measured on small squares
@@ -476,12 +492,13 @@ int run_gemm(int transA, int transB, int64_t M64, int64_t N64, int64_t K64, int 
     // slices and a reduction kernel, the warp-specialised kernel (operands
     // packed k-major) shares every tile's K steps evenly over all blocks in
     // one launch, the last contributor to a tile adding the others' partial
-    // sums -- while a tile has at most about four contributors (its fix-up is
-    // one block's reads).  Every block's step range must be non-empty.
+    // sums -- while a tile has at most about GB300_SG_SKALL_MAX_SHARE
+    // contributors (its fix-up is one block's reads).  Every block's step
+    // range must be non-empty.
     const int64_t kiters = (K + ts.bk - 1) / ts.bk;
     const bool sk_all = splits > 1 && !narrow && sg_ws_enabled() && sg_sk_enabled() &&
-                        sg_pack_enabled() && (double)M * N * K >= (double)(1ll << 30) &&
-                        tiles * 4 >= G && tiles * kiters >= G;
+                        sg_pack_enabled() && (double)M * N * K >= SG_PACK_MIN &&
+                        tiles * GB300_SG_SKALL_MAX_SHARE >= G && tiles * kiters >= G;
     if (sk_all) {
       splits = 1;
       k_slice = K;
@@ -503,7 +520,7 @@ int run_gemm(int transA, int transB, int64_t M64, int64_t N64, int64_t K64, int 
     // transposing A would double its traffic: only a misaligned operand is
     // copied there, and it splits over K, so the test is on the problem size.)
     const bool big = (splits == 1 || narrow) && sg_pack_enabled() &&
-                     (double)M * N * K >= (double)(1ll << 30);
+                     (double)M * N * K >= SG_PACK_MIN;
     auto misaligned = [](const void* p, int64_t ld) { return ((uintptr_t)p % 16) != 0 || ld % 4 != 0; };
     const bool packA = big && ((!transA && !narrow) || misaligned(A, lda));
     const bool packB = big && (transB || misaligned(B, ldb));
