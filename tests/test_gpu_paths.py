@@ -92,9 +92,9 @@ for v in ("nn", "tn", "nt", "tt"):
                             c_fill="integer")
     r = check_problem(p, exact=True)
     assert r["path"] == "ffma", r
-    # fewer tiles than SMs on a large problem (64 of 128 x 128): every tile's
-    # K steps shared over all blocks in one launch of the warp-specialised
-    # kernel, up to 3 contributors a tile; otherwise split K; exact
+    # fewer tiles than SMs on a large problem (64 of 128 x 128, 32 of
+    # 128 x 256, 128 of 128 x 64): every tile's K steps shared over all blocks
+    # in one launch, up to 5 contributors a tile; otherwise split K; exact
     p = inputs.make_problem(1000, 1000, 1100, tA, tB, "f32", "integer", seed=614, beta=1.0,
                             c_fill="integer")
     r = check_problem(p, exact=True)
@@ -122,7 +122,7 @@ def test_forced_fp32_configuration(lib_path, gpu, pack, sk, tile, ws):
     tiles) or by every warp's cp.async copies (GEMM_GB300_SG_WS=0)."""
     env = dict(os.environ, GEMM_GB300_SG_PACK=pack, GEMM_GB300_SG_SK=sk, GEMM_GB300_SG_TILE=tile,
                GEMM_GB300_SG_WS=ws)
-    all_shared = pack == "1" and sk == "1" and ws == "1" and tile in ("0", "3")
+    all_shared = pack == "1" and sk == "1" and ws == "1"
     code = SCRIPT_F32.format(root=ROOT, tests=os.path.join(ROOT, "tests"), tile=tile,
                              all_shared=all_shared)
     r = subprocess.run([sys.executable, "-c", code], env=env, capture_output=True, text=True,
