@@ -185,8 +185,10 @@ int gemm_host(int transA, int transB, int64_t M, int64_t N, int64_t K, int dtype
  *   - a tensor-core problem whose shared tiles would not fit the array runs
  *     with whole tiles only (no scratch needed);
  *   - gemm()'s scratch-based steps are left out: the fp32 operand packing and
- *     persistent stream-K launch on large problems, and the aligned working
- *     copy of an unaligned fp16 C (the kernel stores such a C row by row);
+ *     persistent stream-K launch on large problems (where gemm() shares the K
+ *     steps of fewer tiles than SMs in one launch, this call keeps the K
+ *     slices and their reduction), and the aligned working copy of an
+ *     unaligned fp16 C (the kernel stores such a C row by row);
  *   - fp16/bf16 operands must have 16-byte aligned bases and row pitches (lda,
  *     ldb multiples of 8), else GEMM_ERR_UNSUPPORTED (padding them would need
  *     scratch); GEMM_F32_TF32 and GEMM_F32_3XTF32 are not accepted.
