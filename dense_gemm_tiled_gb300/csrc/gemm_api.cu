@@ -13,10 +13,12 @@
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
+#include <stdio.h>
 #include <stdlib.h>
 #include <string.h>
 
 #include <atomic>
+#include <memory>
 #include <mutex>
 
 #include "../../include/gemm.h"
@@ -156,6 +158,23 @@ int host_pipeline_enabled() {
   static const int v = [] {
     const char* s = getenv("GEMM_GB300_HOST_PIPELINE");
     return (s && s[0] == '0') ? 0 : 1;
+  }();
+  return v;
+}
+
+// gemm_host's schedule on large problems (env GEMM_GB300_HOST_SCHED="P,S,T"):
+// P row panels, the first run as S products over K slices (fp32 C), the last
+// cut into T pieces so that the final read-back is short.  Zero fields take
+// the defaults.
+struct HostSched {
+  int panels, kslices, tail;
+};
+HostSched host_sched_env() {
+  static const HostSched v = [] {
+    HostSched h{0, 0, 0};
+    const char* s = getenv("GEMM_GB300_HOST_SCHED");
+    if (s) sscanf(s, "%d,%d,%d", &h.panels, &h.kslices, &h.tail);
+    return h;
   }();
   return v;
 }
@@ -660,12 +679,14 @@ cudaError_t side_streams(cudaStream_t* in, cudaStream_t* out) {
 }
 
 struct EventSet {
-  cudaEvent_t ev[2 * 8 + 2] = {};
+  static constexpr int CAP = 2 * 72 + 2 + 16;
+  cudaEvent_t ev[CAP] = {};
   int n = 0;
   ~EventSet() {
     for (int i = 0; i < n; ++i) cudaEventDestroy(ev[i]);
   }
   cudaError_t make(int count) {
+    if (count > CAP) return cudaErrorInvalidValue;
     for (; n < count; ++n) {
       cudaError_t e = cudaEventCreateWithFlags(&ev[n], cudaEventDisableTiming);
       if (e != cudaSuccess) return e;
@@ -673,6 +694,17 @@ struct EventSet {
     return cudaSuccess;
   }
 };
+
+// gemm_host's pipeline events, kept per thread and device: created on first
+// use and reused, since every call synchronises before it returns (no event
+// is still pending when the next call records it).  Creating them per call
+// put ~20 event creations ahead of the first copy.
+EventSet* host_events(int dev) {
+  thread_local std::unique_ptr<EventSet> sets[MAX_DEVICES];
+  if (dev < 0 || dev >= MAX_DEVICES) return nullptr;
+  if (!sets[dev]) sets[dev].reset(new EventSet());
+  return sets[dev].get();
+}
 
 // Host buffers in, `panels` row panels of C computed and copied out as each
 // finishes; returns after the caller's stream has synchronised.
@@ -692,13 +724,40 @@ int host_pipelined(int transA, int transB, int64_t M, int64_t N, int64_t K, int 
   // once its slice of B (and of the panel's A rows) has arrived, accumulating
   // in C (beta = 1 after the first); so the first GEMM waits for a quarter of
   // B rather than all of it.  (16-bit C would be rounded between slices.)
-  const int NK = is_f32(dtype) && K >= 1024 ? 4 : 1;
+  const HostSched hs = host_sched_env();
+  if (hs.panels > 0) panels = hs.panels < 64 ? hs.panels : 64;
+  int NK = is_f32(dtype) && K >= 1024 ? 4 : 1;
+  if (hs.kslices > 0 && is_f32(dtype)) NK = hs.kslices < 16 ? hs.kslices : 16;
+  // (measured at 4096^3 fp32, whole calls: the last panel in two pieces
+  // 2.353 ms, in one 2.37-2.38, in four 2.37; 8 panels 2.40-2.44; 2 K slices
+  // 2.38, 8 K slices 2.47)
+  const int tail = hs.tail > 0 ? (hs.tail < 8 ? hs.tail : 8) : 2;
   const int64_t kl = ((K + NK - 1) / NK + 63) / 64 * 64;  // K per slice
+  // row ranges: panels of a whole number of 128-row tiles, the last one cut
+  // into `tail` pieces
+  int64_t rows[72];
+  int np = 0;
+  {
+    const int64_t pr = ((M + panels - 1) / panels + 127) / 128 * 128;
+    int64_t r = 0;
+    for (int p = 0; p < panels - 1 && r < M && np < 64; ++p, r += pr) rows[np++] = r;
+    if (r < M) {
+      const int64_t left = M - r;
+      const int64_t tr = ((left + tail - 1) / tail + 127) / 128 * 128;
+      for (int t = 0; t < tail && r < M && np < 71; ++t, r += tr) rows[np++] = r;
+    }
+    rows[np] = M;
+  }
   cudaStream_t sin, sout;
   cudaError_t ce = side_streams(&sin, &sout);
   if (ce != cudaSuccess) return cuda_fail(ce);
-  EventSet evs;
-  ce = evs.make(2 * panels + 2 + NK);
+  int dev = 0;
+  ce = cudaGetDevice(&dev);
+  if (ce != cudaSuccess) return cuda_fail(ce);
+  EventSet* evp = host_events(dev);
+  if (!evp) return GEMM_ERR_UNSUPPORTED;
+  EventSet& evs = *evp;
+  ce = evs.make(2 * np + 2 + NK);
   if (ce != cudaSuccess) return cuda_fail(ce);
   Scratch buf;
   ce = buf.get(nA + nB + nC, stream);
@@ -706,9 +765,7 @@ int host_pipelined(int transA, int transB, int64_t M, int64_t N, int64_t K, int 
   char* dA = (char*)buf.ptr;
   char* dB = dA + nA;
   char* dC = dB + nB;
-  cudaEvent_t ev_alloc = evs.ev[2 * panels], ev_out = evs.ev[2 * panels + 1];
-  // rows per panel: a whole number of 128-row tiles
-  const int64_t pr = ((M + panels - 1) / panels + 127) / 128 * 128;
+  cudaEvent_t ev_alloc = evs.ev[2 * np], ev_out = evs.ev[2 * np + 1];
   int path = GEMM_PATH_NONE, launches = 0;
   ce = cudaEventRecord(ev_alloc, stream);
   if (ce == cudaSuccess) ce = cudaStreamWaitEvent(sin, ev_alloc, 0);
@@ -716,9 +773,8 @@ int host_pipelined(int transA, int transB, int64_t M, int64_t N, int64_t K, int 
   if (ce == cudaSuccess && NK == 1)
     ce = cudaMemcpy2DAsync(dB, ldb_d * e, B, ldb * e, bc * e, br, cudaMemcpyHostToDevice, sin);
   int rc = GEMM_OK;
-  for (int p = 0; p < panels && ce == cudaSuccess && rc == GEMM_OK; ++p) {
-    const int64_t r0 = p * pr, r1 = r0 + pr < M ? r0 + pr : M;
-    if (r0 >= M) break;
+  for (int p = 0; p < np && ce == cudaSuccess && rc == GEMM_OK; ++p) {
+    const int64_t r0 = rows[p], r1 = rows[p + 1];
     const int64_t mp = r1 - r0;
     if (p == 0 && NK > 1) {
       // panel 0 (rows 0 .. mp), slice by slice: B rows k0..k1 of B[K,N] or
@@ -745,7 +801,7 @@ int host_pipelined(int transA, int transB, int64_t M, int64_t N, int64_t K, int 
         if (ce == cudaSuccess && c == 0 && beta != 0.f)
           ce = cudaMemcpy2DAsync(dC0, ldc_d * e, hC0, ldc * e, N * e, mp, cudaMemcpyHostToDevice,
                                  sin);
-        cudaEvent_t evk = evs.ev[2 * panels + 2 + c];
+        cudaEvent_t evk = evs.ev[2 * np + 2 + c];
         if (ce == cudaSuccess) ce = cudaEventRecord(evk, sin);
         if (ce == cudaSuccess) ce = cudaStreamWaitEvent(stream, evk, 0);
         if (ce != cudaSuccess) break;
