@@ -440,11 +440,13 @@ def skinny_hbm(dev, stream, peaks, reps: int = 30):
     return out
 
 
-def lora_step(dev, stream, reps: int = 20):
+def lora_step(dev, stream, peak_tflops, reps: int = 20):
     """The 18 GEMMs of one LoRA MLP-block training step ("Metal GEMM Kernels for
     LoRA Training", section 5: T=512, d=2048, FFN=5632, rank 32), fp16 with fp32
-    accumulation: per-GEMM device time (CUDA events, median; details on
-    stderr) and the whole set replayed as one CUDA graph."""
+    accumulation: per-GEMM device time (CUDA events around an eager call,
+    median; and the call alone in a CUDA graph replayed back to back, with its
+    fraction of the measured tensor peak; details on stderr) and the whole set
+    replayed as one CUDA graph."""
     import torch
     from dense_gemm_tiled_gb300 import binding, inputs
     gemms = inputs.lora_step_gemms()
@@ -464,10 +466,29 @@ def lora_step(dev, stream, reps: int = 20):
         one(op)
     torch.cuda.synchronize()
     per = {}
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     for op in ops:
         med, _, _ = spread(time_launches(lambda: one(op), stream, reps))
         per[op[0].name] = {"us": round(med * 1e3, 2), "path": binding.last_path(),
                            "shape": [op[0].M, op[0].N, op[0].K], "variant": op[0].variant}
+        # the call alone in a CUDA graph, replayed back to back: device time
+        # without the host's share of an eager call
+        g1 = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g1, stream=stream):
+            one(op)
+        for _ in range(3):
+            g1.replay()
+        torch.cuda.synchronize()
+        e0.record()
+        for _ in range(reps):
+            g1.replay()
+        e1.record()
+        e1.synchronize()
+        gus = e0.elapsed_time(e1) / reps * 1e3
+        fl = 2.0 * op[0].M * op[0].N * op[0].K
+        per[op[0].name]["graph_us"] = round(gus, 2)
+        per[op[0].name]["graph_frac"] = round(fl / (gus * 1e-6) / 1e12 / peak_tflops, 4)
+        del g1
     graph = torch.cuda.CUDAGraph()
     with torch.cuda.graph(graph, stream=stream):
         for op in ops:
@@ -486,7 +507,9 @@ def lora_step(dev, stream, reps: int = 20):
     detail("lora_step_per_gemm", per)
     return {"gemms": len(gemms), "gflop": round(flops / 1e9, 2), "graph_ms": round(graph_ms, 4),
             "graph_tflops": round(flops / (graph_ms * 1e-3) / 1e12, 1),
-            "sum_of_gemms_ms": round(sum(v["us"] for v in per.values()) / 1e3, 4)}
+            "sum_of_gemms_ms": round(sum(v["us"] for v in per.values()) / 1e3, 4),
+            "large_graph_frac": {k: v["graph_frac"] for k, v in per.items()
+                                 if min(v["shape"]) >= 512}}
 
 
 def control(dev, peaks):
@@ -804,7 +827,7 @@ def main():
         tf32 = None if args.no_fp16 else tf32_4096(dev, stream, flops, peaks, args)
         tf32x3 = None if args.no_fp16 else tf32x3_4096(dev, stream, flops, peaks, args)
         skinny = None if args.no_lora else skinny_hbm(dev, stream, peaks)
-        lora = None if args.no_lora else lora_step(dev, stream)
+        lora = None if args.no_lora else lora_step(dev, stream, peaks["bf16_tflops"])
         attn = None if args.no_attention else attention_step(dev, stream)
         clocks_run = clk.summary(start=0)
     ctl_after = control(dev, peaks) if not args.no_control else None
