@@ -104,10 +104,13 @@ constexpr int64_t RASTER_L2_BYTES = 32ll << 20;
 
 // Compile-time tuning knobs (measured on GB300 at 4096^3; the defaults won;
 // K step and stage count are GB300_SG_BK in internal.h and GB300_SG_STAGES:
-// 64 x 3 beat 32 x 3, 32 x 4, 64 x 2 and 16 x 6 by 0.4-5 %; 128 x 64 tiles
-// at two blocks per SM (GB300_SG_BN=64, GB300_SG_MIN_BLOCKS=2) were 1-3 %
-// slower; loading the next K step's fragments into a second register set
-// gained nothing):
+// with cp.async staging 64 x 3 beat 32 x 3, 32 x 4, 64 x 2 and 16 x 6 by
+// 0.4-5 %, and with TMA staging 32 x 6 was 2.5 % slower (1.968 against 1.919
+// ms; 8192^3 3 %); 128 x 64 tiles at two blocks per SM (GB300_SG_BN=64,
+// GB300_SG_MIN_BLOCKS=2) were 1-3 % slower; loading the next K step's
+// fragments into a second register set gained nothing; unrolling the whole
+// 16-chunk loop (GB300_SG_KC_UNROLL=16) was level at 4096^3 and up to 6 %
+// slower on short K):
 //  GB300_SG_MIN_BLOCKS  blocks per SM the register budget is sized for
 //  GB300_SG_KC_UNROLL   unrolling of the 4-k chunk loop
 #ifndef GB300_SG_KC_UNROLL
