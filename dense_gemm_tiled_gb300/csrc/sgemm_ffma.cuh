@@ -401,13 +401,22 @@ __device__ __forceinline__ void compute_sync() {
   else asm volatile("bar.sync 1, %0;" ::"n"(N) : "memory");
 }
 
+// Output row (within the tile) of a lane's i-th row: blocks of four, rows
+// arow + {0..3} and arow + 32 + {0..3} (RI false), or interleaved by eight,
+// rows arow + 8 i (RI true, the layout that reads a 128-byte-swizzled row
+// tile without bank conflicts).
+template <bool RI>
+__device__ __forceinline__ int lane_row(int arow, int i) {
+  return RI ? arow + 8 * i : arow + (i < 4 ? i : 32 + i - 4);
+}
+
 // The end of a work item.  A tile shared between blocks (not `whole`, a
 // persistent launch) has its partial sums published; only its last
 // contributor goes on, with the sum of all contributions.  Then the epilogue
 // (alpha, beta, bias, activation) stores the lane's block of C, or, in a
 // split launch, its raw sums in slice blockIdx.z of `partial`.  SYNC: the
-// barrier over the computing threads (compute_sync).
-template <class TL, int KIND, int SYNC>
+// barrier over the computing threads (compute_sync); RI: lane_row's layout.
+template <class TL, int KIND, int SYNC, bool RI = false>
 __device__ __forceinline__ void finish_item(const Params& p, uint64_t (&acc)[8][TL::JP],
                                             const Item& w, int64_t sk_first, int m0, int n0,
                                             float* Cg, int tid, int arow, int bcol, int& s_last) {
@@ -473,7 +482,7 @@ __device__ __forceinline__ void finish_item(const Params& p, uint64_t (&acc)[8][
   // epilogue: lane columns bcol + 16 h + {0..3} (pairs 2h, 2h + 1)
 #pragma unroll
   for (int i = 0; i < 8; ++i) {
-    const int gm = m0 + arow + (i < 4 ? i : 32 + i - 4);
+    const int gm = m0 + lane_row<RI>(arow, i);
     if (gm >= p.M) continue;
 #pragma unroll
     for (int h = 0; h < HB; ++h) {
@@ -648,21 +657,33 @@ __global__ void __launch_bounds__(TL::THREADS, TL::MIN_BLOCKS) sgemm_ffma_kernel
 }
 
 // ---------------------------------------------------------------- warp-specialised
-// Persistent variant for operands stored k-major with 16-byte aligned rows
-// (A as [K, M], B as [K, N]: the layouts the packing pre-pass writes).  One
-// extra warp streams both operand tiles of every K step into the NST-stage
-// ring by TMA, each stage's arrival counted on its `full` mbarrier; the
-// computing warps wait only for the stage they need and release it with one
-// arrival per warp on its `empty` mbarrier.  No block-wide barrier and no
-// copy instruction sits in the main loop, and the loads of the next item's
-// first stages overlap the current item's epilogue.  Tile parts past M, N or
-// K read as zeros (the tensor maps' out-of-range fill).  Every wait is
-// bounded: a warp whose wait expires stops computing (the status word then
-// holds GEMM_ERR_TIMEOUT) but still walks its items, so the computing warps'
-// barriers stay matched; the producer drains its copies in flight.
+// Variant for a B stored k-major ([K, N]) and an A stored either way, all rows
+// 16-byte aligned (the layouts the packing pre-pass writes, and the narrow
+// tile's A as given).  One extra warp streams both operand tiles of every K
+// step into the NST-stage ring by TMA, each stage's arrival counted on its
+// `full` mbarrier; the computing warps wait only for the stage they need and
+// release it with one arrival per warp on its `empty` mbarrier.  No
+// block-wide barrier and no copy instruction sits in the main loop, and in a
+// persistent launch the loads of the next item's first stages overlap the
+// current item's epilogue.  Tile parts past M, N or K read as zeros (the
+// tensor maps' out-of-range fill).
+//
+// A stored [K, M] (A_K false) arrives as BK dense rows of BM floats.  A
+// stored [M, K] (A_K true, K step 32) arrives as BM rows of 32 floats = 128
+// bytes with the tensor unit's 128-byte swizzle (16-byte chunk j of row r at
+// chunk j ^ (r & 7)); a lane then owns rows interleaved by eight (lane_row),
+// so that the eight row groups of a warp read eight different chunks: no bank
+// conflicts.
+//
+// KIND_PERSIST walks whole tiles and then a stream-K step range (Walk);
+// KIND_SPLIT and KIND_TILE give every block one item (tile blockIdx.x, K
+// slice blockIdx.z).  Every wait is bounded: a warp whose wait expires stops
+// computing (the status word then holds GEMM_ERR_TIMEOUT) but still walks its
+// items, so the computing warps' barriers stay matched; the producer drains
+// its copies in flight.
 template <class TL>
 struct WsCfg {
-  static constexpr int A_BYTES = TL::BM * TL::BK * 4;  // [BK][BM], dense rows
+  static constexpr int A_BYTES = TL::BM * TL::BK * 4;  // [BK][BM] or [BM][BK]
   static constexpr int B_BYTES = TL::BN * TL::BK * 4;  // [BK][BN]
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
   static constexpr int THREADS = TL::THREADS + 32;
@@ -670,12 +691,13 @@ struct WsCfg {
   static_assert(A_BYTES % 1024 == 0 && B_BYTES % 1024 == 0, "stage alignment");
 };
 
-template <class TL>
+template <class TL, bool A_K, int KIND>
 __global__ void __launch_bounds__(TL::THREADS + 32, TL::MIN_BLOCKS)
     sgemm_ws_kernel(const __grid_constant__ CUtensorMap tmA,
                     const __grid_constant__ CUtensorMap tmB, const Params p) {
   constexpr int BM = TL::BM, BN = TL::BN, BK = TL::BK, NST = TL::NSTAGES, JP = TL::JP;
   constexpr int WARPS = TL::THREADS / 32;
+  static_assert(!A_K || BK == 32, "row tiles of A: 128-byte rows");
   using WC = WsCfg<TL>;
   extern __shared__ __align__(1024) uint8_t ws_smem[];
   __shared__ __align__(8) uint64_t bars[2 * NST];
@@ -703,7 +725,23 @@ __global__ void __launch_bounds__(TL::THREADS + 32, TL::MIN_BLOCKS)
   const WaitCtl wc{p.status, &s_abort, p.timeout_ns};
   const int G = gridDim.x;
   Walk walk = {};
-  walk.init(p, blockIdx.x, G);
+  if constexpr (KIND == KIND_PERSIST) walk.init(p, blockIdx.x, G);
+  bool single_done = false;
+  // the next work item of this block (the same sequence for every warp)
+  auto next = [&](Item& w) -> bool {
+    if constexpr (KIND == KIND_PERSIST) {
+      return walk.next<BK>(p, G, w);
+    } else {
+      if (single_done) return false;
+      single_done = true;
+      w.t = blockIdx.x;
+      w.kbeg = blockIdx.z * p.k_slice;
+      w.kend = min(p.K, w.kbeg + p.k_slice);
+      w.seg0 = 0;
+      w.whole = true;
+      return w.kbeg < w.kend;
+    }
+  };
   Item w;
 
   if (warp == WARPS) {
@@ -714,7 +752,7 @@ __global__ void __launch_bounds__(TL::THREADS + 32, TL::MIN_BLOCKS)
       int stage = 0;
       uint32_t phase = 0, pending = 0, pend_phase = 0;  // per stage: last load issued / its parity
       bool ok = true, first = true;
-      while (ok && walk.next<BK>(p, G, w)) {
+      while (ok && next(w)) {
         int m0, n0;
         tile_origin<TL>(p, w.t, m0, n0);
         for (int k0 = w.kbeg; k0 < w.kend; k0 += BK) {
@@ -725,7 +763,8 @@ __global__ void __launch_bounds__(TL::THREADS + 32, TL::MIN_BLOCKS)
           if (!skip) {
             const uint32_t sa = ring + (uint32_t)(stage * WC::STAGE_BYTES);
             mbar_arrive_expect_tx(full_bar(stage), WC::STAGE_BYTES);
-            tma_load_3d(sa, &tmA, m0, k0, 0, full_bar(stage));
+            if constexpr (A_K) tma_load_3d(sa, &tmA, k0, m0, 0, full_bar(stage));
+            else tma_load_3d(sa, &tmA, m0, k0, 0, full_bar(stage));
             tma_load_3d(sa + WC::A_BYTES, &tmB, n0, k0, 0, full_bar(stage));
             pending |= 1u << stage;
             pend_phase = (pend_phase & ~(1u << stage)) | (phase << stage);
@@ -744,13 +783,14 @@ __global__ void __launch_bounds__(TL::THREADS + 32, TL::MIN_BLOCKS)
   const int wm = (warp / TL::WARPS_N) * 64;          // warp's first row in the tile
   const int wn = (warp % TL::WARPS_N) * TL::WARP_N;  // warp's first column
   const int ty = lane >> 2, tx = lane & 3;
-  const int arow = wm + ty * 4;  // lane rows: arow + {0..3}, arow + 32 + {0..3}
-  const int bcol = wn + tx * 4;  // lane cols: bcol + 16 h + {0..3}, h < HB
+  // lane rows: lane_row<A_K>(arow, i), i < 8; lane cols: bcol + 16 h + {0..3}
+  const int arow = A_K ? wm + ty : wm + ty * 4;
+  const int bcol = wn + tx * 4;
   uint64_t acc[8][JP];
   int stage = 0;
   uint32_t phase = 0;
   bool failed = false;
-  while (walk.next<BK>(p, G, w)) {
+  while (next(w)) {
     int m0, n0;
     tile_origin<TL>(p, w.t, m0, n0);
 #pragma unroll
@@ -762,15 +802,35 @@ __global__ void __launch_bounds__(TL::THREADS + 32, TL::MIN_BLOCKS)
       if (!failed) {
         const float* As = ring_f + stage * (WC::STAGE_BYTES / 4);
         const float* Bs = As + BM * BK;
-#pragma unroll KC_UNROLL
-        for (int kc = 0; kc < BK / 4; ++kc) {
+        if constexpr (A_K) {
+          // row r = arow + 8 i holds its k = 4 c + e at chunk c ^ (r & 7) = c ^ ty
+          const float* Ar = As + arow * BK;
 #pragma unroll
-          for (int kk = 0; kk < 4; ++kk) {
-            const int k = kc * 4 + kk;
-            const float4 lo = lds128(As + k * BM + arow);
-            const float4 hi = lds128(As + k * BM + arow + 32);
-            const float av[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
-            fma_k<TL>(acc, av, Bs + k * BN + bcol);
+          for (int kc = 0; kc < BK / 4; ++kc) {
+            const int ch = ((kc ^ ty) & 7) * 4;
+#pragma unroll
+            for (int kk = 0; kk < 4; kk += 2) {
+              float2 v[8];
+#pragma unroll
+              for (int i = 0; i < 8; ++i)
+                v[i] = *reinterpret_cast<const float2*>(Ar + i * 8 * BK + ch + kk);
+              const float a0[8] = {v[0].x, v[1].x, v[2].x, v[3].x, v[4].x, v[5].x, v[6].x, v[7].x};
+              const float a1[8] = {v[0].y, v[1].y, v[2].y, v[3].y, v[4].y, v[5].y, v[6].y, v[7].y};
+              fma_k<TL>(acc, a0, Bs + (kc * 4 + kk) * BN + bcol);
+              fma_k<TL>(acc, a1, Bs + (kc * 4 + kk + 1) * BN + bcol);
+            }
+          }
+        } else {
+#pragma unroll KC_UNROLL
+          for (int kc = 0; kc < BK / 4; ++kc) {
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk) {
+              const int k = kc * 4 + kk;
+              const float4 lo = lds128(As + k * BM + arow);
+              const float4 hi = lds128(As + k * BM + arow + 32);
+              const float av[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
+              fma_k<TL>(acc, av, Bs + k * BN + bcol);
+            }
           }
         }
         __syncwarp();
@@ -778,9 +838,34 @@ __global__ void __launch_bounds__(TL::THREADS + 32, TL::MIN_BLOCKS)
       }
       if (++stage == NST) { stage = 0; phase ^= 1u; }
     }
-    finish_item<TL, KIND_PERSIST, TL::THREADS>(p, acc, w, walk.sk_first, m0, n0, p.C, tid, arow,
-                                               bcol, s_last);
+    finish_item<TL, KIND, TL::THREADS, A_K>(p, acc, w, walk.sk_first, m0, n0, p.C, tid, arow,
+                                            bcol, s_last);
   }
+}
+
+// The warp-specialised launch of `grid` blocks of kind KIND.
+template <class TL, bool A_K, int KIND>
+cudaError_t launch_ws(const Params& p, const SgemmArgs& a, dim3 grid, cudaStream_t stream) {
+  using WC = WsCfg<TL>;
+  // A as [K, M] (boxes of BK rows x BM) or [M, K] (BM rows x 32, swizzled),
+  // B as [K, N] (BK rows x BN), fp32
+  CUtensorMap mA, mB;
+  const bool okA =
+      A_K ? make_map(&mA, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, a.A, a.M, a.K, a.lda, TL::BK, TL::BM,
+                     CU_TENSOR_MAP_SWIZZLE_128B, 1, 0, 4)
+          : make_map(&mA, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, a.A, a.K, a.M, a.lda, TL::BM, TL::BK,
+                     CU_TENSOR_MAP_SWIZZLE_NONE, 1, 0, 4);
+  if (!okA || !make_map(&mB, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, a.B, a.K, a.N, a.ldb, TL::BN,
+                        TL::BK, CU_TENSOR_MAP_SWIZZLE_NONE, 1, 0, 4))
+    return cudaErrorNotSupported;
+  auto kern = sgemm_ws_kernel<TL, A_K, KIND>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       WC::SMEM_BYTES);
+  if (e == cudaSuccess && TL::MIN_BLOCKS > 1)
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout,
+                             (int)cudaSharedmemCarveoutMaxShared);
+  if (e != cudaSuccess) return e;
+  return launch_kernel(kern, grid, dim3(WC::THREADS), WC::SMEM_BYTES, stream, 1, mA, mB, p);
 }
 
 template <class TL, bool A_K, bool B_K, bool VEC, int KIND>
@@ -813,27 +898,6 @@ cudaError_t launch_vs(const Params& p, bool vec, int kind, dim3 grid, cudaStream
   }
   if (kind == KIND_SPLIT) return launch_one<TL, A_K, B_K, false, KIND_SPLIT>(p, grid, s);
   return launch_one<TL, A_K, B_K, false, KIND_TILE>(p, grid, s);
-}
-
-// The warp-specialised launch: grid blocks over the persistent plan in p.
-template <class TL>
-cudaError_t launch_ws(const Params& p, const SgemmArgs& a, dim3 grid, cudaStream_t stream) {
-  using WC = WsCfg<TL>;
-  // A as [K, M] and B as [K, N], fp32, boxes of BK rows of the block tile's width
-  CUtensorMap mA, mB;
-  if (!make_map(&mA, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, a.A, a.K, a.M, a.lda, TL::BM, TL::BK,
-                CU_TENSOR_MAP_SWIZZLE_NONE, 1, 0, 4) ||
-      !make_map(&mB, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, a.B, a.K, a.N, a.ldb, TL::BN, TL::BK,
-                CU_TENSOR_MAP_SWIZZLE_NONE, 1, 0, 4))
-    return cudaErrorNotSupported;
-  auto kern = sgemm_ws_kernel<TL>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       WC::SMEM_BYTES);
-  if (e == cudaSuccess && TL::MIN_BLOCKS > 1)
-    e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout,
-                             (int)cudaSharedmemCarveoutMaxShared);
-  if (e != cudaSuccess) return e;
-  return launch_kernel(kern, grid, dim3(WC::THREADS), WC::SMEM_BYTES, stream, 1, mA, mB, p);
 }
 
 // The whole launch for tile TL (host side of launch_sgemm).
@@ -894,19 +958,33 @@ cudaError_t launch_sgemm_t(const SgemmArgs& a, LaunchCtx& ctx) {
   }
   const bool A_K = !a.transA, B_K = a.transB;
   cudaError_t e = cudaErrorInvalidValue;
-  // warp-specialised TMA staging (tiles with 8 x 8 lane blocks: with the
+  // Warp-specialised TMA staging, for tiles with 8 x 8 lane blocks (with the
   // extra warp ptxas holds a thread to 168 registers, where the 8 x 16 block
-  // spills): persistent over the stream-K plan, or one block per tile
-  // without one
-  constexpr bool WS = PERSIST && TL::LN == 8;
-  const bool ws = WS && a.ws && !split && batch == 1 && vec && !A_K && !B_K;
-  if (ws) {
+  // spills), one GEMM, aligned rows, B stored [K, N]:
+  //  - tiles with a persistent launch (128 x 128, 128 x 64): A stored [K, M]
+  //    (packed so on large problems), no K split; persistent over the
+  //    stream-K plan, or one block per tile without one;
+  //  - the narrow tile (256 x 32, K step 32): A stored either way, one block
+  //    per tile or per (tile, K slice).
+  constexpr bool WS_P = PERSIST && TL::LN == 8;
+  constexpr bool WS_N = !PERSIST && TL::LN == 8 && TL::BK == 32;
+  const bool ws_ok = a.ws && batch == 1 && vec && !B_K;
+  if (WS_P && ws_ok && !split && !A_K) {
     if (kind != KIND_PERSIST) {
       p.kiters = (a.K + BK - 1) / BK;
       p.dp_tiles = tiles;
       grid = dim3(tiles, 1, 1);
     }
-    if constexpr (WS) e = launch_ws<TL>(p, a, grid, ctx.stream);
+    if constexpr (WS_P) e = launch_ws<TL, false, KIND_PERSIST>(p, a, grid, ctx.stream);
+  } else if (WS_N && ws_ok) {
+    if constexpr (WS_N) {
+      if (A_K)
+        e = split ? launch_ws<TL, true, KIND_SPLIT>(p, a, grid, ctx.stream)
+                  : launch_ws<TL, true, KIND_TILE>(p, a, grid, ctx.stream);
+      else
+        e = split ? launch_ws<TL, false, KIND_SPLIT>(p, a, grid, ctx.stream)
+                  : launch_ws<TL, false, KIND_TILE>(p, a, grid, ctx.stream);
+    }
   } else if (A_K && !B_K) e = launch_vs<TL, true, false, PERSIST>(p, vec, kind, grid, ctx.stream);
   else if (!A_K && !B_K) e = launch_vs<TL, false, false, PERSIST>(p, vec, kind, grid, ctx.stream);
   else if (A_K && B_K) e = launch_vs<TL, true, true, PERSIST>(p, vec, kind, grid, ctx.stream);

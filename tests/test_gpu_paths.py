@@ -149,15 +149,25 @@ for v in ("nn", "tn", "nt", "tt"):
     check_problem(p, exact=True)
     p = inputs.make_problem(8191, 29, 4601, tA, tB, "f32", "uniform", seed=623)
     check_problem(p)
+    # aligned rows, N = 32 and N = 24 (B tile past N), split over K and
+    # not, integer inputs: exact
+    p = inputs.make_problem(2304, 32, 1024, tA, tB, "f32", "integer", seed=624, beta=1.0,
+                            c_fill="integer")
+    check_problem(p, exact=True)
+    p = inputs.make_problem(40000, 24, 256, tA, tB, "f32", "integer", seed=625)
+    check_problem(p, exact=True)
 print("ok")
 """
 
 
-@pytest.mark.parametrize("narrow", ["1", "0"])
-def test_fp32_narrow_tile(lib_path, gpu, narrow):
+@pytest.mark.parametrize("narrow,ws", [("1", "1"), ("1", "0"), ("0", "1")])
+def test_fp32_narrow_tile(lib_path, gpu, narrow, ws):
     """N <= 32 on the fp32 path: the 256 x 32 tile (default) or the general
-    128 x 128 tile (GEMM_GB300_SG_NARROW=0), split over K or not."""
-    env = dict(os.environ, GEMM_GB300_SG_NARROW=narrow)
+    128 x 128 tile (GEMM_GB300_SG_NARROW=0), split over K or not; with
+    aligned rows and B stored [K, N], the narrow tile's operands arrive by TMA
+    (A row tiles 128-byte swizzled when A is stored [M, K]), else
+    (GEMM_GB300_SG_WS=0, or unaligned rows) by every warp's cp.async copies."""
+    env = dict(os.environ, GEMM_GB300_SG_NARROW=narrow, GEMM_GB300_SG_WS=ws)
     code = SCRIPT_NARROW.format(root=ROOT, tests=os.path.join(ROOT, "tests"))
     r = subprocess.run([sys.executable, "-c", code], env=env, capture_output=True, text=True,
                        timeout=900)
