@@ -962,20 +962,24 @@ cudaError_t launch_sgemm_t(const SgemmArgs& a, LaunchCtx& ctx) {
   // extra warp ptxas holds a thread to 168 registers, where the 8 x 16 block
   // spills), one GEMM, aligned rows, B stored [K, N]:
   //  - tiles with a persistent launch (128 x 128, 128 x 64): A stored [K, M]
-  //    (packed so on large problems), no K split; persistent over the
-  //    stream-K plan, or one block per tile without one;
+  //    (packed so on large problems); persistent over the stream-K plan, one
+  //    block per tile without one, or one per (tile, K slice);
   //  - the narrow tile (256 x 32, K step 32): A stored either way, one block
   //    per tile or per (tile, K slice).
   constexpr bool WS_P = PERSIST && TL::LN == 8;
   constexpr bool WS_N = !PERSIST && TL::LN == 8 && TL::BK == 32;
   const bool ws_ok = a.ws && batch == 1 && vec && !B_K;
-  if (WS_P && ws_ok && !split && !A_K) {
-    if (kind != KIND_PERSIST) {
-      p.kiters = (a.K + BK - 1) / BK;
-      p.dp_tiles = tiles;
-      grid = dim3(tiles, 1, 1);
+  if (WS_P && ws_ok && !A_K) {
+    if (split) {
+      if constexpr (WS_P) e = launch_ws<TL, false, KIND_SPLIT>(p, a, grid, ctx.stream);
+    } else {
+      if (kind != KIND_PERSIST) {
+        p.kiters = (a.K + BK - 1) / BK;
+        p.dp_tiles = tiles;
+        grid = dim3(tiles, 1, 1);
+      }
+      if constexpr (WS_P) e = launch_ws<TL, false, KIND_PERSIST>(p, a, grid, ctx.stream);
     }
-    if constexpr (WS_P) e = launch_ws<TL, false, KIND_PERSIST>(p, a, grid, ctx.stream);
   } else if (WS_N && ws_ok) {
     if constexpr (WS_N) {
       if (A_K)
