@@ -803,22 +803,23 @@ __global__ void __launch_bounds__(TL::THREADS + 32, TL::MIN_BLOCKS)
         const float* As = ring_f + stage * (WC::STAGE_BYTES / 4);
         const float* Bs = As + BM * BK;
         if constexpr (A_K) {
-          // row r = arow + 8 i holds its k = 4 c + e at chunk c ^ (r & 7) = c ^ ty
+          // row r = arow + 8 i holds its k = 4 c + e at chunk c ^ (r & 7) = c ^ ty:
+          // one 128-bit load a row gives four k
           const float* Ar = As + arow * BK;
 #pragma unroll
           for (int kc = 0; kc < BK / 4; ++kc) {
             const int ch = ((kc ^ ty) & 7) * 4;
+            float4 v[8];
 #pragma unroll
-            for (int kk = 0; kk < 4; kk += 2) {
-              float2 v[8];
-#pragma unroll
-              for (int i = 0; i < 8; ++i)
-                v[i] = *reinterpret_cast<const float2*>(Ar + i * 8 * BK + ch + kk);
-              const float a0[8] = {v[0].x, v[1].x, v[2].x, v[3].x, v[4].x, v[5].x, v[6].x, v[7].x};
-              const float a1[8] = {v[0].y, v[1].y, v[2].y, v[3].y, v[4].y, v[5].y, v[6].y, v[7].y};
-              fma_k<TL>(acc, a0, Bs + (kc * 4 + kk) * BN + bcol);
-              fma_k<TL>(acc, a1, Bs + (kc * 4 + kk + 1) * BN + bcol);
-            }
+            for (int i = 0; i < 8; ++i) v[i] = lds128(Ar + i * 8 * BK + ch);
+            const float a0[8] = {v[0].x, v[1].x, v[2].x, v[3].x, v[4].x, v[5].x, v[6].x, v[7].x};
+            const float a1[8] = {v[0].y, v[1].y, v[2].y, v[3].y, v[4].y, v[5].y, v[6].y, v[7].y};
+            const float a2[8] = {v[0].z, v[1].z, v[2].z, v[3].z, v[4].z, v[5].z, v[6].z, v[7].z};
+            const float a3[8] = {v[0].w, v[1].w, v[2].w, v[3].w, v[4].w, v[5].w, v[6].w, v[7].w};
+            fma_k<TL>(acc, a0, Bs + (kc * 4 + 0) * BN + bcol);
+            fma_k<TL>(acc, a1, Bs + (kc * 4 + 1) * BN + bcol);
+            fma_k<TL>(acc, a2, Bs + (kc * 4 + 2) * BN + bcol);
+            fma_k<TL>(acc, a3, Bs + (kc * 4 + 3) * BN + bcol);
           }
         } else {
 #pragma unroll KC_UNROLL
