@@ -183,8 +183,15 @@ constexpr int SG_BLOCKS_PER_SM = GB300_SG_MIN_BLOCKS;
 #ifndef GB300_SGN_MIN_BLOCKS
 #define GB300_SGN_MIN_BLOCKS 2
 #endif
+// (stages of its ring: three at two blocks per SM; two stages at three
+// blocks per SM measured level or slower: 512 x 32 x 5632 nn kernel 23.2 ->
+// 25.2 us, 8192 x 32 x 8192 88.7 us either way)
+#ifndef GB300_SGN_STAGES
+#define GB300_SGN_STAGES 3
+#endif
 constexpr int SGN_BM = 64 * GB300_SGN_WARPS_M, SGN_BN = 32, SGN_BK = GB300_SGN_BK;
 constexpr int SGN_BLOCKS_PER_SM = GB300_SGN_MIN_BLOCKS;
+constexpr int SGN_STAGES = GB300_SGN_STAGES;
 // fp32 big tile: 128 x 256 at K step 32 in a 4-stage ring, one block of 8
 // warps per SM, each lane 8 rows x 16 columns -- per K a lane builds its 8
 // splatted A pairs once for 64 paired FMAs (32 with 8 x 8), and the block

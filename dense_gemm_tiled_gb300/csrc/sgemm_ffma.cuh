@@ -87,7 +87,7 @@ struct Tile {
 // the general tile (128 x 128 at the defaults: 195 KiB at BK 64, 3 stages) and
 // the narrow one for N <= 32 (256 x 32, BK 32, two blocks per SM)
 using TileWide = Tile<SG_WARPS_M, SG_BN / 32, SG_BK, SG_BLOCKS_PER_SM>;
-using TileNarrow = Tile<SGN_BM / 64, SGN_BN / 32, SGN_BK, SGN_BLOCKS_PER_SM>;
+using TileNarrow = Tile<SGN_BM / 64, SGN_BN / 32, SGN_BK, SGN_BLOCKS_PER_SM, 8, SGN_STAGES>;
 using TileBig = Tile<SGB_BM / 64, SGB_BN / 64, SGB_BK, 1, 16, SGB_STAGES>;
 using TileHalf = Tile<SGH_BM / 64, SGH_BN / 32, SGH_BK, SGH_BLOCKS_PER_SM, 8, SGH_STAGES>;
 static_assert(TileWide::BM == SG_BM && TileWide::BN == SG_BN, "tile shape");
