@@ -98,8 +98,11 @@ static_assert(TileHalf::BM == SGH_BM && TileHalf::BN == SGH_BN, "tile shape");
 // Tile rasterisation: blocks walk GROUP tile-rows column by column, so each B
 // panel is fetched from DRAM once per group while the group's A panels stay in
 // L2.  The host picks GROUP so those A panels take about a quarter of L2
-// (32 MB): measured at 4096^3, 8-row groups read 352 MB from DRAM and 32-row
-// groups (64 MB of A panels) 520 MB -- the L2 is split between the two dies.
+// (32 MB): measured at 4096^3, 8-row groups read 352 MB from DRAM, 16-row
+// groups (the pick there) 334-336 MB and 32-row groups (64 MB of A panels)
+// 520 MB -- the L2 is split between the two dies.  (Even at 16 rows an A
+// panel's K slice comes back one wave of 152 tiles later, after ~61 MB of
+// other slices, and is read again.)
 constexpr int64_t RASTER_L2_BYTES = 32ll << 20;
 
 // Compile-time tuning knobs (measured on GB300 at 4096^3; the defaults won;
